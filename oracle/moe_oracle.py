@@ -1,0 +1,250 @@
+"""Plain fp64 CPU oracle of the post-router MoE layer, forward and backward.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import or call anything under ``oracle/``. The
+product path (the CUDA library and its Python binding) never does, and shares
+no code, table or helper with it.
+
+What the layer computes (sources, by page and section):
+
+* "feat(moe): add a megakernel backend with MOK integration" (Megatron-LM PR
+  #6572), Summary: the backend replaces the post-router path -- dispatch,
+  routed and shared expert computation, combine.
+* same page, Design > Authoritative routing maps: the dense routing map is
+  turned into a fixed-width top-k representation, missing routes carry expert
+  id -1, the matching probabilities are gathered; in backward the router-weight
+  gradients go back into the dense probability tensor.
+* same page, Design > Gradient accumulation, and "Add Mixture-of-Kittens MoE
+  backend on main" (PR #8210), review thread on wgrad precision: expert weight
+  gradients are accumulated into fp32 main_grad buffers (fused accumulation).
+* same page #6572, Supported configurations > limitations: routed and shared
+  experts share one intermediate size; shared expert BF16, no output gate.
+* "core.transformer.moe.megakernel.mok.runtime", _gate_up_weight_arguments and
+  _MoKWeightArguments: FC1 is a combined [2I, H] weight, rows [0,I) gate and
+  [I,2I) up; argument order shared gate/up/down, routed gate/up/down.
+* "core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward:
+  out = layer(hidden[T,H], probs[T,E], routing_map[T,E]) with hidden's shape.
+
+Readings where the pages are silent (each also listed in the design notes):
+the expert is a SwiGLU MLP, a = silu(x W_g^T) * (x W_u^T), y = a W_d^T with
+silu(z) = z / (1 + e^-z); the prob weights the expert output after the down
+projection; slots list a token's experts in ascending id order, -1 padding at
+the tail; a row with more than k routes is an error, not truncated; a routed
+(t, e) with prob 0 is still computed; probs off the map are ignored and get
+gradient 0; within an expert, routes are ordered by token index.
+
+Everything here is fp64 numpy; ``@`` (a BLAS matmul) is the only library step.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+class RoutingError(ValueError):
+    """A token row of the routing map has more than k routes."""
+
+
+# --------------------------------------------------------------------------
+# weights: the six-argument order shared gate/up/down, routed gate/up/down
+# --------------------------------------------------------------------------
+class DenseWeights:
+    """fp64 weights held in memory: Wg, Wu [I,H] (per expert [E,I,H]), Wd [H,I]."""
+
+    def __init__(self, shared_gate, shared_up, shared_down, routed_gate, routed_up, routed_down):
+        self.sg, self.su, self.sd = (np.asarray(a, np.float64) for a in (shared_gate, shared_up, shared_down))
+        self.rg, self.ru, self.rd = (np.asarray(a, np.float64) for a in (routed_gate, routed_up, routed_down))
+
+    @classmethod
+    def from_combined(cls, shared_fc1, shared_fc2, routed_fc1, routed_fc2):
+        """Split combined FC1 [.., 2I, H] into gate rows [0,I) and up rows [I,2I)
+        ("core.transformer.moe.megakernel.mok.runtime", _gate_up_weight_arguments)."""
+        inter = shared_fc1.shape[0] // 2
+        return cls(shared_fc1[:inter], shared_fc1[inter:], shared_fc2,
+                   routed_fc1[:, :inter], routed_fc1[:, inter:], routed_fc2)
+
+    @property
+    def num_experts(self):
+        return self.rg.shape[0]
+
+    def shared(self):
+        return self.sg, self.su, self.sd
+
+    def routed(self, e):
+        return self.rg[e], self.ru[e], self.rd[e]
+
+
+# --------------------------------------------------------------------------
+# routing: dense map -> fixed-width ids, then per-expert segments
+# --------------------------------------------------------------------------
+def route_pack(routing_map, probs, k):
+    """Dense routing_map[T,E] -> ids[T,k] (ascending expert ids, -1 padding) and
+    pp[T,k] (the probs at those ids, 0 for -1); ``over[t]`` marks rows with > k
+    routes. PR #6572, Design > Authoritative routing maps."""
+    routing_map = np.asarray(routing_map, bool)
+    probs = np.asarray(probs, np.float64)
+    T = routing_map.shape[0]
+    ids = np.full((T, k), -1, np.int32)
+    pp = np.zeros((T, k), np.float64)
+    over = np.zeros(T, bool)
+    for t in range(T):
+        experts = np.flatnonzero(routing_map[t])
+        if experts.size > k:
+            over[t] = True
+            continue
+        ids[t, :experts.size] = experts
+        pp[t, :experts.size] = probs[t, experts]
+    return ids, pp, over
+
+
+def dispatch_indices(ids, num_experts):
+    """Dispatch on one GPU = a local permutation (PR #6572, Summary: dispatch).
+
+    Valid routes (t, s) are ordered by (expert, token). Returns counts[E],
+    offsets[E+1] (exclusive scan), perm_src[R] (token of each permuted row),
+    perm_slot[R] (its slot) and row_of[T,k] (permuted row of each slot, -1 for
+    missing routes)."""
+    T, k = ids.shape
+    tok, slot = np.nonzero(ids >= 0)
+    exp = ids[tok, slot]
+    order = np.lexsort((tok, exp))          # primary key expert, then token
+    perm_src = tok[order].astype(np.int64)
+    perm_slot = slot[order].astype(np.int64)
+    counts = np.bincount(exp, minlength=num_experts).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    row_of = np.full((T, k), -1, np.int64)
+    row_of[perm_src, perm_slot] = np.arange(perm_src.size)
+    return counts, offsets, perm_src, perm_slot, row_of
+
+
+# --------------------------------------------------------------------------
+# the expert MLP (SwiGLU) and its derivative
+# --------------------------------------------------------------------------
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    return z * sigmoid(z)
+
+
+def silu_grad(z):
+    s = sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
+def expert_forward(x, Wg, Wu, Wd):
+    """SwiGLU expert on rows x[n,H]: g = x Wg^T, u = x Wu^T, a = silu(g) u, y = a Wd^T."""
+    g = x @ Wg.T
+    u = x @ Wu.T
+    a = silu(g) * u
+    y = a @ Wd.T
+    return g, u, a, y
+
+
+def expert_backward(x, dy, g, u, a, Wg, Wu, Wd):
+    """Gradients of sum(dy * y) for one expert: dx, dWg, dWu, dWd."""
+    da = dy @ Wd
+    dg = da * u * silu_grad(g)
+    du = da * silu(g)
+    dx = dg @ Wg + du @ Wu
+    return dx, dg.T @ x, du.T @ x, dy.T @ a
+
+
+# --------------------------------------------------------------------------
+# the layer
+# --------------------------------------------------------------------------
+def forward(hidden, probs, routing_map, W, k):
+    """out[T,H] = SwiGLU_shared(x) + sum over valid slots s of pp[t,s] * SwiGLU_{ids[t,s]}(x).
+
+    "core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward, and PR
+    #6572 Summary (dispatch, routed and shared experts, combine). Returns
+    (out, cache); the cache feeds ``backward``."""
+    x = np.asarray(hidden, np.float64)
+    T, H = x.shape
+    ids, pp, over = route_pack(routing_map, probs, k)
+    if over.any():
+        raise RoutingError(f"{int(over.sum())} token rows have more than k={k} routes")
+    E = W.num_experts
+    counts, offsets, perm_src, perm_slot, row_of = dispatch_indices(ids, E)
+
+    gs, us, as_, ys = expert_forward(x, *W.shared())
+
+    R = perm_src.size
+    y = np.zeros((R, H))
+    routed = {}
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            continue
+        xe = x[perm_src[lo:hi]]
+        g, u, a, ye = expert_forward(xe, *W.routed(e))
+        y[lo:hi] = ye
+        routed[e] = (g, u, a)
+
+    out = ys.copy()
+    for s in range(k):                        # combine, in slot order
+        v = ids[:, s] >= 0
+        out[v] += pp[v, s, None] * y[row_of[v, s]]
+
+    cache = dict(x=x, ids=ids, pp=pp, counts=counts, offsets=offsets, perm_src=perm_src,
+                 perm_slot=perm_slot, row_of=row_of, shared=(gs, us, as_), y=y, routed=routed, k=k)
+    return out, cache
+
+
+def backward(grad_out, cache, W):
+    """Gradients of L = sum(grad_out * out).
+
+    Returns dhidden[T,H], dprobs[T,E] (dense: <grad_out_t, y_{t,e}> on routed
+    (t,e), 0 elsewhere -- PR #6572, Design > Authoritative routing maps, the
+    backward adapter) and the six weight gradients {shared_gate, shared_up,
+    shared_down} plus {e: (dWg, dWu, dWd)} for every expert with tokens.
+    "core.transformer.moe.megakernel.mok.runtime", _MoKAutograd.backward."""
+    go = np.asarray(grad_out, np.float64)
+    x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
+    offsets, perm_src, perm_slot, y = cache["offsets"], cache["perm_src"], cache["perm_slot"], cache["y"]
+    T, H = x.shape
+    E = W.num_experts
+
+    gs, us, as_ = cache["shared"]
+    dx_s, dWsg, dWsu, dWsd = expert_backward(x, go, gs, us, as_, *W.shared())
+
+    R = perm_src.size
+    dx_perm = np.zeros((R, H))
+    dprob_perm = np.zeros(R)
+    routed_grads = {}
+    pp_perm = pp[perm_src, perm_slot] if R else np.zeros(0)
+    for e, (g, u, a) in cache["routed"].items():
+        lo, hi = offsets[e], offsets[e + 1]
+        go_e = go[perm_src[lo:hi]]
+        dprob_perm[lo:hi] = np.sum(go_e * y[lo:hi], axis=1)
+        dy = pp_perm[lo:hi, None] * go_e
+        dx, dWg, dWu, dWd = expert_backward(x[perm_src[lo:hi]], dy, g, u, a, *W.routed(e))
+        dx_perm[lo:hi] = dx
+        routed_grads[e] = (dWg, dWu, dWd)
+
+    dhidden = dx_s.copy()
+    dprobs = np.zeros((T, E))
+    for s in range(cache["k"]):               # un-permute reduce, in slot order
+        v = ids[:, s] >= 0
+        dhidden[v] += dx_perm[row_of[v, s]]
+        dprobs[np.flatnonzero(v), ids[v, s]] = dprob_perm[row_of[v, s]]
+
+    grads = dict(shared_gate=dWsg, shared_up=dWsu, shared_down=dWsd, routed=routed_grads)
+    return dhidden, dprobs, grads
+
+
+def accumulate_main_grads(main_grads, grads):
+    """Fused accumulation: main_grad <- main_grad + dW, in fp64 (PR #6572, Design >
+    Gradient accumulation; PR #8210 review: fp32 accumulator through the
+    reduction-store). ``main_grads`` holds shared_gate/up/down [I,H]/[I,H]/[H,I]
+    and routed_gate/up/down [E,..]; experts with no tokens are left as they are."""
+    out = {name: np.array(v, np.float64, copy=True) for name, v in main_grads.items()}
+    out["shared_gate"] += grads["shared_gate"]
+    out["shared_up"] += grads["shared_up"]
+    out["shared_down"] += grads["shared_down"]
+    for e, (dWg, dWu, dWd) in grads["routed"].items():
+        out["routed_gate"][e] += dWg
+        out["routed_up"][e] += dWu
+        out["routed_down"][e] += dWd
+    return out
+

@@ -1,0 +1,136 @@
+"""Pins for the oracle's backward pass and main_grad accumulation.
+
+* central finite differences of L = sum(grad_out * forward(...)) in fp64 for
+  dhidden, every on-map dprob and all six weight gradients (the forward is
+  pinned by test_oracle_forward, so this pins backward to it);
+* dprobs is exactly 0 off the map; the hand-derived worked example;
+* main_grad accumulation adds dW once; a zero-token expert's buffers are left
+  bitwise unchanged.
+"""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from tests.test_oracle_forward import eval_closed_form, load_worked_example
+
+H_FD = 1e-6
+
+
+def _tiny_case(seed, T=6, H=5, I=3, E=4, k=2):
+    rng = np.random.default_rng(seed)
+    W = O.DenseWeights(rng.standard_normal((I, H)) * 0.5, rng.standard_normal((I, H)) * 0.5,
+                       rng.standard_normal((H, I)) * 0.5, rng.standard_normal((E, I, H)) * 0.5,
+                       rng.standard_normal((E, I, H)) * 0.5, rng.standard_normal((E, H, I)) * 0.5)
+    x = rng.standard_normal((T, H))
+    go = rng.standard_normal((T, H))
+    m = np.zeros((T, E), bool)
+    for t in range(T):
+        m[t, rng.choice(E - 1, size=int(rng.integers(1, k + 1)), replace=False)] = True  # expert E-1 idle
+    m[T - 1] = False                                                                      # a row with no route
+    probs = rng.random((T, E))
+    return W, x, go, m, probs, k
+
+
+def _loss(W, x, go, m, probs, k):
+    out, _ = O.forward(x, probs, m, W, k)
+    return float(np.sum(go * out))
+
+
+def _fd(f, arr, idx):
+    old = arr[idx]
+    arr[idx] = old + H_FD
+    lp = f()
+    arr[idx] = old - H_FD
+    lm = f()
+    arr[idx] = old
+    return (lp - lm) / (2 * H_FD)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_backward_matches_finite_differences(seed):
+    W, x, go, m, probs, k = _tiny_case(seed)
+    _, cache = O.forward(x, probs, m, W, k)
+    dx, dprobs, grads = O.backward(go, cache, W)
+
+    f = lambda: _loss(W, x, go, m, probs, k)   # noqa: E731  (closes over the arrays it perturbs)
+    fd_dx = np.array([[_fd(f, x, (t, h)) for h in range(x.shape[1])] for t in range(x.shape[0])])
+    np.testing.assert_allclose(dx, fd_dx, rtol=1e-6, atol=1e-8)
+
+    for t, e in zip(*np.nonzero(m)):
+        assert dprobs[t, e] == pytest.approx(_fd(f, probs, (t, e)), rel=1e-6, abs=1e-8)
+    assert np.all(dprobs[~m] == 0)
+    for t, e in zip(*np.nonzero(~m)):           # off-map probs do not change the loss
+        assert _fd(f, probs, (t, e)) == 0.0
+
+    def check(arr, grad):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            fd[idx] = _fd(f, arr, idx)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8)
+
+    check(W.sg, grads["shared_gate"])
+    check(W.su, grads["shared_up"])
+    check(W.sd, grads["shared_down"])
+    E = W.num_experts
+    for e in range(E):
+        if e in grads["routed"]:
+            dWg, dWu, dWd = grads["routed"][e]
+        else:
+            dWg = np.zeros_like(W.rg[e]); dWu = np.zeros_like(W.ru[e]); dWd = np.zeros_like(W.rd[e])
+        check(W.rg[e], dWg)
+        check(W.ru[e], dWu)
+        check(W.rd[e], dWd)
+
+
+def test_worked_example_backward():
+    ex, W = load_worked_example()
+    _, cache = O.forward(np.array(ex["hidden"]), np.array(ex["probs"]),
+                         np.array(ex["routing_map"], bool), W, ex["k"])
+    dx, dprobs, g = O.backward(np.array(ex["grad_out"]), cache, W)
+    e = ex["expected"]
+    tol = dict(rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dx, eval_closed_form(e["dhidden"]), **tol)
+    np.testing.assert_allclose(dprobs, eval_closed_form(e["dprobs"]), **tol)
+    np.testing.assert_allclose(g["shared_down"], eval_closed_form(e["dW_shared_down"]), **tol)
+    np.testing.assert_allclose(g["shared_gate"], eval_closed_form(e["dW_shared_gate"]), **tol)
+    np.testing.assert_allclose(g["shared_up"], eval_closed_form(e["dW_shared_up"]), **tol)
+    for ex_id in (0, 1):
+        dWg, dWu, dWd = g["routed"][ex_id]
+        np.testing.assert_allclose(dWg, eval_closed_form(e[f"dW_routed_gate_{ex_id}"]), **tol)
+        np.testing.assert_allclose(dWu, eval_closed_form(e[f"dW_routed_up_{ex_id}"]), **tol)
+        np.testing.assert_allclose(dWd, eval_closed_form(e[f"dW_routed_down_{ex_id}"]), **tol)
+
+
+def test_main_grad_accumulation_and_idle_expert():
+    W, x, go, m, probs, k = _tiny_case(3)
+    _, cache = O.forward(x, probs, m, W, k)
+    _, _, grads = O.backward(go, cache, W)
+    rng = np.random.default_rng(5)
+    E = W.num_experts
+    mg = dict(shared_gate=rng.standard_normal(W.sg.shape), shared_up=rng.standard_normal(W.su.shape),
+              shared_down=rng.standard_normal(W.sd.shape), routed_gate=rng.standard_normal(W.rg.shape),
+              routed_up=rng.standard_normal(W.ru.shape), routed_down=rng.standard_normal(W.rd.shape))
+    out = O.accumulate_main_grads(mg, grads)
+    zero = {n: np.zeros_like(v) for n, v in mg.items()}
+    dW = O.accumulate_main_grads(zero, grads)
+    for n in mg:
+        np.testing.assert_allclose(out[n], mg[n] + dW[n], rtol=1e-15, atol=1e-15)
+    idle = E - 1
+    assert idle not in grads["routed"]
+    for n in ("routed_gate", "routed_up", "routed_down"):
+        assert np.array_equal(out[n][idle], mg[n][idle])
+    busy = next(iter(grads["routed"]))
+    assert np.any(out["routed_gate"][busy] != mg["routed_gate"][busy])
+
+
+def test_backward_tokens_are_independent():
+    """dhidden and dprobs of a token depend only on that token (the sampled
+    full-size checks rest on this)."""
+    W, x, go, m, probs, k = _tiny_case(4, T=10)
+    _, cache = O.forward(x, probs, m, W, k)
+    dx, dp, _ = O.backward(go, cache, W)
+    sub = np.array([1, 4, 9])
+    _, cs = O.forward(x[sub], probs[sub], m[sub], W, k)
+    dxs, dps, _ = O.backward(go[sub], cs, W)
+    np.testing.assert_allclose(dxs, dx[sub], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dps, dp[sub], rtol=1e-13, atol=1e-14)
