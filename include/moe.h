@@ -1,0 +1,163 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE layer library (libmoe.so).
+ *
+ * The library runs the post-router Mixture-of-Experts layer on one GPU,
+ * forward and backward: route-pack, dispatch (a local permutation), routed
+ * SwiGLU experts, the shared SwiGLU expert, prob-weighted combine; then
+ * dgrad of the hidden states, router-prob gradients scattered into the dense
+ * [T,E] tensor, and weight gradients accumulated into fp32 main_grad buffers.
+ * Sources: "feat(moe): add a megakernel backend with MOK integration"
+ * (Megatron-LM PR #6572), Summary and Design; "Add Mixture-of-Kittens MoE
+ * backend on main" (PR #8210), What does this PR do; API pages
+ * "core.transformer.moe.megakernel.mok.backend" (MoKMegakernel.forward) and
+ * "core.transformer.moe.megakernel.mok.runtime" (_MoKWeightArguments,
+ * _gate_up_weight_arguments, _gate_up_main_grad_arguments, _MoKAutograd).
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers unless a comment says otherwise;
+ *    the caller owns them. Weights and main_grads are non-owning views: nothing
+ *    is copied or registered (runtime page, _MoKWeightArguments).
+ *  - Layouts are row-major; strides are in ELEMENTS. bf16 is passed as void*.
+ *  - `stream` is a cudaStream_t passed as void*; every call is asynchronous on
+ *    it and performs no host synchronisation, except moe_device_status.
+ *  - Argument errors are reported synchronously, before anything is launched.
+ *    Errors found by kernels (a routing row with more than k routes, a
+ *    bounded wait that gave up) are recorded in a device status word that
+ *    moe_device_status reads; the outputs of such a call are undefined.
+ *  - The library allocates no device memory: workspace and saved-state
+ *    memory come from the caller (sizes from the *_size queries).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, misaligned view */
+    MOE_ERR_UNSUPPORTED = 2,  /* a configuration the pages' backend also rejects, or a shape this build does not tile */
+    MOE_ERR_ROUTING = 3,      /* a routing_map row has more than k routes (device-detected) */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    MOE_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (device-detected) */
+    MOE_ERR_STATE = 6         /* call order violated (e.g. backward without a forward into `saved`) */
+} moe_status;
+
+typedef enum { MOE_W_BF16 = 0, MOE_W_MXFP8 = 1 } moe_wtype;
+
+/* Layer shape. Routed and shared experts share `inter` (PR #6572, Supported
+ * configurations: MOK limitations). hidden and inter must be multiples of 64;
+ * 1 <= topk <= 32; 1 <= num_experts <= 1024. swiglu_limit must be 0: the clamp
+ * exists on the pages (PR #8210 review: swiglu_limit) without a definition. */
+typedef struct {
+    int64_t max_tokens;   /* largest T any call will pass */
+    int64_t hidden;       /* H */
+    int64_t num_experts;  /* E, routed experts */
+    int64_t topk;         /* k, fixed route width */
+    int64_t inter;        /* I, intermediate size of routed and shared experts */
+    int32_t routed_wtype; /* moe_wtype of the routed weights; shared weights are always bf16 */
+    float swiglu_limit;   /* must be 0 */
+} moe_config;
+
+/* One weight argument in the external ABI order (runtime page,
+ * _MoKWeightArguments: shared_gate, shared_up, shared_down, routed_gate,
+ * routed_up, routed_down). Gate/up are [I,H] (routed [E,I,H]), down is [H,I]
+ * (routed [E,H,I]). A combined FC1 [.., 2I, H] is passed as two views whose
+ * data pointers differ by I rows (runtime page, _gate_up_weight_arguments).
+ * data must be 16-byte aligned and row_stride*elem_size a multiple of 16. */
+typedef struct {
+    const void* data;         /* bf16 elements (MXFP8: e4m3 rowwise payload) */
+    int64_t expert_stride;    /* elements between experts (routed views) */
+    int64_t row_stride;       /* elements between rows */
+    const uint8_t* scale;     /* MXFP8 only: E8M0 rowwise scales [E, N, K/32], compact */
+    const void* col_data;     /* MXFP8 only: e4m3 columnwise payload, same shape/strides as data */
+    const uint8_t* col_scale; /* MXFP8 only: E8M0 columnwise scales [E, N/32, K], compact */
+} moe_wview;
+
+typedef struct {
+    moe_wview shared_gate, shared_up, shared_down, routed_gate, routed_up, routed_down;
+} moe_weights;
+
+/* fp32 main_grad buffers in the six-buffer order (runtime page,
+ * _gate_up_main_grad_arguments). Shapes as the matching weights.
+ * strides[i] = {expert_stride, row_stride} in elements (expert_stride unused
+ * for the shared three). Fused accumulation is mandatory (PR #6572, Design >
+ * Gradient accumulation): every pointer must be non-null, 16-byte aligned,
+ * row_stride a multiple of 4. */
+typedef struct {
+    float *shared_gate, *shared_up, *shared_down, *routed_gate, *routed_up, *routed_down;
+    int64_t strides[6][2];
+} moe_main_grads;
+
+typedef struct moe_handle moe_handle;
+typedef struct moe_saved moe_saved;
+
+/* Bytes of device workspace a handle needs for `cfg` (worst case R = T*k). */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Creates a handle over caller-owned device workspace (256-byte aligned,
+ * >= moe_workspace_size bytes, kept alive and unused by others until
+ * moe_destroy). The handle itself is host memory owned by the library. The
+ * current CUDA device at this call is the device of every later call. */
+moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_handle** out);
+void moe_destroy(moe_handle* h);
+
+/* Saved forward state (routing, permuted activations, SwiGLU intermediates)
+ * lives in caller-owned device memory of moe_saved_size bytes. */
+moe_status moe_saved_size(const moe_config* cfg, size_t* bytes);
+moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved** out);
+void moe_saved_destroy(moe_saved* s);
+
+/* Forward: out[T,H] = SharedSwiGLU(hidden) + sum_s pp[t,s] * RoutedSwiGLU_{ids[t,s]}(hidden)
+ * ("core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward;
+ * PR #6572 Summary: dispatch, routed and shared experts, combine).
+ *   hidden[T,H] bf16, probs[T,E] fp32, routing_map[T,E] bytes (0/1, e.g.
+ *   torch.bool), out[T,H] bf16. 0 <= T <= max_tokens.
+ * The routing map is authoritative (PR #6572, Design > Authoritative routing
+ * maps): a token's experts are its map's true entries in ascending id order;
+ * fewer than k leaves -1 slots that contribute nothing; probs off the map are
+ * ignored; more than k is MOE_ERR_ROUTING (device status).
+ * `saved` receives what backward needs. It keeps `hidden` and the weight
+ * views BY POINTER: they must stay alive and unchanged until the matching
+ * moe_backward. */
+moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float* probs,
+                       const uint8_t* routing_map, const moe_weights* w, void* out,
+                       moe_saved* saved, void* stream);
+
+/* Backward of L = sum(grad_out * out) for the forward recorded in `saved`
+ * (runtime page, _MoKAutograd.backward; PR #6572, Design > Authoritative
+ * routing maps (backward adapter) and > Gradient accumulation).
+ *   grad_out[T,H] bf16 -> dhidden[T,H] bf16, dprobs[T,E] fp32 (dense: every
+ *   element written; 0 where the map is false), and main_grad += dW for all
+ *   six buffers, in fp32, one add per element (deterministic). Experts that
+ *   received no tokens keep their main_grad bitwise. `saved` is not consumed. */
+moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved,
+                        void* dhidden, float* dprobs, const moe_main_grads* mg, void* stream);
+
+/* Test hook: copies the routing of `saved` into caller device buffers.
+ * ids[T,k] int32 (-1 = missing), pp[T,k] fp32, counts[E] int32,
+ * offsets[E+1] int32 (exclusive scan of counts), perm_src[T*k] int32 (token of
+ * each permuted route, compact, first offsets[E] entries written), row_of[T,k]
+ * int32 (compact permuted row of each slot, -1 = missing). Any pointer may be
+ * NULL to skip it. */
+moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* ids, float* pp,
+                              int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                              int32_t* row_of, void* stream);
+
+/* Synchronises `stream`, returns the device status recorded since the last
+ * call (MOE_OK, MOE_ERR_ROUTING or MOE_ERR_TIMEOUT) and clears it. */
+moe_status moe_device_status(moe_handle* h, void* stream);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t moe_launch_count(void);
+
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

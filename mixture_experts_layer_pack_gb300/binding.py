@@ -1,0 +1,256 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h): same names, argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; PyTorch only
+supplies device memory (tensors) and streams. There is no other code path: if
+the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+c_int64, c_int32, c_float, c_void_p, c_size_t = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                                 ctypes.c_void_p, ctypes.c_size_t)
+
+MOE_OK = 0
+MOE_W_BF16, MOE_W_MXFP8 = 0, 1
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ROUTING",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_STATE"}
+WEIGHT_NAMES = ("shared_gate", "shared_up", "shared_down", "routed_gate", "routed_up", "routed_down")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("max_tokens", c_int64), ("hidden", c_int64), ("num_experts", c_int64), ("topk", c_int64),
+                ("inter", c_int64), ("routed_wtype", c_int32), ("swiglu_limit", c_float)]
+
+
+class moe_wview(ctypes.Structure):
+    _fields_ = [("data", c_void_p), ("expert_stride", c_int64), ("row_stride", c_int64), ("scale", c_void_p),
+                ("col_data", c_void_p), ("col_scale", c_void_p)]
+
+
+class moe_weights(ctypes.Structure):
+    _fields_ = [(n, moe_wview) for n in WEIGHT_NAMES]
+
+
+class moe_main_grads(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in WEIGHT_NAMES] + [("strides", (c_int64 * 2) * 6)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({_status_string(status)})")
+
+
+_LIB = None
+_LOCK = threading.Lock()
+EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size", "moe_saved_create",
+            "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
+            "moe_launch_count", "moe_status_string")
+
+
+def lib_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libmoe.so")
+
+
+def load(build_if_missing: bool = True):
+    """Loads libmoe.so (building it first if it is absent)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        path = lib_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise OSError(f"{path} is not built")
+            from . import build_lib
+            build_lib.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.POINTER
+        L.moe_workspace_size.argtypes = [P(moe_config), P(c_size_t)]
+        L.moe_saved_size.argtypes = [P(moe_config), P(c_size_t)]
+        L.moe_create.argtypes = [P(moe_config), c_void_p, c_size_t, P(c_void_p)]
+        L.moe_destroy.argtypes = [c_void_p]
+        L.moe_destroy.restype = None
+        L.moe_saved_create.argtypes = [c_void_p, c_void_p, c_size_t, P(c_void_p)]
+        L.moe_saved_destroy.argtypes = [c_void_p]
+        L.moe_saved_destroy.restype = None
+        L.moe_forward.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, P(moe_weights), c_void_p,
+                                  c_void_p, c_void_p]
+        L.moe_backward.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, P(moe_main_grads), c_void_p]
+        L.moe_export_routing.argtypes = [c_void_p, c_void_p] + [c_void_p] * 6 + [c_void_p]
+        L.moe_device_status.argtypes = [c_void_p, c_void_p]
+        L.moe_launch_count.argtypes = []
+        L.moe_launch_count.restype = ctypes.c_uint64
+        L.moe_status_string.argtypes = [c_int32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        for name in ("moe_workspace_size", "moe_saved_size", "moe_create", "moe_saved_create", "moe_forward",
+                     "moe_backward", "moe_export_routing", "moe_device_status"):
+            getattr(L, name).restype = c_int32
+        _LIB = L
+        return L
+
+
+def _status_string(status: int) -> str:
+    try:
+        return load().moe_status_string(status).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ------------------------------------------------------------------ the C ABI, same names
+def moe_workspace_size(cfg: moe_config) -> int:
+    n = c_size_t(0)
+    _check(load().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_saved_size(cfg: moe_config) -> int:
+    n = c_size_t(0)
+    _check(load().moe_saved_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_saved_size")
+    return n.value
+
+
+def moe_create(cfg: moe_config, workspace) -> c_void_p:
+    h = c_void_p()
+    _check(load().moe_create(ctypes.byref(cfg), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             ctypes.byref(h)), "moe_create")
+    return h
+
+
+def moe_destroy(h):
+    load().moe_destroy(h)
+
+
+def moe_saved_create(h, memory) -> c_void_p:
+    s = c_void_p()
+    _check(load().moe_saved_create(h, _ptr(memory), memory.numel() * memory.element_size(), ctypes.byref(s)),
+           "moe_saved_create")
+    return s
+
+
+def moe_saved_destroy(s):
+    load().moe_saved_destroy(s)
+
+
+def moe_forward(h, T, hidden, probs, routing_map, weights: moe_weights, out, saved, stream=None):
+    _check(load().moe_forward(h, int(T), _ptr(hidden), _ptr(probs), _ptr(routing_map), ctypes.byref(weights),
+                              _ptr(out), saved, _stream_ptr(stream)), "moe_forward")
+
+
+def moe_backward(h, grad_out, saved, dhidden, dprobs, main_grads: moe_main_grads, stream=None):
+    _check(load().moe_backward(h, _ptr(grad_out), saved, _ptr(dhidden), _ptr(dprobs), ctypes.byref(main_grads),
+                               _stream_ptr(stream)), "moe_backward")
+
+
+def moe_export_routing(h, saved, ids=None, pp=None, counts=None, offsets=None, perm_src=None, row_of=None,
+                       stream=None):
+    _check(load().moe_export_routing(h, saved, _ptr(ids), _ptr(pp), _ptr(counts), _ptr(offsets), _ptr(perm_src),
+                                     _ptr(row_of), _stream_ptr(stream)), "moe_export_routing")
+
+
+def moe_device_status(h, stream=None) -> int:
+    return int(load().moe_device_status(h, _stream_ptr(stream)))
+
+
+def moe_launch_count() -> int:
+    return int(load().moe_launch_count())
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def wview(t, scale=None, col_data=None, col_scale=None) -> moe_wview:
+    """View of a 2-D [N,K] or 3-D [E,N,K] tensor (strides taken from the tensor)."""
+    if t.dim() == 3:
+        es, rs = t.stride(0), t.stride(1)
+    else:
+        es, rs = 0, t.stride(0)
+    return moe_wview(t.data_ptr(), es, rs, None if scale is None else scale.data_ptr(),
+                     None if col_data is None else col_data.data_ptr(),
+                     None if col_scale is None else col_scale.data_ptr())
+
+
+def weights_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2) -> moe_weights:
+    """Gate/up views of combined FC1 weights ([2I,H], [E,2I,H]): rows [0,I) gate, [I,2I) up."""
+    inter = shared_fc1.shape[0] // 2
+    return moe_weights(wview(shared_fc1[:inter]), wview(shared_fc1[inter:]), wview(shared_fc2),
+                       wview(routed_fc1[:, :inter]), wview(routed_fc1[:, inter:]), wview(routed_fc2))
+
+
+def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2) -> moe_main_grads:
+    """Six-buffer main_grad order over combined FC1/FC2 fp32 buffers."""
+    inter = shared_fc1.shape[0] // 2
+    views = (shared_fc1[:inter], shared_fc1[inter:], shared_fc2,
+             routed_fc1[:, :inter], routed_fc1[:, inter:], routed_fc2)
+    m = moe_main_grads(*[v.data_ptr() for v in views])
+    for i, v in enumerate(views):
+        if v.dim() == 3:
+            m.strides[i][0], m.strides[i][1] = v.stride(0), v.stride(1)
+        else:
+            m.strides[i][0], m.strides[i][1] = 0, v.stride(0)
+    return m
+
+
+class MoELayer:
+    """Holds a handle, its workspace and one saved-state block (all torch device memory)."""
+
+    def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16):
+        import torch
+        self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, 0.0)
+        self.device = torch.device(device)
+        ws = moe_workspace_size(self.cfg)
+        sv = moe_saved_size(self.cfg)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
+        self.saved_mem = torch.empty(sv, dtype=torch.uint8, device=self.device)
+        with torch.cuda.device(self.device):
+            self.handle = moe_create(self.cfg, self.workspace)
+            self.saved = moe_saved_create(self.handle, self.saved_mem)
+
+    def forward(self, hidden, probs, routing_map, weights: moe_weights, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(hidden)
+        moe_forward(self.handle, hidden.shape[0], hidden, probs, routing_map, weights, out, self.saved, stream)
+        return out
+
+    def backward(self, grad_out, main_grads: moe_main_grads, dhidden=None, dprobs=None, stream=None):
+        import torch
+        T = grad_out.shape[0]
+        if dhidden is None:
+            dhidden = torch.empty_like(grad_out)
+        if dprobs is None:
+            dprobs = torch.empty((T, self.cfg.num_experts), dtype=torch.float32, device=grad_out.device)
+        moe_backward(self.handle, grad_out, self.saved, dhidden, dprobs, main_grads, stream)
+        return dhidden, dprobs
+
+    def device_status(self, stream=None) -> int:
+        return moe_device_status(self.handle, stream)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            moe_saved_destroy(self.saved)
+            moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

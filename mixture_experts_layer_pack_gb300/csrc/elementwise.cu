@@ -1,0 +1,153 @@
+// Bandwidth-bound kernels of the MoE layer: the dispatch gather, the combine
+// (un-permute + prob-weighted sum + shared expert), and the backward
+// un-permute reduction with the dense dprobs scatter.
+//
+// "feat(moe): add a megakernel backend with MOK integration", Summary
+// (dispatch, combine) and Design > Authoritative routing maps (the backward
+// adapter scatters router-weight gradients into the dense prob tensor).
+//
+// Rows are moved as 16-byte vectors; the routed and shared partial results
+// arrive in fp32 and every sum runs in fp32 in slot order, so the results are
+// deterministic and rounded to bf16 once.
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+// dst[r] = src[perm_src[r]] for every permuted row (zero for padding rows);
+// one warp per row, 16-byte vectors
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                          const int* __restrict__ perm_src,
+                                                          const int* __restrict__ meta, int max_rows, int vec_per_row,
+                                                          uint4* __restrict__ dst) {
+    const int rows = min(meta[2], max_rows);
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+        const int t = perm_src[r];
+        uint4* d = dst + int64_t(r) * vec_per_row;
+        if (t >= 0) {
+            const uint4* s = src + int64_t(t) * vec_per_row;
+            for (int v = lane; v < vec_per_row; v += 32) d[v] = __ldg(s + v);
+        } else {
+            for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+__device__ __forceinline__ void add_f32x8(float (&acc)[8], const float4* p) {
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    acc[0] += a.x;
+    acc[1] += a.y;
+    acc[2] += a.z;
+    acc[3] += a.w;
+    acc[4] += b.x;
+    acc[5] += b.y;
+    acc[6] += b.z;
+    acc[7] += b.w;
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
+    return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                      pack_bf16x2(acc[6], acc[7]));
+}
+
+// out[t] = y_shared[t] + sum over valid slots s of y[row_of[t,s]], fp32 inputs,
+// one bf16 rounding at the end (y rows already carry their prob: the down
+// projection's epilogue scales them); 8 columns per thread
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ ys, const float4* __restrict__ y,
+                                                      const int* __restrict__ row_of, int T, int vec_per_row, int k,
+                                                      uint4* __restrict__ out) {
+    const int64_t total = int64_t(T) * vec_per_row;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int t = int(i / vec_per_row);
+        const int v = int(i - int64_t(t) * vec_per_row);
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        add_f32x8(acc, ys + 2 * i);
+        for (int s = 0; s < k; ++s) {
+            const int r = __ldg(row_of + int64_t(t) * k + s);
+            if (r >= 0) add_f32x8(acc, y + 2 * (int64_t(r) * vec_per_row + v));
+        }
+        out[i] = pack_bf16x8(acc);
+    }
+}
+
+// dhidden[t] = dx_shared[t] + sum over valid slots of dx_perm[row_of[t,s]];
+// dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map
+__global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict__ dxs, const float4* __restrict__ dxp,
+                                                        const int* __restrict__ row_of, const int* __restrict__ ids,
+                                                        const float* __restrict__ partial, int n_part, int T,
+                                                        int vec_per_row, int k, int E, uint4* __restrict__ dhidden,
+                                                        float* __restrict__ dprobs) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const int64_t total = int64_t(T) * vec_per_row;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += stride) {
+        const int t = int(i / vec_per_row);
+        const int v = int(i - int64_t(t) * vec_per_row);
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        add_f32x8(acc, dxs + 2 * i);
+        for (int s = 0; s < k; ++s) {
+            const int r = __ldg(row_of + int64_t(t) * k + s);
+            if (r >= 0) add_f32x8(acc, dxp + 2 * (int64_t(r) * vec_per_row + v));
+        }
+        dhidden[i] = pack_bf16x8(acc);
+    }
+    const int64_t total_p = int64_t(T) * E;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total_p; i += stride) {
+        const int t = int(i / E);
+        const int e = int(i - int64_t(t) * E);
+        float val = 0.0f;
+        for (int s = 0; s < k; ++s) {
+            if (__ldg(ids + int64_t(t) * k + s) == e) {
+                const int r = __ldg(row_of + int64_t(t) * k + s);
+                const float* p = partial + int64_t(r) * n_part;
+                for (int j = 0; j < n_part; ++j) val += p[j];
+            }
+        }
+        dprobs[i] = val;
+    }
+}
+
+int grid_for(int64_t work, int threads, int num_sms) {
+    int64_t g = (work + threads - 1) / threads;
+    const int64_t cap = int64_t(num_sms) * 8;
+    if (g > cap) g = cap;
+    return g < 1 ? 1 : int(g);
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
+                               __nv_bfloat16* dst, int num_sms, cudaStream_t st) {
+    const int grid = grid_for(int64_t(max_rows) * 32, 256, num_sms);
+    gather_rows_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(src), perm_src, meta, max_rows, H / 8,
+                                              reinterpret_cast<uint4*>(dst));
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
+                           __nv_bfloat16* out, int num_sms, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
+    combine_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(ys), reinterpret_cast<const float4*>(y),
+                                          row_of, T, H / 8, k, reinterpret_cast<uint4*>(out));
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
+                             const float* partial, int n_part, int T, int H, int k, int E, __nv_bfloat16* dhidden,
+                             float* dprobs, int num_sms, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
+    unpermute_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(dxs), reinterpret_cast<const float4*>(dxp),
+                                            row_of, ids, partial, n_part, T, H / 8, k, E,
+                                            reinterpret_cast<uint4*>(dhidden), dprobs);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

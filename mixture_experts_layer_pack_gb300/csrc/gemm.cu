@@ -1,0 +1,502 @@
+// Grouped GEMMs of the MoE layer on the 5th-generation tensor cores (sm_103a).
+//
+// One persistent kernel template serves the five GEMM shapes of the layer
+// (expert computation of "feat(moe): add a megakernel backend with MOK
+// integration", Summary: routed and shared expert computation; backward per
+// "core.transformer.moe.megakernel.mok.runtime", _MoKAutograd.backward):
+//
+//   OP_FWD_GU   [R,2I] = X_perm[R,H] . W_fc1[e]^T     epilogue a = silu(g)*u (bf16), keeps g,u (fp32)
+//   OP_FWD_DOWN [R,H]  = a[R,I] . W_down[e]^T          epilogue y = p * acc (fp32)
+//   OP_BWD_DOWN [R,I]  = go_perm[R,H] . W_down[e]      epilogue SwiGLU backward, dprob partials
+//   OP_BWD_GU   [R,H]  = [dg|du][R,2I] . W_fc1[e]      epilogue store (fp32)
+//   OP_WGRAD    [M,N] += A[seg,M]^T . B[seg,N]        epilogue fp32 read-add-store into main_grad
+//
+// Rows of the routed GEMMs are the dispatch permutation, each expert's
+// segment padded to a multiple of 128 rows (zero rows), so a 128-row tile
+// never straddles two experts; the expert of each tile comes from a device
+// table, so nothing is read back to the host.
+//
+// Block = 6 warps: warp 0 issues TMA loads into a STAGES-deep shared-memory
+// ring, warp 1 owns TMEM and issues tcgen05.mma (M=128, N=BN, K=16 steps),
+// warps 2..5 drain the double-buffered TMEM accumulator through tcgen05.ld
+// and run the fused epilogue while the next tile accumulates. Operands use the
+// 128-byte swizzle: K-major tiles are 128 rows x 128 bytes; M/N-major tiles are
+// 64-element (128-byte) columns x 64 K-rows, 8 KB apart.
+#include "device_common.cuh"
+#include "internal.h"
+
+#include <climits>
+
+namespace moe {
+
+namespace {
+
+constexpr uint32_t kSwizzleAtom = 1024;   // 8 rows x 128 bytes
+constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
+
+template <int BN>
+struct Cfg {
+    static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+    static constexpr uint32_t B_BYTES = BN * kBK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
+    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + 1024 + 256;
+};
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((addr >> 4) & 0x3FFF);
+    d |= uint64_t((lbo >> 4) & 0x3FFF) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFF) << 32;
+    d |= 1ull << 46;  // descriptor version for tcgen05
+    d |= 2ull << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, M = 128
+template <int BN, bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t instr_desc() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+           (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+}
+
+struct Tile {
+    int mt, nt, e, k_lo, kblocks;
+};
+
+template <int OP>
+__device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a) {
+    Tile t;
+    if (OP == OP_WGRAD) {
+        const int per = a.m_tiles * a.n_tiles;
+        t.e = tile / per;
+        const int r = tile - t.e * per;
+        t.mt = r / a.n_tiles;
+        t.nt = r - t.mt * a.n_tiles;
+        const int lo = a.seg_off ? a.seg_off[t.e] : 0;
+        const int hi = a.seg_off ? a.seg_off[t.e + 1] : a.seg_len;
+        t.k_lo = lo;
+        t.kblocks = (hi - lo + kBK - 1) / kBK;
+    } else {
+        t.mt = tile / a.n_tiles;
+        t.nt = tile - t.mt * a.n_tiles;
+        t.e = a.mtile_expert ? a.mtile_expert[t.mt] : 0;
+        t.k_lo = 0;
+        t.kblocks = a.k_blocks;
+    }
+    return t;
+}
+
+// bounded wait that ignores the abort flag (used while winding down)
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int OP, int BN>
+__device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, uint8_t* sb, const CUtensorMap* mA,
+                                            const CUtensorMap* mB0, const CUtensorMap* mB1, uint64_t* bar,
+                                            const GemmArgs& a) {
+    const int k0 = kb * kBK;
+    if (OP == OP_WGRAD) {
+        const int krow = t.k_lo + k0;
+#pragma unroll
+        for (int c = 0; c < kBM / 64; ++c) tma_load_2d(sa + c * kMnChunkBytes, mA, bar, t.mt * kBM + 64 * c, krow);
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * kMnChunkBytes, mB0, bar, t.nt * BN + 64 * c, krow);
+        return;
+    }
+    tma_load_2d(sa, mA, bar, k0, t.mt * kBM);
+    if (OP == OP_FWD_GU) {
+        const int j0 = t.nt * (BN / 2);
+        tma_load_3d(sb, mB0, bar, k0, j0, t.e);
+        tma_load_3d(sb + (BN / 2) * 128, mB1, bar, k0, j0, t.e);
+    } else if (OP == OP_FWD_DOWN) {
+        tma_load_3d(sb, mB0, bar, k0, t.nt * BN, t.e);
+    } else if (OP == OP_BWD_DOWN) {
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * kMnChunkBytes, mB0, bar, t.nt * BN + 64 * c, k0, t.e);
+    } else {  // OP_BWD_GU: K rows [0,I) come from the gate view, [I,2I) from the up view
+        const bool up = k0 >= a.gate_up_split;
+        const CUtensorMap* m = up ? mB1 : mB0;
+        const int kk = up ? k0 - a.gate_up_split : k0;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * kMnChunkBytes, m, bar, t.nt * BN + 64 * c, kk, t.e);
+    }
+}
+
+template <int OP, int BN>
+__device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int r_local, const GemmArgs& a) {
+    if (OP == OP_WGRAD) {
+        const int m = t.mt * kBM + r_local;
+        float* dst;
+        if (m < a.m_split)
+            dst = a.mg0 + int64_t(t.e) * a.mg0_es + int64_t(m) * a.mg0_rs;
+        else
+            dst = a.mg1 + int64_t(t.e) * a.mg1_es + int64_t(m - a.m_split) * a.mg1_rs;
+        dst += t.nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(t_row + c * 32, v);
+            float4* p = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 o = p[q];
+                o.x += v[4 * q + 0];
+                o.y += v[4 * q + 1];
+                o.z += v[4 * q + 2];
+                o.w += v[4 * q + 3];
+                p[q] = o;
+            }
+        }
+        return;
+    }
+
+    const int row = t.mt * kBM + r_local;
+    const bool store = row < a.rows_valid;
+
+    if (OP == OP_FWD_GU) {
+        const int j0 = t.nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+            float g[32], u[32];
+            tmem_ld32(t_row + c * 32, g);
+            tmem_ld32(t_row + BN / 2 + c * 32, u);
+            if (store) {
+                float act[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) act[i] = g[i] * sigmoidf_(g[i]) * u[i];
+                const int j = j0 + c * 32;
+                store_bf16x32(a.out0 + int64_t(row) * a.ld_out0 + j, act);
+                store_f32x32(a.outf + int64_t(row) * a.ld_outf + j, g);
+                store_f32x32(a.outf + int64_t(row) * a.ld_outf + a.inter + j, u);
+            }
+        }
+    } else if (OP == OP_FWD_DOWN || OP == OP_BWD_GU) {
+        const float scale = (store && a.row_scale) ? a.row_scale[row] : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(t_row + c * 32, v);
+            if (store) {
+                if (OP == OP_FWD_DOWN) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= scale;
+                }
+                store_f32x32(a.outf + int64_t(row) * a.ld_outf + t.nt * BN + c * 32, v);
+            }
+        }
+    } else {  // OP_BWD_DOWN: acc = da_u = go . W_down[e] for columns i of the tile
+        const float p = (store && a.row_scale) ? a.row_scale[row] : 1.0f;
+        float part = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float d[32];
+            tmem_ld32(t_row + c * 32, d);
+            if (!store) continue;
+            const int i0 = t.nt * BN + c * 32;
+            const uint4* pa = reinterpret_cast<const uint4*>(a.in0 + int64_t(row) * a.ld_in0 + i0);
+            const float4* pg = reinterpret_cast<const float4*>(a.inf + int64_t(row) * a.ld_inf + i0);
+            const float4* pu = reinterpret_cast<const float4*>(a.inf + int64_t(row) * a.ld_inf + a.inter + i0);
+            uint4* pdg = reinterpret_cast<uint4*>(a.out0 + int64_t(row) * a.ld_out0 + i0);
+            uint4* pdu = reinterpret_cast<uint4*>(a.out0 + int64_t(row) * a.ld_out0 + a.inter + i0);
+            uint4* pap = a.out1 ? reinterpret_cast<uint4*>(a.out1 + int64_t(row) * a.ld_out1 + i0) : nullptr;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 wa = pa[q];
+                const float4 g0 = pg[2 * q], g1 = pg[2 * q + 1], u0 = pu[2 * q], u1 = pu[2 * q + 1];
+                const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w};
+                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                uint32_t dgw[4], duw[4], apw[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float av[2];
+                    unpack_bf16x2(aw[h], av[0], av[1]);
+                    float dg[2], du[2], ap[2];
+#pragma unroll
+                    for (int z = 0; z < 2; ++z) {
+                        const float dd = d[8 * q + 2 * h + z];
+                        const float gg = gv[2 * h + z], uu = uv[2 * h + z];
+                        part = fmaf(av[z], dd, part);
+                        const float sg = sigmoidf_(gg);
+                        const float da = p * dd;
+                        dg[z] = da * uu * (sg * (1.0f + gg * (1.0f - sg)));
+                        du[z] = da * (gg * sg);
+                        ap[z] = p * av[z];
+                    }
+                    dgw[h] = pack_bf16x2(dg[0], dg[1]);
+                    duw[h] = pack_bf16x2(du[0], du[1]);
+                    apw[h] = pack_bf16x2(ap[0], ap[1]);
+                }
+                pdg[q] = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
+                pdu[q] = make_uint4(duw[0], duw[1], duw[2], duw[3]);
+                if (pap) pap[q] = make_uint4(apw[0], apw[1], apw[2], apw[3]);
+            }
+        }
+        if (store && a.partial) a.partial[int64_t(row) * a.n_tiles + t.nt] = part;
+    }
+}
+
+template <int OP, int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+    using C = Cfg<BN>;
+    constexpr bool A_MN = (OP == OP_WGRAD);
+    constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD);
+    constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN>();
+    constexpr int STAGES = C::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB0);
+        if (OP == OP_FWD_GU || OP == OP_BWD_GU) tma_prefetch_map(&tmB1);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int total_tiles;
+    if (OP == OP_WGRAD)
+        total_tiles = args.groups * args.m_tiles * args.n_tiles;
+    else
+        total_tiles = (args.num_mtiles_dev ? *args.num_mtiles_dev : args.num_mtiles) * args.n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;  // per stage: ever filled / parity of its last fill
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Tile t = decode_tile<OP>(tile, args);
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    issue_loads<OP, BN>(t, kb, sa, sa + C::A_BYTES, &tmA, &tmB0, &tmB1, &full[stage], args);
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // wind down: let every copy this thread issued land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_parity >> s) & 1, args.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Tile t = decode_tile<OP>(tile, args);
+                if (t.kblocks == 0) continue;
+                const int buf = it & 1;
+                const uint32_t use = uint32_t(it >> 1);
+                ++it;
+                if (!mbar_wait(&tempty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = A_MN ? smem_desc(a_addr + kk * 2048, kMnChunkBytes, kSwizzleAtom)
+                                                 : smem_desc(a_addr + kk * 32, 16, kSwizzleAtom);
+                        const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 2048, kMnChunkBytes, kSwizzleAtom)
+                                                 : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
+                        mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) mma_commit(&tfull[buf]);
+            }
+            // every MMA issued by this thread completes before TMEM is released
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, args.status);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+        const int q = warp & 3;
+        const int r_local = q * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const Tile t = decode_tile<OP>(tile, args);
+            if (t.kblocks == 0) continue;
+            const int buf = it & 1;
+            const uint32_t use = uint32_t(it >> 1);
+            ++it;
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(&tfull[buf], use & 1, abort_flag, args.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+            epilogue_tile<OP, BN>(t, t_row, r_local, args);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int OP, int BN>
+cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+    static bool attr_set = false;
+    auto kern = moe_gemm_kernel<OP, BN>;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<BN>::SMEM));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<grid, kGemmThreads, Cfg<BN>::SMEM, st>>>(m.a, m.b0, m.b1, a);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int OP>
+cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+    switch (bn) {
+        case 256: return launch_one<OP, 256>(m, a, grid, st);
+        case 128: return launch_one<OP, 128>(m, a, grid, st);
+        case 64: return launch_one<OP, 64>(m, a, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int bn) {
+    return bn == 256 ? Cfg<256>::SMEM : (bn == 128 ? Cfg<128>::SMEM : Cfg<64>::SMEM);
+}
+
+int pick_bn(int64_t n, bool split_gate_up) {
+    // split_gate_up: n is 2I and each half of the tile must divide I
+    const int cands[3] = {256, 128, 64};
+    for (int bn : cands) {
+        if (split_gate_up) {
+            if (bn >= 128 && (n / 2) % (bn / 2) == 0) return bn;
+        } else if (n % bn == 0) {
+            return bn;
+        }
+    }
+    return 0;
+}
+
+cudaError_t launch_gemm(int op, int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+    if (grid <= 0) return cudaSuccess;
+    switch (op) {
+        case OP_FWD_GU: return launch_bn<OP_FWD_GU>(bn, m, a, grid, st);
+        case OP_FWD_DOWN: return launch_bn<OP_FWD_DOWN>(bn, m, a, grid, st);
+        case OP_BWD_DOWN: return launch_bn<OP_BWD_DOWN>(bn, m, a, grid, st);
+        case OP_BWD_GU: return launch_bn<OP_BWD_GU>(bn, m, a, grid, st);
+        case OP_WGRAD: return launch_bn<OP_WGRAD>(bn, m, a, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ------------------------------------------------------------------ tensor maps
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+}  // namespace
+
+bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3], s[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), d, s, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace moe

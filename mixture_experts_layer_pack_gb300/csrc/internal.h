@@ -1,0 +1,102 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kBM = 128;        // GEMM tile rows (= TMEM lanes) and expert segment padding
+constexpr int kBK = 64;         // GEMM K block (64 bf16 = one 128-byte swizzle row)
+constexpr int kChunk = 128;     // tokens per routing chunk
+constexpr int kGemmThreads = 192;
+
+// device status word bits (read back by moe_device_status)
+constexpr int kStatusRouting = 1;  // a routing_map row had more than k routes
+constexpr int kStatusTimeout = 2;  // a bounded wait gave up
+
+// the five GEMM shapes of the layer
+enum GemmOp : int {
+    OP_FWD_GU = 0,    // [a | g,u] = SwiGLU(X W_fc1^T): A K-major rows, B = gate/up rows (K-major)
+    OP_FWD_DOWN = 1,  // y = p * (a W_down^T): A K-major, B = W_down rows (K-major)
+    OP_BWD_DOWN = 2,  // da_u = go W_down; SwiGLU backward epilogue: A K-major, B = W_down (N-major)
+    OP_BWD_GU = 3,    // dx = [dg|du] W_fc1: A K-major (K = 2I), B = gate/up (N-major)
+    OP_WGRAD = 4,     // main_grad += A^T B over a token segment: A, B both M/N-major
+};
+
+struct GemmArgs {
+    // row-tile scheduling (OP 0..3)
+    const int* mtile_expert;    // expert of each 128-row tile; null: expert 0 for every tile
+    const int* num_mtiles_dev;  // device-resident tile count; null: use num_mtiles
+    int num_mtiles;
+    int n_tiles;                // N / BN
+    int k_blocks;               // K / 64
+    int rows_valid;             // output rows >= rows_valid are not stored
+    int gate_up_split;          // I: offset of the up half (N for FWD_GU, K for BWD_GU)
+    // segment scheduling (OP_WGRAD)
+    const int* seg_off;         // [groups+1] row offsets of each group's K range; null: [0, seg_len)
+    int seg_len;
+    int groups;
+    int m_tiles;                // M / 128
+    // epilogue operands
+    __nv_bfloat16* out0;        // bf16 GEMM operands produced here: a, [dg|du]
+    int64_t ld_out0;
+    __nv_bfloat16* out1;        // p * a
+    int64_t ld_out1;
+    float* outf;                // fp32 intermediates: [g|u], p*y, dx
+    int64_t ld_outf;
+    const __nv_bfloat16* in0;   // a
+    int64_t ld_in0;
+    const float* inf;           // [g|u]
+    int64_t ld_inf;
+    const float* row_scale;     // per-row prob (null: 1)
+    float* partial;             // per-row, per-N-tile partial dot products (null: skip)
+    float* mg0;
+    int64_t mg0_es, mg0_rs;
+    float* mg1;
+    int64_t mg1_es, mg1_rs;
+    int m_split;                // WGRAD rows >= m_split go to mg1 at row - m_split
+    int inter;
+    int* status;
+};
+
+struct GemmMaps {
+    CUtensorMap a, b0, b1;
+};
+
+// tensor-map construction (driver entry point resolved at first use)
+bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box);
+
+// picks the N tile (256, 128 or 64) for an output width
+int pick_bn(int64_t n, bool split_gate_up);
+
+cudaError_t launch_gemm(int op, int bn, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
+size_t gemm_smem_bytes(int bn);
+
+// routing
+cudaError_t launch_route_pack(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
+                              int* row_of, int* hist, int* status, cudaStream_t st);
+cudaError_t launch_route_scan(int* hist, int nchunks, int E, int* counts, int* offsets, int* offs_pad,
+                              int* mtile_expert, int* meta, int* perm_src, float* pp_perm, cudaStream_t st);
+cudaError_t launch_route_place(const int* ids, const float* pp, int T, int E, int k, const int* hist,
+                               const int* offs_pad, int* perm_src, float* pp_perm, int* row_of, cudaStream_t st);
+cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* perm_src_pad, const int* counts,
+                                  const int* offsets, const int* offs_pad, const int* mtile_expert, const int* meta,
+                                  int T, int k, int max_rows, int32_t* perm_src_out, int32_t* row_of_out,
+                                  cudaStream_t st);
+
+// elementwise / copy
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
+                               __nv_bfloat16* dst, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
+                           __nv_bfloat16* out, int num_sms, cudaStream_t st);
+cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
+                             const float* partial, int n_part, int T, int H, int k, int E, __nv_bfloat16* dhidden,
+                             float* dprobs, int num_sms, cudaStream_t st);
+
+void count_launch(int n = 1);
+
+}  // namespace moe

@@ -1,0 +1,606 @@
+// C ABI of the MoE layer library: argument checks, memory carving, tensor
+// maps and the launch sequence of forward and backward. Declarations and the
+// contract of every entry point are in include/moe.h.
+#include "../../include/moe.h"
+#include "internal.h"
+
+#include <atomic>
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+namespace moe {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Shape {
+    int64_t Tmax, H, E, k, I;
+    int64_t rows;     // permuted rows incl. padding, worst case
+    int64_t nchunks;  // routing chunks, worst case
+    int bn_gu, bn_down, bn_bd, bn_bgu, bn_wfc1, bn_wd;
+    int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM)
+};
+
+// carves consecutive 256-byte aligned pieces out of one block
+struct Carver {
+    uint8_t* base;
+    size_t off = 0;
+    template <typename T>
+    T* take(size_t count) {
+        off = align_up(off, kAlign);
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+moe_status check_config(const moe_config* c, Shape* s) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->max_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->topk <= 0 || c->inter <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c->swiglu_limit != 0.0f) return MOE_ERR_UNSUPPORTED;
+    if (c->routed_wtype != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->num_experts > 1024 || c->topk > 32 || c->topk > c->num_experts) return MOE_ERR_UNSUPPORTED;
+    if (c->hidden % 128 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
+    s->Tmax = c->max_tokens;
+    s->H = c->hidden;
+    s->E = c->num_experts;
+    s->k = c->topk;
+    s->I = c->inter;
+    s->rows = align_up(size_t(s->Tmax * s->k + s->E * (kBM - 1)), kBM);
+    s->nchunks = (s->Tmax + kChunk - 1) / kChunk;
+    if (s->rows >= INT_MAX / 2 || s->Tmax * s->k >= INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    s->bn_gu = pick_bn(2 * s->I, true);
+    s->bn_down = pick_bn(s->H, false);
+    s->bn_bd = pick_bn(s->I, false);
+    s->bn_bgu = pick_bn(s->H, false);
+    s->bn_wfc1 = pick_bn(s->H, false);
+    s->bn_wd = pick_bn(s->I, false);
+    if (!s->bn_gu || !s->bn_down || !s->bn_bd || !s->bn_bgu || !s->bn_wfc1 || !s->bn_wd) return MOE_ERR_UNSUPPORTED;
+    s->n_part = int(s->I / s->bn_bd);
+    return MOE_OK;
+}
+
+struct Workspace {
+    int* status;
+    int* hist;
+    __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
+    float *yx, *ys_dxs;  // forward: p*y (routed rows), y_shared; backward: dx (routed rows), dx_shared
+    float* partial;
+};
+
+struct SavedBufs {
+    int *ids, *row_of, *counts, *offsets, *offs_pad, *meta, *mtile_expert, *perm_src;
+    float *pp, *pp_perm;
+    __nv_bfloat16 *x_perm, *a, *a_s;
+    float *gu, *gu_s;
+};
+
+size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
+    Carver c{base};
+    w->status = c.take<int>(64);
+    w->hist = c.take<int>(size_t(s.nchunks) * s.E);
+    w->go_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
+    w->dgdu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
+    w->ap = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
+    w->yx = c.take<float>(size_t(s.rows) * s.H);
+    w->partial = c.take<float>(size_t(s.rows) * s.n_part);
+    w->ys_dxs = c.take<float>(size_t(s.Tmax) * s.H);
+    w->dgdu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
+    return align_up(c.off, kAlign);
+}
+
+size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
+    Carver c{base};
+    const size_t tk = size_t(s.Tmax * s.k);
+    b->ids = c.take<int>(tk);
+    b->pp = c.take<float>(tk);
+    b->row_of = c.take<int>(tk);
+    b->counts = c.take<int>(s.E);
+    b->offsets = c.take<int>(s.E + 1);
+    b->offs_pad = c.take<int>(s.E + 1);
+    b->meta = c.take<int>(4);
+    b->mtile_expert = c.take<int>(s.rows / kBM);
+    b->perm_src = c.take<int>(s.rows);
+    b->pp_perm = c.take<float>(s.rows);
+    b->x_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
+    b->a = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
+    b->gu = c.take<float>(size_t(s.rows) * 2 * s.I);
+    b->a_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
+    b->gu_s = c.take<float>(size_t(s.Tmax) * 2 * s.I);
+    return align_up(c.off, kAlign);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// a weight view of N rows x K columns (per expert when routed)
+bool check_view(const moe_wview& v, int64_t N, int64_t K, bool routed) {
+    if (!v.data || !aligned16(v.data)) return false;
+    if (v.row_stride < K || (v.row_stride * 2) % 16) return false;
+    if (routed && (v.expert_stride < N * v.row_stride || (v.expert_stride * 2) % 16)) return false;
+    return true;
+}
+
+bool check_weights(const Shape& s, const moe_weights* w) {
+    if (!w) return false;
+    return check_view(w->shared_gate, s.I, s.H, false) && check_view(w->shared_up, s.I, s.H, false) &&
+           check_view(w->shared_down, s.H, s.I, false) && check_view(w->routed_gate, s.I, s.H, true) &&
+           check_view(w->routed_up, s.I, s.H, true) && check_view(w->routed_down, s.H, s.I, true);
+}
+
+bool check_mg(const moe_main_grads* m) {
+    if (!m) return false;
+    float* const p[6] = {m->shared_gate, m->shared_up, m->shared_down, m->routed_gate, m->routed_up, m->routed_down};
+    for (int i = 0; i < 6; ++i) {
+        if (!p[i] || !aligned16(p[i])) return false;
+        if (m->strides[i][1] % 4 || m->strides[i][1] <= 0) return false;
+        if (i >= 3 && (m->strides[i][0] % 4 || m->strides[i][0] <= 0)) return false;
+    }
+    return true;
+}
+
+// 2D K-major operand: rows x K bf16 matrix, box 64 x 128 rows
+bool map_kmajor(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t ld) {
+    const uint64_t dims[2] = {uint64_t(K), uint64_t(rows)};
+    const uint64_t strides[1] = {uint64_t(ld) * 2};
+    const uint32_t box[2] = {64, uint32_t(kBM)};
+    return encode_map(m, base, 2, dims, strides, box);
+}
+
+// 2D M/N-major operand: K-rows x MN bf16 matrix (MN contiguous), box 64 x 64
+bool map_mnmajor(CUtensorMap* m, const void* base, int64_t rows, int64_t mn, int64_t ld) {
+    const uint64_t dims[2] = {uint64_t(mn), uint64_t(rows)};
+    const uint64_t strides[1] = {uint64_t(ld) * 2};
+    const uint32_t box[2] = {64, 64};
+    return encode_map(m, base, 2, dims, strides, box);
+}
+
+// 3D weight view [E][rows][cols] with a box of (64 cols, box_rows rows, 1 expert)
+bool map_weight(CUtensorMap* m, const moe_wview& v, int64_t E, int64_t rows, int64_t cols, uint32_t box_cols,
+                uint32_t box_rows) {
+    const int64_t es = E > 1 ? v.expert_stride : rows * v.row_stride;
+    const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(E)};
+    const uint64_t strides[2] = {uint64_t(v.row_stride) * 2, uint64_t(es) * 2};
+    const uint32_t box[3] = {box_cols, box_rows, 1};
+    return encode_map(m, v.data, 3, dims, strides, box);
+}
+
+GemmArgs base_args(int* status, int inter) {
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.rows_valid = INT_MAX;
+    a.m_split = INT_MAX;
+    a.inter = inter;
+    a.status = status;
+    return a;
+}
+
+int grid_of(int64_t tiles, int sms) { return int(tiles < sms ? tiles : sms); }
+
+}  // namespace
+
+struct moe_handle {
+    moe_config cfg;
+    Shape s;
+    Workspace ws;
+    int device;
+    int sms;
+};
+
+struct moe_saved {
+    moe_handle* h;
+    SavedBufs b;
+    int64_t T;
+    const void* hidden;
+    moe_weights w;
+    bool valid;
+};
+
+extern "C" {
+
+const char* moe_status_string(moe_status st) {
+    switch (st) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_ROUTING: return "a routing_map row has more than topk routes";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "a device-side wait timed out";
+        case MOE_ERR_STATE: return "invalid call order";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+    Shape s;
+    moe_status st = check_config(cfg, &s);
+    if (st != MOE_OK) return st;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    Workspace w;
+    *bytes = carve_workspace(s, nullptr, &w);
+    return MOE_OK;
+}
+
+moe_status moe_saved_size(const moe_config* cfg, size_t* bytes) {
+    Shape s;
+    moe_status st = check_config(cfg, &s);
+    if (st != MOE_OK) return st;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    SavedBufs b;
+    *bytes = carve_saved(s, nullptr, &b);
+    return MOE_OK;
+}
+
+moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_handle** out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    Shape s;
+    moe_status st = check_config(cfg, &s);
+    if (st != MOE_OK) return st;
+    Workspace w;
+    const size_t need = carve_workspace(s, nullptr, &w);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+        return MOE_ERR_INVALID_ARG;
+    moe_handle* h = new (std::nothrow) moe_handle;
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->cfg = *cfg;
+    h->s = s;
+    carve_workspace(s, static_cast<uint8_t*>(workspace), &h->ws);
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+        cudaMemset(h->ws.status, 0, sizeof(int)) != cudaSuccess) {
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+void moe_destroy(moe_handle* h) { delete h; }
+
+moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved** out) {
+    if (!h || !out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    SavedBufs b;
+    const size_t need = carve_saved(h->s, nullptr, &b);
+    if (!memory || bytes < need || (reinterpret_cast<uintptr_t>(memory) % kAlign)) return MOE_ERR_INVALID_ARG;
+    moe_saved* sv = new (std::nothrow) moe_saved;
+    if (!sv) return MOE_ERR_INVALID_ARG;
+    std::memset(sv, 0, sizeof(*sv));
+    sv->h = h;
+    carve_saved(h->s, static_cast<uint8_t*>(memory), &sv->b);
+    *out = sv;
+    return MOE_OK;
+}
+
+void moe_saved_destroy(moe_saved* s) { delete s; }
+
+#define MOE_CU(x)                                        \
+    do {                                                 \
+        if ((x) != cudaSuccess) return MOE_ERR_CUDA;     \
+    } while (0)
+
+moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float* probs, const uint8_t* routing_map,
+                       const moe_weights* w, void* out, moe_saved* saved, void* stream) {
+    if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
+    const Shape& s = h->s;
+    if (T < 0 || T > s.Tmax) return MOE_ERR_INVALID_ARG;
+    if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!hidden || !probs || !routing_map || !out || !aligned16(hidden) || !aligned16(out)))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const SavedBufs& b = saved->b;
+    const Workspace& ws = h->ws;
+    saved->T = T;
+    saved->hidden = hidden;
+    saved->w = *w;
+    saved->valid = true;
+    if (T == 0) return MOE_OK;
+
+    const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
+    const int nchunks = (Ti + kChunk - 1) / kChunk;
+    const int rows = int(s.rows);
+
+    // dispatch: route-pack, segment scan, stable placement, row gather
+    MOE_CU(launch_route_pack(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.hist, ws.status, st));
+    MOE_CU(launch_route_scan(ws.hist, nchunks, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta, b.perm_src,
+                             b.pp_perm, st));
+    MOE_CU(launch_route_place(b.ids, b.pp, Ti, E, k, ws.hist, b.offs_pad, b.perm_src, b.pp_perm, b.row_of, st));
+    MOE_CU(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), b.perm_src, b.meta, rows, H, b.x_perm,
+                              h->sms, st));
+
+    GemmMaps m;
+    // routed gate/up + SwiGLU
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_gu;
+        if (!map_kmajor(&m.a, b.x_perm, rows, H, H) || !map_weight(&m.b0, w->routed_gate, E, I, H, 64, bn / 2) ||
+            !map_weight(&m.b1, w->routed_up, E, I, H, 64, bn / 2))
+            return MOE_ERR_INVALID_ARG;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = 2 * I / bn;
+        a.k_blocks = H / kBK;
+        a.gate_up_split = I;
+        a.out0 = b.a;
+        a.ld_out0 = I;
+        a.outf = b.gu;
+        a.ld_outf = 2 * I;
+        MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // shared gate/up + SwiGLU
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_gu;
+        if (!map_kmajor(&m.a, hidden, Ti, H, H) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, bn / 2) ||
+            !map_weight(&m.b1, w->shared_up, 1, I, H, 64, bn / 2))
+            return MOE_ERR_INVALID_ARG;
+        a.num_mtiles = (Ti + kBM - 1) / kBM;
+        a.n_tiles = 2 * I / bn;
+        a.k_blocks = H / kBK;
+        a.rows_valid = Ti;
+        a.gate_up_split = I;
+        a.out0 = b.a_s;
+        a.ld_out0 = I;
+        a.outf = b.gu_s;
+        a.ld_outf = 2 * I;
+        MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // routed down projection, scaled by the route's prob
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_down;
+        if (!map_kmajor(&m.a, b.a, rows, I, I) || !map_weight(&m.b0, w->routed_down, E, H, I, 64, bn))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = H / bn;
+        a.k_blocks = I / kBK;
+        a.row_scale = b.pp_perm;
+        a.outf = ws.yx;
+        a.ld_outf = H;
+        MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // shared down projection
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_down;
+        if (!map_kmajor(&m.a, b.a_s, Ti, I, I) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, bn))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.num_mtiles = (Ti + kBM - 1) / kBM;
+        a.n_tiles = H / bn;
+        a.k_blocks = I / kBK;
+        a.rows_valid = Ti;
+        a.outf = ws.ys_dxs;
+        a.ld_outf = H;
+        MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // combine
+    MOE_CU(launch_combine(ws.ys_dxs, ws.yx, b.row_of, Ti, H, k, static_cast<__nv_bfloat16*>(out), h->sms, st));
+    return MOE_OK;
+}
+
+moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved, void* dhidden, float* dprobs,
+                        const moe_main_grads* mg, void* stream) {
+    if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
+    if (!saved->valid) return MOE_ERR_STATE;
+    if (!check_mg(mg)) return MOE_ERR_INVALID_ARG;
+    const Shape& s = h->s;
+    const int64_t T = saved->T;
+    if (T == 0) return MOE_OK;
+    if (!grad_out || !dhidden || !dprobs || !aligned16(grad_out) || !aligned16(dhidden)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const SavedBufs& b = saved->b;
+    const Workspace& ws = h->ws;
+    const moe_weights* w = &saved->w;
+    const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
+    const int rows = int(s.rows);
+    const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(grad_out);
+
+    MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, h->sms, st));
+
+    GemmMaps m;
+    // routed dgrad through the down projection + SwiGLU backward + dprob partials
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_bd;
+        if (!map_kmajor(&m.a, ws.go_perm, rows, H, H) || !map_weight(&m.b0, w->routed_down, E, H, I, 64, 64))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = I / bn;
+        a.k_blocks = H / kBK;
+        a.in0 = b.a;
+        a.ld_in0 = I;
+        a.inf = b.gu;
+        a.ld_inf = 2 * I;
+        a.row_scale = b.pp_perm;
+        a.partial = ws.partial;
+        a.out0 = ws.dgdu;
+        a.ld_out0 = 2 * I;
+        a.out1 = ws.ap;
+        a.ld_out1 = I;
+        MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // shared dgrad through the down projection + SwiGLU backward
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_bd;
+        if (!map_kmajor(&m.a, go, Ti, H, H) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, 64))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.num_mtiles = (Ti + kBM - 1) / kBM;
+        a.n_tiles = I / bn;
+        a.k_blocks = H / kBK;
+        a.rows_valid = Ti;
+        a.in0 = b.a_s;
+        a.ld_in0 = I;
+        a.inf = b.gu_s;
+        a.ld_inf = 2 * I;
+        a.out0 = ws.dgdu_s;
+        a.ld_out0 = 2 * I;
+        MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // routed dgrad through gate/up
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_bgu;
+        if (!map_kmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I) || !map_weight(&m.b0, w->routed_gate, E, I, H, 64, 64) ||
+            !map_weight(&m.b1, w->routed_up, E, I, H, 64, 64))
+            return MOE_ERR_INVALID_ARG;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = H / bn;
+        a.k_blocks = 2 * I / kBK;
+        a.gate_up_split = I;
+        a.outf = ws.yx;
+        a.ld_outf = H;
+        MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // shared dgrad through gate/up
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_bgu;
+        if (!map_kmajor(&m.a, ws.dgdu_s, Ti, 2 * I, 2 * I) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, 64) ||
+            !map_weight(&m.b1, w->shared_up, 1, I, H, 64, 64))
+            return MOE_ERR_INVALID_ARG;
+        a.num_mtiles = (Ti + kBM - 1) / kBM;
+        a.n_tiles = H / bn;
+        a.k_blocks = 2 * I / kBK;
+        a.rows_valid = Ti;
+        a.gate_up_split = I;
+        a.outf = ws.ys_dxs;
+        a.ld_outf = H;
+        MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    }
+    // routed wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_wfc1;
+        if (!map_mnmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I) || !map_mnmajor(&m.b0, b.x_perm, rows, H, H))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.seg_off = b.offs_pad;
+        a.groups = E;
+        a.m_tiles = 2 * I / kBM;
+        a.n_tiles = H / bn;
+        a.mg0 = mg->routed_gate;
+        a.mg0_es = mg->strides[3][0];
+        a.mg0_rs = mg->strides[3][1];
+        a.mg1 = mg->routed_up;
+        a.mg1_es = mg->strides[4][0];
+        a.mg1_rs = mg->strides[4][1];
+        a.m_split = I;
+        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
+    }
+    // routed wgrad of down: main_grad[e] += go_perm_e^T (p a)_e
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_wd;
+        if (!map_mnmajor(&m.a, ws.go_perm, rows, H, H) || !map_mnmajor(&m.b0, ws.ap, rows, I, I))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.seg_off = b.offs_pad;
+        a.groups = E;
+        a.m_tiles = H / kBM;
+        a.n_tiles = I / bn;
+        a.mg0 = mg->routed_down;
+        a.mg0_es = mg->strides[5][0];
+        a.mg0_rs = mg->strides[5][1];
+        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
+    }
+    // shared wgrad of gate/up
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_wfc1;
+        if (!map_mnmajor(&m.a, ws.dgdu_s, Ti, 2 * I, 2 * I) || !map_mnmajor(&m.b0, saved->hidden, Ti, H, H))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.seg_len = Ti;
+        a.groups = 1;
+        a.m_tiles = 2 * I / kBM;
+        a.n_tiles = H / bn;
+        a.mg0 = mg->shared_gate;
+        a.mg0_rs = mg->strides[0][1];
+        a.mg1 = mg->shared_up;
+        a.mg1_rs = mg->strides[1][1];
+        a.m_split = I;
+        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
+    }
+    // shared wgrad of down
+    {
+        GemmArgs a = base_args(ws.status, I);
+        const int bn = s.bn_wd;
+        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, b.a_s, Ti, I, I)) return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.seg_len = Ti;
+        a.groups = 1;
+        a.m_tiles = H / kBM;
+        a.n_tiles = I / bn;
+        a.mg0 = mg->shared_down;
+        a.mg0_rs = mg->strides[2][1];
+        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
+    }
+    // dhidden = shared + un-permuted routed dgrad; dense dprobs
+    MOE_CU(launch_unpermute(ws.ys_dxs, ws.yx, b.row_of, b.ids, ws.partial, s.n_part, Ti, H, k, E,
+                            static_cast<__nv_bfloat16*>(dhidden), dprobs, h->sms, st));
+    return MOE_OK;
+}
+
+moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* ids, float* pp, int32_t* counts,
+                              int32_t* offsets, int32_t* perm_src, int32_t* row_of, void* stream) {
+    if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
+    if (!saved->valid) return MOE_ERR_STATE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Shape& s = h->s;
+    const SavedBufs& b = saved->b;
+    const int64_t T = saved->T;
+    if (T == 0) {
+        if (counts) MOE_CU(cudaMemsetAsync(counts, 0, s.E * sizeof(int32_t), st));
+        if (offsets) MOE_CU(cudaMemsetAsync(offsets, 0, (s.E + 1) * sizeof(int32_t), st));
+        return MOE_OK;
+    }
+    const size_t tk = size_t(T * s.k);
+    if (ids) MOE_CU(cudaMemcpyAsync(ids, b.ids, tk * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    if (pp) MOE_CU(cudaMemcpyAsync(pp, b.pp, tk * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    if (counts) MOE_CU(cudaMemcpyAsync(counts, b.counts, s.E * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    if (offsets)
+        MOE_CU(cudaMemcpyAsync(offsets, b.offsets, (s.E + 1) * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    if (perm_src || row_of)
+        MOE_CU(launch_export_routing(b.ids, b.row_of, b.perm_src, b.counts, b.offsets, b.offs_pad, b.mtile_expert,
+                                     b.meta, int(T), int(s.k), int(s.rows), perm_src, row_of, st));
+    return MOE_OK;
+}
+
+moe_status moe_device_status(moe_handle* h, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    MOE_CU(cudaStreamSynchronize(st));
+    MOE_CU(cudaMemcpy(&v, h->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
+    MOE_CU(cudaMemset(h->ws.status, 0, sizeof(int)));
+    if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+    if (v & kStatusRouting) return MOE_ERR_ROUTING;
+    return MOE_OK;
+}
+
+}  // extern "C"

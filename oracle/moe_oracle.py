@@ -33,6 +33,16 @@ the tail; a row with more than k routes is an error, not truncated; a routed
 (t, e) with prob 0 is still computed; probs off the map are ignored and get
 gradient 0; within an expert, routes are ordered by token index.
 
+Precision. The pages fix it for the expert GEMMs: BF16 routed and shared
+experts (PR #6572, Supported configurations) with an FP32 GEMM accumulator
+and FP32 main_grad accumulation (PR #8210, review thread on wgrad
+precision). ``precision="exact"`` is the plain definition in fp64.
+``precision="bf16"`` holds each expert GEMM's operands in bf16 -- the
+activation a between the two projections, the SwiGLU gradients dg and du,
+and the prob-weighted activation p*a that multiplies grad_out in the down
+projection's weight gradient -- and accumulates in fp64. Inputs (hidden,
+grad_out, weights) are bf16 already.
+
 Everything here is fp64 numpy; ``@`` (a BLAS matmul) is the only library step.
 """
 from __future__ import annotations
@@ -117,6 +127,24 @@ def dispatch_indices(ids, num_experts):
 
 
 # --------------------------------------------------------------------------
+# operand precision
+# --------------------------------------------------------------------------
+def bf16_round(x):
+    """Round to the nearest bf16 value (8 significant bits), ties to even."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)                     # x = m * 2^e, |m| in [0.5, 1)
+    return np.ldexp(np.round(m * 256.0), e - 8)   # np.round: half to even
+
+
+def _rounder(precision):
+    if precision == "exact":
+        return lambda v: v
+    if precision == "bf16":
+        return bf16_round
+    raise ValueError(precision)
+
+
+# --------------------------------------------------------------------------
 # the expert MLP (SwiGLU) and its derivative
 # --------------------------------------------------------------------------
 def sigmoid(z):
@@ -132,33 +160,36 @@ def silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def expert_forward(x, Wg, Wu, Wd):
-    """SwiGLU expert on rows x[n,H]: g = x Wg^T, u = x Wu^T, a = silu(g) u, y = a Wd^T."""
+def expert_forward(x, Wg, Wu, Wd, rnd=lambda v: v):
+    """SwiGLU expert on rows x[n,H]: g = x Wg^T, u = x Wu^T, a = silu(g) u, y = a Wd^T
+    (``rnd`` holds a, the down projection's operand, at the GEMM precision)."""
     g = x @ Wg.T
     u = x @ Wu.T
-    a = silu(g) * u
+    a = rnd(silu(g) * u)
     y = a @ Wd.T
     return g, u, a, y
 
 
-def expert_backward(x, dy, g, u, a, Wg, Wu, Wd):
-    """Gradients of sum(dy * y) for one expert: dx, dWg, dWu, dWd."""
-    da = dy @ Wd
-    dg = da * u * silu_grad(g)
-    du = da * silu(g)
+def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, rnd=lambda v: v):
+    """Gradients of sum(go * (p y)) for one expert, p[n] the rows' probs:
+    returns dx, dWg, dWu, dWd (``rnd`` holds dg, du and p*a at the GEMM precision)."""
+    da = p[:, None] * (go @ Wd)
+    dg = rnd(da * u * silu_grad(g))
+    du = rnd(da * silu(g))
     dx = dg @ Wg + du @ Wu
-    return dx, dg.T @ x, du.T @ x, dy.T @ a
+    return dx, dg.T @ x, du.T @ x, go.T @ rnd(p[:, None] * a)
 
 
 # --------------------------------------------------------------------------
 # the layer
 # --------------------------------------------------------------------------
-def forward(hidden, probs, routing_map, W, k):
+def forward(hidden, probs, routing_map, W, k, precision="exact"):
     """out[T,H] = SwiGLU_shared(x) + sum over valid slots s of pp[t,s] * SwiGLU_{ids[t,s]}(x).
 
     "core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward, and PR
     #6572 Summary (dispatch, routed and shared experts, combine). Returns
     (out, cache); the cache feeds ``backward``."""
+    rnd = _rounder(precision)
     x = np.asarray(hidden, np.float64)
     T, H = x.shape
     ids, pp, over = route_pack(routing_map, probs, k)
@@ -167,7 +198,7 @@ def forward(hidden, probs, routing_map, W, k):
     E = W.num_experts
     counts, offsets, perm_src, perm_slot, row_of = dispatch_indices(ids, E)
 
-    gs, us, as_, ys = expert_forward(x, *W.shared())
+    gs, us, as_, ys = expert_forward(x, *W.shared(), rnd=rnd)
 
     R = perm_src.size
     y = np.zeros((R, H))
@@ -177,7 +208,7 @@ def forward(hidden, probs, routing_map, W, k):
         if hi == lo:
             continue
         xe = x[perm_src[lo:hi]]
-        g, u, a, ye = expert_forward(xe, *W.routed(e))
+        g, u, a, ye = expert_forward(xe, *W.routed(e), rnd=rnd)
         y[lo:hi] = ye
         routed[e] = (g, u, a)
 
@@ -187,7 +218,8 @@ def forward(hidden, probs, routing_map, W, k):
         out[v] += pp[v, s, None] * y[row_of[v, s]]
 
     cache = dict(x=x, ids=ids, pp=pp, counts=counts, offsets=offsets, perm_src=perm_src,
-                 perm_slot=perm_slot, row_of=row_of, shared=(gs, us, as_), y=y, routed=routed, k=k)
+                 perm_slot=perm_slot, row_of=row_of, shared=(gs, us, as_), y=y, routed=routed, k=k,
+                 precision=precision)
     return out, cache
 
 
@@ -199,6 +231,7 @@ def backward(grad_out, cache, W):
     backward adapter) and the six weight gradients {shared_gate, shared_up,
     shared_down} plus {e: (dWg, dWu, dWd)} for every expert with tokens.
     "core.transformer.moe.megakernel.mok.runtime", _MoKAutograd.backward."""
+    rnd = _rounder(cache["precision"])
     go = np.asarray(grad_out, np.float64)
     x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
     offsets, perm_src, perm_slot, y = cache["offsets"], cache["perm_src"], cache["perm_slot"], cache["y"]
@@ -206,7 +239,7 @@ def backward(grad_out, cache, W):
     E = W.num_experts
 
     gs, us, as_ = cache["shared"]
-    dx_s, dWsg, dWsu, dWsd = expert_backward(x, go, gs, us, as_, *W.shared())
+    dx_s, dWsg, dWsu, dWsd = expert_backward(x, go, np.ones(T), gs, us, as_, *W.shared(), rnd=rnd)
 
     R = perm_src.size
     dx_perm = np.zeros((R, H))
@@ -217,8 +250,8 @@ def backward(grad_out, cache, W):
         lo, hi = offsets[e], offsets[e + 1]
         go_e = go[perm_src[lo:hi]]
         dprob_perm[lo:hi] = np.sum(go_e * y[lo:hi], axis=1)
-        dy = pp_perm[lo:hi, None] * go_e
-        dx, dWg, dWu, dWd = expert_backward(x[perm_src[lo:hi]], dy, g, u, a, *W.routed(e))
+        dx, dWg, dWu, dWd = expert_backward(x[perm_src[lo:hi]], go_e, pp_perm[lo:hi], g, u, a, *W.routed(e),
+                                            rnd=rnd)
         dx_perm[lo:hi] = dx
         routed_grads[e] = (dWg, dWu, dWd)
 

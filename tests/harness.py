@@ -1,0 +1,155 @@
+"""Shared test plumbing: run the CUDA layer through the C ABI on seeded inputs and
+run the fp64 oracle on the same inputs. No layer arithmetic lives here.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+import moe_inputs as MI
+from oracle import moe_oracle as O
+
+
+@dataclasses.dataclass
+class Case:
+    T: int
+    H: int
+    E: int
+    k: int
+    I: int
+    seed: int
+    routing: str = "topk"
+    drop: str = "none"
+
+
+def config_case(cfg_id: int, T: int | None = None, variant: str | None = None) -> Case:
+    c = MI.CONFIGS[cfg_id]
+    return Case(T or c["T"], c["H"], c["E"], c["k"], c["I"], MI.seed_of(cfg_id), variant or c["routing"], c["drop"])
+
+
+@dataclasses.dataclass
+class Inputs:
+    case: Case
+    hidden: torch.Tensor       # bf16 [T,H] on device
+    grad_out: torch.Tensor     # bf16 [T,H]
+    probs: torch.Tensor        # f32 [T,E]
+    routing_map: torch.Tensor  # bool [T,E]
+    weights: dict              # combined-layout bf16 tensors
+    main_grads: dict           # fp32 combined-layout buffers (initial values)
+    probs_np: np.ndarray
+    map_np: np.ndarray
+
+
+def make_inputs(case: Case, device="cuda", routing=None) -> Inputs:
+    r = routing or MI.make_routing(case.T, case.E, case.k, case.seed, case.routing, case.drop)
+    w = MI.make_weights(case.H, case.I, case.E, case.seed, device=device)
+    hidden, grad_out = MI.make_activations(case.T, case.H, case.seed, device=device)
+    mg = MI.make_main_grads(case.H, case.I, case.E, case.seed, device=device)
+    probs = torch.from_numpy(r.probs).to(device)
+    rmap = torch.from_numpy(r.routing_map).to(device)
+    return Inputs(case, hidden, grad_out, probs, rmap, w, mg, r.probs, r.routing_map)
+
+
+@dataclasses.dataclass
+class GpuResult:
+    out: torch.Tensor
+    dhidden: torch.Tensor
+    dprobs: torch.Tensor
+    main_grads: dict
+    layer: object
+
+
+def run_gpu(inp: Inputs, backward=True, main_grads=None, layer=None) -> GpuResult:
+    import mixture_experts_layer_pack_gb300 as M
+    c = inp.case
+    if layer is None:
+        layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, device=inp.hidden.device)
+    w = inp.weights
+    wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
+    out = layer.forward(inp.hidden, inp.probs, inp.routing_map.view(torch.uint8), wv)
+    dh = dp = None
+    mg = None
+    if backward:
+        mg = {n: t.clone() for n, t in (main_grads or inp.main_grads).items()}
+        mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
+        dh, dp = layer.backward(inp.grad_out, mgv)
+    torch.cuda.synchronize()
+    return GpuResult(out, dh, dp, mg, layer)
+
+
+class TorchWeights:
+    """Oracle weight accessor over device bf16 tensors: fp64 copies per expert."""
+
+    def __init__(self, w: dict):
+        self.w = w
+        self.I = w["shared_fc1"].shape[0] // 2
+        self._shared = None
+
+    @property
+    def num_experts(self):
+        return self.w["routed_fc1"].shape[0]
+
+    @staticmethod
+    def _f64(t):
+        return t.detach().to("cpu", torch.float64).numpy()
+
+    def shared(self):
+        if self._shared is None:
+            fc1 = self._f64(self.w["shared_fc1"])
+            self._shared = (fc1[:self.I], fc1[self.I:], self._f64(self.w["shared_fc2"]))
+        return self._shared
+
+    def routed(self, e):
+        fc1 = self._f64(self.w["routed_fc1"][e])
+        return fc1[:self.I], fc1[self.I:], self._f64(self.w["routed_fc2"][e])
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def oracle_full(inp: Inputs, precision="bf16"):
+    """Oracle forward + backward over all tokens."""
+    W = TorchWeights(inp.weights)
+    out, cache = O.forward(f64(inp.hidden), inp.probs_np, inp.map_np, W, inp.case.k, precision=precision)
+    dx, dprobs, grads = O.backward(f64(inp.grad_out), cache, W)
+    return out, dx, dprobs, grads, cache
+
+
+def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3):
+    """Per element |gpu - ref| <= rtol*|ref| + atol_frac*max|ref| (the BF16 tolerance)."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (name, gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{name}: non-finite values in the CUDA result"
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    err = np.abs(gpu - ref)
+    bound = rtol * np.abs(ref) + atol_frac * scale
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} elements out of tolerance; worst at {i}: "
+                             f"gpu={gpu[i]:.6g} ref={ref[i]:.6g}; max|err|/max|ref|={err.max() / max(scale, 1e-300):.3g}")
+    return float(err.max() / max(scale, 1e-300)) if ref.size else 0.0
+
+
+# Normwise bound against the exact (fp64, unrounded) oracle. Each result passes
+# through at most three bf16 operand roundings of relative rms error ~1.7e-3
+# (unit roundoff 2^-8); the largest of millions of Gaussian-like errors is
+# ~5.5 sigma, the largest |ref| at least ~4 rms, so max|err|/max|ref| stays
+# below ~4e-3; 1e-2 leaves headroom without hiding a real fault.
+EXACT_NORMWISE = 1e-2
+
+
+def assert_normwise(gpu, ref, name, bound=EXACT_NORMWISE):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if scale == 0.0:
+        assert np.all(gpu == 0), name
+        return 0.0
+    r = float(np.max(np.abs(gpu - ref)) / scale)
+    assert r <= bound, f"{name}: max|gpu-exact|/max|exact| = {r:.3g} > {bound}"
+    return r

@@ -1,0 +1,280 @@
+"""Parity of the CUDA layer (through the C ABI) with the fp64 oracle.
+
+Routing ids, probs, counts, offsets and permutation are compared bit-exactly.
+Floating-point results are compared, per element, with the oracle at the
+expert GEMMs' operand precision (bf16 operands, exact accumulation) within
+|gpu - ref| <= 2e-2 |ref| + 1e-3 max|ref|, and normwise with the exact oracle
+(no rounding anywhere) within max|gpu - ref| / max|ref| <= 1e-2. Main-grad
+updates are compared as (main_grad_after - main_grad_before) against dW.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_inputs import make_routing
+from oracle import moe_oracle as O
+from tests.harness import (Case, TorchWeights, assert_close, assert_normwise, config_case, f64, make_inputs,
+                           oracle_full, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "cfg1": config_case(1),
+    "tiles_ragged": Case(T=300, H=256, E=8, k=2, I=128, seed=21, drop="iid"),
+    "bn64_skewed": Case(T=517, H=384, E=12, k=3, I=192, seed=22, routing="zipf", drop="multi"),
+    "one_token": Case(T=1, H=128, E=4, k=2, I=64, seed=23),
+}
+
+
+def _export_routing(res, inp):
+    import mixture_experts_layer_pack_gb300 as M
+    c = inp.case
+    dev = inp.hidden.device
+    ids = torch.empty((c.T, c.k), dtype=torch.int32, device=dev)
+    pp = torch.empty((c.T, c.k), dtype=torch.float32, device=dev)
+    counts = torch.empty(c.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(c.E + 1, dtype=torch.int32, device=dev)
+    perm = torch.full((c.T * c.k,), -7, dtype=torch.int32, device=dev)
+    row_of = torch.empty((c.T, c.k), dtype=torch.int32, device=dev)
+    M.moe_export_routing(res.layer.handle, res.layer.saved, ids, pp, counts, offsets, perm, row_of)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in (ids, pp, counts, offsets, perm, row_of)]
+
+
+def _check_routing(res, inp):
+    ids, pp, counts, offsets, perm, row_of = _export_routing(res, inp)
+    rids, rpp, over = O.route_pack(inp.map_np, inp.probs_np, inp.case.k)
+    assert not over.any()
+    rc, ro, rsrc, rslot, rrow = O.dispatch_indices(rids, inp.case.E)
+    R = int(rc.sum())
+    assert np.array_equal(ids, rids)
+    assert np.array_equal(pp.astype(np.float64), rpp)          # fp32 gather: bit-exact
+    assert np.array_equal(counts, rc)
+    assert np.array_equal(offsets, ro)
+    assert np.array_equal(perm[:R], rsrc)
+    assert np.all(perm[R:] == -7)
+    assert np.array_equal(row_of, rrow)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_routing_bit_exact(name):
+    inp = make_inputs(SMALL[name])
+    res = run_gpu(inp, backward=False)
+    _check_routing(res, inp)
+    assert res.layer.device_status() == 0
+
+
+@pytest.mark.parametrize("cfg,variant", [(2, None), (2, "balanced"), (5, None)])
+def test_routing_bit_exact_full_size(cfg, variant):
+    c = config_case(cfg, variant=variant)
+    inp = make_inputs(Case(c.T, 128, c.E, c.k, 64, c.seed, c.routing, c.drop))   # routing only depends on T, E, k
+    res = run_gpu(inp, backward=False)
+    _check_routing(res, inp)
+    if variant == "balanced":
+        _, _, counts, *_ = _export_routing(res, inp)
+        assert np.all(counts == 256)
+
+
+def _compare_full(inp, res, exact=True):
+    out, dx, dprobs, grads, _ = oracle_full(inp, "bf16")
+    c = inp.case
+    I = c.I
+    mg0 = {n: f64(t) for n, t in inp.main_grads.items()}
+    mg1 = {n: f64(t) for n, t in res.main_grads.items()}
+    d = {n: mg1[n] - mg0[n] for n in mg0}
+    got = {"out": f64(res.out), "dhidden": f64(res.dhidden), "dprobs": f64(res.dprobs),
+           "dW shared gate": d["shared_fc1"][:I], "dW shared up": d["shared_fc1"][I:],
+           "dW shared down": d["shared_fc2"]}
+
+    def refs(out, dx, dprobs, grads):
+        return {"out": out, "dhidden": dx, "dprobs": dprobs, "dW shared gate": grads["shared_gate"],
+                "dW shared up": grads["shared_up"], "dW shared down": grads["shared_down"]}
+
+    errs = {n: assert_close(got[n], r, n) for n, r in refs(out, dx, dprobs, grads).items()}
+    for e in range(c.E):
+        if e in grads["routed"]:
+            dWg, dWu, dWd = grads["routed"][e]
+            assert_close(d["routed_fc1"][e, :I], dWg, f"dW routed gate[{e}]")
+            assert_close(d["routed_fc1"][e, I:], dWu, f"dW routed up[{e}]")
+            assert_close(d["routed_fc2"][e], dWd, f"dW routed down[{e}]")
+        else:   # an expert with no tokens keeps its main_grad bitwise
+            assert np.array_equal(mg1["routed_fc1"][e], mg0["routed_fc1"][e])
+            assert np.array_equal(mg1["routed_fc2"][e], mg0["routed_fc2"][e])
+    if exact:
+        out, dx, dprobs, grads, _ = oracle_full(inp, "exact")
+        for n, r in refs(out, dx, dprobs, grads).items():
+            errs["exact " + n] = assert_normwise(got[n], r, n)
+        for e, (dWg, dWu, dWd) in grads["routed"].items():
+            assert_normwise(d["routed_fc1"][e, :I], dWg, f"dW routed gate[{e}]")
+            assert_normwise(d["routed_fc1"][e, I:], dWu, f"dW routed up[{e}]")
+            assert_normwise(d["routed_fc2"][e], dWd, f"dW routed down[{e}]")
+    return errs
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_parity_small(name):
+    inp = make_inputs(SMALL[name])
+    res = run_gpu(inp)
+    _compare_full(inp, res)
+    assert res.layer.device_status() == 0
+
+
+def test_layer_parity_config2_full():
+    """Proxy-like layer (T=4096, H=2048, E=96, top-6, I=1024): every output element."""
+    inp = make_inputs(config_case(2))
+    res = run_gpu(inp)
+    errs = _compare_full(inp, res)
+    print("config 2 max|err|/max|ref|:", {n: f"{v:.2e}" for n, v in errs.items()})
+
+
+def test_layer_parity_config2_force_balanced():
+    inp = make_inputs(config_case(2, variant="balanced"))
+    res = run_gpu(inp)
+    _compare_full(inp, res)
+
+
+def test_wgrad_accumulates_once_bitwise():
+    """main_grad += dW is one fp32 add per element: a pass from zero gives dW
+    exactly, a pass from mg0 must equal fl32(mg0 + dW) bit for bit."""
+    inp = make_inputs(SMALL["tiles_ragged"])
+    zero = {n: torch.zeros_like(t) for n, t in inp.main_grads.items()}
+    r0 = run_gpu(inp, main_grads=zero)
+    r1 = run_gpu(inp, layer=r0.layer)
+    for n in inp.main_grads:
+        expect = inp.main_grads[n] + r0.main_grads[n]       # fp32 add on the device
+        assert torch.equal(r1.main_grads[n], expect), n
+
+
+def test_backward_twice_accumulates_twice():
+    """Two backward passes over one forward (the skewed workload accumulates over
+    two calls): the second adds the same dW again."""
+    import mixture_experts_layer_pack_gb300 as M
+    inp = make_inputs(SMALL["bn64_skewed"])
+    zero = {n: torch.zeros_like(t) for n, t in inp.main_grads.items()}
+    r0 = run_gpu(inp, main_grads=zero)
+    mg = {n: t.clone() for n, t in inp.main_grads.items()}
+    mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
+    r0.layer.backward(inp.grad_out, mgv)
+    r0.layer.backward(inp.grad_out, mgv)
+    torch.cuda.synchronize()
+    for n in mg:
+        expect = (inp.main_grads[n] + r0.main_grads[n]) + r0.main_grads[n]
+        assert torch.equal(mg[n], expect), n
+
+
+def test_determinism():
+    inp = make_inputs(SMALL["bn64_skewed"])
+    a = run_gpu(inp)
+    b = run_gpu(inp)
+    assert torch.equal(a.out, b.out) and torch.equal(a.dhidden, b.dhidden) and torch.equal(a.dprobs, b.dprobs)
+    for n in a.main_grads:
+        assert torch.equal(a.main_grads[n], b.main_grads[n]), n
+
+
+def test_rows_without_routes_and_zero_token_experts():
+    c = Case(T=200, H=128, E=6, k=2, I=64, seed=31)
+    r = make_routing(c.T, c.E, c.k, c.seed)
+    r.routing_map[:, 4] = False           # expert 4 gets no token
+    r.probs[:, 4] = 0.0
+    r.routing_map[::7] = False            # every 7th token has no route at all
+    r.probs[::7] = 0.0
+    inp = make_inputs(c, routing=r)
+    res = run_gpu(inp)
+    _compare_full(inp, res)
+    assert torch.equal(res.main_grads["routed_fc1"][4], inp.main_grads["routed_fc1"][4])
+    assert torch.equal(res.main_grads["routed_fc2"][4], inp.main_grads["routed_fc2"][4])
+    assert torch.all(res.dprobs[::7] == 0)
+
+
+def test_off_map_probs_ignored_and_prob_zero_routes():
+    c = Case(T=150, H=128, E=5, k=2, I=64, seed=32)
+    r = make_routing(c.T, c.E, c.k, c.seed)
+    r.probs[~r.routing_map] = 123.0       # off-map probs: must be ignored
+    on = np.argwhere(r.routing_map)[:10]
+    r.probs[on[:, 0], on[:, 1]] = 0.0     # routed with prob 0: still computed
+    inp = make_inputs(c, routing=r)
+    res = run_gpu(inp)
+    _compare_full(inp, res)
+    assert torch.all(res.dprobs[~inp.routing_map] == 0)
+
+
+def test_zero_tokens():
+    import mixture_experts_layer_pack_gb300 as M
+    c = Case(T=0, H=128, E=4, k=2, I=64, seed=33)
+    inp = make_inputs(c)
+    layer = M.MoELayer(16, c.H, c.E, c.k, c.I)
+    w = inp.weights
+    wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
+    layer.forward(inp.hidden, inp.probs, inp.routing_map.view(torch.uint8), wv)
+    mg = {n: t.clone() for n, t in inp.main_grads.items()}
+    mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
+    layer.backward(inp.grad_out, mgv)
+    torch.cuda.synchronize()
+    for n in mg:
+        assert torch.equal(mg[n], inp.main_grads[n])
+    assert layer.device_status() == 0
+
+
+def test_row_with_too_many_routes_is_reported():
+    c = Case(T=64, H=128, E=6, k=2, I=64, seed=34)
+    r = make_routing(c.T, c.E, c.k, c.seed)
+    r.routing_map[5, :3] = True           # three routes with k = 2
+    inp = make_inputs(c, routing=r)
+    res = run_gpu(inp, backward=False)
+    assert res.layer.device_status() == 3     # MOE_ERR_ROUTING
+    assert res.layer.device_status() == 0     # cleared by the read
+
+
+def _routed_expert_grads(inp, W, e):
+    """Oracle dW of expert e from the tokens routed to it (dW_e depends on nothing else)."""
+    toks = np.flatnonzero(inp.map_np[:, e])
+    m = np.zeros((toks.size, inp.case.E), bool)
+    m[:, e] = True
+    _, cache = O.forward(f64(inp.hidden[torch.from_numpy(toks).to(inp.hidden.device)]), inp.probs_np[toks], m, W,
+                         inp.case.k, precision="bf16")
+    _, _, g = O.backward(f64(inp.grad_out[torch.from_numpy(toks).to(inp.hidden.device)]), cache, W)
+    return g["routed"][e]
+
+
+@pytest.mark.slow
+def test_layer_parity_config5_sampled():
+    """Skewed layer (T=16384, H=4096, E=128, top-8, I=1536) at full size: sampled
+    tokens for out/dhidden/dprobs, the hottest and a median expert for routed
+    main_grad, all tokens for the shared expert's main_grad."""
+    inp = make_inputs(config_case(5))
+    res = run_gpu(inp)
+    c = inp.case
+    W = TorchWeights(inp.weights)
+    rng = np.random.default_rng(5)
+    toks = np.sort(rng.choice(c.T, 48, replace=False))
+    tt = torch.from_numpy(toks).to(inp.hidden.device)
+    out, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], inp.map_np[toks], W, c.k, precision="bf16")
+    dx, dprobs, _ = O.backward(f64(inp.grad_out[tt]), cache, W)
+    assert_close(f64(res.out[tt]), out, "out (sampled)")
+    assert_close(f64(res.dhidden[tt]), dx, "dhidden (sampled)")
+    assert_close(f64(res.dprobs[tt]), dprobs, "dprobs (sampled)")
+    assert torch.isfinite(res.out).all() and torch.isfinite(res.dhidden).all() and torch.isfinite(res.dprobs).all()
+
+    counts = inp.map_np.sum(0)
+    hot = int(np.argmax(counts))
+    med = int(np.argsort(counts)[c.E // 2])
+    I = c.I
+    for e in (hot, med):
+        dWg, dWu, dWd = _routed_expert_grads(inp, W, e)
+        d1 = f64(res.main_grads["routed_fc1"][e]) - f64(inp.main_grads["routed_fc1"][e])
+        d2 = f64(res.main_grads["routed_fc2"][e]) - f64(inp.main_grads["routed_fc2"][e])
+        assert_close(d1[:I], dWg, f"dW routed gate[{e}]")
+        assert_close(d1[I:], dWu, f"dW routed up[{e}]")
+        assert_close(d2, dWd, f"dW routed down[{e}]")
+    for e in np.flatnonzero(counts == 0):
+        assert torch.equal(res.main_grads["routed_fc1"][e], inp.main_grads["routed_fc1"][e])
+
+    # shared expert over all tokens: a map with no routes leaves only the shared path
+    m0 = np.zeros_like(inp.map_np)
+    _, cache = O.forward(f64(inp.hidden), inp.probs_np, m0, W, c.k, precision="bf16")
+    _, _, g = O.backward(f64(inp.grad_out), cache, W)
+    d1 = f64(res.main_grads["shared_fc1"]) - f64(inp.main_grads["shared_fc1"])
+    d2 = f64(res.main_grads["shared_fc2"]) - f64(inp.main_grads["shared_fc2"])
+    assert_close(d1[:I], g["shared_gate"], "dW shared gate")
+    assert_close(d1[I:], g["shared_up"], "dW shared up")
+    assert_close(d2, g["shared_down"], "dW shared down")
