@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""MoE layer forward+backward throughput on GB300 (tokens/s, useful TFLOPS, roofline).
+
+One step = one forward and one backward of the whole layer (route-pack,
+dispatch, routed and shared SwiGLU experts, combine; dgrad, dense dprobs,
+fused fp32 main_grad accumulation) over one batch of seeded synthetic input,
+through the library's C ABI. Default workload: the Proxy-like layer, T=4096
+tokens, H=2048, 96 routed experts top-6, one shared expert, I=1024, BF16.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N>1 runs one independent replica per GPU (launched by torch.distributed.run);
+the layer has no exchange step on one GPU. `--impl reference` times the fp64
+CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s and TFLOPS, % of GB300 BF16/MXFP8 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- cross-rank helpers
+def reduce_max(values, world, device):
+    """Elementwise max over ranks (values: list of floats)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(units_per_rank, elapsed_s_max):
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    return sum(units_per_rank) / elapsed_s_max if elapsed_s_max > 0 else 0.0
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_id)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(dev_index):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return dev_index
+
+
+# ----------------------------------------------------------------- algorithmic work
+def kernel_work(name, T, H, E, k, I, R, E_act):
+    """(algorithmic flops, algorithmic HBM bytes) of one launch of a kernel class.
+
+    Bytes count each operand read once and each result written once (no padding
+    rows, no re-reads); flops count a multiply-add as 2. Weights of experts
+    without tokens are not read."""
+    b2, b4 = 2, 4
+    W_fc1, W_down = E_act * 2 * I * H * b2, E_act * H * I * b2
+    table = {
+        "route_pack": (0, T * E + T * k * (b4 * 3 + b4)),
+        "route_scan": (0, 0),
+        "route_place": (0, T * k * 8 + R * 12),
+        "gather_rows": (0, 2 * R * H * b2),
+        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * b2 + W_fc1 + R * I * b2 + R * 2 * I * b4),
+        "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * b2 + T * 2 * I * b4),
+        "gemm_fwd_down_routed": (2 * R * I * H, R * I * b2 + W_down + R * H * b4),
+        "gemm_fwd_down_shared": (2 * T * I * H, T * I * b2 + H * I * b2 + T * H * b4),
+        "combine": (0, T * H * b4 + R * H * b4 + T * H * b2),
+        "gemm_bwd_down_routed": (2 * R * H * I, R * H * b2 + W_down + R * I * b2 + R * 2 * I * b4
+                                 + R * 2 * I * b2 + R * I * b2),
+        "gemm_bwd_down_shared": (2 * T * H * I, T * H * b2 + H * I * b2 + T * I * b2 + T * 2 * I * b4
+                                 + T * 2 * I * b2),
+        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * b2 + W_fc1 + R * H * b4),
+        "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * b2 + 2 * I * H * b2 + T * H * b4),
+        "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * b2 + R * H * b2 + E_act * 2 * I * H * 8),
+        "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * b2 + E_act * H * I * 8),
+        "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * b2 + T * H * b2 + 2 * I * H * 8),
+        "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * b2 + H * I * 8),
+        "unpermute": (0, T * H * b4 + R * H * b4 + T * H * b2 + T * E * b4),
+    }
+    return table[name]
+
+
+def roofline_of(name, ms_per_launch, work, peaks, peaks_kind, traffic=None):
+    flops, nbytes = work
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops > 0 and flops / max(nbytes, 1) > ridge:
+        achieved = flops / (ms_per_launch * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
+    else:
+        achieved = nbytes / (ms_per_launch * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
+    r.update({"frac": achieved / peak, "traffic": traffic, "kernel": name, "ms_per_launch": ms_per_launch,
+              "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "peak_source": f"of {peaks_kind}"})
+    return r
+
+
+def useful_flops(R, T, H, I):
+    """18 (R + T) H I: forward, dgrad and wgrad are 6 (R+T) H I each."""
+    return 18 * (R + T) * H * I
+
+
+# ----------------------------------------------------------------- the oracle leg
+def oracle_sample(cfg_id, T_sample, offset=0):
+    """Inputs for the CPU oracle: a token sample of the workload, full weights (fp64)."""
+    import numpy as np
+    import torch
+
+    import moe_inputs as MI
+    from oracle import moe_oracle as O
+    c = MI.CONFIGS[cfg_id]
+    seed = MI.seed_of(cfg_id)
+    r = MI.config_routing(cfg_id)
+    w = MI.make_weights(c["H"], c["I"], c["E"], seed, device="cpu")
+    hidden, grad_out = MI.make_activations(c["T"], c["H"], seed, device="cpu")
+    W = O.DenseWeights.from_combined(*(w[n].to(torch.float64).numpy() for n in
+                                       ("shared_fc1", "shared_fc2", "routed_fc1", "routed_fc2")))
+    sl = slice(offset, offset + T_sample)
+    return dict(W=W, x=hidden[sl].to(torch.float64).numpy(), go=grad_out[sl].to(torch.float64).numpy(),
+                probs=r.probs[sl], map=np.ascontiguousarray(r.routing_map[sl]), k=c["k"])
+
+
+def time_oracle(sample):
+    from oracle import moe_oracle as O
+    t0 = time.perf_counter()
+    _, cache = O.forward(sample["x"], sample["probs"], sample["map"], sample["W"], sample["k"])
+    O.backward(sample["go"], cache, sample["W"])
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(cfg_id, T_sample=1024):
+    s = oracle_sample(cfg_id, T_sample)
+    dt = time_oracle(s)
+    return {"value": T_sample / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, forward+backward of the first {T_sample} tokens of the workload "
+                      f"(full weights), {dt:.2f} s"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import moe_inputs as MI
+    c = MI.CONFIGS[args.config]
+    T_step = 128
+    s = oracle_sample(args.config, T_step * 8)
+    subs = []
+    for j in range(8):
+        sl = slice(j * T_step, (j + 1) * T_step)
+        subs.append(dict(W=s["W"], x=s["x"][sl], go=s["go"][sl], probs=s["probs"][sl], map=s["map"][sl], k=s["k"]))
+    for i in range(args.warmup):
+        time_oracle(subs[i % 8])
+    t = 0.0
+    for i in range(args.steps):
+        t += time_oracle(subs[i % 8])
+    value = args.steps * T_step / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; the pages' training data are not available)",
+            "config": {"workload": MI.WORKLOAD_NAMES[args.config], "T": c["T"], "H": c["H"], "E": c["E"],
+                       "k": c["k"], "I": c["I"], "sample_tokens_per_step": T_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{T_step} tokens of the workload per step (full weights), fp64 numpy"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import mixture_experts_layer_pack_gb300 as M
+    import moe_inputs as MI
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    cid = args.config
+    c = MI.CONFIGS[cid]
+    if c["routed"] != "bf16":
+        raise SystemExit(f"config {cid}: routed {c['routed']} weights are not built into this bench")
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    seed = MI.seed_of(cid)
+    r = MI.config_routing(cid)
+    R = int(r.routing_map.sum())
+    E_act = int((r.routing_map.sum(0) > 0).sum())
+    w = MI.make_weights(H, I, E, seed, device=dev)
+    hidden, grad_out = MI.make_activations(T, H, seed, device=dev)
+    mg = MI.make_main_grads(H, I, E, seed, device=dev)
+    probs = torch.from_numpy(r.probs).to(dev)
+    rmap = torch.from_numpy(r.routing_map).to(dev).view(torch.uint8)
+
+    layer = M.MoELayer(T, H, E, k, I, device=dev)
+    wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
+    mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
+    out = torch.empty_like(hidden)
+    dh = torch.empty_like(hidden)
+    dp = torch.empty((T, E), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        M.moe_forward(layer.handle, T, hidden, probs, rmap, wv, out, layer.saved, stream)
+        M.moe_backward(layer.handle, grad_out, layer.saved, dh, dp, mgv, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise SystemExit("device status reported an error during warm-up")
+
+    # ---- timed region: K steps, per-kernel events inside, clocks sampled
+    sampler = ClockSampler(gpu_id_for(local_rank))
+    sampler.start()
+    M.moe_profile_read(layer.handle)                     # drop anything recorded before
+    M.moe_profile_enable(layer.handle, True)
+    launches0 = M.moe_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = M.moe_launch_count() - launches0
+    M.moe_profile_enable(layer.handle, False)
+    clocks = sampler.stop()
+    kernels = M.moe_profile_read(layer.handle)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = reduce_max([ms], world, dev)[0]
+    value = aggregate([args.steps * T] * world, ms_max / 1e3)
+    flops = useful_flops(R, T, H, I)
+    tflops = flops * args.steps * world / (ms_max / 1e3) / 1e12
+    peaks, peaks_kind = load_peaks()
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    h_hidden = hidden.cpu().pin_memory()
+    h_grad = grad_out.cpu().pin_memory()
+    h_probs = probs.cpu().pin_memory()
+    h_map = rmap.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_dh = torch.empty(dh.shape, dtype=dh.dtype, pin_memory=True)
+    h_dp = torch.empty(dp.shape, dtype=dp.dtype, pin_memory=True)
+    d_hidden, d_grad, d_probs, d_map = (torch.empty_like(t, device=dev) for t in (h_hidden, h_grad, h_probs, h_map))
+
+    def e2e_step():
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_probs.copy_(h_probs, non_blocking=True)
+        d_map.copy_(h_map, non_blocking=True)
+        d_grad.copy_(h_grad, non_blocking=True)
+        layer.forward(d_hidden, d_probs, d_map, wv, out=out, stream=stream)
+        layer.backward(d_grad, mgv, dhidden=dh, dprobs=dp, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_dh.copy_(dh, non_blocking=True)
+        h_dp.copy_(dp, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(10, args.steps // 4)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = reduce_max([time.perf_counter() - t0], world, dev)[0]
+    h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_grad, h_probs, h_map))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dh, h_dp))
+    e2e = {"value": aggregate([e2e_steps * T] * world, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---- roofline of the dominant kernel
+    per_kernel = {}
+    for name, (tot, n) in kernels.items():
+        if n:
+            per_kernel[name] = {"ms_per_launch": tot / n, "launches": n, "share": 0.0}
+    total_k = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
+    for v in per_kernel.values():
+        v["share"] = v["ms_per_launch"] * v["launches"] / total_k if total_k else 0.0
+    top = max(per_kernel, key=lambda n: per_kernel[n]["share"])
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            traffic = json.load(open(tr_path)).get(MI.WORKLOAD_NAMES[cid], {}).get(top)
+        except Exception:
+            traffic = None
+    roof = roofline_of(top, per_kernel[top]["ms_per_launch"], kernel_work(top, T, H, E, k, I, R, E_act), peaks,
+                       peaks_kind, traffic)
+    for name, v in per_kernel.items():
+        f, b = kernel_work(name, T, H, E, k, I, R, E_act)
+        ms_l = v["ms_per_launch"] * 1e-3
+        v["tflops"] = f / ms_l / 1e12 if f else 0.0
+        v["gbs"] = b / ms_l / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded routing, N(0,0.02) weights, N(0,1) activations; random init)",
+            "config": {"workload": MI.WORKLOAD_NAMES[cid], "T": T, "H": H, "E": E, "k": k, "I": I,
+                       "valid_routes": R, "routing": "softmax over N(0,1) logits, top-6, dense probs/map",
+                       "main_grad": "fp32, accumulated in place every step",
+                       "l2": "inputs larger than L2: routed weights %.2f GB + main_grad %.2f GB per step"
+                             % (3 * E * I * H * 2 / 1e9, 3 * (E + 1) * I * H * 4 / 1e9),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tflops": tflops,
+            "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+            "peaks": {**peaks, "source": peaks_kind},
+            "useful_flops_per_step": flops,
+            "roofline": roof, "kernels": per_kernel, "gpu_launches": launches, "clocks": clocks, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cid)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

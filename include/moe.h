@@ -50,7 +50,7 @@ typedef enum {
 typedef enum { MOE_W_BF16 = 0, MOE_W_MXFP8 = 1 } moe_wtype;
 
 /* Layer shape. Routed and shared experts share `inter` (PR #6572, Supported
- * configurations: MOK limitations). hidden and inter must be multiples of 64;
+ * configurations: MOK limitations). hidden must be a multiple of 128, inter of 64;
  * 1 <= topk <= 32; 1 <= num_experts <= 1024. swiglu_limit must be 0: the clamp
  * exists on the pages (PR #8210 review: swiglu_limit) without a definition. */
 typedef struct {
@@ -154,6 +154,28 @@ moe_status moe_device_status(moe_handle* h, void* stream);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t moe_launch_count(void);
+
+/* Kernel classes of the layer, in the order moe_profile_read reports them. */
+enum {
+    MOE_K_ROUTE_PACK = 0, MOE_K_ROUTE_SCAN, MOE_K_ROUTE_PLACE, MOE_K_GATHER,
+    MOE_K_FWD_GU_ROUTED, MOE_K_FWD_GU_SHARED, MOE_K_FWD_DOWN_ROUTED, MOE_K_FWD_DOWN_SHARED, MOE_K_COMBINE,
+    MOE_K_BWD_DOWN_ROUTED, MOE_K_BWD_DOWN_SHARED, MOE_K_BWD_GU_ROUTED, MOE_K_BWD_GU_SHARED,
+    MOE_K_WGRAD_FC1_ROUTED, MOE_K_WGRAD_DOWN_ROUTED, MOE_K_WGRAD_FC1_SHARED, MOE_K_WGRAD_DOWN_SHARED,
+    MOE_K_UNPERMUTE, MOE_K_COUNT
+};
+
+/* Per-kernel timing for measurement. While enabled, every kernel the handle
+ * launches is bracketed by a pair of CUDA events recorded on the launch
+ * stream: no extra GPU work and no host synchronisation. */
+moe_status moe_profile_enable(moe_handle* h, int enable);
+
+/* Synchronises the recorded events and writes, per kernel class (n entries,
+ * n <= MOE_K_COUNT), the summed device time in milliseconds and the number of
+ * launches since the previous read; then forgets them. Host arrays. */
+moe_status moe_profile_read(moe_handle* h, double* total_ms, int64_t* launches, int n);
+
+/* Name of a kernel class ("gemm_wgrad_fc1_routed", ...), or NULL. */
+const char* moe_kernel_name(int kernel_class);
 
 const char* moe_status_string(moe_status s);
 

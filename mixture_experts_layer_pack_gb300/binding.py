@@ -48,7 +48,8 @@ _LIB = None
 _LOCK = threading.Lock()
 EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size", "moe_saved_create",
             "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
-            "moe_launch_count", "moe_status_string")
+            "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name")
+MOE_K_COUNT = 18
 
 
 def lib_path() -> str:
@@ -84,10 +85,15 @@ def load(build_if_missing: bool = True):
         L.moe_device_status.argtypes = [c_void_p, c_void_p]
         L.moe_launch_count.argtypes = []
         L.moe_launch_count.restype = ctypes.c_uint64
+        L.moe_profile_enable.argtypes = [c_void_p, c_int32]
+        L.moe_profile_read.argtypes = [c_void_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int64), c_int32]
+        L.moe_kernel_name.argtypes = [c_int32]
+        L.moe_kernel_name.restype = ctypes.c_char_p
         L.moe_status_string.argtypes = [c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_workspace_size", "moe_saved_size", "moe_create", "moe_saved_create", "moe_forward",
-                     "moe_backward", "moe_export_routing", "moe_device_status"):
+                     "moe_backward", "moe_export_routing", "moe_device_status", "moe_profile_enable",
+                     "moe_profile_read"):
             getattr(L, name).restype = c_int32
         _LIB = L
         return L
@@ -173,6 +179,23 @@ def moe_device_status(h, stream=None) -> int:
 
 def moe_launch_count() -> int:
     return int(load().moe_launch_count())
+
+
+def moe_profile_enable(h, enable: bool = True):
+    _check(load().moe_profile_enable(h, 1 if enable else 0), "moe_profile_enable")
+
+
+def moe_profile_read(h) -> dict:
+    """{kernel name: (summed ms, launches)} since the previous read."""
+    ms = (ctypes.c_double * MOE_K_COUNT)()
+    n = (c_int64 * MOE_K_COUNT)()
+    _check(load().moe_profile_read(h, ms, n, MOE_K_COUNT), "moe_profile_read")
+    return {moe_kernel_name(i): (ms[i], n[i]) for i in range(MOE_K_COUNT)}
+
+
+def moe_kernel_name(i: int) -> str:
+    r = load().moe_kernel_name(i)
+    return r.decode() if r else None
 
 
 # ------------------------------------------------------------------ marshalling helpers

@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 namespace moe {
 static std::atomic<uint64_t> g_launches{0};
@@ -195,7 +196,58 @@ struct moe_handle {
     Workspace ws;
     int device;
     int sms;
+    // per-kernel timing (moe_profile_enable)
+    bool profiling = false;
+    struct Rec {
+        int cls;
+        cudaEvent_t start, stop;
+    };
+    std::vector<Rec> recs;        // recorded, not yet read
+    std::vector<cudaEvent_t> pool;  // free events
 };
+
+namespace {
+
+cudaEvent_t take_event(moe_handle* h) {
+    if (!h->pool.empty()) {
+        cudaEvent_t e = h->pool.back();
+        h->pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// brackets the launches of one kernel class with events while profiling
+struct Timed {
+    moe_handle* h;
+    int cls;
+    cudaStream_t st;
+    cudaEvent_t start = nullptr;
+    Timed(moe_handle* h_, int cls_, cudaStream_t st_) : h(h_), cls(cls_), st(st_) {
+        if (h->profiling && (start = take_event(h)) != nullptr) cudaEventRecord(start, st);
+    }
+    ~Timed() {
+        if (!start) return;
+        cudaEvent_t stop = take_event(h);
+        if (!stop) {
+            h->pool.push_back(start);
+            return;
+        }
+        cudaEventRecord(stop, st);
+        h->recs.push_back({cls, start, stop});
+    }
+};
+
+const char* const kKernelNames[MOE_K_COUNT] = {
+    "route_pack", "route_scan", "route_place", "gather_rows",
+    "gemm_fwd_gu_routed", "gemm_fwd_gu_shared", "gemm_fwd_down_routed", "gemm_fwd_down_shared", "combine",
+    "gemm_bwd_down_routed", "gemm_bwd_down_shared", "gemm_bwd_gu_routed", "gemm_bwd_gu_shared",
+    "gemm_wgrad_fc1_routed", "gemm_wgrad_down_routed", "gemm_wgrad_fc1_shared", "gemm_wgrad_down_shared",
+    "unpermute"};
+
+}  // namespace
 
 struct moe_saved {
     moe_handle* h;
@@ -268,7 +320,15 @@ moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_b
     return MOE_OK;
 }
 
-void moe_destroy(moe_handle* h) { delete h; }
+void moe_destroy(moe_handle* h) {
+    if (!h) return;
+    for (auto& r : h->recs) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
+    delete h;
+}
 
 moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved** out) {
     if (!h || !out) return MOE_ERR_INVALID_ARG;
@@ -314,12 +374,16 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     const int rows = int(s.rows);
 
     // dispatch: route-pack, segment scan, stable placement, row gather
-    MOE_CU(launch_route_pack(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.hist, ws.status, st));
+    { Timed tm_(h, MOE_K_ROUTE_PACK, st);
+    MOE_CU(launch_route_pack(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.hist, ws.status, st)); }
+    { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
     MOE_CU(launch_route_scan(ws.hist, nchunks, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta, b.perm_src,
-                             b.pp_perm, st));
-    MOE_CU(launch_route_place(b.ids, b.pp, Ti, E, k, ws.hist, b.offs_pad, b.perm_src, b.pp_perm, b.row_of, st));
+                             b.pp_perm, st)); }
+    { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
+    MOE_CU(launch_route_place(b.ids, b.pp, Ti, E, k, ws.hist, b.offs_pad, b.perm_src, b.pp_perm, b.row_of, st)); }
+    { Timed tm_(h, MOE_K_GATHER, st);
     MOE_CU(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), b.perm_src, b.meta, rows, H, b.x_perm,
-                              h->sms, st));
+                              h->sms, st)); }
 
     GemmMaps m;
     // routed gate/up + SwiGLU
@@ -339,6 +403,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.ld_out0 = I;
         a.outf = b.gu;
         a.ld_outf = 2 * I;
+        Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // shared gate/up + SwiGLU
@@ -357,6 +422,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.ld_out0 = I;
         a.outf = b.gu_s;
         a.ld_outf = 2 * I;
+        Timed tm_(h, MOE_K_FWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // routed down projection, scaled by the route's prob
@@ -374,6 +440,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.row_scale = b.pp_perm;
         a.outf = ws.yx;
         a.ld_outf = H;
+        Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // shared down projection
@@ -389,9 +456,11 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.rows_valid = Ti;
         a.outf = ws.ys_dxs;
         a.ld_outf = H;
+        Timed tm_(h, MOE_K_FWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // combine
+    Timed tm_(h, MOE_K_COMBINE, st);
     MOE_CU(launch_combine(ws.ys_dxs, ws.yx, b.row_of, Ti, H, k, static_cast<__nv_bfloat16*>(out), h->sms, st));
     return MOE_OK;
 }
@@ -413,7 +482,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     const int rows = int(s.rows);
     const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(grad_out);
 
-    MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, h->sms, st));
+    { Timed tm_(h, MOE_K_GATHER, st);
+    MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, h->sms, st)); }
 
     GemmMaps m;
     // routed dgrad through the down projection + SwiGLU backward + dprob partials
@@ -438,6 +508,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.ld_out0 = 2 * I;
         a.out1 = ws.ap;
         a.ld_out1 = I;
+        Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // shared dgrad through the down projection + SwiGLU backward
@@ -457,6 +528,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.ld_inf = 2 * I;
         a.out0 = ws.dgdu_s;
         a.ld_out0 = 2 * I;
+        Timed tm_(h, MOE_K_BWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // routed dgrad through gate/up
@@ -474,6 +546,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.gate_up_split = I;
         a.outf = ws.yx;
         a.ld_outf = H;
+        Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // shared dgrad through gate/up
@@ -490,6 +563,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.gate_up_split = I;
         a.outf = ws.ys_dxs;
         a.ld_outf = H;
+        Timed tm_(h, MOE_K_BWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // routed wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e
@@ -510,6 +584,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.mg1_es = mg->strides[4][0];
         a.mg1_rs = mg->strides[4][1];
         a.m_split = I;
+        Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
     // routed wgrad of down: main_grad[e] += go_perm_e^T (p a)_e
@@ -526,6 +601,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.mg0 = mg->routed_down;
         a.mg0_es = mg->strides[5][0];
         a.mg0_rs = mg->strides[5][1];
+        Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
     // shared wgrad of gate/up
@@ -544,6 +620,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.mg1 = mg->shared_up;
         a.mg1_rs = mg->strides[1][1];
         a.m_split = I;
+        Timed tm_(h, MOE_K_WGRAD_FC1_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
     // shared wgrad of down
@@ -558,9 +635,11 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = I / bn;
         a.mg0 = mg->shared_down;
         a.mg0_rs = mg->strides[2][1];
+        Timed tm_(h, MOE_K_WGRAD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
     // dhidden = shared + un-permuted routed dgrad; dense dprobs
+    Timed tm_(h, MOE_K_UNPERMUTE, st);
     MOE_CU(launch_unpermute(ws.ys_dxs, ws.yx, b.row_of, b.ids, ws.partial, s.n_part, Ti, H, k, E,
                             static_cast<__nv_bfloat16*>(dhidden), dprobs, h->sms, st));
     return MOE_OK;
@@ -589,6 +668,38 @@ moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* id
         MOE_CU(launch_export_routing(b.ids, b.row_of, b.perm_src, b.counts, b.offsets, b.offs_pad, b.mtile_expert,
                                      b.meta, int(T), int(s.k), int(s.rows), perm_src, row_of, st));
     return MOE_OK;
+}
+
+moe_status moe_profile_enable(moe_handle* h, int enable) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->profiling = enable != 0;
+    return MOE_OK;
+}
+
+moe_status moe_profile_read(moe_handle* h, double* total_ms, int64_t* launches, int n) {
+    if (!h || n < 0 || n > MOE_K_COUNT || (n > 0 && (!total_ms || !launches))) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        total_ms[i] = 0.0;
+        launches[i] = 0;
+    }
+    moe_status st = MOE_OK;
+    for (auto& r : h->recs) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+            st = MOE_ERR_CUDA;
+        if (r.cls < n) {
+            total_ms[r.cls] += ms;
+            launches[r.cls] += 1;
+        }
+        h->pool.push_back(r.start);
+        h->pool.push_back(r.stop);
+    }
+    h->recs.clear();
+    return st;
+}
+
+const char* moe_kernel_name(int kernel_class) {
+    return (kernel_class >= 0 && kernel_class < MOE_K_COUNT) ? kKernelNames[kernel_class] : nullptr;
 }
 
 moe_status moe_device_status(moe_handle* h, void* stream) {

@@ -43,6 +43,13 @@ and the prob-weighted activation p*a that multiplies grad_out in the down
 projection's weight gradient -- and accumulates in fp64. Inputs (hidden,
 grad_out, weights) are bf16 already.
 
+A bf16 rounding is a discrete decision taken on a value the kernel evaluates
+in fp32 (FP32 accumulator), so near a rounding midpoint both neighbours are
+correct results. ``envelope`` (bf16 mode) bounds, per output element, how far
+the other valid roundings of every operand that lies within the fp32
+evaluation band of a midpoint can move the result (propagated with absolute
+values); elsewhere it is 0.
+
 Everything here is fp64 numpy; ``@`` (a BLAS matmul) is the only library step.
 """
 from __future__ import annotations
@@ -134,6 +141,31 @@ def bf16_round(x):
     x = np.asarray(x, np.float64)
     m, e = np.frexp(x)                     # x = m * 2^e, |m| in [0.5, 1)
     return np.ldexp(np.round(m * 256.0), e - 8)   # np.round: half to even
+
+
+U32 = 2.0 ** -24        # fp32 unit roundoff
+
+
+def bf16_alternative(x, band):
+    """Distance from bf16_round(x) to the other neighbour of x where x lies
+    within ``band`` of a rounding midpoint (both roundings are then valid
+    results of an fp32 evaluation of x), else 0."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    ulp = np.ldexp(1.0, e - 8)
+    scaled = np.abs(m) * 256.0
+    dist = np.abs(scaled - np.floor(scaled) - 0.5) * ulp
+    return np.where(dist <= band, ulp, 0.0)
+
+
+def fp32_dot_band(terms_sq_sum, K):
+    """Evaluation band of an fp32-accumulated dot product of length K whose
+    terms t have sum(t^2) = terms_sq_sum: U32 * sqrt(K) * ||t||_2 (about ten
+    times the typical accumulation error)."""
+    return U32 * np.sqrt(K) * np.sqrt(terms_sq_sum)
+
+
+ELEMENTWISE_BAND = 2.0 ** -20   # relative band of fp32 elementwise evaluation (exp, products)
 
 
 def _rounder(precision):
@@ -281,3 +313,77 @@ def accumulate_main_grads(main_grads, grads):
         out["routed_down"][e] += dWd
     return out
 
+
+
+def silu_grad2_bound():
+    """max |d^2 silu / dz^2| over the reals (about 0.5)."""
+    return 0.5
+
+
+def _expert_envelope(x, go, p, g, u, Wg, Wu, Wd):
+    """Envelopes (bf16 mode) of one expert's results for rows x[n,H] with probs p[n]:
+    returns env_y [n,H], env_dx [n,H], env_dWg [I,H], env_dWu [I,H], env_dWd [H,I]
+    and the a-envelope alt_a [n,I]."""
+    H = x.shape[1]
+    I = g.shape[1]
+    dg_band = fp32_dot_band((x * x) @ (Wg * Wg).T, H)          # |g_fp32 - g|
+    du_band = fp32_dot_band((x * x) @ (Wu * Wu).T, H)
+    s1 = silu_grad(g)
+    a_val = silu(g) * u
+    band_a = np.abs(s1 * u) * dg_band + np.abs(silu(g)) * du_band + ELEMENTWISE_BAND * np.abs(a_val)
+    alt_a = bf16_alternative(a_val, band_a)
+    env_y = alt_a @ np.abs(Wd).T
+    a_b = bf16_round(a_val)
+
+    da_u = go @ Wd
+    da = p[:, None] * da_u
+    dda = np.abs(p)[:, None] * fp32_dot_band((go * go) @ (Wd * Wd), H)
+    dg_val = da * u * s1
+    du_val = da * silu(g)
+    band_dg = (np.abs(u * s1) * dda + np.abs(da * s1) * du_band +
+               np.abs(da * u) * silu_grad2_bound() * dg_band + ELEMENTWISE_BAND * np.abs(dg_val))
+    band_du = np.abs(silu(g)) * dda + np.abs(da * s1) * dg_band + ELEMENTWISE_BAND * np.abs(du_val)
+    alt_dg = bf16_alternative(dg_val, band_dg)
+    alt_du = bf16_alternative(du_val, band_du)
+    env_dx = alt_dg @ np.abs(Wg) + alt_du @ np.abs(Wu)
+    env_dWg = alt_dg.T @ np.abs(x)
+    env_dWu = alt_du.T @ np.abs(x)
+
+    pa_val = p[:, None] * a_b
+    alt_pa = bf16_alternative(pa_val, 2 * U32 * np.abs(pa_val))
+    alt_pa = alt_pa + np.where(alt_a > 0, np.abs(p)[:, None] * alt_a + np.ldexp(1.0, np.frexp(pa_val)[1] - 8), 0.0)
+    env_dWd = np.abs(go).T @ alt_pa
+    return env_y, env_dx, env_dWg, env_dWu, env_dWd, alt_a
+
+
+def envelope(grad_out, cache, W):
+    """Per-element envelopes of out, dhidden, dprobs and the six weight
+    gradients for a bf16-mode forward/backward (see the module notes)."""
+    go = np.asarray(grad_out, np.float64)
+    x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
+    offsets, perm_src, perm_slot = cache["offsets"], cache["perm_src"], cache["perm_slot"]
+    T, H = x.shape
+    E = W.num_experts
+    gs, us, _ = cache["shared"]
+    ey_s, edx_s, eg_s, eu_s, ed_s, _ = _expert_envelope(x, go, np.ones(T), gs, us, *W.shared())
+    R = perm_src.size
+    ey = np.zeros((R, H))
+    edx = np.zeros((R, H))
+    pp_perm = pp[perm_src, perm_slot] if R else np.zeros(0)
+    routed = {}
+    for e, (g, u, _) in cache["routed"].items():
+        lo, hi = offsets[e], offsets[e + 1]
+        ey[lo:hi], edx[lo:hi], eg, eu, ed, _ = _expert_envelope(x[perm_src[lo:hi]], go[perm_src[lo:hi]],
+                                                              pp_perm[lo:hi], g, u, *W.routed(e))
+        routed[e] = (eg, eu, ed)
+    env_out = ey_s.copy()
+    env_dh = edx_s.copy()
+    env_dp = np.zeros((T, E))
+    for s in range(cache["k"]):
+        v = ids[:, s] >= 0
+        r = row_of[v, s]
+        env_out[v] += np.abs(pp[v, s, None]) * ey[r]
+        env_dh[v] += edx[r]
+        env_dp[np.flatnonzero(v), ids[v, s]] = np.sum(np.abs(go[v]) * ey[r], axis=1)
+    return dict(out=env_out, dhidden=env_dh, dprobs=env_dp, shared_gate=eg_s, shared_up=eu_s,
+                shared_down=ed_s, routed=routed)

@@ -111,15 +111,19 @@ def f64(t):
 
 
 def oracle_full(inp: Inputs, precision="bf16"):
-    """Oracle forward + backward over all tokens."""
+    """Oracle forward + backward over all tokens (bf16 mode: with its rounding envelope)."""
     W = TorchWeights(inp.weights)
     out, cache = O.forward(f64(inp.hidden), inp.probs_np, inp.map_np, W, inp.case.k, precision=precision)
-    dx, dprobs, grads = O.backward(f64(inp.grad_out), cache, W)
+    go = f64(inp.grad_out)
+    dx, dprobs, grads = O.backward(go, cache, W)
+    cache["envelope"] = O.envelope(go, cache, W) if precision == "bf16" else None
     return out, dx, dprobs, grads, cache
 
 
-def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3):
-    """Per element |gpu - ref| <= rtol*|ref| + atol_frac*max|ref| (the BF16 tolerance)."""
+def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3, env=None):
+    """Per element |gpu - ref| <= rtol*|ref| + atol_frac*max|ref| (the BF16 tolerance),
+    plus the oracle's rounding envelope ``env`` where given (the other valid bf16
+    roundings of operands that sit at a rounding midpoint within fp32 precision)."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     assert gpu.shape == ref.shape, (name, gpu.shape, ref.shape)
@@ -127,6 +131,8 @@ def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3):
     scale = float(np.max(np.abs(ref))) if ref.size else 0.0
     err = np.abs(gpu - ref)
     bound = rtol * np.abs(ref) + atol_frac * scale
+    if env is not None:
+        bound = bound + np.asarray(env, np.float64)
     bad = err > bound
     if bad.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)

@@ -3,7 +3,9 @@
 Routing ids, probs, counts, offsets and permutation are compared bit-exactly.
 Floating-point results are compared, per element, with the oracle at the
 expert GEMMs' operand precision (bf16 operands, exact accumulation) within
-|gpu - ref| <= 2e-2 |ref| + 1e-3 max|ref|, and normwise with the exact oracle
+|gpu - ref| <= 2e-2 |ref| + 1e-3 max|ref| + env, env being the oracle's
+envelope of the other valid roundings of operands that sit at a bf16 rounding
+midpoint within fp32 evaluation precision, and normwise with the exact oracle
 (no rounding anywhere) within max|gpu - ref| / max|ref| <= 1e-2. Main-grad
 updates are compared as (main_grad_after - main_grad_before) against dW.
 """
@@ -76,7 +78,8 @@ def test_routing_bit_exact_full_size(cfg, variant):
 
 
 def _compare_full(inp, res, exact=True):
-    out, dx, dprobs, grads, _ = oracle_full(inp, "bf16")
+    out, dx, dprobs, grads, cache = oracle_full(inp, "bf16")
+    env = cache["envelope"]
     c = inp.case
     I = c.I
     mg0 = {n: f64(t) for n, t in inp.main_grads.items()}
@@ -85,18 +88,22 @@ def _compare_full(inp, res, exact=True):
     got = {"out": f64(res.out), "dhidden": f64(res.dhidden), "dprobs": f64(res.dprobs),
            "dW shared gate": d["shared_fc1"][:I], "dW shared up": d["shared_fc1"][I:],
            "dW shared down": d["shared_fc2"]}
+    env_of = {"out": env["out"], "dhidden": env["dhidden"], "dprobs": env["dprobs"],
+              "dW shared gate": env["shared_gate"], "dW shared up": env["shared_up"],
+              "dW shared down": env["shared_down"]}
 
     def refs(out, dx, dprobs, grads):
         return {"out": out, "dhidden": dx, "dprobs": dprobs, "dW shared gate": grads["shared_gate"],
                 "dW shared up": grads["shared_up"], "dW shared down": grads["shared_down"]}
 
-    errs = {n: assert_close(got[n], r, n) for n, r in refs(out, dx, dprobs, grads).items()}
+    errs = {n: assert_close(got[n], r, n, env=env_of[n]) for n, r in refs(out, dx, dprobs, grads).items()}
     for e in range(c.E):
         if e in grads["routed"]:
             dWg, dWu, dWd = grads["routed"][e]
-            assert_close(d["routed_fc1"][e, :I], dWg, f"dW routed gate[{e}]")
-            assert_close(d["routed_fc1"][e, I:], dWu, f"dW routed up[{e}]")
-            assert_close(d["routed_fc2"][e], dWd, f"dW routed down[{e}]")
+            eg, eu, ed = env["routed"][e]
+            assert_close(d["routed_fc1"][e, :I], dWg, f"dW routed gate[{e}]", env=eg)
+            assert_close(d["routed_fc1"][e, I:], dWu, f"dW routed up[{e}]", env=eu)
+            assert_close(d["routed_fc2"][e], dWd, f"dW routed down[{e}]", env=ed)
         else:   # an expert with no tokens keeps its main_grad bitwise
             assert np.array_equal(mg1["routed_fc1"][e], mg0["routed_fc1"][e])
             assert np.array_equal(mg1["routed_fc2"][e], mg0["routed_fc2"][e])
@@ -226,14 +233,16 @@ def test_row_with_too_many_routes_is_reported():
 
 
 def _routed_expert_grads(inp, W, e):
-    """Oracle dW of expert e from the tokens routed to it (dW_e depends on nothing else)."""
+    """Oracle dW of expert e from the tokens routed to it (dW_e depends on nothing
+    else), with its rounding envelope."""
     toks = np.flatnonzero(inp.map_np[:, e])
     m = np.zeros((toks.size, inp.case.E), bool)
     m[:, e] = True
-    _, cache = O.forward(f64(inp.hidden[torch.from_numpy(toks).to(inp.hidden.device)]), inp.probs_np[toks], m, W,
-                         inp.case.k, precision="bf16")
-    _, _, g = O.backward(f64(inp.grad_out[torch.from_numpy(toks).to(inp.hidden.device)]), cache, W)
-    return g["routed"][e]
+    tt = torch.from_numpy(toks).to(inp.hidden.device)
+    _, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], m, W, inp.case.k, precision="bf16")
+    go = f64(inp.grad_out[tt])
+    _, _, g = O.backward(go, cache, W)
+    return g["routed"][e], O.envelope(go, cache, W)["routed"][e]
 
 
 @pytest.mark.slow
@@ -250,9 +259,10 @@ def test_layer_parity_config5_sampled():
     tt = torch.from_numpy(toks).to(inp.hidden.device)
     out, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], inp.map_np[toks], W, c.k, precision="bf16")
     dx, dprobs, _ = O.backward(f64(inp.grad_out[tt]), cache, W)
-    assert_close(f64(res.out[tt]), out, "out (sampled)")
-    assert_close(f64(res.dhidden[tt]), dx, "dhidden (sampled)")
-    assert_close(f64(res.dprobs[tt]), dprobs, "dprobs (sampled)")
+    env = O.envelope(f64(inp.grad_out[tt]), cache, W)
+    assert_close(f64(res.out[tt]), out, "out (sampled)", env=env["out"])
+    assert_close(f64(res.dhidden[tt]), dx, "dhidden (sampled)", env=env["dhidden"])
+    assert_close(f64(res.dprobs[tt]), dprobs, "dprobs (sampled)", env=env["dprobs"])
     assert torch.isfinite(res.out).all() and torch.isfinite(res.dhidden).all() and torch.isfinite(res.dprobs).all()
 
     counts = inp.map_np.sum(0)
@@ -260,21 +270,23 @@ def test_layer_parity_config5_sampled():
     med = int(np.argsort(counts)[c.E // 2])
     I = c.I
     for e in (hot, med):
-        dWg, dWu, dWd = _routed_expert_grads(inp, W, e)
+        (dWg, dWu, dWd), (eg, eu, ed) = _routed_expert_grads(inp, W, e)
         d1 = f64(res.main_grads["routed_fc1"][e]) - f64(inp.main_grads["routed_fc1"][e])
         d2 = f64(res.main_grads["routed_fc2"][e]) - f64(inp.main_grads["routed_fc2"][e])
-        assert_close(d1[:I], dWg, f"dW routed gate[{e}]")
-        assert_close(d1[I:], dWu, f"dW routed up[{e}]")
-        assert_close(d2, dWd, f"dW routed down[{e}]")
+        assert_close(d1[:I], dWg, f"dW routed gate[{e}]", env=eg)
+        assert_close(d1[I:], dWu, f"dW routed up[{e}]", env=eu)
+        assert_close(d2, dWd, f"dW routed down[{e}]", env=ed)
     for e in np.flatnonzero(counts == 0):
         assert torch.equal(res.main_grads["routed_fc1"][e], inp.main_grads["routed_fc1"][e])
 
     # shared expert over all tokens: a map with no routes leaves only the shared path
     m0 = np.zeros_like(inp.map_np)
     _, cache = O.forward(f64(inp.hidden), inp.probs_np, m0, W, c.k, precision="bf16")
-    _, _, g = O.backward(f64(inp.grad_out), cache, W)
+    go = f64(inp.grad_out)
+    _, _, g = O.backward(go, cache, W)
+    env = O.envelope(go, cache, W)
     d1 = f64(res.main_grads["shared_fc1"]) - f64(inp.main_grads["shared_fc1"])
     d2 = f64(res.main_grads["shared_fc2"]) - f64(inp.main_grads["shared_fc2"])
-    assert_close(d1[:I], g["shared_gate"], "dW shared gate")
-    assert_close(d1[I:], g["shared_up"], "dW shared up")
-    assert_close(d2, g["shared_down"], "dW shared down")
+    assert_close(d1[:I], g["shared_gate"], "dW shared gate", env=env["shared_gate"])
+    assert_close(d1[I:], g["shared_up"], "dW shared up", env=env["shared_up"])
+    assert_close(d2, g["shared_down"], "dW shared down", env=env["shared_down"])

@@ -123,3 +123,80 @@ def test_bf16_mode_within_rounding_bounds(seed):
         a_b = cb["routed"][e][2]
         bd = np.abs(go[src]).T @ (U * (np.abs(p[:, None] * a_b) + np.abs(p[:, None] * a_e)))
         assert np.all(np.abs(g_b["routed"][e][2] - dWd) <= bd * (1 + 1e-9) + 1e-15)
+
+
+def _fp32_layer(x, go, m, probs, W, k):
+    """An independent fp32 evaluation of the layer (numpy float32 matmuls and
+    elementwise math, bf16 rounding of the GEMM operands, fp64 afterwards):
+    stands in for any kernel that evaluates the operands in fp32."""
+    f32 = np.float32
+    rnd = O.bf16_round
+
+    def sig(z):
+        return f32(1) / (f32(1) + np.exp(-z))
+
+    def expert(xr, gor, p, Wg, Wu, Wd):
+        xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xr, Wg, Wu, Wd, gor))
+        g = xr32 @ Wg32.T
+        u = xr32 @ Wu32.T
+        s = sig(g)
+        a = rnd((g * s * u).astype(np.float64))
+        y = a @ Wd.T
+        da = p.astype(f32)[:, None] * (go32 @ Wd32)
+        dg = rnd((da * u * (s * (f32(1) + g * (f32(1) - s)))).astype(np.float64))
+        du = rnd((da * (g * s)).astype(np.float64))
+        pa = rnd((p.astype(f32)[:, None] * a.astype(f32)).astype(np.float64))
+        return y, dg @ Wg + du @ Wu, dg.T @ xr, du.T @ xr, gor.T @ pa
+
+    T = x.shape[0]
+    ys, dxs, gsg, gsu, gsd = expert(x, go, np.ones(T), *W.shared())
+    out, dh = ys.copy(), dxs.copy()
+    ids, pp, _ = O.route_pack(m, probs, k)
+    routed = {}
+    for e in range(W.num_experts):
+        rows, slots = np.nonzero(ids == e)
+        if rows.size == 0:
+            continue
+        y, dx, g1, g2, g3 = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e))
+        out[rows] += pp[rows, slots, None] * y
+        dh[rows] += dx
+        routed[e] = (g1, g2, g3)
+    return out, dh, dict(shared_gate=gsg, shared_up=gsu, shared_down=gsd, routed=routed)
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_envelope_covers_fp32_evaluation(seed):
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k = 192, 256, 256, 3, 2
+    W = O.DenseWeights(*(rng.standard_normal(s) * 0.06 for s in
+                         ((I, H), (I, H), (H, I), (E, I, H), (E, I, H), (E, H, I))))
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    go = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    m = np.zeros((T, E), bool)
+    for t in range(T):
+        m[t, rng.choice(E, 2, replace=False)] = True
+    probs = rng.random((T, E)).astype(np.float32).astype(np.float64)
+    out_b, cache = O.forward(x, probs, m, W, k, precision="bf16")
+    dh_b, _, g_b = O.backward(go, cache, W)
+    env = O.envelope(go, cache, W)
+    out_f, dh_f, g_f = _fp32_layer(x, go, m, probs, W, k)
+
+    def check(a, b, ev, name):
+        slack = 1e-5 * np.abs(b).max()          # fp32 differences that flip nothing
+        d = np.abs(a - b)
+        assert np.all(d <= ev + slack), f"{name}: {np.sum(d > ev + slack)} outside the envelope"
+        return np.sum(d > slack)
+
+    flipped = check(out_f, out_b, env["out"], "out")
+    flipped += check(dh_f, dh_b, env["dhidden"], "dhidden")
+    for n in ("shared_gate", "shared_up", "shared_down"):
+        flipped += check(g_f[n], g_b[n], env[n], n)
+    for e, gs in g_f["routed"].items():
+        for j, n in enumerate(("gate", "up", "down")):
+            flipped += check(gs[j], g_b["routed"][e][j], env["routed"][e][j], f"routed {n}[{e}]")
+    assert flipped > 0, "the fp32 evaluation flipped no rounding: the test would prove nothing"
+    # the envelope mostly stays far below the tolerance floor (1e-3 max|ref|) it is added to
+    for n, ref in (("out", out_b), ("dhidden", dh_b), ("shared_gate", g_b["shared_gate"])):
+        sc = np.abs(ref).max()
+        assert np.median(env[n]) < 1e-4 * sc and np.percentile(env[n], 99) < 1e-3 * sc, n
+        assert env[n].max() < 5e-3 * sc, n
