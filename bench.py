@@ -157,8 +157,8 @@ def kernel_work(name, T, H, E, k, I, R, E_act):
     W_fc1, W_down = E_act * 2 * I * H * b2, E_act * H * I * b2
     table = {
         "route_pack": (0, T * E + T * k * (b4 * 3 + b4)),
-        "route_scan": (0, 0),
-        "route_place": (0, T * k * 8 + R * 12),
+        "route_scan": (0, T * E + T * k * b4 + E * b4),
+        "route_place": (0, T * k * 12 + R * 12 + 2 * R * H * b2),
         "gather_rows": (0, 2 * R * H * b2),
         "gemm_fwd_gu_routed": (4 * R * H * I, R * H * b2 + W_fc1 + R * I * b2 + R * 2 * I * b4),
         "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * b2 + T * 2 * I * b4),

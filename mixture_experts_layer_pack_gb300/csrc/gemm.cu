@@ -16,12 +16,14 @@
 // never straddles two experts; the expert of each tile comes from a device
 // table, so nothing is read back to the host.
 //
-// Block = 6 warps: warp 0 issues TMA loads into a STAGES-deep shared-memory
+// Block = 10 warps: warp 0 issues TMA loads into a STAGES-deep shared-memory
 // ring, warp 1 owns TMEM and issues tcgen05.mma (M=128, N=BN, K=16 steps),
-// warps 2..5 drain the double-buffered TMEM accumulator through tcgen05.ld
-// and run the fused epilogue while the next tile accumulates. Operands use the
-// 128-byte swizzle: K-major tiles are 128 rows x 128 bytes; M/N-major tiles are
-// 64-element (128-byte) columns x 64 K-rows, 8 KB apart.
+// warps 2..9 drain the double-buffered TMEM accumulator through tcgen05.ld
+// (two warps per 32-lane quarter, alternating 32-column chunks) and run the
+// fused epilogue while the next tile accumulates. Operands use the 128-byte
+// swizzle: K-major tiles are 128 rows x 128 bytes; M/N-major tiles are
+// 64-element (128-byte) columns x 64 K-rows, 8 KB apart. The weight-gradient
+// epilogue adds into main_grad with TMA reduce-add boxes of 32 x 32 fp32.
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -34,6 +36,8 @@ namespace {
 constexpr uint32_t kSwizzleAtom = 1024;   // 8 rows x 128 bytes
 constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
 
+constexpr uint32_t kStageTileBytes = 32 * 32 * 4;  // fp32 staging box of one epilogue warp (32 rows x 32 cols)
+
 template <int BN>
 struct Cfg {
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
@@ -41,7 +45,8 @@ struct Cfg {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
-    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + 1024 + 256;
+    static constexpr uint32_t STAGING = kEpiWarps * kStageTileBytes;
+    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING + 1024 + 256;
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle
@@ -134,28 +139,33 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, 
 }
 
 template <int OP, int BN>
-__device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int r_local, const GemmArgs& a) {
+__device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int q, int half, const GemmArgs& a,
+                                              float* staging, const CUtensorMap* mC0, const CUtensorMap* mC1) {
+    const int lane = threadIdx.x & 31;
+    const int r_local = q * 32 + lane;
     if (OP == OP_WGRAD) {
-        const int m = t.mt * kBM + r_local;
-        float* dst;
-        if (m < a.m_split)
-            dst = a.mg0 + int64_t(t.e) * a.mg0_es + int64_t(m) * a.mg0_rs;
-        else
-            dst = a.mg1 + int64_t(t.e) * a.mg1_es + int64_t(m - a.m_split) * a.mg1_rs;
-        dst += t.nt * BN;
+        // main_grad[e][m][n] += acc through TMA reduce-add: the warp stages its 32
+        // rows x 32 columns in shared memory (128-byte swizzle) and one lane
+        // issues the reduction; the L2 performs one fp32 add per element
+        const int m0 = t.mt * kBM + q * 32;
+        const bool hi = m0 >= a.m_split;
+        const CUtensorMap* mc = hi ? mC1 : mC0;
+        const int row0 = hi ? m0 - a.m_split : m0;
+        float4* srow = reinterpret_cast<float4*>(staging + lane * 32);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half; c < BN / 32; c += kEpiHalves) {
             float v[32];
             tmem_ld32(t_row + c * 32, v);
-            float4* p = reinterpret_cast<float4*>(dst + c * 32);
+            if (lane == 0) bulk_wait_read<0>();      // the previous box has left the staging buffer
+            __syncwarp();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float4 o = p[q];
-                o.x += v[4 * q + 0];
-                o.y += v[4 * q + 1];
-                o.z += v[4 * q + 2];
-                o.w += v[4 * q + 3];
-                p[q] = o;
+            for (int j = 0; j < 8; ++j)
+                srow[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_reduce_add_3d(mc, staging, t.nt * BN + c * 32, row0, t.e);
+                bulk_commit();
             }
         }
         return;
@@ -167,7 +177,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
     if (OP == OP_FWD_GU) {
         const int j0 = t.nt * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = half; c < BN / 64; c += kEpiHalves) {
             float g[32], u[32];
             tmem_ld32(t_row + c * 32, g);
             tmem_ld32(t_row + BN / 2 + c * 32, u);
@@ -184,7 +194,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
     } else if (OP == OP_FWD_DOWN || OP == OP_BWD_GU) {
         const float scale = (store && a.row_scale) ? a.row_scale[row] : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half; c < BN / 32; c += kEpiHalves) {
             float v[32];
             tmem_ld32(t_row + c * 32, v);
             if (store) {
@@ -199,7 +209,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
         const float p = (store && a.row_scale) ? a.row_scale[row] : 1.0f;
         float part = 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half; c < BN / 32; c += kEpiHalves) {
             float d[32];
             tmem_ld32(t_row + c * 32, d);
             if (!store) continue;
@@ -243,14 +253,15 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                 if (pap) pap[q] = make_uint4(apw[0], apw[1], apw[2], apw[3]);
             }
         }
-        if (store && a.partial) a.partial[int64_t(row) * a.n_tiles + t.nt] = part;
+        if (store && a.partial) a.partial[(int64_t(row) * a.n_tiles + t.nt) * kEpiHalves + half] = part;
     }
 }
 
 template <int OP, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
+                    const __grid_constant__ CUtensorMap tmC1, const GemmArgs args) {
     using C = Cfg<BN>;
     constexpr bool A_MN = (OP == OP_WGRAD);
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD);
@@ -259,7 +270,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    float* staging = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);  // 1024-byte aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -285,6 +297,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB0);
         if (OP == OP_FWD_GU || OP == OP_BWD_GU) tma_prefetch_map(&tmB1);
+        if (OP == OP_WGRAD) {
+            tma_prefetch_map(&tmC0);
+            tma_prefetch_map(&tmC1);
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
@@ -376,9 +392,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+        // ---------------- epilogue warps 2..: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4
         const int q = warp & 3;
-        const int r_local = q * 32 + lane;
+        const int half = (warp - 2) >> 2;
+        float* my_staging = staging + (warp - 2) * (kStageTileBytes / 4);
         int it = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Tile t = decode_tile<OP>(tile, args);
@@ -393,11 +410,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            epilogue_tile<OP, BN>(t, t_row, r_local, args);
+            epilogue_tile<OP, BN>(t, t_row, q, half, args, my_staging, &tmC0, &tmC1);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
         }
+        if (OP == OP_WGRAD && lane == 0) bulk_wait<0>();   // every reduction has landed
+        __syncwarp();
     }
 
     __syncthreads();
@@ -416,7 +435,7 @@ cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStrea
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<grid, kGemmThreads, Cfg<BN>::SMEM, st>>>(m.a, m.b0, m.b1, a);
+    kern<<<grid, kGemmThreads, Cfg<BN>::SMEM, st>>>(m.a, m.b0, m.b1, m.c0, m.c1, a);
     count_launch();
     return cudaGetLastError();
 }
@@ -483,7 +502,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                const uint32_t* box) {
+                const uint32_t* box, bool fp32) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t d[3], s[2];
@@ -493,7 +512,7 @@ bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims
         b[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), d, s, b, es,
+    CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), d, s, b, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

@@ -10,8 +10,9 @@ namespace moe {
 
 constexpr int kBM = 128;        // GEMM tile rows (= TMEM lanes) and expert segment padding
 constexpr int kBK = 64;         // GEMM K block (64 bf16 = one 128-byte swizzle row)
-constexpr int kChunk = 128;     // tokens per routing chunk
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;    // epilogue warps: two per TMEM lane quarter, alternating 32-column chunks
+constexpr int kEpiHalves = kEpiWarps / 4;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
 // device status word bits (read back by moe_device_status)
 constexpr int kStatusRouting = 1;  // a routing_map row had more than k routes
@@ -52,23 +53,21 @@ struct GemmArgs {
     const float* inf;           // [g|u]
     int64_t ld_inf;
     const float* row_scale;     // per-row prob (null: 1)
-    float* partial;             // per-row, per-N-tile partial dot products (null: skip)
-    float* mg0;
-    int64_t mg0_es, mg0_rs;
-    float* mg1;
-    int64_t mg1_es, mg1_rs;
-    int m_split;                // WGRAD rows >= m_split go to mg1 at row - m_split
+    float* partial;             // per row: n_tiles * kEpiHalves partial dot products (null: skip)
+    int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
     int inter;
     int* status;
 };
 
 struct GemmMaps {
     CUtensorMap a, b0, b1;
+    CUtensorMap c0, c1;  // OP_WGRAD: fp32 main_grad destinations (rows < m_split, rows >= m_split)
 };
 
-// tensor-map construction (driver entry point resolved at first use)
+// tensor-map construction (driver entry point resolved at first use); bf16
+// elements unless fp32 is set, 128-byte swizzle
 bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                const uint32_t* box);
+                const uint32_t* box, bool fp32 = false);
 
 // picks the N tile (256, 128 or 64) for an output width
 int pick_bn(int64_t n, bool split_gate_up);
@@ -77,12 +76,16 @@ cudaError_t launch_gemm(int op, int bn, const GemmMaps& maps, const GemmArgs& ar
 size_t gemm_smem_bytes(int bn);
 
 // routing
+int route_rank_max_tokens();
 cudaError_t launch_route_pack(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
-                              int* row_of, int* hist, int* status, cudaStream_t st);
-cudaError_t launch_route_scan(int* hist, int nchunks, int E, int* counts, int* offsets, int* offs_pad,
-                              int* mtile_expert, int* meta, int* perm_src, float* pp_perm, cudaStream_t st);
-cudaError_t launch_route_place(const int* ids, const float* pp, int T, int E, int k, const int* hist,
-                               const int* offs_pad, int* perm_src, float* pp_perm, int* row_of, cudaStream_t st);
+                              int* row_of, int* status, cudaStream_t st);
+cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, int k, int* rank, int* counts,
+                              cudaStream_t st);
+cudaError_t launch_route_scan(const int* counts, int E, int* offsets, int* offs_pad, int* mtile_expert, int* meta,
+                              cudaStream_t st);
+cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* counts,
+                               const int* offs_pad, int T, int E, int k, const __nv_bfloat16* hidden, int H,
+                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, cudaStream_t st);
 cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* perm_src_pad, const int* counts,
                                   const int* offsets, const int* offs_pad, const int* mtile_expert, const int* meta,
                                   int T, int k, int max_rows, int32_t* perm_src_out, int32_t* row_of_out,

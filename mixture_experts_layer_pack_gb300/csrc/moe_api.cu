@@ -27,7 +27,6 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Shape {
     int64_t Tmax, H, E, k, I;
     int64_t rows;     // permuted rows incl. padding, worst case
-    int64_t nchunks;  // routing chunks, worst case
     int bn_gu, bn_down, bn_bd, bn_bgu, bn_wfc1, bn_wd;
     int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM)
 };
@@ -59,8 +58,8 @@ moe_status check_config(const moe_config* c, Shape* s) {
     s->k = c->topk;
     s->I = c->inter;
     s->rows = align_up(size_t(s->Tmax * s->k + s->E * (kBM - 1)), kBM);
-    s->nchunks = (s->Tmax + kChunk - 1) / kChunk;
     if (s->rows >= INT_MAX / 2 || s->Tmax * s->k >= INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (s->Tmax > route_rank_max_tokens()) return MOE_ERR_UNSUPPORTED;
     s->bn_gu = pick_bn(2 * s->I, true);
     s->bn_down = pick_bn(s->H, false);
     s->bn_bd = pick_bn(s->I, false);
@@ -68,13 +67,13 @@ moe_status check_config(const moe_config* c, Shape* s) {
     s->bn_wfc1 = pick_bn(s->H, false);
     s->bn_wd = pick_bn(s->I, false);
     if (!s->bn_gu || !s->bn_down || !s->bn_bd || !s->bn_bgu || !s->bn_wfc1 || !s->bn_wd) return MOE_ERR_UNSUPPORTED;
-    s->n_part = int(s->I / s->bn_bd);
+    s->n_part = int(s->I / s->bn_bd) * kEpiHalves;
     return MOE_OK;
 }
 
 struct Workspace {
     int* status;
-    int* hist;
+    int* rank;  // rank of each route inside its expert
     __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
     float *yx, *ys_dxs;  // forward: p*y (routed rows), y_shared; backward: dx (routed rows), dx_shared
     float* partial;
@@ -90,7 +89,7 @@ struct SavedBufs {
 size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     Carver c{base};
     w->status = c.take<int>(64);
-    w->hist = c.take<int>(size_t(s.nchunks) * s.E);
+    w->rank = c.take<int>(size_t(s.Tmax) * s.k);
     w->go_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     w->dgdu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
     w->ap = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
@@ -164,6 +163,16 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int64_t rows, int64_t mn, int
     const uint64_t strides[1] = {uint64_t(ld) * 2};
     const uint32_t box[2] = {64, 64};
     return encode_map(m, base, 2, dims, strides, box);
+}
+
+// 3D fp32 main_grad view [E][rows][cols] (expert stride es, row stride rs) as a
+// TMA reduce destination, box 32 cols x 32 rows
+bool map_main_grad(CUtensorMap* m, float* base, int64_t E, int64_t rows, int64_t cols, int64_t es, int64_t rs) {
+    if (E <= 1) es = rows * rs;
+    const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(E)};
+    const uint64_t strides[2] = {uint64_t(rs) * 4, uint64_t(es) * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    return encode_map(m, base, 3, dims, strides, box, true);
 }
 
 // 3D weight view [E][rows][cols] with a box of (64 cols, box_rows rows, 1 expert)
@@ -370,20 +379,18 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     if (T == 0) return MOE_OK;
 
     const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
-    const int nchunks = (Ti + kChunk - 1) / kChunk;
     const int rows = int(s.rows);
 
-    // dispatch: route-pack, segment scan, stable placement, row gather
+    // dispatch: route-pack, per-expert ranks, segment scan, placement + row gather
     { Timed tm_(h, MOE_K_ROUTE_PACK, st);
-    MOE_CU(launch_route_pack(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.hist, ws.status, st)); }
+    MOE_CU(launch_route_pack(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.status, st)); }
     { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
-    MOE_CU(launch_route_scan(ws.hist, nchunks, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta, b.perm_src,
-                             b.pp_perm, st)); }
+    MOE_CU(launch_route_rank(routing_map, b.ids, Ti, E, k, ws.rank, b.counts, st));
+    MOE_CU(launch_route_scan(b.counts, E, b.offsets, b.offs_pad, b.mtile_expert, b.meta, st)); }
     { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
-    MOE_CU(launch_route_place(b.ids, b.pp, Ti, E, k, ws.hist, b.offs_pad, b.perm_src, b.pp_perm, b.row_of, st)); }
-    { Timed tm_(h, MOE_K_GATHER, st);
-    MOE_CU(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), b.perm_src, b.meta, rows, H, b.x_perm,
-                              h->sms, st)); }
+    MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, b.counts, b.offs_pad, Ti, E, k,
+                              static_cast<const __nv_bfloat16*>(hidden), H, b.perm_src, b.pp_perm, b.row_of, b.x_perm,
+                              st)); }
 
     GemmMaps m;
     // routed gate/up + SwiGLU
@@ -577,12 +584,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = E;
         a.m_tiles = 2 * I / kBM;
         a.n_tiles = H / bn;
-        a.mg0 = mg->routed_gate;
-        a.mg0_es = mg->strides[3][0];
-        a.mg0_rs = mg->strides[3][1];
-        a.mg1 = mg->routed_up;
-        a.mg1_es = mg->strides[4][0];
-        a.mg1_rs = mg->strides[4][1];
+        if (!map_main_grad(&m.c0, mg->routed_gate, E, I, H, mg->strides[3][0], mg->strides[3][1]) ||
+            !map_main_grad(&m.c1, mg->routed_up, E, I, H, mg->strides[4][0], mg->strides[4][1]))
+            return MOE_ERR_INVALID_ARG;
         a.m_split = I;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
@@ -598,9 +602,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = E;
         a.m_tiles = H / kBM;
         a.n_tiles = I / bn;
-        a.mg0 = mg->routed_down;
-        a.mg0_es = mg->strides[5][0];
-        a.mg0_rs = mg->strides[5][1];
+        if (!map_main_grad(&m.c0, mg->routed_down, E, H, I, mg->strides[5][0], mg->strides[5][1]))
+            return MOE_ERR_INVALID_ARG;
+        m.c1 = m.c0;
         Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
@@ -615,10 +619,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = 1;
         a.m_tiles = 2 * I / kBM;
         a.n_tiles = H / bn;
-        a.mg0 = mg->shared_gate;
-        a.mg0_rs = mg->strides[0][1];
-        a.mg1 = mg->shared_up;
-        a.mg1_rs = mg->strides[1][1];
+        if (!map_main_grad(&m.c0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1]) ||
+            !map_main_grad(&m.c1, mg->shared_up, 1, I, H, 0, mg->strides[1][1]))
+            return MOE_ERR_INVALID_ARG;
         a.m_split = I;
         Timed tm_(h, MOE_K_WGRAD_FC1_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
@@ -633,8 +636,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = 1;
         a.m_tiles = H / kBM;
         a.n_tiles = I / bn;
-        a.mg0 = mg->shared_down;
-        a.mg0_rs = mg->strides[2][1];
+        if (!map_main_grad(&m.c0, mg->shared_down, 1, H, I, 0, mg->strides[2][1])) return MOE_ERR_INVALID_ARG;
+        m.c1 = m.c0;
         Timed tm_(h, MOE_K_WGRAD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }

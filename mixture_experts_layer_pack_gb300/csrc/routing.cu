@@ -1,5 +1,6 @@
 // Routing kernels: dense routing map -> fixed-width expert ids, then the
-// dispatch permutation (per-expert token segments), all on the device.
+// dispatch permutation (per-expert token segments) and the dispatch gather,
+// all on the device.
 //
 // "feat(moe): add a megakernel backend with MOK integration", Design >
 // Authoritative routing maps: the router's dense map is converted into a
@@ -10,12 +11,16 @@
 // Order is deterministic: slots list a token's experts in ascending id order;
 // within an expert, routes are ordered by token index. Each expert segment is
 // padded to a multiple of 128 rows so that a GEMM row tile never spans two
-// experts; padding rows have source token -1 and prob 0.
+// experts; padding rows have source token -1, prob 0 and zero activations.
 //
-// Three launches: (1) pack + per-chunk expert histogram (smem atomics),
-// (2) one block scans the histogram over chunks and experts, writes the
-// segment offsets and the expert of every 128-row tile, (3) each chunk places
-// its routes at their stable positions.
+// Four launches, each parallel over its whole index space:
+//   pack   one warp per token: ids[t,:], pp[t,:], -1 slots; flags rows with > k routes
+//   rank   one block per expert: a stable scan of the expert's map column gives
+//          every routed token its rank inside the expert, and the expert's count
+//   scan   one block: exclusive scans of counts (compact and 128-padded), the
+//          expert of every 128-row tile, the tile count
+//   place  one warp per route (and per padding row): writes the permutation
+//          entries and copies the token's hidden row into its permuted row
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -23,67 +28,53 @@ namespace moe {
 
 namespace {
 
-constexpr int kPackThreads = 256;
+constexpr int kWarpsPerBlock = 8;
+constexpr int kRankThreads = 1024;
 
-__global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const uint8_t* __restrict__ map,
-                                                                  const float* __restrict__ probs, int T, int E,
-                                                                  int k, int* __restrict__ ids, float* __restrict__ pp,
-                                                                  int* __restrict__ row_of, int* __restrict__ hist,
-                                                                  int* status) {
-    extern __shared__ int s_hist[];  // [E]
-    const int chunk = blockIdx.x;
-    const int t0 = chunk * kChunk;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
+__global__ void __launch_bounds__(32 * kWarpsPerBlock) route_pack_kernel(const uint8_t* __restrict__ map,
+                                                                       const float* __restrict__ probs, int T, int E,
+                                                                       int k, int* __restrict__ ids,
+                                                                       float* __restrict__ pp,
+                                                                       int* __restrict__ row_of, int* status) {
+    const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int t_end = min(t0 + kChunk, T);
-    for (int t = t0 + warp; t < t_end; t += nwarps) {
-        const uint8_t* row = map + int64_t(t) * E;
-        // pass 1: count the row's routes
-        int cnt = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const bool on = e < E && row[e] != 0;
-            cnt += __popc(__ballot_sync(0xffffffffu, on));
-        }
-        int* ids_t = ids + int64_t(t) * k;
-        float* pp_t = pp + int64_t(t) * k;
-        int* ro_t = row_of + int64_t(t) * k;
-        if (cnt > k) {
-            // more routes than slots: flag it and drop the row's routes
-            if (lane == 0) atomicOr(status, kStatusRouting);
-            for (int s = lane; s < k; s += 32) {
-                ids_t[s] = -1;
-                pp_t[s] = 0.0f;
-                ro_t[s] = -1;
-            }
-            continue;
-        }
-        // pass 2: write slots in ascending expert order
-        int slot_base = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const bool on = e < E && row[e] != 0;
-            const unsigned m = __ballot_sync(0xffffffffu, on);
-            if (on) {
-                const int slot = slot_base + __popc(m & lt_mask);
-                ids_t[slot] = e;
-                pp_t[slot] = probs[int64_t(t) * E + e];
-                atomicAdd(&s_hist[e], 1);
-            }
-            slot_base += __popc(m);
-        }
-        for (int s = cnt + lane; s < k; s += 32) {
-            ids_t[s] = -1;
-            pp_t[s] = 0.0f;
-            ro_t[s] = -1;
-        }
+    const uint8_t* row = map + int64_t(t) * E;
+    // lane holds experts lane, lane+32, ...: bit j of `mine` = map[t, lane + 32 j]
+    uint32_t mine = 0;
+    const int rounds = (E + 31) >> 5;
+    for (int j = 0; j < rounds; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && __ldg(row + e) != 0) mine |= 1u << j;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[int64_t(chunk) * E + e] = s_hist[e];
+    int cnt = 0;
+    for (int j = 0; j < rounds; ++j) cnt += __popc(__ballot_sync(0xffffffffu, (mine >> j) & 1u));
+    int* ids_t = ids + int64_t(t) * k;
+    float* pp_t = pp + int64_t(t) * k;
+    int* ro_t = row_of + int64_t(t) * k;
+    if (cnt > k) {  // more routes than slots: flag it, drop the row's routes
+        if (lane == 0) atomicOr(status, kStatusRouting);
+        cnt = 0;
+        mine = 0;
+    }
+    int base = 0;
+    for (int j = 0; j < rounds; ++j) {
+        const bool on = (mine >> j) & 1u;
+        const unsigned m = __ballot_sync(0xffffffffu, on);
+        if (on) {
+            const int slot = base + __popc(m & lt_mask);
+            const int e = lane + 32 * j;
+            ids_t[slot] = e;
+            pp_t[slot] = __ldg(probs + int64_t(t) * E + e);
+        }
+        base += __popc(m);
+    }
+    for (int s = cnt + lane; s < k; s += 32) {
+        ids_t[s] = -1;
+        pp_t[s] = 0.0f;
+        ro_t[s] = -1;
+    }
 }
 
 // block-wide exclusive scan of one int per thread (blockDim.x <= 1024)
@@ -114,35 +105,58 @@ __device__ int block_excl_scan(int v, int* s_warp, int& total) {
     return warp_prefix + x - v;
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(int* __restrict__ hist, int nchunks, int E,
-                                                          int* __restrict__ counts, int* __restrict__ offsets,
-                                                          int* __restrict__ offs_pad, int* __restrict__ mtile_expert,
-                                                          int* __restrict__ meta, int* __restrict__ perm_src,
-                                                          float* __restrict__ pp_perm) {
+// block e: thread i owns tokens [i*C, (i+1)*C); a stable block scan of their
+// routes to expert e gives each one its rank; rank[t*k + s] for ids[t,s] == e
+__global__ void __launch_bounds__(kRankThreads) route_rank_kernel(const uint8_t* __restrict__ map,
+                                                                  const int* __restrict__ ids, int T, int E, int k,
+                                                                  int* __restrict__ rank, int* __restrict__ counts) {
     __shared__ int s_warp[32];
-    const int e = threadIdx.x;
-    int cnt = 0;
-    if (e < E) {
-        // exclusive scan over chunks, in place: hist[c][e] becomes the chunk's base
-        for (int c = 0; c < nchunks; ++c) {
-            const int v = hist[int64_t(c) * E + e];
-            hist[int64_t(c) * E + e] = cnt;
-            cnt += v;
+    const int e = blockIdx.x;
+    const int C = (T + blockDim.x - 1) / blockDim.x;
+    const int t0 = threadIdx.x * C;
+    const int t1 = min(t0 + C, T);
+    uint64_t bits = 0;  // C <= 64 is checked on the host
+    int n = 0;
+    for (int t = t0; t < t1; ++t) {
+        // a row with more than k routes was dropped by the pack kernel: ids decide
+        if (__ldg(map + int64_t(t) * E + e) != 0) bits |= 1ull << (t - t0);
+    }
+    for (int t = t0; t < t1; ++t) {
+        if ((bits >> (t - t0)) & 1ull) {
+            const int* ids_t = ids + int64_t(t) * k;
+            bool found = false;
+            for (int s = 0; s < k; ++s) found |= (ids_t[s] == e);
+            if (!found) bits &= ~(1ull << (t - t0));
         }
     }
+    n = __popcll(bits);
+    int total;
+    int r = block_excl_scan(n, s_warp, total);
+    for (int t = t0; t < t1; ++t) {
+        if ((bits >> (t - t0)) & 1ull) {
+            const int* ids_t = ids + int64_t(t) * k;
+            for (int s = 0; s < k; ++s)
+                if (ids_t[s] == e) rank[int64_t(t) * k + s] = r;
+            ++r;
+        }
+    }
+    if (threadIdx.x == 0) counts[e] = total;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict__ counts_in, int E,
+                                                          int* __restrict__ offsets, int* __restrict__ offs_pad,
+                                                          int* __restrict__ mtile_expert, int* __restrict__ meta) {
+    __shared__ int s_warp[32];
+    const int e = threadIdx.x;
+    const int cnt = e < E ? counts_in[e] : 0;
     const int padded = (cnt + kBM - 1) / kBM * kBM;
     int total_cnt, total_pad;
     const int off = block_excl_scan(cnt, s_warp, total_cnt);
     const int offp = block_excl_scan(padded, s_warp, total_pad);
     if (e < E) {
-        counts[e] = cnt;
         offsets[e] = off;
         offs_pad[e] = offp;
         for (int j = 0; j < padded / kBM; ++j) mtile_expert[offp / kBM + j] = e;
-        for (int j = cnt; j < padded; ++j) {
-            perm_src[offp + j] = -1;
-            pp_perm[offp + j] = 0.0f;
-        }
     }
     if (e == 0) {
         offsets[E] = total_cnt;
@@ -153,33 +167,44 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int* __restrict__ hist
     }
 }
 
-__global__ void __launch_bounds__(512) route_place_kernel(const int* __restrict__ ids, const float* __restrict__ pp,
-                                                          int T, int E, int k, const int* __restrict__ hist,
-                                                          const int* __restrict__ offs_pad,
-                                                          int* __restrict__ perm_src, float* __restrict__ pp_perm,
-                                                          int* __restrict__ row_of) {
-    extern __shared__ int s_ids[];  // [kChunk * k]
-    const int chunk = blockIdx.x;
-    const int t0 = chunk * kChunk;
-    const int n = kChunk * k;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int t = t0 + i / k;
-        s_ids[i] = t < T ? ids[int64_t(t0) * k + i] : -1;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int pos = offs_pad[e] + hist[int64_t(chunk) * E + e];
-        for (int i = 0; i < n; ++i) {
-            if (s_ids[i] == e) {
-                const int t = t0 + i / k;
-                const int64_t ts = int64_t(t0) * k + i;
-                perm_src[pos] = t;
-                pp_perm[pos] = pp[ts];
-                row_of[ts] = pos;
-                ++pos;
-            }
+// items [0, T*k): routes; items [T*k, T*k + E*128): padding rows (expert j/128, row j%128)
+__global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
+    const int* __restrict__ ids, const float* __restrict__ pp, const int* __restrict__ rank,
+    const int* __restrict__ counts, const int* __restrict__ offs_pad, int T, int E, int k,
+    const uint4* __restrict__ hidden, int vec_per_row, int* __restrict__ perm_src, float* __restrict__ pp_perm,
+    int* __restrict__ row_of, uint4* __restrict__ x_perm) {
+    const int64_t item = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int64_t n_routes = int64_t(T) * k;
+    if (item < n_routes) {
+        const int e = __ldg(ids + item);
+        if (e < 0) return;
+        const int t = int(item / k);
+        const int pos = __ldg(offs_pad + e) + __ldg(rank + item);
+        if (lane == 0) {
+            perm_src[pos] = t;
+            pp_perm[pos] = __ldg(pp + item);
+            row_of[item] = pos;
         }
+        const uint4* src = hidden + int64_t(t) * vec_per_row;
+        uint4* dst = x_perm + int64_t(pos) * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+        return;
     }
+    const int64_t j = item - n_routes;
+    if (j >= int64_t(E) * kBM) return;
+    const int e = int(j / kBM);
+    const int r = int(j % kBM);
+    const int cnt = __ldg(counts + e);
+    const int pad = (cnt + kBM - 1) / kBM * kBM - cnt;
+    if (r >= pad) return;
+    const int pos = __ldg(offs_pad + e) + cnt + r;
+    if (lane == 0) {
+        perm_src[pos] = -1;
+        pp_perm[pos] = 0.0f;
+    }
+    uint4* dst = x_perm + int64_t(pos) * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
 }
 
 __global__ void export_routing_kernel(const int* __restrict__ ids, const int* __restrict__ row_of,
@@ -207,32 +232,40 @@ __global__ void export_routing_kernel(const int* __restrict__ ids, const int* __
 
 }  // namespace
 
+int route_rank_max_tokens() { return kRankThreads * 64; }
+
 cudaError_t launch_route_pack(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
-                              int* row_of, int* hist, int* status, cudaStream_t st) {
-    const int nchunks = (T + kChunk - 1) / kChunk;
-    if (nchunks == 0) return cudaSuccess;
-    route_pack_kernel<<<nchunks, kPackThreads, E * sizeof(int), st>>>(map, probs, T, E, k, ids, pp, row_of, hist,
-                                                                      status);
+                              int* row_of, int* status, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    route_pack_kernel<<<(T + kWarpsPerBlock - 1) / kWarpsPerBlock, 32 * kWarpsPerBlock, 0, st>>>(
+        map, probs, T, E, k, ids, pp, row_of, status);
     count_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_route_scan(int* hist, int nchunks, int E, int* counts, int* offsets, int* offs_pad,
-                              int* mtile_expert, int* meta, int* perm_src, float* pp_perm, cudaStream_t st) {
+cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, int k, int* rank, int* counts,
+                              cudaStream_t st) {
+    route_rank_kernel<<<E, kRankThreads, 0, st>>>(map, ids, T, E, k, rank, counts);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan(const int* counts, int E, int* offsets, int* offs_pad, int* mtile_expert, int* meta,
+                              cudaStream_t st) {
     const int threads = (E + 31) / 32 * 32;
-    route_scan_kernel<<<1, threads, 0, st>>>(hist, nchunks, E, counts, offsets, offs_pad, mtile_expert, meta,
-                                             perm_src, pp_perm);
+    route_scan_kernel<<<1, threads, 0, st>>>(counts, E, offsets, offs_pad, mtile_expert, meta);
     count_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_route_place(const int* ids, const float* pp, int T, int E, int k, const int* hist,
-                               const int* offs_pad, int* perm_src, float* pp_perm, int* row_of, cudaStream_t st) {
-    const int nchunks = (T + kChunk - 1) / kChunk;
-    if (nchunks == 0) return cudaSuccess;
-    const int threads = E < 512 ? (E + 31) / 32 * 32 : 512;
-    route_place_kernel<<<nchunks, threads, kChunk * k * sizeof(int), st>>>(ids, pp, T, E, k, hist, offs_pad,
-                                                                           perm_src, pp_perm, row_of);
+cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* counts,
+                               const int* offs_pad, int T, int E, int k, const __nv_bfloat16* hidden, int H,
+                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, cudaStream_t st) {
+    const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
+    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    route_place_kernel<<<unsigned(blocks), 32 * kWarpsPerBlock, 0, st>>>(
+        ids, pp, rank, counts, offs_pad, T, E, k, reinterpret_cast<const uint4*>(hidden), H / 8, perm_src, pp_perm,
+        row_of, reinterpret_cast<uint4*>(x_perm));
     count_launch();
     return cudaGetLastError();
 }

@@ -160,9 +160,11 @@ def bf16_alternative(x, band):
 
 def fp32_dot_band(terms_sq_sum, K):
     """Evaluation band of an fp32-accumulated dot product of length K whose
-    terms t have sum(t^2) = terms_sq_sum: U32 * sqrt(K) * ||t||_2 (about ten
-    times the typical accumulation error)."""
-    return U32 * np.sqrt(K) * np.sqrt(terms_sq_sum)
+    terms t have sum(t^2) = terms_sq_sum: 8 U32 sqrt(K) ||t||_2. An accumulator
+    that adds 16-term partial products with truncation, not round-to-nearest,
+    drifts by about U32 (K/16)^(3/2) rms(t) (~1.5 U32 sqrt(K) ||t|| at K=2048);
+    the factor 8 covers that bias several times over."""
+    return 8.0 * U32 * np.sqrt(K) * np.sqrt(terms_sq_sum)
 
 
 ELEMENTWISE_BAND = 2.0 ** -20   # relative band of fp32 elementwise evaluation (exp, products)
