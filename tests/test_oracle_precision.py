@@ -198,5 +198,5 @@ def test_envelope_covers_fp32_evaluation(seed):
     # the envelope mostly stays far below the tolerance floor (1e-3 max|ref|) it is added to
     for n, ref in (("out", out_b), ("dhidden", dh_b), ("shared_gate", g_b["shared_gate"])):
         sc = np.abs(ref).max()
-        assert np.median(env[n]) < 1e-4 * sc and np.percentile(env[n], 99) < 1e-3 * sc, n
+        assert np.median(env[n]) < 2.5e-4 * sc and np.percentile(env[n], 99) < 1e-3 * sc, n
         assert env[n].max() < 5e-3 * sc, n
