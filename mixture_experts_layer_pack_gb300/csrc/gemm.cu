@@ -138,11 +138,29 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, 
     }
 }
 
+// Writes a warp's 32x32 fp32 chunk (lane = row) into its 4 KB staging buffer,
+// 128-byte swizzled (16-byte unit j of row r at j ^ (r % 8)): conflict-free
+// both for this write and for the transposed read below, and the layout a TMA
+// box with 128-byte swizzle expects.
+__device__ __forceinline__ void stage_chunk(float* staging, const float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+    float4* srow = reinterpret_cast<float4*>(staging + lane * 32);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) srow[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+}
+
+// step i of the transposed read: row i*4 + lane/8, columns 4*(lane%8) .. +3
+__device__ __forceinline__ float4 staged(const float* staging, int i) {
+    const int lane = threadIdx.x & 31;
+    const int r = i * 4 + (lane >> 3);
+    return reinterpret_cast<const float4*>(staging + r * 32)[(lane & 7) ^ (r & 7)];
+}
+
 template <int OP, int BN>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int q, int half, const GemmArgs& a,
                                               float* staging, const CUtensorMap* mC0, const CUtensorMap* mC1) {
     const int lane = threadIdx.x & 31;
-    const int r_local = q * 32 + lane;
     if (OP == OP_WGRAD) {
         // main_grad[e][m][n] += acc through TMA reduce-add: the warp stages its 32
         // rows x 32 columns in shared memory (128-byte swizzle) and one lane
@@ -151,16 +169,13 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
         const bool hi = m0 >= a.m_split;
         const CUtensorMap* mc = hi ? mC1 : mC0;
         const int row0 = hi ? m0 - a.m_split : m0;
-        float4* srow = reinterpret_cast<float4*>(staging + lane * 32);
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += kEpiHalves) {
             float v[32];
             tmem_ld32(t_row + c * 32, v);
             if (lane == 0) bulk_wait_read<0>();      // the previous box has left the staging buffer
             __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                srow[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            stage_chunk(staging, v);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -171,8 +186,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
         return;
     }
 
-    const int row = t.mt * kBM + r_local;
-    const bool store = row < a.rows_valid;
+    // The warp owns rows [m_base, m_base+32) of the tile. Each 32x32 fp32 chunk
+    // read from TMEM (lane = row) is transposed through the warp's staging
+    // buffer so that global loads and stores cover whole row segments: in step
+    // i a lane holds row i*4 + lane/8, columns 4*(lane%8) .. +3.
+    const int m_base = t.mt * kBM + q * 32;
+    const int sub_row = lane >> 3;
+    const int sub_col = 4 * (lane & 7);
+    const bool lane_row_valid = m_base + lane < a.rows_valid;
 
     if (OP == OP_FWD_GU) {
         const int j0 = t.nt * (BN / 2);
@@ -181,79 +202,128 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             float g[32], u[32];
             tmem_ld32(t_row + c * 32, g);
             tmem_ld32(t_row + BN / 2 + c * 32, u);
-            if (store) {
-                float act[32];
+            float4 gv[8], uv[8];
+            stage_chunk(staging, g);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) act[i] = g[i] * sigmoidf_(g[i]) * u[i];
-                const int j = j0 + c * 32;
-                store_bf16x32(a.out0 + int64_t(row) * a.ld_out0 + j, act);
-                store_f32x32(a.outf + int64_t(row) * a.ld_outf + j, g);
-                store_f32x32(a.outf + int64_t(row) * a.ld_outf + a.inter + j, u);
+            for (int i = 0; i < 8; ++i) gv[i] = staged(staging, i);
+            __syncwarp();
+            stage_chunk(staging, u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) uv[i] = staged(staging, i);
+            __syncwarp();
+            const int col = j0 + c * 32 + sub_col;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int row = m_base + i * 4 + sub_row;
+                if (row >= a.rows_valid) continue;
+                const float4 g4 = gv[i], u4 = uv[i];
+                const float a0 = g4.x * sigmoidf_(g4.x) * u4.x, a1 = g4.y * sigmoidf_(g4.y) * u4.y;
+                const float a2 = g4.z * sigmoidf_(g4.z) * u4.z, a3 = g4.w * sigmoidf_(g4.w) * u4.w;
+                *reinterpret_cast<uint2*>(a.out0 + int64_t(row) * a.ld_out0 + col) =
+                    make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
+                float* gu = a.outf + int64_t(row) * a.ld_outf;
+                *reinterpret_cast<float4*>(gu + col) = g4;
+                *reinterpret_cast<float4*>(gu + a.inter + col) = u4;
             }
         }
     } else if (OP == OP_FWD_DOWN || OP == OP_BWD_GU) {
-        const float scale = (store && a.row_scale) ? a.row_scale[row] : 1.0f;
+        const float lane_scale = (OP == OP_FWD_DOWN && a.row_scale && lane_row_valid) ? a.row_scale[m_base + lane]
+                                                                                       : 1.0f;
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += kEpiHalves) {
             float v[32];
             tmem_ld32(t_row + c * 32, v);
-            if (store) {
-                if (OP == OP_FWD_DOWN) {
+            stage_chunk(staging, v);
+            const int col = t.nt * BN + c * 32 + sub_col;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= scale;
+            for (int i = 0; i < 8; ++i) {
+                const int r_local = i * 4 + sub_row;
+                const float sc = __shfl_sync(0xffffffffu, lane_scale, r_local);
+                float4 x = staged(staging, i);
+                const int row = m_base + r_local;
+                if (row >= a.rows_valid) continue;
+                if (OP == OP_FWD_DOWN) {
+                    x.x *= sc;
+                    x.y *= sc;
+                    x.z *= sc;
+                    x.w *= sc;
                 }
-                store_f32x32(a.outf + int64_t(row) * a.ld_outf + t.nt * BN + c * 32, v);
+                *reinterpret_cast<float4*>(a.outf + int64_t(row) * a.ld_outf + col) = x;
             }
+            __syncwarp();
         }
     } else {  // OP_BWD_DOWN: acc = da_u = go . W_down[e] for columns i of the tile
-        const float p = (store && a.row_scale) ? a.row_scale[row] : 1.0f;
-        float part = 0.0f;
+        const float lane_p = (a.row_scale && lane_row_valid) ? a.row_scale[m_base + lane] : 1.0f;
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = 0.0f;
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += kEpiHalves) {
             float d[32];
             tmem_ld32(t_row + c * 32, d);
-            if (!store) continue;
-            const int i0 = t.nt * BN + c * 32;
-            const uint4* pa = reinterpret_cast<const uint4*>(a.in0 + int64_t(row) * a.ld_in0 + i0);
-            const float4* pg = reinterpret_cast<const float4*>(a.inf + int64_t(row) * a.ld_inf + i0);
-            const float4* pu = reinterpret_cast<const float4*>(a.inf + int64_t(row) * a.ld_inf + a.inter + i0);
-            uint4* pdg = reinterpret_cast<uint4*>(a.out0 + int64_t(row) * a.ld_out0 + i0);
-            uint4* pdu = reinterpret_cast<uint4*>(a.out0 + int64_t(row) * a.ld_out0 + a.inter + i0);
-            uint4* pap = a.out1 ? reinterpret_cast<uint4*>(a.out1 + int64_t(row) * a.ld_out1 + i0) : nullptr;
+            stage_chunk(staging, d);
+            const int col = t.nt * BN + c * 32 + sub_col;
+            // load phase: every input of the chunk is requested before any result
+            // is stored, so the eight row steps share one memory latency
+            uint2 aw[8];
+            float4 g4[8], u4[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 wa = pa[q];
-                const float4 g0 = pg[2 * q], g1 = pg[2 * q + 1], u0 = pu[2 * q], u1 = pu[2 * q + 1];
-                const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w};
-                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                uint32_t dgw[4], duw[4], apw[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    float av[2];
-                    unpack_bf16x2(aw[h], av[0], av[1]);
-                    float dg[2], du[2], ap[2];
-#pragma unroll
-                    for (int z = 0; z < 2; ++z) {
-                        const float dd = d[8 * q + 2 * h + z];
-                        const float gg = gv[2 * h + z], uu = uv[2 * h + z];
-                        part = fmaf(av[z], dd, part);
-                        const float sg = sigmoidf_(gg);
-                        const float da = p * dd;
-                        dg[z] = da * uu * (sg * (1.0f + gg * (1.0f - sg)));
-                        du[z] = da * (gg * sg);
-                        ap[z] = p * av[z];
-                    }
-                    dgw[h] = pack_bf16x2(dg[0], dg[1]);
-                    duw[h] = pack_bf16x2(du[0], du[1]);
-                    apw[h] = pack_bf16x2(ap[0], ap[1]);
+            for (int i = 0; i < 8; ++i) {
+                const int row = m_base + i * 4 + sub_row;
+                if (row < a.rows_valid) {
+                    aw[i] = __ldg(reinterpret_cast<const uint2*>(a.in0 + int64_t(row) * a.ld_in0 + col));
+                    const float* gu = a.inf + int64_t(row) * a.ld_inf;
+                    g4[i] = __ldg(reinterpret_cast<const float4*>(gu + col));
+                    u4[i] = __ldg(reinterpret_cast<const float4*>(gu + a.inter + col));
+                } else {
+                    aw[i] = make_uint2(0, 0);
+                    g4[i] = u4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                pdg[q] = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
-                pdu[q] = make_uint4(duw[0], duw[1], duw[2], duw[3]);
-                if (pap) pap[q] = make_uint4(apw[0], apw[1], apw[2], apw[3]);
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r_local = i * 4 + sub_row;
+                const float p = __shfl_sync(0xffffffffu, lane_p, r_local);
+                const float4 d4 = staged(staging, i);
+                const int row = m_base + r_local;
+                if (row >= a.rows_valid) continue;
+                float av[4];
+                unpack_bf16x2(aw[i].x, av[0], av[1]);
+                unpack_bf16x2(aw[i].y, av[2], av[3]);
+                const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float gv[4] = {g4[i].x, g4[i].y, g4[i].z, g4[i].w};
+                const float uv[4] = {u4[i].x, u4[i].y, u4[i].z, u4[i].w};
+                float dg[4], du[4], ap[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    part[i] = fmaf(av[z], dv[z], part[i]);
+                    const float sg = sigmoidf_(gv[z]);
+                    const float da = p * dv[z];
+                    dg[z] = da * uv[z] * (sg * (1.0f + gv[z] * (1.0f - sg)));
+                    du[z] = da * (gv[z] * sg);
+                    ap[z] = p * av[z];
+                }
+                __nv_bfloat16* o = a.out0 + int64_t(row) * a.ld_out0;
+                *reinterpret_cast<uint2*>(o + col) = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
+                *reinterpret_cast<uint2*>(o + a.inter + col) =
+                    make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
+                if (a.out1)
+                    *reinterpret_cast<uint2*>(a.out1 + int64_t(row) * a.ld_out1 + col) =
+                        make_uint2(pack_bf16x2(ap[0], ap[1]), pack_bf16x2(ap[2], ap[3]));
+            }
+            __syncwarp();
         }
-        if (store && a.partial) a.partial[(int64_t(row) * a.n_tiles + t.nt) * kEpiHalves + half] = part;
+        // the 8 lanes holding one row's columns add up their partial dot products
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float v = part[i];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            const int row = m_base + i * 4 + sub_row;
+            if ((lane & 7) == 0 && row < a.rows_valid && a.partial)
+                a.partial[(int64_t(row) * a.n_tiles + t.nt) * kEpiHalves + half] = v;
+        }
     }
 }
 
