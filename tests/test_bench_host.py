@@ -1,0 +1,66 @@
+"""Host logic of bench.py's multi-replica mode on CPU ranks (gloo, world size 2):
+max-over-ranks timing, whole-job throughput, and the reference arm's rank rule."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        elapsed = [1.5 + rank, 10.0 * (rank + 1)]                      # rank 1 is the slow one
+        mx = bench.reduce_max(elapsed, world, torch.device("cpu"))
+        bench.barrier(world)
+        value = bench.aggregate([100] * world, mx[0])
+        out[rank] = (mx, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_throughput():
+    world = 2
+    manager = mp.Manager()
+    out = manager.dict()
+    mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+    for rank in range(world):
+        mx, value = out[rank]
+        assert mx == [2.5, 20.0]                       # every rank sees the slowest rank's time
+        assert value == pytest.approx(200 / 2.5)       # units of all ranks / slowest time
+
+
+def test_single_rank_helpers_need_no_process_group():
+    assert bench.reduce_max([3.0, 4.0], 1, torch.device("cpu")) == [3.0, 4.0]
+    assert bench.aggregate([50], 0.5) == 100.0
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    args = bench.parse_args(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"])
+    assert bench.run_reference(args) == 0              # returns at once, prints nothing
+
+
+def test_kernel_work_table_covers_every_kernel_class():
+    import mixture_experts_layer_pack_gb300 as M
+    names = [M.moe_kernel_name(i) for i in range(18)]
+    for n in names:
+        f, b = bench.kernel_work(n, 4096, 2048, 96, 6, 1024, 24576, 96)
+        assert f >= 0 and b >= 0
+    # the dominant wgrad kernel is HBM-bound at the proxy-like shape
+    peaks = dict(hbm_gbs=6791.0, bf16_tflops=1902.3, bf16_tflops_sustained=1710.5)
+    r = bench.roofline_of("gemm_wgrad_fc1_routed", 0.65, bench.kernel_work("gemm_wgrad_fc1_routed", 4096, 2048, 96,
+                                                                           6, 1024, 24576, 96), peaks, "measured")
+    assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5
