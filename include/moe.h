@@ -148,6 +148,29 @@ moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* id
                               int32_t* counts, int32_t* offsets, int32_t* perm_src,
                               int32_t* row_of, void* stream);
 
+/* Routing without any device allocation, for callers that cannot allocate
+ * device memory: code that runs where cudaMalloc is not allowed or not
+ * wanted, such as a plugin called from a host framework that owns all device
+ * memory through its own pool, a serving loop that forbids allocation after
+ * start-up, or a memory budget that must stay fixed. The pages have no
+ * counterpart to this call.
+ * It computes the same routing as moe_forward and moe_export_routing, in the
+ * same compact form, into caller device buffers: ids[T,k] int32 (-1 =
+ * missing), pp[T,k] fp32, counts[E] int32, offsets[E+1] int32, perm_src[T*k]
+ * int32 (first offsets[E] entries), row_of[T,k] int32, and routing_error[1]
+ * int32 (1 when a row has more than k routes; such rows are dropped).
+ * Its only scratch is a library-owned device array of 2^17 int32 (512 KB)
+ * that every GPU loading the library keeps until the process exits, so
+ * T*k must not exceed 131072 (and T not 65536): larger sizes return
+ * MOE_ERR_UNSUPPORTED. The array is shared by every call and keeps the last
+ * call's contents; calls whose kernels overlap on the GPU (two streams, two
+ * threads) race on it. The first call on each device resolves the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture. Asynchronous on `stream`; nothing is allocated or freed. */
+moe_status moe_route_noalloc(int64_t T, int64_t E, int64_t k, const uint8_t* routing_map, const float* probs,
+                             int32_t* ids, float* pp, int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                             int32_t* row_of, int32_t* routing_error, void* stream);
+
 /* Synchronises `stream`, returns the device status recorded since the last
  * call (MOE_OK, MOE_ERR_ROUTING or MOE_ERR_TIMEOUT) and clears it. */
 moe_status moe_device_status(moe_handle* h, void* stream);

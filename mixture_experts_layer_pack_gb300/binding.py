@@ -48,7 +48,8 @@ _LIB = None
 _LOCK = threading.Lock()
 EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size", "moe_saved_create",
             "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
-            "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name")
+            "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name",
+            "moe_route_noalloc")
 MOE_K_COUNT = 18
 
 
@@ -89,11 +90,12 @@ def load(build_if_missing: bool = True):
         L.moe_profile_read.argtypes = [c_void_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int64), c_int32]
         L.moe_kernel_name.argtypes = [c_int32]
         L.moe_kernel_name.restype = ctypes.c_char_p
+        L.moe_route_noalloc.argtypes = [c_int64, c_int64, c_int64] + [c_void_p] * 10
         L.moe_status_string.argtypes = [c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_workspace_size", "moe_saved_size", "moe_create", "moe_saved_create", "moe_forward",
                      "moe_backward", "moe_export_routing", "moe_device_status", "moe_profile_enable",
-                     "moe_profile_read"):
+                     "moe_profile_read", "moe_route_noalloc"):
             getattr(L, name).restype = c_int32
         _LIB = L
         return L
@@ -175,6 +177,14 @@ def moe_export_routing(h, saved, ids=None, pp=None, counts=None, offsets=None, p
 
 def moe_device_status(h, stream=None) -> int:
     return int(load().moe_device_status(h, _stream_ptr(stream)))
+
+
+def moe_route_noalloc(T, E, k, routing_map, probs, ids, pp, counts, offsets, perm_src, row_of, routing_error,
+                      stream=None):
+    """Routing into caller buffers with no device allocation (see include/moe.h)."""
+    _check(load().moe_route_noalloc(int(T), int(E), int(k), _ptr(routing_map), _ptr(probs), _ptr(ids), _ptr(pp),
+                                    _ptr(counts), _ptr(offsets), _ptr(perm_src), _ptr(row_of), _ptr(routing_error),
+                                    _stream_ptr(stream)), "moe_route_noalloc")
 
 
 def moe_launch_count() -> int:

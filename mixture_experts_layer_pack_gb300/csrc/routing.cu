@@ -21,8 +21,11 @@
 //          expert of every 128-row tile, the tile count
 //   place  one warp per route (and per padding row): writes the permutation
 //          entries and copies the token's hidden row into its permuted row
+#include "../../include/moe.h"
 #include "device_common.cuh"
 #include "internal.h"
+
+#include <mutex>
 
 namespace moe {
 
@@ -281,3 +284,96 @@ cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* 
 }
 
 }  // namespace moe
+
+// ======================================================================
+// Routing without any device allocation (moe_route_noalloc).
+//
+// Its only scratch -- the rank of every route inside its expert -- is this
+// file-scope device array, which every GPU that loads the library holds until
+// the process exits. Every call shares it; nothing in it has to start at zero
+// (each call writes the rank of every route it later reads), and calls whose
+// kernels overlap on the GPU race on it.
+// ======================================================================
+namespace moe {
+namespace {
+
+constexpr int64_t kNoAllocMaxRoutes = int64_t(1) << 17;  // T * k, 512 KB of int32
+static __device__ __align__(256) int g_noalloc_rank[kNoAllocMaxRoutes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int* g_noalloc_rank_ptr[kMaxDevices] = {};
+
+// device address of the scratch array on the current device, resolved once
+int* noalloc_scratch(int device) {
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_rank_ptr[device]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || !p) return nullptr;
+        g_noalloc_rank_ptr[device] = static_cast<int*>(p);
+    }
+    return g_noalloc_rank_ptr[device];
+}
+
+__global__ void __launch_bounds__(1024) route_scan_compact_kernel(const int* __restrict__ counts, int E,
+                                                                  int* __restrict__ offsets) {
+    __shared__ int s_warp[32];
+    const int e = threadIdx.x;
+    const int cnt = e < E ? counts[e] : 0;
+    int total;
+    const int off = block_excl_scan(cnt, s_warp, total);
+    if (e < E) offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(256) route_place_compact_kernel(const int* __restrict__ ids,
+                                                                  const int* __restrict__ rank,
+                                                                  const int* __restrict__ offsets, int T, int k,
+                                                                  int* __restrict__ perm_src,
+                                                                  int* __restrict__ row_of) {
+    const int64_t item = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (item >= int64_t(T) * k) return;
+    const int e = ids[item];
+    if (e < 0) return;  // the pack kernel already wrote row_of = -1
+    const int pos = offsets[e] + rank[item];
+    perm_src[pos] = int(item / k);
+    row_of[item] = pos;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(int64_t T, int64_t E, int64_t k, const uint8_t* routing_map,
+                                        const float* probs, int32_t* ids, float* pp, int32_t* counts,
+                                        int32_t* offsets, int32_t* perm_src, int32_t* row_of,
+                                        int32_t* routing_error, void* stream) {
+    using namespace moe;
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_INVALID_ARG;
+    if (T * k > kNoAllocMaxRoutes || T > route_rank_max_tokens()) return MOE_ERR_UNSUPPORTED;
+    if (!counts || !offsets || !routing_error) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!routing_map || !probs || !ids || !pp || !perm_src || !row_of)) return MOE_ERR_INVALID_ARG;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return MOE_ERR_CUDA;
+    int* rank = noalloc_scratch(device);
+    if (!rank) return MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(routing_error, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (T == 0) {
+        if (cudaMemsetAsync(counts, 0, E * sizeof(int32_t), st) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    const int Ti = int(T), Ei = int(E), ki = int(k);
+    if (launch_route_pack(routing_map, probs, Ti, Ei, ki, ids, pp, row_of, routing_error, st) != cudaSuccess ||
+        launch_route_rank(routing_map, ids, Ti, Ei, ki, rank, counts, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    route_scan_compact_kernel<<<1, (Ei + 31) / 32 * 32, 0, st>>>(counts, Ei, offsets);
+    count_launch();
+    const int64_t n = T * k;
+    route_place_compact_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(ids, rank, offsets, Ti, ki, perm_src,
+                                                                          row_of);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
