@@ -68,7 +68,15 @@ typedef struct {
  * routed_up, routed_down). Gate/up are [I,H] (routed [E,I,H]), down is [H,I]
  * (routed [E,H,I]). A combined FC1 [.., 2I, H] is passed as two views whose
  * data pointers differ by I rows (runtime page, _gate_up_weight_arguments).
- * data must be 16-byte aligned and row_stride*elem_size a multiple of 16. */
+ * data must be 16-byte aligned and row_stride*elem_size a multiple of 16.
+ * MXFP8 routed views (PR #6572, Supported configurations; PR #8210 review on
+ * rowwise/columnwise payloads and scales): data is the E4M3 payload quantised
+ * in blocks of 32 along K (the row), col_data the payload quantised in blocks
+ * of 32 down the rows (N), both with expert_stride/row_stride in bytes
+ * (multiples of 32). E8M0 scales are indexed with those strides:
+ * scale[e][n][kb] at e*expert_stride/32 + n*row_stride/32 + kb, and
+ * col_scale[e][nb][k] at e*expert_stride/32 + nb*row_stride + k -- for a
+ * compact payload these are the compact [E,N,K/32] and [E,N/32,K] arrays. */
 typedef struct {
     const void* data;         /* bf16 elements (MXFP8: e4m3 rowwise payload) */
     int64_t expert_stride;    /* elements between experts (routed views) */
@@ -137,6 +145,26 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
  *   received no tokens keep their main_grad bitwise. `saved` is not consumed. */
 moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved,
                         void* dhidden, float* dprobs, const moe_main_grads* mg, void* stream);
+
+/* MXFP8 weight preparation (PR #6572, Design > MCore-owned parameters:
+ * converted scale layouts refreshed once per optimizer iteration at stable
+ * addresses; PR #8210 review on _swizzle_mxfp8_scale): converts the routed
+ * weights' compact E8M0 scales (rowwise and columnwise, all experts in one
+ * launch each) into the scale-factor layout of the block-scaled MMA, in the
+ * handle's workspace. Call after every change of the routed weights' scales
+ * and before moe_forward; payloads are read in place. No-op for BF16 handles.
+ * moe_forward on an MXFP8 handle before the first call returns MOE_ERR_STATE. */
+moe_status moe_prepare_weights(moe_handle* h, const moe_weights* w, void* stream);
+
+/* MXFP8 quantisation of a bf16 matrix x[rows, cols] (row stride ld elements):
+ * E4M3 elements (round to nearest even, saturating at +-448) and one E8M0
+ * shared exponent per 32 elements, floor(log2 amax) - 8 + 127 clamped to
+ * [0, 254] (OCP MX v1.0; the pages name MXFP8 without restating it).
+ * axis 1: blocks along each row (cols % 32 == 0), scales[rows, cols/32];
+ * axis 0: blocks down each column (rows % 32 == 0), scales[rows/32, cols].
+ * q[rows, cols] E4M3 bytes with row stride ldq; all device pointers. */
+moe_status moe_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t axis, uint8_t* q,
+                              int64_t ldq, uint8_t* scales, void* stream);
 
 /* Test hook: copies the routing of `saved` into caller device buffers.
  * ids[T,k] int32 (-1 = missing), pp[T,k] fp32, counts[E] int32,

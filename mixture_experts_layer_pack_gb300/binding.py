@@ -49,7 +49,7 @@ _LOCK = threading.Lock()
 EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size", "moe_saved_create",
             "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
             "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name",
-            "moe_route_noalloc")
+            "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8")
 MOE_K_COUNT = 18
 
 
@@ -91,11 +91,14 @@ def load(build_if_missing: bool = True):
         L.moe_kernel_name.argtypes = [c_int32]
         L.moe_kernel_name.restype = ctypes.c_char_p
         L.moe_route_noalloc.argtypes = [c_int64, c_int64, c_int64] + [c_void_p] * 10
+        L.moe_prepare_weights.argtypes = [c_void_p, P(moe_weights), c_void_p]
+        L.moe_quantize_mxfp8.argtypes = [c_void_p, c_int64, c_int64, c_int64, c_int32, c_void_p, c_int64, c_void_p,
+                                         c_void_p]
         L.moe_status_string.argtypes = [c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_workspace_size", "moe_saved_size", "moe_create", "moe_saved_create", "moe_forward",
                      "moe_backward", "moe_export_routing", "moe_device_status", "moe_profile_enable",
-                     "moe_profile_read", "moe_route_noalloc"):
+                     "moe_profile_read", "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8"):
             getattr(L, name).restype = c_int32
         _LIB = L
         return L
@@ -187,6 +190,40 @@ def moe_route_noalloc(T, E, k, routing_map, probs, ids, pp, counts, offsets, per
                                     _stream_ptr(stream)), "moe_route_noalloc")
 
 
+def moe_prepare_weights(h, weights: moe_weights, stream=None):
+    _check(load().moe_prepare_weights(h, ctypes.byref(weights), _stream_ptr(stream)), "moe_prepare_weights")
+
+
+def moe_quantize_mxfp8(x, axis, q, scales, stream=None):
+    """MXFP8-quantise a 2-D bf16 tensor x into q (uint8, same shape) and compact scales."""
+    rows, cols = x.shape
+    _check(load().moe_quantize_mxfp8(_ptr(x), rows, cols, x.stride(0), int(axis), _ptr(q), q.stride(0),
+                                     _ptr(scales), _stream_ptr(stream)), "moe_quantize_mxfp8")
+
+
+def mxfp8_weight(w):
+    """Quantises a bf16 weight [E, N, K] (or a combined-FC1 row view of one) on the
+    device with moe_quantize_mxfp8: returns (rowwise payload, compact row scales,
+    columnwise payload, compact column scales) as [E, N, K], [E, N, K/32],
+    [E, N, K], [E, N/32, K] uint8 tensors."""
+    import torch
+    E, N, K = w.shape
+    x = w.reshape(E * N, K).contiguous()
+    q = torch.empty((E * N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((E * N, K // 32), dtype=torch.uint8, device=w.device)
+    moe_quantize_mxfp8(x, 1, q, s)
+    qc = torch.empty((E * N, K), dtype=torch.uint8, device=w.device)
+    sc = torch.empty((E * N // 32, K), dtype=torch.uint8, device=w.device)
+    moe_quantize_mxfp8(x, 0, qc, sc)
+    return q.view(E, N, K), s.view(E, N, K // 32), qc.view(E, N, K), sc.view(E, N // 32, K)
+
+
+def mxfp8_view(payload, scale, col_payload, col_scale) -> moe_wview:
+    """moe_wview of an MXFP8 routed weight ([E, N, K] payloads, strides in bytes)."""
+    return moe_wview(payload.data_ptr(), payload.stride(0), payload.stride(1), scale.data_ptr(),
+                     col_payload.data_ptr(), col_scale.data_ptr())
+
+
 def moe_launch_count() -> int:
     return int(load().moe_launch_count())
 
@@ -255,6 +292,9 @@ class MoELayer:
         with torch.cuda.device(self.device):
             self.handle = moe_create(self.cfg, self.workspace)
             self.saved = moe_saved_create(self.handle, self.saved_mem)
+
+    def prepare_weights(self, weights: moe_weights, stream=None):
+        moe_prepare_weights(self.handle, weights, stream)
 
     def forward(self, hidden, probs, routing_map, weights: moe_weights, out=None, stream=None):
         import torch

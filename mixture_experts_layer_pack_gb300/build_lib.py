@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmoe.so")
-SOURCES = ["gemm.cu", "routing.cu", "elementwise.cu", "moe_api.cu"]
+SOURCES = ["gemm.cu", "routing.cu", "elementwise.cu", "mxfp8.cu", "moe_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 
@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     libdir = _cuda_lib_dir(nvcc)
     tmp = LIB + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp,
-           "-Xlinker", f"-rpath,{libdir}"]
+           "-Xlinker", f"-rpath,{libdir}", "-Xlinker", "--no-undefined"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

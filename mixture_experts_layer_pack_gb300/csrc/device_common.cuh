@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -216,6 +217,85 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v
         unpack_bf16x2(w.y, v[8 * q + 2], v[8 * q + 3]);
         unpack_bf16x2(w.z, v[8 * q + 4], v[8 * q + 5]);
         unpack_bf16x2(w.w, v[8 * q + 6], v[8 * q + 7]);
+    }
+}
+
+// ---------------------------------------------------------------- MXFP8 (OCP MX v1.0)
+// Shared-exponent code of a 32-element block whose largest magnitude is amax:
+// floor(log2 amax) - 8 (8 = largest E4M3 exponent) + 127, clamped to [0, 254];
+// an all-zero block gets 0. For a normal fp32 amax floor(log2 amax) is its
+// unbiased exponent, so the code is the biased exponent minus 8.
+__device__ __forceinline__ uint32_t e8m0_code(float amax) {
+    const int eb = int((__float_as_uint(amax) >> 23) & 0xFF);
+    const int c = eb - 8;
+    return uint32_t(c < 0 ? 0 : (c > 254 ? 254 : c));
+}
+
+// 2^(127 - code) as an fp32 (exact; code 254 gives the subnormal 2^-127)
+__device__ __forceinline__ float e8m0_inv_scale(uint32_t code) {
+    const int e = 254 - int(code);
+    return e > 0 ? __uint_as_float(uint32_t(e) << 23) : __uint_as_float(0x00400000u);
+}
+
+// 2^(code - 127) as an fp32
+__device__ __forceinline__ float e8m0_scale(uint32_t code) {
+    return code > 0 ? __uint_as_float(code << 23) : __uint_as_float(0x00400000u);
+}
+
+// four fp32 -> four E4M3 codes (round to nearest even, saturating at +-448), first in the low byte
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    return uint32_t(__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3)) |
+           (uint32_t(__nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3)) << 8) |
+           (uint32_t(__nv_cvt_float_to_fp8(c, __NV_SATFINITE, __NV_E4M3)) << 16) |
+           (uint32_t(__nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3)) << 24);
+}
+
+// value of an E4M3 code
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(code & 0xFF), __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// Byte offset of the scale of (row r, 32-element K block kb) in the scale-factor
+// layout the block-scaled MMA reads: per 128 rows x 4 K blocks one 512-byte atom,
+// byte 16*(r%32) + 4*((r%128)/32) + kb%4; atoms ordered [r/128][kb/4].
+__device__ __forceinline__ int64_t sf_atom_offset(int64_t r, int kb, int k_blocks) {
+    return ((r >> 7) * (k_blocks >> 2) + (kb >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) + (kb & 3);
+}
+
+// Warp-wide copy of one bf16 row (src null: zeros) that also writes its MXFP8
+// quantisation along the row: a lane owns 8 consecutive elements (16 bytes), 4
+// consecutive lanes one 32-element block. vec_per_row = row length / 8 must be
+// a multiple of 4; all 32 lanes must call it.
+__device__ __forceinline__ void copy_quant_row(const uint4* src, uint4* dst, uint8_t* q, uint8_t* sf, int64_t row,
+                                               int vec_per_row) {
+    const int lane = threadIdx.x & 31;
+    const int k_blocks = vec_per_row / 4;
+    uint8_t* qrow = q + row * int64_t(vec_per_row) * 8;
+    for (int base = 0; base < vec_per_row; base += 32) {
+        const int v = base + lane;
+        const bool active = v < vec_per_row;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (active && src) w = __ldg(src + v);
+        float f[8];
+        unpack_bf16x2(w.x, f[0], f[1]);
+        unpack_bf16x2(w.y, f[2], f[3]);
+        unpack_bf16x2(w.z, f[4], f[5]);
+        unpack_bf16x2(w.w, f[6], f[7]);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t code = e8m0_code(amax);
+        const float mul = e8m0_inv_scale(code);
+        if (active) {
+            dst[v] = w;
+            *reinterpret_cast<uint2*>(qrow + int64_t(v) * 8) =
+                make_uint2(e4m3x4(f[0] * mul, f[1] * mul, f[2] * mul, f[3] * mul),
+                           e4m3x4(f[4] * mul, f[5] * mul, f[6] * mul, f[7] * mul));
+            if ((lane & 3) == 0) sf[sf_atom_offset(row, v >> 2, k_blocks)] = uint8_t(code);
+        }
     }
 }
 

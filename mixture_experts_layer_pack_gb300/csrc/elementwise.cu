@@ -21,13 +21,18 @@ namespace {
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                           const int* __restrict__ perm_src,
                                                           const int* __restrict__ meta, int max_rows, int vec_per_row,
-                                                          uint4* __restrict__ dst) {
+                                                          uint4* __restrict__ dst, uint8_t* __restrict__ dst_q,
+                                                          uint8_t* __restrict__ dst_sf) {
     const int rows = min(meta[2], max_rows);
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
         const int t = perm_src[r];
         uint4* d = dst + int64_t(r) * vec_per_row;
+        if (dst_q) {  // also quantise the row to MXFP8 (the routed dgrad-down GEMM's operand)
+            copy_quant_row(t >= 0 ? src + int64_t(t) * vec_per_row : nullptr, d, dst_q, dst_sf, r, vec_per_row);
+            continue;
+        }
         if (t >= 0) {
             const uint4* s = src + int64_t(t) * vec_per_row;
             for (int v = lane; v < vec_per_row; v += 32) d[v] = __ldg(s + v);
@@ -120,10 +125,10 @@ int grid_for(int64_t work, int threads, int num_sms) {
 }  // namespace
 
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
-                               __nv_bfloat16* dst, int num_sms, cudaStream_t st) {
+                               __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms, cudaStream_t st) {
     const int grid = grid_for(int64_t(max_rows) * 32, 256, num_sms);
     gather_rows_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(src), perm_src, meta, max_rows, H / 8,
-                                              reinterpret_cast<uint4*>(dst));
+                                              reinterpret_cast<uint4*>(dst), dst_q, dst_sf);
     count_launch();
     return cudaGetLastError();
 }

@@ -157,7 +157,20 @@ __device__ __forceinline__ float4 staged(const float* staging, int i) {
     return reinterpret_cast<const float4*>(staging + r * 32)[(lane & 7) ^ (r & 7)];
 }
 
-template <int OP, int BN>
+// Quantises the 32-column block that 8 consecutive lanes hold (4 columns each,
+// same row) to MXFP8: returns the E4M3 codes of this lane's 4 values and the
+// block's E8M0 code (the block amax is reduced over the 8 lanes).
+__device__ __forceinline__ uint32_t mx_quant_lane4(const float (&v)[4], uint32_t& code) {
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    code = e8m0_code(amax);
+    const float mul = e8m0_inv_scale(code);
+    return e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
+}
+
+template <int OP, int BN, bool MX = false>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int q, int half, const GemmArgs& a,
                                               float* staging, const CUtensorMap* mC0, const CUtensorMap* mC1) {
     const int lane = threadIdx.x & 31;
@@ -215,12 +228,25 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = m_base + i * 4 + sub_row;
-                if (row >= a.rows_valid) continue;
                 const float4 g4 = gv[i], u4 = uv[i];
-                const float a0 = g4.x * sigmoidf_(g4.x) * u4.x, a1 = g4.y * sigmoidf_(g4.y) * u4.y;
-                const float a2 = g4.z * sigmoidf_(g4.z) * u4.z, a3 = g4.w * sigmoidf_(g4.w) * u4.w;
+                float av[4] = {g4.x * sigmoidf_(g4.x) * u4.x, g4.y * sigmoidf_(g4.y) * u4.y,
+                               g4.z * sigmoidf_(g4.z) * u4.z, g4.w * sigmoidf_(g4.w) * u4.w};
+                if (MX) {
+                    // the down projection's operand: a quantised along I (this chunk is one
+                    // 32-column block); a itself becomes its exact dequantised value
+                    uint32_t code;
+                    const uint32_t qv = mx_quant_lane4(av, code);
+                    if (row < a.rows_valid) {
+                        *reinterpret_cast<uint32_t*>(a.q_out + int64_t(row) * a.ld_q + col) = qv;
+                        if ((lane & 7) == 0) a.q_sf[sf_atom_offset(row, col >> 5, a.q_kblocks)] = uint8_t(code);
+                    }
+                    const float sc = e8m0_scale(code);
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) av[z] = e4m3_value(qv >> (8 * z)) * sc;
+                }
+                if (row >= a.rows_valid) continue;
                 *reinterpret_cast<uint2*>(a.out0 + int64_t(row) * a.ld_out0 + col) =
-                    make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
+                    make_uint2(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]));
                 float* gu = a.outf + int64_t(row) * a.ld_outf;
                 *reinterpret_cast<float4*>(gu + col) = g4;
                 *reinterpret_cast<float4*>(gu + a.inter + col) = u4;
@@ -286,7 +312,6 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                 const float p = __shfl_sync(0xffffffffu, lane_p, r_local);
                 const float4 d4 = staged(staging, i);
                 const int row = m_base + r_local;
-                if (row >= a.rows_valid) continue;
                 float av[4];
                 unpack_bf16x2(aw[i].x, av[0], av[1]);
                 unpack_bf16x2(aw[i].y, av[2], av[3]);
@@ -303,6 +328,22 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                     du[z] = da * (gv[z] * sg);
                     ap[z] = p * av[z];
                 }
+                if (MX) {
+                    // the gate/up dgrad operand [dg|du] quantised along 2I (32-column blocks)
+                    uint32_t cg, cu;
+                    const uint32_t qg = mx_quant_lane4(dg, cg);
+                    const uint32_t qu = mx_quant_lane4(du, cu);
+                    if (row < a.rows_valid) {
+                        uint8_t* qo = a.q_out + int64_t(row) * a.ld_q;
+                        *reinterpret_cast<uint32_t*>(qo + col) = qg;
+                        *reinterpret_cast<uint32_t*>(qo + a.inter + col) = qu;
+                        if ((lane & 7) == 0) {
+                            a.q_sf[sf_atom_offset(row, col >> 5, a.q_kblocks)] = uint8_t(cg);
+                            a.q_sf[sf_atom_offset(row, (a.inter + col) >> 5, a.q_kblocks)] = uint8_t(cu);
+                        }
+                    }
+                }
+                if (row >= a.rows_valid) continue;
                 __nv_bfloat16* o = a.out0 + int64_t(row) * a.ld_out0;
                 *reinterpret_cast<uint2*>(o + col) = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
                 *reinterpret_cast<uint2*>(o + a.inter + col) =
@@ -496,6 +537,247 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
+
+// ---------------------------------------------------------------- block-scaled MXFP8 GEMM
+// Same roles and pipeline as moe_gemm_kernel; operands are E4M3 (K stage = 128
+// elements = one 128-byte swizzle row), each stage also brings the 512-byte
+// scale-factor atoms of A (128 rows x 4 K blocks) and B, which the MMA warp
+// copies into a per-stage TMEM slot with tcgen05.cp; the four K=32 MMAs of a
+// stage select their K block through the scale-factor id of the instruction
+// descriptor.
+struct MxCfg {
+    static constexpr uint32_t A_BYTES = kBM * kMxBK;
+    static constexpr uint32_t B_BYTES = kMxBN * kMxBK;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t SF_BYTES = 1024;  // A atom + B atom
+    static constexpr int STAGES = 5;
+    static constexpr uint32_t STAGING = kEpiWarps * kStageTileBytes;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t SF_TMEM = 2 * kMxBN;  // scale slots after the two accumulators, 8 columns a stage
+    static constexpr size_t SMEM = size_t(STAGES) * (STAGE_BYTES + SF_BYTES) + STAGING + 1024 + 256;
+};
+
+// instruction descriptor of kind::mxf8f6f4 with E4M3 A and B, UE8M0 scales, M = 128, N = 128
+template <bool B_MN>
+__device__ __forceinline__ uint32_t mx_idesc(uint32_t sf_id) {
+    return (sf_id << 4) | ((B_MN ? 1u : 0u) << 16) | (uint32_t(kMxBN >> 3) << 17) | (1u << 23) |
+           (uint32_t(kBM >> 4) << 24) | (sf_id << 29);
+}
+
+// shared-memory descriptor of a 32-row x 16-byte scale atom (no swizzle, 8-row groups 128 B apart)
+__device__ __forceinline__ uint64_t sf_smem_desc(uint32_t addr) {
+    return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t(128 >> 4) << 32) | (1ull << 46);
+}
+
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+template <int OP>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+    using C = MxCfg;
+    constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU);
+    constexpr int STAGES = C::STAGES;
+    constexpr int BN = kMxBN;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sf_smem = smem + STAGES * C::STAGE_BYTES;
+    float* staging = reinterpret_cast<float*>(sf_smem + STAGES * C::SF_BYTES);  // 1024-byte aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(staging) + C::STAGING);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB0);
+        if (OP == OP_FWD_GU || OP == OP_BWD_GU) tma_prefetch_map(&tmB1);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_tiles = (args.num_mtiles_dev ? *args.num_mtiles_dev : args.num_mtiles) * args.n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Tile t = decode_tile<OP>(tile, args);
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    uint8_t* sb = sa + C::A_BYTES;
+                    uint8_t* ssf = sf_smem + stage * C::SF_BYTES;
+                    uint64_t* bar = &full[stage];
+                    const int k0 = kb * kMxBK;
+                    mbar_arrive_expect_tx(bar, C::STAGE_BYTES + C::SF_BYTES);
+                    tma_load_2d(sa, &tmA, bar, k0, t.mt * kBM);
+                    if (OP == OP_FWD_GU) {
+                        tma_load_3d(sb, &tmB0, bar, k0, t.nt * (BN / 2), t.e);
+                        tma_load_3d(sb + (BN / 2) * kMxBK, &tmB1, bar, k0, t.nt * (BN / 2), t.e);
+                    } else if (OP == OP_FWD_DOWN) {
+                        tma_load_3d(sb, &tmB0, bar, k0, t.nt * BN, t.e);
+                    } else if (OP == OP_BWD_DOWN) {
+                        tma_load_3d(sb, &tmB0, bar, t.nt * BN, k0, t.e);
+                    } else {
+                        const bool up = k0 >= args.gate_up_split;
+                        tma_load_3d(sb, up ? &tmB1 : &tmB0, bar, t.nt * BN, up ? k0 - args.gate_up_split : k0, t.e);
+                    }
+                    bulk_load(ssf, args.sfa + (int64_t(t.mt) * args.sfa_kgroups + kb) * 512, 512, bar);
+                    bulk_load(ssf + 512,
+                              args.sfb + ((int64_t(t.e) * args.sfb_ntiles + t.nt) * args.sfb_kgroups + kb) * 512,
+                              512, bar);
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < STAGES; ++s)
+                    if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_parity >> s) & 1, args.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Tile t = decode_tile<OP>(tile, args);
+                const int buf = it & 1;
+                const uint32_t use = uint32_t(it >> 1);
+                ++it;
+                if (!mbar_wait(&tempty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+                    const uint32_t sf_addr = smem_u32(sf_smem + stage * C::SF_BYTES);
+                    const uint32_t sfa_t = tmem_base + C::SF_TMEM + uint32_t(stage * 8);
+                    const uint32_t sfb_t = sfa_t + 4;
+                    tmem_cp_sf(sfa_t, sf_smem_desc(sf_addr));
+                    tmem_cp_sf(sfb_t, sf_smem_desc(sf_addr + 512));
+#pragma unroll
+                    for (int kk = 0; kk < kMxBK / 32; ++kk) {
+                        const uint64_t ad = smem_desc(a_addr + kk * 32, 16, kSwizzleAtom);
+                        const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 32 * 128, 16384, kSwizzleAtom)
+                                                 : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
+                        mma_mx(d_tmem, ad, bd, mx_idesc<B_MN>(uint32_t(kk)), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) mma_commit(&tfull[buf]);
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, args.status);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        float* my_staging = staging + (warp - 2) * (kStageTileBytes / 4);
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const Tile t = decode_tile<OP>(tile, args);
+            const int buf = it & 1;
+            const uint32_t use = uint32_t(it >> 1);
+            ++it;
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(&tfull[buf], use & 1, abort_flag, args.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+            epilogue_tile<OP, BN, true>(t, t_row, q, half, args, my_staging, nullptr, nullptr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int OP>
+cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+    static bool attr_set = false;
+    auto kern = moe_gemm_mx_kernel<OP>;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(MxCfg::SMEM));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<grid, kGemmThreads, MxCfg::SMEM, st>>>(m.a, m.b0, m.b1, a);
+    count_launch();
+    return cudaGetLastError();
+}
+
 template <int OP, int BN>
 cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     static bool attr_set = false;
@@ -521,6 +803,17 @@ cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cu
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+    if (grid <= 0) return cudaSuccess;
+    switch (op) {
+        case OP_FWD_GU: return launch_mx_one<OP_FWD_GU>(m, a, grid, st);
+        case OP_FWD_DOWN: return launch_mx_one<OP_FWD_DOWN>(m, a, grid, st);
+        case OP_BWD_DOWN: return launch_mx_one<OP_BWD_DOWN>(m, a, grid, st);
+        case OP_BWD_GU: return launch_mx_one<OP_BWD_GU>(m, a, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 size_t gemm_smem_bytes(int bn) {
     return bn == 256 ? Cfg<256>::SMEM : (bn == 128 ? Cfg<128>::SMEM : Cfg<64>::SMEM);
@@ -572,7 +865,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                const uint32_t* box, bool fp32) {
+                const uint32_t* box, int type) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t d[3], s[2];
@@ -582,7 +875,10 @@ bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims
         b[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-    CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), d, s, b, es,
+    const CUtensorMapDataType dt = type == MAP_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : type == MAP_U8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = fn(m, dt, cuuint32_t(rank), const_cast<void*>(base), d, s, b, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

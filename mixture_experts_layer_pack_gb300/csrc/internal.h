@@ -57,6 +57,15 @@ struct GemmArgs {
     int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
     int inter;
     int* status;
+    // MXFP8 (block-scaled) GEMMs
+    uint8_t* q_out;             // E4M3 copy of the epilogue's GEMM-operand output (a, or [dg|du])
+    int64_t ld_q;
+    uint8_t* q_sf;              // its scale atoms (K blocks of 32 = q_kblocks)
+    int q_kblocks;
+    const uint8_t* sfa;         // A operand scale atoms [m tiles][K/128][512 B]
+    int sfa_kgroups;
+    const uint8_t* sfb;         // B operand scale atoms [E][n tiles][K/128][512 B]
+    int sfb_ntiles, sfb_kgroups;
 };
 
 struct GemmMaps {
@@ -64,15 +73,19 @@ struct GemmMaps {
     CUtensorMap c0, c1;  // OP_WGRAD: fp32 main_grad destinations (rows < m_split, rows >= m_split)
 };
 
-// tensor-map construction (driver entry point resolved at first use); bf16
-// elements unless fp32 is set, 128-byte swizzle
+// tensor-map construction (driver entry point resolved at first use), 128-byte swizzle
+enum MapType : int { MAP_BF16 = 0, MAP_F32 = 1, MAP_U8 = 2 };
 bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                const uint32_t* box, bool fp32 = false);
+                const uint32_t* box, int type = MAP_BF16);
 
 // picks the N tile (256, 128 or 64) for an output width
 int pick_bn(int64_t n, bool split_gate_up);
 
 cudaError_t launch_gemm(int op, int bn, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
+// block-scaled MXFP8 GEMM (N tile 128, K stage 128); ops FWD_GU, FWD_DOWN, BWD_DOWN, BWD_GU
+cudaError_t launch_gemm_mx(int op, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
+constexpr int kMxBN = 128;
+constexpr int kMxBK = 128;
 size_t gemm_smem_bytes(int bn);
 
 // routing
@@ -85,7 +98,10 @@ cudaError_t launch_route_scan(const int* counts, int E, int* offsets, int* offs_
                               cudaStream_t st);
 cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* counts,
                                const int* offs_pad, int T, int E, int k, const __nv_bfloat16* hidden, int H,
-                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, cudaStream_t st);
+                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, uint8_t* x_q,
+                               uint8_t* x_sf, cudaStream_t st);
+cudaError_t launch_swizzle_scales(int mode, const uint8_t* src0, const uint8_t* src1, int64_t src_es, int64_t src_rs,
+                                  int E, int n_tiles, int k_blocks, int kb_split, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* perm_src_pad, const int* counts,
                                   const int* offsets, const int* offs_pad, const int* mtile_expert, const int* meta,
                                   int T, int k, int max_rows, int32_t* perm_src_out, int32_t* row_of_out,
@@ -93,7 +109,7 @@ cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* 
 
 // elementwise / copy
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
-                               __nv_bfloat16* dst, int num_sms, cudaStream_t st);
+                               __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
                            __nv_bfloat16* out, int num_sms, cudaStream_t st);
 cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,

@@ -28,7 +28,8 @@ struct Shape {
     int64_t Tmax, H, E, k, I;
     int64_t rows;     // permuted rows incl. padding, worst case
     int bn_gu, bn_down, bn_bd, bn_bgu, bn_wfc1, bn_wd;
-    int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM)
+    int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM x epilogue halves)
+    bool mx;          // routed weights MXFP8: block-scaled fprop and dgrad GEMMs
 };
 
 // carves consecutive 256-byte aligned pieces out of one block
@@ -49,7 +50,9 @@ moe_status check_config(const moe_config* c, Shape* s) {
     if (c->max_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->topk <= 0 || c->inter <= 0)
         return MOE_ERR_INVALID_ARG;
     if (c->swiglu_limit != 0.0f) return MOE_ERR_UNSUPPORTED;
-    if (c->routed_wtype != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->routed_wtype != MOE_W_BF16 && c->routed_wtype != MOE_W_MXFP8) return MOE_ERR_UNSUPPORTED;
+    s->mx = c->routed_wtype == MOE_W_MXFP8;
+    if (s->mx && (c->hidden % 128 || c->inter % 128)) return MOE_ERR_UNSUPPORTED;
     if (c->num_experts > 1024 || c->topk > 32 || c->topk > c->num_experts) return MOE_ERR_UNSUPPORTED;
     if (c->hidden % 128 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
     s->Tmax = c->max_tokens;
@@ -67,7 +70,7 @@ moe_status check_config(const moe_config* c, Shape* s) {
     s->bn_wfc1 = pick_bn(s->H, false);
     s->bn_wd = pick_bn(s->I, false);
     if (!s->bn_gu || !s->bn_down || !s->bn_bd || !s->bn_bgu || !s->bn_wfc1 || !s->bn_wd) return MOE_ERR_UNSUPPORTED;
-    s->n_part = int(s->I / s->bn_bd) * kEpiHalves;
+    s->n_part = int(s->I / (s->mx ? kMxBN : s->bn_bd)) * kEpiHalves;
     return MOE_OK;
 }
 
@@ -77,6 +80,9 @@ struct Workspace {
     __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
     float *yx, *ys_dxs;  // forward: p*y (routed rows), y_shared; backward: dx (routed rows), dx_shared
     float* partial;
+    // MXFP8 only: quantised backward operands and the swizzled weight scales
+    uint8_t *go_q, *go_sf, *dgdu_q, *dgdu_sf;
+    uint8_t *sf_fc1_row, *sf_down_row, *sf_down_col, *sf_fc1_col;
 };
 
 struct SavedBufs {
@@ -84,7 +90,11 @@ struct SavedBufs {
     float *pp, *pp_perm;
     __nv_bfloat16 *x_perm, *a, *a_s;
     float *gu, *gu_s;
+    uint8_t *x_q, *x_sf, *a_q, *a_sf;  // MXFP8 only
 };
+
+// bytes of MXFP8 scale atoms for R rows (multiple of 128) and K columns (multiple of 128)
+size_t sf_atoms_bytes(int64_t rows, int64_t K) { return size_t(rows / 128) * size_t(K / 128) * 512; }
 
 size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     Carver c{base};
@@ -97,6 +107,19 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->partial = c.take<float>(size_t(s.rows) * s.n_part);
     w->ys_dxs = c.take<float>(size_t(s.Tmax) * s.H);
     w->dgdu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
+    if (s.mx) {
+        w->go_q = c.take<uint8_t>(size_t(s.rows) * s.H);
+        w->go_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
+        w->dgdu_q = c.take<uint8_t>(size_t(s.rows) * 2 * s.I);
+        w->dgdu_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, 2 * s.I));
+        w->sf_fc1_row = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(2 * s.I, s.H));
+        w->sf_down_row = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(s.H, s.I));
+        w->sf_down_col = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(s.I, s.H));
+        w->sf_fc1_col = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(s.H, 2 * s.I));
+    } else {
+        w->go_q = w->go_sf = w->dgdu_q = w->dgdu_sf = nullptr;
+        w->sf_fc1_row = w->sf_down_row = w->sf_down_col = w->sf_fc1_col = nullptr;
+    }
     return align_up(c.off, kAlign);
 }
 
@@ -118,6 +141,14 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->gu = c.take<float>(size_t(s.rows) * 2 * s.I);
     b->a_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
     b->gu_s = c.take<float>(size_t(s.Tmax) * 2 * s.I);
+    if (s.mx) {
+        b->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
+        b->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
+        b->a_q = c.take<uint8_t>(size_t(s.rows) * s.I);
+        b->a_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.I));
+    } else {
+        b->x_q = b->x_sf = b->a_q = b->a_sf = nullptr;
+    }
     return align_up(c.off, kAlign);
 }
 
@@ -131,11 +162,42 @@ bool check_view(const moe_wview& v, int64_t N, int64_t K, bool routed) {
     return true;
 }
 
+// an MXFP8 view of N rows x K columns per expert: E4M3 payloads (row stride in bytes), scales
+// indexed with the payload strides (see include/moe.h)
+bool check_mx_view(const moe_wview& v, int64_t N, int64_t K) {
+    if (!v.data || !v.col_data || !v.scale || !v.col_scale) return false;
+    if (!aligned16(v.data) || !aligned16(v.col_data)) return false;
+    if (v.row_stride < K || v.row_stride % 32 || v.expert_stride < N * v.row_stride || v.expert_stride % 32)
+        return false;
+    return true;
+}
+
 bool check_weights(const Shape& s, const moe_weights* w) {
     if (!w) return false;
-    return check_view(w->shared_gate, s.I, s.H, false) && check_view(w->shared_up, s.I, s.H, false) &&
-           check_view(w->shared_down, s.H, s.I, false) && check_view(w->routed_gate, s.I, s.H, true) &&
-           check_view(w->routed_up, s.I, s.H, true) && check_view(w->routed_down, s.H, s.I, true);
+    const bool shared = check_view(w->shared_gate, s.I, s.H, false) && check_view(w->shared_up, s.I, s.H, false) &&
+                        check_view(w->shared_down, s.H, s.I, false);
+    if (s.mx)
+        return shared && check_mx_view(w->routed_gate, s.I, s.H) && check_mx_view(w->routed_up, s.I, s.H) &&
+               check_mx_view(w->routed_down, s.H, s.I);
+    return shared && check_view(w->routed_gate, s.I, s.H, true) && check_view(w->routed_up, s.I, s.H, true) &&
+           check_view(w->routed_down, s.H, s.I, true);
+}
+
+// 2D K-major E4M3 operand: rows x K bytes, box 128 x 128 rows
+bool map_u8_kmajor(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t ld) {
+    const uint64_t dims[2] = {uint64_t(K), uint64_t(rows)};
+    const uint64_t strides[1] = {uint64_t(ld)};
+    const uint32_t box[2] = {128, uint32_t(kBM)};
+    return encode_map(m, base, 2, dims, strides, box, MAP_U8);
+}
+
+// 3D E4M3 weight view [E][rows][cols] (strides in bytes), box (128 cols, box_rows rows, 1 expert)
+bool map_u8_weight(CUtensorMap* m, const void* data, const moe_wview& v, int64_t E, int64_t rows, int64_t cols,
+                   uint32_t box_rows) {
+    const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(E)};
+    const uint64_t strides[2] = {uint64_t(v.row_stride), uint64_t(v.expert_stride)};
+    const uint32_t box[3] = {128, box_rows, 1};
+    return encode_map(m, data, 3, dims, strides, box, MAP_U8);
 }
 
 bool check_mg(const moe_main_grads* m) {
@@ -172,7 +234,7 @@ bool map_main_grad(CUtensorMap* m, float* base, int64_t E, int64_t rows, int64_t
     const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(E)};
     const uint64_t strides[2] = {uint64_t(rs) * 4, uint64_t(es) * 4};
     const uint32_t box[3] = {32, 32, 1};
-    return encode_map(m, base, 3, dims, strides, box, true);
+    return encode_map(m, base, 3, dims, strides, box, MAP_F32);
 }
 
 // 3D weight view [E][rows][cols] with a box of (64 cols, box_rows rows, 1 expert)
@@ -205,6 +267,7 @@ struct moe_handle {
     Workspace ws;
     int device;
     int sms;
+    bool weights_prepared = false;  // MXFP8: moe_prepare_weights has run
     // per-kernel timing (moe_profile_enable)
     bool profiling = false;
     struct Rec {
@@ -369,6 +432,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!hidden || !probs || !routing_map || !out || !aligned16(hidden) || !aligned16(out)))
         return MOE_ERR_INVALID_ARG;
+    const bool mx = s.mx;
+    if (mx && !h->weights_prepared) return MOE_ERR_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const SavedBufs& b = saved->b;
     const Workspace& ws = h->ws;
@@ -390,10 +455,38 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
     MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, b.counts, b.offs_pad, Ti, E, k,
                               static_cast<const __nv_bfloat16*>(hidden), H, b.perm_src, b.pp_perm, b.row_of, b.x_perm,
-                              st)); }
+                              mx ? b.x_q : nullptr, mx ? b.x_sf : nullptr, st)); }
 
     GemmMaps m;
     // routed gate/up + SwiGLU
+    if (mx) {
+        GemmArgs a = base_args(ws.status, I);
+        if (!map_u8_kmajor(&m.a, b.x_q, rows, H, H) ||
+            !map_u8_weight(&m.b0, w->routed_gate.data, w->routed_gate, E, I, H, kMxBN / 2) ||
+            !map_u8_weight(&m.b1, w->routed_up.data, w->routed_up, E, I, H, kMxBN / 2))
+            return MOE_ERR_INVALID_ARG;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = 2 * I / kMxBN;
+        a.k_blocks = H / kMxBK;
+        a.gate_up_split = I;
+        a.out0 = b.a;
+        a.ld_out0 = I;
+        a.outf = b.gu;
+        a.ld_outf = 2 * I;
+        a.q_out = b.a_q;
+        a.ld_q = I;
+        a.q_sf = b.a_sf;
+        a.q_kblocks = I / 32;
+        a.sfa = b.x_sf;
+        a.sfa_kgroups = H / 128;
+        a.sfb = ws.sf_fc1_row;
+        a.sfb_ntiles = 2 * I / 128;
+        a.sfb_kgroups = H / 128;
+        Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
+        MOE_CU(launch_gemm_mx(OP_FWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    } else
     {
         GemmArgs a = base_args(ws.status, I);
         const int bn = s.bn_gu;
@@ -433,6 +526,28 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // routed down projection, scaled by the route's prob
+    if (mx) {
+        GemmArgs a = base_args(ws.status, I);
+        if (!map_u8_kmajor(&m.a, b.a_q, rows, I, I) ||
+            !map_u8_weight(&m.b0, w->routed_down.data, w->routed_down, E, H, I, kMxBN))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = H / kMxBN;
+        a.k_blocks = I / kMxBK;
+        a.row_scale = b.pp_perm;
+        a.outf = ws.yx;
+        a.ld_outf = H;
+        a.sfa = b.a_sf;
+        a.sfa_kgroups = I / 128;
+        a.sfb = ws.sf_down_row;
+        a.sfb_ntiles = H / 128;
+        a.sfb_kgroups = I / 128;
+        Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
+        MOE_CU(launch_gemm_mx(OP_FWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    } else
     {
         GemmArgs a = base_args(ws.status, I);
         const int bn = s.bn_down;
@@ -481,6 +596,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     const int64_t T = saved->T;
     if (T == 0) return MOE_OK;
     if (!grad_out || !dhidden || !dprobs || !aligned16(grad_out) || !aligned16(dhidden)) return MOE_ERR_INVALID_ARG;
+    const bool mx = s.mx;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const SavedBufs& b = saved->b;
     const Workspace& ws = h->ws;
@@ -490,10 +606,44 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(grad_out);
 
     { Timed tm_(h, MOE_K_GATHER, st);
-    MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, h->sms, st)); }
+    MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, mx ? ws.go_q : nullptr,
+                              mx ? ws.go_sf : nullptr, h->sms, st)); }
 
     GemmMaps m;
     // routed dgrad through the down projection + SwiGLU backward + dprob partials
+    if (mx) {
+        GemmArgs a = base_args(ws.status, I);
+        if (!map_u8_kmajor(&m.a, ws.go_q, rows, H, H) ||
+            !map_u8_weight(&m.b0, w->routed_down.col_data, w->routed_down, E, H, I, 128))
+            return MOE_ERR_INVALID_ARG;
+        m.b1 = m.b0;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = I / kMxBN;
+        a.k_blocks = H / kMxBK;
+        a.in0 = b.a;
+        a.ld_in0 = I;
+        a.inf = b.gu;
+        a.ld_inf = 2 * I;
+        a.row_scale = b.pp_perm;
+        a.partial = ws.partial;
+        a.out0 = ws.dgdu;
+        a.ld_out0 = 2 * I;
+        a.out1 = ws.ap;
+        a.ld_out1 = I;
+        a.q_out = ws.dgdu_q;
+        a.ld_q = 2 * I;
+        a.q_sf = ws.dgdu_sf;
+        a.q_kblocks = 2 * I / 32;
+        a.sfa = ws.go_sf;
+        a.sfa_kgroups = H / 128;
+        a.sfb = ws.sf_down_col;
+        a.sfb_ntiles = I / 128;
+        a.sfb_kgroups = H / 128;
+        Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
+        MOE_CU(launch_gemm_mx(OP_BWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    } else
     {
         GemmArgs a = base_args(ws.status, I);
         const int bn = s.bn_bd;
@@ -539,6 +689,28 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // routed dgrad through gate/up
+    if (mx) {
+        GemmArgs a = base_args(ws.status, I);
+        if (!map_u8_kmajor(&m.a, ws.dgdu_q, rows, 2 * I, 2 * I) ||
+            !map_u8_weight(&m.b0, w->routed_gate.col_data, w->routed_gate, E, I, H, 128) ||
+            !map_u8_weight(&m.b1, w->routed_up.col_data, w->routed_up, E, I, H, 128))
+            return MOE_ERR_INVALID_ARG;
+        a.mtile_expert = b.mtile_expert;
+        a.num_mtiles_dev = b.meta;
+        a.num_mtiles = rows / kBM;
+        a.n_tiles = H / kMxBN;
+        a.k_blocks = 2 * I / kMxBK;
+        a.gate_up_split = I;
+        a.outf = ws.yx;
+        a.ld_outf = H;
+        a.sfa = ws.dgdu_sf;
+        a.sfa_kgroups = 2 * I / 128;
+        a.sfb = ws.sf_fc1_col;
+        a.sfb_ntiles = H / 128;
+        a.sfb_kgroups = 2 * I / 128;
+        Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
+        MOE_CU(launch_gemm_mx(OP_BWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+    } else
     {
         GemmArgs a = base_args(ws.status, I);
         const int bn = s.bn_bgu;
@@ -645,6 +817,28 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     Timed tm_(h, MOE_K_UNPERMUTE, st);
     MOE_CU(launch_unpermute(ws.ys_dxs, ws.yx, b.row_of, b.ids, ws.partial, s.n_part, Ti, H, k, E,
                             static_cast<__nv_bfloat16*>(dhidden), dprobs, h->sms, st));
+    return MOE_OK;
+}
+
+moe_status moe_prepare_weights(moe_handle* h, const moe_weights* w, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    const Shape& s = h->s;
+    if (!s.mx) return MOE_OK;
+    if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
+    const moe_wview &g = w->routed_gate, &u = w->routed_up, &d = w->routed_down;
+    if (g.expert_stride != u.expert_stride || g.row_stride != u.row_stride) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int E = int(s.E), H = int(s.H), I = int(s.I);
+    const Workspace& ws = h->ws;
+    MOE_CU(launch_swizzle_scales(1 /*rows, gate|up tiles*/, g.scale, u.scale, g.expert_stride / 32, g.row_stride / 32,
+                                 E, 2 * I / 128, H / 32, 0, ws.sf_fc1_row, st));
+    MOE_CU(launch_swizzle_scales(0 /*rows*/, d.scale, nullptr, d.expert_stride / 32, d.row_stride / 32, E, H / 128,
+                                 I / 32, 0, ws.sf_down_row, st));
+    MOE_CU(launch_swizzle_scales(2 /*columns*/, d.col_scale, nullptr, d.expert_stride / 32, d.row_stride, E, I / 128,
+                                 H / 32, 0, ws.sf_down_col, st));
+    MOE_CU(launch_swizzle_scales(3 /*columns, gate then up*/, g.col_scale, u.col_scale, g.expert_stride / 32,
+                                 g.row_stride, E, H / 128, 2 * I / 32, I / 32, ws.sf_fc1_col, st));
+    h->weights_prepared = true;
     return MOE_OK;
 }
 

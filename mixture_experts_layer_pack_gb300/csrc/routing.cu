@@ -170,12 +170,15 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
     }
 }
 
-// items [0, T*k): routes; items [T*k, T*k + E*128): padding rows (expert j/128, row j%128)
+// items [0, T*k): routes; items [T*k, T*k + E*128): padding rows (expert j/128, row j%128).
+// With x_q set, the copied row is also quantised to MXFP8 along H (the routed
+// gate/up GEMM's operand): E4M3 codes to x_q, scales to x_sf in the MMA's
+// scale-factor layout.
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     const int* __restrict__ ids, const float* __restrict__ pp, const int* __restrict__ rank,
     const int* __restrict__ counts, const int* __restrict__ offs_pad, int T, int E, int k,
     const uint4* __restrict__ hidden, int vec_per_row, int* __restrict__ perm_src, float* __restrict__ pp_perm,
-    int* __restrict__ row_of, uint4* __restrict__ x_perm) {
+    int* __restrict__ row_of, uint4* __restrict__ x_perm, uint8_t* __restrict__ x_q, uint8_t* __restrict__ x_sf) {
     const int64_t item = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int64_t n_routes = int64_t(T) * k;
@@ -191,7 +194,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         }
         const uint4* src = hidden + int64_t(t) * vec_per_row;
         uint4* dst = x_perm + int64_t(pos) * vec_per_row;
-        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+        if (x_q)
+            copy_quant_row(src, dst, x_q, x_sf, pos, vec_per_row);
+        else
+            for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
         return;
     }
     const int64_t j = item - n_routes;
@@ -207,7 +213,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         pp_perm[pos] = 0.0f;
     }
     uint4* dst = x_perm + int64_t(pos) * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    if (x_q)
+        copy_quant_row(nullptr, dst, x_q, x_sf, pos, vec_per_row);
+    else
+        for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
 }
 
 __global__ void export_routing_kernel(const int* __restrict__ ids, const int* __restrict__ row_of,
@@ -263,12 +272,13 @@ cudaError_t launch_route_scan(const int* counts, int E, int* offsets, int* offs_
 
 cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* counts,
                                const int* offs_pad, int T, int E, int k, const __nv_bfloat16* hidden, int H,
-                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, cudaStream_t st) {
+                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, uint8_t* x_q,
+                               uint8_t* x_sf, cudaStream_t st) {
     const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     route_place_kernel<<<unsigned(blocks), 32 * kWarpsPerBlock, 0, st>>>(
         ids, pp, rank, counts, offs_pad, T, E, k, reinterpret_cast<const uint4*>(hidden), H / 8, perm_src, pp_perm,
-        row_of, reinterpret_cast<uint4*>(x_perm));
+        row_of, reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
     count_launch();
     return cudaGetLastError();
 }

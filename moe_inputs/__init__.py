@@ -14,7 +14,10 @@ precision):
   and a bool ``routing_map[T,E]``; no renormalisation;
 * dense tensors: a seeded ``torch.Generator`` on the target device; fp32 draws
   RNE-cast to bf16 (weights ~ N(0,0.02), hidden ~ N(0,1), grad_out ~ N(0,1));
-  main_grad ~ N(0,1e-3) fp32.
+  main_grad ~ N(0,1e-3) fp32;
+* MXFP8 routed weights are input data too (the framework that owns the
+  weights quantises them): made from the bf16 masters with PyTorch's
+  float8_e4m3fn cast, rowwise and columnwise, OCP MX block rule.
 """
 from __future__ import annotations
 
@@ -167,3 +170,49 @@ def make_main_grads(H: int, I: int, E: int, seed: int, device="cpu", std: float 
         shared_fc1=draw(2 * I, H), shared_fc2=draw(H, I),
         routed_fc1=draw(E, 2 * I, H), routed_fc2=draw(E, H, I),
     )
+
+
+def mxfp8_quantize_torch(w, axis):
+    """MXFP8 input weights from bf16 masters with PyTorch ops (float8_e4m3fn cast):
+    blocks of 32 along ``axis`` (-1: along K, the row; -2: down the rows),
+    E8M0 code = floor(log2 amax) - 8 + 127 clamped to [0, 254] (0 for an all-zero
+    block), elements = x / 2^(code-127) clamped to +-448 and cast (round to nearest
+    even). Returns (payload uint8 with w's shape, scale codes uint8)."""
+    torch = _torch()
+    x = w.float()
+    if axis == -2:
+        x = x.transpose(-1, -2)
+    shp = x.shape
+    blocks = x.reshape(*shp[:-1], shp[-1] // 32, 32)
+    amax = blocks.abs().amax(dim=-1)
+    _, ex = torch.frexp(amax)                                  # amax = m 2^ex, m in [0.5, 1)
+    code = torch.clamp(ex - 1 - 8 + 127, 0, 254)
+    code = torch.where(amax > 0, code, torch.zeros_like(code))
+    scaled = blocks * torch.exp2(127.0 - code.float()).unsqueeze(-1)
+    payload = torch.clamp(scaled, -448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).reshape(shp)
+    code = code.to(torch.uint8)
+    if axis == -2:
+        payload = payload.transpose(-1, -2).contiguous()
+        code = code.transpose(-1, -2).contiguous()
+    return payload.contiguous(), code.contiguous()
+
+
+def make_mxfp8_weights(w: dict) -> dict:
+    """MXFP8 copies of the routed weights (combined FC1 [E,2I,H], FC2 [E,H,I]):
+    rowwise payload + scales [E,N,K/32] for forward, columnwise payload +
+    scales [E,N/32,K] for dgrad. FC1 is quantised as its gate and up halves
+    separately, so no 32-row block of the columnwise copy spans both."""
+    torch = _torch()
+    out = {}
+    E, two_i, H = w["routed_fc1"].shape
+    inter = two_i // 2
+    for name, t in (("routed_fc1", w["routed_fc1"]), ("routed_fc2", w["routed_fc2"])):
+        q, s = mxfp8_quantize_torch(t, -1)
+        if name == "routed_fc1":
+            qcs = [mxfp8_quantize_torch(t[:, h * inter:(h + 1) * inter], -2) for h in range(2)]
+            qc = torch.cat([qcs[0][0], qcs[1][0]], dim=1)
+            sc = torch.cat([qcs[0][1], qcs[1][1]], dim=1)
+        else:
+            qc, sc = mxfp8_quantize_torch(t, -2)
+        out[name] = (q, s, qc, sc)
+    return out

@@ -41,11 +41,16 @@ precision). ``precision="exact"`` is the plain definition in fp64.
 activation a between the two projections, the SwiGLU gradients dg and du,
 and the prob-weighted activation p*a that multiplies grad_out in the down
 projection's weight gradient -- and accumulates in fp64. Inputs (hidden,
-grad_out, weights) are bf16 already.
+grad_out, weights) are bf16 already. ``precision="mxfp8"`` (MXFP8 routed
+experts, same pages) quantises the routed experts' forward and dgrad GEMM
+operands to MXFP8 in blocks of 32 along each GEMM's K -- x and a in forward,
+grad_out and [dg|du] in dgrad -- with the weights given dequantised
+(rowwise for forward, columnwise for dgrad through ``routed_dgrad``); the
+weight-gradient GEMMs and the shared expert keep bf16 operands.
 
 A bf16 rounding is a discrete decision taken on a value the kernel evaluates
 in fp32 (FP32 accumulator), so near a rounding midpoint both neighbours are
-correct results. ``envelope`` (bf16 mode) bounds, per output element, how far
+correct results. ``envelope`` (bf16 and mxfp8 modes) bounds, per output element, how far
 the other valid roundings of every operand that lies within the fp32
 evaluation band of a midpoint can move the result (propagated with absolute
 values); elsewhere it is 0.
@@ -88,6 +93,10 @@ class DenseWeights:
 
     def routed(self, e):
         return self.rg[e], self.ru[e], self.rd[e]
+
+    def routed_dgrad(self, e):
+        """Weights the dgrad GEMMs see (MXFP8: the columnwise-quantised copy)."""
+        return self.routed(e)
 
 
 # --------------------------------------------------------------------------
@@ -173,9 +182,44 @@ ELEMENTWISE_BAND = 2.0 ** -20   # relative band of fp32 elementwise evaluation (
 def _rounder(precision):
     if precision == "exact":
         return lambda v: v
-    if precision == "bf16":
+    if precision in ("bf16", "mxfp8"):
         return bf16_round
     raise ValueError(precision)
+
+
+def mxfp8_round(v):
+    """Value of v after MXFP8 quantisation in blocks of 32 along the last axis."""
+    from oracle import mxfp8
+    q, sc = mxfp8.quantize(v, axis=-1)
+    return mxfp8.dequantize(q, sc, axis=-1)
+
+
+class Operands:
+    """Where one expert's GEMM operands are rounded: identity (exact), bf16, or,
+    for routed experts in mxfp8 mode, MXFP8 along K for the forward and dgrad
+    GEMMs (bf16 for the weight-gradient GEMMs)."""
+
+    def __init__(self, precision, routed=True):
+        self.rnd = _rounder(precision)
+        self.mx = precision == "mxfp8" and routed
+
+    def x(self, x):                       # gate/up projection input, K = H
+        return mxfp8_round(x) if self.mx else x
+
+    def a(self, a):                       # down projection input, K = I
+        return mxfp8_round(a) if self.mx else self.rnd(a)
+
+    def go(self, go):                     # dgrad through the down projection, K = H
+        return mxfp8_round(go) if self.mx else go
+
+    def dgdu(self, dg, du):               # dgrad through gate/up, K = 2I
+        if self.mx:
+            q = mxfp8_round(np.concatenate([dg, du], axis=1))
+            return q[:, :dg.shape[1]], q[:, dg.shape[1]:]
+        return self.rnd(dg), self.rnd(du)
+
+    def wgrad(self, v):                   # weight-gradient operands
+        return self.rnd(v)
 
 
 # --------------------------------------------------------------------------
@@ -194,24 +238,34 @@ def silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def expert_forward(x, Wg, Wu, Wd, rnd=lambda v: v):
+def expert_forward(x, Wg, Wu, Wd, ops=None):
     """SwiGLU expert on rows x[n,H]: g = x Wg^T, u = x Wu^T, a = silu(g) u, y = a Wd^T
-    (``rnd`` holds a, the down projection's operand, at the GEMM precision)."""
-    g = x @ Wg.T
-    u = x @ Wu.T
-    a = rnd(silu(g) * u)
+    (``ops`` holds the GEMM operands x and a at the GEMM precision)."""
+    ops = ops or Operands("exact")
+    xq = ops.x(x)
+    g = xq @ Wg.T
+    u = xq @ Wu.T
+    a = ops.a(silu(g) * u)
     y = a @ Wd.T
     return g, u, a, y
 
 
-def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, rnd=lambda v: v):
-    """Gradients of sum(go * (p y)) for one expert, p[n] the rows' probs:
-    returns dx, dWg, dWu, dWd (``rnd`` holds dg, du and p*a at the GEMM precision)."""
-    da = p[:, None] * (go @ Wd)
-    dg = rnd(da * u * silu_grad(g))
-    du = rnd(da * silu(g))
-    dx = dg @ Wg + du @ Wu
-    return dx, dg.T @ x, du.T @ x, go.T @ rnd(p[:, None] * a)
+def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, ops=None):
+    """Gradients of sum(go * (p y)) for one expert, p[n] the rows' probs, with the
+    dgrad weights Wg, Wu, Wd: returns dx, dWg, dWu, dWd and dprob[n] =
+    sum_i a_i (go Wd)_i (= <go, y> in exact arithmetic). ``ops`` holds every
+    GEMM operand (go, [dg|du], and the weight-gradient operands dg, du, p*a)
+    at its GEMM's precision."""
+    ops = ops or Operands("exact")
+    da_u = ops.go(go) @ Wd
+    da = p[:, None] * da_u
+    dg = da * u * silu_grad(g)
+    du = da * silu(g)
+    dgq, duq = ops.dgdu(dg, du)
+    dx = dgq @ Wg + duq @ Wu
+    dgw, duw = ops.wgrad(dg), ops.wgrad(du)
+    dprob = np.sum(a * da_u, axis=1)
+    return dx, dgw.T @ x, duw.T @ x, go.T @ ops.wgrad(p[:, None] * a), dprob
 
 
 # --------------------------------------------------------------------------
@@ -223,7 +277,7 @@ def forward(hidden, probs, routing_map, W, k, precision="exact"):
     "core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward, and PR
     #6572 Summary (dispatch, routed and shared experts, combine). Returns
     (out, cache); the cache feeds ``backward``."""
-    rnd = _rounder(precision)
+    shared_ops, routed_ops = Operands(precision, routed=False), Operands(precision)
     x = np.asarray(hidden, np.float64)
     T, H = x.shape
     ids, pp, over = route_pack(routing_map, probs, k)
@@ -232,7 +286,7 @@ def forward(hidden, probs, routing_map, W, k, precision="exact"):
     E = W.num_experts
     counts, offsets, perm_src, perm_slot, row_of = dispatch_indices(ids, E)
 
-    gs, us, as_, ys = expert_forward(x, *W.shared(), rnd=rnd)
+    gs, us, as_, ys = expert_forward(x, *W.shared(), ops=shared_ops)
 
     R = perm_src.size
     y = np.zeros((R, H))
@@ -242,7 +296,7 @@ def forward(hidden, probs, routing_map, W, k, precision="exact"):
         if hi == lo:
             continue
         xe = x[perm_src[lo:hi]]
-        g, u, a, ye = expert_forward(xe, *W.routed(e), rnd=rnd)
+        g, u, a, ye = expert_forward(xe, *W.routed(e), ops=routed_ops)
         y[lo:hi] = ye
         routed[e] = (g, u, a)
 
@@ -265,15 +319,15 @@ def backward(grad_out, cache, W):
     backward adapter) and the six weight gradients {shared_gate, shared_up,
     shared_down} plus {e: (dWg, dWu, dWd)} for every expert with tokens.
     "core.transformer.moe.megakernel.mok.runtime", _MoKAutograd.backward."""
-    rnd = _rounder(cache["precision"])
+    shared_ops, routed_ops = Operands(cache["precision"], routed=False), Operands(cache["precision"])
     go = np.asarray(grad_out, np.float64)
     x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
-    offsets, perm_src, perm_slot, y = cache["offsets"], cache["perm_src"], cache["perm_slot"], cache["y"]
+    offsets, perm_src, perm_slot = cache["offsets"], cache["perm_src"], cache["perm_slot"]
     T, H = x.shape
     E = W.num_experts
 
     gs, us, as_ = cache["shared"]
-    dx_s, dWsg, dWsu, dWsd = expert_backward(x, go, np.ones(T), gs, us, as_, *W.shared(), rnd=rnd)
+    dx_s, dWsg, dWsu, dWsd, _ = expert_backward(x, go, np.ones(T), gs, us, as_, *W.shared(), ops=shared_ops)
 
     R = perm_src.size
     dx_perm = np.zeros((R, H))
@@ -283,9 +337,8 @@ def backward(grad_out, cache, W):
     for e, (g, u, a) in cache["routed"].items():
         lo, hi = offsets[e], offsets[e + 1]
         go_e = go[perm_src[lo:hi]]
-        dprob_perm[lo:hi] = np.sum(go_e * y[lo:hi], axis=1)
-        dx, dWg, dWu, dWd = expert_backward(x[perm_src[lo:hi]], go_e, pp_perm[lo:hi], g, u, a, *W.routed(e),
-                                            rnd=rnd)
+        dx, dWg, dWu, dWd, dprob_perm[lo:hi] = expert_backward(x[perm_src[lo:hi]], go_e, pp_perm[lo:hi], g, u, a,
+                                                              *W.routed_dgrad(e), ops=routed_ops)
         dx_perm[lo:hi] = dx
         routed_grads[e] = (dWg, dWu, dWd)
 
@@ -322,32 +375,73 @@ def silu_grad2_bound():
     return 0.5
 
 
-def _expert_envelope(x, go, p, g, u, Wg, Wu, Wd):
-    """Envelopes (bf16 mode) of one expert's results for rows x[n,H] with probs p[n]:
-    returns env_y [n,H], env_dx [n,H], env_dWg [I,H], env_dWu [I,H], env_dWd [H,I]
-    and the a-envelope alt_a [n,I]."""
+def mxfp8_alternative(v, band):
+    """mxfp8 mode: per element of v (blocks of 32 along the last axis), the
+    distance to the other valid quantised value where v lies within ``band``
+    of an E4M3 rounding midpoint (in value units), and, for every element of a
+    block whose amax lies within its band of a power of two (the shared
+    exponent may go either way), a bound on the change a coarser scale makes."""
+    from oracle import mxfp8
+    v = np.asarray(v, np.float64)
+    band = np.broadcast_to(np.asarray(band, np.float64), v.shape)
+    shp = v.shape
+    vb = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    bb = band.reshape(vb.shape)
+    amax = np.max(np.abs(vb), axis=-1)
+    scale = mxfp8.e8m0_value(mxfp8.e8m0_scale_code(amax))[..., None]
+    y = np.minimum(np.abs(vb) / scale, mxfp8.E4M3_MAX)
+    grid = mxfp8._POS_VALUES
+    hi = np.clip(np.searchsorted(grid, y), 1, grid.size - 1)
+    lo = hi - 1
+    mid = (grid[lo] + grid[hi]) / 2
+    spacing = grid[hi] - grid[lo]
+    alt = np.where(np.abs(y - mid) * scale <= bb, spacing * scale, 0.0)
+    # shared exponent at a power-of-two boundary of amax
+    _, ex = np.frexp(amax)
+    edge = np.ldexp(0.5, ex)                   # the power of two at or below amax
+    bband = np.max(bb, axis=-1)
+    near = (np.abs(amax - edge) <= bband) | (np.abs(amax - 2 * edge) <= bband)
+    alt = np.where(near[..., None], np.maximum(alt, np.abs(vb) / 8 + 2 * scale * 2.0 ** -9), alt)
+    return alt.reshape(shp)
+
+
+def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed):
+    """Envelopes of one expert's results for rows x[n,H] with probs p[n]. Wf are
+    the forward weights (Wg, Wu, Wd), Wb the dgrad weights. Returns env_y [n,H],
+    env_dx [n,H], env_dWg [I,H], env_dWu [I,H], env_dWd [H,I], env_dprob [n]."""
+    ops = Operands(precision, routed)
+    Wg, Wu, Wd = Wf
+    Bg, Bu, Bd = Wb
+    xq = ops.x(x)
     H = x.shape[1]
     I = g.shape[1]
-    dg_band = fp32_dot_band((x * x) @ (Wg * Wg).T, H)          # |g_fp32 - g|
-    du_band = fp32_dot_band((x * x) @ (Wu * Wu).T, H)
+    dg_band = fp32_dot_band((xq * xq) @ (Wg * Wg).T, H)          # |g_fp32 - g|
+    du_band = fp32_dot_band((xq * xq) @ (Wu * Wu).T, H)
     s1 = silu_grad(g)
     a_val = silu(g) * u
     band_a = np.abs(s1 * u) * dg_band + np.abs(silu(g)) * du_band + ELEMENTWISE_BAND * np.abs(a_val)
-    alt_a = bf16_alternative(a_val, band_a)
+    alt_a = mxfp8_alternative(a_val, band_a) if ops.mx else bf16_alternative(a_val, band_a)
     env_y = alt_a @ np.abs(Wd).T
-    a_b = bf16_round(a_val)
+    a_b = ops.a(a_val)
 
-    da_u = go @ Wd
+    goq = ops.go(go)
+    da_u = goq @ Bd
+    env_dprob = np.sum(alt_a * np.abs(da_u), axis=1)
     da = p[:, None] * da_u
-    dda = np.abs(p)[:, None] * fp32_dot_band((go * go) @ (Wd * Wd), H)
+    dda = np.abs(p)[:, None] * fp32_dot_band((goq * goq) @ (Bd * Bd), H)
     dg_val = da * u * s1
     du_val = da * silu(g)
     band_dg = (np.abs(u * s1) * dda + np.abs(da * s1) * du_band +
                np.abs(da * u) * silu_grad2_bound() * dg_band + ELEMENTWISE_BAND * np.abs(dg_val))
     band_du = np.abs(silu(g)) * dda + np.abs(da * s1) * dg_band + ELEMENTWISE_BAND * np.abs(du_val)
-    alt_dg = bf16_alternative(dg_val, band_dg)
+    alt_dg = bf16_alternative(dg_val, band_dg)            # weight-gradient operands (bf16)
     alt_du = bf16_alternative(du_val, band_du)
-    env_dx = alt_dg @ np.abs(Wg) + alt_du @ np.abs(Wu)
+    if ops.mx:                                            # dgrad operand [dg|du] (MXFP8)
+        alt_q = mxfp8_alternative(np.concatenate([dg_val, du_val], axis=1),
+                                  np.concatenate([band_dg, band_du], axis=1))
+        env_dx = alt_q[:, :I] @ np.abs(Bg) + alt_q[:, I:] @ np.abs(Bu)
+    else:
+        env_dx = alt_dg @ np.abs(Bg) + alt_du @ np.abs(Bu)
     env_dWg = alt_dg.T @ np.abs(x)
     env_dWu = alt_du.T @ np.abs(x)
 
@@ -355,28 +449,32 @@ def _expert_envelope(x, go, p, g, u, Wg, Wu, Wd):
     alt_pa = bf16_alternative(pa_val, 2 * U32 * np.abs(pa_val))
     alt_pa = alt_pa + np.where(alt_a > 0, np.abs(p)[:, None] * alt_a + np.ldexp(1.0, np.frexp(pa_val)[1] - 8), 0.0)
     env_dWd = np.abs(go).T @ alt_pa
-    return env_y, env_dx, env_dWg, env_dWu, env_dWd, alt_a
+    return env_y, env_dx, env_dWg, env_dWu, env_dWd, env_dprob
 
 
 def envelope(grad_out, cache, W):
     """Per-element envelopes of out, dhidden, dprobs and the six weight
-    gradients for a bf16-mode forward/backward (see the module notes)."""
+    gradients for a bf16- or mxfp8-mode forward/backward (see the module notes)."""
     go = np.asarray(grad_out, np.float64)
+    prec = cache["precision"]
     x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
     offsets, perm_src, perm_slot = cache["offsets"], cache["perm_src"], cache["perm_slot"]
     T, H = x.shape
     E = W.num_experts
     gs, us, _ = cache["shared"]
-    ey_s, edx_s, eg_s, eu_s, ed_s, _ = _expert_envelope(x, go, np.ones(T), gs, us, *W.shared())
+    ey_s, edx_s, eg_s, eu_s, ed_s, _ = _expert_envelope(x, go, np.ones(T), gs, us, W.shared(), W.shared(), prec,
+                                                        routed=False)
     R = perm_src.size
     ey = np.zeros((R, H))
     edx = np.zeros((R, H))
+    edp = np.zeros(R)
     pp_perm = pp[perm_src, perm_slot] if R else np.zeros(0)
     routed = {}
     for e, (g, u, _) in cache["routed"].items():
         lo, hi = offsets[e], offsets[e + 1]
-        ey[lo:hi], edx[lo:hi], eg, eu, ed, _ = _expert_envelope(x[perm_src[lo:hi]], go[perm_src[lo:hi]],
-                                                              pp_perm[lo:hi], g, u, *W.routed(e))
+        ey[lo:hi], edx[lo:hi], eg, eu, ed, edp[lo:hi] = _expert_envelope(
+            x[perm_src[lo:hi]], go[perm_src[lo:hi]], pp_perm[lo:hi], g, u, W.routed(e), W.routed_dgrad(e), prec,
+            routed=True)
         routed[e] = (eg, eu, ed)
     env_out = ey_s.copy()
     env_dh = edx_s.copy()
@@ -386,6 +484,6 @@ def envelope(grad_out, cache, W):
         r = row_of[v, s]
         env_out[v] += np.abs(pp[v, s, None]) * ey[r]
         env_dh[v] += edx[r]
-        env_dp[np.flatnonzero(v), ids[v, s]] = np.sum(np.abs(go[v]) * ey[r], axis=1)
+        env_dp[np.flatnonzero(v), ids[v, s]] = edp[r]
     return dict(out=env_out, dhidden=env_dh, dprobs=env_dp, shared_gate=eg_s, shared_up=eu_s,
                 shared_down=ed_s, routed=routed)

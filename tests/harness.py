@@ -22,11 +22,13 @@ class Case:
     seed: int
     routing: str = "topk"
     drop: str = "none"
+    mx: bool = False      # MXFP8 routed weights
 
 
 def config_case(cfg_id: int, T: int | None = None, variant: str | None = None) -> Case:
     c = MI.CONFIGS[cfg_id]
-    return Case(T or c["T"], c["H"], c["E"], c["k"], c["I"], MI.seed_of(cfg_id), variant or c["routing"], c["drop"])
+    return Case(T or c["T"], c["H"], c["E"], c["k"], c["I"], MI.seed_of(cfg_id), variant or c["routing"], c["drop"],
+                c["routed"] == "mxfp8")
 
 
 @dataclasses.dataclass
@@ -40,6 +42,7 @@ class Inputs:
     main_grads: dict           # fp32 combined-layout buffers (initial values)
     probs_np: np.ndarray
     map_np: np.ndarray
+    mx: dict = None            # MXFP8 routed weights: name -> (payload, scale, col payload, col scale)
 
 
 def make_inputs(case: Case, device="cuda", routing=None) -> Inputs:
@@ -49,7 +52,22 @@ def make_inputs(case: Case, device="cuda", routing=None) -> Inputs:
     mg = MI.make_main_grads(case.H, case.I, case.E, case.seed, device=device)
     probs = torch.from_numpy(r.probs).to(device)
     rmap = torch.from_numpy(r.routing_map).to(device)
-    return Inputs(case, hidden, grad_out, probs, rmap, w, mg, r.probs, r.routing_map)
+    mx = MI.make_mxfp8_weights(w) if case.mx else None
+    return Inputs(case, hidden, grad_out, probs, rmap, w, mg, r.probs, r.routing_map, mx)
+
+
+def weight_views(inp: Inputs):
+    """moe_weights of the inputs: bf16 combined-FC1 views, or MXFP8 routed views."""
+    import mixture_experts_layer_pack_gb300 as M
+    w = inp.weights
+    wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
+    if inp.mx:
+        I = inp.case.I
+        q1, s1, c1, cs1 = inp.mx["routed_fc1"]
+        wv.routed_gate = M.mxfp8_view(q1[:, :I], s1[:, :I], c1[:, :I], cs1[:, :I // 32])
+        wv.routed_up = M.mxfp8_view(q1[:, I:], s1[:, I:], c1[:, I:], cs1[:, I // 32:])
+        wv.routed_down = M.mxfp8_view(*inp.mx["routed_fc2"])
+    return wv
 
 
 @dataclasses.dataclass
@@ -65,9 +83,11 @@ def run_gpu(inp: Inputs, backward=True, main_grads=None, layer=None) -> GpuResul
     import mixture_experts_layer_pack_gb300 as M
     c = inp.case
     if layer is None:
-        layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, device=inp.hidden.device)
-    w = inp.weights
-    wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
+        layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, device=inp.hidden.device,
+                           routed_wtype=M.binding.MOE_W_MXFP8 if c.mx else M.binding.MOE_W_BF16)
+    wv = weight_views(inp)
+    if c.mx:
+        layer.prepare_weights(wv)
     out = layer.forward(inp.hidden, inp.probs, inp.routing_map.view(torch.uint8), wv)
     dh = dp = None
     mg = None
@@ -105,6 +125,40 @@ class TorchWeights:
         fc1 = self._f64(self.w["routed_fc1"][e])
         return fc1[:self.I], fc1[self.I:], self._f64(self.w["routed_fc2"][e])
 
+    def routed_dgrad(self, e):
+        return self.routed(e)
+
+
+class TorchMxWeights(TorchWeights):
+    """Oracle weight accessor for MXFP8 routed weights: the oracle codec's exact
+    dequantisation of the input payloads (rowwise for forward, columnwise for
+    dgrad); shared weights bf16."""
+
+    def __init__(self, w: dict, mx: dict):
+        super().__init__(w)
+        self.mx = mx
+
+    @staticmethod
+    def _deq(q, s, axis):
+        from oracle import mxfp8
+        return mxfp8.dequantize(q.cpu().numpy(), s.cpu().numpy(), axis=axis)
+
+    def routed(self, e):
+        q1, s1, _, _ = self.mx["routed_fc1"]
+        q2, s2, _, _ = self.mx["routed_fc2"]
+        fc1 = self._deq(q1[e], s1[e], 1)
+        return fc1[:self.I], fc1[self.I:], self._deq(q2[e], s2[e], 1)
+
+    def routed_dgrad(self, e):
+        _, _, c1, cs1 = self.mx["routed_fc1"]
+        _, _, c2, cs2 = self.mx["routed_fc2"]
+        fc1 = self._deq(c1[e], cs1[e], 0)
+        return fc1[:self.I], fc1[self.I:], self._deq(c2[e], cs2[e], 0)
+
+
+def oracle_weights(inp: Inputs):
+    return TorchMxWeights(inp.weights, inp.mx) if inp.mx else TorchWeights(inp.weights)
+
 
 def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
@@ -112,11 +166,11 @@ def f64(t):
 
 def oracle_full(inp: Inputs, precision="bf16"):
     """Oracle forward + backward over all tokens (bf16 mode: with its rounding envelope)."""
-    W = TorchWeights(inp.weights)
+    W = oracle_weights(inp)
     out, cache = O.forward(f64(inp.hidden), inp.probs_np, inp.map_np, W, inp.case.k, precision=precision)
     go = f64(inp.grad_out)
     dx, dprobs, grads = O.backward(go, cache, W)
-    cache["envelope"] = O.envelope(go, cache, W) if precision == "bf16" else None
+    cache["envelope"] = O.envelope(go, cache, W) if precision in ("bf16", "mxfp8") else None
     return out, dx, dprobs, grads, cache
 
 

@@ -103,3 +103,16 @@ def test_dequantize_known_payload():
     scale = np.array([[130]], np.uint8)                                     # 2^3
     deq = M.dequantize(payload, scale, axis=1)
     assert deq[0, :4].tolist() == [8.0, 16.0, -8.0, 0.0]
+
+
+def test_input_quantiser_agrees_with_the_oracle_codec():
+    """The seeded MXFP8 input weights (PyTorch float8 cast) follow the same OCP MX
+    rule as the oracle's codec, so both describe the same weights."""
+    import moe_inputs as MI
+    g = torch.Generator().manual_seed(3)
+    w = (torch.randn(2, 64, 96, generator=g) * 0.02).to(torch.bfloat16)
+    w[0, :32, :32] = 0                                     # all-zero blocks
+    for axis, np_axis in ((-1, 2), (-2, 1)):
+        q, s = MI.mxfp8_quantize_torch(w, axis)
+        rq, rs = M.quantize(w.double().numpy(), axis=np_axis)
+        assert np.array_equal(q.numpy(), rq) and np.array_equal(s.numpy(), rs)

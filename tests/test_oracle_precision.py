@@ -125,31 +125,45 @@ def test_bf16_mode_within_rounding_bounds(seed):
         assert np.all(np.abs(g_b["routed"][e][2] - dWd) <= bd * (1 + 1e-9) + 1e-15)
 
 
-def _fp32_layer(x, go, m, probs, W, k):
+def _fp32_layer(x, go, m, probs, W, k, mx=False):
     """An independent fp32 evaluation of the layer (numpy float32 matmuls and
-    elementwise math, bf16 rounding of the GEMM operands, fp64 afterwards):
-    stands in for any kernel that evaluates the operands in fp32."""
+    elementwise math, bf16 rounding of the GEMM operands -- MXFP8 for the routed
+    forward/dgrad operands when mx -- fp64 afterwards): stands in for any kernel
+    that evaluates the operands in fp32."""
+    from oracle import mxfp8 as MXC
     f32 = np.float32
     rnd = O.bf16_round
+
+    def mxr(v):
+        q, sc = MXC.quantize(np.asarray(v, np.float64), axis=-1)
+        return MXC.dequantize(q, sc, axis=-1)
 
     def sig(z):
         return f32(1) / (f32(1) + np.exp(-z))
 
-    def expert(xr, gor, p, Wg, Wu, Wd):
-        xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xr, Wg, Wu, Wd, gor))
+    def expert(xr, gor, p, Wg, Wu, Wd, quant):
+        xq = mxr(xr) if quant else xr
+        goq = mxr(gor) if quant else gor
+        xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xq, Wg, Wu, Wd, goq))
         g = xr32 @ Wg32.T
         u = xr32 @ Wu32.T
         s = sig(g)
-        a = rnd((g * s * u).astype(np.float64))
+        a = (mxr if quant else rnd)((g * s * u).astype(np.float64))
         y = a @ Wd.T
         da = p.astype(f32)[:, None] * (go32 @ Wd32)
-        dg = rnd((da * u * (s * (f32(1) + g * (f32(1) - s)))).astype(np.float64))
-        du = rnd((da * (g * s)).astype(np.float64))
+        dg32 = da * u * (s * (f32(1) + g * (f32(1) - s)))
+        du32 = da * (g * s)
+        dg, du = rnd(dg32.astype(np.float64)), rnd(du32.astype(np.float64))
+        if quant:
+            qq = mxr(np.concatenate([dg32, du32], axis=1).astype(np.float64))
+            dx = qq[:, :dg.shape[1]] @ Wg + qq[:, dg.shape[1]:] @ Wu
+        else:
+            dx = dg @ Wg + du @ Wu
         pa = rnd((p.astype(f32)[:, None] * a.astype(f32)).astype(np.float64))
-        return y, dg @ Wg + du @ Wu, dg.T @ xr, du.T @ xr, gor.T @ pa
+        return y, dx, dg.T @ xr, du.T @ xr, gor.T @ pa
 
     T = x.shape[0]
-    ys, dxs, gsg, gsu, gsd = expert(x, go, np.ones(T), *W.shared())
+    ys, dxs, gsg, gsu, gsd = expert(x, go, np.ones(T), *W.shared(), False)
     out, dh = ys.copy(), dxs.copy()
     ids, pp, _ = O.route_pack(m, probs, k)
     routed = {}
@@ -157,7 +171,7 @@ def _fp32_layer(x, go, m, probs, W, k):
         rows, slots = np.nonzero(ids == e)
         if rows.size == 0:
             continue
-        y, dx, g1, g2, g3 = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e))
+        y, dx, g1, g2, g3 = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e), mx)
         out[rows] += pp[rows, slots, None] * y
         dh[rows] += dx
         routed[e] = (g1, g2, g3)
@@ -200,3 +214,30 @@ def test_envelope_covers_fp32_evaluation(seed):
         sc = np.abs(ref).max()
         assert np.median(env[n]) < 2.5e-4 * sc and np.percentile(env[n], 99) < 1e-3 * sc, n
         assert env[n].max() < 5e-3 * sc, n
+
+
+@pytest.mark.parametrize("seed", [21, 22])
+def test_mxfp8_envelope_covers_fp32_evaluation(seed):
+    """mxfp8 mode: an fp32 evaluation that quantises the routed forward/dgrad
+    operands with the codec stays within the oracle's result plus its envelope."""
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k = 256, 256, 256, 3, 2
+    W = O.DenseWeights(*(rng.standard_normal(s) * 0.06 for s in
+                         ((I, H), (I, H), (H, I), (E, I, H), (E, I, H), (E, H, I))))
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    go = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    m = np.zeros((T, E), bool)
+    for t in range(T):
+        m[t, rng.choice(E, 2, replace=False)] = True
+    probs = rng.random((T, E)).astype(np.float32).astype(np.float64)
+    out_b, cache = O.forward(x, probs, m, W, k, precision="mxfp8")
+    dh_b, _, g_b = O.backward(go, cache, W)
+    env = O.envelope(go, cache, W)
+    out_f, dh_f, g_f = _fp32_layer(x, go, m, probs, W, k, mx=True)
+    for a, b, ev, name in ((out_f, out_b, env["out"], "out"), (dh_f, dh_b, env["dhidden"], "dhidden")):
+        slack = 1e-5 * np.abs(b).max()
+        assert np.all(np.abs(a - b) <= ev + slack), name
+    for e, gs in g_f["routed"].items():
+        for j in range(3):
+            b = g_b["routed"][e][j]
+            assert np.all(np.abs(gs[j] - b) <= env["routed"][e][j] + 1e-5 * np.abs(b).max()), (e, j)
