@@ -147,29 +147,40 @@ def gpu_id_for(dev_index):
 
 
 # ----------------------------------------------------------------- algorithmic work
-def kernel_work(name, T, H, E, k, I, R, E_act):
+MX_ROUTED_GEMMS = ("gemm_fwd_gu_routed", "gemm_fwd_down_routed", "gemm_bwd_down_routed", "gemm_bwd_gu_routed")
+
+
+def kernel_work(name, T, H, E, k, I, R, E_act, mx=False):
     """(algorithmic flops, algorithmic HBM bytes) of one launch of a kernel class.
 
     Bytes count each operand read once and each result written once (no padding
     rows, no re-reads); flops count a multiply-add as 2. Weights of experts
-    without tokens are not read."""
+    without tokens are not read. mx: the routed forward/dgrad GEMMs read MXFP8
+    operands (1 byte + 1/32 byte of scale per element) and the producers of
+    those operands also write their MXFP8 copies."""
     b2, b4 = 2, 4
-    W_fc1, W_down = E_act * 2 * I * H * b2, E_act * H * I * b2
+    bq = 1 + 1 / 32                          # MXFP8 element incl. its share of the scale
+    wb = bq if mx else b2                    # routed weight element
+    ab = bq if mx else b2                    # routed fprop/dgrad activation operand element
+    W_fc1, W_down = E_act * 2 * I * H * wb, E_act * H * I * wb
+    q_a = R * I * bq if mx else 0
+    q_dgdu = R * 2 * I * bq if mx else 0
+    q_rows = R * H * bq if mx else 0
     table = {
         "route_pack": (0, T * E + T * k * (b4 * 3 + b4)),
         "route_scan": (0, T * E + T * k * b4 + E * b4),
-        "route_place": (0, T * k * 12 + R * 12 + 2 * R * H * b2),
-        "gather_rows": (0, 2 * R * H * b2),
-        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * b2 + W_fc1 + R * I * b2 + R * 2 * I * b4),
+        "route_place": (0, T * k * 12 + R * 12 + 2 * R * H * b2 + q_rows),
+        "gather_rows": (0, 2 * R * H * b2 + q_rows),
+        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * ab + W_fc1 + R * I * b2 + R * 2 * I * b4 + q_a),
         "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * b2 + T * 2 * I * b4),
-        "gemm_fwd_down_routed": (2 * R * I * H, R * I * b2 + W_down + R * H * b4),
+        "gemm_fwd_down_routed": (2 * R * I * H, R * I * ab + W_down + R * H * b4),
         "gemm_fwd_down_shared": (2 * T * I * H, T * I * b2 + H * I * b2 + T * H * b4),
         "combine": (0, T * H * b4 + R * H * b4 + T * H * b2),
-        "gemm_bwd_down_routed": (2 * R * H * I, R * H * b2 + W_down + R * I * b2 + R * 2 * I * b4
-                                 + R * 2 * I * b2 + R * I * b2),
+        "gemm_bwd_down_routed": (2 * R * H * I, R * H * ab + W_down + R * I * b2 + R * 2 * I * b4
+                                 + R * 2 * I * b2 + R * I * b2 + q_dgdu),
         "gemm_bwd_down_shared": (2 * T * H * I, T * H * b2 + H * I * b2 + T * I * b2 + T * 2 * I * b4
                                  + T * 2 * I * b2),
-        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * b2 + W_fc1 + R * H * b4),
+        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * ab + W_fc1 + R * H * b4),
         "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * b2 + 2 * I * H * b2 + T * H * b4),
         "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * b2 + R * H * b2 + E_act * 2 * I * H * 8),
         "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * b2 + E_act * H * I * 8),
@@ -180,12 +191,16 @@ def kernel_work(name, T, H, E, k, I, R, E_act):
     return table[name]
 
 
-def roofline_of(name, ms_per_launch, work, peaks, peaks_kind, traffic=None):
+def roofline_of(name, ms_per_launch, work, peaks, peaks_kind, traffic=None, fp8=False):
+    """Roofline of one kernel: tensor-bound if its intensity exceeds the ridge of
+    the peak for its own dtype (fp8 = the measured bf16 peak x 2, the nominal
+    dense ratio), else HBM-bound."""
     flops, nbytes = work
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_peak = peaks["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if flops > 0 and flops / max(nbytes, 1) > ridge:
         achieved = flops / (ms_per_launch * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak = tensor_peak
         r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
     else:
         achieved = nbytes / (ms_per_launch * 1e-3) / 1e9
@@ -292,8 +307,7 @@ def run_ours(args):
 
     cid = args.config
     c = MI.CONFIGS[cid]
-    if c["routed"] != "bf16":
-        raise SystemExit(f"config {cid}: routed {c['routed']} weights are not built into this bench")
+    mx = c["routed"] == "mxfp8"
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
     seed = MI.seed_of(cid)
     r = MI.config_routing(cid)
@@ -305,8 +319,18 @@ def run_ours(args):
     probs = torch.from_numpy(r.probs).to(dev)
     rmap = torch.from_numpy(r.routing_map).to(dev).view(torch.uint8)
 
-    layer = M.MoELayer(T, H, E, k, I, device=dev)
+    layer = M.MoELayer(T, H, E, k, I, device=dev,
+                       routed_wtype=M.binding.MOE_W_MXFP8 if mx else M.binding.MOE_W_BF16)
     wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
+    if mx:   # MXFP8 routed weights (rowwise + columnwise), prepared outside the timed region
+        wmx = MI.make_mxfp8_weights(w)
+        w["routed_fc1"] = w["routed_fc2"] = None
+        q1, s1, c1, cs1 = wmx["routed_fc1"]
+        wv.routed_gate = M.mxfp8_view(q1[:, :I], s1[:, :I], c1[:, :I], cs1[:, :I // 32])
+        wv.routed_up = M.mxfp8_view(q1[:, I:], s1[:, I:], c1[:, I:], cs1[:, I // 32:])
+        wv.routed_down = M.mxfp8_view(*wmx["routed_fc2"])
+        layer.prepare_weights(wv)
+        torch.cuda.synchronize()
     mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
     out = torch.empty_like(hidden)
     dh = torch.empty_like(hidden)
@@ -401,26 +425,27 @@ def run_ours(args):
             traffic = json.load(open(tr_path)).get(MI.WORKLOAD_NAMES[cid], {}).get(top)
         except Exception:
             traffic = None
-    roof = roofline_of(top, per_kernel[top]["ms_per_launch"], kernel_work(top, T, H, E, k, I, R, E_act), peaks,
-                       peaks_kind, traffic)
+    roof = roofline_of(top, per_kernel[top]["ms_per_launch"], kernel_work(top, T, H, E, k, I, R, E_act, mx), peaks,
+                       peaks_kind, traffic, fp8=mx and top in MX_ROUTED_GEMMS)
     for name, v in per_kernel.items():
-        f, b = kernel_work(name, T, H, E, k, I, R, E_act)
+        f, b = kernel_work(name, T, H, E, k, I, R, E_act, mx)
         ms_l = v["ms_per_launch"] * 1e-3
         v["tflops"] = f / ms_l / 1e12 if f else 0.0
         v["gbs"] = b / ms_l / 1e9
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 routed / bf16 shared" if mx else "bf16",
             "data": "synthetic (seeded routing, N(0,0.02) weights, N(0,1) activations; random init)",
             "config": {"workload": MI.WORKLOAD_NAMES[cid], "T": T, "H": H, "E": E, "k": k, "I": I,
-                       "valid_routes": R, "routing": "softmax over N(0,1) logits, top-6, dense probs/map",
+                       "valid_routes": R, "routing": f"seeded router stand-in ({c['routing']}, drop={c['drop']})",
                        "main_grad": "fp32, accumulated in place every step",
                        "l2": "inputs larger than L2: routed weights %.2f GB + main_grad %.2f GB per step"
                              % (3 * E * I * H * 2 / 1e9, 3 * (E + 1) * I * H * 4 / 1e9),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tflops": tflops,
             "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+            "pct_fp8_peak": 100.0 * tflops / (2 * peaks["bf16_tflops"]) if mx else None,
             "peaks": {**peaks, "source": peaks_kind},
             "useful_flops_per_step": flops,
             "roofline": roof, "kernels": per_kernel, "gpu_launches": launches, "clocks": clocks, "e2e": e2e}

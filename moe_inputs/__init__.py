@@ -200,19 +200,19 @@ def mxfp8_quantize_torch(w, axis):
 def make_mxfp8_weights(w: dict) -> dict:
     """MXFP8 copies of the routed weights (combined FC1 [E,2I,H], FC2 [E,H,I]):
     rowwise payload + scales [E,N,K/32] for forward, columnwise payload +
-    scales [E,N/32,K] for dgrad. FC1 is quantised as its gate and up halves
-    separately, so no 32-row block of the columnwise copy spans both."""
+    scales [E,N/32,K] for dgrad (quantised one expert at a time to bound the
+    temporary memory)."""
     torch = _torch()
     out = {}
-    E, two_i, H = w["routed_fc1"].shape
-    inter = two_i // 2
-    for name, t in (("routed_fc1", w["routed_fc1"]), ("routed_fc2", w["routed_fc2"])):
-        q, s = mxfp8_quantize_torch(t, -1)
-        if name == "routed_fc1":
-            qcs = [mxfp8_quantize_torch(t[:, h * inter:(h + 1) * inter], -2) for h in range(2)]
-            qc = torch.cat([qcs[0][0], qcs[1][0]], dim=1)
-            sc = torch.cat([qcs[0][1], qcs[1][1]], dim=1)
-        else:
-            qc, sc = mxfp8_quantize_torch(t, -2)
+    for name in ("routed_fc1", "routed_fc2"):
+        t = w[name]
+        E, N, K = t.shape
+        q = torch.empty((E, N, K), dtype=torch.uint8, device=t.device)
+        s = torch.empty((E, N, K // 32), dtype=torch.uint8, device=t.device)
+        qc = torch.empty((E, N, K), dtype=torch.uint8, device=t.device)
+        sc = torch.empty((E, N // 32, K), dtype=torch.uint8, device=t.device)
+        for e in range(E):
+            q[e], s[e] = mxfp8_quantize_torch(t[e], -1)
+            qc[e], sc[e] = mxfp8_quantize_torch(t[e], -2)
         out[name] = (q, s, qc, sc)
     return out

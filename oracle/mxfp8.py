@@ -92,9 +92,14 @@ def quantize(x, axis):
     return np.moveaxis(payload, -1, axis), np.moveaxis(sc, -1, axis)
 
 
+_DECODE_TABLE = e4m3_decode(np.arange(256, dtype=np.uint8))
+_E8M0_TABLE = e8m0_value(np.arange(256, dtype=np.uint8))
+
+
 def dequantize(payload, scale, axis):
     """Exact fp64 value of an MXFP8 tensor: decode(payload) * 2^(scale - 127),
-    one scale per 32 elements along ``axis``."""
-    v = e4m3_decode(payload)
-    s = np.repeat(e8m0_value(scale), BLOCK, axis=axis)
+    one scale per 32 elements along ``axis`` (decoding through 256-entry tables
+    of e4m3_decode and e8m0_value)."""
+    v = _DECODE_TABLE[np.asarray(payload, np.uint8)]
+    s = np.repeat(_E8M0_TABLE[np.asarray(scale, np.uint8)], BLOCK, axis=axis)
     return v * s

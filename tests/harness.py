@@ -138,6 +138,10 @@ class TorchMxWeights(TorchWeights):
         super().__init__(w)
         self.mx = mx
 
+    @property
+    def num_experts(self):
+        return self.mx["routed_fc1"][0].shape[0]
+
     @staticmethod
     def _deq(q, s, axis):
         from oracle import mxfp8

@@ -109,3 +109,78 @@ def test_mxfp8_layer_parity_config3_full():
     print("config 3 routed dW vs exact oracle, worst expert:",
           {k: f"{max(v for n, v in errs.items() if n.startswith('exact dW routed ' + k)):.2e}"
            for k in ("gate", "up", "down")})
+
+
+@pytest.mark.slow
+def test_mxfp8_layer_parity_config4_sampled():
+    """DSv4-like layer (T=8192, H=7168, E=384, top-6, I=2048, MXFP8 routed, 2% of
+    routes missing) at full size: sampled tokens for out/dhidden/dprobs, the
+    busiest and a median expert for routed main_grad, all tokens for the shared
+    expert's main_grad; the backward accumulates in place (main_grad is 68 GB)."""
+    import mixture_experts_layer_pack_gb300 as M
+    from oracle import moe_oracle as O
+    from tests.harness import TorchMxWeights, weight_views
+    inp = make_inputs(config_case(4))
+    c = inp.case
+    I = c.I
+    W = TorchMxWeights(inp.weights, inp.mx)
+    counts = inp.map_np.sum(0)
+    hot = int(np.argmax(counts))
+    med = int(np.argsort(counts)[c.E // 2])
+    mg0 = {e: (inp.main_grads["routed_fc1"][e].cpu(), inp.main_grads["routed_fc2"][e].cpu()) for e in (hot, med)}
+    mg0_shared = {n: inp.main_grads[n].cpu() for n in ("shared_fc1", "shared_fc2")}
+    idle = np.flatnonzero(counts == 0)
+    idle_before = {int(e): inp.main_grads["routed_fc1"][e].clone() for e in idle[:2]}
+
+    layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, routed_wtype=M.binding.MOE_W_MXFP8)
+    wv = weight_views(inp)
+    layer.prepare_weights(wv)
+    inp.weights["routed_fc1"] = inp.weights["routed_fc2"] = None        # the layer reads the MXFP8 copies
+    torch.cuda.empty_cache()
+    out = layer.forward(inp.hidden, inp.probs, inp.routing_map.view(torch.uint8), wv)
+    mg = inp.main_grads
+    mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
+    dh, dp = layer.backward(inp.grad_out, mgv)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert torch.isfinite(out).all() and torch.isfinite(dh).all() and torch.isfinite(dp).all()
+
+    rng = np.random.default_rng(4)
+    toks = np.sort(rng.choice(c.T, 16, replace=False))
+    tt = torch.from_numpy(toks).to(inp.hidden.device)
+    ref, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], inp.map_np[toks], W, c.k, precision="mxfp8")
+    go = f64(inp.grad_out[tt])
+    rdx, rdp, _ = O.backward(go, cache, W)
+    env = O.envelope(go, cache, W)
+    kw = dict(rtol=MX_RTOL, atol_frac=MX_ATOL)
+    assert_close(f64(out[tt]), ref, "out (sampled)", env=env["out"], **kw)
+    assert_close(f64(dh[tt]), rdx, "dhidden (sampled)", env=env["dhidden"], **kw)
+    assert_close(f64(dp[tt]), rdp, "dprobs (sampled)", env=env["dprobs"], **kw)
+
+    for e in (hot, med):
+        rows = np.flatnonzero(inp.map_np[:, e])
+        m = np.zeros((rows.size, c.E), bool)
+        m[:, e] = True
+        rt = torch.from_numpy(rows).to(inp.hidden.device)
+        _, ce = O.forward(f64(inp.hidden[rt]), inp.probs_np[rows], m, W, c.k, precision="mxfp8")
+        goe = f64(inp.grad_out[rt])
+        _, _, ge = O.backward(goe, ce, W)
+        ee = O.envelope(goe, ce, W)["routed"][e]
+        d1 = f64(mg["routed_fc1"][e]) - mg0[e][0].double().numpy()
+        d2 = f64(mg["routed_fc2"][e]) - mg0[e][1].double().numpy()
+        assert_close(d1[:I], ge["routed"][e][0], f"dW routed gate[{e}]", env=ee[0], **kw)
+        assert_close(d1[I:], ge["routed"][e][1], f"dW routed up[{e}]", env=ee[1], **kw)
+        assert_close(d2, ge["routed"][e][2], f"dW routed down[{e}]", env=ee[2], **kw)
+    for e, before in idle_before.items():
+        assert torch.equal(mg["routed_fc1"][e], before)
+
+    m0 = np.zeros_like(inp.map_np)
+    _, cs = O.forward(f64(inp.hidden), inp.probs_np, m0, W, c.k, precision="mxfp8")
+    gall = f64(inp.grad_out)
+    _, _, gs = O.backward(gall, cs, W)
+    es = O.envelope(gall, cs, W)
+    d1 = f64(mg["shared_fc1"]) - mg0_shared["shared_fc1"].double().numpy()
+    d2 = f64(mg["shared_fc2"]) - mg0_shared["shared_fc2"].double().numpy()
+    assert_close(d1[:I], gs["shared_gate"], "dW shared gate", env=es["shared_gate"], **kw)
+    assert_close(d1[I:], gs["shared_up"], "dW shared up", env=es["shared_up"], **kw)
+    assert_close(d2, gs["shared_down"], "dW shared down", env=es["shared_down"], **kw)
