@@ -98,10 +98,10 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
         : "memory");
 }
 
-// TMA reduce-add of a shared-memory box into global memory (one add per element)
-__device__ __forceinline__ void tma_reduce_add_3d(const void* map, const void* src, int x, int y, int z) {
+// TMA store of a shared-memory box into global memory
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int x, int y, int z) {
     asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
             reinterpret_cast<uint64_t>(map)),
         "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
         : "memory");

@@ -9,7 +9,7 @@
 //   OP_FWD_DOWN [R,H]  = a[R,I] . W_down[e]^T          epilogue y = p * acc (fp32)
 //   OP_BWD_DOWN [R,I]  = go_perm[R,H] . W_down[e]      epilogue SwiGLU backward, dprob partials
 //   OP_BWD_GU   [R,H]  = [dg|du][R,2I] . W_fc1[e]      epilogue store (fp32)
-//   OP_WGRAD    [M,N] += A[seg,M]^T . B[seg,N]        epilogue fp32 read-add-store into main_grad
+//   OP_WGRAD    [M,N] += A[seg,M]^T . B[seg,N]        epilogue fp32 load-add-store of main_grad
 //
 // Rows of the routed GEMMs are the dispatch permutation, each expert's
 // segment padded to a multiple of 128 rows (zero rows), so a 128-row tile
@@ -23,7 +23,10 @@
 // fused epilogue while the next tile accumulates. Operands use the 128-byte
 // swizzle: K-major tiles are 128 rows x 128 bytes; M/N-major tiles are
 // 64-element (128-byte) columns x 64 K-rows, 8 KB apart. The weight-gradient
-// epilogue adds into main_grad with TMA reduce-add boxes of 32 x 32 fp32.
+// epilogue moves main_grad in TMA boxes of 32 x 32 fp32: each box is loaded
+// one box ahead into a double buffer, gets the accumulator added in shared
+// memory and is stored back (a TMA reduce-add into L2 streams main_grad at
+// only ~3/4 of the rate of a plain load and store on this part).
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -38,15 +41,20 @@ constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
 
 constexpr uint32_t kStageTileBytes = 32 * 32 * 4;  // fp32 staging box of one epilogue warp (32 rows x 32 cols)
 
-template <int BN>
+template <int OP, int BN>
 struct Cfg {
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = BN * kBK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    // the weight-gradient epilogue double-buffers its main_grad boxes, so it
+    // gives up operand stages (its K per tile is one expert's short segment)
+    static constexpr int BUFS = (OP == OP_WGRAD) ? 2 : 1;
+    static constexpr int STAGES = (OP == OP_WGRAD) ? ((BN == 256) ? 3 : (BN == 128 ? 5 : 6))
+                                                   : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
-    static constexpr uint32_t STAGING = kEpiWarps * kStageTileBytes;
-    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING + 1024 + 256;
+    static constexpr uint32_t STAGING = kEpiWarps * BUFS * kStageTileBytes;
+    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING + 1024 + 512;
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle
@@ -172,33 +180,8 @@ __device__ __forceinline__ uint32_t mx_quant_lane4(const float (&v)[4], uint32_t
 
 template <int OP, int BN, bool MX = false>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int q, int half, const GemmArgs& a,
-                                              float* staging, const CUtensorMap* mC0, const CUtensorMap* mC1) {
+                                              float* staging) {
     const int lane = threadIdx.x & 31;
-    if (OP == OP_WGRAD) {
-        // main_grad[e][m][n] += acc through TMA reduce-add: the warp stages its 32
-        // rows x 32 columns in shared memory (128-byte swizzle) and one lane
-        // issues the reduction; the L2 performs one fp32 add per element
-        const int m0 = t.mt * kBM + q * 32;
-        const bool hi = m0 >= a.m_split;
-        const CUtensorMap* mc = hi ? mC1 : mC0;
-        const int row0 = hi ? m0 - a.m_split : m0;
-#pragma unroll 1
-        for (int c = half; c < BN / 32; c += kEpiHalves) {
-            float v[32];
-            tmem_ld32(t_row + c * 32, v);
-            if (lane == 0) bulk_wait_read<0>();      // the previous box has left the staging buffer
-            __syncwarp();
-            stage_chunk(staging, v);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_reduce_add_3d(mc, staging, t.nt * BN + c * 32, row0, t.e);
-                bulk_commit();
-            }
-        }
-        return;
-    }
-
     // The warp owns rows [m_base, m_base+32) of the tile. Each 32x32 fp32 chunk
     // read from TMEM (lane = row) is transposed through the warp's staging
     // buffer so that global loads and stores cover whole row segments: in step
@@ -368,12 +351,131 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
     }
 }
 
+// Weight-gradient epilogue of one warp: main_grad[e][m][n] += acc for its
+// 32-row quarter of every tile and its share of the 32-column chunks. Each
+// 32x32 fp32 box of main_grad is TMA-loaded into one of two 4 KB buffers one
+// box ahead (the next tile's first box is fetched while this tile's last box is
+// added), the accumulator chunk read from TMEM (lane = row) is added in shared
+// memory, and the box is TMA-stored back: one fp32 add per element, so the
+// result is fl32(main_grad + dW) whatever the schedule.
+template <int BN>
+__device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_tiles, uint32_t tmem_base, int q,
+                                               int half, float* bufs, uint64_t* mg_bar, uint64_t* tfull,
+                                               uint64_t* tempty, volatile int* abort_flag, const CUtensorMap* mC0,
+                                               const CUtensorMap* mC1) {
+    constexpr int CH = BN / 32 / kEpiHalves;  // chunks of this warp per tile
+    const int lane = threadIdx.x & 31;
+    auto next_valid = [&](int tile) {
+        for (; tile < total_tiles; tile += gridDim.x)
+            if (decode_tile<OP_WGRAD>(tile, args).kblocks > 0) return tile;
+        return total_tiles;
+    };
+    // box (tile t, chunk c): destination map and coordinates
+    auto box = [&](const Tile& t, int c, const CUtensorMap*& mc, int& x, int& y) {
+        const int m0 = t.mt * kBM + q * 32;
+        const bool hi = m0 >= args.m_split;
+        mc = hi ? mC1 : mC0;
+        y = hi ? m0 - args.m_split : m0;
+        x = t.nt * BN + (half + c * kEpiHalves) * 32;
+    };
+    auto load_box = [&](const Tile& t, int c, int b) {
+        const CUtensorMap* mc;
+        int x, y;
+        box(t, c, mc, x, y);
+        mbar_arrive_expect_tx(&mg_bar[b], kStageTileBytes);
+        tma_load_3d(bufs + b * (kStageTileBytes / 4), mc, &mg_bar[b], x, y, t.e);
+    };
+
+    int cur = next_valid(blockIdx.x);
+    Tile t = decode_tile<OP_WGRAD>(cur < total_tiles ? cur : 0, args);
+    uint32_t pending = 0, parity = 0;  // per buffer: a load in flight / parity of its next completion
+    if (cur < total_tiles && lane == 0) {
+        load_box(t, 0, 0);
+        pending = 1;
+    }
+    int jb = 0, it = 0;
+    bool ok = true;
+    while (ok && cur < total_tiles) {
+        const int acc = it & 1;
+        const uint32_t use = uint32_t(it >> 1);
+        ++it;
+        int w = 0;
+        if (lane == 0) w = mbar_wait(&tfull[acc], use & 1, abort_flag, args.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w, 0)) break;
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+        const int nxt = next_valid(cur + gridDim.x);
+        const Tile tn = decode_tile<OP_WGRAD>(nxt < total_tiles ? nxt : 0, args);
+#pragma unroll 1
+        for (int c = 0; c < CH; ++c) {
+            const int b = jb & 1;
+            if (lane == 0) {
+                // prefetch the box after this one into the other buffer, once the
+                // store that last used it has read it out
+                const bool more = c + 1 < CH || nxt < total_tiles;
+                if (more) {
+                    bulk_wait_read<0>();
+                    load_box(c + 1 < CH ? t : tn, c + 1 < CH ? c + 1 : 0, b ^ 1);
+                    pending |= 1u << (b ^ 1);
+                }
+            }
+            float v[32];
+            tmem_ld32(t_row + uint32_t((half + c * kEpiHalves) * 32), v);
+            if (lane == 0) w = mbar_wait(&mg_bar[b], (parity >> b) & 1, abort_flag, args.status) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, w, 0)) {
+                ok = false;
+                break;
+            }
+            // the phase has completed: every lane's own successful test acquires the box
+            (void)mbar_try_wait(&mg_bar[b], (parity >> b) & 1);
+            __syncwarp();
+            pending &= ~(1u << b);
+            parity ^= 1u << b;
+            // row `lane` of the box, 128-byte swizzled as the TMA wrote it
+            float4* srow = reinterpret_cast<float4*>(bufs + b * (kStageTileBytes / 4) + lane * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float4 m = srow[j ^ (lane & 7)];
+                m.x += v[4 * j];
+                m.y += v[4 * j + 1];
+                m.z += v[4 * j + 2];
+                m.w += v[4 * j + 3];
+                srow[j ^ (lane & 7)] = m;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const CUtensorMap* mc;
+                int x, y;
+                box(t, c, mc, x, y);
+                tma_store_3d(mc, bufs + b * (kStageTileBytes / 4), x, y, t.e);
+                bulk_commit();
+            }
+            ++jb;
+        }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        cur = nxt;
+        t = tn;
+    }
+    if (lane == 0) {
+        // wind down: loads still in flight land, every store completes
+        for (int b = 0; b < 2; ++b)
+            if (pending & (1u << b)) mbar_wait_drain(&mg_bar[b], (parity >> b) & 1, args.status);
+        bulk_wait<0>();
+    }
+    __syncwarp();
+}
+
 template <int OP, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
                     const __grid_constant__ CUtensorMap tmC1, const GemmArgs args) {
-    using C = Cfg<BN>;
+    using C = Cfg<OP, BN>;
     constexpr bool A_MN = (OP == OP_WGRAD);
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD);
     constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN>();
@@ -387,7 +489,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* mg_bar = drain + 1;  // weight gradient: two box buffers per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mg_bar + 2 * kEpiWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -403,6 +506,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(drain, 1);
+        if (OP == OP_WGRAD)
+            for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&mg_bar[b], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tmA);
@@ -506,27 +611,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ---------------- epilogue warps 2..: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
-        float* my_staging = staging + (warp - 2) * (kStageTileBytes / 4);
-        int it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile<OP>(tile, args);
-            if (t.kblocks == 0) continue;
-            const int buf = it & 1;
-            const uint32_t use = uint32_t(it >> 1);
-            ++it;
-            int ok = 0;
-            if (lane == 0) ok = mbar_wait(&tfull[buf], use & 1, abort_flag, args.status) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            __syncwarp();
-            tc_fence_after();
-            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            epilogue_tile<OP, BN>(t, t_row, q, half, args, my_staging, &tmC0, &tmC1);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
+        float* my_staging = staging + (warp - 2) * C::BUFS * (kStageTileBytes / 4);
+        if constexpr (OP == OP_WGRAD) {
+            wgrad_epilogue<BN>(args, total_tiles, tmem_base, q, half, my_staging, mg_bar + 2 * (warp - 2), tfull,
+                               tempty, abort_flag, &tmC0, &tmC1);
+        } else {
+            int it = 0;
+            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+                const Tile t = decode_tile<OP>(tile, args);
+                if (t.kblocks == 0) continue;
+                const int buf = it & 1;
+                const uint32_t use = uint32_t(it >> 1);
+                ++it;
+                int ok = 0;
+                if (lane == 0) ok = mbar_wait(&tfull[buf], use & 1, abort_flag, args.status) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                __syncwarp();
+                tc_fence_after();
+                const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+                epilogue_tile<OP, BN>(t, t_row, q, half, args, my_staging);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+            }
         }
-        if (OP == OP_WGRAD && lane == 0) bulk_wait<0>();   // every reduction has landed
         __syncwarp();
     }
 
@@ -609,7 +718,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* mg_bar = drain + 1;  // weight gradient: two box buffers per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mg_bar + 2 * kEpiWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -625,6 +735,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(drain, 1);
+        if (OP == OP_WGRAD)
+            for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&mg_bar[b], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tmA);
@@ -750,7 +862,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            epilogue_tile<OP, BN, true>(t, t_row, q, half, args, my_staging, nullptr, nullptr);
+            epilogue_tile<OP, BN, true>(t, t_row, q, half, args, my_staging);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -783,11 +895,12 @@ cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStrea
     static bool attr_set = false;
     auto kern = moe_gemm_kernel<OP, BN>;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<BN>::SMEM));
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<OP, BN>::SMEM));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<grid, kGemmThreads, Cfg<BN>::SMEM, st>>>(m.a, m.b0, m.b1, m.c0, m.c1, a);
+    kern<<<grid, kGemmThreads, Cfg<OP, BN>::SMEM, st>>>(m.a, m.b0, m.b1, m.c0, m.c1, a);
     count_launch();
     return cudaGetLastError();
 }
@@ -813,10 +926,6 @@ cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int gri
         case OP_BWD_GU: return launch_mx_one<OP_BWD_GU>(m, a, grid, st);
         default: return cudaErrorInvalidValue;
     }
-}
-
-size_t gemm_smem_bytes(int bn) {
-    return bn == 256 ? Cfg<256>::SMEM : (bn == 128 ? Cfg<128>::SMEM : Cfg<64>::SMEM);
 }
 
 int pick_bn(int64_t n, bool split_gate_up) {

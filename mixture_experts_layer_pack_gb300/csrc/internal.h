@@ -86,7 +86,6 @@ cudaError_t launch_gemm(int op, int bn, const GemmMaps& maps, const GemmArgs& ar
 cudaError_t launch_gemm_mx(int op, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
 constexpr int kMxBN = 128;
 constexpr int kMxBK = 128;
-size_t gemm_smem_bytes(int bn);
 
 // routing
 int route_rank_max_tokens();

@@ -228,7 +228,7 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int64_t rows, int64_t mn, int
 }
 
 // 3D fp32 main_grad view [E][rows][cols] (expert stride es, row stride rs) as a
-// TMA reduce destination, box 32 cols x 32 rows
+// TMA load and store map, box 32 cols x 32 rows
 bool map_main_grad(CUtensorMap* m, float* base, int64_t E, int64_t rows, int64_t cols, int64_t es, int64_t rs) {
     if (E <= 1) es = rows * rs;
     const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(E)};
