@@ -187,6 +187,8 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False):
         "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * b2 + T * H * b2 + 2 * I * H * 8),
         "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * b2 + H * I * 8),
         "unpermute": (0, T * H * b4 + R * H * b4 + T * H * b2 + T * E * b4),
+        "shared_gate_fwd": (2 * T * H, T * H * b2 + H * b2 + T * b4),
+        "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 8),
     }
     return table[name]
 

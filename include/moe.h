@@ -51,8 +51,14 @@ typedef enum { MOE_W_BF16 = 0, MOE_W_MXFP8 = 1 } moe_wtype;
 
 /* Layer shape. Routed and shared experts share `inter` (PR #6572, Supported
  * configurations: MOK limitations). hidden must be a multiple of 128, inter of 64;
- * 1 <= topk <= 32; 1 <= num_experts <= 1024. swiglu_limit must be 0: the clamp
- * exists on the pages (PR #8210 review: swiglu_limit) without a definition. */
+ * 1 <= topk <= 32; 1 <= num_experts <= 1024.
+ * swiglu_limit (PR #8210 review: the backend's swiglu_limit, taken from the
+ * layer's activation clamp value; the pages give no formula): 0 disables it;
+ * L > 0 clamps the SwiGLU inputs of every expert, routed and shared, before
+ * the activation: a = silu(min(g, L)) * min(max(u, -L), L) for g = x Wg^T,
+ * u = x Wu^T. Gradients pass where the clamp is inactive, bounds included
+ * (dg = 0 where g > L, du = 0 where |u| > L). Negative or non-finite values are
+ * MOE_ERR_INVALID_ARG. */
 typedef struct {
     int64_t max_tokens;   /* largest T any call will pass */
     int64_t hidden;       /* H */
@@ -60,7 +66,7 @@ typedef struct {
     int64_t topk;         /* k, fixed route width */
     int64_t inter;        /* I, intermediate size of routed and shared experts */
     int32_t routed_wtype; /* moe_wtype of the routed weights; shared weights are always bf16 */
-    float swiglu_limit;   /* must be 0 */
+    float swiglu_limit;   /* 0: no clamp; L > 0: SwiGLU input clamp (above) */
 } moe_config;
 
 /* One weight argument in the external ABI order (runtime page,
@@ -88,6 +94,13 @@ typedef struct {
 
 typedef struct {
     moe_wview shared_gate, shared_up, shared_down, routed_gate, routed_up, routed_down;
+    /* Optional output gate of the shared expert ("core.transformer.moe.megakernel.
+     * mok.runtime", _MoKAutograd.forward: shared_output_gate_weight;
+     * "...mok.backend", _register_shared_weights(use_output_gate)): bf16 [H],
+     * 16-byte aligned, or NULL for an ungated shared expert. The pages name the
+     * weight without its formula; the layer reads it as a per-token scalar
+     * gate on the shared expert's output: y_shared[t] *= sigmoid(hidden[t] . w). */
+    const void* shared_output_gate;
 } moe_weights;
 
 /* fp32 main_grad buffers in the six-buffer order (runtime page,
@@ -95,10 +108,13 @@ typedef struct {
  * strides[i] = {expert_stride, row_stride} in elements (expert_stride unused
  * for the shared three). Fused accumulation is mandatory (PR #6572, Design >
  * Gradient accumulation): every pointer must be non-null, 16-byte aligned,
- * row_stride a multiple of 4. */
+ * row_stride a multiple of 4. shared_output_gate is the fp32 [H] main_grad of
+ * the shared expert's output gate: required (16-byte aligned) when the forward
+ * recorded in `saved` had a gate, ignored otherwise. */
 typedef struct {
     float *shared_gate, *shared_up, *shared_down, *routed_gate, *routed_up, *routed_down;
     int64_t strides[6][2];
+    float* shared_output_gate;
 } moe_main_grads;
 
 typedef struct moe_handle moe_handle;
@@ -120,7 +136,8 @@ moe_status moe_saved_size(const moe_config* cfg, size_t* bytes);
 moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved** out);
 void moe_saved_destroy(moe_saved* s);
 
-/* Forward: out[T,H] = SharedSwiGLU(hidden) + sum_s pp[t,s] * RoutedSwiGLU_{ids[t,s]}(hidden)
+/* Forward: out[T,H] = gate[t] * SharedSwiGLU(hidden) + sum_s pp[t,s] * RoutedSwiGLU_{ids[t,s]}(hidden),
+ * gate[t] = sigmoid(hidden[t] . w->shared_output_gate) (1 without a gate)
  * ("core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward;
  * PR #6572 Summary: dispatch, routed and shared experts, combine).
  *   hidden[T,H] bf16, probs[T,E] fp32, routing_map[T,E] bytes (0/1, e.g.
@@ -142,7 +159,10 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
  *   grad_out[T,H] bf16 -> dhidden[T,H] bf16, dprobs[T,E] fp32 (dense: every
  *   element written; 0 where the map is false), and main_grad += dW for all
  *   six buffers, in fp32, one add per element (deterministic). Experts that
- *   received no tokens keep their main_grad bitwise. `saved` is not consumed. */
+ *   received no tokens keep their main_grad bitwise. `saved` is not consumed.
+ *   With a shared output gate, also main_grad_gate[h] += sum_t dz[t] hidden[t,h]
+ *   and dhidden[t] += dz[t] w, dz[t] = gate[t] (1 - gate[t]) <grad_out[t], y_shared[t]>
+ *   (y_shared before the gate), in fp32 with a fixed summation order. */
 moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved,
                         void* dhidden, float* dprobs, const moe_main_grads* mg, void* stream);
 
@@ -212,7 +232,7 @@ enum {
     MOE_K_FWD_GU_ROUTED, MOE_K_FWD_GU_SHARED, MOE_K_FWD_DOWN_ROUTED, MOE_K_FWD_DOWN_SHARED, MOE_K_COMBINE,
     MOE_K_BWD_DOWN_ROUTED, MOE_K_BWD_DOWN_SHARED, MOE_K_BWD_GU_ROUTED, MOE_K_BWD_GU_SHARED,
     MOE_K_WGRAD_FC1_ROUTED, MOE_K_WGRAD_DOWN_ROUTED, MOE_K_WGRAD_FC1_SHARED, MOE_K_WGRAD_DOWN_SHARED,
-    MOE_K_UNPERMUTE, MOE_K_COUNT
+    MOE_K_UNPERMUTE, MOE_K_SHARED_GATE_FWD, MOE_K_SHARED_GATE_BWD, MOE_K_COUNT
 };
 
 /* Per-kernel timing for measurement. While enabled, every kernel the handle

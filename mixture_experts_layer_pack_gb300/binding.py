@@ -31,11 +31,12 @@ class moe_wview(ctypes.Structure):
 
 
 class moe_weights(ctypes.Structure):
-    _fields_ = [(n, moe_wview) for n in WEIGHT_NAMES]
+    _fields_ = [(n, moe_wview) for n in WEIGHT_NAMES] + [("shared_output_gate", c_void_p)]
 
 
 class moe_main_grads(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in WEIGHT_NAMES] + [("strides", (c_int64 * 2) * 6)]
+    _fields_ = ([(n, c_void_p) for n in WEIGHT_NAMES] + [("strides", (c_int64 * 2) * 6)] +
+                [("shared_output_gate", c_void_p)])
 
 
 class MoeError(RuntimeError):
@@ -50,7 +51,7 @@ EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size",
             "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
             "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name",
             "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8")
-MOE_K_COUNT = 18
+MOE_K_COUNT = 20
 
 
 def lib_path() -> str:
@@ -257,19 +258,23 @@ def wview(t, scale=None, col_data=None, col_scale=None) -> moe_wview:
                      None if col_scale is None else col_scale.data_ptr())
 
 
-def weights_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2) -> moe_weights:
-    """Gate/up views of combined FC1 weights ([2I,H], [E,2I,H]): rows [0,I) gate, [I,2I) up."""
+def weights_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, shared_output_gate=None) -> moe_weights:
+    """Gate/up views of combined FC1 weights ([2I,H], [E,2I,H]): rows [0,I) gate, [I,2I) up;
+    optional bf16 [H] shared-expert output gate."""
     inter = shared_fc1.shape[0] // 2
     return moe_weights(wview(shared_fc1[:inter]), wview(shared_fc1[inter:]), wview(shared_fc2),
-                       wview(routed_fc1[:, :inter]), wview(routed_fc1[:, inter:]), wview(routed_fc2))
+                       wview(routed_fc1[:, :inter]), wview(routed_fc1[:, inter:]), wview(routed_fc2),
+                       None if shared_output_gate is None else shared_output_gate.data_ptr())
 
 
-def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2) -> moe_main_grads:
-    """Six-buffer main_grad order over combined FC1/FC2 fp32 buffers."""
+def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, shared_output_gate=None) -> moe_main_grads:
+    """Six-buffer main_grad order over combined FC1/FC2 fp32 buffers (plus the
+    optional fp32 [H] main_grad of the shared-expert output gate)."""
     inter = shared_fc1.shape[0] // 2
     views = (shared_fc1[:inter], shared_fc1[inter:], shared_fc2,
              routed_fc1[:, :inter], routed_fc1[:, inter:], routed_fc2)
     m = moe_main_grads(*[v.data_ptr() for v in views])
+    m.shared_output_gate = None if shared_output_gate is None else shared_output_gate.data_ptr()
     for i, v in enumerate(views):
         if v.dim() == 3:
             m.strides[i][0], m.strides[i][1] = v.stride(0), v.stride(1)
@@ -281,9 +286,10 @@ def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2) -> 
 class MoELayer:
     """Holds a handle, its workspace and one saved-state block (all torch device memory)."""
 
-    def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16):
+    def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16,
+                 swiglu_limit=0.0):
         import torch
-        self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, 0.0)
+        self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, float(swiglu_limit))
         self.device = torch.device(device)
         ws = moe_workspace_size(self.cfg)
         sv = moe_saved_size(self.cfg)

@@ -79,13 +79,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     }
 }
 
-// dhidden[t] = dx_shared[t] + sum over valid slots of dx_perm[row_of[t,s]];
+// dhidden[t] = dx_shared[t] (+ dz[t] w, the shared output gate's term) + sum
+// over valid slots of dx_perm[row_of[t,s]];
 // dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map
 __global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict__ dxs, const float4* __restrict__ dxp,
                                                         const int* __restrict__ row_of, const int* __restrict__ ids,
                                                         const float* __restrict__ partial, int n_part, int T,
-                                                        int vec_per_row, int k, int E, uint4* __restrict__ dhidden,
-                                                        float* __restrict__ dprobs) {
+                                                        int vec_per_row, int k, int E, const float* __restrict__ dz,
+                                                        const uint4* __restrict__ gate_w,
+                                                        uint4* __restrict__ dhidden, float* __restrict__ dprobs) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     const int64_t total = int64_t(T) * vec_per_row;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += stride) {
@@ -93,6 +95,17 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         add_f32x8(acc, dxs + 2 * i);
+        if (dz) {
+            const float d = __ldg(dz + t);
+            const uint4 wv = __ldg(gate_w + v);
+            float wf[8];
+            unpack_bf16x2(wv.x, wf[0], wf[1]);
+            unpack_bf16x2(wv.y, wf[2], wf[3]);
+            unpack_bf16x2(wv.z, wf[4], wf[5]);
+            unpack_bf16x2(wv.w, wf[6], wf[7]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(d, wf[j], acc[j]);
+        }
         for (int s = 0; s < k; ++s) {
             const int r = __ldg(row_of + int64_t(t) * k + s);
             if (r >= 0) add_f32x8(acc, dxp + 2 * (int64_t(r) * vec_per_row + v));
@@ -144,13 +157,15 @@ cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, i
 }
 
 cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
-                             const float* partial, int n_part, int T, int H, int k, int E, __nv_bfloat16* dhidden,
-                             float* dprobs, int num_sms, cudaStream_t st) {
+                             const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
+                             const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, int num_sms,
+                             cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
     unpermute_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(dxs), reinterpret_cast<const float4*>(dxp),
-                                            row_of, ids, partial, n_part, T, H / 8, k, E,
-                                            reinterpret_cast<uint4*>(dhidden), dprobs);
+                                            row_of, ids, partial, n_part, T, H / 8, k, E, dz,
+                                            reinterpret_cast<const uint4*>(gate_w), reinterpret_cast<uint4*>(dhidden),
+                                            dprobs);
     count_launch();
     return cudaGetLastError();
 }

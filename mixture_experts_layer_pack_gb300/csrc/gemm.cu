@@ -178,7 +178,7 @@ __device__ __forceinline__ uint32_t mx_quant_lane4(const float (&v)[4], uint32_t
     return e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
 }
 
-template <int OP, int BN, bool MX = false>
+template <int OP, int BN, bool MX = false, bool CLAMP = false>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int q, int half, const GemmArgs& a,
                                               float* staging) {
     const int lane = threadIdx.x & 31;
@@ -212,8 +212,17 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             for (int i = 0; i < 8; ++i) {
                 const int row = m_base + i * 4 + sub_row;
                 const float4 g4 = gv[i], u4 = uv[i];
-                float av[4] = {g4.x * sigmoidf_(g4.x) * u4.x, g4.y * sigmoidf_(g4.y) * u4.y,
-                               g4.z * sigmoidf_(g4.z) * u4.z, g4.w * sigmoidf_(g4.w) * u4.w};
+                float gc[4] = {g4.x, g4.y, g4.z, g4.w}, uc[4] = {u4.x, u4.y, u4.z, u4.w};
+                if (CLAMP) {  // clamped SwiGLU inputs; g, u are saved unclamped
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) {
+                        gc[z] = fminf(gc[z], a.swiglu_limit);
+                        uc[z] = fminf(fmaxf(uc[z], -a.swiglu_limit), a.swiglu_limit);
+                    }
+                }
+                float av[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) av[z] = gc[z] * sigmoidf_(gc[z]) * uc[z];
                 if (MX) {
                     // the down projection's operand: a quantised along I (this chunk is one
                     // 32-column block); a itself becomes its exact dequantised value
@@ -305,10 +314,18 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
                     part[i] = fmaf(av[z], dv[z], part[i]);
-                    const float sg = sigmoidf_(gv[z]);
+                    float g = gv[z], u = uv[z], mg = 1.0f, mu = 1.0f;
+                    if (CLAMP) {  // gradients pass only where the clamp is inactive
+                        const float L = a.swiglu_limit;
+                        mg = g <= L ? 1.0f : 0.0f;
+                        mu = (u >= -L && u <= L) ? 1.0f : 0.0f;
+                        g = fminf(g, L);
+                        u = fminf(fmaxf(u, -L), L);
+                    }
+                    const float sg = sigmoidf_(g);
                     const float da = p * dv[z];
-                    dg[z] = da * uv[z] * (sg * (1.0f + gv[z] * (1.0f - sg)));
-                    du[z] = da * (gv[z] * sg);
+                    dg[z] = da * u * (sg * (1.0f + g * (1.0f - sg))) * mg;
+                    du[z] = da * (g * sg) * mu;
                     ap[z] = p * av[z];
                 }
                 if (MX) {
@@ -470,7 +487,7 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
     __syncwarp();
 }
 
-template <int OP, int BN>
+template <int OP, int BN, bool CLAMP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
@@ -630,7 +647,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 __syncwarp();
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-                epilogue_tile<OP, BN>(t, t_row, q, half, args, my_staging);
+                epilogue_tile<OP, BN, false, CLAMP>(t, t_row, q, half, args, my_staging);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -700,7 +717,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-template <int OP>
+template <int OP, bool CLAMP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
@@ -862,7 +879,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            epilogue_tile<OP, BN, true>(t, t_row, q, half, args, my_staging);
+            epilogue_tile<OP, BN, true, CLAMP>(t, t_row, q, half, args, my_staging);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -876,10 +893,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int OP>
+template <int OP, bool CLAMP>
 cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     static bool attr_set = false;
-    auto kern = moe_gemm_mx_kernel<OP>;
+    auto kern = moe_gemm_mx_kernel<OP, CLAMP>;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(MxCfg::SMEM));
         if (e != cudaSuccess) return e;
@@ -890,10 +907,10 @@ cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaSt
     return cudaGetLastError();
 }
 
-template <int OP, int BN>
+template <int OP, int BN, bool CLAMP>
 cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     static bool attr_set = false;
-    auto kern = moe_gemm_kernel<OP, BN>;
+    auto kern = moe_gemm_kernel<OP, BN, CLAMP>;
     if (!attr_set) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<OP, BN>::SMEM));
@@ -905,12 +922,12 @@ cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStrea
     return cudaGetLastError();
 }
 
-template <int OP>
+template <int OP, bool CLAMP = false>
 cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     switch (bn) {
-        case 256: return launch_one<OP, 256>(m, a, grid, st);
-        case 128: return launch_one<OP, 128>(m, a, grid, st);
-        case 64: return launch_one<OP, 64>(m, a, grid, st);
+        case 256: return launch_one<OP, 256, CLAMP>(m, a, grid, st);
+        case 128: return launch_one<OP, 128, CLAMP>(m, a, grid, st);
+        case 64: return launch_one<OP, 64, CLAMP>(m, a, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -919,11 +936,17 @@ cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cu
 
 cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     if (grid <= 0) return cudaSuccess;
+    const bool clamp = a.swiglu_limit > 0.0f;
     switch (op) {
-        case OP_FWD_GU: return launch_mx_one<OP_FWD_GU>(m, a, grid, st);
-        case OP_FWD_DOWN: return launch_mx_one<OP_FWD_DOWN>(m, a, grid, st);
-        case OP_BWD_DOWN: return launch_mx_one<OP_BWD_DOWN>(m, a, grid, st);
-        case OP_BWD_GU: return launch_mx_one<OP_BWD_GU>(m, a, grid, st);
+        // the SwiGLU epilogues come in a clamped and an unclamped build
+        case OP_FWD_GU:
+            return clamp ? launch_mx_one<OP_FWD_GU, true>(m, a, grid, st)
+                         : launch_mx_one<OP_FWD_GU, false>(m, a, grid, st);
+        case OP_FWD_DOWN: return launch_mx_one<OP_FWD_DOWN, false>(m, a, grid, st);
+        case OP_BWD_DOWN:
+            return clamp ? launch_mx_one<OP_BWD_DOWN, true>(m, a, grid, st)
+                         : launch_mx_one<OP_BWD_DOWN, false>(m, a, grid, st);
+        case OP_BWD_GU: return launch_mx_one<OP_BWD_GU, false>(m, a, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -943,10 +966,14 @@ int pick_bn(int64_t n, bool split_gate_up) {
 
 cudaError_t launch_gemm(int op, int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     if (grid <= 0) return cudaSuccess;
+    const bool clamp = a.swiglu_limit > 0.0f;
     switch (op) {
-        case OP_FWD_GU: return launch_bn<OP_FWD_GU>(bn, m, a, grid, st);
+        case OP_FWD_GU:
+            return clamp ? launch_bn<OP_FWD_GU, true>(bn, m, a, grid, st) : launch_bn<OP_FWD_GU>(bn, m, a, grid, st);
         case OP_FWD_DOWN: return launch_bn<OP_FWD_DOWN>(bn, m, a, grid, st);
-        case OP_BWD_DOWN: return launch_bn<OP_BWD_DOWN>(bn, m, a, grid, st);
+        case OP_BWD_DOWN:
+            return clamp ? launch_bn<OP_BWD_DOWN, true>(bn, m, a, grid, st)
+                         : launch_bn<OP_BWD_DOWN>(bn, m, a, grid, st);
         case OP_BWD_GU: return launch_bn<OP_BWD_GU>(bn, m, a, grid, st);
         case OP_WGRAD: return launch_bn<OP_WGRAD>(bn, m, a, grid, st);
         default: return cudaErrorInvalidValue;

@@ -56,6 +56,7 @@ struct GemmArgs {
     float* partial;             // per row: n_tiles * kEpiHalves partial dot products (null: skip)
     int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
     int inter;
+    float swiglu_limit;         // > 0: SwiGLU inputs clamped, g <= L, |u| <= L (FWD_GU, BWD_DOWN epilogues)
     int* status;
     // MXFP8 (block-scaled) GEMMs
     uint8_t* q_out;             // E4M3 copy of the epilogue's GEMM-operand output (a, or [dg|du])
@@ -112,8 +113,16 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, co
 cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
                            __nv_bfloat16* out, int num_sms, cudaStream_t st);
 cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
-                             const float* partial, int n_part, int T, int H, int k, int E, __nv_bfloat16* dhidden,
-                             float* dprobs, int num_sms, cudaStream_t st);
+                             const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
+                             const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, int num_sms,
+                             cudaStream_t st);
+
+// shared-expert output gate
+constexpr int kGateChunk = 128;  // tokens per partial sum of the gate weight's gradient
+cudaError_t launch_gate_forward(const __nv_bfloat16* hidden, const __nv_bfloat16* w, int T, int H, float* gate,
+                                cudaStream_t st);
+cudaError_t launch_gate_backward(const __nv_bfloat16* hidden, const float* gate, const float* partial, int n_part,
+                                 int T, int H, float* dz, float* gpart, float* mg_gate, cudaStream_t st);
 
 void count_launch(int n = 1);
 

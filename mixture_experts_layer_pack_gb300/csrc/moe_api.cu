@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -29,7 +30,9 @@ struct Shape {
     int64_t rows;     // permuted rows incl. padding, worst case
     int bn_gu, bn_down, bn_bd, bn_bgu, bn_wfc1, bn_wd;
     int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM x epilogue halves)
+    int n_part_s;     // the same for the shared expert's (always BF16) dgrad-down GEMM
     bool mx;          // routed weights MXFP8: block-scaled fprop and dgrad GEMMs
+    float limit;      // swiglu_limit (0: none)
 };
 
 // carves consecutive 256-byte aligned pieces out of one block
@@ -49,7 +52,8 @@ moe_status check_config(const moe_config* c, Shape* s) {
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->max_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->topk <= 0 || c->inter <= 0)
         return MOE_ERR_INVALID_ARG;
-    if (c->swiglu_limit != 0.0f) return MOE_ERR_UNSUPPORTED;
+    if (!(c->swiglu_limit >= 0.0f) || !std::isfinite(c->swiglu_limit)) return MOE_ERR_INVALID_ARG;
+    s->limit = c->swiglu_limit;
     if (c->routed_wtype != MOE_W_BF16 && c->routed_wtype != MOE_W_MXFP8) return MOE_ERR_UNSUPPORTED;
     s->mx = c->routed_wtype == MOE_W_MXFP8;
     if (s->mx && (c->hidden % 128 || c->inter % 128)) return MOE_ERR_UNSUPPORTED;
@@ -71,6 +75,7 @@ moe_status check_config(const moe_config* c, Shape* s) {
     s->bn_wd = pick_bn(s->I, false);
     if (!s->bn_gu || !s->bn_down || !s->bn_bd || !s->bn_bgu || !s->bn_wfc1 || !s->bn_wd) return MOE_ERR_UNSUPPORTED;
     s->n_part = int(s->I / (s->mx ? kMxBN : s->bn_bd)) * kEpiHalves;
+    s->n_part_s = int(s->I / s->bn_bd) * kEpiHalves;
     return MOE_OK;
 }
 
@@ -80,6 +85,10 @@ struct Workspace {
     __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
     float *yx, *ys_dxs;  // forward: p*y (routed rows), y_shared; backward: dx (routed rows), dx_shared
     float* partial;
+    // shared output gate: the shared rows' dprob partials, dz, chunk sums of the
+    // gate weight's gradient, gate * a_shared (the gated down wgrad operand)
+    float *partial_s, *dz, *gpart;
+    __nv_bfloat16* ap_s;
     // MXFP8 only: quantised backward operands and the swizzled weight scales
     uint8_t *go_q, *go_sf, *dgdu_q, *dgdu_sf;
     uint8_t *sf_fc1_row, *sf_down_row, *sf_down_col, *sf_fc1_col;
@@ -88,6 +97,7 @@ struct Workspace {
 struct SavedBufs {
     int *ids, *row_of, *counts, *offsets, *offs_pad, *meta, *mtile_expert, *perm_src;
     float *pp, *pp_perm;
+    float* gate;  // shared output gate per token
     __nv_bfloat16 *x_perm, *a, *a_s;
     float *gu, *gu_s;
     uint8_t *x_q, *x_sf, *a_q, *a_sf;  // MXFP8 only
@@ -107,6 +117,10 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->partial = c.take<float>(size_t(s.rows) * s.n_part);
     w->ys_dxs = c.take<float>(size_t(s.Tmax) * s.H);
     w->dgdu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
+    w->partial_s = c.take<float>(size_t(s.Tmax) * s.n_part_s);
+    w->dz = c.take<float>(size_t(s.Tmax));
+    w->gpart = c.take<float>(size_t((s.Tmax + kGateChunk - 1) / kGateChunk) * s.H);
+    w->ap_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
     if (s.mx) {
         w->go_q = c.take<uint8_t>(size_t(s.rows) * s.H);
         w->go_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -136,6 +150,7 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->mtile_expert = c.take<int>(s.rows / kBM);
     b->perm_src = c.take<int>(s.rows);
     b->pp_perm = c.take<float>(s.rows);
+    b->gate = c.take<float>(size_t(s.Tmax));
     b->x_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     b->a = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
     b->gu = c.take<float>(size_t(s.rows) * 2 * s.I);
@@ -247,12 +262,13 @@ bool map_weight(CUtensorMap* m, const moe_wview& v, int64_t E, int64_t rows, int
     return encode_map(m, v.data, 3, dims, strides, box);
 }
 
-GemmArgs base_args(int* status, int inter) {
+GemmArgs base_args(int* status, const Shape& s) {
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     a.rows_valid = INT_MAX;
     a.m_split = INT_MAX;
-    a.inter = inter;
+    a.inter = int(s.I);
+    a.swiglu_limit = s.limit;
     a.status = status;
     return a;
 }
@@ -317,7 +333,7 @@ const char* const kKernelNames[MOE_K_COUNT] = {
     "gemm_fwd_gu_routed", "gemm_fwd_gu_shared", "gemm_fwd_down_routed", "gemm_fwd_down_shared", "combine",
     "gemm_bwd_down_routed", "gemm_bwd_down_shared", "gemm_bwd_gu_routed", "gemm_bwd_gu_shared",
     "gemm_wgrad_fc1_routed", "gemm_wgrad_down_routed", "gemm_wgrad_fc1_shared", "gemm_wgrad_down_shared",
-    "unpermute"};
+    "unpermute", "shared_gate_fwd", "shared_gate_bwd"};
 
 }  // namespace
 
@@ -328,6 +344,7 @@ struct moe_saved {
     const void* hidden;
     moe_weights w;
     bool valid;
+    bool gated;  // the forward had a shared output gate
 };
 
 extern "C" {
@@ -434,6 +451,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         return MOE_ERR_INVALID_ARG;
     const bool mx = s.mx;
     if (mx && !h->weights_prepared) return MOE_ERR_STATE;
+    const bool gated = w->shared_output_gate != nullptr;
+    if (gated && !aligned16(w->shared_output_gate)) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const SavedBufs& b = saved->b;
     const Workspace& ws = h->ws;
@@ -441,6 +460,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     saved->hidden = hidden;
     saved->w = *w;
     saved->valid = true;
+    saved->gated = gated;
     if (T == 0) return MOE_OK;
 
     const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
@@ -460,7 +480,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     GemmMaps m;
     // routed gate/up + SwiGLU
     if (mx) {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.x_q, rows, H, H) ||
             !map_u8_weight(&m.b0, w->routed_gate.data, w->routed_gate, E, I, H, kMxBN / 2) ||
             !map_u8_weight(&m.b1, w->routed_up.data, w->routed_up, E, I, H, kMxBN / 2))
@@ -488,7 +508,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         MOE_CU(launch_gemm_mx(OP_FWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     } else
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
         if (!map_kmajor(&m.a, b.x_perm, rows, H, H) || !map_weight(&m.b0, w->routed_gate, E, I, H, 64, bn / 2) ||
             !map_weight(&m.b1, w->routed_up, E, I, H, 64, bn / 2))
@@ -508,7 +528,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     }
     // shared gate/up + SwiGLU
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
         if (!map_kmajor(&m.a, hidden, Ti, H, H) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, bn / 2) ||
             !map_weight(&m.b1, w->shared_up, 1, I, H, 64, bn / 2))
@@ -527,7 +547,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     }
     // routed down projection, scaled by the route's prob
     if (mx) {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.a_q, rows, I, I) ||
             !map_u8_weight(&m.b0, w->routed_down.data, w->routed_down, E, H, I, kMxBN))
             return MOE_ERR_INVALID_ARG;
@@ -549,7 +569,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         MOE_CU(launch_gemm_mx(OP_FWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     } else
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
         if (!map_kmajor(&m.a, b.a, rows, I, I) || !map_weight(&m.b0, w->routed_down, E, H, I, 64, bn))
             return MOE_ERR_INVALID_ARG;
@@ -565,9 +585,15 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
+    // shared output gate: gate[t] = sigmoid(hidden[t] . w), scales the shared down projection
+    if (gated) {
+        Timed tm_(h, MOE_K_SHARED_GATE_FWD, st);
+        MOE_CU(launch_gate_forward(static_cast<const __nv_bfloat16*>(hidden),
+                                   static_cast<const __nv_bfloat16*>(w->shared_output_gate), Ti, H, b.gate, st));
+    }
     // shared down projection
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
         if (!map_kmajor(&m.a, b.a_s, Ti, I, I) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, bn))
             return MOE_ERR_INVALID_ARG;
@@ -578,6 +604,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.rows_valid = Ti;
         a.outf = ws.ys_dxs;
         a.ld_outf = H;
+        a.row_scale = gated ? b.gate : nullptr;
         Timed tm_(h, MOE_K_FWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -592,6 +619,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
     if (!saved->valid) return MOE_ERR_STATE;
     if (!check_mg(mg)) return MOE_ERR_INVALID_ARG;
+    const bool gated = saved->gated;
+    if (gated && (!mg->shared_output_gate || !aligned16(mg->shared_output_gate))) return MOE_ERR_INVALID_ARG;
     const Shape& s = h->s;
     const int64_t T = saved->T;
     if (T == 0) return MOE_OK;
@@ -612,7 +641,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     GemmMaps m;
     // routed dgrad through the down projection + SwiGLU backward + dprob partials
     if (mx) {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, ws.go_q, rows, H, H) ||
             !map_u8_weight(&m.b0, w->routed_down.col_data, w->routed_down, E, H, I, 128))
             return MOE_ERR_INVALID_ARG;
@@ -645,7 +674,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         MOE_CU(launch_gemm_mx(OP_BWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     } else
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
         if (!map_kmajor(&m.a, ws.go_perm, rows, H, H) || !map_weight(&m.b0, w->routed_down, E, H, I, 64, 64))
             return MOE_ERR_INVALID_ARG;
@@ -670,7 +699,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // shared dgrad through the down projection + SwiGLU backward
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
         if (!map_kmajor(&m.a, go, Ti, H, H) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, 64))
             return MOE_ERR_INVALID_ARG;
@@ -685,12 +714,23 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.ld_inf = 2 * I;
         a.out0 = ws.dgdu_s;
         a.ld_out0 = 2 * I;
+        if (gated) {  // the gate acts as the shared rows' prob: dgate partials, gate * a_shared
+            a.row_scale = b.gate;
+            a.partial = ws.partial_s;
+            a.out1 = ws.ap_s;
+            a.ld_out1 = I;
+        }
         Timed tm_(h, MOE_K_BWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
+    if (gated) {
+        Timed tm_(h, MOE_K_SHARED_GATE_BWD, st);
+        MOE_CU(launch_gate_backward(static_cast<const __nv_bfloat16*>(saved->hidden), b.gate, ws.partial_s, s.n_part_s,
+                                    Ti, H, ws.dz, ws.gpart, mg->shared_output_gate, st));
+    }
     // routed dgrad through gate/up
     if (mx) {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, ws.dgdu_q, rows, 2 * I, 2 * I) ||
             !map_u8_weight(&m.b0, w->routed_gate.col_data, w->routed_gate, E, I, H, 128) ||
             !map_u8_weight(&m.b1, w->routed_up.col_data, w->routed_up, E, I, H, 128))
@@ -712,7 +752,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         MOE_CU(launch_gemm_mx(OP_BWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     } else
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
         if (!map_kmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I) || !map_weight(&m.b0, w->routed_gate, E, I, H, 64, 64) ||
             !map_weight(&m.b1, w->routed_up, E, I, H, 64, 64))
@@ -730,7 +770,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // shared dgrad through gate/up
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
         if (!map_kmajor(&m.a, ws.dgdu_s, Ti, 2 * I, 2 * I) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, 64) ||
             !map_weight(&m.b1, w->shared_up, 1, I, H, 64, 64))
@@ -747,7 +787,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // routed wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wfc1;
         if (!map_mnmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I) || !map_mnmajor(&m.b0, b.x_perm, rows, H, H))
             return MOE_ERR_INVALID_ARG;
@@ -765,7 +805,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // routed wgrad of down: main_grad[e] += go_perm_e^T (p a)_e
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wd;
         if (!map_mnmajor(&m.a, ws.go_perm, rows, H, H) || !map_mnmajor(&m.b0, ws.ap, rows, I, I))
             return MOE_ERR_INVALID_ARG;
@@ -782,7 +822,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // shared wgrad of gate/up
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wfc1;
         if (!map_mnmajor(&m.a, ws.dgdu_s, Ti, 2 * I, 2 * I) || !map_mnmajor(&m.b0, saved->hidden, Ti, H, H))
             return MOE_ERR_INVALID_ARG;
@@ -800,9 +840,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // shared wgrad of down
     {
-        GemmArgs a = base_args(ws.status, I);
+        GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wd;
-        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, b.a_s, Ti, I, I)) return MOE_ERR_INVALID_ARG;
+        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, gated ? ws.ap_s : b.a_s, Ti, I, I))
+            return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
         a.seg_len = Ti;
         a.groups = 1;
@@ -816,6 +857,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     // dhidden = shared + un-permuted routed dgrad; dense dprobs
     Timed tm_(h, MOE_K_UNPERMUTE, st);
     MOE_CU(launch_unpermute(ws.ys_dxs, ws.yx, b.row_of, b.ids, ws.partial, s.n_part, Ti, H, k, E,
+                            gated ? ws.dz : nullptr,
+                            gated ? static_cast<const __nv_bfloat16*>(w->shared_output_gate) : nullptr,
                             static_cast<__nv_bfloat16*>(dhidden), dprobs, h->sms, st));
     return MOE_OK;
 }

@@ -172,6 +172,17 @@ def make_main_grads(H: int, I: int, E: int, seed: int, device="cpu", std: float 
     )
 
 
+def make_shared_output_gate(H: int, seed: int, device="cpu", std: float = 0.05):
+    """Shared-expert output gate weight, bf16 [H] ~ N(0, std), and its fp32 [H]
+    main_grad ~ N(0, 1e-3). With hidden ~ N(0,1) the gate logit has std
+    std * sqrt(H) (about 2.3 at H = 2048), so gates spread over (0, 1)."""
+    torch = _torch()
+    g = torch.Generator(device=device).manual_seed(seed + 19)
+    w = _draw_bf16(g, (H,), std, device)
+    mg = torch.randn((H,), generator=g, device=device, dtype=torch.float32) * 1e-3
+    return w, mg
+
+
 def mxfp8_quantize_torch(w, axis):
     """MXFP8 input weights from bf16 masters with PyTorch ops (float8_e4m3fn cast):
     blocks of 32 along ``axis`` (-1: along K, the row; -2: down the rows),

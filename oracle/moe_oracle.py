@@ -25,6 +25,16 @@ What the layer computes (sources, by page and section):
 * "core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward:
   out = layer(hidden[T,H], probs[T,E], routing_map[T,E]) with hidden's shape.
 
+Two optional inputs the pages name without a formula, read as follows:
+
+* ``swiglu_limit`` ("Add Mixture-of-Kittens MoE backend on main", review thread
+  on the backend's swiglu_limit = the layer's activation clamp value): L > 0
+  clamps the SwiGLU inputs of every expert, a = silu(min(g, L)) * clip(u, -L, L);
+  the gradient passes where the clamp is inactive, bounds included.
+* the shared expert's output gate ("core.transformer.moe.megakernel.mok.runtime",
+  _MoKAutograd.forward: shared_output_gate_weight): a per-token scalar
+  gate[t] = sigmoid(x_t . w) multiplies the shared expert's output.
+
 Readings where the pages are silent (each also listed in the design notes):
 the expert is a SwiGLU MLP, a = silu(x W_g^T) * (x W_u^T), y = a W_d^T with
 silu(z) = z / (1 + e^-z); the prob weights the expert output after the down
@@ -72,9 +82,12 @@ class RoutingError(ValueError):
 class DenseWeights:
     """fp64 weights held in memory: Wg, Wu [I,H] (per expert [E,I,H]), Wd [H,I]."""
 
-    def __init__(self, shared_gate, shared_up, shared_down, routed_gate, routed_up, routed_down):
+    def __init__(self, shared_gate, shared_up, shared_down, routed_gate, routed_up, routed_down,
+                 shared_output_gate=None):
         self.sg, self.su, self.sd = (np.asarray(a, np.float64) for a in (shared_gate, shared_up, shared_down))
         self.rg, self.ru, self.rd = (np.asarray(a, np.float64) for a in (routed_gate, routed_up, routed_down))
+        # optional [H] output gate of the shared expert (None: ungated)
+        self.shared_output_gate = None if shared_output_gate is None else np.asarray(shared_output_gate, np.float64)
 
     @classmethod
     def from_combined(cls, shared_fc1, shared_fc2, routed_fc1, routed_fc2):
@@ -238,29 +251,42 @@ def silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def expert_forward(x, Wg, Wu, Wd, ops=None):
+def clamp_inputs(g, u, limit):
+    """SwiGLU inputs after the swiglu_limit clamp (limit 0: unclamped) and the
+    masks where the gradient passes: min(g, L), clip(u, -L, L), g <= L, |u| <= L."""
+    if not limit:
+        one = np.ones_like(g)
+        return g, u, one, one
+    return (np.minimum(g, limit), np.clip(u, -limit, limit), (g <= limit).astype(np.float64),
+            ((u >= -limit) & (u <= limit)).astype(np.float64))
+
+
+def expert_forward(x, Wg, Wu, Wd, ops=None, limit=0.0):
     """SwiGLU expert on rows x[n,H]: g = x Wg^T, u = x Wu^T, a = silu(g) u, y = a Wd^T
-    (``ops`` holds the GEMM operands x and a at the GEMM precision)."""
+    (``ops`` holds the GEMM operands x and a at the GEMM precision; ``limit`` the
+    swiglu_limit clamp of g and u). Returns the unclamped g, u."""
     ops = ops or Operands("exact")
     xq = ops.x(x)
     g = xq @ Wg.T
     u = xq @ Wu.T
-    a = ops.a(silu(g) * u)
+    gc, uc, _, _ = clamp_inputs(g, u, limit)
+    a = ops.a(silu(gc) * uc)
     y = a @ Wd.T
     return g, u, a, y
 
 
-def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, ops=None):
+def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, ops=None, limit=0.0):
     """Gradients of sum(go * (p y)) for one expert, p[n] the rows' probs, with the
     dgrad weights Wg, Wu, Wd: returns dx, dWg, dWu, dWd and dprob[n] =
     sum_i a_i (go Wd)_i (= <go, y> in exact arithmetic). ``ops`` holds every
     GEMM operand (go, [dg|du], and the weight-gradient operands dg, du, p*a)
-    at its GEMM's precision."""
+    at its GEMM's precision; g, u are the unclamped SwiGLU inputs."""
     ops = ops or Operands("exact")
+    gc, uc, mg, mu = clamp_inputs(g, u, limit)
     da_u = ops.go(go) @ Wd
     da = p[:, None] * da_u
-    dg = da * u * silu_grad(g)
-    du = da * silu(g)
+    dg = da * uc * silu_grad(gc) * mg
+    du = da * silu(gc) * mu
     dgq, duq = ops.dgdu(dg, du)
     dx = dgq @ Wg + duq @ Wu
     dgw, duw = ops.wgrad(dg), ops.wgrad(du)
@@ -271,8 +297,9 @@ def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, ops=None):
 # --------------------------------------------------------------------------
 # the layer
 # --------------------------------------------------------------------------
-def forward(hidden, probs, routing_map, W, k, precision="exact"):
-    """out[T,H] = SwiGLU_shared(x) + sum over valid slots s of pp[t,s] * SwiGLU_{ids[t,s]}(x).
+def forward(hidden, probs, routing_map, W, k, precision="exact", swiglu_limit=0.0):
+    """out[T,H] = gate[t] SwiGLU_shared(x) + sum over valid slots s of pp[t,s] * SwiGLU_{ids[t,s]}(x),
+    gate[t] = sigmoid(x_t . w) with the shared output gate w (1 without it).
 
     "core.transformer.moe.megakernel.mok.backend", MoKMegakernel.forward, and PR
     #6572 Summary (dispatch, routed and shared experts, combine). Returns
@@ -286,7 +313,12 @@ def forward(hidden, probs, routing_map, W, k, precision="exact"):
     E = W.num_experts
     counts, offsets, perm_src, perm_slot, row_of = dispatch_indices(ids, E)
 
-    gs, us, as_, ys = expert_forward(x, *W.shared(), ops=shared_ops)
+    gs, us, as_, ys = expert_forward(x, *W.shared(), ops=shared_ops, limit=swiglu_limit)
+    w_gate = getattr(W, "shared_output_gate", None)
+    gate = None
+    if w_gate is not None:
+        gate = sigmoid(x @ w_gate)
+        ys = gate[:, None] * ys
 
     R = perm_src.size
     y = np.zeros((R, H))
@@ -296,7 +328,7 @@ def forward(hidden, probs, routing_map, W, k, precision="exact"):
         if hi == lo:
             continue
         xe = x[perm_src[lo:hi]]
-        g, u, a, ye = expert_forward(xe, *W.routed(e), ops=routed_ops)
+        g, u, a, ye = expert_forward(xe, *W.routed(e), ops=routed_ops, limit=swiglu_limit)
         y[lo:hi] = ye
         routed[e] = (g, u, a)
 
@@ -307,7 +339,7 @@ def forward(hidden, probs, routing_map, W, k, precision="exact"):
 
     cache = dict(x=x, ids=ids, pp=pp, counts=counts, offsets=offsets, perm_src=perm_src,
                  perm_slot=perm_slot, row_of=row_of, shared=(gs, us, as_), y=y, routed=routed, k=k,
-                 precision=precision)
+                 precision=precision, limit=swiglu_limit, gate=gate)
     return out, cache
 
 
@@ -326,8 +358,16 @@ def backward(grad_out, cache, W):
     T, H = x.shape
     E = W.num_experts
 
+    limit, gate = cache["limit"], cache["gate"]
     gs, us, as_ = cache["shared"]
-    dx_s, dWsg, dWsu, dWsd, _ = expert_backward(x, go, np.ones(T), gs, us, as_, *W.shared(), ops=shared_ops)
+    p_s = np.ones(T) if gate is None else gate
+    dx_s, dWsg, dWsu, dWsd, dgate = expert_backward(x, go, p_s, gs, us, as_, *W.shared(), ops=shared_ops,
+                                                    limit=limit)
+    dW_gate = None
+    if gate is not None:                      # d/dz of gate * y_s, z = x . w
+        dz = gate * (1.0 - gate) * dgate
+        dx_s = dx_s + dz[:, None] * W.shared_output_gate[None, :]
+        dW_gate = x.T @ dz
 
     R = perm_src.size
     dx_perm = np.zeros((R, H))
@@ -338,7 +378,7 @@ def backward(grad_out, cache, W):
         lo, hi = offsets[e], offsets[e + 1]
         go_e = go[perm_src[lo:hi]]
         dx, dWg, dWu, dWd, dprob_perm[lo:hi] = expert_backward(x[perm_src[lo:hi]], go_e, pp_perm[lo:hi], g, u, a,
-                                                              *W.routed_dgrad(e), ops=routed_ops)
+                                                              *W.routed_dgrad(e), ops=routed_ops, limit=limit)
         dx_perm[lo:hi] = dx
         routed_grads[e] = (dWg, dWu, dWd)
 
@@ -350,6 +390,8 @@ def backward(grad_out, cache, W):
         dprobs[np.flatnonzero(v), ids[v, s]] = dprob_perm[row_of[v, s]]
 
     grads = dict(shared_gate=dWsg, shared_up=dWsu, shared_down=dWsd, routed=routed_grads)
+    if dW_gate is not None:
+        grads["shared_output_gate"] = dW_gate
     return dhidden, dprobs, grads
 
 
@@ -362,6 +404,8 @@ def accumulate_main_grads(main_grads, grads):
     out["shared_gate"] += grads["shared_gate"]
     out["shared_up"] += grads["shared_up"]
     out["shared_down"] += grads["shared_down"]
+    if "shared_output_gate" in grads:
+        out["shared_output_gate"] += grads["shared_output_gate"]
     for e, (dWg, dWu, dWd) in grads["routed"].items():
         out["routed_gate"][e] += dWg
         out["routed_up"][e] += dWu
@@ -405,21 +449,27 @@ def mxfp8_alternative(v, band):
     return alt.reshape(shp)
 
 
-def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed):
+def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_band=None):
     """Envelopes of one expert's results for rows x[n,H] with probs p[n]. Wf are
-    the forward weights (Wg, Wu, Wd), Wb the dgrad weights. Returns env_y [n,H],
-    env_dx [n,H], env_dWg [I,H], env_dWu [I,H], env_dWd [H,I], env_dprob [n]."""
+    the forward weights (Wg, Wu, Wd), Wb the dgrad weights; ``limit`` the
+    swiglu_limit clamp; ``p_band`` a bound on the kernel's error in p (the
+    shared output gate, which the kernel evaluates in fp32; None: p is exact).
+    Returns env_y [n,H], env_dx [n,H], env_dWg [I,H], env_dWu [I,H],
+    env_dWd [H,I], env_dprob [n]."""
     ops = Operands(precision, routed)
     Wg, Wu, Wd = Wf
     Bg, Bu, Bd = Wb
     xq = ops.x(x)
     H = x.shape[1]
     I = g.shape[1]
+    p_band = np.zeros_like(p) if p_band is None else p_band
     dg_band = fp32_dot_band((xq * xq) @ (Wg * Wg).T, H)          # |g_fp32 - g|
     du_band = fp32_dot_band((xq * xq) @ (Wu * Wu).T, H)
-    s1 = silu_grad(g)
-    a_val = silu(g) * u
-    band_a = np.abs(s1 * u) * dg_band + np.abs(silu(g)) * du_band + ELEMENTWISE_BAND * np.abs(a_val)
+    gc, uc, mg, mu = clamp_inputs(g, u, limit)
+    s1 = silu_grad(gc)
+    a_val = silu(gc) * uc
+    # a is continuous across the clamp bounds: the unmasked slopes bound it on both sides
+    band_a = np.abs(s1 * uc) * dg_band + np.abs(silu(gc)) * du_band + ELEMENTWISE_BAND * np.abs(a_val)
     alt_a = mxfp8_alternative(a_val, band_a) if ops.mx else bf16_alternative(a_val, band_a)
     env_y = alt_a @ np.abs(Wd).T
     a_b = ops.a(a_val)
@@ -428,17 +478,26 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed):
     da_u = goq @ Bd
     env_dprob = np.sum(alt_a * np.abs(da_u), axis=1)
     da = p[:, None] * da_u
-    dda = np.abs(p)[:, None] * fp32_dot_band((goq * goq) @ (Bd * Bd), H)
-    dg_val = da * u * s1
-    du_val = da * silu(g)
-    band_dg = (np.abs(u * s1) * dda + np.abs(da * s1) * du_band +
-               np.abs(da * u) * silu_grad2_bound() * dg_band + ELEMENTWISE_BAND * np.abs(dg_val))
-    band_du = np.abs(silu(g)) * dda + np.abs(da * s1) * dg_band + ELEMENTWISE_BAND * np.abs(du_val)
-    alt_dg = bf16_alternative(dg_val, band_dg)            # weight-gradient operands (bf16)
-    alt_du = bf16_alternative(du_val, band_du)
+    dda = (np.abs(p)[:, None] * fp32_dot_band((goq * goq) @ (Bd * Bd), H) +
+           p_band[:, None] * np.abs(da_u))
+    dg_val = da * uc * s1 * mg
+    du_val = da * silu(gc) * mu
+    band_dg = (np.abs(uc * s1) * dda + np.abs(da * s1) * du_band +
+               np.abs(da * uc) * silu_grad2_bound() * dg_band + ELEMENTWISE_BAND * np.abs(dg_val)) * mg
+    band_du = (np.abs(silu(gc)) * dda + np.abs(da * s1) * dg_band + ELEMENTWISE_BAND * np.abs(du_val)) * mu
+    # the clamp's masks jump at its bounds: within the fp32 band of a bound the
+    # kernel may take either side, so the whole unmasked value is an alternative
+    jump_dg = jump_du = 0.0
+    if limit:
+        jump_dg = np.where(np.abs(g - limit) <= dg_band, np.abs(da * uc * s1), 0.0)
+        jump_du = np.where(np.abs(np.abs(u) - limit) <= du_band, np.abs(da * silu(gc)), 0.0)
+    alt_dg = bf16_alternative(dg_val, band_dg) + jump_dg   # weight-gradient operands (bf16)
+    alt_du = bf16_alternative(du_val, band_du) + jump_du
     if ops.mx:                                            # dgrad operand [dg|du] (MXFP8)
         alt_q = mxfp8_alternative(np.concatenate([dg_val, du_val], axis=1),
-                                  np.concatenate([band_dg, band_du], axis=1))
+                                  np.concatenate([band_dg + jump_dg, band_du + jump_du], axis=1))
+        alt_q = alt_q + np.concatenate([np.broadcast_to(jump_dg, dg_val.shape),
+                                        np.broadcast_to(jump_du, du_val.shape)], axis=1)
         env_dx = alt_q[:, :I] @ np.abs(Bg) + alt_q[:, I:] @ np.abs(Bu)
     else:
         env_dx = alt_dg @ np.abs(Bg) + alt_du @ np.abs(Bu)
@@ -446,7 +505,7 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed):
     env_dWu = alt_du.T @ np.abs(x)
 
     pa_val = p[:, None] * a_b
-    alt_pa = bf16_alternative(pa_val, 2 * U32 * np.abs(pa_val))
+    alt_pa = bf16_alternative(pa_val, 2 * U32 * np.abs(pa_val) + p_band[:, None] * np.abs(a_b))
     alt_pa = alt_pa + np.where(alt_a > 0, np.abs(p)[:, None] * alt_a + np.ldexp(1.0, np.frexp(pa_val)[1] - 8), 0.0)
     env_dWd = np.abs(go).T @ alt_pa
     return env_y, env_dx, env_dWg, env_dWu, env_dWd, env_dprob
@@ -462,8 +521,22 @@ def envelope(grad_out, cache, W):
     T, H = x.shape
     E = W.num_experts
     gs, us, _ = cache["shared"]
-    ey_s, edx_s, eg_s, eu_s, ed_s, _ = _expert_envelope(x, go, np.ones(T), gs, us, W.shared(), W.shared(), prec,
-                                                        routed=False)
+    limit, gate = cache["limit"], cache["gate"]
+    if gate is None:
+        p_s, p_band = np.ones(T), None
+    else:                                  # the kernel's fp32 logit and sigmoid
+        w_gate = W.shared_output_gate
+        z_band = fp32_dot_band((x * x) @ (w_gate * w_gate), H)
+        p_band = gate * (1.0 - gate) * z_band + ELEMENTWISE_BAND * gate
+        p_s = gate
+    ey_s, edx_s, eg_s, eu_s, ed_s, edg = _expert_envelope(x, go, p_s, gs, us, W.shared(), W.shared(), prec,
+                                                          routed=False, limit=limit, p_band=p_band)
+    env_gate = None
+    if gate is not None:
+        ey_s = gate[:, None] * ey_s
+        env_dz = gate * (1.0 - gate) * edg
+        edx_s = edx_s + env_dz[:, None] * np.abs(W.shared_output_gate)[None, :]
+        env_gate = np.abs(x).T @ env_dz
     R = perm_src.size
     ey = np.zeros((R, H))
     edx = np.zeros((R, H))
@@ -474,7 +547,7 @@ def envelope(grad_out, cache, W):
         lo, hi = offsets[e], offsets[e + 1]
         ey[lo:hi], edx[lo:hi], eg, eu, ed, edp[lo:hi] = _expert_envelope(
             x[perm_src[lo:hi]], go[perm_src[lo:hi]], pp_perm[lo:hi], g, u, W.routed(e), W.routed_dgrad(e), prec,
-            routed=True)
+            routed=True, limit=limit)
         routed[e] = (eg, eu, ed)
     env_out = ey_s.copy()
     env_dh = edx_s.copy()
@@ -485,5 +558,8 @@ def envelope(grad_out, cache, W):
         env_out[v] += np.abs(pp[v, s, None]) * ey[r]
         env_dh[v] += edx[r]
         env_dp[np.flatnonzero(v), ids[v, s]] = edp[r]
-    return dict(out=env_out, dhidden=env_dh, dprobs=env_dp, shared_gate=eg_s, shared_up=eu_s,
-                shared_down=ed_s, routed=routed)
+    env = dict(out=env_out, dhidden=env_dh, dprobs=env_dp, shared_gate=eg_s, shared_up=eu_s,
+               shared_down=ed_s, routed=routed)
+    if env_gate is not None:
+        env["shared_output_gate"] = env_gate
+    return env

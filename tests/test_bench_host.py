@@ -55,7 +55,8 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
 
 def test_kernel_work_table_covers_every_kernel_class():
     import mixture_experts_layer_pack_gb300 as M
-    names = [M.moe_kernel_name(i) for i in range(18)]
+    names = [M.moe_kernel_name(i) for i in range(M.binding.MOE_K_COUNT)]
+    assert None not in names and M.moe_kernel_name(M.binding.MOE_K_COUNT) is None
     for n in names:
         f, b = bench.kernel_work(n, 4096, 2048, 96, 6, 1024, 24576, 96)
         assert f >= 0 and b >= 0

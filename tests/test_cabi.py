@@ -51,7 +51,9 @@ def test_workspace_sizes_scale_with_config():
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(swiglu_limit=7.0), 2),          # clamp: defined nowhere on the pages
+    (dict(swiglu_limit=-1.0), 1),         # the clamp bound must be >= 0 (0 = off)
+    (dict(swiglu_limit=float("nan")), 1),
+    (dict(swiglu_limit=float("inf")), 1),
     (dict(hidden=2000), 2),               # H not a multiple of 128
     (dict(inter=1000), 2),                # I not a multiple of 64
     (dict(topk=0), 1),
@@ -63,6 +65,10 @@ def test_bad_configs_rejected(kw, status):
     with pytest.raises(B.MoeError) as ei:
         M.moe_workspace_size(_cfg(**kw))
     assert ei.value.status == status
+
+
+def test_swiglu_limit_accepted():
+    assert M.moe_workspace_size(_cfg(swiglu_limit=7.0)) == M.moe_workspace_size(_cfg())
 
 
 def test_null_arguments_rejected():

@@ -77,6 +77,11 @@ def _compare(inp, res):
         ref["dW shared gate"], got["dW shared gate"] = grads["shared_gate"], d["shared_fc1"][:I]
         ref["dW shared up"], got["dW shared up"] = grads["shared_up"], d["shared_fc1"][I:]
         ref["dW shared down"], got["dW shared down"] = grads["shared_down"], d["shared_fc2"]
+        if "shared_output_gate" in grads:
+            ref["dW shared output gate"] = grads["shared_output_gate"]
+            got["dW shared output gate"] = d["shared_output_gate"]
+            if env is not None:
+                ev["dW shared output gate"] = env["shared_output_gate"]
         for n, r in ref.items():
             if prec == "mxfp8":
                 errs[n] = assert_close(got[n], r, n, rtol=MX_RTOL, atol_frac=MX_ATOL, env=ev.get(n))

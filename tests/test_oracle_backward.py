@@ -134,3 +134,93 @@ def test_backward_tokens_are_independent():
     dxs, dps, _ = O.backward(go[sub], cs, W)
     np.testing.assert_allclose(dxs, dx[sub], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(dps, dp[sub], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- swiglu_limit clamp and shared output gate
+def _gated_case(seed, limit):
+    W, x, go, m, probs, k = _tiny_case(seed)
+    rng = np.random.default_rng(100 + seed)
+    W.shared_output_gate = rng.standard_normal(x.shape[1]) * 0.5
+    # the clamp must be active somewhere and no input may sit within reach of
+    # a finite-difference step of a clamp bound
+    gs = []
+    for Wg, Wu in [(W.sg, W.su)] + [(W.rg[e], W.ru[e]) for e in range(W.num_experts)]:
+        gs.append((x @ Wg.T, x @ Wu.T))
+    g_all = np.concatenate([g.ravel() for g, _ in gs])
+    u_all = np.concatenate([u.ravel() for _, u in gs])
+    assert np.any(g_all > limit) and np.any(np.abs(u_all) > limit) and np.any(g_all < limit)
+    assert np.min(np.abs(g_all - limit)) > 1e-4 and np.min(np.abs(np.abs(u_all) - limit)) > 1e-4
+    return W, x, go, m, probs, k
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_clamp_and_gate_match_finite_differences(seed):
+    limit = 0.6
+    W, x, go, m, probs, k = _gated_case(seed, limit)
+    _, cache = O.forward(x, probs, m, W, k, swiglu_limit=limit)
+    dx, dprobs, grads = O.backward(go, cache, W)
+
+    def f():
+        out, _ = O.forward(x, probs, m, W, k, swiglu_limit=limit)
+        return float(np.sum(go * out))
+
+    def check(arr, grad):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            fd[idx] = _fd(f, arr, idx)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8)
+
+    check(x, dx)
+    for t, e in zip(*np.nonzero(m)):
+        assert dprobs[t, e] == pytest.approx(_fd(f, probs, (t, e)), rel=1e-6, abs=1e-8)
+    check(W.shared_output_gate, grads["shared_output_gate"])
+    check(W.sg, grads["shared_gate"])
+    check(W.su, grads["shared_up"])
+    check(W.sd, grads["shared_down"])
+    for e, (dWg, dWu, dWd) in grads["routed"].items():
+        check(W.rg[e], dWg)
+        check(W.ru[e], dWu)
+        check(W.rd[e], dWd)
+
+
+def test_clamp_single_unit_by_hand():
+    """H = I = 1, one token, one expert: g = 3 > L = 1 and u = -6 < -L, so
+    a = silu(1) * (-1), and neither clamped input passes a gradient."""
+    W = O.DenseWeights(np.zeros((1, 1)), np.zeros((1, 1)), np.zeros((1, 1)),
+                       np.array([[[1.5]]]), np.array([[[-3.0]]]), np.array([[[2.0]]]))
+    x = np.array([[2.0]])
+    m = np.array([[True]])
+    p = np.array([[0.25]])
+    out, cache = O.forward(x, p, m, W, 1, swiglu_limit=1.0)
+    a = -1.0 / (1.0 + np.exp(-1.0))                 # silu(1) * (-1)
+    assert out[0, 0] == pytest.approx(0.25 * 2.0 * a, rel=1e-15)
+    dx, dp, g = O.backward(np.array([[4.0]]), cache, W)
+    assert dx[0, 0] == 0.0
+    dWg, dWu, dWd = g["routed"][0]
+    assert dWg[0, 0] == 0.0 and dWu[0, 0] == 0.0
+    assert dWd[0, 0] == pytest.approx(4.0 * 0.25 * a, rel=1e-15)
+    assert dp[0, 0] == pytest.approx(4.0 * 2.0 * a, rel=1e-15)
+
+
+def test_large_limit_changes_nothing():
+    W, x, go, m, probs, k = _tiny_case(5)
+    out0, c0 = O.forward(x, probs, m, W, k)
+    out1, c1 = O.forward(x, probs, m, W, k, swiglu_limit=1e6)
+    assert np.array_equal(out0, out1)
+    d0 = O.backward(go, c0, W)
+    d1 = O.backward(go, c1, W)
+    assert np.array_equal(d0[0], d1[0]) and np.array_equal(d0[1], d1[1])
+
+
+def test_zero_gate_weight_halves_the_shared_expert():
+    """w = 0: gate = 1/2 for every token; the gate weight's gradient is
+    x^T (1/4 <go, y_shared>), with y_shared the ungated shared expert."""
+    W, x, go, m, probs, k = _tiny_case(6)
+    out_u, _ = O.forward(x, probs, m, W, k)
+    _, _, _, ys = O.expert_forward(x, *W.shared())
+    W.shared_output_gate = np.zeros(x.shape[1])
+    out_g, cache = O.forward(x, probs, m, W, k)
+    np.testing.assert_allclose(out_g, out_u - 0.5 * ys, rtol=1e-13, atol=1e-13)
+    _, _, grads = O.backward(go, cache, W)
+    np.testing.assert_allclose(grads["shared_output_gate"], x.T @ (0.25 * np.sum(go * ys, axis=1)),
+                               rtol=1e-12, atol=1e-13)

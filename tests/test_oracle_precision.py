@@ -125,11 +125,12 @@ def test_bf16_mode_within_rounding_bounds(seed):
         assert np.all(np.abs(g_b["routed"][e][2] - dWd) <= bd * (1 + 1e-9) + 1e-15)
 
 
-def _fp32_layer(x, go, m, probs, W, k, mx=False):
+def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
     """An independent fp32 evaluation of the layer (numpy float32 matmuls and
     elementwise math, bf16 rounding of the GEMM operands -- MXFP8 for the routed
     forward/dgrad operands when mx -- fp64 afterwards): stands in for any kernel
-    that evaluates the operands in fp32."""
+    that evaluates the operands in fp32. ``limit`` clamps the SwiGLU inputs;
+    W.shared_output_gate (if set) gates the shared expert with an fp32 sigmoid."""
     from oracle import mxfp8 as MXC
     f32 = np.float32
     rnd = O.bf16_round
@@ -147,12 +148,21 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False):
         xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xq, Wg, Wu, Wd, goq))
         g = xr32 @ Wg32.T
         u = xr32 @ Wu32.T
+        mg = mu = f32(1)
+        if limit:
+            L = f32(limit)
+            mg = (g <= L).astype(f32)
+            mu = ((u >= -L) & (u <= L)).astype(f32)
+            g = np.minimum(g, L)
+            u = np.clip(u, -L, L)
         s = sig(g)
         a = (mxr if quant else rnd)((g * s * u).astype(np.float64))
-        y = a @ Wd.T
-        da = p.astype(f32)[:, None] * (go32 @ Wd32)
-        dg32 = da * u * (s * (f32(1) + g * (f32(1) - s)))
-        du32 = da * (g * s)
+        y = p[:, None] * (a @ Wd.T)
+        da_u = go32 @ Wd32
+        dprob = np.sum(a.astype(f32) * da_u, axis=1).astype(np.float64)
+        da = p.astype(f32)[:, None] * da_u
+        dg32 = da * u * (s * (f32(1) + g * (f32(1) - s))) * mg
+        du32 = da * (g * s) * mu
         dg, du = rnd(dg32.astype(np.float64)), rnd(du32.astype(np.float64))
         if quant:
             qq = mxr(np.concatenate([dg32, du32], axis=1).astype(np.float64))
@@ -160,10 +170,17 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False):
         else:
             dx = dg @ Wg + du @ Wu
         pa = rnd((p.astype(f32)[:, None] * a.astype(f32)).astype(np.float64))
-        return y, dx, dg.T @ xr, du.T @ xr, gor.T @ pa
+        return y, dx, dg.T @ xr, du.T @ xr, gor.T @ pa, dprob
 
     T = x.shape[0]
-    ys, dxs, gsg, gsu, gsd = expert(x, go, np.ones(T), *W.shared(), False)
+    w_gate = getattr(W, "shared_output_gate", None)
+    gate = np.ones(T) if w_gate is None else sig(x.astype(f32) @ w_gate.astype(f32)).astype(np.float64)
+    ys, dxs, gsg, gsu, gsd, dgate = expert(x, go, gate, *W.shared(), False)
+    grads = dict(shared_gate=gsg, shared_up=gsu, shared_down=gsd)
+    if w_gate is not None:
+        dz = (gate * (1 - gate)).astype(f32) * dgate.astype(f32)
+        dxs = dxs + (dz[:, None] * w_gate.astype(f32)[None, :]).astype(np.float64)
+        grads["shared_output_gate"] = (x.astype(f32).T @ dz).astype(np.float64)
     out, dh = ys.copy(), dxs.copy()
     ids, pp, _ = O.route_pack(m, probs, k)
     routed = {}
@@ -171,11 +188,12 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False):
         rows, slots = np.nonzero(ids == e)
         if rows.size == 0:
             continue
-        y, dx, g1, g2, g3 = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e), mx)
-        out[rows] += pp[rows, slots, None] * y
+        y, dx, g1, g2, g3, _ = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e), mx)
+        out[rows] += y
         dh[rows] += dx
         routed[e] = (g1, g2, g3)
-    return out, dh, dict(shared_gate=gsg, shared_up=gsu, shared_down=gsd, routed=routed)
+    grads["routed"] = routed
+    return out, dh, grads
 
 
 @pytest.mark.parametrize("seed", [11, 12, 13])
@@ -237,6 +255,43 @@ def test_mxfp8_envelope_covers_fp32_evaluation(seed):
     for a, b, ev, name in ((out_f, out_b, env["out"], "out"), (dh_f, dh_b, env["dhidden"], "dhidden")):
         slack = 1e-5 * np.abs(b).max()
         assert np.all(np.abs(a - b) <= ev + slack), name
+    for e, gs in g_f["routed"].items():
+        for j in range(3):
+            b = g_b["routed"][e][j]
+            assert np.all(np.abs(gs[j] - b) <= env["routed"][e][j] + 1e-5 * np.abs(b).max()), (e, j)
+
+
+@pytest.mark.parametrize("seed", [31, 32])
+def test_envelope_covers_fp32_evaluation_with_clamp_and_gate(seed):
+    """bf16 mode with the swiglu_limit clamp active on a fifth of the SwiGLU
+    inputs and a gated shared expert: an fp32 evaluation stays within the
+    oracle's result plus its envelope (clamp bounds and the fp32 gate included)."""
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k = 192, 256, 256, 3, 2
+    limit = 0.8
+    W = O.DenseWeights(*(rng.standard_normal(s) * 0.06 for s in
+                         ((I, H), (I, H), (H, I), (E, I, H), (E, I, H), (E, H, I))),
+                       shared_output_gate=torch.from_numpy(rng.standard_normal(H) * 0.06).to(torch.bfloat16)
+                       .double().numpy())
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    go = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    m = np.zeros((T, E), bool)
+    for t in range(T):
+        m[t, rng.choice(E, 2, replace=False)] = True
+    probs = rng.random((T, E)).astype(np.float32).astype(np.float64)
+    out_b, cache = O.forward(x, probs, m, W, k, precision="bf16", swiglu_limit=limit)
+    g_s, u_s, _ = cache["shared"]
+    assert 0.05 < np.mean(g_s > limit) < 0.5 and 0.05 < np.mean(np.abs(u_s) > limit) < 0.6
+    dh_b, _, g_b = O.backward(go, cache, W)
+    env = O.envelope(go, cache, W)
+    out_f, dh_f, g_f = _fp32_layer(x, go, m, probs, W, k, limit=limit)
+    for a, b, ev, name in ((out_f, out_b, env["out"], "out"), (dh_f, dh_b, env["dhidden"], "dhidden"),
+                           (g_f["shared_output_gate"], g_b["shared_output_gate"], env["shared_output_gate"], "gate")):
+        slack = 1e-5 * np.abs(b).max()
+        d = np.abs(a - b)
+        assert np.all(d <= ev + slack), f"{name}: {np.sum(d > ev + slack)} outside the envelope"
+    for n in ("shared_gate", "shared_up", "shared_down"):
+        assert np.all(np.abs(g_f[n] - g_b[n]) <= env[n] + 1e-5 * np.abs(g_b[n]).max()), n
     for e, gs in g_f["routed"].items():
         for j in range(3):
             b = g_b["routed"][e][j]
