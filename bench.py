@@ -40,6 +40,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--config", type=int, default=2)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--main-grad-dtype", choices=("fp32", "bf16"), default="fp32",
+                   help="dtype of the main_grad buffers the backward accumulates into")
     return p.parse_args(argv)
 
 
@@ -150,14 +152,15 @@ def gpu_id_for(dev_index):
 MX_ROUTED_GEMMS = ("gemm_fwd_gu_routed", "gemm_fwd_down_routed", "gemm_bwd_down_routed", "gemm_bwd_gu_routed")
 
 
-def kernel_work(name, T, H, E, k, I, R, E_act, mx=False):
+def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4):
     """(algorithmic flops, algorithmic HBM bytes) of one launch of a kernel class.
 
     Bytes count each operand read once and each result written once (no padding
     rows, no re-reads); flops count a multiply-add as 2. Weights of experts
     without tokens are not read. mx: the routed forward/dgrad GEMMs read MXFP8
     operands (1 byte + 1/32 byte of scale per element) and the producers of
-    those operands also write their MXFP8 copies."""
+    those operands also write their MXFP8 copies. mg_bytes: main_grad element
+    size (read and written once by the weight-gradient kernels)."""
     b2, b4 = 2, 4
     bq = 1 + 1 / 32                          # MXFP8 element incl. its share of the scale
     wb = bq if mx else b2                    # routed weight element
@@ -182,13 +185,13 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False):
                                  + T * 2 * I * b2),
         "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * ab + W_fc1 + R * H * b4),
         "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * b2 + 2 * I * H * b2 + T * H * b4),
-        "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * b2 + R * H * b2 + E_act * 2 * I * H * 8),
-        "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * b2 + E_act * H * I * 8),
-        "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * b2 + T * H * b2 + 2 * I * H * 8),
-        "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * b2 + H * I * 8),
+        "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * b2 + R * H * b2 + E_act * 2 * I * H * 2 * mg_bytes),
+        "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * b2 + E_act * H * I * 2 * mg_bytes),
+        "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * b2 + T * H * b2 + 2 * I * H * 2 * mg_bytes),
+        "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * b2 + H * I * 2 * mg_bytes),
         "unpermute": (0, T * H * b4 + R * H * b4 + T * H * b2 + T * E * b4),
         "shared_gate_fwd": (2 * T * H, T * H * b2 + H * b2 + T * b4),
-        "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 8),
+        "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 2 * mg_bytes),
     }
     return table[name]
 
@@ -322,6 +325,11 @@ def run_ours(args):
     w = MI.make_weights(H, I, E, seed, device=dev)
     hidden, grad_out = MI.make_activations(T, H, seed, device=dev)
     mg = MI.make_main_grads(H, I, E, seed, device=dev)
+    mg_bf16 = args.main_grad_dtype == "bf16"
+    mg_bytes = 2 if mg_bf16 else 4
+    workload = MI.WORKLOAD_NAMES[cid] + ("-bf16-main-grad" if mg_bf16 else "")
+    if mg_bf16:
+        mg = {n: t.to(torch.bfloat16) for n, t in mg.items()}
     probs = torch.from_numpy(r.probs).to(dev)
     rmap = torch.from_numpy(r.routing_map).to(dev).view(torch.uint8)
 
@@ -428,13 +436,13 @@ def run_ours(args):
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
         try:
-            traffic = json.load(open(tr_path)).get(MI.WORKLOAD_NAMES[cid], {}).get(top)
+            traffic = json.load(open(tr_path)).get(workload, {}).get(top)
         except Exception:
             traffic = None
-    roof = roofline_of(top, per_kernel[top]["ms_per_launch"], kernel_work(top, T, H, E, k, I, R, E_act, mx), peaks,
+    roof = roofline_of(top, per_kernel[top]["ms_per_launch"], kernel_work(top, T, H, E, k, I, R, E_act, mx, mg_bytes), peaks,
                        peaks_kind, traffic, fp8=mx and top in MX_ROUTED_GEMMS)
     for name, v in per_kernel.items():
-        f, b = kernel_work(name, T, H, E, k, I, R, E_act, mx)
+        f, b = kernel_work(name, T, H, E, k, I, R, E_act, mx, mg_bytes)
         ms_l = v["ms_per_launch"] * 1e-3
         v["tflops"] = f / ms_l / 1e12 if f else 0.0
         v["gbs"] = b / ms_l / 1e9
@@ -443,11 +451,11 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 routed / bf16 shared" if mx else "bf16",
             "data": "synthetic (seeded routing, N(0,0.02) weights, N(0,1) activations; random init)",
-            "config": {"workload": MI.WORKLOAD_NAMES[cid], "T": T, "H": H, "E": E, "k": k, "I": I,
+            "config": {"workload": workload, "T": T, "H": H, "E": E, "k": k, "I": I,
                        "valid_routes": R, "routing": f"seeded router stand-in ({c['routing']}, drop={c['drop']})",
-                       "main_grad": "fp32, accumulated in place every step",
+                       "main_grad": f"{args.main_grad_dtype}, accumulated in place every step",
                        "l2": "inputs larger than L2: routed weights %.2f GB + main_grad %.2f GB per step"
-                             % (3 * E * I * H * 2 / 1e9, 3 * (E + 1) * I * H * 4 / 1e9),
+                             % (3 * E * I * H * 2 / 1e9, 3 * (E + 1) * I * H * (2 if mg_bf16 else 4) / 1e9),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tflops": tflops,
             "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],

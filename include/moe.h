@@ -49,6 +49,10 @@ typedef enum {
 
 typedef enum { MOE_W_BF16 = 0, MOE_W_MXFP8 = 1 } moe_wtype;
 
+/* dtype of the main_grad buffers (PR #8210 review thread on wgrad precision:
+ * main_grad.dtype selects the accumulation, one dtype for all buffers). */
+typedef enum { MOE_G_FP32 = 0, MOE_G_BF16 = 1 } moe_gtype;
+
 /* Layer shape. Routed and shared experts share `inter` (PR #6572, Supported
  * configurations: MOK limitations). hidden must be a multiple of 128, inter of 64;
  * 1 <= topk <= 32; 1 <= num_experts <= 1024.
@@ -103,18 +107,24 @@ typedef struct {
     const void* shared_output_gate;
 } moe_weights;
 
-/* fp32 main_grad buffers in the six-buffer order (runtime page,
+/* main_grad buffers in the six-buffer order (runtime page,
  * _gate_up_main_grad_arguments). Shapes as the matching weights.
  * strides[i] = {expert_stride, row_stride} in elements (expert_stride unused
  * for the shared three). Fused accumulation is mandatory (PR #6572, Design >
  * Gradient accumulation): every pointer must be non-null, 16-byte aligned,
- * row_stride a multiple of 4. shared_output_gate is the fp32 [H] main_grad of
+ * strides multiples of 16 bytes. shared_output_gate is the [H] main_grad of
  * the shared expert's output gate: required (16-byte aligned) when the forward
- * recorded in `saved` had a gate, ignored otherwise. */
+ * recorded in `saved` had a gate, ignored otherwise.
+ * dtype (moe_gtype) applies to every buffer. MOE_G_FP32: main_grad += dW in
+ * fp32, one add per element. MOE_G_BF16 (PR #8210 review: with BF16 main_grad
+ * each contribution is rounded to BF16 before the BF16 reduction-store):
+ * main_grad = bf16(main_grad + bf16(dW)), dW the fp32 GEMM accumulator, both
+ * roundings to nearest even. */
 typedef struct {
-    float *shared_gate, *shared_up, *shared_down, *routed_gate, *routed_up, *routed_down;
+    void *shared_gate, *shared_up, *shared_down, *routed_gate, *routed_up, *routed_down;
     int64_t strides[6][2];
-    float* shared_output_gate;
+    void* shared_output_gate;
+    int32_t dtype;
 } moe_main_grads;
 
 typedef struct moe_handle moe_handle;
@@ -158,11 +168,11 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
  * routing maps (backward adapter) and > Gradient accumulation).
  *   grad_out[T,H] bf16 -> dhidden[T,H] bf16, dprobs[T,E] fp32 (dense: every
  *   element written; 0 where the map is false), and main_grad += dW for all
- *   six buffers, in fp32, one add per element (deterministic). Experts that
+ *   six buffers, one add per element in mg->dtype (deterministic). Experts that
  *   received no tokens keep their main_grad bitwise. `saved` is not consumed.
  *   With a shared output gate, also main_grad_gate[h] += sum_t dz[t] hidden[t,h]
  *   and dhidden[t] += dz[t] w, dz[t] = gate[t] (1 - gate[t]) <grad_out[t], y_shared[t]>
- *   (y_shared before the gate), in fp32 with a fixed summation order. */
+ *   (y_shared before the gate), summed in fp32 in a fixed order. */
 moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved,
                         void* dhidden, float* dprobs, const moe_main_grads* mg, void* stream);
 

@@ -15,6 +15,7 @@ c_int64, c_int32, c_float, c_void_p, c_size_t = (ctypes.c_int64, ctypes.c_int32,
 
 MOE_OK = 0
 MOE_W_BF16, MOE_W_MXFP8 = 0, 1
+MOE_G_FP32, MOE_G_BF16 = 0, 1
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ROUTING",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_STATE"}
 WEIGHT_NAMES = ("shared_gate", "shared_up", "shared_down", "routed_gate", "routed_up", "routed_down")
@@ -36,7 +37,7 @@ class moe_weights(ctypes.Structure):
 
 class moe_main_grads(ctypes.Structure):
     _fields_ = ([(n, c_void_p) for n in WEIGHT_NAMES] + [("strides", (c_int64 * 2) * 6)] +
-                [("shared_output_gate", c_void_p)])
+                [("shared_output_gate", c_void_p), ("dtype", c_int32)])
 
 
 class MoeError(RuntimeError):
@@ -268,12 +269,17 @@ def weights_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, shared
 
 
 def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, shared_output_gate=None) -> moe_main_grads:
-    """Six-buffer main_grad order over combined FC1/FC2 fp32 buffers (plus the
-    optional fp32 [H] main_grad of the shared-expert output gate)."""
+    """Six-buffer main_grad order over combined FC1/FC2 buffers, all fp32 or all
+    bf16 (plus the optional [H] main_grad of the shared-expert output gate)."""
+    import torch
     inter = shared_fc1.shape[0] // 2
     views = (shared_fc1[:inter], shared_fc1[inter:], shared_fc2,
              routed_fc1[:, :inter], routed_fc1[:, inter:], routed_fc2)
+    dtypes = {v.dtype for v in views} | ({shared_output_gate.dtype} if shared_output_gate is not None else set())
+    if dtypes not in ({torch.float32}, {torch.bfloat16}):
+        raise ValueError(f"main_grad buffers must be all fp32 or all bf16, got {dtypes}")
     m = moe_main_grads(*[v.data_ptr() for v in views])
+    m.dtype = MOE_G_BF16 if dtypes == {torch.bfloat16} else MOE_G_FP32
     m.shared_output_gate = None if shared_output_gate is None else shared_output_gate.data_ptr()
     for i, v in enumerate(views):
         if v.dim() == 3:

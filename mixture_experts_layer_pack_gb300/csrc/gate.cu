@@ -78,14 +78,20 @@ __global__ void __launch_bounds__(256) gate_grad_chunk_kernel(const uint4* __res
     }
 }
 
-// mg[h] += sum over chunks c (in order) of gpart[c][h]
+// mg[h] += sum over chunks c (in order) of gpart[c][h]; bf16 main_grad:
+// mg[h] = bf16(mg[h] + bf16(sum))
 __global__ void __launch_bounds__(256) gate_grad_reduce_kernel(const float* __restrict__ gpart, int chunks, int H,
-                                                               float* __restrict__ mg) {
+                                                               void* __restrict__ mg, int mg_bf16) {
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
     float sum = 0.0f;
     for (int c = 0; c < chunks; ++c) sum += gpart[int64_t(c) * H + h];
-    mg[h] += sum;
+    if (mg_bf16) {
+        __nv_bfloat16* m = static_cast<__nv_bfloat16*>(mg) + h;
+        *m = __float2bfloat16_rn(__bfloat162float(*m) + __bfloat162float(__float2bfloat16_rn(sum)));
+    } else {
+        static_cast<float*>(mg)[h] += sum;
+    }
 }
 
 }  // namespace
@@ -101,7 +107,7 @@ cudaError_t launch_gate_forward(const __nv_bfloat16* hidden, const __nv_bfloat16
 }
 
 cudaError_t launch_gate_backward(const __nv_bfloat16* hidden, const float* gate, const float* partial, int n_part,
-                                 int T, int H, float* dz, float* gpart, float* mg_gate, cudaStream_t st) {
+                                 int T, int H, float* dz, float* gpart, void* mg_gate, bool mg_bf16, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int chunks = (T + kGateChunk - 1) / kGateChunk;
     gate_grad_chunk_kernel<<<chunks, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden), gate, partial, n_part, T,
@@ -109,7 +115,7 @@ cudaError_t launch_gate_backward(const __nv_bfloat16* hidden, const float* gate,
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    gate_grad_reduce_kernel<<<(H + 255) / 256, 256, 0, st>>>(gpart, chunks, H, mg_gate);
+    gate_grad_reduce_kernel<<<(H + 255) / 256, 256, 0, st>>>(gpart, chunks, H, mg_gate, mg_bf16 ? 1 : 0);
     count_launch();
     return cudaGetLastError();
 }

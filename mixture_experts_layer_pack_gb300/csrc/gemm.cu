@@ -369,31 +369,36 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 }
 
 // Weight-gradient epilogue of one warp: main_grad[e][m][n] += acc for its
-// 32-row quarter of every tile and its share of the 32-column chunks. Each
-// 32x32 fp32 box of main_grad is TMA-loaded into one of two 4 KB buffers one
-// box ahead (the next tile's first box is fetched while this tile's last box is
-// added), the accumulator chunk read from TMEM (lane = row) is added in shared
-// memory, and the box is TMA-stored back: one fp32 add per element, so the
-// result is fl32(main_grad + dW) whatever the schedule.
+// 32-row quarter of every tile and its share of the tile's boxes (fp32
+// main_grad: 32 x 32 boxes, bf16: 32 rows x 64 columns -- 4 KB and 128-byte
+// rows either way; the two warps of a quarter take alternate boxes). Each box
+// is TMA-loaded into one of two 4 KB buffers one box ahead (the next tile's
+// first box is fetched while this tile's last box is added), the accumulator
+// columns read from TMEM (lane = row) are added in shared memory, and the box
+// is TMA-stored back: one add per element, so the result is
+// fl32(main_grad + dW), or bf16(main_grad + bf16(dW)) for bf16 main_grad,
+// whatever the schedule.
 template <int BN>
 __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_tiles, uint32_t tmem_base, int q,
                                                int half, float* bufs, uint64_t* mg_bar, uint64_t* tfull,
                                                uint64_t* tempty, volatile int* abort_flag, const CUtensorMap* mC0,
                                                const CUtensorMap* mC1) {
-    constexpr int CH = BN / 32 / kEpiHalves;  // chunks of this warp per tile
     const int lane = threadIdx.x & 31;
+    const bool bf = args.mg_bf16 != 0;
+    const int bw = bf ? 64 : 32;                           // box width in elements
+    const int nb = (BN / bw - half + kEpiHalves - 1) / kEpiHalves;  // boxes of this warp per tile
     auto next_valid = [&](int tile) {
         for (; tile < total_tiles; tile += gridDim.x)
             if (decode_tile<OP_WGRAD>(tile, args).kblocks > 0) return tile;
         return total_tiles;
     };
-    // box (tile t, chunk c): destination map and coordinates
+    // box (tile t, c-th box of this warp): destination map and coordinates
     auto box = [&](const Tile& t, int c, const CUtensorMap*& mc, int& x, int& y) {
         const int m0 = t.mt * kBM + q * 32;
         const bool hi = m0 >= args.m_split;
         mc = hi ? mC1 : mC0;
         y = hi ? m0 - args.m_split : m0;
-        x = t.nt * BN + (half + c * kEpiHalves) * 32;
+        x = t.nt * BN + (half + c * kEpiHalves) * bw;
     };
     auto load_box = [&](const Tile& t, int c, int b) {
         const CUtensorMap* mc;
@@ -406,7 +411,7 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
     int cur = next_valid(blockIdx.x);
     Tile t = decode_tile<OP_WGRAD>(cur < total_tiles ? cur : 0, args);
     uint32_t pending = 0, parity = 0;  // per buffer: a load in flight / parity of its next completion
-    if (cur < total_tiles && lane == 0) {
+    if (nb > 0 && cur < total_tiles && lane == 0) {
         load_box(t, 0, 0);
         pending = 1;
     }
@@ -425,20 +430,22 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
         const int nxt = next_valid(cur + gridDim.x);
         const Tile tn = decode_tile<OP_WGRAD>(nxt < total_tiles ? nxt : 0, args);
 #pragma unroll 1
-        for (int c = 0; c < CH; ++c) {
+        for (int c = 0; c < nb; ++c) {
             const int b = jb & 1;
             if (lane == 0) {
                 // prefetch the box after this one into the other buffer, once the
                 // store that last used it has read it out
-                const bool more = c + 1 < CH || nxt < total_tiles;
+                const bool more = c + 1 < nb || nxt < total_tiles;
                 if (more) {
                     bulk_wait_read<0>();
-                    load_box(c + 1 < CH ? t : tn, c + 1 < CH ? c + 1 : 0, b ^ 1);
+                    load_box(c + 1 < nb ? t : tn, c + 1 < nb ? c + 1 : 0, b ^ 1);
                     pending |= 1u << (b ^ 1);
                 }
             }
-            float v[32];
-            tmem_ld32(t_row + uint32_t((half + c * kEpiHalves) * 32), v);
+            const uint32_t col = uint32_t((half + c * kEpiHalves) * bw);
+            float v[32], v2[32];
+            tmem_ld32(t_row + col, v);
+            if (bf) tmem_ld32(t_row + col + 32, v2);
             if (lane == 0) w = mbar_wait(&mg_bar[b], (parity >> b) & 1, abort_flag, args.status) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, w, 0)) {
                 ok = false;
@@ -449,16 +456,36 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
             __syncwarp();
             pending &= ~(1u << b);
             parity ^= 1u << b;
-            // row `lane` of the box, 128-byte swizzled as the TMA wrote it
-            float4* srow = reinterpret_cast<float4*>(bufs + b * (kStageTileBytes / 4) + lane * 32);
+            // row `lane` of the box: 128 bytes, 16-byte unit j at j ^ (lane % 8) (128-byte swizzle)
+            uint4* srow = reinterpret_cast<uint4*>(bufs + b * (kStageTileBytes / 4) + lane * 32);
+            if (bf) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float4 m = srow[j ^ (lane & 7)];
-                m.x += v[4 * j];
-                m.y += v[4 * j + 1];
-                m.z += v[4 * j + 2];
-                m.w += v[4 * j + 3];
-                srow[j ^ (lane & 7)] = m;
+                for (int j = 0; j < 8; ++j) {
+                    uint4 m = srow[j ^ (lane & 7)];
+                    uint32_t* mw = reinterpret_cast<uint32_t*>(&m);
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) {
+                        const int cidx = 8 * (j & 3) + 2 * z;
+                        const float d0 = j < 4 ? v[cidx] : v2[cidx];
+                        const float d1 = j < 4 ? v[cidx + 1] : v2[cidx + 1];
+                        float lo, hi;
+                        unpack_bf16x2(mw[z], lo, hi);
+                        lo += __bfloat162float(__float2bfloat16_rn(d0));
+                        hi += __bfloat162float(__float2bfloat16_rn(d1));
+                        mw[z] = pack_bf16x2(lo, hi);
+                    }
+                    srow[j ^ (lane & 7)] = m;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float4 m = reinterpret_cast<float4*>(srow)[j ^ (lane & 7)];
+                    m.x += v[4 * j];
+                    m.y += v[4 * j + 1];
+                    m.z += v[4 * j + 2];
+                    m.w += v[4 * j + 3];
+                    reinterpret_cast<float4*>(srow)[j ^ (lane & 7)] = m;
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();

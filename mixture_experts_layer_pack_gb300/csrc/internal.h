@@ -57,6 +57,7 @@ struct GemmArgs {
     int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
     int inter;
     float swiglu_limit;         // > 0: SwiGLU inputs clamped, g <= L, |u| <= L (FWD_GU, BWD_DOWN epilogues)
+    int mg_bf16;                // WGRAD: main_grad is bf16 (bf16(mg + bf16(dW))), else fp32 (mg + dW)
     int* status;
     // MXFP8 (block-scaled) GEMMs
     uint8_t* q_out;             // E4M3 copy of the epilogue's GEMM-operand output (a, or [dg|du])
@@ -122,7 +123,7 @@ constexpr int kGateChunk = 128;  // tokens per partial sum of the gate weight's 
 cudaError_t launch_gate_forward(const __nv_bfloat16* hidden, const __nv_bfloat16* w, int T, int H, float* gate,
                                 cudaStream_t st);
 cudaError_t launch_gate_backward(const __nv_bfloat16* hidden, const float* gate, const float* partial, int n_part,
-                                 int T, int H, float* dz, float* gpart, float* mg_gate, cudaStream_t st);
+                                 int T, int H, float* dz, float* gpart, void* mg_gate, bool mg_bf16, cudaStream_t st);
 
 void count_launch(int n = 1);
 

@@ -217,11 +217,13 @@ bool map_u8_weight(CUtensorMap* m, const void* data, const moe_wview& v, int64_t
 
 bool check_mg(const moe_main_grads* m) {
     if (!m) return false;
-    float* const p[6] = {m->shared_gate, m->shared_up, m->shared_down, m->routed_gate, m->routed_up, m->routed_down};
+    if (m->dtype != MOE_G_FP32 && m->dtype != MOE_G_BF16) return false;
+    const int64_t q = m->dtype == MOE_G_BF16 ? 8 : 4;  // elements per 16 bytes
+    void* const p[6] = {m->shared_gate, m->shared_up, m->shared_down, m->routed_gate, m->routed_up, m->routed_down};
     for (int i = 0; i < 6; ++i) {
         if (!p[i] || !aligned16(p[i])) return false;
-        if (m->strides[i][1] % 4 || m->strides[i][1] <= 0) return false;
-        if (i >= 3 && (m->strides[i][0] % 4 || m->strides[i][0] <= 0)) return false;
+        if (m->strides[i][1] % q || m->strides[i][1] <= 0) return false;
+        if (i >= 3 && (m->strides[i][0] % q || m->strides[i][0] <= 0)) return false;
     }
     return true;
 }
@@ -242,14 +244,17 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int64_t rows, int64_t mn, int
     return encode_map(m, base, 2, dims, strides, box);
 }
 
-// 3D fp32 main_grad view [E][rows][cols] (expert stride es, row stride rs) as a
-// TMA load and store map, box 32 cols x 32 rows
-bool map_main_grad(CUtensorMap* m, float* base, int64_t E, int64_t rows, int64_t cols, int64_t es, int64_t rs) {
+// 3D main_grad view [E][rows][cols] (expert stride es, row stride rs, elements)
+// as a TMA load and store map with 128-byte box rows: 32 fp32 or 64 bf16
+// columns x 32 rows
+bool map_main_grad(CUtensorMap* m, void* base, int64_t E, int64_t rows, int64_t cols, int64_t es, int64_t rs,
+                   bool bf16) {
     if (E <= 1) es = rows * rs;
+    const uint64_t eb = bf16 ? 2 : 4;
     const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(E)};
-    const uint64_t strides[2] = {uint64_t(rs) * 4, uint64_t(es) * 4};
-    const uint32_t box[3] = {32, 32, 1};
-    return encode_map(m, base, 3, dims, strides, box, MAP_F32);
+    const uint64_t strides[2] = {uint64_t(rs) * eb, uint64_t(es) * eb};
+    const uint32_t box[3] = {bf16 ? 64u : 32u, 32, 1};
+    return encode_map(m, base, 3, dims, strides, box, bf16 ? MAP_BF16 : MAP_F32);
 }
 
 // 3D weight view [E][rows][cols] with a box of (64 cols, box_rows rows, 1 expert)
@@ -621,6 +626,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     if (!check_mg(mg)) return MOE_ERR_INVALID_ARG;
     const bool gated = saved->gated;
     if (gated && (!mg->shared_output_gate || !aligned16(mg->shared_output_gate))) return MOE_ERR_INVALID_ARG;
+    const bool mg_bf16 = mg->dtype == MOE_G_BF16;
     const Shape& s = h->s;
     const int64_t T = saved->T;
     if (T == 0) return MOE_OK;
@@ -726,7 +732,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     if (gated) {
         Timed tm_(h, MOE_K_SHARED_GATE_BWD, st);
         MOE_CU(launch_gate_backward(static_cast<const __nv_bfloat16*>(saved->hidden), b.gate, ws.partial_s, s.n_part_s,
-                                    Ti, H, ws.dz, ws.gpart, mg->shared_output_gate, st));
+                                    Ti, H, ws.dz, ws.gpart, mg->shared_output_gate, mg_bf16, st));
     }
     // routed dgrad through gate/up
     if (mx) {
@@ -796,10 +802,11 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = E;
         a.m_tiles = 2 * I / kBM;
         a.n_tiles = H / bn;
-        if (!map_main_grad(&m.c0, mg->routed_gate, E, I, H, mg->strides[3][0], mg->strides[3][1]) ||
-            !map_main_grad(&m.c1, mg->routed_up, E, I, H, mg->strides[4][0], mg->strides[4][1]))
+        if (!map_main_grad(&m.c0, mg->routed_gate, E, I, H, mg->strides[3][0], mg->strides[3][1], mg_bf16) ||
+            !map_main_grad(&m.c1, mg->routed_up, E, I, H, mg->strides[4][0], mg->strides[4][1], mg_bf16))
             return MOE_ERR_INVALID_ARG;
         a.m_split = I;
+        a.mg_bf16 = mg_bf16;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
@@ -814,9 +821,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = E;
         a.m_tiles = H / kBM;
         a.n_tiles = I / bn;
-        if (!map_main_grad(&m.c0, mg->routed_down, E, H, I, mg->strides[5][0], mg->strides[5][1]))
+        if (!map_main_grad(&m.c0, mg->routed_down, E, H, I, mg->strides[5][0], mg->strides[5][1], mg_bf16))
             return MOE_ERR_INVALID_ARG;
         m.c1 = m.c0;
+        a.mg_bf16 = mg_bf16;
         Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
@@ -831,10 +839,11 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = 1;
         a.m_tiles = 2 * I / kBM;
         a.n_tiles = H / bn;
-        if (!map_main_grad(&m.c0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1]) ||
-            !map_main_grad(&m.c1, mg->shared_up, 1, I, H, 0, mg->strides[1][1]))
+        if (!map_main_grad(&m.c0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1], mg_bf16) ||
+            !map_main_grad(&m.c1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
             return MOE_ERR_INVALID_ARG;
         a.m_split = I;
+        a.mg_bf16 = mg_bf16;
         Timed tm_(h, MOE_K_WGRAD_FC1_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
@@ -849,8 +858,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = 1;
         a.m_tiles = H / kBM;
         a.n_tiles = I / bn;
-        if (!map_main_grad(&m.c0, mg->shared_down, 1, H, I, 0, mg->strides[2][1])) return MOE_ERR_INVALID_ARG;
+        if (!map_main_grad(&m.c0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16)) return MOE_ERR_INVALID_ARG;
         m.c1 = m.c0;
+        a.mg_bf16 = mg_bf16;
         Timed tm_(h, MOE_K_WGRAD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }

@@ -395,21 +395,31 @@ def backward(grad_out, cache, W):
     return dhidden, dprobs, grads
 
 
-def accumulate_main_grads(main_grads, grads):
-    """Fused accumulation: main_grad <- main_grad + dW, in fp64 (PR #6572, Design >
-    Gradient accumulation; PR #8210 review: fp32 accumulator through the
-    reduction-store). ``main_grads`` holds shared_gate/up/down [I,H]/[I,H]/[H,I]
-    and routed_gate/up/down [E,..]; experts with no tokens are left as they are."""
+def accumulate_main_grads(main_grads, grads, dtype="fp32"):
+    """Fused accumulation (PR #6572, Design > Gradient accumulation). ``main_grads``
+    holds shared_gate/up/down [I,H]/[I,H]/[H,I] and routed_gate/up/down [E,..]
+    (and shared_output_gate [H] when present); experts with no tokens are left
+    as they are.
+
+    dtype "fp32": main_grad <- main_grad + dW, in fp64 (PR #8210 review: the
+    fp32 accumulator stays fp32 through the reduction-store). dtype "bf16"
+    (same review: with BF16 main_grad each contribution is rounded to BF16
+    before the BF16 reduction-store): main_grad <- bf16(main_grad + bf16(dW)),
+    both roundings to nearest even, the sum exact before its rounding."""
+    if dtype not in ("fp32", "bf16"):
+        raise ValueError(dtype)
+
+    def add(m, d):
+        return m + d if dtype == "fp32" else bf16_round(m + bf16_round(d))
+
     out = {name: np.array(v, np.float64, copy=True) for name, v in main_grads.items()}
-    out["shared_gate"] += grads["shared_gate"]
-    out["shared_up"] += grads["shared_up"]
-    out["shared_down"] += grads["shared_down"]
-    if "shared_output_gate" in grads:
-        out["shared_output_gate"] += grads["shared_output_gate"]
+    for n in ("shared_gate", "shared_up", "shared_down", "shared_output_gate"):
+        if n in grads:
+            out[n] = add(out[n], grads[n])
     for e, (dWg, dWu, dWd) in grads["routed"].items():
-        out["routed_gate"][e] += dWg
-        out["routed_up"][e] += dWu
-        out["routed_down"][e] += dWd
+        out["routed_gate"][e] = add(out["routed_gate"][e], dWg)
+        out["routed_up"][e] = add(out["routed_up"][e], dWu)
+        out["routed_down"][e] = add(out["routed_down"][e], dWd)
     return out
 
 

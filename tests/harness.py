@@ -25,6 +25,7 @@ class Case:
     mx: bool = False      # MXFP8 routed weights
     limit: float = 0.0    # swiglu_limit
     gated: bool = False   # shared expert with an output gate
+    mg_bf16: bool = False  # bf16 main_grad buffers
 
 
 def config_case(cfg_id: int, T: int | None = None, variant: str | None = None) -> Case:
@@ -59,6 +60,8 @@ def make_inputs(case: Case, device="cuda", routing=None) -> Inputs:
     gate_w = None
     if case.gated:
         gate_w, mg["shared_output_gate"] = MI.make_shared_output_gate(case.H, case.seed, device=device)
+    if case.mg_bf16:
+        mg = {n: t.to(torch.bfloat16) for n, t in mg.items()}
     return Inputs(case, hidden, grad_out, probs, rmap, w, mg, r.probs, r.routing_map, mx, gate_w)
 
 

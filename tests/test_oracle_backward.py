@@ -224,3 +224,41 @@ def test_zero_gate_weight_halves_the_shared_expert():
     _, _, grads = O.backward(go, cache, W)
     np.testing.assert_allclose(grads["shared_output_gate"], x.T @ (0.25 * np.sum(go * ys, axis=1)),
                                rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- BF16 main_grad accumulation
+def test_bf16_main_grad_rounds_the_contribution_then_the_sum():
+    """bf16(mg + bf16(dW)) by hand (bf16: 8 significant bits, ulp(1) = 2^-7):
+    * dW = 2^-8 (exact in bf16): 1 + 2^-8 is a tie between 1 and 1 + 2^-7 -> even, 1;
+    * dW = 3 2^-8: 1 + 1.5 2^-7 is a tie -> even mantissa, 1 + 2^-6;
+    * dW = 2^-8 + 2^-20 rounds to 2^-8 first, so the sum is the tie of the first
+      case (1), where rounding the exact sum once would give 1 + 2^-7;
+    * dW = -3 (exact): 1 - 3 = -2 exactly."""
+    mg = {n: np.ones((1, 4)) for n in ("shared_gate", "shared_up", "shared_down")}
+    mg.update({n: np.ones((1, 1, 4)) for n in ("routed_gate", "routed_up", "routed_down")})
+    dW = np.array([[2.0 ** -8, 3 * 2.0 ** -8, 2.0 ** -8 + 2.0 ** -20, -3.0]])
+    grads = dict(shared_gate=dW, shared_up=dW, shared_down=dW, routed={0: (dW, dW, dW)})
+    out = O.accumulate_main_grads(mg, grads, dtype="bf16")
+    want = np.array([[1.0, 1.0 + 2.0 ** -6, 1.0, -2.0]])
+    for n in ("shared_gate", "shared_up", "shared_down"):
+        np.testing.assert_array_equal(out[n], want)
+    for n in ("routed_gate", "routed_up", "routed_down"):
+        np.testing.assert_array_equal(out[n][0], want)
+    single = O.bf16_round(1.0 + dW)                          # one rounding of the exact sum
+    assert single[0, 2] == 1.0 + 2.0 ** -7 and out["shared_gate"][0, 2] == 1.0
+    fp32 = O.accumulate_main_grads(mg, grads)                  # the fp32 path adds exactly
+    np.testing.assert_array_equal(fp32["shared_gate"], 1.0 + dW)
+
+
+def test_bf16_main_grad_matches_torch_bf16_arithmetic():
+    import torch
+    rng = np.random.default_rng(9)
+    mg0 = torch.from_numpy(rng.standard_normal(4096).astype(np.float32) * 1e-3).to(torch.bfloat16)
+    dW = rng.standard_normal(4096) * 10.0 ** rng.integers(-5, 1, 4096)
+    dW32 = torch.from_numpy(dW.astype(np.float32))
+    ref = (mg0.float() + dW32.to(torch.bfloat16).float()).to(torch.bfloat16).double().numpy()
+    mg = {n: mg0.double().numpy().reshape(1, -1) for n in ("shared_gate", "shared_up", "shared_down")}
+    mg.update({n: mg0.double().numpy().reshape(1, 1, -1) for n in ("routed_gate", "routed_up", "routed_down")})
+    d = dW32.double().numpy().reshape(1, -1)
+    out = O.accumulate_main_grads(mg, dict(shared_gate=d, shared_up=d, shared_down=d, routed={}), dtype="bf16")
+    np.testing.assert_array_equal(out["shared_gate"][0], ref)
