@@ -94,6 +94,13 @@ typedef struct {
     const uint8_t* scale;     /* MXFP8 only: E8M0 rowwise scales [E, N, K/32], compact */
     const void* col_data;     /* MXFP8 only: e4m3 columnwise payload, same shape/strides as data */
     const uint8_t* col_scale; /* MXFP8 only: E8M0 columnwise scales [E, N/32, K], compact */
+    /* Optional per-expert descriptor table of a routed BF16 view (PR #6572,
+     * Design > MCore-owned parameters: non-single expert weights are described
+     * expert by expert): a HOST array of E device pointers, expert e's [N,K]
+     * matrix at expert_ptrs[e] with row_stride (each 16-byte aligned); data and
+     * expert_stride are then ignored. NULL: the strided view above. Read during
+     * the call only. MXFP8 views do not take tables (MOE_ERR_UNSUPPORTED). */
+    const void* const* expert_ptrs;
 } moe_wview;
 
 typedef struct {
@@ -125,6 +132,14 @@ typedef struct {
     int64_t strides[6][2];
     void* shared_output_gate;
     int32_t dtype;
+    /* Optional per-expert descriptor tables of the routed gate, up and down
+     * main_grads ("core.transformer.moe.megakernel.mok.runtime",
+     * main_grad_arguments: logical main grads and optional per-expert
+     * descriptors): HOST arrays of E device pointers (16-byte aligned), expert
+     * e's buffer at expert_ptrs[i][e] with row stride strides[3+i][1]; the
+     * matching routed_* pointer and expert stride are then ignored. NULL: the
+     * strided buffer. Read during the call only. */
+    void* const* expert_ptrs[3];
 } moe_main_grads;
 
 typedef struct moe_handle moe_handle;
@@ -136,7 +151,12 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 /* Creates a handle over caller-owned device workspace (256-byte aligned,
  * >= moe_workspace_size bytes, kept alive and unused by others until
  * moe_destroy). The handle itself is host memory owned by the library. The
- * current CUDA device at this call is the device of every later call. */
+ * current CUDA device at this call is the device of every later call.
+ * Per-expert descriptor tables (moe_wview.expert_ptrs,
+ * moe_main_grads.expert_ptrs) become TMA descriptors in this workspace; they
+ * are re-encoded and uploaded only when a table's pointers change, and such an
+ * upload (a host-to-device copy from library host memory) waits for the work
+ * already queued on `stream` before it starts. */
 moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_handle** out);
 void moe_destroy(moe_handle* h);
 

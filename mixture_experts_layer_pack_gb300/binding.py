@@ -28,7 +28,7 @@ class moe_config(ctypes.Structure):
 
 class moe_wview(ctypes.Structure):
     _fields_ = [("data", c_void_p), ("expert_stride", c_int64), ("row_stride", c_int64), ("scale", c_void_p),
-                ("col_data", c_void_p), ("col_scale", c_void_p)]
+                ("col_data", c_void_p), ("col_scale", c_void_p), ("expert_ptrs", c_void_p)]
 
 
 class moe_weights(ctypes.Structure):
@@ -37,7 +37,7 @@ class moe_weights(ctypes.Structure):
 
 class moe_main_grads(ctypes.Structure):
     _fields_ = ([(n, c_void_p) for n in WEIGHT_NAMES] + [("strides", (c_int64 * 2) * 6)] +
-                [("shared_output_gate", c_void_p), ("dtype", c_int32)])
+                [("shared_output_gate", c_void_p), ("dtype", c_int32), ("expert_ptrs", c_void_p * 3)])
 
 
 class MoeError(RuntimeError):
@@ -287,6 +287,45 @@ def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, sha
         else:
             m.strides[i][0], m.strides[i][1] = 0, v.stride(0)
     return m
+
+
+def _pointer_table(tensors):
+    """HOST array of the tensors' device pointers (ctypes), one per expert."""
+    return (c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def set_expert_tables(weights: moe_weights, gate=None, up=None, down=None) -> moe_weights:
+    """Describes routed BF16 weights expert by expert: each argument a list of E
+    [N,K] tensors sharing one row stride (PR #6572 per-expert non-single
+    weights). The host pointer arrays are kept alive on ``weights``."""
+    keep = list(getattr(weights, "_tables", []))
+    for name, ts in (("routed_gate", gate), ("routed_up", up), ("routed_down", down)):
+        if ts is None:
+            continue
+        arr = _pointer_table(ts)
+        v = getattr(weights, name)
+        v.expert_ptrs = ctypes.cast(arr, c_void_p).value
+        v.row_stride = ts[0].stride(0)
+        v.data = None
+        v.expert_stride = 0
+        keep.append(arr)
+    weights._tables = keep
+    return weights
+
+
+def set_main_grad_tables(main_grads: moe_main_grads, gate=None, up=None, down=None) -> moe_main_grads:
+    """Describes the routed main_grads expert by expert: lists of E [N,K] tensors
+    (one row stride per list). The host pointer arrays are kept alive on ``main_grads``."""
+    keep = list(getattr(main_grads, "_tables", []))
+    for i, ts in enumerate((gate, up, down)):
+        if ts is None:
+            continue
+        arr = _pointer_table(ts)
+        main_grads.expert_ptrs[i] = ctypes.cast(arr, c_void_p).value
+        main_grads.strides[3 + i][1] = ts[0].stride(0)
+        keep.append(arr)
+    main_grads._tables = keep
+    return main_grads
 
 
 class MoELayer:

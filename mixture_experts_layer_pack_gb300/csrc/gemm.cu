@@ -128,21 +128,27 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, 
         return;
     }
     tma_load_2d(sa, mA, bar, k0, t.mt * kBM);
+    // an expert's weights: its own descriptor (z = 0) from a per-expert table, or the 3D map at z = e
+    const CUtensorMap* B0 = a.b0_tab ? a.b0_tab + t.e : mB0;
+    const CUtensorMap* B1 = a.b1_tab ? a.b1_tab + t.e : mB1;
+    const int z0 = a.b0_tab ? 0 : t.e;
+    const int z1 = a.b1_tab ? 0 : t.e;
     if (OP == OP_FWD_GU) {
         const int j0 = t.nt * (BN / 2);
-        tma_load_3d(sb, mB0, bar, k0, j0, t.e);
-        tma_load_3d(sb + (BN / 2) * 128, mB1, bar, k0, j0, t.e);
+        tma_load_3d(sb, B0, bar, k0, j0, z0);
+        tma_load_3d(sb + (BN / 2) * 128, B1, bar, k0, j0, z1);
     } else if (OP == OP_FWD_DOWN) {
-        tma_load_3d(sb, mB0, bar, k0, t.nt * BN, t.e);
+        tma_load_3d(sb, B0, bar, k0, t.nt * BN, z0);
     } else if (OP == OP_BWD_DOWN) {
 #pragma unroll
-        for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * kMnChunkBytes, mB0, bar, t.nt * BN + 64 * c, k0, t.e);
+        for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * kMnChunkBytes, B0, bar, t.nt * BN + 64 * c, k0, z0);
     } else {  // OP_BWD_GU: K rows [0,I) come from the gate view, [I,2I) from the up view
         const bool up = k0 >= a.gate_up_split;
-        const CUtensorMap* m = up ? mB1 : mB0;
+        const CUtensorMap* m = up ? B1 : B0;
+        const int z = up ? z1 : z0;
         const int kk = up ? k0 - a.gate_up_split : k0;
 #pragma unroll
-        for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * kMnChunkBytes, m, bar, t.nt * BN + 64 * c, kk, t.e);
+        for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * kMnChunkBytes, m, bar, t.nt * BN + 64 * c, kk, z);
     }
 }
 
@@ -392,20 +398,23 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
             if (decode_tile<OP_WGRAD>(tile, args).kblocks > 0) return tile;
         return total_tiles;
     };
-    // box (tile t, c-th box of this warp): destination map and coordinates
-    auto box = [&](const Tile& t, int c, const CUtensorMap*& mc, int& x, int& y) {
+    // box (tile t, c-th box of this warp): destination map and coordinates (an
+    // expert's own descriptor at z = 0 when main_grad comes as a per-expert table)
+    auto box = [&](const Tile& t, int c, const CUtensorMap*& mc, int& x, int& y, int& z) {
         const int m0 = t.mt * kBM + q * 32;
         const bool hi = m0 >= args.m_split;
-        mc = hi ? mC1 : mC0;
+        const CUtensorMap* tab = hi ? args.c1_tab : args.c0_tab;
+        mc = tab ? tab + t.e : (hi ? mC1 : mC0);
+        z = tab ? 0 : t.e;
         y = hi ? m0 - args.m_split : m0;
         x = t.nt * BN + (half + c * kEpiHalves) * bw;
     };
     auto load_box = [&](const Tile& t, int c, int b) {
         const CUtensorMap* mc;
-        int x, y;
-        box(t, c, mc, x, y);
+        int x, y, z;
+        box(t, c, mc, x, y, z);
         mbar_arrive_expect_tx(&mg_bar[b], kStageTileBytes);
-        tma_load_3d(bufs + b * (kStageTileBytes / 4), mc, &mg_bar[b], x, y, t.e);
+        tma_load_3d(bufs + b * (kStageTileBytes / 4), mc, &mg_bar[b], x, y, z);
     };
 
     int cur = next_valid(blockIdx.x);
@@ -491,9 +500,9 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
             __syncwarp();
             if (lane == 0) {
                 const CUtensorMap* mc;
-                int x, y;
-                box(t, c, mc, x, y);
-                tma_store_3d(mc, bufs + b * (kStageTileBytes / 4), x, y, t.e);
+                int x, y, z;
+                box(t, c, mc, x, y, z);
+                tma_store_3d(mc, bufs + b * (kStageTileBytes / 4), x, y, z);
                 bulk_commit();
             }
             ++jb;

@@ -58,6 +58,12 @@ struct GemmArgs {
     int inter;
     float swiglu_limit;         // > 0: SwiGLU inputs clamped, g <= L, |u| <= L (FWD_GU, BWD_DOWN epilogues)
     int mg_bf16;                // WGRAD: main_grad is bf16 (bf16(mg + bf16(dW))), else fp32 (mg + dW)
+    // per-expert descriptor tables in device memory (null: the 3D maps, expert = z);
+    // entry e is expert e's own map (z = 0)
+    const CUtensorMap* b0_tab;
+    const CUtensorMap* b1_tab;
+    const CUtensorMap* c0_tab;
+    const CUtensorMap* c1_tab;
     int* status;
     // MXFP8 (block-scaled) GEMMs
     uint8_t* q_out;             // E4M3 copy of the epilogue's GEMM-operand output (a, or [dg|du])

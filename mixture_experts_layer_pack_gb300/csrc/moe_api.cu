@@ -4,6 +4,8 @@
 #include "../../include/moe.h"
 #include "internal.h"
 
+#include <algorithm>
+#include <array>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -22,6 +24,13 @@ using namespace moe;
 namespace {
 
 constexpr size_t kAlign = 256;
+
+// per-expert descriptor tables: one TMA descriptor per expert for each use of a
+// routed weight (each GEMM loads its own box shape) and of a routed main_grad
+enum TableId : int {
+    TB_FWD_GU_G = 0, TB_FWD_GU_U, TB_FWD_DOWN, TB_BWD_DOWN, TB_BWD_GU_G, TB_BWD_GU_U,
+    TB_MG_G, TB_MG_U, TB_MG_D, kTables
+};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -89,6 +98,8 @@ struct Workspace {
     // gate weight's gradient, gate * a_shared (the gated down wgrad operand)
     float *partial_s, *dz, *gpart;
     __nv_bfloat16* ap_s;
+    // per-expert TMA descriptors of the tables (kTables x E)
+    CUtensorMap* tabs;
     // MXFP8 only: quantised backward operands and the swizzled weight scales
     uint8_t *go_q, *go_sf, *dgdu_q, *dgdu_sf;
     uint8_t *sf_fc1_row, *sf_down_row, *sf_down_col, *sf_fc1_col;
@@ -121,6 +132,7 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->dz = c.take<float>(size_t(s.Tmax));
     w->gpart = c.take<float>(size_t((s.Tmax + kGateChunk - 1) / kGateChunk) * s.H);
     w->ap_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
+    w->tabs = c.take<CUtensorMap>(size_t(kTables) * s.E);
     if (s.mx) {
         w->go_q = c.take<uint8_t>(size_t(s.rows) * s.H);
         w->go_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -171,8 +183,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 // a weight view of N rows x K columns (per expert when routed)
 bool check_view(const moe_wview& v, int64_t N, int64_t K, bool routed) {
-    if (!v.data || !aligned16(v.data)) return false;
     if (v.row_stride < K || (v.row_stride * 2) % 16) return false;
+    if (routed && v.expert_ptrs) return true;  // per-expert pointers: checked as they are encoded
+    if (!v.data || !aligned16(v.data)) return false;
     if (routed && (v.expert_stride < N * v.row_stride || (v.expert_stride * 2) % 16)) return false;
     return true;
 }
@@ -221,8 +234,9 @@ bool check_mg(const moe_main_grads* m) {
     const int64_t q = m->dtype == MOE_G_BF16 ? 8 : 4;  // elements per 16 bytes
     void* const p[6] = {m->shared_gate, m->shared_up, m->shared_down, m->routed_gate, m->routed_up, m->routed_down};
     for (int i = 0; i < 6; ++i) {
-        if (!p[i] || !aligned16(p[i])) return false;
         if (m->strides[i][1] % q || m->strides[i][1] <= 0) return false;
+        if (i >= 3 && m->expert_ptrs[i - 3]) continue;  // per-expert table: checked as it is encoded
+        if (!p[i] || !aligned16(p[i])) return false;
         if (i >= 3 && (m->strides[i][0] % q || m->strides[i][0] <= 0)) return false;
     }
     return true;
@@ -289,6 +303,14 @@ struct moe_handle {
     int device;
     int sms;
     bool weights_prepared = false;  // MXFP8: moe_prepare_weights has run
+    // host copies of the per-expert descriptor tables last uploaded to ws.tabs
+    struct Table {
+        bool valid = false;
+        std::array<int64_t, 4> key{};        // what else the descriptors encode (strides, box, dtype)
+        std::vector<const void*> ptrs;
+        std::vector<CUtensorMap> maps;
+    };
+    Table tables[kTables];
     // per-kernel timing (moe_profile_enable)
     bool profiling = false;
     struct Rec {
@@ -310,6 +332,65 @@ cudaEvent_t take_event(moe_handle* h) {
     cudaEvent_t e = nullptr;
     if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
     return e;
+}
+
+// Per-expert descriptor table `id`: encodes one descriptor per expert with
+// enc(map, expert pointer) when the pointers or `key` (what else the
+// descriptors encode) changed since the last upload, and uploads them into the
+// workspace; *tab = their device address, *first = expert 0's descriptor (a
+// valid map for the kernel's own map parameter).
+template <class Enc>
+moe_status expert_table(moe_handle* h, int id, const void* const* ptrs, const std::array<int64_t, 4>& key, Enc enc,
+                        cudaStream_t st, const CUtensorMap** tab, CUtensorMap* first) {
+    moe_handle::Table& tb = h->tables[id];
+    const int64_t E = h->s.E;
+    CUtensorMap* dev = h->ws.tabs + size_t(id) * size_t(E);
+    if (!(tb.valid && tb.key == key && std::equal(ptrs, ptrs + E, tb.ptrs.begin()))) {
+        tb.valid = false;
+        tb.ptrs.assign(ptrs, ptrs + E);
+        tb.maps.resize(size_t(E));
+        for (int64_t e = 0; e < E; ++e)
+            if (!ptrs[e] || (reinterpret_cast<uintptr_t>(ptrs[e]) & 15) || !enc(&tb.maps[size_t(e)], ptrs[e]))
+                return MOE_ERR_INVALID_ARG;
+        // pageable source: the copy is staged before the call returns, so the host copy may change later
+        if (cudaMemcpyAsync(dev, tb.maps.data(), size_t(E) * sizeof(CUtensorMap), cudaMemcpyHostToDevice, st) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        tb.key = key;
+        tb.valid = true;
+    }
+    *tab = dev;
+    *first = tb.maps[0];
+    return MOE_OK;
+}
+
+// B-operand map of a routed BF16 weight view: the 3D map over all experts, or,
+// for a per-expert table, expert descriptors (box of 64 columns x box_rows rows)
+moe_status routed_map(moe_handle* h, int id, const moe_wview& v, int64_t rows, int64_t cols, uint32_t box_rows,
+                      cudaStream_t st, CUtensorMap* m, const CUtensorMap** tab) {
+    *tab = nullptr;
+    if (!v.expert_ptrs)
+        return map_weight(m, v, h->s.E, rows, cols, 64, box_rows) ? MOE_OK : MOE_ERR_INVALID_ARG;
+    return expert_table(
+        h, id, v.expert_ptrs, {v.row_stride, rows, cols, int64_t(box_rows)},
+        [&](CUtensorMap* mm, const void* p) {
+            moe_wview one = v;
+            one.data = p;
+            return map_weight(mm, one, 1, rows, cols, 64, box_rows);
+        },
+        st, tab, m);
+}
+
+// map of a routed main_grad: the 3D map, or per-expert descriptors from a table
+moe_status routed_mg_map(moe_handle* h, int id, void* base, void* const* table, int64_t rows, int64_t cols,
+                         int64_t es, int64_t rs, bool bf16, cudaStream_t st, CUtensorMap* m, const CUtensorMap** tab) {
+    *tab = nullptr;
+    if (!table)
+        return map_main_grad(m, base, h->s.E, rows, cols, es, rs, bf16) ? MOE_OK : MOE_ERR_INVALID_ARG;
+    return expert_table(
+        h, id, const_cast<const void* const*>(table), {rs, rows, cols, bf16 ? 1 : 0},
+        [&](CUtensorMap* mm, const void* p) { return map_main_grad(mm, const_cast<void*>(p), 1, rows, cols, 0, rs, bf16); },
+        st, tab, m);
 }
 
 // brackets the launches of one kernel class with events while profiling
@@ -446,11 +527,19 @@ void moe_saved_destroy(moe_saved* s) { delete s; }
         if ((x) != cudaSuccess) return MOE_ERR_CUDA;     \
     } while (0)
 
+#define MOE_TRY(x)                                       \
+    do {                                                 \
+        const moe_status st_ = (x);                      \
+        if (st_ != MOE_OK) return st_;                   \
+    } while (0)
+
 moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float* probs, const uint8_t* routing_map,
                        const moe_weights* w, void* out, moe_saved* saved, void* stream) {
     if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
     const Shape& s = h->s;
     if (T < 0 || T > s.Tmax) return MOE_ERR_INVALID_ARG;
+    if (w && s.mx && (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs))
+        return MOE_ERR_UNSUPPORTED;  // per-expert tables are for BF16 routed weights
     if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!hidden || !probs || !routing_map || !out || !aligned16(hidden) || !aligned16(out)))
         return MOE_ERR_INVALID_ARG;
@@ -515,9 +604,9 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
-        if (!map_kmajor(&m.a, b.x_perm, rows, H, H) || !map_weight(&m.b0, w->routed_gate, E, I, H, 64, bn / 2) ||
-            !map_weight(&m.b1, w->routed_up, E, I, H, 64, bn / 2))
-            return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, b.x_perm, rows, H, H)) return MOE_ERR_INVALID_ARG;
+        MOE_TRY(routed_map(h, TB_FWD_GU_G, w->routed_gate, I, H, bn / 2, st, &m.b0, &a.b0_tab));
+        MOE_TRY(routed_map(h, TB_FWD_GU_U, w->routed_up, I, H, bn / 2, st, &m.b1, &a.b1_tab));
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
         a.num_mtiles = rows / kBM;
@@ -576,8 +665,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
-        if (!map_kmajor(&m.a, b.a, rows, I, I) || !map_weight(&m.b0, w->routed_down, E, H, I, 64, bn))
-            return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, b.a, rows, I, I)) return MOE_ERR_INVALID_ARG;
+        MOE_TRY(routed_map(h, TB_FWD_DOWN, w->routed_down, H, I, bn, st, &m.b0, &a.b0_tab));
         m.b1 = m.b0;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
@@ -682,8 +771,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
-        if (!map_kmajor(&m.a, ws.go_perm, rows, H, H) || !map_weight(&m.b0, w->routed_down, E, H, I, 64, 64))
-            return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, ws.go_perm, rows, H, H)) return MOE_ERR_INVALID_ARG;
+        MOE_TRY(routed_map(h, TB_BWD_DOWN, w->routed_down, H, I, 64, st, &m.b0, &a.b0_tab));
         m.b1 = m.b0;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
@@ -760,9 +849,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
-        if (!map_kmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I) || !map_weight(&m.b0, w->routed_gate, E, I, H, 64, 64) ||
-            !map_weight(&m.b1, w->routed_up, E, I, H, 64, 64))
-            return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
+        MOE_TRY(routed_map(h, TB_BWD_GU_G, w->routed_gate, I, H, 64, st, &m.b0, &a.b0_tab));
+        MOE_TRY(routed_map(h, TB_BWD_GU_U, w->routed_up, I, H, 64, st, &m.b1, &a.b1_tab));
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
         a.num_mtiles = rows / kBM;
@@ -802,9 +891,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = E;
         a.m_tiles = 2 * I / kBM;
         a.n_tiles = H / bn;
-        if (!map_main_grad(&m.c0, mg->routed_gate, E, I, H, mg->strides[3][0], mg->strides[3][1], mg_bf16) ||
-            !map_main_grad(&m.c1, mg->routed_up, E, I, H, mg->strides[4][0], mg->strides[4][1], mg_bf16))
-            return MOE_ERR_INVALID_ARG;
+        MOE_TRY(routed_mg_map(h, TB_MG_G, mg->routed_gate, mg->expert_ptrs[0], I, H, mg->strides[3][0],
+                              mg->strides[3][1], mg_bf16, st, &m.c0, &a.c0_tab));
+        MOE_TRY(routed_mg_map(h, TB_MG_U, mg->routed_up, mg->expert_ptrs[1], I, H, mg->strides[4][0],
+                              mg->strides[4][1], mg_bf16, st, &m.c1, &a.c1_tab));
         a.m_split = I;
         a.mg_bf16 = mg_bf16;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
@@ -821,8 +911,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.groups = E;
         a.m_tiles = H / kBM;
         a.n_tiles = I / bn;
-        if (!map_main_grad(&m.c0, mg->routed_down, E, H, I, mg->strides[5][0], mg->strides[5][1], mg_bf16))
-            return MOE_ERR_INVALID_ARG;
+        MOE_TRY(routed_mg_map(h, TB_MG_D, mg->routed_down, mg->expert_ptrs[2], H, I, mg->strides[5][0],
+                              mg->strides[5][1], mg_bf16, st, &m.c0, &a.c0_tab));
         m.c1 = m.c0;
         a.mg_bf16 = mg_bf16;
         Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
@@ -877,6 +967,9 @@ moe_status moe_prepare_weights(moe_handle* h, const moe_weights* w, void* stream
     if (!h) return MOE_ERR_INVALID_ARG;
     const Shape& s = h->s;
     if (!s.mx) return MOE_OK;
+    if (!w) return MOE_ERR_INVALID_ARG;
+    if (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs)
+        return MOE_ERR_UNSUPPORTED;
     if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
     const moe_wview &g = w->routed_gate, &u = w->routed_up, &d = w->routed_down;
     if (g.expert_stride != u.expert_stride || g.row_stride != u.row_stride) return MOE_ERR_INVALID_ARG;
