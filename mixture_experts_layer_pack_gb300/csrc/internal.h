@@ -96,17 +96,20 @@ constexpr int kMxBN = 128;
 constexpr int kMxBK = 128;
 
 // routing
+constexpr int kRankChunk = 128;  // tokens per block of the fused pack/rank kernel
 int route_rank_max_tokens();
+cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
+                                   int* row_of, int* rank, int* hist, int* status, cudaStream_t st);
+cudaError_t launch_route_scan_chunks(int* hist, int T, int E, int* counts, int* offsets, int* offs_pad,
+                                     int* mtile_expert, int* meta, cudaStream_t st);
 cudaError_t launch_route_pack(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
                               int* row_of, int* status, cudaStream_t st);
 cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, int k, int* rank, int* counts,
                               cudaStream_t st);
-cudaError_t launch_route_scan(const int* counts, int E, int* offsets, int* offs_pad, int* mtile_expert, int* meta,
-                              cudaStream_t st);
-cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* counts,
-                               const int* offs_pad, int T, int E, int k, const __nv_bfloat16* hidden, int H,
-                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, uint8_t* x_q,
-                               uint8_t* x_sf, cudaStream_t st);
+cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* chunk_base,
+                               const int* counts, const int* offs_pad, int T, int E, int k,
+                               const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
+                               __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st);
 cudaError_t launch_swizzle_scales(int mode, const uint8_t* src0, const uint8_t* src1, int64_t src_es, int64_t src_rs,
                                   int E, int n_tiles, int k_blocks, int kb_split, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* perm_src_pad, const int* counts,

@@ -91,6 +91,7 @@ moe_status check_config(const moe_config* c, Shape* s) {
 struct Workspace {
     int* status;
     int* rank;  // rank of each route inside its expert
+    int* hist;  // per 128-token chunk and expert: route count, then the chunk's rank offset
     __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
     float *yx, *ys_dxs;  // forward: p*y (routed rows), y_shared; backward: dx (routed rows), dx_shared
     float* partial;
@@ -121,6 +122,7 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     Carver c{base};
     w->status = c.take<int>(64);
     w->rank = c.take<int>(size_t(s.Tmax) * s.k);
+    w->hist = c.take<int>(size_t((s.Tmax + kRankChunk - 1) / kRankChunk) * s.E);
     w->go_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     w->dgdu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
     w->ap = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
@@ -562,12 +564,12 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
 
     // dispatch: route-pack, per-expert ranks, segment scan, placement + row gather
     { Timed tm_(h, MOE_K_ROUTE_PACK, st);
-    MOE_CU(launch_route_pack(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.status, st)); }
+    MOE_CU(launch_route_pack_rank(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.rank, ws.hist, ws.status,
+                                  st)); }
     { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
-    MOE_CU(launch_route_rank(routing_map, b.ids, Ti, E, k, ws.rank, b.counts, st));
-    MOE_CU(launch_route_scan(b.counts, E, b.offsets, b.offs_pad, b.mtile_expert, b.meta, st)); }
+    MOE_CU(launch_route_scan_chunks(ws.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta, st)); }
     { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
-    MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, b.counts, b.offs_pad, Ti, E, k,
+    MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, ws.hist, b.counts, b.offs_pad, Ti, E, k,
                               static_cast<const __nv_bfloat16*>(hidden), H, b.perm_src, b.pp_perm, b.row_of, b.x_perm,
                               mx ? b.x_q : nullptr, mx ? b.x_sf : nullptr, st)); }
 

@@ -13,14 +13,17 @@
 // padded to a multiple of 128 rows so that a GEMM row tile never spans two
 // experts; padding rows have source token -1, prob 0 and zero activations.
 //
-// Four launches, each parallel over its whole index space:
-//   pack   one warp per token: ids[t,:], pp[t,:], -1 slots; flags rows with > k routes
-//   rank   one block per expert: a stable scan of the expert's map column gives
-//          every routed token its rank inside the expert, and the expert's count
-//   scan   one block: exclusive scans of counts (compact and 128-padded), the
-//          expert of every 128-row tile, the tile count
-//   place  one warp per route (and per padding row): writes the permutation
-//          entries and copies the token's hidden row into its permuted row
+// The forward's three launches:
+//   pack+rank  one thread per token, 128-token blocks: ids[t,:], pp[t,:], -1 slots;
+//              flags rows with > k routes; a ballot per expert ranks the routes
+//              inside the block and counts them per expert
+//   scan       one block: each expert's chunk counts scanned in token order (the
+//              chunk's rank offset, the expert's count), then exclusive scans of
+//              counts (compact and 128-padded), the expert of every 128-row tile
+//   place      one warp per route (and per padding row): writes the permutation
+//              entries and copies the token's hidden row into its permuted row
+// moe_route_noalloc (end of file) ranks with one block per expert instead
+// (route_pack_kernel, route_rank_kernel), whose only scratch is one int per route.
 #include "../../include/moe.h"
 #include "device_common.cuh"
 #include "internal.h"
@@ -146,12 +149,194 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(const uint8_t*
     if (threadIdx.x == 0) counts[e] = total;
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict__ counts_in, int E,
-                                                          int* __restrict__ offsets, int* __restrict__ offs_pad,
-                                                          int* __restrict__ mtile_expert, int* __restrict__ meta) {
+// Fused route-pack and chunk-local rank (the forward's routing). Block c owns
+// tokens [c*C, c*C+C) (C = kRankChunk), one thread per token, warp w its 32
+// tokens. The block first copies its C map rows (one contiguous, coalesced
+// range of the map) into shared memory, rows padded to an odd number of words
+// so that the threads' row reads fall in distinct banks. Each thread counts its
+// row: more than k routes flags the status and drops the row; otherwise its
+// experts, ascending, fill ids/pp (-1 / 0 / row_of -1 pad the slots). One ballot
+// per expert gives the warp's tokens routed to it: a route's rank among them
+// (earlier lanes = earlier tokens) and the warp's count. The counts' exclusive
+// prefix over the block's warps is added to every rank, and the block's totals
+// go to hist[c][e]; a later scan over blocks completes the stable (expert,
+// token) order.
+__global__ void __launch_bounds__(kRankChunk) route_pack_rank_kernel(const uint8_t* __restrict__ map,
+                                                                     const float* __restrict__ probs, int T, int E,
+                                                                     int k, int* __restrict__ ids,
+                                                                     float* __restrict__ pp, int* __restrict__ row_of,
+                                                                     int* __restrict__ rank, int* __restrict__ hist,
+                                                                     int words_aligned, int* status) {
+    constexpr int W = kRankChunk / 32;
+    extern __shared__ int s_dyn[];
+    int* s_cnt = s_dyn;                                           // [W][E]: warp counts, then warp offsets
+    int* s_e = s_cnt + W * E;                                     // [kRankChunk][k]: a token's experts
+    int* s_r = s_e + kRankChunk * k;                              // [kRankChunk][k]: their ranks in the warp
+    const int RW = (E + 3) / 4 + (((E + 3) / 4) % 2 == 0 ? 1 : 0);  // row stride in words (odd)
+    uint32_t* s_rows = reinterpret_cast<uint32_t*>(s_r + kRankChunk * k);  // [kRankChunk][RW]
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * kRankChunk;
+    const int nt = min(kRankChunk, T - t0);
+    const int t = t0 + threadIdx.x;
+    const bool in = threadIdx.x < nt;
+
+    // the chunk's rows: bytes [t0*E, (t0+nt)*E) of the map
+    const uint8_t* src = map + int64_t(t0) * E;
+    if (words_aligned == 4) {  // E % 16 == 0 and a 16-byte aligned map: 16-byte loads, 8 in flight
+        const int eq = E / 16;
+        const int nq = nt * eq;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        for (int i0 = threadIdx.x; i0 < nq; i0 += 8 * blockDim.x) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < nq) v[j] = __ldg(s4 + i);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < nq) {
+                    const int r = i / eq;
+                    uint32_t* d = s_rows + r * RW + 4 * (i - r * eq);
+                    d[0] = v[j].x;
+                    d[1] = v[j].y;
+                    d[2] = v[j].z;
+                    d[3] = v[j].w;
+                }
+            }
+        }
+    } else if (words_aligned) {  // E % 4 == 0 and a 4-byte aligned map
+        const int ew = E / 4;
+        const int nw = nt * ew;
+        for (int i = threadIdx.x; i < nw; i += blockDim.x) {
+            const int r = i / ew;
+            s_rows[r * RW + (i - r * ew)] = __ldg(reinterpret_cast<const uint32_t*>(src) + i);
+        }
+    } else {
+        uint8_t* rows8 = reinterpret_cast<uint8_t*>(s_rows);
+        const int nb = nt * E;
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+            const int r = i / E;
+            rows8[r * RW * 4 + (i - r * E)] = __ldg(src + i);
+        }
+        // zero the tail bytes of each row's last word
+        for (int r = threadIdx.x; r < nt; r += blockDim.x)
+            for (int b = E; b < ((E + 3) / 4) * 4; ++b) rows8[r * RW * 4 + b] = 0;
+    }
+    __syncthreads();
+
+    const uint32_t* my = s_rows + threadIdx.x * RW;
+    const int EW = (E + 3) / 4;
+    int cnt = 0;
+    if (in)
+        for (int j = 0; j < EW; ++j) {
+            const uint32_t v = my[j];
+            cnt += ((v & 0xffu) != 0) + ((v & 0xff00u) != 0) + ((v & 0xff0000u) != 0) + ((v & 0xff000000u) != 0);
+        }
+    bool valid = in;
+    if (in && cnt > k) {  // more routes than slots: flag it, drop the row's routes
+        atomicOr(status, kStatusRouting);
+        valid = false;
+    }
+    // one ballot per expert; only shared memory is touched inside the loop
+    const unsigned lt = (1u << lane) - 1u;
+    int* my_e = s_e + threadIdx.x * k;
+    int* my_r = s_r + threadIdx.x * k;
+    int sl = 0;
+    for (int j = 0; j < EW; ++j) {
+        const uint32_t v = valid ? my[j] : 0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int e = 4 * j + b;
+            if (e >= E) break;
+            const bool on = ((v >> (8 * b)) & 0xffu) != 0;
+            const unsigned m = __ballot_sync(0xffffffffu, on);
+            if (lane == 0) s_cnt[w * E + e] = __popc(m);
+            if (on) {
+                my_e[sl] = e;
+                my_r[sl] = __popc(m & lt);
+                ++sl;
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+#pragma unroll
+        for (int ww = 0; ww < W; ++ww) {
+            const int c = s_cnt[ww * E + e];
+            s_cnt[ww * E + e] = run;
+            run += c;
+        }
+        hist[int64_t(blockIdx.x) * E + e] = run;
+    }
+    __syncthreads();
+    if (!in) return;
+    int* ids_t = ids + int64_t(t) * k;
+    float* pp_t = pp + int64_t(t) * k;
+    int* rk_t = rank + int64_t(t) * k;
+    for (int s0 = 0; s0 < k; s0 += 8) {  // the probs of eight slots in flight at a time
+        float pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            pv[j] = (s0 + j < sl) ? __ldg(probs + int64_t(t) * E + my_e[s0 + j]) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s = s0 + j;
+            if (s >= k) break;
+            if (s < sl) {
+                const int e = my_e[s];
+                ids_t[s] = e;
+                pp_t[s] = pv[j];
+                rk_t[s] = my_r[s] + s_cnt[w * E + e];
+            } else {
+                ids_t[s] = -1;
+                pp_t[s] = 0.0f;
+                row_of[int64_t(t) * k + s] = -1;
+            }
+        }
+    }
+}
+
+size_t pack_rank_smem(int E, int k) {
+    const int RW = (E + 3) / 4 + (((E + 3) / 4) % 2 == 0 ? 1 : 0);
+    return size_t(kRankChunk / 32) * E * sizeof(int) + 2 * size_t(kRankChunk) * k * sizeof(int) +
+           size_t(kRankChunk) * RW * 4;
+}
+
+// One block, thread e per expert: exclusive scan of the chunk totals of
+// expert e in chunk order (hist[c][e] becomes the expert's rank offset of
+// chunk c) and the expert's count, then exclusive scans of the counts
+// (compact and 128-padded), the expert of every 128-row tile and the totals.
+__global__ void __launch_bounds__(1024) route_scan_chunks_kernel(int* __restrict__ hist, int chunks, int E,
+                                                                 int* __restrict__ counts, int* __restrict__ offsets,
+                                                                 int* __restrict__ offs_pad,
+                                                                 int* __restrict__ mtile_expert,
+                                                                 int* __restrict__ meta) {
     __shared__ int s_warp[32];
     const int e = threadIdx.x;
-    const int cnt = e < E ? counts_in[e] : 0;
+    int cnt = 0;
+    if (e < E) {
+        int c = 0;
+        for (; c + 8 <= chunks; c += 8) {  // eight loads in flight per step
+            int h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = hist[int64_t(c + j) * E + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                hist[int64_t(c + j) * E + e] = cnt;
+                cnt += h[j];
+            }
+        }
+        for (; c < chunks; ++c) {
+            const int h = hist[int64_t(c) * E + e];
+            hist[int64_t(c) * E + e] = cnt;
+            cnt += h;
+        }
+        counts[e] = cnt;
+    }
     const int padded = (cnt + kBM - 1) / kBM * kBM;
     int total_cnt, total_pad;
     const int off = block_excl_scan(cnt, s_warp, total_cnt);
@@ -164,9 +349,9 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
     if (e == 0) {
         offsets[E] = total_cnt;
         offs_pad[E] = total_pad;
-        meta[0] = total_pad / kBM;  // number of 128-row tiles
-        meta[1] = total_cnt;        // R, valid routes
-        meta[2] = total_pad;        // rows including padding
+        meta[0] = total_pad / kBM;
+        meta[1] = total_cnt;
+        meta[2] = total_pad;
     }
 }
 
@@ -176,7 +361,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
 // scale-factor layout.
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     const int* __restrict__ ids, const float* __restrict__ pp, const int* __restrict__ rank,
-    const int* __restrict__ counts, const int* __restrict__ offs_pad, int T, int E, int k,
+    const int* __restrict__ chunk_base, const int* __restrict__ counts, const int* __restrict__ offs_pad, int T,
+    int E, int k,
     const uint4* __restrict__ hidden, int vec_per_row, int* __restrict__ perm_src, float* __restrict__ pp_perm,
     int* __restrict__ row_of, uint4* __restrict__ x_perm, uint8_t* __restrict__ x_q, uint8_t* __restrict__ x_sf) {
     const int64_t item = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -186,7 +372,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         const int e = __ldg(ids + item);
         if (e < 0) return;
         const int t = int(item / k);
-        const int pos = __ldg(offs_pad + e) + __ldg(rank + item);
+        const int pos = __ldg(offs_pad + e) + __ldg(rank + item) +
+                        (chunk_base ? __ldg(chunk_base + int64_t(t / kRankChunk) * E + e) : 0);
         if (lane == 0) {
             perm_src[pos] = t;
             pp_perm[pos] = __ldg(pp + item);
@@ -262,23 +449,46 @@ cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_route_scan(const int* counts, int E, int* offsets, int* offs_pad, int* mtile_expert, int* meta,
-                              cudaStream_t st) {
-    const int threads = (E + 31) / 32 * 32;
-    route_scan_kernel<<<1, threads, 0, st>>>(counts, E, offsets, offs_pad, mtile_expert, meta);
+cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
+                                   int* row_of, int* rank, int* hist, int* status, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const size_t smem = pack_rank_smem(E, k);
+    static size_t smem_set = 48 * 1024;
+    if (smem > smem_set) {
+        const cudaError_t e = cudaFuncSetAttribute(route_pack_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(pack_rank_smem(1024, 32)));
+        if (e != cudaSuccess) return e;
+        smem_set = pack_rank_smem(1024, 32);
+    }
+    // 4: 16-byte loads (E % 16 == 0, 16-byte aligned map); 1: 4-byte loads; 0: bytes
+    const uintptr_t mp = reinterpret_cast<uintptr_t>(map);
+    const int words = (E % 16 == 0 && (mp & 15) == 0) ? 4 : ((E % 4 == 0 && (mp & 3) == 0) ? 1 : 0);
+    route_pack_rank_kernel<<<(T + kRankChunk - 1) / kRankChunk, kRankChunk, smem, st>>>(map, probs, T, E, k, ids, pp,
+                                                                                         row_of, rank, hist, words,
+                                                                                         status);
     count_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* counts,
-                               const int* offs_pad, int T, int E, int k, const __nv_bfloat16* hidden, int H,
-                               int* perm_src, float* pp_perm, int* row_of, __nv_bfloat16* x_perm, uint8_t* x_q,
-                               uint8_t* x_sf, cudaStream_t st) {
+cudaError_t launch_route_scan_chunks(int* hist, int T, int E, int* counts, int* offsets, int* offs_pad,
+                                     int* mtile_expert, int* meta, cudaStream_t st) {
+    const int threads = (E + 31) / 32 * 32;
+    route_scan_chunks_kernel<<<1, threads, 0, st>>>(hist, (T + kRankChunk - 1) / kRankChunk, E, counts, offsets,
+                                                    offs_pad, mtile_expert, meta);
+    count_launch();
+    return cudaGetLastError();
+}
+
+
+cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* chunk_base,
+                               const int* counts, const int* offs_pad, int T, int E, int k,
+                               const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
+                               __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st) {
     const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     route_place_kernel<<<unsigned(blocks), 32 * kWarpsPerBlock, 0, st>>>(
-        ids, pp, rank, counts, offs_pad, T, E, k, reinterpret_cast<const uint4*>(hidden), H / 8, perm_src, pp_perm,
-        row_of, reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
+        ids, pp, rank, chunk_base, counts, offs_pad, T, E, k, reinterpret_cast<const uint4*>(hidden), H / 8,
+        perm_src, pp_perm, row_of, reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
     count_launch();
     return cudaGetLastError();
 }

@@ -25,6 +25,7 @@ SMALL = {
     "tiles_ragged": Case(T=300, H=256, E=8, k=2, I=128, seed=21, drop="iid"),
     "bn64_skewed": Case(T=517, H=384, E=12, k=3, I=192, seed=22, routing="zipf", drop="multi"),
     "one_token": Case(T=1, H=128, E=4, k=2, I=64, seed=23),
+    "odd_experts": Case(T=333, H=128, E=13, k=3, I=64, seed=24, drop="iid"),   # byte-wise map rows
 }
 
 
