@@ -270,6 +270,11 @@ enum {
  * stream: no extra GPU work and no host synchronisation. */
 moe_status moe_profile_enable(moe_handle* h, int enable);
 
+/* Restricts the timing to the kernel classes whose bits are set in class_mask
+ * (bit i = class i; all classes by default), so that a measurement can time one
+ * kernel without events between the others. Host-only. */
+moe_status moe_profile_select(moe_handle* h, uint32_t class_mask);
+
 /* Synchronises the recorded events and writes, per kernel class (n entries,
  * n <= MOE_K_COUNT), the summed device time in milliseconds and the number of
  * launches since the previous read; then forgets them. Host arrays. */

@@ -51,7 +51,7 @@ _LOCK = threading.Lock()
 EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size", "moe_saved_create",
             "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
             "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name",
-            "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8")
+            "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8", "moe_profile_select")
 MOE_K_COUNT = 20
 
 
@@ -89,6 +89,7 @@ def load(build_if_missing: bool = True):
         L.moe_launch_count.argtypes = []
         L.moe_launch_count.restype = ctypes.c_uint64
         L.moe_profile_enable.argtypes = [c_void_p, c_int32]
+        L.moe_profile_select.argtypes = [c_void_p, ctypes.c_uint32]
         L.moe_profile_read.argtypes = [c_void_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int64), c_int32]
         L.moe_kernel_name.argtypes = [c_int32]
         L.moe_kernel_name.restype = ctypes.c_char_p
@@ -100,7 +101,8 @@ def load(build_if_missing: bool = True):
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_workspace_size", "moe_saved_size", "moe_create", "moe_saved_create", "moe_forward",
                      "moe_backward", "moe_export_routing", "moe_device_status", "moe_profile_enable",
-                     "moe_profile_read", "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8"):
+                     "moe_profile_read", "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8",
+                     "moe_profile_select"):
             getattr(L, name).restype = c_int32
         _LIB = L
         return L
@@ -232,6 +234,18 @@ def moe_launch_count() -> int:
 
 def moe_profile_enable(h, enable: bool = True):
     _check(load().moe_profile_enable(h, 1 if enable else 0), "moe_profile_enable")
+
+
+def moe_profile_select(h, classes=None):
+    """Time only the given kernel classes (names or indices); None: all of them."""
+    if classes is None:
+        mask = 0xFFFFFFFF
+    else:
+        names = [moe_kernel_name(i) for i in range(MOE_K_COUNT)]
+        mask = 0
+        for c in classes:
+            mask |= 1 << (names.index(c) if isinstance(c, str) else int(c))
+    _check(load().moe_profile_select(h, mask), "moe_profile_select")
 
 
 def moe_profile_read(h) -> dict:

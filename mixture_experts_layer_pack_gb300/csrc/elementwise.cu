@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int* __restrict__ meta, int max_rows, int vec_per_row,
                                                           uint4* __restrict__ dst, uint8_t* __restrict__ dst_q,
                                                           uint8_t* __restrict__ dst_sf) {
+    pdl_wait();
+    pdl_trigger();
     const int rows = min(meta[2], max_rows);
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -65,6 +67,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ ys, const float4* __restrict__ y,
                                                       const int* __restrict__ row_of, int T, int vec_per_row, int k,
                                                       uint4* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t total = int64_t(T) * vec_per_row;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
         const int t = int(i / vec_per_row);
@@ -88,6 +92,8 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict
                                                         int vec_per_row, int k, int E, const float* __restrict__ dz,
                                                         const uint4* __restrict__ gate_w,
                                                         uint4* __restrict__ dhidden, float* __restrict__ dprobs) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     const int64_t total = int64_t(T) * vec_per_row;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += stride) {
@@ -140,20 +146,22 @@ int grid_for(int64_t work, int threads, int num_sms) {
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
                                __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms, cudaStream_t st) {
     const int grid = grid_for(int64_t(max_rows) * 32, 256, num_sms);
-    gather_rows_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(src), perm_src, meta, max_rows, H / 8,
-                                              reinterpret_cast<uint4*>(dst), dst_q, dst_sf);
+    const cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, st,
+                                     reinterpret_cast<const uint4*>(src), perm_src, meta, max_rows, H / 8,
+                                     reinterpret_cast<uint4*>(dst), dst_q, dst_sf);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
                            __nv_bfloat16* out, int num_sms, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
-    combine_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(ys), reinterpret_cast<const float4*>(y),
-                                          row_of, T, H / 8, k, reinterpret_cast<uint4*>(out));
+    const cudaError_t e = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, reinterpret_cast<const float4*>(ys),
+                                     reinterpret_cast<const float4*>(y), row_of, T, H / 8, k,
+                                     reinterpret_cast<uint4*>(out));
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
@@ -162,12 +170,12 @@ cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_
                              cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
-    unpermute_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(dxs), reinterpret_cast<const float4*>(dxp),
-                                            row_of, ids, partial, n_part, T, H / 8, k, E, dz,
-                                            reinterpret_cast<const uint4*>(gate_w), reinterpret_cast<uint4*>(dhidden),
-                                            dprobs);
+    const cudaError_t e = launch_pdl(unpermute_kernel, dim3(grid), dim3(256), 0, st,
+                                     reinterpret_cast<const float4*>(dxs), reinterpret_cast<const float4*>(dxp), row_of,
+                                     ids, partial, n_part, T, H / 8, k, E, dz, reinterpret_cast<const uint4*>(gate_w),
+                                     reinterpret_cast<uint4*>(dhidden), dprobs);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

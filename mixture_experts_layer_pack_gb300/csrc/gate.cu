@@ -26,6 +26,8 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 // combined by a fixed butterfly
 __global__ void __launch_bounds__(256) gate_forward_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
                                                            int T, int vec_per_row, float* __restrict__ gate) {
+    pdl_wait();
+    pdl_trigger();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(256) gate_grad_chunk_kernel(const uint4* __res
                                                               const float* __restrict__ partial, int n_part, int T,
                                                               int vec_per_row, float* __restrict__ dz,
                                                               float4* __restrict__ gpart) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_dz[kGateChunk];
     const int t0 = blockIdx.x * kGateChunk;
     const int nt = min(kGateChunk, T - t0);
@@ -82,6 +86,8 @@ __global__ void __launch_bounds__(256) gate_grad_chunk_kernel(const uint4* __res
 // mg[h] = bf16(mg[h] + bf16(sum))
 __global__ void __launch_bounds__(256) gate_grad_reduce_kernel(const float* __restrict__ gpart, int chunks, int H,
                                                                void* __restrict__ mg, int mg_bf16) {
+    pdl_wait();
+    pdl_trigger();
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
     float sum = 0.0f;
@@ -100,24 +106,26 @@ cudaError_t launch_gate_forward(const __nv_bfloat16* hidden, const __nv_bfloat16
                                 cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int blocks = (T * 32 + 255) / 256;
-    gate_forward_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden),
-                                                reinterpret_cast<const uint4*>(w), T, H / 8, gate);
+    const cudaError_t e = launch_pdl(gate_forward_kernel, dim3(blocks), dim3(256), 0, st,
+                                     reinterpret_cast<const uint4*>(hidden), reinterpret_cast<const uint4*>(w), T,
+                                     H / 8, gate);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_gate_backward(const __nv_bfloat16* hidden, const float* gate, const float* partial, int n_part,
                                  int T, int H, float* dz, float* gpart, void* mg_gate, bool mg_bf16, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int chunks = (T + kGateChunk - 1) / kGateChunk;
-    gate_grad_chunk_kernel<<<chunks, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden), gate, partial, n_part, T,
-                                                   H / 8, dz, reinterpret_cast<float4*>(gpart));
+    cudaError_t e = launch_pdl(gate_grad_chunk_kernel, dim3(chunks), dim3(256), 0, st,
+                               reinterpret_cast<const uint4*>(hidden), gate, partial, n_part, T, H / 8, dz,
+                               reinterpret_cast<float4*>(gpart));
     count_launch();
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    gate_grad_reduce_kernel<<<(H + 255) / 256, 256, 0, st>>>(gpart, chunks, H, mg_gate, mg_bf16 ? 1 : 0);
+    e = launch_pdl(gate_grad_reduce_kernel, dim3((H + 255) / 256), dim3(256), 0, st, gpart, chunks, H, mg_gate,
+                   mg_bf16 ? 1 : 0);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

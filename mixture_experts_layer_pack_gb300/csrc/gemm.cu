@@ -576,6 +576,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // from here on the predecessor's writes are visible (prologue above touched no global memory)
+    pdl_trigger();
 
     int total_tiles;
     if (OP == OP_WGRAD)
@@ -801,6 +803,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // from here on the predecessor's writes are visible (prologue above touched no global memory)
+    pdl_trigger();
     const int total_tiles = (args.num_mtiles_dev ? *args.num_mtiles_dev : args.num_mtiles) * args.n_tiles;
 
     if (warp == 0) {
@@ -938,9 +942,9 @@ cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaSt
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<grid, kGemmThreads, MxCfg::SMEM, st>>>(m.a, m.b0, m.b1, a);
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), MxCfg::SMEM, st, m.a, m.b0, m.b1, a);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int OP, int BN, bool CLAMP>
@@ -953,9 +957,10 @@ cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStrea
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<grid, kGemmThreads, Cfg<OP, BN>::SMEM, st>>>(m.a, m.b0, m.b1, m.c0, m.c1, a);
+    const cudaError_t e =
+        launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg<OP, BN>::SMEM, st, m.a, m.b0, m.b1, m.c0, m.c1, a);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int OP, bool CLAMP = false>

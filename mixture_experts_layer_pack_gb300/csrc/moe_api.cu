@@ -313,8 +313,9 @@ struct moe_handle {
         std::vector<CUtensorMap> maps;
     };
     Table tables[kTables];
-    // per-kernel timing (moe_profile_enable)
+    // per-kernel timing (moe_profile_enable, moe_profile_select)
     bool profiling = false;
+    uint32_t profile_mask = ~0u;  // kernel classes bracketed by events
     struct Rec {
         int cls;
         cudaEvent_t start, stop;
@@ -402,7 +403,8 @@ struct Timed {
     cudaStream_t st;
     cudaEvent_t start = nullptr;
     Timed(moe_handle* h_, int cls_, cudaStream_t st_) : h(h_), cls(cls_), st(st_) {
-        if (h->profiling && (start = take_event(h)) != nullptr) cudaEventRecord(start, st);
+        if (h->profiling && ((h->profile_mask >> cls) & 1u) && (start = take_event(h)) != nullptr)
+            cudaEventRecord(start, st);
     }
     ~Timed() {
         if (!start) return;
@@ -1012,6 +1014,12 @@ moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* id
     if (perm_src || row_of)
         MOE_CU(launch_export_routing(b.ids, b.row_of, b.perm_src, b.counts, b.offsets, b.offs_pad, b.mtile_expert,
                                      b.meta, int(T), int(s.k), int(s.rows), perm_src, row_of, st));
+    return MOE_OK;
+}
+
+moe_status moe_profile_select(moe_handle* h, uint32_t class_mask) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->profile_mask = class_mask;
     return MOE_OK;
 }
 

@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kRankChunk) route_pack_rank_kernel(const uint8
                                                                      float* __restrict__ pp, int* __restrict__ row_of,
                                                                      int* __restrict__ rank, int* __restrict__ hist,
                                                                      int words_aligned, int* status) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int W = kRankChunk / 32;
     extern __shared__ int s_dyn[];
     int* s_cnt = s_dyn;                                           // [W][E]: warp counts, then warp offsets
@@ -315,6 +317,8 @@ __global__ void __launch_bounds__(1024) route_scan_chunks_kernel(int* __restrict
                                                                  int* __restrict__ offs_pad,
                                                                  int* __restrict__ mtile_expert,
                                                                  int* __restrict__ meta) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_warp[32];
     const int e = threadIdx.x;
     int cnt = 0;
@@ -365,6 +369,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     int E, int k,
     const uint4* __restrict__ hidden, int vec_per_row, int* __restrict__ perm_src, float* __restrict__ pp_perm,
     int* __restrict__ row_of, uint4* __restrict__ x_perm, uint8_t* __restrict__ x_q, uint8_t* __restrict__ x_sf) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t item = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int64_t n_routes = int64_t(T) * k;
@@ -463,20 +469,21 @@ cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T
     // 4: 16-byte loads (E % 16 == 0, 16-byte aligned map); 1: 4-byte loads; 0: bytes
     const uintptr_t mp = reinterpret_cast<uintptr_t>(map);
     const int words = (E % 16 == 0 && (mp & 15) == 0) ? 4 : ((E % 4 == 0 && (mp & 3) == 0) ? 1 : 0);
-    route_pack_rank_kernel<<<(T + kRankChunk - 1) / kRankChunk, kRankChunk, smem, st>>>(map, probs, T, E, k, ids, pp,
-                                                                                         row_of, rank, hist, words,
-                                                                                         status);
+    const cudaError_t e = launch_pdl(route_pack_rank_kernel, dim3((T + kRankChunk - 1) / kRankChunk),
+                                     dim3(kRankChunk), smem, st, map, probs, T, E, k, ids, pp, row_of, rank, hist,
+                                     words, status);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_route_scan_chunks(int* hist, int T, int E, int* counts, int* offsets, int* offs_pad,
                                      int* mtile_expert, int* meta, cudaStream_t st) {
     const int threads = (E + 31) / 32 * 32;
-    route_scan_chunks_kernel<<<1, threads, 0, st>>>(hist, (T + kRankChunk - 1) / kRankChunk, E, counts, offsets,
-                                                    offs_pad, mtile_expert, meta);
+    const cudaError_t e = launch_pdl(route_scan_chunks_kernel, dim3(1), dim3(threads), 0, st, hist,
+                                     (T + kRankChunk - 1) / kRankChunk, E, counts, offsets, offs_pad, mtile_expert,
+                                     meta);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 
@@ -486,11 +493,12 @@ cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank,
                                __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st) {
     const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    route_place_kernel<<<unsigned(blocks), 32 * kWarpsPerBlock, 0, st>>>(
-        ids, pp, rank, chunk_base, counts, offs_pad, T, E, k, reinterpret_cast<const uint4*>(hidden), H / 8,
-        perm_src, pp_perm, row_of, reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
+    const cudaError_t e = launch_pdl(route_place_kernel, dim3(unsigned(blocks)), dim3(32 * kWarpsPerBlock), 0, st,
+                                     ids, pp, rank, chunk_base, counts, offs_pad, T, E, k,
+                                     reinterpret_cast<const uint4*>(hidden), H / 8, perm_src, pp_perm, row_of,
+                                     reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* perm_src_pad, const int* counts,
