@@ -174,22 +174,22 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4):
         "route_scan": (0, T * E + T * k * b4 + E * b4),
         "route_place": (0, T * k * 12 + R * 12 + 2 * R * H * b2 + q_rows),
         "gather_rows": (0, 2 * R * H * b2 + q_rows),
-        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * ab + W_fc1 + R * I * b2 + R * 2 * I * b4 + q_a),
-        "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * b2 + T * 2 * I * b4),
-        "gemm_fwd_down_routed": (2 * R * I * H, R * I * ab + W_down + R * H * b4),
-        "gemm_fwd_down_shared": (2 * T * I * H, T * I * b2 + H * I * b2 + T * H * b4),
-        "combine": (0, T * H * b4 + R * H * b4 + T * H * b2),
-        "gemm_bwd_down_routed": (2 * R * H * I, R * H * ab + W_down + R * I * b2 + R * 2 * I * b4
+        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * ab + W_fc1 + R * I * b2 + R * 2 * I * b2 + q_a),
+        "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * b2 + T * 2 * I * b2),
+        "gemm_fwd_down_routed": (2 * R * I * H, R * I * ab + W_down + R * H * b2),
+        "gemm_fwd_down_shared": (2 * T * I * H, T * I * b2 + H * I * b2 + T * H * b2),
+        "combine": (0, T * H * b2 + R * H * b2 + T * k * b4 + T * H * b2),
+        "gemm_bwd_down_routed": (2 * R * H * I, R * H * ab + W_down + R * I * b2 + R * 2 * I * b2
                                  + R * 2 * I * b2 + R * I * b2 + q_dgdu),
-        "gemm_bwd_down_shared": (2 * T * H * I, T * H * b2 + H * I * b2 + T * I * b2 + T * 2 * I * b4
+        "gemm_bwd_down_shared": (2 * T * H * I, T * H * b2 + H * I * b2 + T * I * b2 + T * 2 * I * b2
                                  + T * 2 * I * b2),
-        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * ab + W_fc1 + R * H * b4),
-        "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * b2 + 2 * I * H * b2 + T * H * b4),
+        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * ab + W_fc1 + R * H * b2),
+        "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * b2 + 2 * I * H * b2 + T * H * b2),
         "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * b2 + R * H * b2 + E_act * 2 * I * H * 2 * mg_bytes),
         "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * b2 + E_act * H * I * 2 * mg_bytes),
         "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * b2 + T * H * b2 + 2 * I * H * 2 * mg_bytes),
         "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * b2 + H * I * 2 * mg_bytes),
-        "unpermute": (0, T * H * b4 + R * H * b4 + T * H * b2 + T * E * b4),
+        "unpermute": (0, T * H * b2 + R * H * b2 + T * H * b2 + T * E * b4),
         "shared_gate_fwd": (2 * T * H, T * H * b2 + H * b2 + T * b4),
         "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 2 * mg_bytes),
     }

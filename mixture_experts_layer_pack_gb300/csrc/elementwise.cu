@@ -6,8 +6,8 @@
 // (dispatch, combine) and Design > Authoritative routing maps (the backward
 // adapter scatters router-weight gradients into the dense prob tensor).
 //
-// Rows are moved as 16-byte vectors; the routed and shared partial results
-// arrive in fp32 and every sum runs in fp32 in slot order, so the results are
+// Rows are moved as 16-byte vectors of 8 bf16; the experts' bf16 outputs and
+// input gradients are summed in fp32 in slot order, so the results are
 // deterministic and rounded to bf16 once.
 #include "device_common.cuh"
 #include "internal.h"
@@ -44,16 +44,28 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     }
 }
 
-__device__ __forceinline__ void add_f32x8(float (&acc)[8], const float4* p) {
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    acc[0] += a.x;
-    acc[1] += a.y;
-    acc[2] += a.z;
-    acc[3] += a.w;
-    acc[4] += b.x;
-    acc[5] += b.y;
-    acc[6] += b.z;
-    acc[7] += b.w;
+// acc += w * (8 bf16 at p)
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], const uint4* p, float w) {
+    const uint4 v = __ldg(p);
+    float f[8];
+    unpack_bf16x2(v.x, f[0], f[1]);
+    unpack_bf16x2(v.y, f[2], f[3]);
+    unpack_bf16x2(v.z, f[4], f[5]);
+    unpack_bf16x2(v.w, f[6], f[7]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
+}
+
+// acc += 8 bf16 at p
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4* p) {
+    const uint4 v = __ldg(p);
+    float f[8];
+    unpack_bf16x2(v.x, f[0], f[1]);
+    unpack_bf16x2(v.y, f[2], f[3]);
+    unpack_bf16x2(v.z, f[4], f[5]);
+    unpack_bf16x2(v.w, f[6], f[7]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] += f[j];
 }
 
 __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
@@ -61,11 +73,12 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
                       pack_bf16x2(acc[6], acc[7]));
 }
 
-// out[t] = y_shared[t] + sum over valid slots s of y[row_of[t,s]], fp32 inputs,
-// one bf16 rounding at the end (y rows already carry their prob: the down
-// projection's epilogue scales them); 8 columns per thread
-__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ ys, const float4* __restrict__ y,
-                                                      const int* __restrict__ row_of, int T, int vec_per_row, int k,
+// out[t] = gate[t] y_shared[t] + sum over valid slots s of pp[t,s] y[row_of[t,s]]
+// (gate 1 without a shared output gate): bf16 expert outputs, fp32 sum in slot
+// order, one bf16 rounding at the end; 8 columns per thread
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ ys, const float* __restrict__ gate,
+                                                      const uint4* __restrict__ y, const int* __restrict__ row_of,
+                                                      const float* __restrict__ pp, int T, int vec_per_row, int k,
                                                       uint4* __restrict__ out) {
     pdl_wait();
     pdl_trigger();
@@ -74,10 +87,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
         const int t = int(i / vec_per_row);
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        add_f32x8(acc, ys + 2 * i);
+        fma_bf16x8(acc, ys + i, gate ? __ldg(gate + t) : 1.0f);
         for (int s = 0; s < k; ++s) {
             const int r = __ldg(row_of + int64_t(t) * k + s);
-            if (r >= 0) add_f32x8(acc, y + 2 * (int64_t(r) * vec_per_row + v));
+            if (r >= 0) fma_bf16x8(acc, y + int64_t(r) * vec_per_row + v, __ldg(pp + int64_t(t) * k + s));
         }
         out[i] = pack_bf16x8(acc);
     }
@@ -86,7 +99,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
 // dhidden[t] = dx_shared[t] (+ dz[t] w, the shared output gate's term) + sum
 // over valid slots of dx_perm[row_of[t,s]];
 // dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map
-__global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict__ dxs, const float4* __restrict__ dxp,
+__global__ void __launch_bounds__(256) unpermute_kernel(const uint4* __restrict__ dxs, const uint4* __restrict__ dxp,
                                                         const int* __restrict__ row_of, const int* __restrict__ ids,
                                                         const float* __restrict__ partial, int n_part, int T,
                                                         int vec_per_row, int k, int E, const float* __restrict__ dz,
@@ -100,7 +113,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict
         const int t = int(i / vec_per_row);
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        add_f32x8(acc, dxs + 2 * i);
+        add_bf16x8(acc, dxs + i);
         if (dz) {
             const float d = __ldg(dz + t);
             const uint4 wv = __ldg(gate_w + v);
@@ -114,7 +127,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const float4* __restrict
         }
         for (int s = 0; s < k; ++s) {
             const int r = __ldg(row_of + int64_t(t) * k + s);
-            if (r >= 0) add_f32x8(acc, dxp + 2 * (int64_t(r) * vec_per_row + v));
+            if (r >= 0) add_bf16x8(acc, dxp + int64_t(r) * vec_per_row + v);
         }
         dhidden[i] = pack_bf16x8(acc);
     }
@@ -153,25 +166,25 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, co
     return e;
 }
 
-cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
-                           __nv_bfloat16* out, int num_sms, cudaStream_t st) {
+cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __nv_bfloat16* y, const int* row_of,
+                           const float* pp, int T, int H, int k, __nv_bfloat16* out, int num_sms, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
-    const cudaError_t e = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, reinterpret_cast<const float4*>(ys),
-                                     reinterpret_cast<const float4*>(y), row_of, T, H / 8, k,
+    const cudaError_t e = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, reinterpret_cast<const uint4*>(ys),
+                                     gate, reinterpret_cast<const uint4*>(y), row_of, pp, T, H / 8, k,
                                      reinterpret_cast<uint4*>(out));
     count_launch();
     return e;
 }
 
-cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
+cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,
                              const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
                              const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, int num_sms,
                              cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
     const cudaError_t e = launch_pdl(unpermute_kernel, dim3(grid), dim3(256), 0, st,
-                                     reinterpret_cast<const float4*>(dxs), reinterpret_cast<const float4*>(dxp), row_of,
+                                     reinterpret_cast<const uint4*>(dxs), reinterpret_cast<const uint4*>(dxp), row_of,
                                      ids, partial, n_part, T, H / 8, k, E, dz, reinterpret_cast<const uint4*>(gate_w),
                                      reinterpret_cast<uint4*>(dhidden), dprobs);
     count_launch();

@@ -5,10 +5,10 @@
 // integration", Summary: routed and shared expert computation; backward per
 // "core.transformer.moe.megakernel.mok.runtime", _MoKAutograd.backward):
 //
-//   OP_FWD_GU   [R,2I] = X_perm[R,H] . W_fc1[e]^T     epilogue a = silu(g)*u (bf16), keeps g,u (fp32)
-//   OP_FWD_DOWN [R,H]  = a[R,I] . W_down[e]^T          epilogue y = p * acc (fp32)
+//   OP_FWD_GU   [R,2I] = X_perm[R,H] . W_fc1[e]^T     epilogue g,u -> bf16 (kept), a = silu(g)*u (bf16)
+//   OP_FWD_DOWN [R,H]  = a[R,I] . W_down[e]^T          epilogue y -> bf16 (the combine weights it)
 //   OP_BWD_DOWN [R,I]  = go_perm[R,H] . W_down[e]      epilogue SwiGLU backward, dprob partials
-//   OP_BWD_GU   [R,H]  = [dg|du][R,2I] . W_fc1[e]      epilogue store (fp32)
+//   OP_BWD_GU   [R,H]  = [dg|du][R,2I] . W_fc1[e]      epilogue dx -> bf16
 //   OP_WGRAD    [M,N] += A[seg,M]^T . B[seg,N]        epilogue fp32 load-add-store of main_grad
 //
 // Rows of the routed GEMMs are the dispatch permutation, each expert's
@@ -218,7 +218,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             for (int i = 0; i < 8; ++i) {
                 const int row = m_base + i * 4 + sub_row;
                 const float4 g4 = gv[i], u4 = uv[i];
-                float gc[4] = {g4.x, g4.y, g4.z, g4.w}, uc[4] = {u4.x, u4.y, u4.z, u4.w};
+                // g, u are passed on in bf16; a is computed from those values
+                const uint2 gb = make_uint2(pack_bf16x2(g4.x, g4.y), pack_bf16x2(g4.z, g4.w));
+                const uint2 ub = make_uint2(pack_bf16x2(u4.x, u4.y), pack_bf16x2(u4.z, u4.w));
+                float gc[4], uc[4];
+                unpack_bf16x2(gb.x, gc[0], gc[1]);
+                unpack_bf16x2(gb.y, gc[2], gc[3]);
+                unpack_bf16x2(ub.x, uc[0], uc[1]);
+                unpack_bf16x2(ub.y, uc[2], uc[3]);
                 if (CLAMP) {  // clamped SwiGLU inputs; g, u are saved unclamped
 #pragma unroll
                     for (int z = 0; z < 4; ++z) {
@@ -245,14 +252,12 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                 if (row >= a.rows_valid) continue;
                 *reinterpret_cast<uint2*>(a.out0 + int64_t(row) * a.ld_out0 + col) =
                     make_uint2(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]));
-                float* gu = a.outf + int64_t(row) * a.ld_outf;
-                *reinterpret_cast<float4*>(gu + col) = g4;
-                *reinterpret_cast<float4*>(gu + a.inter + col) = u4;
+                __nv_bfloat16* gu = a.outh + int64_t(row) * a.ld_outh;
+                *reinterpret_cast<uint2*>(gu + col) = gb;
+                *reinterpret_cast<uint2*>(gu + a.inter + col) = ub;
             }
         }
     } else if (OP == OP_FWD_DOWN || OP == OP_BWD_GU) {
-        const float lane_scale = (OP == OP_FWD_DOWN && a.row_scale && lane_row_valid) ? a.row_scale[m_base + lane]
-                                                                                       : 1.0f;
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += kEpiHalves) {
             float v[32];
@@ -261,18 +266,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             const int col = t.nt * BN + c * 32 + sub_col;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int r_local = i * 4 + sub_row;
-                const float sc = __shfl_sync(0xffffffffu, lane_scale, r_local);
-                float4 x = staged(staging, i);
-                const int row = m_base + r_local;
+                const float4 x = staged(staging, i);
+                const int row = m_base + i * 4 + sub_row;
                 if (row >= a.rows_valid) continue;
-                if (OP == OP_FWD_DOWN) {
-                    x.x *= sc;
-                    x.y *= sc;
-                    x.z *= sc;
-                    x.w *= sc;
-                }
-                *reinterpret_cast<float4*>(a.outf + int64_t(row) * a.ld_outf + col) = x;
+                *reinterpret_cast<uint2*>(a.outh + int64_t(row) * a.ld_outh + col) =
+                    make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
             }
             __syncwarp();
         }
@@ -289,19 +287,17 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             const int col = t.nt * BN + c * 32 + sub_col;
             // load phase: every input of the chunk is requested before any result
             // is stored, so the eight row steps share one memory latency
-            uint2 aw[8];
-            float4 g4[8], u4[8];
+            uint2 aw[8], gw[8], uw[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = m_base + i * 4 + sub_row;
                 if (row < a.rows_valid) {
                     aw[i] = __ldg(reinterpret_cast<const uint2*>(a.in0 + int64_t(row) * a.ld_in0 + col));
-                    const float* gu = a.inf + int64_t(row) * a.ld_inf;
-                    g4[i] = __ldg(reinterpret_cast<const float4*>(gu + col));
-                    u4[i] = __ldg(reinterpret_cast<const float4*>(gu + a.inter + col));
+                    const __nv_bfloat16* gu = a.inh + int64_t(row) * a.ld_inh;
+                    gw[i] = __ldg(reinterpret_cast<const uint2*>(gu + col));
+                    uw[i] = __ldg(reinterpret_cast<const uint2*>(gu + a.inter + col));
                 } else {
-                    aw[i] = make_uint2(0, 0);
-                    g4[i] = u4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    aw[i] = gw[i] = uw[i] = make_uint2(0, 0);
                 }
             }
 #pragma unroll
@@ -314,8 +310,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                 unpack_bf16x2(aw[i].x, av[0], av[1]);
                 unpack_bf16x2(aw[i].y, av[2], av[3]);
                 const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                const float gv[4] = {g4[i].x, g4[i].y, g4[i].z, g4[i].w};
-                const float uv[4] = {u4[i].x, u4[i].y, u4[i].z, u4[i].w};
+                float gv[4], uv[4];
+                unpack_bf16x2(gw[i].x, gv[0], gv[1]);
+                unpack_bf16x2(gw[i].y, gv[2], gv[3]);
+                unpack_bf16x2(uw[i].x, uv[0], uv[1]);
+                unpack_bf16x2(uw[i].y, uv[2], uv[3]);
                 float dg[4], du[4], ap[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {

@@ -21,7 +21,7 @@ constexpr int kStatusTimeout = 2;  // a bounded wait gave up
 // the five GEMM shapes of the layer
 enum GemmOp : int {
     OP_FWD_GU = 0,    // [a | g,u] = SwiGLU(X W_fc1^T): A K-major rows, B = gate/up rows (K-major)
-    OP_FWD_DOWN = 1,  // y = p * (a W_down^T): A K-major, B = W_down rows (K-major)
+    OP_FWD_DOWN = 1,  // y = a W_down^T: A K-major, B = W_down rows (K-major)
     OP_BWD_DOWN = 2,  // da_u = go W_down; SwiGLU backward epilogue: A K-major, B = W_down (N-major)
     OP_BWD_GU = 3,    // dx = [dg|du] W_fc1: A K-major (K = 2I), B = gate/up (N-major)
     OP_WGRAD = 4,     // main_grad += A^T B over a token segment: A, B both M/N-major
@@ -46,13 +46,13 @@ struct GemmArgs {
     int64_t ld_out0;
     __nv_bfloat16* out1;        // p * a
     int64_t ld_out1;
-    float* outf;                // fp32 intermediates: [g|u], p*y, dx
-    int64_t ld_outf;
+    __nv_bfloat16* outh;        // bf16 GEMM results passed on: [g|u] (kept for backward), y, dx
+    int64_t ld_outh;
     const __nv_bfloat16* in0;   // a
     int64_t ld_in0;
-    const float* inf;           // [g|u]
-    int64_t ld_inf;
-    const float* row_scale;     // per-row prob (null: 1)
+    const __nv_bfloat16* inh;   // [g|u]
+    int64_t ld_inh;
+    const float* row_scale;     // BWD_DOWN: per-row prob (null: 1)
     float* partial;             // per row: n_tiles * kEpiHalves partial dot products (null: skip)
     int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
     int inter;
@@ -120,9 +120,9 @@ cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* 
 // elementwise / copy
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
                                __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms, cudaStream_t st);
-cudaError_t launch_combine(const float* ys, const float* y, const int* row_of, int T, int H, int k,
-                           __nv_bfloat16* out, int num_sms, cudaStream_t st);
-cudaError_t launch_unpermute(const float* dxs, const float* dxp, const int* row_of, const int* ids,
+cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __nv_bfloat16* y, const int* row_of,
+                           const float* pp, int T, int H, int k, __nv_bfloat16* out, int num_sms, cudaStream_t st);
+cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,
                              const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
                              const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, int num_sms,
                              cudaStream_t st);

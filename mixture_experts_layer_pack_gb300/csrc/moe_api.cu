@@ -93,7 +93,7 @@ struct Workspace {
     int* rank;  // rank of each route inside its expert
     int* hist;  // per 128-token chunk and expert: route count, then the chunk's rank offset
     __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
-    float *yx, *ys_dxs;  // forward: p*y (routed rows), y_shared; backward: dx (routed rows), dx_shared
+    __nv_bfloat16 *yx, *ys_dxs;  // forward: y (routed rows), y_shared; backward: dx (routed rows), dx_shared
     float* partial;
     // shared output gate: the shared rows' dprob partials, dz, chunk sums of the
     // gate weight's gradient, gate * a_shared (the gated down wgrad operand)
@@ -111,7 +111,7 @@ struct SavedBufs {
     float *pp, *pp_perm;
     float* gate;  // shared output gate per token
     __nv_bfloat16 *x_perm, *a, *a_s;
-    float *gu, *gu_s;
+    __nv_bfloat16 *gu, *gu_s;  // bf16 [g|u] of the routed rows and the shared expert
     uint8_t *x_q, *x_sf, *a_q, *a_sf;  // MXFP8 only
 };
 
@@ -126,9 +126,9 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->go_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     w->dgdu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
     w->ap = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
-    w->yx = c.take<float>(size_t(s.rows) * s.H);
+    w->yx = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     w->partial = c.take<float>(size_t(s.rows) * s.n_part);
-    w->ys_dxs = c.take<float>(size_t(s.Tmax) * s.H);
+    w->ys_dxs = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.H);
     w->dgdu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
     w->partial_s = c.take<float>(size_t(s.Tmax) * s.n_part_s);
     w->dz = c.take<float>(size_t(s.Tmax));
@@ -167,9 +167,9 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->gate = c.take<float>(size_t(s.Tmax));
     b->x_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     b->a = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
-    b->gu = c.take<float>(size_t(s.rows) * 2 * s.I);
+    b->gu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
     b->a_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
-    b->gu_s = c.take<float>(size_t(s.Tmax) * 2 * s.I);
+    b->gu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
     if (s.mx) {
         b->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
         b->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -591,8 +591,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.gate_up_split = I;
         a.out0 = b.a;
         a.ld_out0 = I;
-        a.outf = b.gu;
-        a.ld_outf = 2 * I;
+        a.outh = b.gu;
+        a.ld_outh = 2 * I;
         a.q_out = b.a_q;
         a.ld_q = I;
         a.q_sf = b.a_sf;
@@ -619,8 +619,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.gate_up_split = I;
         a.out0 = b.a;
         a.ld_out0 = I;
-        a.outf = b.gu;
-        a.ld_outf = 2 * I;
+        a.outh = b.gu;
+        a.ld_outh = 2 * I;
         Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -638,12 +638,12 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.gate_up_split = I;
         a.out0 = b.a_s;
         a.ld_out0 = I;
-        a.outf = b.gu_s;
-        a.ld_outf = 2 * I;
+        a.outh = b.gu_s;
+        a.ld_outh = 2 * I;
         Timed tm_(h, MOE_K_FWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // routed down projection, scaled by the route's prob
+    // routed down projection (y in bf16; the combine weights it by the route's prob)
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.a_q, rows, I, I) ||
@@ -655,9 +655,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.num_mtiles = rows / kBM;
         a.n_tiles = H / kMxBN;
         a.k_blocks = I / kMxBK;
-        a.row_scale = b.pp_perm;
-        a.outf = ws.yx;
-        a.ld_outf = H;
+        a.outh = ws.yx;
+        a.ld_outh = H;
         a.sfa = b.a_sf;
         a.sfa_kgroups = I / 128;
         a.sfb = ws.sf_down_row;
@@ -677,13 +676,12 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.num_mtiles = rows / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
-        a.row_scale = b.pp_perm;
-        a.outf = ws.yx;
-        a.ld_outf = H;
+        a.outh = ws.yx;
+        a.ld_outh = H;
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // shared output gate: gate[t] = sigmoid(hidden[t] . w), scales the shared down projection
+    // shared output gate: gate[t] = sigmoid(hidden[t] . w), weights the shared output in the combine
     if (gated) {
         Timed tm_(h, MOE_K_SHARED_GATE_FWD, st);
         MOE_CU(launch_gate_forward(static_cast<const __nv_bfloat16*>(hidden),
@@ -700,15 +698,15 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
         a.rows_valid = Ti;
-        a.outf = ws.ys_dxs;
-        a.ld_outf = H;
-        a.row_scale = gated ? b.gate : nullptr;
+        a.outh = ws.ys_dxs;
+        a.ld_outh = H;
         Timed tm_(h, MOE_K_FWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // combine
     Timed tm_(h, MOE_K_COMBINE, st);
-    MOE_CU(launch_combine(ws.ys_dxs, ws.yx, b.row_of, Ti, H, k, static_cast<__nv_bfloat16*>(out), h->sms, st));
+    MOE_CU(launch_combine(ws.ys_dxs, gated ? b.gate : nullptr, ws.yx, b.row_of, b.pp, Ti, H, k,
+                          static_cast<__nv_bfloat16*>(out), h->sms, st));
     return MOE_OK;
 }
 
@@ -752,8 +750,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.k_blocks = H / kMxBK;
         a.in0 = b.a;
         a.ld_in0 = I;
-        a.inf = b.gu;
-        a.ld_inf = 2 * I;
+        a.inh = b.gu;
+        a.ld_inh = 2 * I;
         a.row_scale = b.pp_perm;
         a.partial = ws.partial;
         a.out0 = ws.dgdu;
@@ -785,8 +783,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.k_blocks = H / kBK;
         a.in0 = b.a;
         a.ld_in0 = I;
-        a.inf = b.gu;
-        a.ld_inf = 2 * I;
+        a.inh = b.gu;
+        a.ld_inh = 2 * I;
         a.row_scale = b.pp_perm;
         a.partial = ws.partial;
         a.out0 = ws.dgdu;
@@ -809,8 +807,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.rows_valid = Ti;
         a.in0 = b.a_s;
         a.ld_in0 = I;
-        a.inf = b.gu_s;
-        a.ld_inf = 2 * I;
+        a.inh = b.gu_s;
+        a.ld_inh = 2 * I;
         a.out0 = ws.dgdu_s;
         a.ld_out0 = 2 * I;
         if (gated) {  // the gate acts as the shared rows' prob: dgate partials, gate * a_shared
@@ -840,8 +838,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = H / kMxBN;
         a.k_blocks = 2 * I / kMxBK;
         a.gate_up_split = I;
-        a.outf = ws.yx;
-        a.ld_outf = H;
+        a.outh = ws.yx;
+        a.ld_outh = H;
         a.sfa = ws.dgdu_sf;
         a.sfa_kgroups = 2 * I / 128;
         a.sfb = ws.sf_fc1_col;
@@ -862,8 +860,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = H / bn;
         a.k_blocks = 2 * I / kBK;
         a.gate_up_split = I;
-        a.outf = ws.yx;
-        a.ld_outf = H;
+        a.outh = ws.yx;
+        a.ld_outh = H;
         Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -879,8 +877,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.k_blocks = 2 * I / kBK;
         a.rows_valid = Ti;
         a.gate_up_split = I;
-        a.outf = ws.ys_dxs;
-        a.ld_outf = H;
+        a.outh = ws.ys_dxs;
+        a.ld_outh = H;
         Timed tm_(h, MOE_K_BWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }

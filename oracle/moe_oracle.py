@@ -47,10 +47,13 @@ Precision. The pages fix it for the expert GEMMs: BF16 routed and shared
 experts (PR #6572, Supported configurations) with an FP32 GEMM accumulator
 and FP32 main_grad accumulation (PR #8210, review thread on wgrad
 precision). ``precision="exact"`` is the plain definition in fp64.
-``precision="bf16"`` holds each expert GEMM's operands in bf16 -- the
-activation a between the two projections, the SwiGLU gradients dg and du,
-and the prob-weighted activation p*a that multiplies grad_out in the down
-projection's weight gradient -- and accumulates in fp64. Inputs (hidden,
+``precision="bf16"`` holds every tensor a BF16 expert passes on in bf16: the
+gate/up projections g and u (kept for backward), the activation a between the
+two projections, the expert's output y (the prob, or the shared expert's
+gate, weights it in the fp32 combine), the SwiGLU gradients dg and du, the
+prob-weighted activation p*a that multiplies grad_out in the down
+projection's weight gradient, and the expert's input gradient dx (summed in
+fp32 by the un-permute); products accumulate in fp64. Inputs (hidden,
 grad_out, weights) are bf16 already. ``precision="mxfp8"`` (MXFP8 routed
 experts, same pages) quantises the routed experts' forward and dgrad GEMM
 operands to MXFP8 in blocks of 32 along each GEMM's K -- x and a in forward,
@@ -210,11 +213,15 @@ def mxfp8_round(v):
 class Operands:
     """Where one expert's GEMM operands are rounded: identity (exact), bf16, or,
     for routed experts in mxfp8 mode, MXFP8 along K for the forward and dgrad
-    GEMMs (bf16 for the weight-gradient GEMMs)."""
+    GEMMs (bf16 for the weight-gradient GEMMs); and the bf16 tensors between
+    the expert's GEMMs and the layer's sums (``inter``: g, u, y, dx)."""
 
     def __init__(self, precision, routed=True):
         self.rnd = _rounder(precision)
         self.mx = precision == "mxfp8" and routed
+
+    def inter(self, v):                   # g, u, y, dx: GEMM results stored in bf16
+        return self.rnd(v)
 
     def x(self, x):                       # gate/up projection input, K = H
         return mxfp8_round(x) if self.mx else x
@@ -267,11 +274,11 @@ def expert_forward(x, Wg, Wu, Wd, ops=None, limit=0.0):
     swiglu_limit clamp of g and u). Returns the unclamped g, u."""
     ops = ops or Operands("exact")
     xq = ops.x(x)
-    g = xq @ Wg.T
-    u = xq @ Wu.T
+    g = ops.inter(xq @ Wg.T)
+    u = ops.inter(xq @ Wu.T)
     gc, uc, _, _ = clamp_inputs(g, u, limit)
     a = ops.a(silu(gc) * uc)
-    y = a @ Wd.T
+    y = ops.inter(a @ Wd.T)
     return g, u, a, y
 
 
@@ -288,7 +295,7 @@ def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, ops=None, limit=0.0):
     dg = da * uc * silu_grad(gc) * mg
     du = da * silu(gc) * mu
     dgq, duq = ops.dgdu(dg, du)
-    dx = dgq @ Wg + duq @ Wu
+    dx = ops.inter(dgq @ Wg + duq @ Wu)
     dgw, duw = ops.wgrad(dg), ops.wgrad(du)
     dprob = np.sum(a * da_u, axis=1)
     return dx, dgw.T @ x, duw.T @ x, go.T @ ops.wgrad(p[:, None] * a), dprob
@@ -461,11 +468,18 @@ def mxfp8_alternative(v, band):
 
 def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_band=None):
     """Envelopes of one expert's results for rows x[n,H] with probs p[n]. Wf are
-    the forward weights (Wg, Wu, Wd), Wb the dgrad weights; ``limit`` the
-    swiglu_limit clamp; ``p_band`` a bound on the kernel's error in p (the
-    shared output gate, which the kernel evaluates in fp32; None: p is exact).
-    Returns env_y [n,H], env_dx [n,H], env_dWg [I,H], env_dWu [I,H],
-    env_dWd [H,I], env_dprob [n]."""
+    the forward weights (Wg, Wu, Wd), Wb the dgrad weights; g, u the mode's
+    (bf16) gate/up values; ``limit`` the swiglu_limit clamp; ``p_band`` a bound
+    on the kernel's error in p (the shared output gate, which the kernel
+    evaluates in fp32; None: p is exact).
+
+    Every bf16 (or MXFP8) tensor is a rounding of a value the kernel evaluates
+    in fp32. Where that value lies within its evaluation band of a rounding
+    midpoint, the other neighbour is also a correct result; the difference it
+    makes is carried forward with absolute values (a change below a later
+    rounding's distance to its midpoint is absorbed by it, a larger one may
+    flip it in turn). Returns env_y [n,H] (the expert's output y), env_dx
+    [n,H], env_dWg [I,H], env_dWu [I,H], env_dWd [H,I], env_dprob [n]."""
     ops = Operands(precision, routed)
     Wg, Wu, Wd = Wf
     Bg, Bu, Bd = Wb
@@ -473,16 +487,23 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_ban
     H = x.shape[1]
     I = g.shape[1]
     p_band = np.zeros_like(p) if p_band is None else p_band
-    dg_band = fp32_dot_band((xq * xq) @ (Wg * Wg).T, H)          # |g_fp32 - g|
-    du_band = fp32_dot_band((xq * xq) @ (Wu * Wu).T, H)
+    # g, u: fp32 GEMM results rounded to bf16
+    g_raw, u_raw = xq @ Wg.T, xq @ Wu.T
+    alt_g = bf16_alternative(g_raw, fp32_dot_band((xq * xq) @ (Wg * Wg).T, H))
+    alt_u = bf16_alternative(u_raw, fp32_dot_band((xq * xq) @ (Wu * Wu).T, H))
     gc, uc, mg, mu = clamp_inputs(g, u, limit)
     s1 = silu_grad(gc)
     a_val = silu(gc) * uc
-    # a is continuous across the clamp bounds: the unmasked slopes bound it on both sides
-    band_a = np.abs(s1 * uc) * dg_band + np.abs(silu(gc)) * du_band + ELEMENTWISE_BAND * np.abs(a_val)
-    alt_a = mxfp8_alternative(a_val, band_a) if ops.mx else bf16_alternative(a_val, band_a)
-    env_y = alt_a @ np.abs(Wd).T
+    # a: elementwise fp32 math on g, u, then rounded (MXFP8 for routed experts in mxfp8 mode);
+    # a flipped g or u moves it by the slopes (a is continuous across the clamp bounds)
+    flip_a = np.abs(s1 * uc) * alt_g + np.abs(silu(gc)) * alt_u
+    band_a = ELEMENTWISE_BAND * np.abs(a_val) + flip_a
+    alt_a = (mxfp8_alternative(a_val, band_a) if ops.mx else bf16_alternative(a_val, band_a)) + flip_a
     a_b = ops.a(a_val)
+    # y = bf16(a_b Wd^T)
+    ey_pre = alt_a @ np.abs(Wd).T
+    band_y = fp32_dot_band((a_b * a_b) @ (Wd * Wd).T, I) + ey_pre
+    env_y = ey_pre + bf16_alternative(a_b @ Wd.T, band_y)
 
     goq = ops.go(go)
     da_u = goq @ Bd
@@ -492,25 +513,35 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_ban
            p_band[:, None] * np.abs(da_u))
     dg_val = da * uc * s1 * mg
     du_val = da * silu(gc) * mu
-    band_dg = (np.abs(uc * s1) * dda + np.abs(da * s1) * du_band +
-               np.abs(da * uc) * silu_grad2_bound() * dg_band + ELEMENTWISE_BAND * np.abs(dg_val)) * mg
-    band_du = (np.abs(silu(gc)) * dda + np.abs(da * s1) * dg_band + ELEMENTWISE_BAND * np.abs(du_val)) * mu
-    # the clamp's masks jump at its bounds: within the fp32 band of a bound the
-    # kernel may take either side, so the whole unmasked value is an alternative
+    # changes of dg, du from a flipped g or u (not absorbed: comparable to their ulp)
+    flip_dg = (np.abs(da * s1) * alt_u + np.abs(da * uc) * silu_grad2_bound() * alt_g) * mg
+    flip_du = np.abs(da * s1) * alt_g * mu
+    band_dg = (np.abs(uc * s1) * dda + ELEMENTWISE_BAND * np.abs(dg_val)) * mg + flip_dg
+    band_du = (np.abs(silu(gc)) * dda + ELEMENTWISE_BAND * np.abs(du_val)) * mu + flip_du
+    # the clamp's masks jump at its bounds: where g or |u| lies within one bf16
+    # ulp of L, its rounding (either neighbour) may fall on either side of L,
+    # and the whole unmasked value is an alternative -- between the kernel and
+    # this mode, and between this mode and the unrounded definition
     jump_dg = jump_du = 0.0
     if limit:
-        jump_dg = np.where(np.abs(g - limit) <= dg_band, np.abs(da * uc * s1), 0.0)
-        jump_du = np.where(np.abs(np.abs(u) - limit) <= du_band, np.abs(da * silu(gc)), 0.0)
-    alt_dg = bf16_alternative(dg_val, band_dg) + jump_dg   # weight-gradient operands (bf16)
-    alt_du = bf16_alternative(du_val, band_du) + jump_du
+        ulp = lambda v: np.ldexp(1.0, np.frexp(v)[1] - 8)  # noqa: E731
+        near_g = np.abs(g_raw - limit) <= ulp(g_raw)
+        near_u = np.abs(np.abs(u_raw) - limit) <= ulp(u_raw)
+        jump_dg = np.where(near_g, np.abs(da * uc * s1), 0.0)
+        jump_du = np.where(near_u, np.abs(da * silu(gc)), 0.0)
+    alt_dg = bf16_alternative(dg_val, band_dg) + flip_dg + jump_dg   # weight-gradient operands (bf16)
+    alt_du = bf16_alternative(du_val, band_du) + flip_du + jump_du
     if ops.mx:                                            # dgrad operand [dg|du] (MXFP8)
+        flips = np.concatenate([flip_dg + jump_dg, flip_du + jump_du], axis=1)
         alt_q = mxfp8_alternative(np.concatenate([dg_val, du_val], axis=1),
-                                  np.concatenate([band_dg + jump_dg, band_du + jump_du], axis=1))
-        alt_q = alt_q + np.concatenate([np.broadcast_to(jump_dg, dg_val.shape),
-                                        np.broadcast_to(jump_du, du_val.shape)], axis=1)
-        env_dx = alt_q[:, :I] @ np.abs(Bg) + alt_q[:, I:] @ np.abs(Bu)
+                                  np.concatenate([band_dg + jump_dg, band_du + jump_du], axis=1)) + flips
+        edx_pre = alt_q[:, :I] @ np.abs(Bg) + alt_q[:, I:] @ np.abs(Bu)
     else:
-        env_dx = alt_dg @ np.abs(Bg) + alt_du @ np.abs(Bu)
+        edx_pre = alt_dg @ np.abs(Bg) + alt_du @ np.abs(Bu)
+    # dx = bf16(dg Bg + du Bu)
+    dgq, duq = ops.dgdu(dg_val, du_val)
+    band_dx = fp32_dot_band((dgq * dgq) @ (Bg * Bg) + (duq * duq) @ (Bu * Bu), 2 * I) + edx_pre
+    env_dx = edx_pre + bf16_alternative(dgq @ Bg + duq @ Bu, band_dx)
     env_dWg = alt_dg.T @ np.abs(x)
     env_dWu = alt_du.T @ np.abs(x)
 

@@ -2,11 +2,12 @@
 
 * ``bf16_round`` against PyTorch's fp32 -> bfloat16 cast (round to nearest even),
   ties included;
-* forward in bf16 mode equals a per-element textbook SwiGLU that rounds the
-  activation a (the down projection's operand) to bf16;
-* rigorous first-order bounds: every bf16-mode result differs from the exact
-  one by no more than the rounding of its operands allows (unit roundoff
-  2^-8 per rounded operand, propagated with absolute values).
+* forward and backward in bf16 mode equal a per-element textbook SwiGLU that
+  rounds, with torch's fp32 -> bf16 cast, every tensor the expert passes on:
+  g, u, a, y in forward; dg, du, p*a and dx in backward;
+* an independent fp32 evaluation stays within the oracle's result plus its
+  rounding envelope (bf16, with the swiglu_limit clamp and the shared output
+  gate, and MXFP8).
 """
 import numpy as np
 import pytest
@@ -36,100 +37,85 @@ def test_bf16_round_idempotent_on_bf16_values():
     assert np.array_equal(O.bf16_round(v), v)
 
 
-def _textbook_swiglu_bf16(x, Wg, Wu, Wd):
+def _b(v):
+    """torch's fp32 -> bf16 cast (round to nearest even) of an fp64 value."""
+    return float(torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).double())
+
+
+def _textbook_expert_bf16(x, go, p, Wg, Wu, Wd):
+    """One token through one BF16 expert, element by element: returns y (the
+    expert output before its prob) and, for grad_out go and prob p, dx, dprob,
+    dWg, dWu, dWd."""
     I, H = Wg.shape
-    a = []
-    for i in range(I):
-        g = sum(Wg[i, h] * x[h] for h in range(H))
-        u = sum(Wu[i, h] * x[h] for h in range(H))
-        a.append(float(torch.tensor(_silu(g) * u, dtype=torch.float32).to(torch.bfloat16).double())
-                 if abs(_silu(g) * u) < 1e30 else _silu(g) * u)
-    return np.array([sum(Wd[h, i] * a[i] for i in range(I)) for h in range(Wd.shape[0])])
+    g = [_b(sum(Wg[i, h] * x[h] for h in range(H))) for i in range(I)]
+    u = [_b(sum(Wu[i, h] * x[h] for h in range(H))) for i in range(I)]
+    a = [_b(_silu(g[i]) * u[i]) for i in range(I)]
+    y = np.array([_b(sum(Wd[h, i] * a[i] for i in range(I))) for h in range(H)])
+    da_u = [sum(go[h] * Wd[h, i] for h in range(H)) for i in range(I)]
+    sig = [1.0 / (1.0 + np.exp(-g[i])) for i in range(I)]
+    dg = [_b(p * da_u[i] * u[i] * sig[i] * (1.0 + g[i] * (1.0 - sig[i]))) for i in range(I)]
+    du = [_b(p * da_u[i] * _silu(g[i])) for i in range(I)]
+    dx = np.array([_b(sum(dg[i] * Wg[i, h] + du[i] * Wu[i, h] for i in range(I))) for h in range(H)])
+    dprob = sum(a[i] * da_u[i] for i in range(I))
+    dWg = np.array([[dg[i] * x[h] for h in range(H)] for i in range(I)])
+    dWu = np.array([[du[i] * x[h] for h in range(H)] for i in range(I)])
+    dWd = np.array([[go[h] * _b(p * a[i]) for i in range(I)] for h in range(H)])
+    return y, dx, dprob, dWg, dWu, dWd
 
 
-def test_bf16_forward_rounds_the_activation_only():
-    rng = np.random.default_rng(3)
+def _one_route_case(seed):
+    rng = np.random.default_rng(seed)
     T, H, I, E, k = 4, 6, 5, 3, 2
     W = _rand_layer(rng, H, I, E)
     x = rng.standard_normal((T, H))
+    go = rng.standard_normal((T, H))
     m = np.zeros((T, E), bool)
     route = [1, 0, 2, 1]
     for t, e in enumerate(route):
         m[t, e] = True
-    probs = rng.random((T, E))
+    return W, x, go, m, rng.random((T, E)), k, route
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_bf16_forward_rounds_every_expert_tensor(seed):
+    W, x, go, m, probs, k, route = _one_route_case(seed)
     out, _ = O.forward(x, probs, m, W, k, precision="bf16")
     for t, e in enumerate(route):
-        ref = probs[t, e] * _textbook_swiglu_bf16(x[t], *W.routed(e)) + _textbook_swiglu_bf16(x[t], *W.shared())
-        np.testing.assert_allclose(out[t], ref, rtol=1e-12, atol=1e-13)
+        y_r = _textbook_expert_bf16(x[t], go[t], probs[t, e], *W.routed(e))[0]
+        y_s = _textbook_expert_bf16(x[t], go[t], 1.0, *W.shared())[0]
+        np.testing.assert_allclose(out[t], probs[t, e] * y_r + y_s, rtol=1e-12, atol=1e-13)
 
 
-def _case(seed, T=12, H=8, I=6, E=4, k=2):
-    rng = np.random.default_rng(seed)
-    W = _rand_layer(rng, H, I, E, scale=0.5)
-    x = rng.standard_normal((T, H))
-    go = rng.standard_normal((T, H))
-    m = np.zeros((T, E), bool)
-    for t in range(T):
-        m[t, rng.choice(E, size=int(rng.integers(1, k + 1)), replace=False)] = True
-    return W, x, go, m, rng.random((T, E)), k
-
-
-@pytest.mark.parametrize("seed", [0, 1, 2])
-def test_bf16_mode_within_rounding_bounds(seed):
-    W, x, go, m, probs, k = _case(seed)
-    out_e, ce = O.forward(x, probs, m, W, k, precision="exact")
-    out_b, cb = O.forward(x, probs, m, W, k, precision="bf16")
-    dx_e, dp_e, g_e = O.backward(go, ce, W)
-    dx_b, dp_b, g_b = O.backward(go, cb, W)
-    assert not np.array_equal(out_e, out_b)          # the mode does round something
-
-    # forward: |delta y| <= sum_i U |a_i| |Wd_hi| per expert, combined with |p|
-    gs, us, as_ = ce["shared"]
-    Wsg, Wsu, Wsd = W.shared()
-    bound = (U * np.abs(as_)) @ np.abs(Wsd).T
-    ids, pp, row_of = ce["ids"], ce["pp"], ce["row_of"]
-    routed_a = np.zeros((ce["perm_src"].size, as_.shape[1]))
-    for e, (g, u, a) in ce["routed"].items():
-        lo, hi = ce["offsets"][e], ce["offsets"][e + 1]
-        routed_a[lo:hi] = a
-    for s in range(k):
-        v = ids[:, s] >= 0
-        for t in np.flatnonzero(v):
-            e = ids[t, s]
-            bound[t] += abs(pp[t, s]) * (U * np.abs(routed_a[row_of[t, s]])) @ np.abs(W.routed(e)[2]).T
-    assert np.all(np.abs(out_b - out_e) <= bound * (1 + 1e-9) + 1e-15)
-
-    # dprobs = <go, y>: |delta| <= sum_h |go_h| |delta y_h|
-    for t, s in zip(*np.nonzero(ids >= 0)):
-        e = ids[t, s]
-        dy = (U * np.abs(routed_a[row_of[t, s]])) @ np.abs(W.routed(e)[2]).T
-        assert abs(dp_b[t, e] - dp_e[t, e]) <= np.abs(go[t]) @ dy * (1 + 1e-9) + 1e-15
-
-    # shared backward: dg, du rounded once; p*a = a (p = 1) already bf16
-    da = go @ Wsd
-    dg = da * us * O.silu_grad(gs)
-    du = da * O.silu(gs)
-    ddg, ddu = U * np.abs(dg), U * np.abs(du)
-    assert np.all(np.abs(g_b["shared_gate"] - g_e["shared_gate"]) <= ddg.T @ np.abs(x) * (1 + 1e-9) + 1e-15)
-    assert np.all(np.abs(g_b["shared_up"] - g_e["shared_up"]) <= ddu.T @ np.abs(x) * (1 + 1e-9) + 1e-15)
-    assert np.all(np.abs(g_b["shared_down"] - g_e["shared_down"]) <=
-                  np.abs(go).T @ (U * np.abs(as_)) * (1 + 1e-9) + 1e-15)
-    # routed down wgrad: p*a rounded after a was: |delta| <= U (|p a_b| + |p a|) per element
-    for e, (dWg, dWu, dWd) in g_e["routed"].items():
-        lo, hi = ce["offsets"][e], ce["offsets"][e + 1]
-        src, slot = ce["perm_src"][lo:hi], ce["perm_slot"][lo:hi]
-        p = pp[src, slot]
-        a_e = ce["routed"][e][2]
-        a_b = cb["routed"][e][2]
-        bd = np.abs(go[src]).T @ (U * (np.abs(p[:, None] * a_b) + np.abs(p[:, None] * a_e)))
-        assert np.all(np.abs(g_b["routed"][e][2] - dWd) <= bd * (1 + 1e-9) + 1e-15)
+@pytest.mark.parametrize("seed", [3, 4])
+def test_bf16_backward_matches_textbook(seed):
+    W, x, go, m, probs, k, route = _one_route_case(seed)
+    _, cache = O.forward(x, probs, m, W, k, precision="bf16")
+    dx, dprobs, grads = O.backward(go, cache, W)
+    sums = {n: 0.0 for n in ("sg", "su", "sd")}
+    routed = {}
+    for t, e in enumerate(route):
+        _, dxr, dpr, g1, g2, g3 = _textbook_expert_bf16(x[t], go[t], probs[t, e], *W.routed(e))
+        _, dxs, _, s1, s2, s3 = _textbook_expert_bf16(x[t], go[t], 1.0, *W.shared())
+        np.testing.assert_allclose(dx[t], dxr + dxs, rtol=1e-12, atol=1e-13)
+        assert dprobs[t, e] == pytest.approx(dpr, rel=1e-12, abs=1e-13)
+        sums["sg"] = sums["sg"] + s1
+        sums["su"] = sums["su"] + s2
+        sums["sd"] = sums["sd"] + s3
+        acc = routed.setdefault(e, [0.0, 0.0, 0.0])
+        acc[0], acc[1], acc[2] = acc[0] + g1, acc[1] + g2, acc[2] + g3
+    for n, key in (("sg", "shared_gate"), ("su", "shared_up"), ("sd", "shared_down")):
+        np.testing.assert_allclose(grads[key], sums[n], rtol=1e-12, atol=1e-13)
+    for e, (g1, g2, g3) in routed.items():
+        for j, ref in enumerate((g1, g2, g3)):
+            np.testing.assert_allclose(grads["routed"][e][j], ref, rtol=1e-12, atol=1e-13)
 
 
 def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
     """An independent fp32 evaluation of the layer (numpy float32 matmuls and
-    elementwise math, bf16 rounding of the GEMM operands -- MXFP8 for the routed
-    forward/dgrad operands when mx -- fp64 afterwards): stands in for any kernel
-    that evaluates the operands in fp32. ``limit`` clamps the SwiGLU inputs;
+    elementwise math, bf16 rounding of every tensor an expert passes on -- g, u,
+    a, y, dg, du, p*a, dx; MXFP8 for the routed forward/dgrad operands when mx --
+    and fp64 sums in the combine, un-permute and weight gradients): stands in for
+    any kernel that evaluates these tensors in fp32. ``limit`` clamps the SwiGLU inputs;
     W.shared_output_gate (if set) gates the shared expert with an fp32 sigmoid."""
     from oracle import mxfp8 as MXC
     f32 = np.float32
@@ -142,12 +128,15 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
     def sig(z):
         return f32(1) / (f32(1) + np.exp(-z))
 
+    def r32(v):                      # bf16 rounding of an fp32 array, kept in fp32
+        return rnd(v.astype(np.float64)).astype(f32)
+
     def expert(xr, gor, p, Wg, Wu, Wd, quant):
         xq = mxr(xr) if quant else xr
         goq = mxr(gor) if quant else gor
         xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xq, Wg, Wu, Wd, goq))
-        g = xr32 @ Wg32.T
-        u = xr32 @ Wu32.T
+        g = r32(xr32 @ Wg32.T)      # g, u stored in bf16
+        u = r32(xr32 @ Wu32.T)
         mg = mu = f32(1)
         if limit:
             L = f32(limit)
@@ -157,7 +146,7 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
             u = np.clip(u, -L, L)
         s = sig(g)
         a = (mxr if quant else rnd)((g * s * u).astype(np.float64))
-        y = p[:, None] * (a @ Wd.T)
+        y = p[:, None] * r32(a.astype(f32) @ Wd32.T).astype(np.float64)   # y stored in bf16, weighted after
         da_u = go32 @ Wd32
         dprob = np.sum(a.astype(f32) * da_u, axis=1).astype(np.float64)
         da = p.astype(f32)[:, None] * da_u
@@ -165,10 +154,10 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
         du32 = da * (g * s) * mu
         dg, du = rnd(dg32.astype(np.float64)), rnd(du32.astype(np.float64))
         if quant:
-            qq = mxr(np.concatenate([dg32, du32], axis=1).astype(np.float64))
-            dx = qq[:, :dg.shape[1]] @ Wg + qq[:, dg.shape[1]:] @ Wu
+            qq = mxr(np.concatenate([dg32, du32], axis=1).astype(np.float64)).astype(f32)
+            dx = r32(qq[:, :dg.shape[1]] @ Wg32 + qq[:, dg.shape[1]:] @ Wu32).astype(np.float64)
         else:
-            dx = dg @ Wg + du @ Wu
+            dx = r32(dg.astype(f32) @ Wg32 + du.astype(f32) @ Wu32).astype(np.float64)   # dx stored in bf16
         pa = rnd((p.astype(f32)[:, None] * a.astype(f32)).astype(np.float64))
         return y, dx, dg.T @ xr, du.T @ xr, gor.T @ pa, dprob
 
@@ -227,11 +216,13 @@ def test_envelope_covers_fp32_evaluation(seed):
         for j, n in enumerate(("gate", "up", "down")):
             flipped += check(gs[j], g_b["routed"][e][j], env["routed"][e][j], f"routed {n}[{e}]")
     assert flipped > 0, "the fp32 evaluation flipped no rounding: the test would prove nothing"
-    # the envelope mostly stays far below the tolerance floor (1e-3 max|ref|) it is added to
+    # the envelope stays below the tolerance it is added to (2e-2 |ref| + 1e-3 max|ref|)
+    # for all but a few elements (an ulp flip of a bf16 y or dx term inside a sum
+    # that cancels), and below 1e-2 max|ref| everywhere
     for n, ref in (("out", out_b), ("dhidden", dh_b), ("shared_gate", g_b["shared_gate"])):
         sc = np.abs(ref).max()
-        assert np.median(env[n]) < 2.5e-4 * sc and np.percentile(env[n], 99) < 1e-3 * sc, n
-        assert env[n].max() < 5e-3 * sc, n
+        assert np.mean(env[n] > 2e-2 * np.abs(ref) + 1e-3 * sc) < 0.03, n
+        assert np.median(env[n]) < 1e-3 * sc and env[n].max() < 1e-2 * sc, n
 
 
 @pytest.mark.parametrize("seed", [21, 22])
