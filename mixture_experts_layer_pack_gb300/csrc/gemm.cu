@@ -40,6 +40,7 @@ constexpr uint32_t kSwizzleAtom = 1024;   // 8 rows x 128 bytes
 constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
 
 constexpr uint32_t kStageTileBytes = 32 * 32 * 4;  // fp32 staging box of one epilogue warp (32 rows x 32 cols)
+constexpr int kRing = 4;  // weight gradient: depth of the claimed-tile ring
 
 template <int OP, int BN>
 struct Cfg {
@@ -384,18 +385,27 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 // fl32(main_grad + dW), or bf16(main_grad + bf16(dW)) for bf16 main_grad,
 // whatever the schedule.
 template <int BN>
-__device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_tiles, uint32_t tmem_base, int q,
-                                               int half, float* bufs, uint64_t* mg_bar, uint64_t* tfull,
-                                               uint64_t* tempty, volatile int* abort_flag, const CUtensorMap* mC0,
-                                               const CUtensorMap* mC1) {
+__device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tmem_base, int q, int half,
+                                               float* bufs, uint64_t* mg_bar, uint64_t* tfull, uint64_t* tempty,
+                                               const uint64_t* ring_full, uint64_t* ring_empty,
+                                               const int* ring_tile, volatile int* abort_flag,
+                                               const CUtensorMap* mC0, const CUtensorMap* mC1) {
     const int lane = threadIdx.x & 31;
     const bool bf = args.mg_bf16 != 0;
     const int bw = bf ? 64 : 32;                           // box width in elements
     const int nb = (BN / bw - half + kEpiHalves - 1) / kEpiHalves;  // boxes of this warp per tile
-    auto next_valid = [&](int tile) {
-        for (; tile < total_tiles; tile += gridDim.x)
-            if (decode_tile<OP_WGRAD>(tile, args).kblocks > 0) return tile;
-        return total_tiles;
+    // tile at ring position pos (-1: no more tiles, -2: the wait gave up); the
+    // position is released to the producer as soon as it has been read
+    auto ring_take = [&](int pos) -> int {
+        int v = -2;
+        if (lane == 0) {
+            const int slot = pos % kRing;
+            if (mbar_wait(const_cast<uint64_t*>(&ring_full[slot]), (pos / kRing) & 1, abort_flag, args.status)) {
+                v = ring_tile[slot];
+                mbar_arrive(&ring_empty[slot]);
+            }
+        }
+        return __shfl_sync(0xffffffffu, v, 0);
     };
     // box (tile t, c-th box of this warp): destination map and coordinates (an
     // expert's own descriptor at z = 0 when main_grad comes as a per-expert table)
@@ -416,16 +426,17 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
         tma_load_3d(bufs + b * (kStageTileBytes / 4), mc, &mg_bar[b], x, y, z);
     };
 
-    int cur = next_valid(blockIdx.x);
-    Tile t = decode_tile<OP_WGRAD>(cur < total_tiles ? cur : 0, args);
+    int rpos = 0;
+    int cur = ring_take(rpos++);
+    Tile t = decode_tile<OP_WGRAD>(cur >= 0 ? cur : 0, args);
     uint32_t pending = 0, parity = 0;  // per buffer: a load in flight / parity of its next completion
-    if (nb > 0 && cur < total_tiles && lane == 0) {
+    if (nb > 0 && cur >= 0 && lane == 0) {
         load_box(t, 0, 0);
         pending = 1;
     }
     int jb = 0, it = 0;
     bool ok = true;
-    while (ok && cur < total_tiles) {
+    while (ok && cur >= 0) {
         const int acc = it & 1;
         const uint32_t use = uint32_t(it >> 1);
         ++it;
@@ -435,15 +446,17 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, int total_t
         __syncwarp();
         tc_fence_after();
         const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
-        const int nxt = next_valid(cur + gridDim.x);
-        const Tile tn = decode_tile<OP_WGRAD>(nxt < total_tiles ? nxt : 0, args);
+        // the producer publishes the next tile once this one's loads are issued
+        const int nxt = ring_take(rpos++);
+        if (nxt == -2) break;
+        const Tile tn = decode_tile<OP_WGRAD>(nxt >= 0 ? nxt : 0, args);
 #pragma unroll 1
         for (int c = 0; c < nb; ++c) {
             const int b = jb & 1;
             if (lane == 0) {
                 // prefetch the box after this one into the other buffer, once the
                 // store that last used it has read it out
-                const bool more = c + 1 < nb || nxt < total_tiles;
+                const bool more = c + 1 < nb || nxt >= 0;
                 if (more) {
                     bulk_wait_read<0>();
                     load_box(c + 1 < nb ? t : tn, c + 1 < nb ? c + 1 : 0, b ^ 1);
@@ -542,7 +555,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint64_t* mg_bar = drain + 1;  // weight gradient: two box buffers per epilogue warp
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mg_bar + 2 * kEpiWarps);
+    // weight gradient: ring of claimed tiles (dynamic scheduling), producer -> MMA and epilogue warps
+    uint64_t* ring_full = mg_bar + 2 * kEpiWarps;
+    uint64_t* ring_empty = ring_full + kRing;
+    int* ring_tile = reinterpret_cast<int*>(ring_empty + kRing);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_tile + kRing);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -558,8 +575,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(drain, 1);
-        if (OP == OP_WGRAD)
+        if (OP == OP_WGRAD) {
             for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&mg_bar[b], 1);
+            for (int r = 0; r < kRing; ++r) {
+                mbar_init(&ring_full[r], 1);
+                mbar_init(&ring_empty[r], 1 + kEpiWarps);  // the MMA thread and every epilogue warp
+            }
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tmA);
@@ -591,7 +613,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per stage: ever filled / parity of its last fill
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            int claimed = 0;  // weight gradient: tiles published into the ring so far
+            for (int next = blockIdx.x; ok; next += gridDim.x) {
+                int tile = next;
+                if (OP == OP_WGRAD) {
+                    // claim the next tile with work from the launch's counter and publish
+                    // it (-1 once the counter has passed the last tile)
+                    const int slot = claimed % kRing;
+                    if (!mbar_wait(&ring_empty[slot], ((claimed / kRing) & 1) ^ 1, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    do {
+                        tile = atomicAdd(args.tile_counter, 1);
+                    } while (tile < total_tiles && decode_tile<OP>(tile, args).kblocks == 0);
+                    ring_tile[slot] = tile < total_tiles ? tile : -1;
+                    mbar_arrive(&ring_full[slot]);
+                    ++claimed;
+                }
+                if (tile >= total_tiles) break;
                 const Tile t = decode_tile<OP>(tile, args);
                 for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) {
@@ -622,8 +662,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
+            int rpos = 0;  // weight gradient: ring positions read so far
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (int next = blockIdx.x; ok; next += gridDim.x) {
+                int tile = next;
+                if (OP == OP_WGRAD) {  // the next claimed tile, in the producer's order
+                    const int slot = rpos % kRing;
+                    if (!mbar_wait(&ring_full[slot], (rpos / kRing) & 1, abort_flag, args.status)) break;
+                    tile = ring_tile[slot];
+                    mbar_arrive(&ring_empty[slot]);
+                    ++rpos;
+                    if (tile < 0) break;
+                }
+                if (tile >= total_tiles) break;
                 const Tile t = decode_tile<OP>(tile, args);
                 if (t.kblocks == 0) continue;
                 const int buf = it & 1;
@@ -667,8 +718,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int half = (warp - 2) >> 2;
         float* my_staging = staging + (warp - 2) * C::BUFS * (kStageTileBytes / 4);
         if constexpr (OP == OP_WGRAD) {
-            wgrad_epilogue<BN>(args, total_tiles, tmem_base, q, half, my_staging, mg_bar + 2 * (warp - 2), tfull,
-                               tempty, abort_flag, &tmC0, &tmC1);
+            wgrad_epilogue<BN>(args, tmem_base, q, half, my_staging, mg_bar + 2 * (warp - 2), tfull, tempty,
+                               ring_full, ring_empty, ring_tile, abort_flag, &tmC0, &tmC1);
         } else {
             int it = 0;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -772,8 +823,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* mg_bar = drain + 1;  // weight gradient: two box buffers per epilogue warp
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mg_bar + 2 * kEpiWarps);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -789,8 +839,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(drain, 1);
-        if (OP == OP_WGRAD)
-            for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&mg_bar[b], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tmA);

@@ -58,6 +58,7 @@ struct GemmArgs {
     int inter;
     float swiglu_limit;         // > 0: SwiGLU inputs clamped, g <= L, |u| <= L (FWD_GU, BWD_DOWN epilogues)
     int mg_bf16;                // WGRAD: main_grad is bf16 (bf16(mg + bf16(dW))), else fp32 (mg + dW)
+    int* tile_counter;          // WGRAD: zeroed before the launch; CTAs claim tiles from it in order
     // per-expert descriptor tables in device memory (null: the 3D maps, expert = z);
     // entry e is expert e's own map (z = 0)
     const CUtensorMap* b0_tab;

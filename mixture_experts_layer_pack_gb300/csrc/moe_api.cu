@@ -92,6 +92,7 @@ struct Workspace {
     int* status;
     int* rank;  // rank of each route inside its expert
     int* hist;  // per 128-token chunk and expert: route count, then the chunk's rank offset
+    int* tile_counters;  // one per weight-gradient launch of a backward (dynamic tile scheduling)
     __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
     __nv_bfloat16 *yx, *ys_dxs;  // forward: y (routed rows), y_shared; backward: dx (routed rows), dx_shared
     float* partial;
@@ -123,6 +124,7 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->status = c.take<int>(64);
     w->rank = c.take<int>(size_t(s.Tmax) * s.k);
     w->hist = c.take<int>(size_t((s.Tmax + kRankChunk - 1) / kRankChunk) * s.E);
+    w->tile_counters = c.take<int>(4);
     w->go_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
     w->dgdu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
     w->ap = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
@@ -731,6 +733,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     const int rows = int(s.rows);
     const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(grad_out);
 
+    // the weight-gradient launches claim their tiles from these counters
+    MOE_CU(cudaMemsetAsync(ws.tile_counters, 0, 4 * sizeof(int), st));
     { Timed tm_(h, MOE_K_GATHER, st);
     MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, mx ? ws.go_q : nullptr,
                               mx ? ws.go_sf : nullptr, h->sms, st)); }
@@ -899,6 +903,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
                               mg->strides[4][1], mg_bf16, st, &m.c1, &a.c1_tab));
         a.m_split = I;
         a.mg_bf16 = mg_bf16;
+        a.tile_counter = ws.tile_counters + 0;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
@@ -917,6 +922,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
                               mg->strides[5][1], mg_bf16, st, &m.c0, &a.c0_tab));
         m.c1 = m.c0;
         a.mg_bf16 = mg_bf16;
+        a.tile_counter = ws.tile_counters + 1;
         Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
     }
@@ -936,6 +942,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
             return MOE_ERR_INVALID_ARG;
         a.m_split = I;
         a.mg_bf16 = mg_bf16;
+        a.tile_counter = ws.tile_counters + 2;
         Timed tm_(h, MOE_K_WGRAD_FC1_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
@@ -953,6 +960,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         if (!map_main_grad(&m.c0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16)) return MOE_ERR_INVALID_ARG;
         m.c1 = m.c0;
         a.mg_bf16 = mg_bf16;
+        a.tile_counter = ws.tile_counters + 3;
         Timed tm_(h, MOE_K_WGRAD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
