@@ -160,7 +160,9 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4):
     without tokens are not read. mx: the routed forward/dgrad GEMMs read MXFP8
     operands (1 byte + 1/32 byte of scale per element) and the producers of
     those operands also write their MXFP8 copies. mg_bytes: main_grad element
-    size (read and written once by the weight-gradient kernels)."""
+    size (read and written once by the weight-gradient kernels). With BF16 routed
+    weights (not mx) the shared expert runs as group 0 of the routed launches:
+    their classes carry the shared work too, and the routing kernels copy its rows."""
     b2, b4 = 2, 4
     bq = 1 + 1 / 32                          # MXFP8 element incl. its share of the scale
     wb = bq if mx else b2                    # routed weight element
@@ -193,6 +195,18 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4):
         "shared_gate_fwd": (2 * T * H, T * H * b2 + H * b2 + T * b4),
         "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 2 * mg_bytes),
     }
+    if not mx:
+        for op in ("fwd_gu", "fwd_down", "bwd_down", "bwd_gu", "wgrad_fc1", "wgrad_down"):
+            rf, rb = table[f"gemm_{op}_routed"]
+            sf, sb = table[f"gemm_{op}_shared"]
+            table[f"gemm_{op}_routed"] = (rf + sf, rb + sb)
+        if name == "gemm_bwd_down_routed":  # the shared rows' p * a and partials, as for the routed rows
+            f, b = table[name]
+            table[name] = (f, b + T * I * b2)
+        f, b = table["route_place"]
+        table["route_place"] = (f, b + 2 * T * H * b2 + T * 8)
+        f, b = table["gather_rows"]
+        table["gather_rows"] = (f, b + 2 * T * H * b2)
     return table[name]
 
 

@@ -152,11 +152,14 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  * >= moe_workspace_size bytes, kept alive and unused by others until
  * moe_destroy). The handle itself is host memory owned by the library. The
  * current CUDA device at this call is the device of every later call.
- * Per-expert descriptor tables (moe_wview.expert_ptrs,
- * moe_main_grads.expert_ptrs) become TMA descriptors in this workspace; they
- * are re-encoded and uploaded only when a table's pointers change, and such an
- * upload (a host-to-device copy from library host memory) waits for the work
- * already queued on `stream` before it starts. */
+ * Weight and main_grad views become per-expert TMA descriptor tables in this
+ * workspace (with BF16 routed weights every view, the shared expert's as entry
+ * 0; with MXFP8 ones the main_grad views given as moe_main_grads.expert_ptrs).
+ * A table is re-encoded and uploaded only when its pointers, strides or dtype
+ * change; such an upload (a host-to-device copy from library host memory)
+ * waits for the work already queued on `stream` before it starts, and cannot
+ * be captured into a CUDA graph: run one call with the same buffers before
+ * capturing. */
 moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_handle** out);
 void moe_destroy(moe_handle* h);
 
@@ -256,7 +259,10 @@ moe_status moe_device_status(moe_handle* h, void* stream);
 /* Number of kernels this library has launched in this process. */
 uint64_t moe_launch_count(void);
 
-/* Kernel classes of the layer, in the order moe_profile_read reports them. */
+/* Kernel classes of the layer, in the order moe_profile_read reports them.
+ * With BF16 routed weights the shared expert runs as group 0 of the ROUTED
+ * classes' grouped GEMMs (its rows before the routed segments), so the
+ * *_SHARED GEMM classes launch only with MXFP8 routed weights. */
 enum {
     MOE_K_ROUTE_PACK = 0, MOE_K_ROUTE_SCAN, MOE_K_ROUTE_PLACE, MOE_K_GATHER,
     MOE_K_FWD_GU_ROUTED, MOE_K_FWD_GU_SHARED, MOE_K_FWD_DOWN_ROUTED, MOE_K_FWD_DOWN_SHARED, MOE_K_COMBINE,

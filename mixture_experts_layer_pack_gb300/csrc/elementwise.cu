@@ -20,12 +20,13 @@ namespace {
 // one warp per row, 16-byte vectors
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                           const int* __restrict__ perm_src,
-                                                          const int* __restrict__ meta, int max_rows, int vec_per_row,
+                                                          const int* __restrict__ n_dev, int row0, int max_rows,
+                                                          int vec_per_row,
                                                           uint4* __restrict__ dst, uint8_t* __restrict__ dst_q,
                                                           uint8_t* __restrict__ dst_sf) {
     pdl_wait();
     pdl_trigger();
-    const int rows = min(meta[2], max_rows);
+    const int rows = min(row0 + *n_dev, max_rows);
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
@@ -156,11 +157,12 @@ int grid_for(int64_t work, int threads, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
-                               __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms, cudaStream_t st) {
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* n_dev, int row0,
+                               int max_rows, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms,
+                               cudaStream_t st) {
     const int grid = grid_for(int64_t(max_rows) * 32, 256, num_sms);
     const cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, st,
-                                     reinterpret_cast<const uint4*>(src), perm_src, meta, max_rows, H / 8,
+                                     reinterpret_cast<const uint4*>(src), perm_src, n_dev, row0, max_rows, H / 8,
                                      reinterpret_cast<uint4*>(dst), dst_q, dst_sf);
     count_launch();
     return e;

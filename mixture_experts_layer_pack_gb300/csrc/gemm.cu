@@ -117,8 +117,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 
 template <int OP, int BN>
 __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, uint8_t* sb, const CUtensorMap* mA,
-                                            const CUtensorMap* mB0, const CUtensorMap* mB1, uint64_t* bar,
-                                            const GemmArgs& a) {
+                                            const CUtensorMap* mB0, const CUtensorMap* mB1, const CUtensorMap* mS0,
+                                            const CUtensorMap* mS1, uint64_t* bar, const GemmArgs& a) {
     const int k0 = kb * kBK;
     if (OP == OP_WGRAD) {
         const int krow = t.k_lo + k0;
@@ -129,11 +129,14 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, 
         return;
     }
     tma_load_2d(sa, mA, bar, k0, t.mt * kBM);
-    // an expert's weights: its own descriptor (z = 0) from a per-expert table, or the 3D map at z = e
-    const CUtensorMap* B0 = a.b0_tab ? a.b0_tab + t.e : mB0;
-    const CUtensorMap* B1 = a.b1_tab ? a.b1_tab + t.e : mB1;
-    const int z0 = a.b0_tab ? 0 : t.e;
-    const int z1 = a.b1_tab ? 0 : t.e;
+    // an expert's weights: group 0's own maps when it is the shared expert, else
+    // routed expert re's descriptor (z = 0) from a per-expert table or the 3D map at z = re
+    const bool sh = a.group0_shared && t.e == 0;
+    const int re = t.e - a.group0_shared;
+    const CUtensorMap* B0 = sh ? mS0 : (a.b0_tab ? a.b0_tab + re : mB0);
+    const CUtensorMap* B1 = sh ? mS1 : (a.b1_tab ? a.b1_tab + re : mB1);
+    const int z0 = (sh || a.b0_tab) ? 0 : re;
+    const int z1 = (sh || a.b1_tab) ? 0 : re;
     if (OP == OP_FWD_GU) {
         const int j0 = t.nt * (BN / 2);
         tma_load_3d(sb, B0, bar, k0, j0, z0);
@@ -389,7 +392,8 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
                                                float* bufs, uint64_t* mg_bar, uint64_t* tfull, uint64_t* tempty,
                                                const uint64_t* ring_full, uint64_t* ring_empty,
                                                const int* ring_tile, volatile int* abort_flag,
-                                               const CUtensorMap* mC0, const CUtensorMap* mC1) {
+                                               const CUtensorMap* mC0, const CUtensorMap* mC1,
+                                               const CUtensorMap* mS0, const CUtensorMap* mS1) {
     const int lane = threadIdx.x & 31;
     const bool bf = args.mg_bf16 != 0;
     const int bw = bf ? 64 : 32;                           // box width in elements
@@ -407,14 +411,17 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
         }
         return __shfl_sync(0xffffffffu, v, 0);
     };
-    // box (tile t, c-th box of this warp): destination map and coordinates (an
-    // expert's own descriptor at z = 0 when main_grad comes as a per-expert table)
+    // box (tile t, c-th box of this warp): destination map and coordinates (group
+    // 0's own maps when it is the shared expert; a routed expert's own descriptor
+    // at z = 0 when main_grad comes as a per-expert table, else the 3D map)
     auto box = [&](const Tile& t, int c, const CUtensorMap*& mc, int& x, int& y, int& z) {
         const int m0 = t.mt * kBM + q * 32;
         const bool hi = m0 >= args.m_split;
+        const bool sh = args.group0_shared && t.e == 0;
+        const int re = t.e - args.group0_shared;
         const CUtensorMap* tab = hi ? args.c1_tab : args.c0_tab;
-        mc = tab ? tab + t.e : (hi ? mC1 : mC0);
-        z = tab ? 0 : t.e;
+        mc = sh ? (hi ? mS1 : mS0) : (tab ? tab + re : (hi ? mC1 : mC0));
+        z = (sh || tab) ? 0 : re;
         y = hi ? m0 - args.m_split : m0;
         x = t.nt * BN + (half + c * kEpiHalves) * bw;
     };
@@ -539,7 +546,8 @@ template <int OP, int BN, bool CLAMP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
-                    const __grid_constant__ CUtensorMap tmC1, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmS0,
+                    const __grid_constant__ CUtensorMap tmS1, const GemmArgs args) {
     using C = Cfg<OP, BN>;
     constexpr bool A_MN = (OP == OP_WGRAD);
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD);
@@ -591,6 +599,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_prefetch_map(&tmC0);
             tma_prefetch_map(&tmC1);
         }
+        if (args.group0_shared) {
+            tma_prefetch_map(&tmS0);
+            if (OP == OP_FWD_GU || OP == OP_BWD_GU || OP == OP_WGRAD) tma_prefetch_map(&tmS1);
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
@@ -640,7 +652,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    issue_loads<OP, BN>(t, kb, sa, sa + C::A_BYTES, &tmA, &tmB0, &tmB1, &full[stage], args);
+                    issue_loads<OP, BN>(t, kb, sa, sa + C::A_BYTES, &tmA, &tmB0, &tmB1, &tmS0, &tmS1, &full[stage],
+                                        args);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -719,7 +732,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float* my_staging = staging + (warp - 2) * C::BUFS * (kStageTileBytes / 4);
         if constexpr (OP == OP_WGRAD) {
             wgrad_epilogue<BN>(args, tmem_base, q, half, my_staging, mg_bar + 2 * (warp - 2), tfull, tempty,
-                               ring_full, ring_empty, ring_tile, abort_flag, &tmC0, &tmC1);
+                               ring_full, ring_empty, ring_tile, abort_flag, &tmC0, &tmC1,
+                               &tmS0, &tmS1);
         } else {
             int it = 0;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -1005,7 +1019,8 @@ cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStrea
         attr_set = true;
     }
     const cudaError_t e =
-        launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg<OP, BN>::SMEM, st, m.a, m.b0, m.b1, m.c0, m.c1, a);
+        launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg<OP, BN>::SMEM, st, m.a, m.b0, m.b1, m.c0, m.c1, m.s0,
+                   m.s1, a);
     count_launch();
     return e;
 }

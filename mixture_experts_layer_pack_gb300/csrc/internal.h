@@ -65,6 +65,9 @@ struct GemmArgs {
     const CUtensorMap* b1_tab;
     const CUtensorMap* c0_tab;
     const CUtensorMap* c1_tab;
+    // 1: group (expert) 0 is the shared expert, with its own maps (GemmMaps s0, s1),
+    // and group e >= 1 routed expert e - 1 (the tables' entry e - 1, or z = e - 1)
+    int group0_shared;
     int* status;
     // MXFP8 (block-scaled) GEMMs
     uint8_t* q_out;             // E4M3 copy of the epilogue's GEMM-operand output (a, or [dg|du])
@@ -79,7 +82,9 @@ struct GemmArgs {
 
 struct GemmMaps {
     CUtensorMap a, b0, b1;
-    CUtensorMap c0, c1;  // OP_WGRAD: fp32 main_grad destinations (rows < m_split, rows >= m_split)
+    CUtensorMap c0, c1;  // OP_WGRAD: main_grad destinations (rows < m_split, rows >= m_split)
+    // group0_shared: the shared expert's b0, b1 (OP 0..3) or c0, c1 (OP_WGRAD)
+    CUtensorMap s0, s1;
 };
 
 // tensor-map construction (driver entry point resolved at first use), 128-byte swizzle
@@ -101,14 +106,20 @@ constexpr int kRankChunk = 128;  // tokens per block of the fused pack/rank kern
 int route_rank_max_tokens();
 cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
                                    int* row_of, int* rank, int* hist, int* status, cudaStream_t st);
+// mtile_x (optional): tile experts of the shared-first grouped GEMM (shared_tiles
+// tiles of group 0, then routed expert e as group e + 1), seg_x its E + 2 row
+// offsets, meta[3] its tile count and meta[4] its row count
 cudaError_t launch_route_scan_chunks(int* hist, int T, int E, int* counts, int* offsets, int* offs_pad,
-                                     int* mtile_expert, int* meta, cudaStream_t st);
+                                     int* mtile_expert, int* meta, int shared_tiles, int* mtile_x, int* seg_x,
+                                     cudaStream_t st);
 cudaError_t launch_route_pack(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
                               int* row_of, int* status, cudaStream_t st);
 cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, int k, int* rank, int* counts,
                               cudaStream_t st);
+// shared_rows > 0: also writes the shared expert's rows, which sit at rows
+// [-shared_rows, 0) of perm_src, pp_perm and x_perm (no MXFP8 copy)
 cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* chunk_base,
-                               const int* counts, const int* offs_pad, int T, int E, int k,
+                               const int* counts, const int* offs_pad, int T, int E, int k, int shared_rows,
                                const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
                                __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st);
 cudaError_t launch_swizzle_scales(int mode, const uint8_t* src0, const uint8_t* src1, int64_t src_es, int64_t src_rs,
@@ -119,8 +130,10 @@ cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* 
                                   cudaStream_t st);
 
 // elementwise / copy
-cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* meta, int max_rows, int H,
-                               __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms, cudaStream_t st);
+// dst row r (r < row0 + *n_dev, r < max_rows) = src row perm_src[r], a zero row where it is -1
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* n_dev, int row0,
+                               int max_rows, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms,
+                               cudaStream_t st);
 cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __nv_bfloat16* y, const int* row_of,
                            const float* pp, int T, int H, int k, __nv_bfloat16* out, int num_sms, cudaStream_t st);
 cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,

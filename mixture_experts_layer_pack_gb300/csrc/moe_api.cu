@@ -37,6 +37,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Shape {
     int64_t Tmax, H, E, k, I;
     int64_t rows;     // permuted rows incl. padding, worst case
+    int64_t srows;    // rows of the shared expert's region (Tmax rounded up to 128)
     int bn_gu, bn_down, bn_bd, bn_bgu, bn_wfc1, bn_wd;
     int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM x epilogue halves)
     int n_part_s;     // the same for the shared expert's (always BF16) dgrad-down GEMM
@@ -74,7 +75,8 @@ moe_status check_config(const moe_config* c, Shape* s) {
     s->k = c->topk;
     s->I = c->inter;
     s->rows = align_up(size_t(s->Tmax * s->k + s->E * (kBM - 1)), kBM);
-    if (s->rows >= INT_MAX / 2 || s->Tmax * s->k >= INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    s->srows = align_up(size_t(s->Tmax), kBM);
+    if (s->rows + s->srows >= INT_MAX / 2 || s->Tmax * s->k >= INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
     if (s->Tmax > route_rank_max_tokens()) return MOE_ERR_UNSUPPORTED;
     s->bn_gu = pick_bn(2 * s->I, true);
     s->bn_down = pick_bn(s->H, false);
@@ -88,18 +90,21 @@ moe_status check_config(const moe_config* c, Shape* s) {
     return MOE_OK;
 }
 
+// Row buffers (per-row operands of the grouped GEMMs) hold the shared expert's
+// rows first, rows [0, R0) with R0 = T rounded up to 128 (token t at row t, zero
+// rows after T), and the routed segments from row R0 on; srows + rows rows each.
 struct Workspace {
     int* status;
     int* rank;  // rank of each route inside its expert
     int* hist;  // per 128-token chunk and expert: route count, then the chunk's rank offset
     int* tile_counters;  // one per weight-gradient launch of a backward (dynamic tile scheduling)
-    __nv_bfloat16 *go_perm, *dgdu, *ap, *dgdu_s;
-    __nv_bfloat16 *yx, *ys_dxs;  // forward: y (routed rows), y_shared; backward: dx (routed rows), dx_shared
-    float* partial;
-    // shared output gate: the shared rows' dprob partials, dz, chunk sums of the
-    // gate weight's gradient, gate * a_shared (the gated down wgrad operand)
-    float *partial_s, *dz, *gpart;
-    __nv_bfloat16* ap_s;
+    __nv_bfloat16 *go_all, *dgdu_all, *ap_all;  // grad_out rows, [dg|du], prob (or gate) * a
+    __nv_bfloat16* yx_all;  // forward: y; backward: dx
+    float* partial_all;     // dgrad-down partial dot products (n_part per row)
+    // MXFP8 routed weights: the shared expert's own dgrad-down partials (n_part_s per row)
+    float* partial_s;
+    // shared output gate: dz and the chunk sums of the gate weight's gradient
+    float *dz, *gpart;
     // per-expert TMA descriptors of the tables (kTables x E)
     CUtensorMap* tabs;
     // MXFP8 only: quantised backward operands and the swizzled weight scales
@@ -108,12 +113,23 @@ struct Workspace {
 };
 
 struct SavedBufs {
-    int *ids, *row_of, *counts, *offsets, *offs_pad, *meta, *mtile_expert, *perm_src;
-    float *pp, *pp_perm;
-    float* gate;  // shared output gate per token
-    __nv_bfloat16 *x_perm, *a, *a_s;
-    __nv_bfloat16 *gu, *gu_s;  // bf16 [g|u] of the routed rows and the shared expert
-    uint8_t *x_q, *x_sf, *a_q, *a_sf;  // MXFP8 only
+    int *ids, *row_of, *counts, *offsets, *offs_pad, *mtile_expert;  // routed segments (relative to row R0)
+    int* meta;  // [0..2] routed tiles, routes, rows; [3], [4] tiles and rows of the shared-first GEMMs
+    int *mtile_x, *seg_x;  // shared-first grouped GEMMs: group of each 128-row tile, E + 2 group row offsets
+    int* perm_src_all;     // source token of each row (-1: zero row)
+    float* pp;
+    float* pp_all;         // per row: the shared output gate (1 without one), the route's prob, 0 for padding
+    __nv_bfloat16 *x_all, *a_all, *gu_all;  // GEMM input rows, SwiGLU output a, bf16 [g|u] (kept for backward)
+    uint8_t *x_q, *x_sf, *a_q, *a_sf;  // MXFP8 only: routed rows (relative to row R0)
+};
+
+// the routed part of the row buffers for a call with T tokens
+struct Views {
+    int R0;  // rows of the shared expert's region
+    int* perm_src;
+    float* pp_perm;
+    __nv_bfloat16 *x_perm, *a, *gu, *go_perm, *dgdu, *ap, *yx;
+    float* partial;
 };
 
 // bytes of MXFP8 scale atoms for R rows (multiple of 128) and K columns (multiple of 128)
@@ -125,17 +141,15 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->rank = c.take<int>(size_t(s.Tmax) * s.k);
     w->hist = c.take<int>(size_t((s.Tmax + kRankChunk - 1) / kRankChunk) * s.E);
     w->tile_counters = c.take<int>(4);
-    w->go_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
-    w->dgdu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
-    w->ap = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
-    w->yx = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
-    w->partial = c.take<float>(size_t(s.rows) * s.n_part);
-    w->ys_dxs = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.H);
-    w->dgdu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
-    w->partial_s = c.take<float>(size_t(s.Tmax) * s.n_part_s);
+    const size_t ra = size_t(s.srows + s.rows);
+    w->go_all = c.take<__nv_bfloat16>(ra * s.H);
+    w->dgdu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
+    w->ap_all = c.take<__nv_bfloat16>(ra * s.I);
+    w->yx_all = c.take<__nv_bfloat16>(ra * s.H);
+    w->partial_all = c.take<float>(ra * s.n_part);
+    w->partial_s = s.mx ? c.take<float>(size_t(s.Tmax) * s.n_part_s) : nullptr;
     w->dz = c.take<float>(size_t(s.Tmax));
     w->gpart = c.take<float>(size_t((s.Tmax + kGateChunk - 1) / kGateChunk) * s.H);
-    w->ap_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
     w->tabs = c.take<CUtensorMap>(size_t(kTables) * s.E);
     if (s.mx) {
         w->go_q = c.take<uint8_t>(size_t(s.rows) * s.H);
@@ -162,16 +176,16 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->counts = c.take<int>(s.E);
     b->offsets = c.take<int>(s.E + 1);
     b->offs_pad = c.take<int>(s.E + 1);
-    b->meta = c.take<int>(4);
+    b->meta = c.take<int>(8);
     b->mtile_expert = c.take<int>(s.rows / kBM);
-    b->perm_src = c.take<int>(s.rows);
-    b->pp_perm = c.take<float>(s.rows);
-    b->gate = c.take<float>(size_t(s.Tmax));
-    b->x_perm = c.take<__nv_bfloat16>(size_t(s.rows) * s.H);
-    b->a = c.take<__nv_bfloat16>(size_t(s.rows) * s.I);
-    b->gu = c.take<__nv_bfloat16>(size_t(s.rows) * 2 * s.I);
-    b->a_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * s.I);
-    b->gu_s = c.take<__nv_bfloat16>(size_t(s.Tmax) * 2 * s.I);
+    const size_t ra = size_t(s.srows + s.rows);
+    b->mtile_x = c.take<int>(ra / kBM);
+    b->seg_x = c.take<int>(s.E + 2);
+    b->perm_src_all = c.take<int>(ra);
+    b->pp_all = c.take<float>(ra);
+    b->x_all = c.take<__nv_bfloat16>(ra * s.H);
+    b->a_all = c.take<__nv_bfloat16>(ra * s.I);
+    b->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
     if (s.mx) {
         b->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
         b->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -181,6 +195,23 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
         b->x_q = b->x_sf = b->a_q = b->a_sf = nullptr;
     }
     return align_up(c.off, kAlign);
+}
+
+Views views_of(const Shape& s, const SavedBufs& b, const Workspace& w, int64_t T) {
+    Views v;
+    v.R0 = int(align_up(size_t(T), kBM));
+    const int64_t r = v.R0;
+    v.perm_src = b.perm_src_all + r;
+    v.pp_perm = b.pp_all + r;
+    v.x_perm = b.x_all + r * s.H;
+    v.a = b.a_all + r * s.I;
+    v.gu = b.gu_all + r * 2 * s.I;
+    v.go_perm = w.go_all + r * s.H;
+    v.dgdu = w.dgdu_all + r * 2 * s.I;
+    v.ap = w.ap_all + r * s.I;
+    v.yx = w.yx_all + r * s.H;
+    v.partial = w.partial_all + r * s.n_part;
+    return v;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -339,8 +370,8 @@ cudaEvent_t take_event(moe_handle* h) {
     return e;
 }
 
-// Per-expert descriptor table `id`: encodes one descriptor per expert with
-// enc(map, expert pointer) when the pointers or `key` (what else the
+// Per-expert descriptor table `id`: encodes one descriptor per routed expert
+// with enc(map, expert pointer) when the pointers or `key` (what else the
 // descriptors encode) changed since the last upload, and uploads them into the
 // workspace; *tab = their device address, *first = expert 0's descriptor (a
 // valid map for the kernel's own map parameter).
@@ -565,20 +596,24 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
 
     const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
     const int rows = int(s.rows);
+    const Views v = views_of(s, b, ws, T);
+    const int rows_all = v.R0 + rows;  // rows of the shared-first grouped GEMMs (BF16 routed weights)
 
     // dispatch: route-pack, per-expert ranks, segment scan, placement + row gather
+    // (with BF16 routed weights also the shared expert's rows, as group 0 of the GEMMs)
     { Timed tm_(h, MOE_K_ROUTE_PACK, st);
     MOE_CU(launch_route_pack_rank(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.rank, ws.hist, ws.status,
                                   st)); }
     { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
-    MOE_CU(launch_route_scan_chunks(ws.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta, st)); }
+    MOE_CU(launch_route_scan_chunks(ws.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta,
+                                    v.R0 / kBM, mx ? nullptr : b.mtile_x, b.seg_x, st)); }
     { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
-    MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, ws.hist, b.counts, b.offs_pad, Ti, E, k,
-                              static_cast<const __nv_bfloat16*>(hidden), H, b.perm_src, b.pp_perm, b.row_of, b.x_perm,
+    MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, ws.hist, b.counts, b.offs_pad, Ti, E, k, mx ? 0 : v.R0,
+                              static_cast<const __nv_bfloat16*>(hidden), H, v.perm_src, v.pp_perm, b.row_of, v.x_perm,
                               mx ? b.x_q : nullptr, mx ? b.x_sf : nullptr, st)); }
 
-    GemmMaps m;
-    // routed gate/up + SwiGLU
+    GemmMaps m{};
+    // gate/up + SwiGLU
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.x_q, rows, H, H) ||
@@ -591,9 +626,9 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.n_tiles = 2 * I / kMxBN;
         a.k_blocks = H / kMxBK;
         a.gate_up_split = I;
-        a.out0 = b.a;
+        a.out0 = v.a;
         a.ld_out0 = I;
-        a.outh = b.gu;
+        a.outh = v.gu;
         a.ld_outh = 2 * I;
         a.q_out = b.a_q;
         a.ld_q = I;
@@ -606,28 +641,30 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.sfb_kgroups = H / 128;
         Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
         MOE_CU(launch_gemm_mx(OP_FWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
-    } else
-    {
+    } else {  // shared expert (group 0) and routed experts in one launch
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
-        if (!map_kmajor(&m.a, b.x_perm, rows, H, H)) return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, b.x_all, rows_all, H, H)) return MOE_ERR_INVALID_ARG;
         MOE_TRY(routed_map(h, TB_FWD_GU_G, w->routed_gate, I, H, bn / 2, st, &m.b0, &a.b0_tab));
         MOE_TRY(routed_map(h, TB_FWD_GU_U, w->routed_up, I, H, bn / 2, st, &m.b1, &a.b1_tab));
-        a.mtile_expert = b.mtile_expert;
-        a.num_mtiles_dev = b.meta;
-        a.num_mtiles = rows / kBM;
+        if (!map_weight(&m.s0, w->shared_gate, 1, I, H, 64, bn / 2) ||
+            !map_weight(&m.s1, w->shared_up, 1, I, H, 64, bn / 2))
+            return MOE_ERR_INVALID_ARG;
+        a.group0_shared = 1;
+        a.mtile_expert = b.mtile_x;
+        a.num_mtiles_dev = b.meta + 3;
+        a.num_mtiles = rows_all / kBM;
         a.n_tiles = 2 * I / bn;
         a.k_blocks = H / kBK;
         a.gate_up_split = I;
-        a.out0 = b.a;
+        a.out0 = b.a_all;
         a.ld_out0 = I;
-        a.outh = b.gu;
+        a.outh = b.gu_all;
         a.ld_outh = 2 * I;
         Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // shared gate/up + SwiGLU
-    {
+    if (mx) {  // shared gate/up + SwiGLU (BF16) into the shared rows
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
         if (!map_kmajor(&m.a, hidden, Ti, H, H) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, bn / 2) ||
@@ -638,14 +675,14 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.k_blocks = H / kBK;
         a.rows_valid = Ti;
         a.gate_up_split = I;
-        a.out0 = b.a_s;
+        a.out0 = b.a_all;
         a.ld_out0 = I;
-        a.outh = b.gu_s;
+        a.outh = b.gu_all;
         a.ld_outh = 2 * I;
         Timed tm_(h, MOE_K_FWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // routed down projection (y in bf16; the combine weights it by the route's prob)
+    // down projection (y in bf16; the combine weights it by the route's prob or the gate)
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.a_q, rows, I, I) ||
@@ -657,7 +694,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.num_mtiles = rows / kBM;
         a.n_tiles = H / kMxBN;
         a.k_blocks = I / kMxBK;
-        a.outh = ws.yx;
+        a.outh = v.yx;
         a.ld_outh = H;
         a.sfa = b.a_sf;
         a.sfa_kgroups = I / 128;
@@ -666,19 +703,21 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
         a.sfb_kgroups = I / 128;
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm_mx(OP_FWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
-    } else
-    {
+    } else {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
-        if (!map_kmajor(&m.a, b.a, rows, I, I)) return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, b.a_all, rows_all, I, I)) return MOE_ERR_INVALID_ARG;
         MOE_TRY(routed_map(h, TB_FWD_DOWN, w->routed_down, H, I, bn, st, &m.b0, &a.b0_tab));
+        if (!map_weight(&m.s0, w->shared_down, 1, H, I, 64, bn)) return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
-        a.mtile_expert = b.mtile_expert;
-        a.num_mtiles_dev = b.meta;
-        a.num_mtiles = rows / kBM;
+        m.s1 = m.s0;
+        a.group0_shared = 1;
+        a.mtile_expert = b.mtile_x;
+        a.num_mtiles_dev = b.meta + 3;
+        a.num_mtiles = rows_all / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
-        a.outh = ws.yx;
+        a.outh = ws.yx_all;
         a.ld_outh = H;
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
@@ -687,27 +726,26 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     if (gated) {
         Timed tm_(h, MOE_K_SHARED_GATE_FWD, st);
         MOE_CU(launch_gate_forward(static_cast<const __nv_bfloat16*>(hidden),
-                                   static_cast<const __nv_bfloat16*>(w->shared_output_gate), Ti, H, b.gate, st));
+                                   static_cast<const __nv_bfloat16*>(w->shared_output_gate), Ti, H, b.pp_all, st));
     }
-    // shared down projection
-    {
+    if (mx) {  // shared down projection (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
-        if (!map_kmajor(&m.a, b.a_s, Ti, I, I) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, bn))
+        if (!map_kmajor(&m.a, b.a_all, Ti, I, I) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, bn))
             return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
         a.num_mtiles = (Ti + kBM - 1) / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
         a.rows_valid = Ti;
-        a.outh = ws.ys_dxs;
+        a.outh = ws.yx_all;
         a.ld_outh = H;
         Timed tm_(h, MOE_K_FWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // combine
     Timed tm_(h, MOE_K_COMBINE, st);
-    MOE_CU(launch_combine(ws.ys_dxs, gated ? b.gate : nullptr, ws.yx, b.row_of, b.pp, Ti, H, k,
+    MOE_CU(launch_combine(ws.yx_all, gated ? b.pp_all : nullptr, v.yx, b.row_of, b.pp, Ti, H, k,
                           static_cast<__nv_bfloat16*>(out), h->sms, st));
     return MOE_OK;
 }
@@ -731,16 +769,21 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     const moe_weights* w = &saved->w;
     const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
     const int rows = int(s.rows);
+    const Views v = views_of(s, b, ws, T);
+    const int rows_all = v.R0 + rows;
     const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(grad_out);
 
     // the weight-gradient launches claim their tiles from these counters
     MOE_CU(cudaMemsetAsync(ws.tile_counters, 0, 4 * sizeof(int), st));
     { Timed tm_(h, MOE_K_GATHER, st);
-    MOE_CU(launch_gather_rows(go, b.perm_src, b.meta, rows, H, ws.go_perm, mx ? ws.go_q : nullptr,
-                              mx ? ws.go_sf : nullptr, h->sms, st)); }
+    if (mx)
+        MOE_CU(launch_gather_rows(go, v.perm_src, b.meta + 2, 0, rows, H, v.go_perm, ws.go_q, ws.go_sf, h->sms, st));
+    else  // the shared expert's rows too
+        MOE_CU(launch_gather_rows(go, b.perm_src_all, b.meta + 2, v.R0, rows_all, H, ws.go_all, nullptr, nullptr,
+                                  h->sms, st)); }
 
-    GemmMaps m;
-    // routed dgrad through the down projection + SwiGLU backward + dprob partials
+    GemmMaps m{};
+    // dgrad through the down projection + SwiGLU backward + dprob partials
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, ws.go_q, rows, H, H) ||
@@ -752,15 +795,15 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.num_mtiles = rows / kBM;
         a.n_tiles = I / kMxBN;
         a.k_blocks = H / kMxBK;
-        a.in0 = b.a;
+        a.in0 = v.a;
         a.ld_in0 = I;
-        a.inh = b.gu;
+        a.inh = v.gu;
         a.ld_inh = 2 * I;
-        a.row_scale = b.pp_perm;
-        a.partial = ws.partial;
-        a.out0 = ws.dgdu;
+        a.row_scale = v.pp_perm;
+        a.partial = v.partial;
+        a.out0 = v.dgdu;
         a.ld_out0 = 2 * I;
-        a.out1 = ws.ap;
+        a.out1 = v.ap;
         a.ld_out1 = I;
         a.q_out = ws.dgdu_q;
         a.ld_q = 2 * I;
@@ -773,33 +816,34 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.sfb_kgroups = H / 128;
         Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm_mx(OP_BWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
-    } else
-    {
+    } else {  // shared expert (group 0: its rows' scale is the gate, or 1) and routed experts
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
-        if (!map_kmajor(&m.a, ws.go_perm, rows, H, H)) return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, ws.go_all, rows_all, H, H)) return MOE_ERR_INVALID_ARG;
         MOE_TRY(routed_map(h, TB_BWD_DOWN, w->routed_down, H, I, 64, st, &m.b0, &a.b0_tab));
+        if (!map_weight(&m.s0, w->shared_down, 1, H, I, 64, 64)) return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
-        a.mtile_expert = b.mtile_expert;
-        a.num_mtiles_dev = b.meta;
-        a.num_mtiles = rows / kBM;
+        m.s1 = m.s0;
+        a.group0_shared = 1;
+        a.mtile_expert = b.mtile_x;
+        a.num_mtiles_dev = b.meta + 3;
+        a.num_mtiles = rows_all / kBM;
         a.n_tiles = I / bn;
         a.k_blocks = H / kBK;
-        a.in0 = b.a;
+        a.in0 = b.a_all;
         a.ld_in0 = I;
-        a.inh = b.gu;
+        a.inh = b.gu_all;
         a.ld_inh = 2 * I;
-        a.row_scale = b.pp_perm;
-        a.partial = ws.partial;
-        a.out0 = ws.dgdu;
+        a.row_scale = b.pp_all;
+        a.partial = ws.partial_all;
+        a.out0 = ws.dgdu_all;
         a.ld_out0 = 2 * I;
-        a.out1 = ws.ap;
+        a.out1 = ws.ap_all;
         a.ld_out1 = I;
         Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // shared dgrad through the down projection + SwiGLU backward
-    {
+    if (mx) {  // shared dgrad through the down projection + SwiGLU backward (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
         if (!map_kmajor(&m.a, go, Ti, H, H) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, 64))
@@ -809,16 +853,16 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = I / bn;
         a.k_blocks = H / kBK;
         a.rows_valid = Ti;
-        a.in0 = b.a_s;
+        a.in0 = b.a_all;
         a.ld_in0 = I;
-        a.inh = b.gu_s;
+        a.inh = b.gu_all;
         a.ld_inh = 2 * I;
-        a.out0 = ws.dgdu_s;
+        a.out0 = ws.dgdu_all;
         a.ld_out0 = 2 * I;
         if (gated) {  // the gate acts as the shared rows' prob: dgate partials, gate * a_shared
-            a.row_scale = b.gate;
+            a.row_scale = b.pp_all;
             a.partial = ws.partial_s;
-            a.out1 = ws.ap_s;
+            a.out1 = ws.ap_all;
             a.ld_out1 = I;
         }
         Timed tm_(h, MOE_K_BWD_DOWN_SHARED, st);
@@ -826,10 +870,11 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     if (gated) {
         Timed tm_(h, MOE_K_SHARED_GATE_BWD, st);
-        MOE_CU(launch_gate_backward(static_cast<const __nv_bfloat16*>(saved->hidden), b.gate, ws.partial_s, s.n_part_s,
-                                    Ti, H, ws.dz, ws.gpart, mg->shared_output_gate, mg_bf16, st));
+        MOE_CU(launch_gate_backward(static_cast<const __nv_bfloat16*>(saved->hidden), b.pp_all,
+                                    mx ? ws.partial_s : ws.partial_all, mx ? s.n_part_s : s.n_part, Ti, H, ws.dz,
+                                    ws.gpart, mg->shared_output_gate, mg_bf16, st));
     }
-    // routed dgrad through gate/up
+    // dgrad through gate/up
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, ws.dgdu_q, rows, 2 * I, 2 * I) ||
@@ -842,7 +887,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = H / kMxBN;
         a.k_blocks = 2 * I / kMxBK;
         a.gate_up_split = I;
-        a.outh = ws.yx;
+        a.outh = v.yx;
         a.ld_outh = H;
         a.sfa = ws.dgdu_sf;
         a.sfa_kgroups = 2 * I / 128;
@@ -851,29 +896,30 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.sfb_kgroups = 2 * I / 128;
         Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
         MOE_CU(launch_gemm_mx(OP_BWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
-    } else
-    {
+    } else {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
-        if (!map_kmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
         MOE_TRY(routed_map(h, TB_BWD_GU_G, w->routed_gate, I, H, 64, st, &m.b0, &a.b0_tab));
         MOE_TRY(routed_map(h, TB_BWD_GU_U, w->routed_up, I, H, 64, st, &m.b1, &a.b1_tab));
-        a.mtile_expert = b.mtile_expert;
-        a.num_mtiles_dev = b.meta;
-        a.num_mtiles = rows / kBM;
+        if (!map_weight(&m.s0, w->shared_gate, 1, I, H, 64, 64) || !map_weight(&m.s1, w->shared_up, 1, I, H, 64, 64))
+            return MOE_ERR_INVALID_ARG;
+        a.group0_shared = 1;
+        a.mtile_expert = b.mtile_x;
+        a.num_mtiles_dev = b.meta + 3;
+        a.num_mtiles = rows_all / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = 2 * I / kBK;
         a.gate_up_split = I;
-        a.outh = ws.yx;
+        a.outh = ws.yx_all;
         a.ld_outh = H;
         Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // shared dgrad through gate/up
-    {
+    if (mx) {  // shared dgrad through gate/up (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
-        if (!map_kmajor(&m.a, ws.dgdu_s, Ti, 2 * I, 2 * I) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, 64) ||
+        if (!map_kmajor(&m.a, ws.dgdu_all, Ti, 2 * I, 2 * I) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, 64) ||
             !map_weight(&m.b1, w->shared_up, 1, I, H, 64, 64))
             return MOE_ERR_INVALID_ARG;
         a.num_mtiles = (Ti + kBM - 1) / kBM;
@@ -881,56 +927,77 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.k_blocks = 2 * I / kBK;
         a.rows_valid = Ti;
         a.gate_up_split = I;
-        a.outh = ws.ys_dxs;
+        a.outh = ws.yx_all;
         a.ld_outh = H;
         Timed tm_(h, MOE_K_BWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // routed wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e
+    // wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e (BF16 routed weights: the
+    // shared expert as group 0, whose long K range is claimed first)
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wfc1;
-        if (!map_mnmajor(&m.a, ws.dgdu, rows, 2 * I, 2 * I) || !map_mnmajor(&m.b0, b.x_perm, rows, H, H))
-            return MOE_ERR_INVALID_ARG;
-        m.b1 = m.b0;
-        a.seg_off = b.offs_pad;
-        a.groups = E;
         a.m_tiles = 2 * I / kBM;
         a.n_tiles = H / bn;
+        a.m_split = I;
+        a.mg_bf16 = mg_bf16;
+        a.tile_counter = ws.tile_counters + 0;
         MOE_TRY(routed_mg_map(h, TB_MG_G, mg->routed_gate, mg->expert_ptrs[0], I, H, mg->strides[3][0],
                               mg->strides[3][1], mg_bf16, st, &m.c0, &a.c0_tab));
         MOE_TRY(routed_mg_map(h, TB_MG_U, mg->routed_up, mg->expert_ptrs[1], I, H, mg->strides[4][0],
                               mg->strides[4][1], mg_bf16, st, &m.c1, &a.c1_tab));
-        a.m_split = I;
-        a.mg_bf16 = mg_bf16;
-        a.tile_counter = ws.tile_counters + 0;
+        if (mx) {
+            if (!map_mnmajor(&m.a, v.dgdu, rows, 2 * I, 2 * I) || !map_mnmajor(&m.b0, v.x_perm, rows, H, H))
+                return MOE_ERR_INVALID_ARG;
+            a.seg_off = b.offs_pad;
+            a.groups = E;
+        } else {
+            if (!map_mnmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I) ||
+                !map_mnmajor(&m.b0, b.x_all, rows_all, H, H) ||
+                !map_main_grad(&m.s0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1], mg_bf16) ||
+                !map_main_grad(&m.s1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
+                return MOE_ERR_INVALID_ARG;
+            a.seg_off = b.seg_x;
+            a.groups = E + 1;
+            a.group0_shared = 1;
+        }
+        m.b1 = m.b0;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
-        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
+        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.groups) * a.m_tiles * a.n_tiles, h->sms), st));
     }
-    // routed wgrad of down: main_grad[e] += go_perm_e^T (p a)_e
+    // wgrad of down: main_grad[e] += go_e^T (p a)_e
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wd;
-        if (!map_mnmajor(&m.a, ws.go_perm, rows, H, H) || !map_mnmajor(&m.b0, ws.ap, rows, I, I))
-            return MOE_ERR_INVALID_ARG;
-        m.b1 = m.b0;
-        a.seg_off = b.offs_pad;
-        a.groups = E;
         a.m_tiles = H / kBM;
         a.n_tiles = I / bn;
-        MOE_TRY(routed_mg_map(h, TB_MG_D, mg->routed_down, mg->expert_ptrs[2], H, I, mg->strides[5][0],
-                              mg->strides[5][1], mg_bf16, st, &m.c0, &a.c0_tab));
-        m.c1 = m.c0;
         a.mg_bf16 = mg_bf16;
         a.tile_counter = ws.tile_counters + 1;
+        MOE_TRY(routed_mg_map(h, TB_MG_D, mg->routed_down, mg->expert_ptrs[2], H, I, mg->strides[5][0],
+                              mg->strides[5][1], mg_bf16, st, &m.c0, &a.c0_tab));
+        if (mx) {
+            if (!map_mnmajor(&m.a, v.go_perm, rows, H, H) || !map_mnmajor(&m.b0, v.ap, rows, I, I))
+                return MOE_ERR_INVALID_ARG;
+            a.seg_off = b.offs_pad;
+            a.groups = E;
+        } else {
+            if (!map_mnmajor(&m.a, ws.go_all, rows_all, H, H) || !map_mnmajor(&m.b0, ws.ap_all, rows_all, I, I) ||
+                !map_main_grad(&m.s0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16))
+                return MOE_ERR_INVALID_ARG;
+            a.seg_off = b.seg_x;
+            a.groups = E + 1;
+            a.group0_shared = 1;
+        }
+        m.b1 = m.b0;
+        m.c1 = m.c0;
+        m.s1 = m.s0;
         Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
-        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(E) * a.m_tiles * a.n_tiles, h->sms), st));
+        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.groups) * a.m_tiles * a.n_tiles, h->sms), st));
     }
-    // shared wgrad of gate/up
-    {
+    if (mx) {  // shared wgrad of gate/up (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wfc1;
-        if (!map_mnmajor(&m.a, ws.dgdu_s, Ti, 2 * I, 2 * I) || !map_mnmajor(&m.b0, saved->hidden, Ti, H, H))
+        if (!map_mnmajor(&m.a, ws.dgdu_all, Ti, 2 * I, 2 * I) || !map_mnmajor(&m.b0, saved->hidden, Ti, H, H))
             return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
         a.seg_len = Ti;
@@ -946,11 +1013,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         Timed tm_(h, MOE_K_WGRAD_FC1_SHARED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
-    // shared wgrad of down
-    {
+    if (mx) {  // shared wgrad of down (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wd;
-        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, gated ? ws.ap_s : b.a_s, Ti, I, I))
+        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, gated ? ws.ap_all : b.a_all, Ti, I, I))
             return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
         a.seg_len = Ti;
@@ -966,7 +1032,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // dhidden = shared + un-permuted routed dgrad; dense dprobs
     Timed tm_(h, MOE_K_UNPERMUTE, st);
-    MOE_CU(launch_unpermute(ws.ys_dxs, ws.yx, b.row_of, b.ids, ws.partial, s.n_part, Ti, H, k, E,
+    MOE_CU(launch_unpermute(ws.yx_all, v.yx, b.row_of, b.ids, v.partial, s.n_part, Ti, H, k, E,
                             gated ? ws.dz : nullptr,
                             gated ? static_cast<const __nv_bfloat16*>(w->shared_output_gate) : nullptr,
                             static_cast<__nv_bfloat16*>(dhidden), dprobs, h->sms, st));
@@ -1018,7 +1084,8 @@ moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* id
     if (offsets)
         MOE_CU(cudaMemcpyAsync(offsets, b.offsets, (s.E + 1) * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
     if (perm_src || row_of)
-        MOE_CU(launch_export_routing(b.ids, b.row_of, b.perm_src, b.counts, b.offsets, b.offs_pad, b.mtile_expert,
+        MOE_CU(launch_export_routing(b.ids, b.row_of, views_of(s, b, h->ws, T).perm_src, b.counts, b.offsets,
+                                     b.offs_pad, b.mtile_expert,
                                      b.meta, int(T), int(s.k), int(s.rows), perm_src, row_of, st));
     return MOE_OK;
 }

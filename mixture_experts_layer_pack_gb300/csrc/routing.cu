@@ -316,7 +316,8 @@ __global__ void __launch_bounds__(1024) route_scan_chunks_kernel(int* __restrict
                                                                  int* __restrict__ counts, int* __restrict__ offsets,
                                                                  int* __restrict__ offs_pad,
                                                                  int* __restrict__ mtile_expert,
-                                                                 int* __restrict__ meta) {
+                                                                 int* __restrict__ meta, int shared_tiles,
+                                                                 int* __restrict__ mtile_x, int* __restrict__ seg_x) {
     pdl_wait();
     pdl_trigger();
     __shared__ int s_warp[32];
@@ -357,16 +358,34 @@ __global__ void __launch_bounds__(1024) route_scan_chunks_kernel(int* __restrict
         meta[1] = total_cnt;
         meta[2] = total_pad;
     }
+    if (!mtile_x) return;
+    // the shared expert and the routed experts as one grouped GEMM: group 0 is the
+    // shared expert over rows [0, 128 * shared_tiles), group e + 1 routed expert e
+    // at its segment shifted by those rows
+    const int r0 = shared_tiles * kBM;
+    for (int j = threadIdx.x; j < shared_tiles; j += blockDim.x) mtile_x[j] = 0;
+    if (e < E) {
+        for (int j = 0; j < padded / kBM; ++j) mtile_x[shared_tiles + offp / kBM + j] = e + 1;
+        seg_x[e + 1] = r0 + offp;
+    }
+    if (e == 0) {
+        seg_x[0] = 0;
+        seg_x[E + 1] = r0 + total_pad;
+        meta[3] = shared_tiles + total_pad / kBM;
+        meta[4] = r0 + total_pad;
+    }
 }
 
-// items [0, T*k): routes; items [T*k, T*k + E*128): padding rows (expert j/128, row j%128).
-// With x_q set, the copied row is also quantised to MXFP8 along H (the routed
+// items [0, T*k): routes; items [T*k, T*k + E*128): padding rows (expert j/128, row
+// j%128); with shared_rows > 0, items [T*k + E*128, ... + shared_rows): the shared
+// expert's rows, which sit before the routed segments at rows -shared_rows + t
+// (token t for t < T, a zero row after it). With x_q set, the copied row is also quantised to MXFP8 along H (the routed
 // gate/up GEMM's operand): E4M3 codes to x_q, scales to x_sf in the MMA's
 // scale-factor layout.
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     const int* __restrict__ ids, const float* __restrict__ pp, const int* __restrict__ rank,
     const int* __restrict__ chunk_base, const int* __restrict__ counts, const int* __restrict__ offs_pad, int T,
-    int E, int k,
+    int E, int k, int shared_rows,
     const uint4* __restrict__ hidden, int vec_per_row, int* __restrict__ perm_src, float* __restrict__ pp_perm,
     int* __restrict__ row_of, uint4* __restrict__ x_perm, uint8_t* __restrict__ x_q, uint8_t* __restrict__ x_sf) {
     pdl_wait();
@@ -394,7 +413,22 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         return;
     }
     const int64_t j = item - n_routes;
-    if (j >= int64_t(E) * kBM) return;
+    if (j >= int64_t(E) * kBM) {
+        const int t = int(j - int64_t(E) * kBM);
+        if (t >= shared_rows) return;
+        const int64_t pos = int64_t(t) - shared_rows;
+        const bool tok = t < T;
+        if (lane == 0) {
+            perm_src[pos] = tok ? t : -1;
+            pp_perm[pos] = tok ? 1.0f : 0.0f;  // the shared output gate, when there is one, overwrites it
+        }
+        uint4* dst = x_perm + pos * vec_per_row;
+        if (tok)
+            for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(hidden + int64_t(t) * vec_per_row + v);
+        else
+            for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        return;
+    }
     const int e = int(j / kBM);
     const int r = int(j % kBM);
     const int cnt = __ldg(counts + e);
@@ -477,24 +511,25 @@ cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T
 }
 
 cudaError_t launch_route_scan_chunks(int* hist, int T, int E, int* counts, int* offsets, int* offs_pad,
-                                     int* mtile_expert, int* meta, cudaStream_t st) {
+                                     int* mtile_expert, int* meta, int shared_tiles, int* mtile_x, int* seg_x,
+                                     cudaStream_t st) {
     const int threads = (E + 31) / 32 * 32;
     const cudaError_t e = launch_pdl(route_scan_chunks_kernel, dim3(1), dim3(threads), 0, st, hist,
                                      (T + kRankChunk - 1) / kRankChunk, E, counts, offsets, offs_pad, mtile_expert,
-                                     meta);
+                                     meta, shared_tiles, mtile_x, seg_x);
     count_launch();
     return e;
 }
 
 
 cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* chunk_base,
-                               const int* counts, const int* offs_pad, int T, int E, int k,
+                               const int* counts, const int* offs_pad, int T, int E, int k, int shared_rows,
                                const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
                                __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st) {
-    const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
+    const int64_t items = int64_t(T) * k + int64_t(E) * kBM + shared_rows;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const cudaError_t e = launch_pdl(route_place_kernel, dim3(unsigned(blocks)), dim3(32 * kWarpsPerBlock), 0, st,
-                                     ids, pp, rank, chunk_base, counts, offs_pad, T, E, k,
+                                     ids, pp, rank, chunk_base, counts, offs_pad, T, E, k, shared_rows,
                                      reinterpret_cast<const uint4*>(hidden), H / 8, perm_src, pp_perm, row_of,
                                      reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
     count_launch();
