@@ -460,27 +460,25 @@ def run_ours(args):
     h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h_dh = torch.empty(dh.shape, dtype=dh.dtype, pin_memory=True)
     h_dp = torch.empty(dp.shape, dtype=dp.dtype, pin_memory=True)
-    d_hidden, d_grad, d_probs, d_map = (torch.empty_like(t, device=dev) for t in (h_hidden, h_grad, h_probs, h_map))
+    # two result sets, so that a step's results are not overwritten by the next
+    # step's download while the host could still be reading them
+    h_res = [(h_out, h_dh, h_dp)] + [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                                           for t in (h_out, h_dh, h_dp))]
+    pipe = layer.host_steps(T)
 
-    def e2e_step():
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        d_probs.copy_(h_probs, non_blocking=True)
-        d_map.copy_(h_map, non_blocking=True)
-        d_grad.copy_(h_grad, non_blocking=True)
-        layer.forward(d_hidden, d_probs, d_map, wv, out=out, stream=stream)
-        layer.backward(d_grad, mgv, dhidden=dh, dprobs=dp, stream=stream)
-        h_out.copy_(out, non_blocking=True)
-        h_dh.copy_(dh, non_blocking=True)
-        h_dp.copy_(dp, non_blocking=True)
+    def e2e_step(i):
+        pipe.step(h_hidden, h_probs, h_map, h_grad, wv, mgv, *h_res[i % 2])
 
-    for _ in range(3):
-        e2e_step()
     torch.cuda.synchronize()
+    for i in range(3):
+        e2e_step(i)
+    pipe.synchronize()
     e2e_steps = max(10, args.steps // 4)
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    pipe.synchronize()
     torch.cuda.synchronize()
     e2e_s = reduce_max([time.perf_counter() - t0], world, dev)[0]
     h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_grad, h_probs, h_map))

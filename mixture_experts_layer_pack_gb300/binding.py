@@ -381,6 +381,10 @@ class MoELayer:
     def device_status(self, stream=None) -> int:
         return moe_device_status(self.handle, stream)
 
+    def host_steps(self, T):
+        """A HostSteps pipeline of forward + backward steps of T tokens from host buffers."""
+        return HostSteps(self, T)
+
     def close(self):
         if getattr(self, "handle", None) is not None:
             moe_saved_destroy(self.saved)
@@ -392,3 +396,86 @@ class MoELayer:
             self.close()
         except Exception:
             pass
+
+
+class HostSteps:
+    """Forward + backward steps of a layer fed from pinned host buffers, with the
+    copies overlapped with the GPU work of the neighbouring steps.
+
+    Each step's inputs go up on an upload stream into one of two device staging
+    sets while the previous step computes; its results come down on a download
+    stream while the next step computes. Every step still uploads its own inputs
+    and downloads its own results. `step` only enqueues work and returns an event
+    that completes when that step's results are in the host buffers; the host
+    buffers of a step must stay untouched until then. Steps run in call order on
+    one compute stream, so main_grad accumulates exactly as with sequential calls."""
+
+    def __init__(self, layer: "MoELayer", T: int):
+        import torch
+        self.layer = layer
+        self.T = int(T)
+        dev = layer.device
+        H, E = layer.cfg.hidden, layer.cfg.num_experts
+        self.up = torch.cuda.Stream(dev)
+        self.compute = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+
+        def staging():
+            return {"hidden": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                    "probs": torch.empty((T, E), dtype=torch.float32, device=dev),
+                    "map": torch.empty((T, E), dtype=torch.uint8, device=dev),
+                    "grad": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                    "out": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                    "dh": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                    "dp": torch.empty((T, E), dtype=torch.float32, device=dev)}
+
+        self.sets = [staging(), staging()]
+        self.uploaded = [torch.cuda.Event(), torch.cuda.Event()]    # the set's inputs are on the device
+        self.computed = [torch.cuda.Event(), torch.cuda.Event()]    # its step ran: inputs free, results ready
+        self.downloaded = [torch.cuda.Event(), torch.cuda.Event()]  # its results are in host memory
+        self.used = [False, False]
+        self.n = 0
+
+    def step(self, hidden, probs, routing_map, grad_out, weights: moe_weights, main_grads: moe_main_grads,
+             out, dhidden, dprobs):
+        """Enqueues one step: host (pinned) hidden[T,H] bf16, probs[T,E] f32, routing_map[T,E]
+        (bool or uint8), grad_out[T,H] bf16 in; host out[T,H], dhidden[T,H] bf16 and
+        dprobs[T,E] f32 receive the results. Returns the step's completion event."""
+        import torch
+        for t in (hidden, probs, routing_map, grad_out, out, dhidden, dprobs):
+            if t.is_cuda or not t.is_pinned():
+                raise ValueError("HostSteps.step takes pinned host tensors")
+        if hidden.shape[0] != self.T:
+            raise ValueError("token count differs from the pipeline's")
+        s = self.n % 2
+        self.n += 1
+        b = self.sets[s]
+        if self.used[s]:
+            self.up.wait_event(self.computed[s])        # the set's previous step has read its inputs
+        with torch.cuda.stream(self.up):
+            b["hidden"].copy_(hidden, non_blocking=True)
+            b["probs"].copy_(probs, non_blocking=True)
+            b["map"].copy_(routing_map.view(torch.uint8), non_blocking=True)
+            b["grad"].copy_(grad_out, non_blocking=True)
+            self.uploaded[s].record(self.up)
+        self.compute.wait_event(self.uploaded[s])
+        if self.used[s]:
+            self.compute.wait_event(self.downloaded[s])  # the set's previous results have left
+        self.layer.forward(b["hidden"], b["probs"], b["map"], weights, out=b["out"], stream=self.compute)
+        self.layer.backward(b["grad"], main_grads, dhidden=b["dh"], dprobs=b["dp"], stream=self.compute)
+        self.computed[s].record(self.compute)
+        self.down.wait_event(self.computed[s])
+        with torch.cuda.stream(self.down):
+            out.copy_(b["out"], non_blocking=True)
+            dhidden.copy_(b["dh"], non_blocking=True)
+            dprobs.copy_(b["dp"], non_blocking=True)
+            self.downloaded[s].record(self.down)
+        self.used[s] = True
+        return self.downloaded[s]
+
+    def synchronize(self):
+        """Waits for every enqueued step (results in host memory)."""
+        self.up.synchronize()
+        self.compute.synchronize()
+        self.down.synchronize()
+
