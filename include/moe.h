@@ -186,11 +186,25 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
                        const uint8_t* routing_map, const moe_weights* w, void* out,
                        moe_saved* saved, void* stream);
 
+/* The same forward fed by the router's top-k output instead of the dense map
+ * (PR #6572, Possible feature work: consuming the router's output directly).
+ *   topk_ids[T,k] int32: expert ids, -1 for an empty slot; topk_probs[T,k]
+ *   fp32: the matching probs (ignored where the id is -1). Device memory, any
+ *   alignment. Slots keep this order (the combine sums them in it). A row with
+ *   an id outside [-1, E) or the same id twice is MOE_ERR_ROUTING (device
+ *   status) and contributes nothing, like a map row with more than k routes.
+ * The matching moe_backward writes dprobs as [T,k] fp32 in the same slot
+ * order (0 for an empty slot) instead of the dense [T,E]. */
+moe_status moe_forward_topk(moe_handle* h, int64_t T, const void* hidden, const int32_t* topk_ids,
+                            const float* topk_probs, const moe_weights* w, void* out,
+                            moe_saved* saved, void* stream);
+
 /* Backward of L = sum(grad_out * out) for the forward recorded in `saved`
  * (runtime page, _MoKAutograd.backward; PR #6572, Design > Authoritative
  * routing maps (backward adapter) and > Gradient accumulation).
  *   grad_out[T,H] bf16 -> dhidden[T,H] bf16, dprobs[T,E] fp32 (dense: every
- *   element written; 0 where the map is false), and main_grad += dW for all
+ *   element written; 0 where the map is false; after moe_forward_topk, [T,k]
+ *   per slot), and main_grad += dW for all
  *   six buffers, one add per element in mg->dtype (deterministic). Experts that
  *   received no tokens keep their main_grad bitwise. `saved` is not consumed.
  *   With a shared output gate, also main_grad_gate[h] += sum_t dz[t] hidden[t,h]

@@ -83,6 +83,8 @@ def load(build_if_missing: bool = True):
         L.moe_saved_destroy.restype = None
         L.moe_forward.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, P(moe_weights), c_void_p,
                                   c_void_p, c_void_p]
+        L.moe_forward_topk.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, P(moe_weights), c_void_p,
+                                       c_void_p, c_void_p]
         L.moe_backward.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, P(moe_main_grads), c_void_p]
         L.moe_export_routing.argtypes = [c_void_p, c_void_p] + [c_void_p] * 6 + [c_void_p]
         L.moe_device_status.argtypes = [c_void_p, c_void_p]
@@ -169,6 +171,11 @@ def moe_saved_destroy(s):
 def moe_forward(h, T, hidden, probs, routing_map, weights: moe_weights, out, saved, stream=None):
     _check(load().moe_forward(h, int(T), _ptr(hidden), _ptr(probs), _ptr(routing_map), ctypes.byref(weights),
                               _ptr(out), saved, _stream_ptr(stream)), "moe_forward")
+
+
+def moe_forward_topk(h, T, hidden, topk_ids, topk_probs, weights: moe_weights, out, saved, stream=None):
+    _check(load().moe_forward_topk(h, int(T), _ptr(hidden), _ptr(topk_ids), _ptr(topk_probs), ctypes.byref(weights),
+                                   _ptr(out), saved, _stream_ptr(stream)), "moe_forward_topk")
 
 
 def moe_backward(h, grad_out, saved, dhidden, dprobs, main_grads: moe_main_grads, stream=None):
@@ -366,6 +373,16 @@ class MoELayer:
         if out is None:
             out = torch.empty_like(hidden)
         moe_forward(self.handle, hidden.shape[0], hidden, probs, routing_map, weights, out, self.saved, stream)
+        self._topk = False
+        return out
+
+    def forward_topk(self, hidden, topk_ids, topk_probs, weights: moe_weights, out=None, stream=None):
+        """Forward from the router's top-k output: int32 ids [T,k] (-1 = empty slot), fp32 probs [T,k]."""
+        import torch
+        if out is None:
+            out = torch.empty_like(hidden)
+        moe_forward_topk(self.handle, hidden.shape[0], hidden, topk_ids, topk_probs, weights, out, self.saved, stream)
+        self._topk = True
         return out
 
     def backward(self, grad_out, main_grads: moe_main_grads, dhidden=None, dprobs=None, stream=None):
@@ -373,8 +390,9 @@ class MoELayer:
         T = grad_out.shape[0]
         if dhidden is None:
             dhidden = torch.empty_like(grad_out)
-        if dprobs is None:
-            dprobs = torch.empty((T, self.cfg.num_experts), dtype=torch.float32, device=grad_out.device)
+        if dprobs is None:  # [T,k] per slot after forward_topk, else dense [T,E]
+            n = self.cfg.topk if getattr(self, "_topk", False) else self.cfg.num_experts
+            dprobs = torch.empty((T, n), dtype=torch.float32, device=grad_out.device)
         moe_backward(self.handle, grad_out, self.saved, dhidden, dprobs, main_grads, stream)
         return dhidden, dprobs
 

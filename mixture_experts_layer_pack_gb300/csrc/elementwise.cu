@@ -99,13 +99,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 
 // dhidden[t] = dx_shared[t] (+ dz[t] w, the shared output gate's term) + sum
 // over valid slots of dx_perm[row_of[t,s]];
-// dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map
+// dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map; with
+// slot_dprobs, dprobs[t,s] of slot s instead (0 for an empty slot)
 __global__ void __launch_bounds__(256) unpermute_kernel(const uint4* __restrict__ dxs, const uint4* __restrict__ dxp,
                                                         const int* __restrict__ row_of, const int* __restrict__ ids,
                                                         const float* __restrict__ partial, int n_part, int T,
                                                         int vec_per_row, int k, int E, const float* __restrict__ dz,
                                                         const uint4* __restrict__ gate_w,
-                                                        uint4* __restrict__ dhidden, float* __restrict__ dprobs) {
+                                                        uint4* __restrict__ dhidden, float* __restrict__ dprobs,
+                                                        int slot_dprobs) {
     pdl_wait();
     pdl_trigger();
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -131,6 +133,18 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint4* __restrict_
             if (r >= 0) add_bf16x8(acc, dxp + int64_t(r) * vec_per_row + v);
         }
         dhidden[i] = pack_bf16x8(acc);
+    }
+    if (slot_dprobs) {
+        for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < int64_t(T) * k; i += stride) {
+            const int r = __ldg(row_of + i);
+            float val = 0.0f;
+            if (r >= 0) {
+                const float* p = partial + int64_t(r) * n_part;
+                for (int j = 0; j < n_part; ++j) val += p[j];
+            }
+            dprobs[i] = val;
+        }
+        return;
     }
     const int64_t total_p = int64_t(T) * E;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total_p; i += stride) {
@@ -181,14 +195,14 @@ cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __n
 
 cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,
                              const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
-                             const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, int num_sms,
-                             cudaStream_t st) {
+                             const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, bool slot_dprobs,
+                             int num_sms, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
     const cudaError_t e = launch_pdl(unpermute_kernel, dim3(grid), dim3(256), 0, st,
                                      reinterpret_cast<const uint4*>(dxs), reinterpret_cast<const uint4*>(dxp), row_of,
                                      ids, partial, n_part, T, H / 8, k, E, dz, reinterpret_cast<const uint4*>(gate_w),
-                                     reinterpret_cast<uint4*>(dhidden), dprobs);
+                                     reinterpret_cast<uint4*>(dhidden), dprobs, slot_dprobs ? 1 : 0);
     count_launch();
     return e;
 }

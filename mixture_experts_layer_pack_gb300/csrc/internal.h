@@ -104,8 +104,10 @@ constexpr int kMxBK = 128;
 // routing
 constexpr int kRankChunk = 128;  // tokens per block of the fused pack/rank kernel
 int route_rank_max_tokens();
-cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
-                                   int* row_of, int* rank, int* hist, int* status, cudaStream_t st);
+// the dense routing map + probs, or (topk_ids set) the router's top-k ids + probs
+cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, const int* topk_ids,
+                                   const float* topk_probs, int T, int E, int k, int* ids, float* pp, int* row_of,
+                                   int* rank, int* hist, int* status, cudaStream_t st);
 // mtile_x (optional): tile experts of the shared-first grouped GEMM (shared_tiles
 // tiles of group 0, then routed expert e as group e + 1), seg_x its E + 2 row
 // offsets, meta[3] its tile count and meta[4] its row count
@@ -138,8 +140,8 @@ cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __n
                            const float* pp, int T, int H, int k, __nv_bfloat16* out, int num_sms, cudaStream_t st);
 cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,
                              const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
-                             const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, int num_sms,
-                             cudaStream_t st);
+                             const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, bool slot_dprobs,
+                             int num_sms, cudaStream_t st);
 
 // shared-expert output gate
 constexpr int kGateChunk = 128;  // tokens per partial sum of the gate weight's gradient

@@ -468,6 +468,7 @@ struct moe_saved {
     moe_weights w;
     bool valid;
     bool gated;  // the forward had a shared output gate
+    bool topk;   // the forward took top-k ids + probs: dprobs per slot [T,k]
 };
 
 extern "C" {
@@ -570,16 +571,20 @@ void moe_saved_destroy(moe_saved* s) { delete s; }
         if (st_ != MOE_OK) return st_;                   \
     } while (0)
 
-moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float* probs, const uint8_t* routing_map,
-                       const moe_weights* w, void* out, moe_saved* saved, void* stream) {
+// the forward from the dense routing map + probs, or (topk_ids set) from the
+// router's top-k ids + probs
+static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, const float* probs,
+                               const uint8_t* routing_map, const int32_t* topk_ids, const float* topk_probs,
+                               const moe_weights* w, void* out, moe_saved* saved, void* stream) {
     if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
     const Shape& s = h->s;
     if (T < 0 || T > s.Tmax) return MOE_ERR_INVALID_ARG;
     if (w && s.mx && (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs))
         return MOE_ERR_UNSUPPORTED;  // per-expert tables are for BF16 routed weights
     if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!hidden || !probs || !routing_map || !out || !aligned16(hidden) || !aligned16(out)))
-        return MOE_ERR_INVALID_ARG;
+    const bool topk = topk_ids != nullptr;
+    if (T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (topk ? !topk_probs : (!probs || !routing_map))) return MOE_ERR_INVALID_ARG;
     const bool mx = s.mx;
     if (mx && !h->weights_prepared) return MOE_ERR_STATE;
     const bool gated = w->shared_output_gate != nullptr;
@@ -592,6 +597,7 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     saved->w = *w;
     saved->valid = true;
     saved->gated = gated;
+    saved->topk = topk;
     if (T == 0) return MOE_OK;
 
     const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
@@ -602,8 +608,8 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     // dispatch: route-pack, per-expert ranks, segment scan, placement + row gather
     // (with BF16 routed weights also the shared expert's rows, as group 0 of the GEMMs)
     { Timed tm_(h, MOE_K_ROUTE_PACK, st);
-    MOE_CU(launch_route_pack_rank(routing_map, probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.rank, ws.hist, ws.status,
-                                  st)); }
+    MOE_CU(launch_route_pack_rank(routing_map, probs, topk_ids, topk_probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.rank,
+                                  ws.hist, ws.status, st)); }
     { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
     MOE_CU(launch_route_scan_chunks(ws.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta,
                                     v.R0 / kBM, mx ? nullptr : b.mtile_x, b.seg_x, st)); }
@@ -748,6 +754,20 @@ moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float
     MOE_CU(launch_combine(ws.yx_all, gated ? b.pp_all : nullptr, v.yx, b.row_of, b.pp, Ti, H, k,
                           static_cast<__nv_bfloat16*>(out), h->sms, st));
     return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle* h, int64_t T, const void* hidden, const float* probs, const uint8_t* routing_map,
+                       const moe_weights* w, void* out, moe_saved* saved, void* stream) {
+    return forward_impl(h, T, hidden, probs, routing_map, nullptr, nullptr, w, out, saved, stream);
+}
+
+moe_status moe_forward_topk(moe_handle* h, int64_t T, const void* hidden, const int32_t* topk_ids,
+                            const float* topk_probs, const moe_weights* w, void* out, moe_saved* saved,
+                            void* stream) {
+    if (T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
+    static const int32_t kNone = -1;  // any non-null marker selects the top-k input when T == 0
+    return forward_impl(h, T, hidden, nullptr, nullptr, T > 0 ? topk_ids : &kNone, topk_probs, w, out, saved,
+                        stream);
 }
 
 moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved, void* dhidden, float* dprobs,
@@ -1035,7 +1055,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     MOE_CU(launch_unpermute(ws.yx_all, v.yx, b.row_of, b.ids, v.partial, s.n_part, Ti, H, k, E,
                             gated ? ws.dz : nullptr,
                             gated ? static_cast<const __nv_bfloat16*>(w->shared_output_gate) : nullptr,
-                            static_cast<__nv_bfloat16*>(dhidden), dprobs, h->sms, st));
+                            static_cast<__nv_bfloat16*>(dhidden), dprobs, saved->topk, h->sms, st));
     return MOE_OK;
 }
 

@@ -161,12 +161,18 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(const uint8_t*
 // prefix over the block's warps is added to every rank, and the block's totals
 // go to hist[c][e]; a later scan over blocks completes the stable (expert,
 // token) order.
+// With topk_ids set (the router's top-k output instead of the dense map), the
+// map rows are built in shared memory from topk_ids[T,k] (-1 = no route); a row
+// with an id outside [-1, E) or a repeated id flags the status and is dropped;
+// the slots keep the caller's order, with probs from topk_probs[T,k].
 __global__ void __launch_bounds__(kRankChunk) route_pack_rank_kernel(const uint8_t* __restrict__ map,
                                                                      const float* __restrict__ probs, int T, int E,
                                                                      int k, int* __restrict__ ids,
                                                                      float* __restrict__ pp, int* __restrict__ row_of,
                                                                      int* __restrict__ rank, int* __restrict__ hist,
-                                                                     int words_aligned, int* status) {
+                                                                     int words_aligned, int* status,
+                                                                     const int* __restrict__ topk_ids,
+                                                                     const float* __restrict__ topk_probs) {
     pdl_wait();
     pdl_trigger();
     constexpr int W = kRankChunk / 32;
@@ -184,8 +190,27 @@ __global__ void __launch_bounds__(kRankChunk) route_pack_rank_kernel(const uint8
     const bool in = threadIdx.x < nt;
 
     // the chunk's rows: bytes [t0*E, (t0+nt)*E) of the map
-    const uint8_t* src = map + int64_t(t0) * E;
-    if (words_aligned == 4) {  // E % 16 == 0 and a 16-byte aligned map: 16-byte loads, 8 in flight
+    const uint8_t* src = topk_ids ? nullptr : map + int64_t(t0) * E;
+    bool bad_ids = false;  // top-k input: an id out of range or repeated in this thread's row
+    if (topk_ids) {
+        for (int i = threadIdx.x; i < kRankChunk * RW; i += blockDim.x) s_rows[i] = 0u;
+        __syncthreads();
+        if (in) {
+            uint8_t* row8 = reinterpret_cast<uint8_t*>(s_rows + threadIdx.x * RW);
+            int n_ids = 0, n_set = 0;
+            for (int s = 0; s < k; ++s) {
+                const int e = __ldg(topk_ids + int64_t(t) * k + s);
+                if (e < -1 || e >= E) {
+                    bad_ids = true;
+                } else if (e >= 0) {
+                    ++n_ids;
+                    n_set += row8[e] == 0 ? 1 : 0;
+                    row8[e] = 1;
+                }
+            }
+            bad_ids = bad_ids || n_set != n_ids;
+        }
+    } else if (words_aligned == 4) {  // E % 16 == 0 and a 16-byte aligned map: 16-byte loads, 8 in flight
         const int eq = E / 16;
         const int nq = nt * eq;
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
@@ -238,7 +263,7 @@ __global__ void __launch_bounds__(kRankChunk) route_pack_rank_kernel(const uint8
             cnt += ((v & 0xffu) != 0) + ((v & 0xff00u) != 0) + ((v & 0xff0000u) != 0) + ((v & 0xff000000u) != 0);
         }
     bool valid = in;
-    if (in && cnt > k) {  // more routes than slots: flag it, drop the row's routes
+    if (in && (cnt > k || bad_ids)) {  // more routes than slots, or bad ids: flag it, drop the row's routes
         atomicOr(status, kStatusRouting);
         valid = false;
     }
@@ -279,6 +304,23 @@ __global__ void __launch_bounds__(kRankChunk) route_pack_rank_kernel(const uint8
     int* ids_t = ids + int64_t(t) * k;
     float* pp_t = pp + int64_t(t) * k;
     int* rk_t = rank + int64_t(t) * k;
+    if (topk_ids) {  // the caller's slot order: find each slot's expert among the ranked ones
+        for (int s = 0; s < k; ++s) {
+            const int e = valid ? __ldg(topk_ids + int64_t(t) * k + s) : -1;
+            int j = 0;
+            while (j < sl && my_e[j] != e) ++j;
+            if (e >= 0 && j < sl) {
+                ids_t[s] = e;
+                pp_t[s] = __ldg(topk_probs + int64_t(t) * k + s);
+                rk_t[s] = my_r[j] + s_cnt[w * E + e];
+            } else {
+                ids_t[s] = -1;
+                pp_t[s] = 0.0f;
+                row_of[int64_t(t) * k + s] = -1;
+            }
+        }
+        return;
+    }
     for (int s0 = 0; s0 < k; s0 += 8) {  // the probs of eight slots in flight at a time
         float pv[8];
 #pragma unroll
@@ -489,8 +531,9 @@ cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T, int E, int k, int* ids, float* pp,
-                                   int* row_of, int* rank, int* hist, int* status, cudaStream_t st) {
+cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, const int* topk_ids,
+                                   const float* topk_probs, int T, int E, int k, int* ids, float* pp, int* row_of,
+                                   int* rank, int* hist, int* status, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const size_t smem = pack_rank_smem(E, k);
     static size_t smem_set = 48 * 1024;
@@ -505,7 +548,7 @@ cudaError_t launch_route_pack_rank(const uint8_t* map, const float* probs, int T
     const int words = (E % 16 == 0 && (mp & 15) == 0) ? 4 : ((E % 4 == 0 && (mp & 3) == 0) ? 1 : 0);
     const cudaError_t e = launch_pdl(route_pack_rank_kernel, dim3((T + kRankChunk - 1) / kRankChunk),
                                      dim3(kRankChunk), smem, st, map, probs, T, E, k, ids, pp, row_of, rank, hist,
-                                     words, status);
+                                     words, status, topk_ids, topk_probs);
     count_launch();
     return e;
 }
