@@ -71,7 +71,18 @@ typedef struct {
     int64_t inter;        /* I, intermediate size of routed and shared experts */
     int32_t routed_wtype; /* moe_wtype of the routed weights; shared weights are always bf16 */
     float swiglu_limit;   /* 0: no clamp; L > 0: SwiGLU input clamp (above) */
+    int32_t recompute_dispatch; /* 0 or 1; see below */
 } moe_config;
+/* recompute_dispatch = 1 (redispatch in backward: PR #8210 review thread on
+ * CUDA graphs, per-layer replay needs the saved schedule and activations to
+ * survive pending microbatches, which a redispatch in backward provides): a
+ * moe_saved then keeps only the routing (a few bytes per route and per row);
+ * the dispatched rows and the SwiGLU intermediates live in the handle's
+ * workspace, and moe_backward first runs the row placement, the shared output
+ * gate and the gate/up GEMMs again from the saved routing, hidden and weights.
+ * Results are bitwise those of recompute_dispatch = 0, for any interleaving of
+ * forwards and backwards over several moe_saved states of one handle on one
+ * stream. Costs one more gate/up GEMM per backward. */
 
 /* One weight argument in the external ABI order (runtime page,
  * _MoKWeightArguments: shared_gate, shared_up, shared_down, routed_gate,

@@ -23,7 +23,8 @@ WEIGHT_NAMES = ("shared_gate", "shared_up", "shared_down", "routed_gate", "route
 
 class moe_config(ctypes.Structure):
     _fields_ = [("max_tokens", c_int64), ("hidden", c_int64), ("num_experts", c_int64), ("topk", c_int64),
-                ("inter", c_int64), ("routed_wtype", c_int32), ("swiglu_limit", c_float)]
+                ("inter", c_int64), ("routed_wtype", c_int32), ("swiglu_limit", c_float),
+                ("recompute_dispatch", c_int32)]
 
 
 class moe_wview(ctypes.Structure):
@@ -353,9 +354,10 @@ class MoELayer:
     """Holds a handle, its workspace and one saved-state block (all torch device memory)."""
 
     def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16,
-                 swiglu_limit=0.0):
+                 swiglu_limit=0.0, recompute_dispatch=False):
         import torch
-        self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, float(swiglu_limit))
+        self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, float(swiglu_limit),
+                              int(bool(recompute_dispatch)))
         self.device = torch.device(device)
         ws = moe_workspace_size(self.cfg)
         sv = moe_saved_size(self.cfg)

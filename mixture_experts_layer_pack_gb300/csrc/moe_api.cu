@@ -42,6 +42,7 @@ struct Shape {
     int n_part;       // dprob partials per row (= N tiles of the dgrad-down GEMM x epilogue halves)
     int n_part_s;     // the same for the shared expert's (always BF16) dgrad-down GEMM
     bool mx;          // routed weights MXFP8: block-scaled fprop and dgrad GEMMs
+    bool recompute;   // recompute_dispatch: the backward redoes placement and gate/up
     float limit;      // swiglu_limit (0: none)
 };
 
@@ -63,6 +64,8 @@ moe_status check_config(const moe_config* c, Shape* s) {
     if (c->max_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->topk <= 0 || c->inter <= 0)
         return MOE_ERR_INVALID_ARG;
     if (!(c->swiglu_limit >= 0.0f) || !std::isfinite(c->swiglu_limit)) return MOE_ERR_INVALID_ARG;
+    if (c->recompute_dispatch != 0 && c->recompute_dispatch != 1) return MOE_ERR_INVALID_ARG;
+    s->recompute = c->recompute_dispatch != 0;
     s->limit = c->swiglu_limit;
     if (c->routed_wtype != MOE_W_BF16 && c->routed_wtype != MOE_W_MXFP8) return MOE_ERR_UNSUPPORTED;
     s->mx = c->routed_wtype == MOE_W_MXFP8;
@@ -95,8 +98,6 @@ moe_status check_config(const moe_config* c, Shape* s) {
 // rows after T), and the routed segments from row R0 on; srows + rows rows each.
 struct Workspace {
     int* status;
-    int* rank;  // rank of each route inside its expert
-    int* hist;  // per 128-token chunk and expert: route count, then the chunk's rank offset
     int* tile_counters;  // one per weight-gradient launch of a backward (dynamic tile scheduling)
     __nv_bfloat16 *go_all, *dgdu_all, *ap_all;  // grad_out rows, [dg|du], prob (or gate) * a
     __nv_bfloat16* yx_all;  // forward: y; backward: dx
@@ -107,6 +108,10 @@ struct Workspace {
     float *dz, *gpart;
     // per-expert TMA descriptors of the tables (kTables x E)
     CUtensorMap* tabs;
+    // recompute_dispatch: the GEMM input rows, a and [g|u] (and their MXFP8 copies)
+    // live here, shared by every saved state of the handle, instead of in each
+    __nv_bfloat16 *x_all, *a_all, *gu_all;
+    uint8_t *x_q, *x_sf, *a_q, *a_sf;
     // MXFP8 only: quantised backward operands and the swizzled weight scales
     uint8_t *go_q, *go_sf, *dgdu_q, *dgdu_sf;
     uint8_t *sf_fc1_row, *sf_down_row, *sf_down_col, *sf_fc1_col;
@@ -114,6 +119,8 @@ struct Workspace {
 
 struct SavedBufs {
     int *ids, *row_of, *counts, *offsets, *offs_pad, *mtile_expert;  // routed segments (relative to row R0)
+    int* rank;  // rank of each route inside its expert
+    int* hist;  // per 128-token chunk and expert: route count, then the chunk's rank offset
     int* meta;  // [0..2] routed tiles, routes, rows; [3], [4] tiles and rows of the shared-first GEMMs
     int *mtile_x, *seg_x;  // shared-first grouped GEMMs: group of each 128-row tile, E + 2 group row offsets
     int* perm_src_all;     // source token of each row (-1: zero row)
@@ -138,8 +145,6 @@ size_t sf_atoms_bytes(int64_t rows, int64_t K) { return size_t(rows / 128) * siz
 size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     Carver c{base};
     w->status = c.take<int>(64);
-    w->rank = c.take<int>(size_t(s.Tmax) * s.k);
-    w->hist = c.take<int>(size_t((s.Tmax + kRankChunk - 1) / kRankChunk) * s.E);
     w->tile_counters = c.take<int>(4);
     const size_t ra = size_t(s.srows + s.rows);
     w->go_all = c.take<__nv_bfloat16>(ra * s.H);
@@ -151,6 +156,19 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->dz = c.take<float>(size_t(s.Tmax));
     w->gpart = c.take<float>(size_t((s.Tmax + kGateChunk - 1) / kGateChunk) * s.H);
     w->tabs = c.take<CUtensorMap>(size_t(kTables) * s.E);
+    w->x_all = w->a_all = w->gu_all = nullptr;
+    w->x_q = w->x_sf = w->a_q = w->a_sf = nullptr;
+    if (s.recompute) {
+        w->x_all = c.take<__nv_bfloat16>(ra * s.H);
+        w->a_all = c.take<__nv_bfloat16>(ra * s.I);
+        w->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
+        if (s.mx) {
+            w->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
+            w->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
+            w->a_q = c.take<uint8_t>(size_t(s.rows) * s.I);
+            w->a_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.I));
+        }
+    }
     if (s.mx) {
         w->go_q = c.take<uint8_t>(size_t(s.rows) * s.H);
         w->go_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -173,6 +191,8 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->ids = c.take<int>(tk);
     b->pp = c.take<float>(tk);
     b->row_of = c.take<int>(tk);
+    b->rank = c.take<int>(tk);
+    b->hist = c.take<int>(size_t((s.Tmax + kRankChunk - 1) / kRankChunk) * s.E);
     b->counts = c.take<int>(s.E);
     b->offsets = c.take<int>(s.E + 1);
     b->offs_pad = c.take<int>(s.E + 1);
@@ -183,16 +203,18 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->seg_x = c.take<int>(s.E + 2);
     b->perm_src_all = c.take<int>(ra);
     b->pp_all = c.take<float>(ra);
-    b->x_all = c.take<__nv_bfloat16>(ra * s.H);
-    b->a_all = c.take<__nv_bfloat16>(ra * s.I);
-    b->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
-    if (s.mx) {
-        b->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
-        b->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
-        b->a_q = c.take<uint8_t>(size_t(s.rows) * s.I);
-        b->a_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.I));
-    } else {
-        b->x_q = b->x_sf = b->a_q = b->a_sf = nullptr;
+    b->x_all = b->a_all = b->gu_all = nullptr;  // recompute_dispatch: the workspace's (moe_saved_create)
+    b->x_q = b->x_sf = b->a_q = b->a_sf = nullptr;
+    if (!s.recompute) {
+        b->x_all = c.take<__nv_bfloat16>(ra * s.H);
+        b->a_all = c.take<__nv_bfloat16>(ra * s.I);
+        b->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
+        if (s.mx) {
+            b->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
+            b->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
+            b->a_q = c.take<uint8_t>(size_t(s.rows) * s.I);
+            b->a_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.I));
+        }
     }
     return align_up(c.off, kAlign);
 }
@@ -554,6 +576,15 @@ moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved
     std::memset(sv, 0, sizeof(*sv));
     sv->h = h;
     carve_saved(h->s, static_cast<uint8_t*>(memory), &sv->b);
+    if (h->s.recompute) {
+        sv->b.x_all = h->ws.x_all;
+        sv->b.a_all = h->ws.a_all;
+        sv->b.gu_all = h->ws.gu_all;
+        sv->b.x_q = h->ws.x_q;
+        sv->b.x_sf = h->ws.x_sf;
+        sv->b.a_q = h->ws.a_q;
+        sv->b.a_sf = h->ws.a_sf;
+    }
     *out = sv;
     return MOE_OK;
 }
@@ -571,53 +602,33 @@ void moe_saved_destroy(moe_saved* s) { delete s; }
         if (st_ != MOE_OK) return st_;                   \
     } while (0)
 
-// the forward from the dense routing map + probs, or (topk_ids set) from the
-// router's top-k ids + probs
-static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, const float* probs,
-                               const uint8_t* routing_map, const int32_t* topk_ids, const float* topk_probs,
-                               const moe_weights* w, void* out, moe_saved* saved, void* stream) {
-    if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
+// Row placement (the routed rows; with BF16 routed weights also the shared
+// expert's rows), the shared output gate's values, and the gate/up GEMMs with
+// the SwiGLU epilogue: the part of the forward that a backward runs again under
+// recompute_dispatch, from the saved routing, hidden and weights.
+static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t st) {
     const Shape& s = h->s;
-    if (T < 0 || T > s.Tmax) return MOE_ERR_INVALID_ARG;
-    if (w && s.mx && (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs))
-        return MOE_ERR_UNSUPPORTED;  // per-expert tables are for BF16 routed weights
-    if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
-    const bool topk = topk_ids != nullptr;
-    if (T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (topk ? !topk_probs : (!probs || !routing_map))) return MOE_ERR_INVALID_ARG;
-    const bool mx = s.mx;
-    if (mx && !h->weights_prepared) return MOE_ERR_STATE;
-    const bool gated = w->shared_output_gate != nullptr;
-    if (gated && !aligned16(w->shared_output_gate)) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     const SavedBufs& b = saved->b;
     const Workspace& ws = h->ws;
-    saved->T = T;
-    saved->hidden = hidden;
-    saved->w = *w;
-    saved->valid = true;
-    saved->gated = gated;
-    saved->topk = topk;
-    if (T == 0) return MOE_OK;
-
+    const moe_weights* w = &saved->w;
+    const void* hidden = saved->hidden;
+    const bool mx = s.mx;
+    const int64_t T = saved->T;
     const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
     const int rows = int(s.rows);
     const Views v = views_of(s, b, ws, T);
-    const int rows_all = v.R0 + rows;  // rows of the shared-first grouped GEMMs (BF16 routed weights)
-
-    // dispatch: route-pack, per-expert ranks, segment scan, placement + row gather
-    // (with BF16 routed weights also the shared expert's rows, as group 0 of the GEMMs)
-    { Timed tm_(h, MOE_K_ROUTE_PACK, st);
-    MOE_CU(launch_route_pack_rank(routing_map, probs, topk_ids, topk_probs, Ti, E, k, b.ids, b.pp, b.row_of, ws.rank,
-                                  ws.hist, ws.status, st)); }
-    { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
-    MOE_CU(launch_route_scan_chunks(ws.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta,
-                                    v.R0 / kBM, mx ? nullptr : b.mtile_x, b.seg_x, st)); }
+    const int rows_all = v.R0 + rows;
     { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
-    MOE_CU(launch_route_place(b.ids, b.pp, ws.rank, ws.hist, b.counts, b.offs_pad, Ti, E, k, mx ? 0 : v.R0,
+    MOE_CU(launch_route_place(b.ids, b.pp, b.rank, b.hist, b.counts, b.offs_pad, Ti, E, k, mx ? 0 : v.R0,
                               static_cast<const __nv_bfloat16*>(hidden), H, v.perm_src, v.pp_perm, b.row_of, v.x_perm,
                               mx ? b.x_q : nullptr, mx ? b.x_sf : nullptr, st)); }
 
+    // shared output gate: gate[t] = sigmoid(hidden[t] . w), the shared rows' scale
+    if (saved->gated) {
+        Timed tm_(h, MOE_K_SHARED_GATE_FWD, st);
+        MOE_CU(launch_gate_forward(static_cast<const __nv_bfloat16*>(hidden),
+                                   static_cast<const __nv_bfloat16*>(w->shared_output_gate), Ti, H, b.pp_all, st));
+    }
     GemmMaps m{};
     // gate/up + SwiGLU
     if (mx) {
@@ -688,6 +699,53 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         Timed tm_(h, MOE_K_FWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
+    return MOE_OK;
+}
+
+// the forward from the dense routing map + probs, or (topk_ids set) from the
+// router's top-k ids + probs
+static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, const float* probs,
+                               const uint8_t* routing_map, const int32_t* topk_ids, const float* topk_probs,
+                               const moe_weights* w, void* out, moe_saved* saved, void* stream) {
+    if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
+    const Shape& s = h->s;
+    if (T < 0 || T > s.Tmax) return MOE_ERR_INVALID_ARG;
+    if (w && s.mx && (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs))
+        return MOE_ERR_UNSUPPORTED;  // per-expert tables are for BF16 routed weights
+    if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
+    const bool topk = topk_ids != nullptr;
+    if (T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (topk ? !topk_probs : (!probs || !routing_map))) return MOE_ERR_INVALID_ARG;
+    const bool mx = s.mx;
+    if (mx && !h->weights_prepared) return MOE_ERR_STATE;
+    const bool gated = w->shared_output_gate != nullptr;
+    if (gated && !aligned16(w->shared_output_gate)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const SavedBufs& b = saved->b;
+    const Workspace& ws = h->ws;
+    saved->T = T;
+    saved->hidden = hidden;
+    saved->w = *w;
+    saved->valid = true;
+    saved->gated = gated;
+    saved->topk = topk;
+    if (T == 0) return MOE_OK;
+
+    const int Ti = int(T), E = int(s.E), k = int(s.k), H = int(s.H), I = int(s.I);
+    const int rows = int(s.rows);
+    const Views v = views_of(s, b, ws, T);
+    const int rows_all = v.R0 + rows;  // rows of the shared-first grouped GEMMs (BF16 routed weights)
+
+    // dispatch: route-pack, per-expert ranks, segment scan, placement + row gather
+    // (with BF16 routed weights also the shared expert's rows, as group 0 of the GEMMs)
+    { Timed tm_(h, MOE_K_ROUTE_PACK, st);
+    MOE_CU(launch_route_pack_rank(routing_map, probs, topk_ids, topk_probs, Ti, E, k, b.ids, b.pp, b.row_of, b.rank,
+                                  b.hist, ws.status, st)); }
+    { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
+    MOE_CU(launch_route_scan_chunks(b.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta,
+                                    v.R0 / kBM, mx ? nullptr : b.mtile_x, b.seg_x, st)); }
+    MOE_TRY(redispatch(h, saved, st));
+    GemmMaps m{};
     // down projection (y in bf16; the combine weights it by the route's prob or the gate)
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
@@ -727,12 +785,6 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         a.ld_outh = H;
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
-    }
-    // shared output gate: gate[t] = sigmoid(hidden[t] . w), weights the shared output in the combine
-    if (gated) {
-        Timed tm_(h, MOE_K_SHARED_GATE_FWD, st);
-        MOE_CU(launch_gate_forward(static_cast<const __nv_bfloat16*>(hidden),
-                                   static_cast<const __nv_bfloat16*>(w->shared_output_gate), Ti, H, b.pp_all, st));
     }
     if (mx) {  // shared down projection (BF16)
         GemmArgs a = base_args(ws.status, s);
@@ -795,6 +847,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
 
     // the weight-gradient launches claim their tiles from these counters
     MOE_CU(cudaMemsetAsync(ws.tile_counters, 0, 4 * sizeof(int), st));
+    // recompute_dispatch: the rows, the gate values and a, [g|u] again, into the workspace
+    if (s.recompute) MOE_TRY(redispatch(h, saved, st));
     { Timed tm_(h, MOE_K_GATHER, st);
     if (mx)
         MOE_CU(launch_gather_rows(go, v.perm_src, b.meta + 2, 0, rows, H, v.go_perm, ws.go_q, ws.go_sf, h->sms, st));

@@ -1,0 +1,78 @@
+"""recompute_dispatch: a saved state keeps only the routing, and the backward
+re-runs the row placement, the shared output gate and the gate/up GEMMs.
+
+Results are bitwise those of the default mode, also with two microbatches in
+flight on one handle (forward 1, forward 2, backward 2, backward 1), and the
+saved state is a small fraction of the default one."""
+import pytest
+import torch
+
+import mixture_experts_layer_pack_gb300 as M
+from tests.harness import Case, make_inputs, weight_views
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "bf16_gated_clamp": Case(T=300, H=256, E=8, k=2, I=128, seed=101, drop="iid", gated=True, limit=0.5),
+    "mxfp8": Case(T=260, H=256, E=6, k=2, I=128, seed=102, mx=True),
+}
+
+
+def _layer(c, recompute):
+    return M.MoELayer(c.T, c.H, c.E, c.k, c.I, routed_wtype=M.binding.MOE_W_MXFP8 if c.mx else M.binding.MOE_W_BF16,
+                      swiglu_limit=c.limit, recompute_dispatch=recompute)
+
+
+def _grads(inp):
+    mg = {n: t.clone() for n, t in inp.main_grads.items()}
+    return mg, M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"],
+                                          mg.get("shared_output_gate"))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_recompute_matches_saved_activations_bitwise(name):
+    inp = make_inputs(CASES[name])
+    c = inp.case
+    wv = weight_views(inp)
+    rmap = inp.routing_map.view(torch.uint8)
+    # two microbatches: the seeded batch and a rescaled, sign-flipped copy
+    batches = [(inp.hidden, inp.grad_out), (inp.hidden * -1.5, inp.grad_out * 0.5)]
+
+    ref = []                                   # default mode, one microbatch at a time
+    A = _layer(c, False)
+    if c.mx:
+        A.prepare_weights(wv)
+    for hid, go in batches:
+        mg, mgv = _grads(inp)
+        out = A.forward(hid, inp.probs, rmap, wv)
+        dh, dp = A.backward(go, mgv)
+        ref.append((out.clone(), dh.clone(), dp.clone(), mg))
+    torch.cuda.synchronize()
+    assert A.device_status() == 0
+
+    B = _layer(c, True)                        # recompute mode, both microbatches in flight
+    if c.mx:
+        B.prepare_weights(wv)
+    assert M.moe_saved_size(B.cfg) * 4 < M.moe_saved_size(A.cfg)
+    mem2 = torch.empty(M.moe_saved_size(B.cfg), dtype=torch.uint8, device=inp.hidden.device)
+    saved = [B.saved, M.moe_saved_create(B.handle, mem2)]
+    outs = [torch.empty_like(inp.hidden) for _ in batches]
+    for i, (hid, _) in enumerate(batches):
+        M.moe_forward(B.handle, c.T, hid, inp.probs, rmap, wv, outs[i], saved[i])
+    got = [None, None]
+    for i in (1, 0):
+        mg, mgv = _grads(inp)
+        dh = torch.empty_like(inp.hidden)
+        dp = torch.empty((c.T, c.E), dtype=torch.float32, device=inp.hidden.device)
+        M.moe_backward(B.handle, batches[i][1], saved[i], dh, dp, mgv)
+        got[i] = (outs[i], dh, dp, mg)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    for i in range(2):
+        for name_, x, y in zip(("out", "dhidden", "dprobs"), got[i][:3], ref[i][:3]):
+            assert torch.equal(x, y), (i, name_)
+        for n in ref[i][3]:
+            assert torch.equal(got[i][3][n], ref[i][3][n]), (i, n)
+    M.moe_saved_destroy(saved[1])
+    A.close()
+    B.close()
