@@ -76,3 +76,58 @@ def test_recompute_matches_saved_activations_bitwise(name):
     M.moe_saved_destroy(saved[1])
     A.close()
     B.close()
+
+
+def test_recompute_with_other_token_counts_and_topk_input():
+    """Microbatches of different sizes (the shared rows' region moves with T) and
+    the top-k input, in recompute mode: bitwise the default mode."""
+    from oracle import moe_oracle as O
+    import numpy as np
+    c = Case(T=300, H=256, E=8, k=3, I=128, seed=103, drop="iid", gated=True)
+    inp = make_inputs(c)
+    wv = weight_views(inp)
+    ids, pp, _ = O.route_pack(inp.map_np, inp.probs_np, c.k)
+    dev = inp.hidden.device
+    ids_d = torch.from_numpy(ids.astype(np.int32)).to(dev)
+    pp_d = torch.from_numpy(pp.astype(np.float32)).to(dev)
+    sizes = [300, 130]                         # R0 = 384 and 256
+
+    def run(layer, order):
+        saved = [layer.saved]
+        mems = []
+        for _ in sizes[1:]:
+            mems.append(torch.empty(M.moe_saved_size(layer.cfg), dtype=torch.uint8, device=dev))
+            saved.append(M.moe_saved_create(layer.handle, mems[-1]))
+        outs = [torch.empty_like(inp.hidden[:T]) for T in sizes]
+        res = [None] * len(sizes)
+        for i, T in enumerate(sizes):
+            M.moe_forward_topk(layer.handle, T, inp.hidden[:T], ids_d[:T], pp_d[:T], wv, outs[i], saved[i])
+            if order == "each":
+                res[i] = _bwd(layer, saved[i], T, outs[i])
+        if order == "reverse":
+            for i in reversed(range(len(sizes))):
+                res[i] = _bwd(layer, saved[i], sizes[i], outs[i])
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        for s_ in saved[1:]:
+            M.moe_saved_destroy(s_)
+        return res
+
+    def _bwd(layer, sv, T, out):
+        mg, mgv = _grads(inp)
+        dh = torch.empty_like(inp.hidden[:T])
+        dp = torch.empty((T, c.k), dtype=torch.float32, device=dev)
+        M.moe_backward(layer.handle, inp.grad_out[:T], sv, dh, dp, mgv)
+        return out, dh, dp, mg
+
+    A = _layer(c, False)
+    ref = run(A, "each")
+    B = _layer(c, True)
+    got = run(B, "reverse")
+    for i in range(len(sizes)):
+        for x, y in zip(got[i][:3], ref[i][:3]):
+            assert torch.equal(x, y), i
+        for n in ref[i][3]:
+            assert torch.equal(got[i][3][n], ref[i][3][n]), (i, n)
+    A.close()
+    B.close()

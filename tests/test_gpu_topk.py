@@ -111,3 +111,22 @@ def test_topk_rows_with_bad_ids_are_reported_and_dropped():
         assert torch.equal(top.main_grads[n], dense.main_grads[n]), n
     dt = top.dprobs.cpu().numpy()
     assert np.all(dt[[5, 9, 11]] == 0)
+
+
+def test_topk_zero_tokens():
+    c = Case(T=64, H=128, E=4, k=2, I=64, seed=94)
+    inp = make_inputs(c)
+    dev = inp.hidden.device
+    layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, device=dev)
+    wv = weight_views(inp)
+    empty_ids = torch.empty((0, c.k), dtype=torch.int32, device=dev)
+    empty_pp = torch.empty((0, c.k), dtype=torch.float32, device=dev)
+    out = layer.forward_topk(inp.hidden[:0], empty_ids, empty_pp, wv)
+    mg = {n: t.clone() for n, t in inp.main_grads.items()}
+    mgv = M.main_grads_from_combined(mg["shared_fc1"], mg["shared_fc2"], mg["routed_fc1"], mg["routed_fc2"])
+    dh, dp = layer.backward(inp.grad_out[:0], mgv)
+    torch.cuda.synchronize()
+    assert out.shape == (0, c.H) and dh.shape == (0, c.H) and dp.shape == (0, c.k)
+    for n in mg:                               # nothing accumulated
+        assert torch.equal(mg[n], inp.main_grads[n]), n
+    assert layer.device_status() == 0
