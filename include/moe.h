@@ -110,7 +110,13 @@ typedef struct {
      * expert by expert): a HOST array of E device pointers, expert e's [N,K]
      * matrix at expert_ptrs[e] with row_stride (each 16-byte aligned); data and
      * expert_stride are then ignored. NULL: the strided view above. Read during
-     * the call only. MXFP8 views do not take tables (MOE_ERR_UNSUPPORTED). */
+     * the call only. For an MXFP8 view the array holds 4*E pointers: rowwise
+     * payloads [0, E), columnwise payloads [E, 2E) (16-byte aligned, row stride
+     * row_stride bytes), rowwise scales [2E, 3E) ([N, K/32], row stride
+     * row_stride/32) and columnwise scales [3E, 4E) ([N/32, K], row stride
+     * row_stride); data, col_data, scale, col_scale and expert_stride are then
+     * ignored. moe_prepare_weights reads the scales, the forward and backward
+     * the payloads. */
     const void* const* expert_ptrs;
 } moe_wview;
 

@@ -335,6 +335,32 @@ def set_expert_tables(weights: moe_weights, gate=None, up=None, down=None) -> mo
     return weights
 
 
+def set_mx_expert_tables(weights: moe_weights, gate=None, up=None, down=None) -> moe_weights:
+    """Describes MXFP8 routed weights expert by expert: each argument a tuple of four
+    lists of E tensors -- rowwise payloads [N,K] uint8, columnwise payloads [N,K],
+    rowwise scales [N,K/32], columnwise scales [N/32,K] -- with the row strides the
+    C ABI expects (payload row stride R; scales R/32 and R). The host pointer
+    arrays are kept alive on ``weights``."""
+    keep = list(getattr(weights, "_tables", []))
+    for name, parts in (("routed_gate", gate), ("routed_up", up), ("routed_down", down)):
+        if parts is None:
+            continue
+        q, cq, sc, csc = parts
+        r = q[0].stride(0)
+        if any(t.stride(0) != r for t in list(q) + list(cq)) or any(t.stride(0) * 32 != r for t in sc) or \
+                any(t.stride(0) != r for t in csc):
+            raise ValueError("per-expert MXFP8 tensors with inconsistent row strides")
+        arr = _pointer_table(list(q) + list(cq) + list(sc) + list(csc))
+        v = getattr(weights, name)
+        v.expert_ptrs = ctypes.cast(arr, c_void_p).value
+        v.row_stride = r
+        v.data = v.col_data = v.scale = v.col_scale = None
+        v.expert_stride = 0
+        keep.append(arr)
+    weights._tables = keep
+    return weights
+
+
 def set_main_grad_tables(main_grads: moe_main_grads, gate=None, up=None, down=None) -> moe_main_grads:
     """Describes the routed main_grads expert by expert: lists of E [N,K] tensors
     (one row stride per list). The host pointer arrays are kept alive on ``main_grads``."""

@@ -888,16 +888,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int k0 = kb * kMxBK;
                     mbar_arrive_expect_tx(bar, C::STAGE_BYTES + C::SF_BYTES);
                     tma_load_2d(sa, &tmA, bar, k0, t.mt * kBM);
+                    // an expert's payload: its own descriptor (z = 0) from a per-expert table, or the 3D map at z = e
+                    const CUtensorMap* B0 = args.b0_tab ? args.b0_tab + t.e : &tmB0;
+                    const CUtensorMap* B1 = args.b1_tab ? args.b1_tab + t.e : &tmB1;
+                    const int z0 = args.b0_tab ? 0 : t.e;
+                    const int z1 = args.b1_tab ? 0 : t.e;
                     if (OP == OP_FWD_GU) {
-                        tma_load_3d(sb, &tmB0, bar, k0, t.nt * (BN / 2), t.e);
-                        tma_load_3d(sb + (BN / 2) * kMxBK, &tmB1, bar, k0, t.nt * (BN / 2), t.e);
+                        tma_load_3d(sb, B0, bar, k0, t.nt * (BN / 2), z0);
+                        tma_load_3d(sb + (BN / 2) * kMxBK, B1, bar, k0, t.nt * (BN / 2), z1);
                     } else if (OP == OP_FWD_DOWN) {
-                        tma_load_3d(sb, &tmB0, bar, k0, t.nt * BN, t.e);
+                        tma_load_3d(sb, B0, bar, k0, t.nt * BN, z0);
                     } else if (OP == OP_BWD_DOWN) {
-                        tma_load_3d(sb, &tmB0, bar, t.nt * BN, k0, t.e);
+                        tma_load_3d(sb, B0, bar, t.nt * BN, k0, z0);
                     } else {
                         const bool up = k0 >= args.gate_up_split;
-                        tma_load_3d(sb, up ? &tmB1 : &tmB0, bar, t.nt * BN, up ? k0 - args.gate_up_split : k0, t.e);
+                        tma_load_3d(sb, up ? B1 : B0, bar, t.nt * BN, up ? k0 - args.gate_up_split : k0,
+                                    up ? z1 : z0);
                     }
                     bulk_load(ssf, args.sfa + (int64_t(t.mt) * args.sfa_kgroups + kb) * 512, 512, bar);
                     bulk_load(ssf + 512,

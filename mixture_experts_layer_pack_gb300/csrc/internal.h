@@ -124,7 +124,9 @@ cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank,
                                const int* counts, const int* offs_pad, int T, int E, int k, int shared_rows,
                                const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
                                __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st);
-cudaError_t launch_swizzle_scales(int mode, const uint8_t* src0, const uint8_t* src1, int64_t src_es, int64_t src_rs,
+// tab0 / tab1: device arrays of E source pointers, expert e's scales at tab[e]
+// with row stride src_rs
+cudaError_t launch_swizzle_scales(int mode, const uint8_t* const* tab0, const uint8_t* const* tab1, int64_t src_rs,
                                   int E, int n_tiles, int k_blocks, int kb_split, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* perm_src_pad, const int* counts,
                                   const int* offsets, const int* offs_pad, const int* mtile_expert, const int* meta,

@@ -115,6 +115,9 @@ struct Workspace {
     // MXFP8 only: quantised backward operands and the swizzled weight scales
     uint8_t *go_q, *go_sf, *dgdu_q, *dgdu_sf;
     uint8_t *sf_fc1_row, *sf_down_row, *sf_down_col, *sf_fc1_col;
+    // MXFP8: per-expert source scale pointers of the swizzle (gate, up, down rowwise;
+    // down, gate, up columnwise; E each)
+    const uint8_t** sf_src;
 };
 
 struct SavedBufs {
@@ -178,9 +181,11 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
         w->sf_down_row = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(s.H, s.I));
         w->sf_down_col = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(s.I, s.H));
         w->sf_fc1_col = c.take<uint8_t>(size_t(s.E) * sf_atoms_bytes(s.H, 2 * s.I));
+        w->sf_src = c.take<const uint8_t*>(6 * size_t(s.E));
     } else {
         w->go_q = w->go_sf = w->dgdu_q = w->dgdu_sf = nullptr;
         w->sf_fc1_row = w->sf_down_row = w->sf_down_col = w->sf_fc1_col = nullptr;
+        w->sf_src = nullptr;
     }
     return align_up(c.off, kAlign);
 }
@@ -250,6 +255,7 @@ bool check_view(const moe_wview& v, int64_t N, int64_t K, bool routed) {
 // an MXFP8 view of N rows x K columns per expert: E4M3 payloads (row stride in bytes), scales
 // indexed with the payload strides (see include/moe.h)
 bool check_mx_view(const moe_wview& v, int64_t N, int64_t K) {
+    if (v.expert_ptrs) return v.row_stride >= K && v.row_stride % 32 == 0;  // pointers checked as they are used
     if (!v.data || !v.col_data || !v.scale || !v.col_scale) return false;
     if (!aligned16(v.data) || !aligned16(v.col_data)) return false;
     if (v.row_stride < K || v.row_stride % 32 || v.expert_stride < N * v.row_stride || v.expert_stride % 32)
@@ -368,6 +374,7 @@ struct moe_handle {
         std::vector<CUtensorMap> maps;
     };
     Table tables[kTables];
+    std::vector<const uint8_t*> sf_src_host;  // MXFP8: the scale pointers last uploaded to ws.sf_src
     // per-kernel timing (moe_profile_enable, moe_profile_select)
     bool profiling = false;
     uint32_t profile_mask = ~0u;  // kernel classes bracketed by events
@@ -435,6 +442,26 @@ moe_status routed_map(moe_handle* h, int id, const moe_wview& v, int64_t rows, i
             moe_wview one = v;
             one.data = p;
             return map_weight(mm, one, 1, rows, cols, 64, box_rows);
+        },
+        st, tab, m);
+}
+
+// B-operand map of a routed MXFP8 payload (rowwise, or columnwise with col): the
+// 3D map over all experts, or, for a per-expert table (expert_ptrs holds the
+// rowwise payloads at [0, E) and the columnwise ones at [E, 2E)), expert
+// descriptors; box of 128 columns x box_rows rows
+moe_status routed_map_u8(moe_handle* h, int id, const moe_wview& v, bool col, int64_t rows, int64_t cols,
+                         uint32_t box_rows, cudaStream_t st, CUtensorMap* m, const CUtensorMap** tab) {
+    *tab = nullptr;
+    if (!v.expert_ptrs)
+        return map_u8_weight(m, col ? v.col_data : v.data, v, h->s.E, rows, cols, box_rows) ? MOE_OK
+                                                                                           : MOE_ERR_INVALID_ARG;
+    return expert_table(
+        h, id, v.expert_ptrs + (col ? h->s.E : 0), {v.row_stride, rows, cols, int64_t(box_rows) + (col ? 1 << 20 : 0)},
+        [&](CUtensorMap* mm, const void* p) {
+            moe_wview one = v;
+            one.expert_stride = rows * v.row_stride;
+            return map_u8_weight(mm, p, one, 1, rows, cols, box_rows);
         },
         st, tab, m);
 }
@@ -634,8 +661,8 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.x_q, rows, H, H) ||
-            !map_u8_weight(&m.b0, w->routed_gate.data, w->routed_gate, E, I, H, kMxBN / 2) ||
-            !map_u8_weight(&m.b1, w->routed_up.data, w->routed_up, E, I, H, kMxBN / 2))
+            routed_map_u8(h, TB_FWD_GU_G, w->routed_gate, false, I, H, kMxBN / 2, st, &m.b0, &a.b0_tab) != MOE_OK ||
+            routed_map_u8(h, TB_FWD_GU_U, w->routed_up, false, I, H, kMxBN / 2, st, &m.b1, &a.b1_tab) != MOE_OK)
             return MOE_ERR_INVALID_ARG;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
@@ -710,8 +737,6 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
     if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
     const Shape& s = h->s;
     if (T < 0 || T > s.Tmax) return MOE_ERR_INVALID_ARG;
-    if (w && s.mx && (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs))
-        return MOE_ERR_UNSUPPORTED;  // per-expert tables are for BF16 routed weights
     if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
     const bool topk = topk_ids != nullptr;
     if (T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
@@ -750,7 +775,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, b.a_q, rows, I, I) ||
-            !map_u8_weight(&m.b0, w->routed_down.data, w->routed_down, E, H, I, kMxBN))
+            routed_map_u8(h, TB_FWD_DOWN, w->routed_down, false, H, I, kMxBN, st, &m.b0, &a.b0_tab) != MOE_OK)
             return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
         a.mtile_expert = b.mtile_expert;
@@ -861,7 +886,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, ws.go_q, rows, H, H) ||
-            !map_u8_weight(&m.b0, w->routed_down.col_data, w->routed_down, E, H, I, 128))
+            routed_map_u8(h, TB_BWD_DOWN, w->routed_down, true, H, I, 128, st, &m.b0, &a.b0_tab) != MOE_OK)
             return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
         a.mtile_expert = b.mtile_expert;
@@ -952,8 +977,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     if (mx) {
         GemmArgs a = base_args(ws.status, s);
         if (!map_u8_kmajor(&m.a, ws.dgdu_q, rows, 2 * I, 2 * I) ||
-            !map_u8_weight(&m.b0, w->routed_gate.col_data, w->routed_gate, E, I, H, 128) ||
-            !map_u8_weight(&m.b1, w->routed_up.col_data, w->routed_up, E, I, H, 128))
+            routed_map_u8(h, TB_BWD_GU_G, w->routed_gate, true, I, H, 128, st, &m.b0, &a.b0_tab) != MOE_OK ||
+            routed_map_u8(h, TB_BWD_GU_U, w->routed_up, true, I, H, 128, st, &m.b1, &a.b1_tab) != MOE_OK)
             return MOE_ERR_INVALID_ARG;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
@@ -1118,22 +1143,40 @@ moe_status moe_prepare_weights(moe_handle* h, const moe_weights* w, void* stream
     const Shape& s = h->s;
     if (!s.mx) return MOE_OK;
     if (!w) return MOE_ERR_INVALID_ARG;
-    if (w->routed_gate.expert_ptrs || w->routed_up.expert_ptrs || w->routed_down.expert_ptrs)
-        return MOE_ERR_UNSUPPORTED;
     if (!check_weights(s, w)) return MOE_ERR_INVALID_ARG;
     const moe_wview &g = w->routed_gate, &u = w->routed_up, &d = w->routed_down;
-    if (g.expert_stride != u.expert_stride || g.row_stride != u.row_stride) return MOE_ERR_INVALID_ARG;
+    if (g.row_stride != u.row_stride) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int E = int(s.E), H = int(s.H), I = int(s.I);
     const Workspace& ws = h->ws;
-    MOE_CU(launch_swizzle_scales(1 /*rows, gate|up tiles*/, g.scale, u.scale, g.expert_stride / 32, g.row_stride / 32,
-                                 E, 2 * I / 128, H / 32, 0, ws.sf_fc1_row, st));
-    MOE_CU(launch_swizzle_scales(0 /*rows*/, d.scale, nullptr, d.expert_stride / 32, d.row_stride / 32, E, H / 128,
-                                 I / 32, 0, ws.sf_down_row, st));
-    MOE_CU(launch_swizzle_scales(2 /*columns*/, d.col_scale, nullptr, d.expert_stride / 32, d.row_stride, E, I / 128,
-                                 H / 32, 0, ws.sf_down_col, st));
-    MOE_CU(launch_swizzle_scales(3 /*columns, gate then up*/, g.col_scale, u.col_scale, g.expert_stride / 32,
-                                 g.row_stride, E, H / 128, 2 * I / 32, I / 32, ws.sf_fc1_col, st));
+    // every expert's rowwise and columnwise scale base, from its table entries
+    // (scales at [2E, 3E) and [3E, 4E)) or from the strided view
+    std::vector<const uint8_t*>& src = h->sf_src_host;
+    src.assign(6 * size_t(E), nullptr);
+    const moe_wview* views[3] = {&g, &u, &d};
+    for (int i = 0; i < 3; ++i) {
+        const moe_wview& v = *views[i];
+        for (int e = 0; e < E; ++e) {
+            const uint8_t* row = v.expert_ptrs ? static_cast<const uint8_t*>(v.expert_ptrs[2 * E + e])
+                                               : v.scale + int64_t(e) * (v.expert_stride / 32);
+            const uint8_t* colp = v.expert_ptrs ? static_cast<const uint8_t*>(v.expert_ptrs[3 * E + e])
+                                                : v.col_scale + int64_t(e) * (v.expert_stride / 32);
+            if (!row || !colp) return MOE_ERR_INVALID_ARG;
+            src[size_t(i) * E + e] = row;              // rowwise: gate, up, down
+            src[size_t(3 + (i + 1) % 3) * E + e] = colp;  // columnwise: down, gate, up
+        }
+    }
+    // pageable source: the copy is staged before the call returns
+    MOE_CU(cudaMemcpyAsync(ws.sf_src, src.data(), src.size() * sizeof(const uint8_t*), cudaMemcpyHostToDevice, st));
+    const uint8_t* const* t = ws.sf_src;
+    MOE_CU(launch_swizzle_scales(1 /*rows, gate|up tiles*/, t, t + E, g.row_stride / 32, E, 2 * I / 128, H / 32, 0,
+                                 ws.sf_fc1_row, st));
+    MOE_CU(launch_swizzle_scales(0 /*rows*/, t + 2 * E, nullptr, d.row_stride / 32, E, H / 128, I / 32, 0,
+                                 ws.sf_down_row, st));
+    MOE_CU(launch_swizzle_scales(2 /*columns*/, t + 3 * E, nullptr, d.row_stride, E, I / 128, H / 32, 0,
+                                 ws.sf_down_col, st));
+    MOE_CU(launch_swizzle_scales(3 /*columns, gate then up*/, t + 4 * E, t + 5 * E, g.row_stride, E, H / 128,
+                                 2 * I / 32, I / 32, ws.sf_fc1_col, st));
     h->weights_prepared = true;
     return MOE_OK;
 }

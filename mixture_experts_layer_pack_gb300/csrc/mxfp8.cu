@@ -90,8 +90,9 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __
 //   SW_COL_GU   kb < kb_split: gate src0[e][kb][..], else up src1[e][kb - kb_split][..]
 enum SwizzleMode : int { SW_ROW = 0, SW_ROW_GU = 1, SW_COL = 2, SW_COL_GU = 3 };
 
-__global__ void __launch_bounds__(256) swizzle_scales_kernel(int mode, const uint8_t* __restrict__ src0,
-                                                             const uint8_t* __restrict__ src1, int64_t src_es,
+// tab0 / tab1: device arrays of the E experts' source bases
+__global__ void __launch_bounds__(256) swizzle_scales_kernel(int mode, const uint8_t* const* __restrict__ tab0,
+                                                             const uint8_t* const* __restrict__ tab1,
                                                              int64_t src_rs, int E, int n_tiles, int k_blocks,
                                                              int kb_split, uint8_t* __restrict__ dst) {
     const int64_t per_expert = int64_t(n_tiles) * k_blocks * 128;
@@ -104,17 +105,18 @@ __global__ void __launch_bounds__(256) swizzle_scales_kernel(int mode, const uin
         rem -= int64_t(nt) * k_blocks * 128;
         const int kb = int(rem / 128);
         const int n = int(rem - int64_t(kb) * 128);
+        const uint8_t* src0 = tab0[e];
         uint8_t v;
         if (mode == SW_ROW) {
-            v = src0[e * src_es + int64_t(nt * 128 + n) * src_rs + kb];
+            v = src0[int64_t(nt * 128 + n) * src_rs + kb];
         } else if (mode == SW_ROW_GU) {
-            const uint8_t* s = n < 64 ? src0 : src1;
-            v = s[e * src_es + int64_t(nt * 64 + (n & 63)) * src_rs + kb];
+            const uint8_t* s = n < 64 ? src0 : tab1[e];
+            v = s[int64_t(nt * 64 + (n & 63)) * src_rs + kb];
         } else if (mode == SW_COL) {
-            v = src0[e * src_es + int64_t(kb) * src_rs + nt * 128 + n];
+            v = src0[int64_t(kb) * src_rs + nt * 128 + n];
         } else {
-            v = kb < kb_split ? src0[e * src_es + int64_t(kb) * src_rs + nt * 128 + n]
-                              : src1[e * src_es + int64_t(kb - kb_split) * src_rs + nt * 128 + n];
+            v = kb < kb_split ? src0[int64_t(kb) * src_rs + nt * 128 + n]
+                              : tab1[e][int64_t(kb - kb_split) * src_rs + nt * 128 + n];
         }
         dst[e * per_expert + sf_atom_offset(int64_t(nt) * 128 + n, kb, k_blocks) - int64_t(nt) * 0] = v;
     }
@@ -128,11 +130,11 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-cudaError_t launch_swizzle_scales(int mode, const uint8_t* src0, const uint8_t* src1, int64_t src_es, int64_t src_rs,
+cudaError_t launch_swizzle_scales(int mode, const uint8_t* const* tab0, const uint8_t* const* tab1, int64_t src_rs,
                                   int E, int n_tiles, int k_blocks, int kb_split, uint8_t* dst, cudaStream_t st) {
     const int64_t total = int64_t(E) * n_tiles * k_blocks * 128;
-    swizzle_scales_kernel<<<grid_for(total, 256), 256, 0, st>>>(mode, src0, src1, src_es, src_rs, E, n_tiles,
-                                                                  k_blocks, kb_split, dst);
+    swizzle_scales_kernel<<<grid_for(total, 256), 256, 0, st>>>(mode, tab0, tab1, src_rs, E, n_tiles, k_blocks,
+                                                                  kb_split, dst);
     count_launch();
     return cudaGetLastError();
 }

@@ -1,4 +1,4 @@
-"""Per-expert descriptor tables (routed BF16 weights and routed main_grads held
+"""Per-expert descriptor tables (routed BF16 or MXFP8 weights and routed main_grads held
 expert by expert in separate allocations, PR #6572 Design > MCore-owned
 parameters and > Gradient accumulation: per-expert non-single storage), through
 the C ABI.
@@ -106,14 +106,44 @@ def test_expert_tables_config2_full():
     _tables_match_strided(config_case(2))
 
 
-def test_mxfp8_tables_rejected():
-    c = Case(T=64, H=256, E=4, k=2, I=128, seed=65, mx=True)
-    inp = make_inputs(c)
+@pytest.mark.parametrize("name,case", [
+    ("mx_ragged", Case(T=300, H=256, E=6, k=2, I=128, seed=65, drop="iid", mx=True)),
+    ("mx_skewed_gated", Case(T=517, H=384, E=12, k=3, I=256, seed=66, routing="zipf", drop="multi", mx=True,
+                             gated=True)),
+])
+def test_mxfp8_expert_tables_bitwise_equal_to_strided(name, case):
+    """MXFP8 routed weights expert by expert (payloads, columnwise payloads and both
+    scale arrays in separate allocations): the scale swizzle and the block-scaled
+    GEMMs read them through per-expert pointers and descriptors, bit for bit the
+    strided run."""
+    inp = make_inputs(case)
+    c = inp.case
+    I = c.I
     layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, routed_wtype=M.binding.MOE_W_MXFP8)
     wv = weight_views(inp)
     layer.prepare_weights(wv)
-    q = inp.mx["routed_fc1"][0]
-    M.set_expert_tables(wv, gate=[q[e, :c.I] for e in range(c.E)])
-    with pytest.raises(M.MoeError) as ei:
-        layer.forward(inp.hidden, inp.probs, inp.routing_map.view(torch.uint8), wv)
-    assert ei.value.status == 2
+    mg_a = {n: t.clone() for n, t in inp.main_grads.items()}
+    ref = _run(inp, layer, wv, M.main_grads_from_combined(mg_a["shared_fc1"], mg_a["shared_fc2"],
+                                                           mg_a["routed_fc1"], mg_a["routed_fc2"],
+                                                           mg_a.get("shared_output_gate")))
+    q1, s1, c1, cs1 = inp.mx["routed_fc1"]
+    q2, s2, c2, cs2 = inp.mx["routed_fc2"]
+    E = c.E
+    gate = ([q1[e, :I].clone() for e in range(E)], [c1[e, :I].clone() for e in range(E)],
+            [s1[e, :I].clone() for e in range(E)], [cs1[e, :I // 32].clone() for e in range(E)])
+    up = ([q1[e, I:].clone() for e in range(E)], [c1[e, I:].clone() for e in range(E)],
+          [s1[e, I:].clone() for e in range(E)], [cs1[e, I // 32:].clone() for e in range(E)])
+    down = ([q2[e].clone() for e in range(E)], [c2[e].clone() for e in range(E)],
+            [s2[e].clone() for e in range(E)], [cs2[e].clone() for e in range(E)])
+    layer2 = M.MoELayer(c.T, c.H, c.E, c.k, c.I, routed_wtype=M.binding.MOE_W_MXFP8)
+    wv2 = weight_views(inp)
+    M.set_mx_expert_tables(wv2, gate=gate, up=up, down=down)
+    layer2.prepare_weights(wv2)
+    mg_b = {n: t.clone() for n, t in inp.main_grads.items()}
+    got = _run(inp, layer2, wv2, M.main_grads_from_combined(mg_b["shared_fc1"], mg_b["shared_fc2"],
+                                                            mg_b["routed_fc1"], mg_b["routed_fc2"],
+                                                            mg_b.get("shared_output_gate")))
+    for a, b, n in zip(got, ref, ("out", "dhidden", "dprobs")):
+        assert torch.equal(a, b), n
+    for n in mg_a:
+        assert torch.equal(mg_b[n], mg_a[n]), n
