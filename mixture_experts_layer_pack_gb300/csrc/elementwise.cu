@@ -69,6 +69,38 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4* p) {
     for (int j = 0; j < 8; ++j) acc[j] += f[j];
 }
 
+// acc += sum over the valid slots s (row_of_t[s] >= 0) of pp_t[s] * (8 bf16 of row
+// row_of_t[s] at column vector v), in slot order: the indices and weights of up to
+// four slots, then their rows, are loaded before any is used
+__device__ __forceinline__ void acc_slots(float (&acc)[8], const uint4* __restrict__ rows, int vec_per_row, int v,
+                                          const int* __restrict__ row_of_t, const float* __restrict__ pp_t, int k) {
+    constexpr int B = 4;
+    for (int s0 = 0; s0 < k; s0 += B) {
+        int r[B];
+        float w[B];
+        uint4 val[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            r[j] = s0 + j < k ? __ldg(row_of_t + s0 + j) : -1;
+            w[j] = s0 + j < k ? __ldg(pp_t + s0 + j) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+            if (r[j] >= 0) val[j] = __ldg(rows + int64_t(r[j]) * vec_per_row + v);
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (r[j] < 0) continue;
+            float f[8];
+            unpack_bf16x2(val[j].x, f[0], f[1]);
+            unpack_bf16x2(val[j].y, f[2], f[3]);
+            unpack_bf16x2(val[j].z, f[4], f[5]);
+            unpack_bf16x2(val[j].w, f[6], f[7]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(w[j], f[q], acc[q]);
+        }
+    }
+}
+
 __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
     return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                       pack_bf16x2(acc[6], acc[7]));
@@ -89,10 +121,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         fma_bf16x8(acc, ys + i, gate ? __ldg(gate + t) : 1.0f);
-        for (int s = 0; s < k; ++s) {
-            const int r = __ldg(row_of + int64_t(t) * k + s);
-            if (r >= 0) fma_bf16x8(acc, y + int64_t(r) * vec_per_row + v, __ldg(pp + int64_t(t) * k + s));
-        }
+        acc_slots(acc, y, vec_per_row, v, row_of + int64_t(t) * k, pp + int64_t(t) * k, k);
         out[i] = pack_bf16x8(acc);
     }
 }
