@@ -487,6 +487,10 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
             // row `lane` of the box: 128 bytes, 16-byte unit j at j ^ (lane % 8) (128-byte swizzle)
             uint4* srow = reinterpret_cast<uint4*>(bufs + b * (kStageTileBytes / 4) + lane * 32);
             if (bf) {
+                // bf16(main_grad + bf16(dW)) as one packed rounding of the exact sum of two
+                // bf16 values: that sum is exact in fp32 unless their exponents differ by
+                // more than 15, and then the smaller lies below half a bf16 ulp of the
+                // larger either way, so this equals the fp32 add followed by rounding
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint4 m = srow[j ^ (lane & 7)];
@@ -496,11 +500,9 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
                         const int cidx = 8 * (j & 3) + 2 * z;
                         const float d0 = j < 4 ? v[cidx] : v2[cidx];
                         const float d1 = j < 4 ? v[cidx + 1] : v2[cidx + 1];
-                        float lo, hi;
-                        unpack_bf16x2(mw[z], lo, hi);
-                        lo += __bfloat162float(__float2bfloat16_rn(d0));
-                        hi += __bfloat162float(__float2bfloat16_rn(d1));
-                        mw[z] = pack_bf16x2(lo, hi);
+                        const __nv_bfloat162 sum =
+                            __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&mw[z]), __floats2bfloat162_rn(d0, d1));
+                        mw[z] = *reinterpret_cast<const uint32_t*>(&sum);
                     }
                     srow[j ^ (lane & 7)] = m;
                 }
