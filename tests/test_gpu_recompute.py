@@ -131,3 +131,28 @@ def test_recompute_with_other_token_counts_and_topk_input():
             assert torch.equal(got[i][3][n], ref[i][3][n]), (i, n)
     A.close()
     B.close()
+
+
+def test_recompute_config2_full_size_bitwise():
+    """Proxy-like layer (T=4096, H=2048, E=96, top-6, I=1024): recompute mode equals the
+    default mode bit for bit, with a saved state a small fraction of the default one."""
+    from tests.harness import config_case
+    inp = make_inputs(config_case(2))
+    c = inp.case
+    wv = weight_views(inp)
+    rmap = inp.routing_map.view(torch.uint8)
+    res = []
+    for recompute in (False, True):
+        layer = _layer(c, recompute)
+        mg, mgv = _grads(inp)
+        out = layer.forward(inp.hidden, inp.probs, rmap, wv)
+        dh, dp = layer.backward(inp.grad_out, mgv)
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        res.append((out, dh, dp, mg, M.moe_saved_size(layer.cfg)))
+        layer.close()
+    (o0, h0, p0, m0, s0), (o1, h1, p1, m1, s1) = res
+    assert s1 * 20 < s0
+    assert torch.equal(o0, o1) and torch.equal(h0, h1) and torch.equal(p0, p1)
+    for n in m0:
+        assert torch.equal(m0[n], m1[n]), n

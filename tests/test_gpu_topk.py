@@ -130,3 +130,22 @@ def test_topk_zero_tokens():
     for n in mg:                               # nothing accumulated
         assert torch.equal(mg[n], inp.main_grads[n]), n
     assert layer.device_status() == 0
+
+
+def test_topk_config2_full_size_matches_the_dense_path_bitwise():
+    """Proxy-like layer (T=4096, H=2048, E=96, top-6, I=1024) fed by its top-k ids and
+    probs: every output, dhidden and main_grad element equal to the dense-map run."""
+    from tests.harness import config_case
+    inp = make_inputs(config_case(2))
+    ids, pp, over = O.route_pack(inp.map_np, inp.probs_np, inp.case.k)
+    assert not over.any()
+    dense = run_gpu(inp)
+    top = _run_topk(inp, ids.astype(np.int32), pp.astype(np.float32))
+    assert top.layer.device_status() == 0
+    assert torch.equal(top.out, dense.out)
+    assert torch.equal(top.dhidden, dense.dhidden)
+    for n in dense.main_grads:
+        assert torch.equal(top.main_grads[n], dense.main_grads[n]), n
+    dd = dense.dprobs.cpu().numpy()
+    want = np.where(ids >= 0, np.take_along_axis(dd, np.maximum(ids, 0), axis=1), 0.0)
+    assert np.array_equal(top.dprobs.cpu().numpy(), want)
