@@ -15,8 +15,8 @@ import torch
 
 from moe_inputs import make_routing
 from oracle import moe_oracle as O
-from tests.harness import (Case, TorchWeights, assert_close, assert_normwise, config_case, f64, make_inputs,
-                           oracle_full, run_gpu)
+from tests.harness import (EXACT_NORMWISE_MIN_TOKENS, Case, TorchWeights, assert_close, assert_normwise, config_case,
+                           f64, make_inputs, oracle_full, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +26,8 @@ SMALL = {
     "bn64_skewed": Case(T=517, H=384, E=12, k=3, I=192, seed=22, routing="zipf", drop="multi"),
     "one_token": Case(T=1, H=128, E=4, k=2, I=64, seed=23),
     "odd_experts": Case(T=333, H=128, E=13, k=3, I=64, seed=24, drop="iid"),   # byte-wise map rows
+    "max_experts_topk": Case(T=256, H=128, E=1024, k=32, I=64, seed=25),         # the largest E and k
+    "single_expert": Case(T=200, H=128, E=1, k=1, I=64, seed=26),
 }
 
 
@@ -118,6 +120,8 @@ def _compare_full(inp, res, exact=True):
         for n, r in refs(out, dx, dprobs, grads).items():
             errs["exact " + n] = assert_normwise(got[n], r, n, env=env_of[n] if jumps else None)
         for e, (dWg, dWu, dWd) in grads["routed"].items():
+            if int(inp.map_np[:, e].sum()) < EXACT_NORMWISE_MIN_TOKENS:
+                continue   # too few tokens for the normwise argument; checked per element above
             eg, eu, ed = env["routed"][e] if jumps else (None, None, None)
             assert_normwise(d["routed_fc1"][e, :I], dWg, f"dW routed gate[{e}]", env=eg)
             assert_normwise(d["routed_fc1"][e, I:], dWu, f"dW routed up[{e}]", env=eu)
