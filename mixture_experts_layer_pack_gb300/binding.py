@@ -525,3 +525,11 @@ class HostSteps:
         self.compute.synchronize()
         self.down.synchronize()
 
+    def __del__(self):
+        # the staging buffers go back to the caching allocator with this object:
+        # no copy or kernel of the pipeline may still be using them
+        try:
+            self.synchronize()
+        except Exception:
+            pass
+
