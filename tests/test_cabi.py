@@ -78,3 +78,73 @@ def test_null_arguments_rejected():
     assert L.moe_create(ctypes.byref(_cfg()), None, 0, ctypes.byref(h)) == 1
     assert L.moe_forward(None, 0, None, None, None, None, None, None, None) == 1
     assert L.moe_backward(None, None, None, None, None, None, None) == 1
+
+
+def _c_layout(tmp_path):
+    """sizeof / offsetof of the ABI structs as a C compiler lays them out from include/moe.h."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {
+        "moe_config": ["max_tokens", "hidden", "num_experts", "topk", "inter", "routed_wtype", "swiglu_limit",
+                       "recompute_dispatch"],
+        "moe_wview": ["data", "expert_stride", "row_stride", "scale", "col_data", "col_scale", "expert_ptrs"],
+        "moe_weights": ["shared_gate", "shared_up", "shared_down", "routed_gate", "routed_up", "routed_down",
+                        "shared_output_gate"],
+        "moe_main_grads": [n for n, _ in B.moe_main_grads._fields_],
+    }
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe.h"', "int main(void) {"]
+    for s, fs in fields.items():
+        lines.append(f'printf("{s} size %zu\\n", sizeof({s}));')
+        for f in fs:
+            lines.append(f'printf("{s} {f} %zu\\n", offsetof({s}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    return {tuple(l.split()[:2]): int(l.split()[2]) for l in out.splitlines()}
+
+
+def test_ctypes_structs_match_the_c_header(tmp_path):
+    """The binding's ctypes structs have the size and field offsets the C header
+    gives, so every argument is marshalled where the library reads it."""
+    c = _c_layout(tmp_path)
+    for s in (B.moe_config, B.moe_wview, B.moe_weights, B.moe_main_grads):
+        assert c[(s.__name__, "size")] == ctypes.sizeof(s), s.__name__
+        for f, _ in s._fields_:
+            assert c[(s.__name__, f)] == getattr(s, f).offset, (s.__name__, f)
+
+
+def test_recompute_dispatch_flag():
+    full = M.moe_saved_size(_cfg())
+    small = M.moe_saved_size(_cfg(recompute_dispatch=1))
+    assert 0 < small * 100 < full                    # the saved state keeps only the routing
+    assert M.moe_workspace_size(_cfg(recompute_dispatch=1)) > M.moe_workspace_size(_cfg())
+    with pytest.raises(M.MoeError) as ei:
+        M.moe_saved_size(_cfg(recompute_dispatch=2))
+    assert ei.value.status == 1
+
+
+def test_mx_expert_tables_pointer_layout():
+    """set_mx_expert_tables: 4E pointers per view in the ABI order (rowwise payloads,
+    columnwise payloads, rowwise scales, columnwise scales), strides checked."""
+    import torch
+    E, N, K = 3, 64, 128
+    q = [torch.zeros((N, K), dtype=torch.uint8) for _ in range(E)]
+    cq = [torch.zeros((N, K), dtype=torch.uint8) for _ in range(E)]
+    sc = [torch.zeros((N, K // 32), dtype=torch.uint8) for _ in range(E)]
+    csc = [torch.zeros((N // 32, K), dtype=torch.uint8) for _ in range(E)]
+    w = B.moe_weights()
+    M.set_mx_expert_tables(w, gate=(q, cq, sc, csc))
+    v = w.routed_gate
+    assert v.row_stride == K and v.data is None and v.expert_stride == 0
+    arr = ctypes.cast(v.expert_ptrs, ctypes.POINTER(ctypes.c_void_p))
+    want = [t.data_ptr() for t in q + cq + sc + csc]
+    assert [arr[i] for i in range(4 * E)] == want
+    bad = [torch.zeros((N, K // 16), dtype=torch.uint8) for _ in range(E)]   # wrong scale row stride
+    with pytest.raises(ValueError):
+        M.set_mx_expert_tables(B.moe_weights(), up=(q, cq, bad, csc))
