@@ -180,8 +180,10 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_handle** out);
 void moe_destroy(moe_handle* h);
 
-/* Saved forward state (routing, permuted activations, SwiGLU intermediates)
- * lives in caller-owned device memory of moe_saved_size bytes. */
+/* Saved forward state (routing, permuted activations, SwiGLU intermediates;
+ * with recompute_dispatch the routing only) lives in caller-owned device memory
+ * of moe_saved_size bytes. A handle serves any number of saved states; their
+ * forwards and backwards may interleave on the handle's stream. */
 moe_status moe_saved_size(const moe_config* cfg, size_t* bytes);
 moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved** out);
 void moe_saved_destroy(moe_saved* s);
