@@ -156,3 +156,37 @@ def test_recompute_config2_full_size_bitwise():
     assert torch.equal(o0, o1) and torch.equal(h0, h1) and torch.equal(p0, p1)
     for n in m0:
         assert torch.equal(m0[n], m1[n]), n
+
+
+def test_default_mode_saved_states_interleave():
+    """Default mode: two saved states of one handle, forward 1, forward 2, backward 2,
+    backward 1, bitwise the sequential order (the workspace is scratch within a call)."""
+    inp = make_inputs(Case(T=300, H=256, E=8, k=2, I=128, seed=104, drop="iid", gated=True))
+    c = inp.case
+    wv = weight_views(inp)
+    rmap = inp.routing_map.view(torch.uint8)
+    batches = [(inp.hidden, inp.grad_out), (inp.hidden * 0.75, inp.grad_out * -2.0)]
+    A = _layer(c, False)
+    ref = []
+    for hid, go in batches:
+        mg, mgv = _grads(inp)
+        out = A.forward(hid, inp.probs, rmap, wv)
+        dh, dp = A.backward(go, mgv)
+        ref.append((out.clone(), dh.clone(), dp.clone(), mg))
+    mem2 = torch.empty(M.moe_saved_size(A.cfg), dtype=torch.uint8, device=inp.hidden.device)
+    saved = [A.saved, M.moe_saved_create(A.handle, mem2)]
+    outs = [torch.empty_like(inp.hidden) for _ in batches]
+    for i, (hid, _) in enumerate(batches):
+        M.moe_forward(A.handle, c.T, hid, inp.probs, rmap, wv, outs[i], saved[i])
+    for i in (1, 0):
+        mg, mgv = _grads(inp)
+        dh = torch.empty_like(inp.hidden)
+        dp = torch.empty((c.T, c.E), dtype=torch.float32, device=inp.hidden.device)
+        M.moe_backward(A.handle, batches[i][1], saved[i], dh, dp, mgv)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref[i][0]) and torch.equal(dh, ref[i][1]) and torch.equal(dp, ref[i][2]), i
+        for n in mg:
+            assert torch.equal(mg[n], ref[i][3][n]), (i, n)
+    assert A.device_status() == 0
+    M.moe_saved_destroy(saved[1])
+    A.close()
