@@ -65,3 +65,23 @@ def test_kernel_work_table_covers_every_kernel_class():
     r = bench.roofline_of("gemm_wgrad_fc1_routed", 0.65, bench.kernel_work("gemm_wgrad_fc1_routed", 4096, 2048, 96,
                                                                            6, 1024, 24576, 96), peaks, "measured")
     assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5
+
+
+def test_kernel_work_counts_the_shared_expert_in_the_bf16_grouped_launches():
+    """BF16 routed weights: the shared expert is group 0 of the routed launches, so their
+    algorithmic work is the routed formula at R + T rows and E_act + 1 experts; with
+    MXFP8 the routed classes count the routed experts only."""
+    T, H, E, k, I, R, Ea = 4096, 2048, 96, 6, 1024, 24576, 96
+    f, b = bench.kernel_work("gemm_wgrad_fc1_routed", T, H, E, k, I, R, Ea, mx=False, mg_bytes=4)
+    assert f == 4 * (R + T) * I * H
+    assert b == (R + T) * 2 * I * 2 + (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 * 4
+    f, b = bench.kernel_work("gemm_fwd_gu_routed", T, H, E, k, I, R, Ea, mx=False)
+    assert f == 4 * (R + T) * H * I
+    assert b == (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 + (R + T) * I * 2 + (R + T) * 2 * I * 2
+    f, _ = bench.kernel_work("gemm_wgrad_fc1_routed", T, H, E, k, I, R, Ea, mx=True)
+    assert f == 4 * R * I * H
+    # the useful flops of a step: forward, dgrad and wgrad over routed and shared rows
+    assert bench.useful_flops(R, T, H, I) == sum(
+        bench.kernel_work(n, T, H, E, k, I, R, Ea, mx=False)[0]
+        for n in ("gemm_fwd_gu_routed", "gemm_fwd_down_routed", "gemm_bwd_down_routed", "gemm_bwd_gu_routed",
+                  "gemm_wgrad_fc1_routed", "gemm_wgrad_down_routed"))
