@@ -43,30 +43,36 @@ the tail; a row with more than k routes is an error, not truncated; a routed
 (t, e) with prob 0 is still computed; probs off the map are ignored and get
 gradient 0; within an expert, routes are ordered by token index.
 
-Precision. The pages fix it for the expert GEMMs: BF16 routed and shared
-experts (PR #6572, Supported configurations) with an FP32 GEMM accumulator
-and FP32 main_grad accumulation (PR #8210, review thread on wgrad
-precision). ``precision="exact"`` is the plain definition in fp64.
-``precision="bf16"`` holds every tensor a BF16 expert passes on in bf16: the
-gate/up projections g and u (kept for backward), the activation a between the
-two projections, the expert's output y (the prob, or the shared expert's
-gate, weights it in the fp32 combine), the SwiGLU gradients dg and du, the
-prob-weighted activation p*a that multiplies grad_out in the down
-projection's weight gradient, and the expert's input gradient dx (summed in
-fp32 by the un-permute); products accumulate in fp64. Inputs (hidden,
-grad_out, weights) are bf16 already. ``precision="mxfp8"`` (MXFP8 routed
-experts, same pages) quantises the routed experts' forward and dgrad GEMM
-operands to MXFP8 in blocks of 32 along each GEMM's K -- x and a in forward,
-grad_out and [dg|du] in dgrad -- with the weights given dequantised
-(rowwise for forward, columnwise for dgrad through ``routed_dgrad``); the
-weight-gradient GEMMs and the shared expert keep bf16 operands.
+Precision. The pages fix the weights (BF16, or MXFP8 routed experts: PR
+#6572, Supported configurations), the FP32 GEMM accumulator and the FP32
+main_grad accumulation (PR #8210, review thread on wgrad precision).
+``precision="exact"`` is the plain definition in fp64, nothing rounded.
+``precision="mxfp8"`` is the MXFP8 method on top of it: the routed experts'
+forward and dgrad GEMM operands are quantised to MXFP8 on the fly, in blocks
+of 32 along each GEMM's K -- x and a in forward, grad_out and [dg|du] in
+dgrad -- with the weights given dequantised (rowwise for forward, columnwise
+for dgrad through ``routed_dgrad``); nothing else is rounded (the dprob and
+the weight gradients take the unquantised a, dg, du, as a backward through a
+quantiser that passes gradients straight through does). ``precision="bf16"``
+is a diagnostic mode for a layer that stores its activations in bf16: every
+tensor a BF16 expert passes on is rounded to bf16 -- the gate/up projections
+g and u (kept for backward), the activation a between the two projections,
+the expert's output y (the prob, or the shared expert's gate, weights it in
+the fp32 combine), the SwiGLU gradients dg and du, the prob-weighted
+activation p*a that multiplies grad_out in the down projection's weight
+gradient, and the expert's input gradient dx (summed in fp32 by the
+un-permute); products accumulate in fp64. Inputs (hidden, grad_out, weights)
+are bf16 already.
 
 A bf16 rounding is a discrete decision taken on a value the kernel evaluates
 in fp32 (FP32 accumulator), so near a rounding midpoint both neighbours are
-correct results. ``envelope`` (bf16 and mxfp8 modes) bounds, per output element, how far
+correct results. ``envelope`` (bf16 mode) bounds, per output element, how far
 the other valid roundings of every operand that lies within the fp32
 evaluation band of a midpoint can move the result (propagated with absolute
-values); elsewhere it is 0.
+values); elsewhere it is 0. The same holds for the swiglu_limit clamp's
+gradient masks, which jump at the clamp bounds: ``clamp_jumps`` (any mode)
+bounds the effect of the other mask value where g or |u| lies within its
+fp32 evaluation band of the bound.
 
 Everything here is fp64 numpy; ``@`` (a BLAS matmul) is the only library step.
 """
@@ -185,10 +191,21 @@ def bf16_alternative(x, band):
 
 def fp32_dot_band(terms_sq_sum, K):
     """Evaluation band of an fp32-accumulated dot product of length K whose
-    terms t have sum(t^2) = terms_sq_sum: 8 U32 sqrt(K) ||t||_2. An accumulator
-    that adds 16-term partial products with truncation, not round-to-nearest,
-    drifts by about U32 (K/16)^(3/2) rms(t) (~1.5 U32 sqrt(K) ||t|| at K=2048);
-    the factor 8 covers that bias several times over."""
+    terms t have sum(t^2) = terms_sq_sum: 8 U32 sqrt(K) ||t||_2.
+
+    Derivation. A sum accumulated in fp32 in any order carries the error
+    sum_j delta_j S_j, S_j the partial sums, |delta_j| <= U32. Under the
+    probabilistic model of Higham and Mary ("A New Approach to Probabilistic
+    Rounding Error Analysis", SIAM J. Sci. Comput. 41(5), 2019: rounding
+    errors independent, mean zero) its variance is at most
+    U32^2 sum_j E[S_j^2] / 3; for terms of random sign E[S_j^2] = j ||t||^2 / K,
+    so the standard deviation is at most U32 sqrt(K) ||t||_2 / sqrt(6). The
+    band is ~20 of those (a tail probability far below 1e-50 for the bounded,
+    independent sum). An accumulator that adds 16-term partial products with
+    truncation has a bias instead, at most U32 |S_j| per addition on partial
+    sums |S_j| ~ sqrt(16 j) rms(t): summed over the K/16 additions at most about
+    3 U32 (K/16)^(3/2) rms(t) = 3 U32 sqrt(K) ||t||_2 sqrt(K) / 64, which stays
+    below the band for K up to 16384 (the layer's longest reductions)."""
     return 8.0 * U32 * np.sqrt(K) * np.sqrt(terms_sq_sum)
 
 
@@ -196,9 +213,9 @@ ELEMENTWISE_BAND = 2.0 ** -20   # relative band of fp32 elementwise evaluation (
 
 
 def _rounder(precision):
-    if precision == "exact":
+    if precision in ("exact", "mxfp8"):
         return lambda v: v
-    if precision in ("bf16", "mxfp8"):
+    if precision == "bf16":
         return bf16_round
     raise ValueError(precision)
 
@@ -211,16 +228,17 @@ def mxfp8_round(v):
 
 
 class Operands:
-    """Where one expert's GEMM operands are rounded: identity (exact), bf16, or,
-    for routed experts in mxfp8 mode, MXFP8 along K for the forward and dgrad
-    GEMMs (bf16 for the weight-gradient GEMMs); and the bf16 tensors between
-    the expert's GEMMs and the layer's sums (``inter``: g, u, y, dx)."""
+    """Where one expert's GEMM operands are rounded: nowhere (exact); bf16
+    everywhere (bf16 mode); or, for routed experts in mxfp8 mode, MXFP8 along K
+    for the forward and dgrad GEMMs' activation operands only; and, in bf16 mode,
+    the bf16 tensors between the expert's GEMMs and the layer's sums (``inter``:
+    g, u, y, dx)."""
 
     def __init__(self, precision, routed=True):
         self.rnd = _rounder(precision)
         self.mx = precision == "mxfp8" and routed
 
-    def inter(self, v):                   # g, u, y, dx: GEMM results stored in bf16
+    def inter(self, v):                   # g, u, y, dx: GEMM results (bf16 mode: stored in bf16)
         return self.rnd(v)
 
     def x(self, x):                       # gate/up projection input, K = H
@@ -240,6 +258,9 @@ class Operands:
 
     def wgrad(self, v):                   # weight-gradient operands
         return self.rnd(v)
+
+    def kept_a(self, a_val, a_op):        # the a that the backward's dprob and p*a take
+        return a_op if self.rnd is bf16_round else a_val
 
 
 # --------------------------------------------------------------------------
@@ -277,9 +298,10 @@ def expert_forward(x, Wg, Wu, Wd, ops=None, limit=0.0):
     g = ops.inter(xq @ Wg.T)
     u = ops.inter(xq @ Wu.T)
     gc, uc, _, _ = clamp_inputs(g, u, limit)
-    a = ops.a(silu(gc) * uc)
-    y = ops.inter(a @ Wd.T)
-    return g, u, a, y
+    a_val = silu(gc) * uc
+    a_op = ops.a(a_val)
+    y = ops.inter(a_op @ Wd.T)
+    return g, u, ops.kept_a(a_val, a_op), y
 
 
 def expert_backward(x, go, p, g, u, a, Wg, Wu, Wd, ops=None, limit=0.0):
@@ -436,54 +458,24 @@ def silu_grad2_bound():
     return 0.5
 
 
-def mxfp8_alternative(v, band):
-    """mxfp8 mode: per element of v (blocks of 32 along the last axis), the
-    distance to the other valid quantised value where v lies within ``band``
-    of an E4M3 rounding midpoint (in value units), and, for every element of a
-    block whose amax lies within its band of a power of two (the shared
-    exponent may go either way), a bound on the change a coarser scale makes."""
-    from oracle import mxfp8
-    v = np.asarray(v, np.float64)
-    band = np.broadcast_to(np.asarray(band, np.float64), v.shape)
-    shp = v.shape
-    vb = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
-    bb = band.reshape(vb.shape)
-    amax = np.max(np.abs(vb), axis=-1)
-    scale = mxfp8.e8m0_value(mxfp8.e8m0_scale_code(amax))[..., None]
-    y = np.minimum(np.abs(vb) / scale, mxfp8.E4M3_MAX)
-    grid = mxfp8._POS_VALUES
-    hi = np.clip(np.searchsorted(grid, y), 1, grid.size - 1)
-    lo = hi - 1
-    mid = (grid[lo] + grid[hi]) / 2
-    spacing = grid[hi] - grid[lo]
-    alt = np.where(np.abs(y - mid) * scale <= bb, spacing * scale, 0.0)
-    # shared exponent at a power-of-two boundary of amax
-    _, ex = np.frexp(amax)
-    edge = np.ldexp(0.5, ex)                   # the power of two at or below amax
-    bband = np.max(bb, axis=-1)
-    near = (np.abs(amax - edge) <= bband) | (np.abs(amax - 2 * edge) <= bband)
-    alt = np.where(near[..., None], np.maximum(alt, np.abs(vb) / 8 + 2 * scale * 2.0 ** -9), alt)
-    return alt.reshape(shp)
-
-
-def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_band=None):
-    """Envelopes of one expert's results for rows x[n,H] with probs p[n]. Wf are
-    the forward weights (Wg, Wu, Wd), Wb the dgrad weights; g, u the mode's
-    (bf16) gate/up values; ``limit`` the swiglu_limit clamp; ``p_band`` a bound
-    on the kernel's error in p (the shared output gate, which the kernel
+def _expert_envelope(x, go, p, g, u, Wf, Wb, limit=0.0, p_band=None):
+    """bf16-mode envelopes of one expert's results for rows x[n,H] with probs
+    p[n]. Wf are the forward weights (Wg, Wu, Wd), Wb the dgrad weights; g, u the
+    mode's (bf16) gate/up values; ``limit`` the swiglu_limit clamp; ``p_band`` a
+    bound on the kernel's error in p (the shared output gate, which the kernel
     evaluates in fp32; None: p is exact).
 
-    Every bf16 (or MXFP8) tensor is a rounding of a value the kernel evaluates
+    Every bf16 tensor is a rounding of a value the kernel evaluates
     in fp32. Where that value lies within its evaluation band of a rounding
     midpoint, the other neighbour is also a correct result; the difference it
     makes is carried forward with absolute values (a change below a later
     rounding's distance to its midpoint is absorbed by it, a larger one may
     flip it in turn). Returns env_y [n,H] (the expert's output y), env_dx
     [n,H], env_dWg [I,H], env_dWu [I,H], env_dWd [H,I], env_dprob [n]."""
-    ops = Operands(precision, routed)
+    ops = Operands("bf16")
     Wg, Wu, Wd = Wf
     Bg, Bu, Bd = Wb
-    xq = ops.x(x)
+    xq = x
     H = x.shape[1]
     I = g.shape[1]
     p_band = np.zeros_like(p) if p_band is None else p_band
@@ -494,18 +486,18 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_ban
     gc, uc, mg, mu = clamp_inputs(g, u, limit)
     s1 = silu_grad(gc)
     a_val = silu(gc) * uc
-    # a: elementwise fp32 math on g, u, then rounded (MXFP8 for routed experts in mxfp8 mode);
-    # a flipped g or u moves it by the slopes (a is continuous across the clamp bounds)
+    # a: elementwise fp32 math on g, u, then rounded; a flipped g or u moves it by
+    # the slopes (a is continuous across the clamp bounds)
     flip_a = np.abs(s1 * uc) * alt_g + np.abs(silu(gc)) * alt_u
     band_a = ELEMENTWISE_BAND * np.abs(a_val) + flip_a
-    alt_a = (mxfp8_alternative(a_val, band_a) if ops.mx else bf16_alternative(a_val, band_a)) + flip_a
+    alt_a = bf16_alternative(a_val, band_a) + flip_a
     a_b = ops.a(a_val)
     # y = bf16(a_b Wd^T)
     ey_pre = alt_a @ np.abs(Wd).T
     band_y = fp32_dot_band((a_b * a_b) @ (Wd * Wd).T, I) + ey_pre
     env_y = ey_pre + bf16_alternative(a_b @ Wd.T, band_y)
 
-    goq = ops.go(go)
+    goq = go
     da_u = goq @ Bd
     env_dprob = np.sum(alt_a * np.abs(da_u), axis=1)
     da = p[:, None] * da_u
@@ -529,15 +521,9 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_ban
         near_u = np.abs(np.abs(u_raw) - limit) <= ulp(u_raw)
         jump_dg = np.where(near_g, np.abs(da * uc * s1), 0.0)
         jump_du = np.where(near_u, np.abs(da * silu(gc)), 0.0)
-    alt_dg = bf16_alternative(dg_val, band_dg) + flip_dg + jump_dg   # weight-gradient operands (bf16)
+    alt_dg = bf16_alternative(dg_val, band_dg) + flip_dg + jump_dg   # dgrad and weight-gradient operands
     alt_du = bf16_alternative(du_val, band_du) + flip_du + jump_du
-    if ops.mx:                                            # dgrad operand [dg|du] (MXFP8)
-        flips = np.concatenate([flip_dg + jump_dg, flip_du + jump_du], axis=1)
-        alt_q = mxfp8_alternative(np.concatenate([dg_val, du_val], axis=1),
-                                  np.concatenate([band_dg + jump_dg, band_du + jump_du], axis=1)) + flips
-        edx_pre = alt_q[:, :I] @ np.abs(Bg) + alt_q[:, I:] @ np.abs(Bu)
-    else:
-        edx_pre = alt_dg @ np.abs(Bg) + alt_du @ np.abs(Bu)
+    edx_pre = alt_dg @ np.abs(Bg) + alt_du @ np.abs(Bu)
     # dx = bf16(dg Bg + du Bu)
     dgq, duq = ops.dgdu(dg_val, du_val)
     band_dx = fp32_dot_band((dgq * dgq) @ (Bg * Bg) + (duq * duq) @ (Bu * Bu), 2 * I) + edx_pre
@@ -554,9 +540,10 @@ def _expert_envelope(x, go, p, g, u, Wf, Wb, precision, routed, limit=0.0, p_ban
 
 def envelope(grad_out, cache, W):
     """Per-element envelopes of out, dhidden, dprobs and the six weight
-    gradients for a bf16- or mxfp8-mode forward/backward (see the module notes)."""
+    gradients for a bf16-mode forward/backward (see the module notes)."""
     go = np.asarray(grad_out, np.float64)
-    prec = cache["precision"]
+    if cache["precision"] != "bf16":
+        raise ValueError("the rounding envelope is defined for the bf16 mode")
     x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
     offsets, perm_src, perm_slot = cache["offsets"], cache["perm_src"], cache["perm_slot"]
     T, H = x.shape
@@ -570,8 +557,8 @@ def envelope(grad_out, cache, W):
         z_band = fp32_dot_band((x * x) @ (w_gate * w_gate), H)
         p_band = gate * (1.0 - gate) * z_band + ELEMENTWISE_BAND * gate
         p_s = gate
-    ey_s, edx_s, eg_s, eu_s, ed_s, edg = _expert_envelope(x, go, p_s, gs, us, W.shared(), W.shared(), prec,
-                                                          routed=False, limit=limit, p_band=p_band)
+    ey_s, edx_s, eg_s, eu_s, ed_s, edg = _expert_envelope(x, go, p_s, gs, us, W.shared(), W.shared(),
+                                                          limit=limit, p_band=p_band)
     env_gate = None
     if gate is not None:
         ey_s = gate[:, None] * ey_s
@@ -587,8 +574,8 @@ def envelope(grad_out, cache, W):
     for e, (g, u, _) in cache["routed"].items():
         lo, hi = offsets[e], offsets[e + 1]
         ey[lo:hi], edx[lo:hi], eg, eu, ed, edp[lo:hi] = _expert_envelope(
-            x[perm_src[lo:hi]], go[perm_src[lo:hi]], pp_perm[lo:hi], g, u, W.routed(e), W.routed_dgrad(e), prec,
-            routed=True, limit=limit)
+            x[perm_src[lo:hi]], go[perm_src[lo:hi]], pp_perm[lo:hi], g, u, W.routed(e), W.routed_dgrad(e),
+            limit=limit)
         routed[e] = (eg, eu, ed)
     env_out = ey_s.copy()
     env_dh = edx_s.copy()
@@ -603,4 +590,64 @@ def envelope(grad_out, cache, W):
                shared_down=ed_s, routed=routed)
     if env_gate is not None:
         env["shared_output_gate"] = env_gate
+    return env
+
+
+def _expert_clamp_jumps(x, go, p, Wf, Wb, ops, limit):
+    """One expert's bounds on the effect of the clamp's other gradient mask where
+    the fp32 evaluation of g = x Wg^T or u = x Wu^T lies within its band
+    (``fp32_dot_band``) of the bound L (g) or of +-L (u): there either mask value
+    is a correct result. Returns (env_dx [n,H], env_dWg [I,H], env_dWu [I,H])."""
+    Wg, Wu, _ = Wf
+    Bg, Bu, Bd = Wb
+    H = x.shape[1]
+    xq = ops.x(x)
+    g, u = xq @ Wg.T, xq @ Wu.T
+    near_g = np.abs(g - limit) <= fp32_dot_band((xq * xq) @ (Wg * Wg).T, H)
+    near_u = np.abs(np.abs(u) - limit) <= fp32_dot_band((xq * xq) @ (Wu * Wu).T, H)
+    gc, uc, _, _ = clamp_inputs(g, u, limit)
+    da = p[:, None] * (ops.go(go) @ Bd)
+    jump_dg = np.where(near_g, np.abs(da * uc * silu_grad(gc)), 0.0)
+    jump_du = np.where(near_u, np.abs(da * silu(gc)), 0.0)
+    return jump_dg @ np.abs(Bg) + jump_du @ np.abs(Bu), jump_dg.T @ np.abs(x), jump_du.T @ np.abs(x)
+
+
+def clamp_jumps(grad_out, cache, W):
+    """Per-element bounds (same keys as ``envelope``; zero for out, dprobs and the
+    down projections' weight gradients, which the masks do not reach) on how far
+    the swiglu_limit clamp's other gradient mask moves dhidden and the gate/up
+    weight gradients, for the SwiGLU inputs whose fp32 evaluation cannot tell
+    which side of a clamp bound they lie on. The clamp itself is continuous, so
+    the forward is unaffected. All zero without a clamp."""
+    go = np.asarray(grad_out, np.float64)
+    x, ids, pp, row_of = cache["x"], cache["ids"], cache["pp"], cache["row_of"]
+    offsets, perm_src, perm_slot = cache["offsets"], cache["perm_src"], cache["perm_slot"]
+    T, H = x.shape
+    E = W.num_experts
+    limit, gate = cache["limit"], cache["gate"]
+    z = lambda a: np.zeros_like(a)  # noqa: E731
+    Ws = W.shared()
+    env = dict(out=np.zeros((T, H)), dhidden=np.zeros((T, H)), dprobs=np.zeros((T, E)), shared_gate=z(Ws[0]),
+               shared_up=z(Ws[1]), shared_down=z(Ws[2]), routed={})
+    if gate is not None:
+        env["shared_output_gate"] = np.zeros(H)
+    for e in cache["routed"]:
+        Wr = W.routed(e)
+        env["routed"][e] = (z(Wr[0]), z(Wr[1]), z(Wr[2]))
+    if not limit:
+        return env
+    p_s = np.ones(T) if gate is None else gate
+    env["dhidden"], env["shared_gate"], env["shared_up"] = _expert_clamp_jumps(
+        x, go, p_s, Ws, Ws, Operands(cache["precision"], routed=False), limit)
+    R = perm_src.size
+    edx = np.zeros((R, H))
+    pp_perm = pp[perm_src, perm_slot] if R else np.zeros(0)
+    for e in cache["routed"]:
+        lo, hi = offsets[e], offsets[e + 1]
+        edx[lo:hi], eg, eu = _expert_clamp_jumps(x[perm_src[lo:hi]], go[perm_src[lo:hi]], pp_perm[lo:hi],
+                                                 W.routed(e), W.routed_dgrad(e), Operands(cache["precision"]), limit)
+        env["routed"][e] = (eg, eu, env["routed"][e][2])
+    for s in range(cache["k"]):
+        v = ids[:, s] >= 0
+        env["dhidden"][v] += edx[row_of[v, s]]
     return env

@@ -110,20 +110,15 @@ def test_bf16_backward_matches_textbook(seed):
             np.testing.assert_allclose(grads["routed"][e][j], ref, rtol=1e-12, atol=1e-13)
 
 
-def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
+def _fp32_layer(x, go, m, probs, W, k, limit=0.0, bf16=True):
     """An independent fp32 evaluation of the layer (numpy float32 matmuls and
-    elementwise math, bf16 rounding of every tensor an expert passes on -- g, u,
-    a, y, dg, du, p*a, dx; MXFP8 for the routed forward/dgrad operands when mx --
-    and fp64 sums in the combine, un-permute and weight gradients): stands in for
-    any kernel that evaluates these tensors in fp32. ``limit`` clamps the SwiGLU inputs;
+    elementwise math; with ``bf16`` a bf16 rounding of every tensor an expert
+    passes on -- g, u, a, y, dg, du, p*a, dx -- else none; fp64 sums in the
+    combine, un-permute and weight gradients): stands in for any kernel that
+    evaluates these tensors in fp32. ``limit`` clamps the SwiGLU inputs;
     W.shared_output_gate (if set) gates the shared expert with an fp32 sigmoid."""
-    from oracle import mxfp8 as MXC
     f32 = np.float32
-    rnd = O.bf16_round
-
-    def mxr(v):
-        q, sc = MXC.quantize(np.asarray(v, np.float64), axis=-1)
-        return MXC.dequantize(q, sc, axis=-1)
+    rnd = O.bf16_round if bf16 else (lambda v: v)
 
     def sig(z):
         return f32(1) / (f32(1) + np.exp(-z))
@@ -131,10 +126,8 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
     def r32(v):                      # bf16 rounding of an fp32 array, kept in fp32
         return rnd(v.astype(np.float64)).astype(f32)
 
-    def expert(xr, gor, p, Wg, Wu, Wd, quant):
-        xq = mxr(xr) if quant else xr
-        goq = mxr(gor) if quant else gor
-        xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xq, Wg, Wu, Wd, goq))
+    def expert(xr, gor, p, Wg, Wu, Wd):
+        xr32, Wg32, Wu32, Wd32, go32 = (a.astype(f32) for a in (xr, Wg, Wu, Wd, gor))
         g = r32(xr32 @ Wg32.T)      # g, u stored in bf16
         u = r32(xr32 @ Wu32.T)
         mg = mu = f32(1)
@@ -145,7 +138,7 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
             g = np.minimum(g, L)
             u = np.clip(u, -L, L)
         s = sig(g)
-        a = (mxr if quant else rnd)((g * s * u).astype(np.float64))
+        a = rnd((g * s * u).astype(np.float64))
         y = p[:, None] * r32(a.astype(f32) @ Wd32.T).astype(np.float64)   # y stored in bf16, weighted after
         da_u = go32 @ Wd32
         dprob = np.sum(a.astype(f32) * da_u, axis=1).astype(np.float64)
@@ -153,18 +146,14 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
         dg32 = da * u * (s * (f32(1) + g * (f32(1) - s))) * mg
         du32 = da * (g * s) * mu
         dg, du = rnd(dg32.astype(np.float64)), rnd(du32.astype(np.float64))
-        if quant:
-            qq = mxr(np.concatenate([dg32, du32], axis=1).astype(np.float64)).astype(f32)
-            dx = r32(qq[:, :dg.shape[1]] @ Wg32 + qq[:, dg.shape[1]:] @ Wu32).astype(np.float64)
-        else:
-            dx = r32(dg.astype(f32) @ Wg32 + du.astype(f32) @ Wu32).astype(np.float64)   # dx stored in bf16
+        dx = r32(dg.astype(f32) @ Wg32 + du.astype(f32) @ Wu32).astype(np.float64)   # dx stored in bf16
         pa = rnd((p.astype(f32)[:, None] * a.astype(f32)).astype(np.float64))
         return y, dx, dg.T @ xr, du.T @ xr, gor.T @ pa, dprob
 
     T = x.shape[0]
     w_gate = getattr(W, "shared_output_gate", None)
     gate = np.ones(T) if w_gate is None else sig(x.astype(f32) @ w_gate.astype(f32)).astype(np.float64)
-    ys, dxs, gsg, gsu, gsd, dgate = expert(x, go, gate, *W.shared(), False)
+    ys, dxs, gsg, gsu, gsd, dgate = expert(x, go, gate, *W.shared())
     grads = dict(shared_gate=gsg, shared_up=gsu, shared_down=gsd)
     if w_gate is not None:
         dz = (gate * (1 - gate)).astype(f32) * dgate.astype(f32)
@@ -177,7 +166,7 @@ def _fp32_layer(x, go, m, probs, W, k, mx=False, limit=0.0):
         rows, slots = np.nonzero(ids == e)
         if rows.size == 0:
             continue
-        y, dx, g1, g2, g3, _ = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e), mx)
+        y, dx, g1, g2, g3, _ = expert(x[rows], go[rows], pp[rows, slots], *W.routed(e))
         out[rows] += y
         dh[rows] += dx
         routed[e] = (g1, g2, g3)
@@ -225,31 +214,102 @@ def test_envelope_covers_fp32_evaluation(seed):
         assert np.median(env[n]) < 1e-3 * sc and env[n].max() < 1e-2 * sc, n
 
 
+def _mx(v):
+    from oracle import mxfp8 as MXC
+    q, sc = MXC.quantize(np.asarray(v, np.float64), axis=-1)
+    return MXC.dequantize(q, sc, axis=-1)
+
+
 @pytest.mark.parametrize("seed", [21, 22])
-def test_mxfp8_envelope_covers_fp32_evaluation(seed):
-    """mxfp8 mode: an fp32 evaluation that quantises the routed forward/dgrad
-    operands with the codec stays within the oracle's result plus its envelope."""
+def test_mxfp8_mode_quantises_exactly_the_four_gemm_operands(seed):
+    """mxfp8 mode, one routed expert by hand: the codec applied to x and a (forward
+    GEMM operands, blocks of 32 along K = H and I) and to grad_out and [dg|du]
+    (dgrad operands, along H and 2I), everything else in exact arithmetic: y from
+    the quantised a, dprob and p*a from the unquantised a, the weight gradients
+    from the unquantised dg, du; the shared expert unquantised."""
     rng = np.random.default_rng(seed)
-    T, H, I, E, k = 256, 256, 256, 3, 2
-    W = O.DenseWeights(*(rng.standard_normal(s) * 0.06 for s in
+    T, H, I, E, k = 40, 64, 64, 2, 1
+    W = O.DenseWeights(*(rng.standard_normal(s) * 0.1 for s in
+                         ((I, H), (I, H), (H, I), (E, I, H), (E, I, H), (E, H, I))))
+    x = rng.standard_normal((T, H))
+    go = rng.standard_normal((T, H))
+    m = np.zeros((T, E), bool)
+    m[:, 1] = True                                     # every token to expert 1
+    probs = rng.random((T, E))
+    out, cache = O.forward(x, probs, m, W, k, precision="mxfp8")
+    dh, dp, grads = O.backward(go, cache, W)
+    # by hand
+    p = probs[:, 1]
+    Wg, Wu, Wd = W.routed(1)
+    sg, su, sd = W.shared()
+    g, u = _mx(x) @ Wg.T, _mx(x) @ Wu.T
+    a = O.silu(g) * u
+    y = _mx(a) @ Wd.T
+    gs, us = x @ sg.T, x @ su.T
+    a_s = O.silu(gs) * us
+    np.testing.assert_allclose(out, a_s @ sd.T + p[:, None] * y, rtol=1e-12, atol=1e-12)
+    da_u = _mx(go) @ Wd
+    da = p[:, None] * da_u
+    dg = da * u * O.silu_grad(g)
+    du = da * O.silu(g)
+    q = _mx(np.concatenate([dg, du], axis=1))
+    da_s = go @ sd
+    dg_s, du_s = da_s * us * O.silu_grad(gs), da_s * O.silu(gs)
+    np.testing.assert_allclose(dh, q[:, :I] @ Wg + q[:, I:] @ Wu + dg_s @ sg + du_s @ su, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dp[:, 1], np.sum(a * da_u, axis=1), rtol=1e-12, atol=1e-12)
+    assert np.all(dp[:, 0] == 0)
+    dWg, dWu, dWd = grads["routed"][1]
+    np.testing.assert_allclose(dWg, dg.T @ x, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dWu, du.T @ x, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dWd, go.T @ (p[:, None] * a), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(grads["shared_gate"], dg_s.T @ x, rtol=1e-12, atol=1e-12)
+    # the quantisation is not a no-op here
+    assert np.max(np.abs(_mx(a) - a)) > 1e-3 * np.max(np.abs(a))
+
+
+@pytest.mark.parametrize("seed", [41, 42])
+def test_clamp_jumps_cover_an_fp32_evaluation_at_the_bounds(seed):
+    """With the clamp bound placed between the fp32 evaluation of a shared-expert
+    SwiGLU input and its exact value, an fp32 evaluation of the layer (no bf16
+    rounding) takes the other gradient mask there; its dhidden and gate/up weight
+    gradients stay within the exact oracle's plus ``clamp_jumps`` (and fp32
+    noise), while without ``clamp_jumps`` some elements would not."""
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k = 128, 128, 64, 3, 2
+    W = O.DenseWeights(*(rng.standard_normal(s) * 0.08 for s in
                          ((I, H), (I, H), (H, I), (E, I, H), (E, I, H), (E, H, I))))
     x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
     go = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).double().numpy()
     m = np.zeros((T, E), bool)
     for t in range(T):
         m[t, rng.choice(E, 2, replace=False)] = True
-    probs = rng.random((T, E)).astype(np.float32).astype(np.float64)
-    out_b, cache = O.forward(x, probs, m, W, k, precision="mxfp8")
-    dh_b, _, g_b = O.backward(go, cache, W)
-    env = O.envelope(go, cache, W)
-    out_f, dh_f, g_f = _fp32_layer(x, go, m, probs, W, k, mx=True)
-    for a, b, ev, name in ((out_f, out_b, env["out"], "out"), (dh_f, dh_b, env["dhidden"], "dhidden")):
-        slack = 1e-5 * np.abs(b).max()
-        assert np.all(np.abs(a - b) <= ev + slack), name
+    probs = rng.random((T, E))
+    # the bound between the fp32 evaluation of one shared-expert g and its exact
+    # value (the fp32 number next to the fp32 g, on the exact value's side)
+    g_exact = x @ W.sg.T
+    g32 = x.astype(np.float32) @ W.sg.astype(np.float32).T
+    ulps = np.abs(g32 - g_exact) / np.spacing(np.abs(g32))
+    t, i = np.unravel_index(np.argmax(np.where(g_exact > 0.05, ulps, 0)), g32.shape)
+    assert ulps[t, i] >= 2
+    limit = float(np.nextafter(g32[t, i], np.float32(g_exact[t, i])))
+    assert (g32[t, i] <= limit) != (g_exact[t, i] <= limit)
+    out, cache = O.forward(x, probs, m, W, k, precision="exact", swiglu_limit=limit)
+    dh, _, grads = O.backward(go, cache, W)
+    jumps = O.clamp_jumps(go, cache, W)
+    assert np.sum(jumps["dhidden"] > 0) > 0
+    _, dh_f, g_f = _fp32_layer(x, go, m, probs, W, k, limit=limit, bf16=False)
+    slack = lambda r: 2e-4 * np.abs(r).max()  # noqa: E731   fp32 noise that flips nothing
+    exceed = 0
+    for a_, b_, ev in ((dh_f, dh, jumps["dhidden"]), (g_f["shared_gate"], grads["shared_gate"], jumps["shared_gate"]),
+                       (g_f["shared_up"], grads["shared_up"], jumps["shared_up"])):
+        d = np.abs(a_ - b_)
+        assert np.all(d <= ev + slack(b_))
+        exceed += np.sum(d > slack(b_))
     for e, gs in g_f["routed"].items():
-        for j in range(3):
-            b = g_b["routed"][e][j]
-            assert np.all(np.abs(gs[j] - b) <= env["routed"][e][j] + 1e-5 * np.abs(b).max()), (e, j)
+        for j in range(2):
+            b_ = grads["routed"][e][j]
+            assert np.all(np.abs(gs[j] - b_) <= jumps["routed"][e][j] + slack(b_)), (e, j)
+    assert exceed > 0, "the fp32 evaluation took no other mask: the test would prove nothing"
 
 
 @pytest.mark.parametrize("seed", [31, 32])
