@@ -53,6 +53,21 @@ typedef enum { MOE_W_BF16 = 0, MOE_W_MXFP8 = 1 } moe_wtype;
  * main_grad.dtype selects the accumulation, one dtype for all buffers). */
 typedef enum { MOE_G_FP32 = 0, MOE_G_BF16 = 1 } moe_gtype;
 
+/* Precision of the activations between an expert's GEMMs (the pages fix the
+ * weights, BF16 or MXFP8, and the FP32 accumulator -- PR #6572, Supported
+ * configurations; PR #8210 review thread on wgrad precision -- but not this).
+ * MOE_ACT_FP32 (the default): the gate/up results g, u, the expert outputs y
+ * and the expert input gradients dx stay fp32, and every GEMM operand the layer
+ * derives (a = silu(g) u, [dg|du], p a) reaches the tensor cores as two bf16
+ * terms hi = bf16(v), lo = bf16(v - hi) whose products add in the same fp32
+ * accumulator (the GEMM runs its K range twice, once per term); results then
+ * follow the layer's exact definition to within fp32 accumulation and the final
+ * bf16 roundings of out and dhidden. MXFP8 routed GEMMs take their operands
+ * quantised as the MXFP8 method does, unsplit. MOE_ACT_BF16: g, u, y, dx and
+ * every derived operand are single bf16 values (faster: no second K pass,
+ * half the bytes; each rounding adds a relative error of up to 2^-8). */
+typedef enum { MOE_ACT_FP32 = 0, MOE_ACT_BF16 = 1 } moe_act;
+
 /* Layer shape. Routed and shared experts share `inter` (PR #6572, Supported
  * configurations: MOK limitations). hidden must be a multiple of 128, inter of 64;
  * 1 <= topk <= 32; 1 <= num_experts <= 1024.
@@ -72,6 +87,7 @@ typedef struct {
     int32_t routed_wtype; /* moe_wtype of the routed weights; shared weights are always bf16 */
     float swiglu_limit;   /* 0: no clamp; L > 0: SwiGLU input clamp (above) */
     int32_t recompute_dispatch; /* 0 or 1; see below */
+    int32_t act_precision; /* moe_act: MOE_ACT_FP32 (0, default) or MOE_ACT_BF16 */
 } moe_config;
 /* recompute_dispatch = 1 (redispatch in backward: PR #8210 review thread on
  * CUDA graphs, per-layer replay needs the saved schedule and activations to
@@ -278,9 +294,14 @@ moe_status moe_export_routing(moe_handle* h, const moe_saved* saved, int32_t* id
  * T*k must not exceed 131072 (and T not 65536): larger sizes return
  * MOE_ERR_UNSUPPORTED. The array is shared by every call and keeps the last
  * call's contents; calls whose kernels overlap on the GPU (two streams, two
- * threads) race on it. The first call on each device resolves the array's
- * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture. Asynchronous on `stream`; nothing is allocated or freed. */
+ * threads) race on it. Every call resolves the array's device address on the
+ * current device (cudaGetSymbolAddress; valid again after a device reset); the
+ * first call on a device loads the library's device code there, so make that
+ * first call before any stream capture. Cost: the per-expert ranking reads the
+ * routing map column by column (about 32 * T * E bytes of L2 traffic, 67 MB at
+ * T = 16384, E = 128), several times the forward's fused routing; it is meant
+ * for callers that cannot allocate, not for the hot path. Asynchronous on
+ * `stream`; nothing is allocated or freed. */
 moe_status moe_route_noalloc(int64_t T, int64_t E, int64_t k, const uint8_t* routing_map, const float* probs,
                              int32_t* ids, float* pp, int32_t* counts, int32_t* offsets, int32_t* perm_src,
                              int32_t* row_of, int32_t* routing_error, void* stream);

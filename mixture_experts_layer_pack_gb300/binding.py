@@ -16,6 +16,7 @@ c_int64, c_int32, c_float, c_void_p, c_size_t = (ctypes.c_int64, ctypes.c_int32,
 MOE_OK = 0
 MOE_W_BF16, MOE_W_MXFP8 = 0, 1
 MOE_G_FP32, MOE_G_BF16 = 0, 1
+MOE_ACT_FP32, MOE_ACT_BF16 = 0, 1   # activations between the expert GEMMs (include/moe.h, moe_act)
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ROUTING",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_STATE"}
 WEIGHT_NAMES = ("shared_gate", "shared_up", "shared_down", "routed_gate", "routed_up", "routed_down")
@@ -24,7 +25,7 @@ WEIGHT_NAMES = ("shared_gate", "shared_up", "shared_down", "routed_gate", "route
 class moe_config(ctypes.Structure):
     _fields_ = [("max_tokens", c_int64), ("hidden", c_int64), ("num_experts", c_int64), ("topk", c_int64),
                 ("inter", c_int64), ("routed_wtype", c_int32), ("swiglu_limit", c_float),
-                ("recompute_dispatch", c_int32)]
+                ("recompute_dispatch", c_int32), ("act_precision", c_int32)]
 
 
 class moe_wview(ctypes.Structure):
@@ -380,10 +381,11 @@ class MoELayer:
     """Holds a handle, its workspace and one saved-state block (all torch device memory)."""
 
     def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16,
-                 swiglu_limit=0.0, recompute_dispatch=False):
+                 swiglu_limit=0.0, recompute_dispatch=False, act_precision=None):
         import torch
         self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, float(swiglu_limit),
-                              int(bool(recompute_dispatch)))
+                              int(bool(recompute_dispatch)),
+                              MOE_ACT_FP32 if act_precision is None else int(act_precision))
         self.device = torch.device(device)
         ws = moe_workspace_size(self.cfg)
         sv = moe_saved_size(self.cfg)

@@ -6,9 +6,9 @@
 // (dispatch, combine) and Design > Authoritative routing maps (the backward
 // adapter scatters router-weight gradients into the dense prob tensor).
 //
-// Rows are moved as 16-byte vectors of 8 bf16; the experts' bf16 outputs and
-// input gradients are summed in fp32 in slot order, so the results are
-// deterministic and rounded to bf16 once.
+// Rows are moved as vectors of 8 elements; the experts' outputs and input
+// gradients (fp32, or bf16 with bf16 activations) are summed in fp32 in slot
+// order, so the results are deterministic and rounded to bf16 once.
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -45,40 +45,67 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     }
 }
 
-// acc += w * (8 bf16 at p)
-__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], const uint4* p, float w) {
-    const uint4 v = __ldg(p);
+// 8 elements of a row, element index 8 * i: one 16-byte vector of bf16 or two of fp32
+template <bool F32>
+struct Vec8 {
+    uint4 v[F32 ? 2 : 1];
+    __device__ __forceinline__ void load(const void* base, int64_t i) {
+        const uint4* p = reinterpret_cast<const uint4*>(base) + i * (F32 ? 2 : 1);
+        v[0] = __ldg(p);
+        if (F32) v[F32 ? 1 : 0] = __ldg(p + 1);
+    }
+    __device__ __forceinline__ void to_float(float (&f)[8]) const {
+        if (F32) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint4 w = v[F32 ? j : 0];
+                f[4 * j] = __uint_as_float(w.x);
+                f[4 * j + 1] = __uint_as_float(w.y);
+                f[4 * j + 2] = __uint_as_float(w.z);
+                f[4 * j + 3] = __uint_as_float(w.w);
+            }
+        } else {
+            unpack_bf16x2(v[0].x, f[0], f[1]);
+            unpack_bf16x2(v[0].y, f[2], f[3]);
+            unpack_bf16x2(v[0].z, f[4], f[5]);
+            unpack_bf16x2(v[0].w, f[6], f[7]);
+        }
+    }
+};
+
+// acc += w * (8 elements at vector i of base)
+template <bool F32>
+__device__ __forceinline__ void fma_x8(float (&acc)[8], const void* base, int64_t i, float w) {
+    Vec8<F32> x;
+    x.load(base, i);
     float f[8];
-    unpack_bf16x2(v.x, f[0], f[1]);
-    unpack_bf16x2(v.y, f[2], f[3]);
-    unpack_bf16x2(v.z, f[4], f[5]);
-    unpack_bf16x2(v.w, f[6], f[7]);
+    x.to_float(f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
 }
 
-// acc += 8 bf16 at p
-__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4* p) {
-    const uint4 v = __ldg(p);
+// acc += 8 elements at vector i of base
+template <bool F32>
+__device__ __forceinline__ void add_x8(float (&acc)[8], const void* base, int64_t i) {
+    Vec8<F32> x;
+    x.load(base, i);
     float f[8];
-    unpack_bf16x2(v.x, f[0], f[1]);
-    unpack_bf16x2(v.y, f[2], f[3]);
-    unpack_bf16x2(v.z, f[4], f[5]);
-    unpack_bf16x2(v.w, f[6], f[7]);
+    x.to_float(f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] += f[j];
 }
 
-// acc += sum over the valid slots s (row_of_t[s] >= 0) of pp_t[s] * (8 bf16 of row
-// row_of_t[s] at column vector v), in slot order: the indices and weights of up to
-// four slots, then their rows, are loaded before any is used
-__device__ __forceinline__ void acc_slots(float (&acc)[8], const uint4* __restrict__ rows, int vec_per_row, int v,
+// acc += sum over the valid slots s (row_of_t[s] >= 0) of pp_t[s] * (8 elements of
+// row row_of_t[s] at column vector v), in slot order: the indices and weights of up
+// to four slots, then their rows, are loaded before any is used
+template <bool F32>
+__device__ __forceinline__ void acc_slots(float (&acc)[8], const void* __restrict__ rows, int vec_per_row, int v,
                                           const int* __restrict__ row_of_t, const float* __restrict__ pp_t, int k) {
     constexpr int B = 4;
     for (int s0 = 0; s0 < k; s0 += B) {
         int r[B];
         float w[B];
-        uint4 val[B];
+        Vec8<F32> val[B];
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             r[j] = s0 + j < k ? __ldg(row_of_t + s0 + j) : -1;
@@ -86,15 +113,12 @@ __device__ __forceinline__ void acc_slots(float (&acc)[8], const uint4* __restri
         }
 #pragma unroll
         for (int j = 0; j < B; ++j)
-            if (r[j] >= 0) val[j] = __ldg(rows + int64_t(r[j]) * vec_per_row + v);
+            if (r[j] >= 0) val[j].load(rows, int64_t(r[j]) * vec_per_row + v);
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             if (r[j] < 0) continue;
             float f[8];
-            unpack_bf16x2(val[j].x, f[0], f[1]);
-            unpack_bf16x2(val[j].y, f[2], f[3]);
-            unpack_bf16x2(val[j].z, f[4], f[5]);
-            unpack_bf16x2(val[j].w, f[6], f[7]);
+            val[j].to_float(f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] = fmaf(w[j], f[q], acc[q]);
         }
@@ -107,10 +131,11 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 }
 
 // out[t] = gate[t] y_shared[t] + sum over valid slots s of pp[t,s] y[row_of[t,s]]
-// (gate 1 without a shared output gate): bf16 expert outputs, fp32 sum in slot
-// order, one bf16 rounding at the end; 8 columns per thread
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ ys, const float* __restrict__ gate,
-                                                      const uint4* __restrict__ y, const int* __restrict__ row_of,
+// (gate 1 without a shared output gate): expert outputs in fp32 (or bf16), fp32 sum
+// in slot order, one bf16 rounding at the end; 8 columns per thread
+template <bool F32>
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ ys, const float* __restrict__ gate,
+                                                      const void* __restrict__ y, const int* __restrict__ row_of,
                                                       const float* __restrict__ pp, int T, int vec_per_row, int k,
                                                       uint4* __restrict__ out) {
     pdl_wait();
@@ -120,8 +145,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         const int t = int(i / vec_per_row);
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        fma_bf16x8(acc, ys + i, gate ? __ldg(gate + t) : 1.0f);
-        acc_slots(acc, y, vec_per_row, v, row_of + int64_t(t) * k, pp + int64_t(t) * k, k);
+        fma_x8<F32>(acc, ys, i, gate ? __ldg(gate + t) : 1.0f);
+        acc_slots<F32>(acc, y, vec_per_row, v, row_of + int64_t(t) * k, pp + int64_t(t) * k, k);
         out[i] = pack_bf16x8(acc);
     }
 }
@@ -130,7 +155,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 // over valid slots of dx_perm[row_of[t,s]];
 // dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map; with
 // slot_dprobs, dprobs[t,s] of slot s instead (0 for an empty slot)
-__global__ void __launch_bounds__(256) unpermute_kernel(const uint4* __restrict__ dxs, const uint4* __restrict__ dxp,
+template <bool F32>
+__global__ void __launch_bounds__(256) unpermute_kernel(const void* __restrict__ dxs, const void* __restrict__ dxp,
                                                         const int* __restrict__ row_of, const int* __restrict__ ids,
                                                         const float* __restrict__ partial, int n_part, int T,
                                                         int vec_per_row, int k, int E, const float* __restrict__ dz,
@@ -145,7 +171,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint4* __restrict_
         const int t = int(i / vec_per_row);
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        add_bf16x8(acc, dxs + i);
+        add_x8<F32>(acc, dxs, i);
         if (dz) {
             const float d = __ldg(dz + t);
             const uint4 wv = __ldg(gate_w + v);
@@ -159,7 +185,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint4* __restrict_
         }
         for (int s = 0; s < k; ++s) {
             const int r = __ldg(row_of + int64_t(t) * k + s);
-            if (r >= 0) add_bf16x8(acc, dxp + int64_t(r) * vec_per_row + v);
+            if (r >= 0) add_x8<F32>(acc, dxp, int64_t(r) * vec_per_row + v);
         }
         dhidden[i] = pack_bf16x8(acc);
     }
@@ -211,27 +237,27 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, co
     return e;
 }
 
-cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __nv_bfloat16* y, const int* row_of,
+cudaError_t launch_combine(const void* ys, const float* gate, const void* y, bool f32, const int* row_of,
                            const float* pp, int T, int H, int k, __nv_bfloat16* out, int num_sms, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
-    const cudaError_t e = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, reinterpret_cast<const uint4*>(ys),
-                                     gate, reinterpret_cast<const uint4*>(y), row_of, pp, T, H / 8, k,
-                                     reinterpret_cast<uint4*>(out));
+    const cudaError_t e =
+        launch_pdl(f32 ? combine_kernel<true> : combine_kernel<false>, dim3(grid), dim3(256), 0, st, ys, gate, y,
+                   row_of, pp, T, H / 8, k, reinterpret_cast<uint4*>(out));
     count_launch();
     return e;
 }
 
-cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,
+cudaError_t launch_unpermute(const void* dxs, const void* dxp, bool f32, const int* row_of, const int* ids,
                              const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
                              const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, bool slot_dprobs,
                              int num_sms, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int grid = grid_for(int64_t(T) * (H / 8), 256, num_sms);
-    const cudaError_t e = launch_pdl(unpermute_kernel, dim3(grid), dim3(256), 0, st,
-                                     reinterpret_cast<const uint4*>(dxs), reinterpret_cast<const uint4*>(dxp), row_of,
-                                     ids, partial, n_part, T, H / 8, k, E, dz, reinterpret_cast<const uint4*>(gate_w),
-                                     reinterpret_cast<uint4*>(dhidden), dprobs, slot_dprobs ? 1 : 0);
+    const cudaError_t e = launch_pdl(f32 ? unpermute_kernel<true> : unpermute_kernel<false>, dim3(grid), dim3(256), 0,
+                                     st, dxs, dxp, row_of, ids, partial, n_part, T, H / 8, k, E, dz,
+                                     reinterpret_cast<const uint4*>(gate_w), reinterpret_cast<uint4*>(dhidden), dprobs,
+                                     slot_dprobs ? 1 : 0);
     count_launch();
     return e;
 }

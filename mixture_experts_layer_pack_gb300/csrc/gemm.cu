@@ -42,16 +42,22 @@ constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
 constexpr uint32_t kStageTileBytes = 32 * 32 * 4;  // fp32 staging box of one epilogue warp (32 rows x 32 cols)
 constexpr int kRing = 4;  // weight gradient: depth of the claimed-tile ring
 
-template <int OP, int BN>
+// SPLIT (the down projection, the dgrad through gate/up): the A operand comes as
+// hi + lo bf16 terms and its lo tile rides in the same stage, so the B tile is
+// loaded once for both products
+template <int OP, int BN, bool SPLIT = false>
 struct Cfg {
+    static_assert(!SPLIT || OP == OP_FWD_DOWN || OP == OP_BWD_GU, "paired lo tiles: A operand of fprop/dgrad");
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = BN * kBK * 2;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t L_BYTES = SPLIT ? A_BYTES : 0;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + L_BYTES;
     // the weight-gradient epilogue double-buffers its main_grad boxes, so it
     // gives up operand stages (its K per tile is one expert's short segment)
     static constexpr int BUFS = (OP == OP_WGRAD) ? 2 : 1;
-    static constexpr int STAGES = (OP == OP_WGRAD) ? ((BN == 256) ? 3 : (BN == 128 ? 5 : 6))
-                                                   : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+    static constexpr int STAGES =
+        (OP == OP_WGRAD) ? ((BN == 256) ? 3 : (BN == 128 ? 5 : 6))
+                         : (SPLIT ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)));
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
     static constexpr uint32_t STAGING = kEpiWarps * BUFS * kStageTileBytes;
     static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING + 1024 + 512;
@@ -76,8 +82,12 @@ __host__ __device__ constexpr uint32_t instr_desc() {
            (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
 }
 
+// Weight gradient with a split operand: the K range runs twice, the first
+// kb_half blocks with the hi terms and the next kb_half with the lo terms (the
+// other operand's blocks load again), into one accumulator. (The forward and
+// dgrad GEMMs carry the lo tile in the same stage instead: SPLIT builds.)
 struct Tile {
-    int mt, nt, e, k_lo, kblocks;
+    int mt, nt, e, k_lo, kblocks, kb_half;
 };
 
 template <int OP>
@@ -93,12 +103,15 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a) {
         const int hi = a.seg_off ? a.seg_off[t.e + 1] : a.seg_len;
         t.k_lo = lo;
         t.kblocks = (hi - lo + kBK - 1) / kBK;
+        t.kb_half = a.split ? t.kblocks : INT_MAX;
+        if (a.split) t.kblocks *= 2;
     } else {
         t.mt = tile / a.n_tiles;
         t.nt = tile - t.mt * a.n_tiles;
         t.e = a.mtile_expert ? a.mtile_expert[t.mt] : 0;
         t.k_lo = 0;
         t.kblocks = a.k_blocks;
+        t.kb_half = INT_MAX;
     }
     return t;
 }
@@ -115,20 +128,33 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     return true;
 }
 
-template <int OP, int BN>
-__device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, uint8_t* sb, const CUtensorMap* mA,
-                                            const CUtensorMap* mB0, const CUtensorMap* mB1, const CUtensorMap* mS0,
-                                            const CUtensorMap* mS1, uint64_t* bar, const GemmArgs& a) {
-    const int k0 = kb * kBK;
+// sl: the stage's lo tile of the split operand (SPLIT builds; a.split 1: A, 2: B)
+// mG: group 0's token rows (a.g0_operand 1: in place of A, 2: of B), at the same
+// row coordinates (group 0's rows are tokens 0 .. T-1, then zero rows)
+template <int OP, int BN, bool SPLIT>
+__device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, uint8_t* sb, uint8_t* sl,
+                                            const CUtensorMap* mA, const CUtensorMap* mB0, const CUtensorMap* mB1,
+                                            const CUtensorMap* mS0, const CUtensorMap* mS1, const CUtensorMap* mL,
+                                            const CUtensorMap* mG, uint64_t* bar, const GemmArgs& a) {
+    const bool g0 = a.g0_operand && a.group0_shared && t.e == 0;
+    if (g0 && a.g0_operand == 1) mA = mG;
     if (OP == OP_WGRAD) {
-        const int krow = t.k_lo + k0;
+        if (g0 && a.g0_operand == 2) mB0 = mG;
+        if (kb >= t.kb_half) {  // the second pass of a split weight gradient: the lo terms
+            kb -= t.kb_half;
+            if (a.split == 1) mA = mL;
+            else mB0 = mL;
+        }
+        const int krow = t.k_lo + kb * kBK;
 #pragma unroll
         for (int c = 0; c < kBM / 64; ++c) tma_load_2d(sa + c * kMnChunkBytes, mA, bar, t.mt * kBM + 64 * c, krow);
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * kMnChunkBytes, mB0, bar, t.nt * BN + 64 * c, krow);
         return;
     }
+    const int k0 = kb * kBK;
     tma_load_2d(sa, mA, bar, k0, t.mt * kBM);
+    if (SPLIT) tma_load_2d(sl, mL, bar, k0, t.mt * kBM);
     // an expert's weights: group 0's own maps when it is the shared expert, else
     // routed expert re's descriptor (z = 0) from a per-expert table or the 3D map at z = re
     const bool sh = a.group0_shared && t.e == 0;
@@ -188,6 +214,20 @@ __device__ __forceinline__ uint32_t mx_quant_lane4(const float (&v)[4], uint32_t
     return e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
 }
 
+// Stores 4 consecutive values as bf16 hi = bf16(v) and, where lo is given,
+// lo = bf16(v - hi) (v - hi is exact in fp32): hi + lo carries 16 significant bits
+__device__ __forceinline__ void store_split4(__nv_bfloat16* hi, __nv_bfloat16* lo, const float (&v)[4]) {
+    const uint32_t h0 = pack_bf16x2(v[0], v[1]), h1 = pack_bf16x2(v[2], v[3]);
+    *reinterpret_cast<uint2*>(hi) = make_uint2(h0, h1);
+    if (lo) {
+        float r[4];
+        unpack_bf16x2(h0, r[0], r[1]);
+        unpack_bf16x2(h1, r[2], r[3]);
+        *reinterpret_cast<uint2*>(lo) =
+            make_uint2(pack_bf16x2(v[0] - r[0], v[1] - r[1]), pack_bf16x2(v[2] - r[2], v[3] - r[3]));
+    }
+}
+
 template <int OP, int BN, bool MX = false, bool CLAMP = false>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int q, int half, const GemmArgs& a,
                                               float* staging) {
@@ -218,6 +258,41 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             for (int i = 0; i < 8; ++i) uv[i] = staged(staging, i);
             __syncwarp();
             const int col = j0 + c * 32 + sub_col;
+            if (a.outf) {
+                // fp32 activations: g, u are kept as accumulated, a is computed from them
+                // and leaves as two bf16 terms (the down projection's split operand)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = m_base + i * 4 + sub_row;
+                    const float4 g4 = gv[i], u4 = uv[i];
+                    float gc[4] = {g4.x, g4.y, g4.z, g4.w}, uc[4] = {u4.x, u4.y, u4.z, u4.w};
+                    if (CLAMP) {
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) {
+                            gc[z] = fminf(gc[z], a.swiglu_limit);
+                            uc[z] = fminf(fmaxf(uc[z], -a.swiglu_limit), a.swiglu_limit);
+                        }
+                    }
+                    float av[4];
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) av[z] = gc[z] * sigmoidf_(gc[z]) * uc[z];
+                    if (MX) {  // the routed down projection's operand: a quantised along I
+                        uint32_t code;
+                        const uint32_t qv = mx_quant_lane4(av, code);
+                        if (row < a.rows_valid) {
+                            *reinterpret_cast<uint32_t*>(a.q_out + int64_t(row) * a.ld_q + col) = qv;
+                            if ((lane & 7) == 0) a.q_sf[sf_atom_offset(row, col >> 5, a.q_kblocks)] = uint8_t(code);
+                        }
+                    }
+                    if (row >= a.rows_valid) continue;
+                    float* gu = a.outf + int64_t(row) * a.ld_outf;
+                    *reinterpret_cast<float4*>(gu + col) = g4;
+                    *reinterpret_cast<float4*>(gu + a.inter + col) = u4;
+                    if (a.out0) store_split4(a.out0 + int64_t(row) * a.ld_out0 + col,
+                                             a.out0lo ? a.out0lo + int64_t(row) * a.ld_out0lo + col : nullptr, av);
+                }
+                continue;
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = m_base + i * 4 + sub_row;
@@ -273,8 +348,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                 const float4 x = staged(staging, i);
                 const int row = m_base + i * 4 + sub_row;
                 if (row >= a.rows_valid) continue;
-                *reinterpret_cast<uint2*>(a.outh + int64_t(row) * a.ld_outh + col) =
-                    make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+                if (a.outf)
+                    *reinterpret_cast<float4*>(a.outf + int64_t(row) * a.ld_outf + col) = x;
+                else
+                    *reinterpret_cast<uint2*>(a.outh + int64_t(row) * a.ld_outh + col) =
+                        make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
             }
             __syncwarp();
         }
@@ -289,6 +367,77 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             tmem_ld32(t_row + c * 32, d);
             stage_chunk(staging, d);
             const int col = t.nt * BN + c * 32 + sub_col;
+            if (a.inf) {
+                // fp32 activations: g, u load in fp32 and a is recomputed from them (the
+                // value the forward's down projection took as hi + lo terms); the dprob
+                // partial, p * a and the SwiGLU gradients come from these fp32 values, and
+                // [dg|du] and p * a leave as hi + lo bf16 terms
+                float4 gq[8], uq[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = m_base + i * 4 + sub_row;
+                    if (row < a.rows_valid) {
+                        const float* gu = a.inf + int64_t(row) * a.ld_inf;
+                        gq[i] = __ldg(reinterpret_cast<const float4*>(gu + col));
+                        uq[i] = __ldg(reinterpret_cast<const float4*>(gu + a.inter + col));
+                    } else {
+                        gq[i] = uq[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r_local = i * 4 + sub_row;
+                    const float p = __shfl_sync(0xffffffffu, lane_p, r_local);
+                    const float4 d4 = staged(staging, i);
+                    const int row = m_base + r_local;
+                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    const float gv[4] = {gq[i].x, gq[i].y, gq[i].z, gq[i].w};
+                    const float uv[4] = {uq[i].x, uq[i].y, uq[i].z, uq[i].w};
+                    float dg[4], du[4], ap[4];
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) {
+                        float g = gv[z], u = uv[z], mg = 1.0f, mu = 1.0f;
+                        if (CLAMP) {
+                            const float L = a.swiglu_limit;
+                            mg = g <= L ? 1.0f : 0.0f;
+                            mu = (u >= -L && u <= L) ? 1.0f : 0.0f;
+                            g = fminf(g, L);
+                            u = fminf(fmaxf(u, -L), L);
+                        }
+                        const float sg = sigmoidf_(g);
+                        const float av = g * sg * u;
+                        part[i] = fmaf(av, dv[z], part[i]);
+                        const float da = p * dv[z];
+                        dg[z] = da * u * (sg * (1.0f + g * (1.0f - sg))) * mg;
+                        du[z] = da * (g * sg) * mu;
+                        ap[z] = p * av;
+                    }
+                    if (MX) {
+                        uint32_t cg, cu;
+                        const uint32_t qg = mx_quant_lane4(dg, cg);
+                        const uint32_t qu = mx_quant_lane4(du, cu);
+                        if (row < a.rows_valid) {
+                            uint8_t* qo = a.q_out + int64_t(row) * a.ld_q;
+                            *reinterpret_cast<uint32_t*>(qo + col) = qg;
+                            *reinterpret_cast<uint32_t*>(qo + a.inter + col) = qu;
+                            if ((lane & 7) == 0) {
+                                a.q_sf[sf_atom_offset(row, col >> 5, a.q_kblocks)] = uint8_t(cg);
+                                a.q_sf[sf_atom_offset(row, (a.inter + col) >> 5, a.q_kblocks)] = uint8_t(cu);
+                            }
+                        }
+                    }
+                    if (row >= a.rows_valid) continue;
+                    const int64_t o = int64_t(row) * a.ld_out0 + col;
+                    const int64_t ol = int64_t(row) * a.ld_out0lo + col;
+                    store_split4(a.out0 + o, a.out0lo ? a.out0lo + ol : nullptr, dg);
+                    store_split4(a.out0 + o + a.inter, a.out0lo ? a.out0lo + ol + a.inter : nullptr, du);
+                    if (a.out1)
+                        store_split4(a.out1 + int64_t(row) * a.ld_out1 + col,
+                                     a.out1lo ? a.out1lo + int64_t(row) * a.ld_out1lo + col : nullptr, ap);
+                }
+                __syncwarp();
+                continue;
+            }
             // load phase: every input of the chunk is requested before any result
             // is stored, so the eight row steps share one memory latency
             uint2 aw[8], gw[8], uw[8];
@@ -544,13 +693,14 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
     __syncwarp();
 }
 
-template <int OP, int BN, bool CLAMP>
+template <int OP, int BN, bool CLAMP, bool SPLIT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
                     const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmS0,
-                    const __grid_constant__ CUtensorMap tmS1, const GemmArgs args) {
-    using C = Cfg<OP, BN>;
+                    const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmL,
+                    const __grid_constant__ CUtensorMap tmG, const GemmArgs args) {
+    using C = Cfg<OP, BN, SPLIT>;
     constexpr bool A_MN = (OP == OP_WGRAD);
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD);
     constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN>();
@@ -601,6 +751,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_prefetch_map(&tmC0);
             tma_prefetch_map(&tmC1);
         }
+        if (SPLIT) tma_prefetch_map(&tmL);
+        if (args.g0_operand) tma_prefetch_map(&tmG);
         if (args.group0_shared) {
             tma_prefetch_map(&tmS0);
             if (OP == OP_FWD_GU || OP == OP_BWD_GU || OP == OP_WGRAD) tma_prefetch_map(&tmS1);
@@ -654,8 +806,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    issue_loads<OP, BN>(t, kb, sa, sa + C::A_BYTES, &tmA, &tmB0, &tmB1, &tmS0, &tmS1, &full[stage],
-                                        args);
+                    issue_loads<OP, BN, SPLIT>(t, kb, sa, sa + C::A_BYTES, sa + C::A_BYTES + C::B_BYTES, &tmA, &tmB0,
+                                               &tmB1, &tmS0, &tmS1, &tmL, &tmG, &full[stage], args);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -713,6 +865,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 2048, kMnChunkBytes, kSwizzleAtom)
                                                  : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
                         mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    if (SPLIT) {  // the lo terms of A times the same B, into the same accumulator
+                        const uint32_t l_addr = b_addr + C::B_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint64_t ad = smem_desc(l_addr + kk * 32, 16, kSwizzleAtom);
+                            const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 2048, kMnChunkBytes, kSwizzleAtom)
+                                                     : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
+                            mma_bf16(d_tmem, ad, bd, IDESC, 1u);
+                        }
                     }
                     mma_commit(&empty[stage]);
                     if (++stage == STAGES) {
@@ -1016,29 +1178,41 @@ cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaSt
     return e;
 }
 
-template <int OP, int BN, bool CLAMP>
+template <int OP, int BN, bool CLAMP, bool SPLIT>
 cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     static bool attr_set = false;
-    auto kern = moe_gemm_kernel<OP, BN, CLAMP>;
+    using C = Cfg<OP, BN, SPLIT>;
+    static_assert(C::SMEM <= 227 * 1024, "shared memory per CTA");
+    auto kern = moe_gemm_kernel<OP, BN, CLAMP, SPLIT>;
     if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<OP, BN>::SMEM));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const cudaError_t e =
-        launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg<OP, BN>::SMEM, st, m.a, m.b0, m.b1, m.c0, m.c1, m.s0,
-                   m.s1, a);
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), C::SMEM, st, m.a, m.b0, m.b1, m.c0, m.c1,
+                                     m.s0, m.s1, m.lo, m.g0, a);
     count_launch();
     return e;
 }
 
+// the split (paired-stage) builds exist for the down projection and the dgrad
+// through gate/up; a split weight gradient runs its K range twice in the plain build
 template <int OP, bool CLAMP = false>
 cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+    constexpr bool CAN_SPLIT = OP == OP_FWD_DOWN || OP == OP_BWD_GU;
+    if (a.split && !CAN_SPLIT && OP != OP_WGRAD) return cudaErrorInvalidValue;
+    if (CAN_SPLIT && a.split) {
+        switch (bn) {
+            case 256: return launch_one<OP, 256, CLAMP, CAN_SPLIT>(m, a, grid, st);
+            case 128: return launch_one<OP, 128, CLAMP, CAN_SPLIT>(m, a, grid, st);
+            case 64: return launch_one<OP, 64, CLAMP, CAN_SPLIT>(m, a, grid, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (bn) {
-        case 256: return launch_one<OP, 256, CLAMP>(m, a, grid, st);
-        case 128: return launch_one<OP, 128, CLAMP>(m, a, grid, st);
-        case 64: return launch_one<OP, 64, CLAMP>(m, a, grid, st);
+        case 256: return launch_one<OP, 256, CLAMP, false>(m, a, grid, st);
+        case 128: return launch_one<OP, 128, CLAMP, false>(m, a, grid, st);
+        case 64: return launch_one<OP, 64, CLAMP, false>(m, a, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -52,6 +52,19 @@ struct GemmArgs {
     int64_t ld_in0;
     const __nv_bfloat16* inh;   // [g|u]
     int64_t ld_inh;
+    // fp32 activations (the default precision): results kept in fp32 and the
+    // derived GEMM operands given as two bf16 terms, hi = bf16(v), lo = bf16(v - hi)
+    float* outf;                // fp32 results (replace outh): FWD_GU [g|u], FWD_DOWN y, BWD_GU dx
+    int64_t ld_outf;
+    const float* inf;           // BWD_DOWN: fp32 [g|u], a recomputed from them (replaces in0, inh)
+    int64_t ld_inf;
+    __nv_bfloat16* out0lo;      // lo terms of out0 (a, [dg|du])
+    int64_t ld_out0lo;
+    __nv_bfloat16* out1lo;      // lo terms of out1 (p * a)
+    int64_t ld_out1lo;
+    int split;                  // 1: A, 2: B operand comes as hi (its map) + lo (map lo) terms
+    int g0_operand;             // group 0 (the shared expert) reads its token rows through map g0:
+                                // 1: the A operand, 2: the B operand (0: the row buffer like the others)
     const float* row_scale;     // BWD_DOWN: per-row prob (null: 1)
     float* partial;             // per row: n_tiles * kEpiHalves partial dot products (null: skip)
     int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
@@ -82,6 +95,8 @@ struct GemmArgs {
 
 struct GemmMaps {
     CUtensorMap a, b0, b1;
+    CUtensorMap lo;      // split operand: the lo terms of A (split 1) or B (split 2), same box as its hi map
+    CUtensorMap g0;      // group 0's token rows (hidden or grad_out, T rows; rows past T read as zeros)
     CUtensorMap c0, c1;  // OP_WGRAD: main_grad destinations (rows < m_split, rows >= m_split)
     // group0_shared: the shared expert's b0, b1 (OP 0..3) or c0, c1 (OP_WGRAD)
     CUtensorMap s0, s1;
@@ -120,8 +135,10 @@ cudaError_t launch_route_rank(const uint8_t* map, const int* ids, int T, int E, 
                               cudaStream_t st);
 // shared_rows > 0: also writes the shared expert's rows, which sit at rows
 // [-shared_rows, 0) of perm_src, pp_perm and x_perm (no MXFP8 copy)
+// copy_shared: also copy the shared rows' hidden rows (else only their source and scale)
 cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* chunk_base,
                                const int* counts, const int* offs_pad, int T, int E, int k, int shared_rows,
+                               bool copy_shared,
                                const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
                                __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st);
 // tab0 / tab1: device arrays of E source pointers, expert e's scales at tab[e]
@@ -138,9 +155,10 @@ cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* 
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* n_dev, int row0,
                                int max_rows, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms,
                                cudaStream_t st);
-cudaError_t launch_combine(const __nv_bfloat16* ys, const float* gate, const __nv_bfloat16* y, const int* row_of,
+// ys, y (and dxs, dxp): fp32 rows when f32, else bf16
+cudaError_t launch_combine(const void* ys, const float* gate, const void* y, bool f32, const int* row_of,
                            const float* pp, int T, int H, int k, __nv_bfloat16* out, int num_sms, cudaStream_t st);
-cudaError_t launch_unpermute(const __nv_bfloat16* dxs, const __nv_bfloat16* dxp, const int* row_of, const int* ids,
+cudaError_t launch_unpermute(const void* dxs, const void* dxp, bool f32, const int* row_of, const int* ids,
                              const float* partial, int n_part, int T, int H, int k, int E, const float* dz,
                              const __nv_bfloat16* gate_w, __nv_bfloat16* dhidden, float* dprobs, bool slot_dprobs,
                              int num_sms, cudaStream_t st);

@@ -43,6 +43,7 @@ struct Shape {
     int n_part_s;     // the same for the shared expert's (always BF16) dgrad-down GEMM
     bool mx;          // routed weights MXFP8: block-scaled fprop and dgrad GEMMs
     bool recompute;   // recompute_dispatch: the backward redoes placement and gate/up
+    bool act32;       // MOE_ACT_FP32: fp32 g|u, y, dx; derived GEMM operands as hi + lo bf16 terms
     float limit;      // swiglu_limit (0: none)
 };
 
@@ -65,7 +66,9 @@ moe_status check_config(const moe_config* c, Shape* s) {
         return MOE_ERR_INVALID_ARG;
     if (!(c->swiglu_limit >= 0.0f) || !std::isfinite(c->swiglu_limit)) return MOE_ERR_INVALID_ARG;
     if (c->recompute_dispatch != 0 && c->recompute_dispatch != 1) return MOE_ERR_INVALID_ARG;
+    if (c->act_precision != MOE_ACT_FP32 && c->act_precision != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
     s->recompute = c->recompute_dispatch != 0;
+    s->act32 = c->act_precision == MOE_ACT_FP32;
     s->limit = c->swiglu_limit;
     if (c->routed_wtype != MOE_W_BF16 && c->routed_wtype != MOE_W_MXFP8) return MOE_ERR_UNSUPPORTED;
     s->mx = c->routed_wtype == MOE_W_MXFP8;
@@ -99,8 +102,11 @@ moe_status check_config(const moe_config* c, Shape* s) {
 struct Workspace {
     int* status;
     int* tile_counters;  // one per weight-gradient launch of a backward (dynamic tile scheduling)
-    __nv_bfloat16 *go_all, *dgdu_all, *ap_all;  // grad_out rows, [dg|du], prob (or gate) * a
-    __nv_bfloat16* yx_all;  // forward: y; backward: dx
+    __nv_bfloat16 *go_all, *dgdu_all, *ap_all;  // grad_out rows, [dg|du] (hi terms), prob (or gate) * a (hi)
+    __nv_bfloat16* yx_all;  // bf16 activations -- forward: y; backward: dx
+    float* yx32;            // fp32 activations -- forward: y; backward: dx
+    // fp32 activations: lo terms of a (forward only), [dg|du] and prob * a
+    __nv_bfloat16 *alo_all, *dgdulo_all, *aplo_all;
     float* partial_all;     // dgrad-down partial dot products (n_part per row)
     // MXFP8 routed weights: the shared expert's own dgrad-down partials (n_part_s per row)
     float* partial_s;
@@ -111,6 +117,7 @@ struct Workspace {
     // recompute_dispatch: the GEMM input rows, a and [g|u] (and their MXFP8 copies)
     // live here, shared by every saved state of the handle, instead of in each
     __nv_bfloat16 *x_all, *a_all, *gu_all;
+    float* gu32;
     uint8_t *x_q, *x_sf, *a_q, *a_sf;
     // MXFP8 only: quantised backward operands and the swizzled weight scales
     uint8_t *go_q, *go_sf, *dgdu_q, *dgdu_sf;
@@ -129,7 +136,8 @@ struct SavedBufs {
     int* perm_src_all;     // source token of each row (-1: zero row)
     float* pp;
     float* pp_all;         // per row: the shared output gate (1 without one), the route's prob, 0 for padding
-    __nv_bfloat16 *x_all, *a_all, *gu_all;  // GEMM input rows, SwiGLU output a, bf16 [g|u] (kept for backward)
+    __nv_bfloat16 *x_all, *a_all, *gu_all;  // GEMM input rows, SwiGLU output a (hi terms), bf16 [g|u]
+    float* gu32;                            // fp32 activations: [g|u] (kept for backward), gu_all unused
     uint8_t *x_q, *x_sf, *a_q, *a_sf;  // MXFP8 only: routed rows (relative to row R0)
 };
 
@@ -139,6 +147,8 @@ struct Views {
     int* perm_src;
     float* pp_perm;
     __nv_bfloat16 *x_perm, *a, *gu, *go_perm, *dgdu, *ap, *yx;
+    float *gu32, *yx32;
+    __nv_bfloat16 *dgdulo, *aplo;
     float* partial;
 };
 
@@ -153,18 +163,31 @@ size_t carve_workspace(const Shape& s, uint8_t* base, Workspace* w) {
     w->go_all = c.take<__nv_bfloat16>(ra * s.H);
     w->dgdu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
     w->ap_all = c.take<__nv_bfloat16>(ra * s.I);
-    w->yx_all = c.take<__nv_bfloat16>(ra * s.H);
+    w->yx_all = w->alo_all = w->dgdulo_all = w->aplo_all = nullptr;
+    w->yx32 = nullptr;
+    if (s.act32) {
+        w->yx32 = c.take<float>(ra * s.H);
+        w->alo_all = c.take<__nv_bfloat16>(ra * s.I);
+        w->dgdulo_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
+        w->aplo_all = c.take<__nv_bfloat16>(ra * s.I);
+    } else {
+        w->yx_all = c.take<__nv_bfloat16>(ra * s.H);
+    }
     w->partial_all = c.take<float>(ra * s.n_part);
     w->partial_s = s.mx ? c.take<float>(size_t(s.Tmax) * s.n_part_s) : nullptr;
     w->dz = c.take<float>(size_t(s.Tmax));
     w->gpart = c.take<float>(size_t((s.Tmax + kGateChunk - 1) / kGateChunk) * s.H);
     w->tabs = c.take<CUtensorMap>(size_t(kTables) * s.E);
     w->x_all = w->a_all = w->gu_all = nullptr;
+    w->gu32 = nullptr;
     w->x_q = w->x_sf = w->a_q = w->a_sf = nullptr;
     if (s.recompute) {
         w->x_all = c.take<__nv_bfloat16>(ra * s.H);
         w->a_all = c.take<__nv_bfloat16>(ra * s.I);
-        w->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
+        if (s.act32)
+            w->gu32 = c.take<float>(ra * 2 * s.I);
+        else
+            w->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
         if (s.mx) {
             w->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
             w->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -209,11 +232,15 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
     b->perm_src_all = c.take<int>(ra);
     b->pp_all = c.take<float>(ra);
     b->x_all = b->a_all = b->gu_all = nullptr;  // recompute_dispatch: the workspace's (moe_saved_create)
+    b->gu32 = nullptr;
     b->x_q = b->x_sf = b->a_q = b->a_sf = nullptr;
     if (!s.recompute) {
         b->x_all = c.take<__nv_bfloat16>(ra * s.H);
         b->a_all = c.take<__nv_bfloat16>(ra * s.I);
-        b->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
+        if (s.act32)
+            b->gu32 = c.take<float>(ra * 2 * s.I);
+        else
+            b->gu_all = c.take<__nv_bfloat16>(ra * 2 * s.I);
         if (s.mx) {
             b->x_q = c.take<uint8_t>(size_t(s.rows) * s.H);
             b->x_sf = c.take<uint8_t>(sf_atoms_bytes(s.rows, s.H));
@@ -232,11 +259,15 @@ Views views_of(const Shape& s, const SavedBufs& b, const Workspace& w, int64_t T
     v.pp_perm = b.pp_all + r;
     v.x_perm = b.x_all + r * s.H;
     v.a = b.a_all + r * s.I;
-    v.gu = b.gu_all + r * 2 * s.I;
+    v.gu = s.act32 ? nullptr : b.gu_all + r * 2 * s.I;
+    v.gu32 = s.act32 ? b.gu32 + r * 2 * s.I : nullptr;
     v.go_perm = w.go_all + r * s.H;
     v.dgdu = w.dgdu_all + r * 2 * s.I;
     v.ap = w.ap_all + r * s.I;
-    v.yx = w.yx_all + r * s.H;
+    v.yx = s.act32 ? nullptr : w.yx_all + r * s.H;
+    v.yx32 = s.act32 ? w.yx32 + r * s.H : nullptr;
+    v.dgdulo = s.act32 ? w.dgdulo_all + r * 2 * s.I : nullptr;
+    v.aplo = s.act32 ? w.aplo_all + r * s.I : nullptr;
     v.partial = w.partial_all + r * s.n_part;
     return v;
 }
@@ -356,6 +387,58 @@ GemmArgs base_args(int* status, const Shape& s) {
 }
 
 int grid_of(int64_t tiles, int sms) { return int(tiles < sms ? tiles : sms); }
+
+// Gate/up epilogue outputs: a (hi terms; with fp32 activations also the lo terms,
+// where a_lo is given) and [g|u] (bf16, or fp32 with fp32 activations).
+void set_gu_outputs(const Shape& s, GemmArgs& a, __nv_bfloat16* a_hi, __nv_bfloat16* a_lo, __nv_bfloat16* gu,
+                    float* gu32) {
+    a.out0 = a_hi;
+    a.ld_out0 = s.I;
+    if (s.act32) {
+        a.outf = gu32;
+        a.ld_outf = 2 * s.I;
+        a.out0lo = a_lo;
+        a.ld_out0lo = s.I;
+    } else {
+        a.outh = gu;
+        a.ld_outh = 2 * s.I;
+    }
+}
+
+// Down / dgrad-gate-up epilogue output rows of width H: y or dx
+void set_row_output(const Shape& s, GemmArgs& a, __nv_bfloat16* bf, float* f32) {
+    if (s.act32) {
+        a.outf = f32;
+        a.ld_outf = s.H;
+    } else {
+        a.outh = bf;
+        a.ld_outh = s.H;
+    }
+}
+
+// Dgrad-down epilogue: its inputs (bf16 a and [g|u], or fp32 [g|u]) and outputs
+// ([dg|du] and, where ap is given, scale * a; each with lo terms under fp32 activations)
+void set_bwd_down_io(const Shape& s, GemmArgs& a, const __nv_bfloat16* a_in, const __nv_bfloat16* gu,
+                     const float* gu32, __nv_bfloat16* dgdu, __nv_bfloat16* dgdu_lo, __nv_bfloat16* ap,
+                     __nv_bfloat16* ap_lo) {
+    if (s.act32) {
+        a.inf = gu32;
+        a.ld_inf = 2 * s.I;
+        a.out0lo = dgdu_lo;
+        a.ld_out0lo = 2 * s.I;
+        a.out1lo = ap ? ap_lo : nullptr;
+        a.ld_out1lo = s.I;
+    } else {
+        a.in0 = a_in;
+        a.ld_in0 = s.I;
+        a.inh = gu;
+        a.ld_inh = 2 * s.I;
+    }
+    a.out0 = dgdu;
+    a.ld_out0 = 2 * s.I;
+    a.out1 = ap;
+    a.ld_out1 = s.I;
+}
 
 }  // namespace
 
@@ -607,6 +690,7 @@ moe_status moe_saved_create(moe_handle* h, void* memory, size_t bytes, moe_saved
         sv->b.x_all = h->ws.x_all;
         sv->b.a_all = h->ws.a_all;
         sv->b.gu_all = h->ws.gu_all;
+        sv->b.gu32 = h->ws.gu32;
         sv->b.x_q = h->ws.x_q;
         sv->b.x_sf = h->ws.x_sf;
         sv->b.a_q = h->ws.a_q;
@@ -646,7 +730,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
     const Views v = views_of(s, b, ws, T);
     const int rows_all = v.R0 + rows;
     { Timed tm_(h, MOE_K_ROUTE_PLACE, st);
-    MOE_CU(launch_route_place(b.ids, b.pp, b.rank, b.hist, b.counts, b.offs_pad, Ti, E, k, mx ? 0 : v.R0,
+    MOE_CU(launch_route_place(b.ids, b.pp, b.rank, b.hist, b.counts, b.offs_pad, Ti, E, k, mx ? 0 : v.R0, false,
                               static_cast<const __nv_bfloat16*>(hidden), H, v.perm_src, v.pp_perm, b.row_of, v.x_perm,
                               mx ? b.x_q : nullptr, mx ? b.x_sf : nullptr, st)); }
 
@@ -670,10 +754,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         a.n_tiles = 2 * I / kMxBN;
         a.k_blocks = H / kMxBK;
         a.gate_up_split = I;
-        a.out0 = v.a;
-        a.ld_out0 = I;
-        a.outh = v.gu;
-        a.ld_outh = 2 * I;
+        set_gu_outputs(s, a, v.a, nullptr, v.gu, v.gu32);
         a.q_out = b.a_q;
         a.ld_q = I;
         a.q_sf = b.a_sf;
@@ -688,7 +769,10 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
     } else {  // shared expert (group 0) and routed experts in one launch
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
-        if (!map_kmajor(&m.a, b.x_all, rows_all, H, H)) return MOE_ERR_INVALID_ARG;
+        // the shared expert's rows are hidden itself (rows past T read as zeros)
+        if (!map_kmajor(&m.a, b.x_all, rows_all, H, H) || !map_kmajor(&m.g0, hidden, Ti, H, H))
+            return MOE_ERR_INVALID_ARG;
+        a.g0_operand = 1;
         MOE_TRY(routed_map(h, TB_FWD_GU_G, w->routed_gate, I, H, bn / 2, st, &m.b0, &a.b0_tab));
         MOE_TRY(routed_map(h, TB_FWD_GU_U, w->routed_up, I, H, bn / 2, st, &m.b1, &a.b1_tab));
         if (!map_weight(&m.s0, w->shared_gate, 1, I, H, 64, bn / 2) ||
@@ -701,10 +785,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         a.n_tiles = 2 * I / bn;
         a.k_blocks = H / kBK;
         a.gate_up_split = I;
-        a.out0 = b.a_all;
-        a.ld_out0 = I;
-        a.outh = b.gu_all;
-        a.ld_outh = 2 * I;
+        set_gu_outputs(s, a, b.a_all, ws.alo_all, b.gu_all, b.gu32);
         Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -719,10 +800,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         a.k_blocks = H / kBK;
         a.rows_valid = Ti;
         a.gate_up_split = I;
-        a.out0 = b.a_all;
-        a.ld_out0 = I;
-        a.outh = b.gu_all;
-        a.ld_outh = 2 * I;
+        set_gu_outputs(s, a, b.a_all, ws.alo_all, b.gu_all, b.gu32);
         Timed tm_(h, MOE_K_FWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -783,8 +861,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         a.num_mtiles = rows / kBM;
         a.n_tiles = H / kMxBN;
         a.k_blocks = I / kMxBK;
-        a.outh = v.yx;
-        a.ld_outh = H;
+        set_row_output(s, a, v.yx, v.yx32);
         a.sfa = b.a_sf;
         a.sfa_kgroups = I / 128;
         a.sfb = ws.sf_down_row;
@@ -796,6 +873,10 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
         if (!map_kmajor(&m.a, b.a_all, rows_all, I, I)) return MOE_ERR_INVALID_ARG;
+        if (s.act32) {  // a as hi + lo terms
+            if (!map_kmajor(&m.lo, ws.alo_all, rows_all, I, I)) return MOE_ERR_INVALID_ARG;
+            a.split = 1;
+        }
         MOE_TRY(routed_map(h, TB_FWD_DOWN, w->routed_down, H, I, bn, st, &m.b0, &a.b0_tab));
         if (!map_weight(&m.s0, w->shared_down, 1, H, I, 64, bn)) return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
@@ -806,8 +887,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         a.num_mtiles = rows_all / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
-        a.outh = ws.yx_all;
-        a.ld_outh = H;
+        set_row_output(s, a, ws.yx_all, ws.yx32);
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -816,19 +896,23 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         const int bn = s.bn_down;
         if (!map_kmajor(&m.a, b.a_all, Ti, I, I) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, bn))
             return MOE_ERR_INVALID_ARG;
+        if (s.act32) {
+            if (!map_kmajor(&m.lo, ws.alo_all, Ti, I, I)) return MOE_ERR_INVALID_ARG;
+            a.split = 1;
+        }
         m.b1 = m.b0;
         a.num_mtiles = (Ti + kBM - 1) / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
         a.rows_valid = Ti;
-        a.outh = ws.yx_all;
-        a.ld_outh = H;
+        set_row_output(s, a, ws.yx_all, ws.yx32);
         Timed tm_(h, MOE_K_FWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
     // combine
     Timed tm_(h, MOE_K_COMBINE, st);
-    MOE_CU(launch_combine(ws.yx_all, gated ? b.pp_all : nullptr, v.yx, b.row_of, b.pp, Ti, H, k,
+    MOE_CU(launch_combine(s.act32 ? static_cast<const void*>(ws.yx32) : ws.yx_all, gated ? b.pp_all : nullptr,
+                          s.act32 ? static_cast<const void*>(v.yx32) : v.yx, s.act32, b.row_of, b.pp, Ti, H, k,
                           static_cast<__nv_bfloat16*>(out), h->sms, st));
     return MOE_OK;
 }
@@ -877,9 +961,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     { Timed tm_(h, MOE_K_GATHER, st);
     if (mx)
         MOE_CU(launch_gather_rows(go, v.perm_src, b.meta + 2, 0, rows, H, v.go_perm, ws.go_q, ws.go_sf, h->sms, st));
-    else  // the shared expert's rows too
-        MOE_CU(launch_gather_rows(go, b.perm_src_all, b.meta + 2, v.R0, rows_all, H, ws.go_all, nullptr, nullptr,
-                                  h->sms, st)); }
+    else  // routed rows (the GEMMs read the shared expert's rows from grad_out itself)
+        MOE_CU(launch_gather_rows(go, v.perm_src, b.meta + 2, 0, rows, H, v.go_perm, nullptr, nullptr, h->sms, st)); }
 
     GemmMaps m{};
     // dgrad through the down projection + SwiGLU backward + dprob partials
@@ -894,16 +977,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.num_mtiles = rows / kBM;
         a.n_tiles = I / kMxBN;
         a.k_blocks = H / kMxBK;
-        a.in0 = v.a;
-        a.ld_in0 = I;
-        a.inh = v.gu;
-        a.ld_inh = 2 * I;
+        set_bwd_down_io(s, a, v.a, v.gu, v.gu32, v.dgdu, v.dgdulo, v.ap, v.aplo);
         a.row_scale = v.pp_perm;
         a.partial = v.partial;
-        a.out0 = v.dgdu;
-        a.ld_out0 = 2 * I;
-        a.out1 = v.ap;
-        a.ld_out1 = I;
         a.q_out = ws.dgdu_q;
         a.ld_q = 2 * I;
         a.q_sf = ws.dgdu_sf;
@@ -918,7 +994,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     } else {  // shared expert (group 0: its rows' scale is the gate, or 1) and routed experts
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
-        if (!map_kmajor(&m.a, ws.go_all, rows_all, H, H)) return MOE_ERR_INVALID_ARG;
+        if (!map_kmajor(&m.a, ws.go_all, rows_all, H, H) || !map_kmajor(&m.g0, go, Ti, H, H))
+            return MOE_ERR_INVALID_ARG;
+        a.g0_operand = 1;
         MOE_TRY(routed_map(h, TB_BWD_DOWN, w->routed_down, H, I, 64, st, &m.b0, &a.b0_tab));
         if (!map_weight(&m.s0, w->shared_down, 1, H, I, 64, 64)) return MOE_ERR_INVALID_ARG;
         m.b1 = m.b0;
@@ -929,16 +1007,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.num_mtiles = rows_all / kBM;
         a.n_tiles = I / bn;
         a.k_blocks = H / kBK;
-        a.in0 = b.a_all;
-        a.ld_in0 = I;
-        a.inh = b.gu_all;
-        a.ld_inh = 2 * I;
+        set_bwd_down_io(s, a, b.a_all, b.gu_all, b.gu32, ws.dgdu_all, ws.dgdulo_all, ws.ap_all, ws.aplo_all);
         a.row_scale = b.pp_all;
         a.partial = ws.partial_all;
-        a.out0 = ws.dgdu_all;
-        a.ld_out0 = 2 * I;
-        a.out1 = ws.ap_all;
-        a.ld_out1 = I;
         Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -952,17 +1023,13 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = I / bn;
         a.k_blocks = H / kBK;
         a.rows_valid = Ti;
-        a.in0 = b.a_all;
-        a.ld_in0 = I;
-        a.inh = b.gu_all;
-        a.ld_inh = 2 * I;
-        a.out0 = ws.dgdu_all;
-        a.ld_out0 = 2 * I;
+        // fp32 activations: the down projection's weight gradient takes (gate *) a from
+        // here as hi + lo terms; bf16 ones: a itself unless gated
+        set_bwd_down_io(s, a, b.a_all, b.gu_all, b.gu32, ws.dgdu_all, ws.dgdulo_all,
+                        (gated || s.act32) ? ws.ap_all : nullptr, ws.aplo_all);
         if (gated) {  // the gate acts as the shared rows' prob: dgate partials, gate * a_shared
             a.row_scale = b.pp_all;
             a.partial = ws.partial_s;
-            a.out1 = ws.ap_all;
-            a.ld_out1 = I;
         }
         Timed tm_(h, MOE_K_BWD_DOWN_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
@@ -986,8 +1053,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = H / kMxBN;
         a.k_blocks = 2 * I / kMxBK;
         a.gate_up_split = I;
-        a.outh = v.yx;
-        a.ld_outh = H;
+        set_row_output(s, a, v.yx, v.yx32);
         a.sfa = ws.dgdu_sf;
         a.sfa_kgroups = 2 * I / 128;
         a.sfb = ws.sf_fc1_col;
@@ -999,6 +1065,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
         if (!map_kmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
+        if (s.act32) {  // [dg|du] as hi + lo terms
+            if (!map_kmajor(&m.lo, ws.dgdulo_all, rows_all, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
+            a.split = 1;
+        }
         MOE_TRY(routed_map(h, TB_BWD_GU_G, w->routed_gate, I, H, 64, st, &m.b0, &a.b0_tab));
         MOE_TRY(routed_map(h, TB_BWD_GU_U, w->routed_up, I, H, 64, st, &m.b1, &a.b1_tab));
         if (!map_weight(&m.s0, w->shared_gate, 1, I, H, 64, 64) || !map_weight(&m.s1, w->shared_up, 1, I, H, 64, 64))
@@ -1010,8 +1080,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = H / bn;
         a.k_blocks = 2 * I / kBK;
         a.gate_up_split = I;
-        a.outh = ws.yx_all;
-        a.ld_outh = H;
+        set_row_output(s, a, ws.yx_all, ws.yx32);
         Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -1021,13 +1090,16 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         if (!map_kmajor(&m.a, ws.dgdu_all, Ti, 2 * I, 2 * I) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, 64) ||
             !map_weight(&m.b1, w->shared_up, 1, I, H, 64, 64))
             return MOE_ERR_INVALID_ARG;
+        if (s.act32) {
+            if (!map_kmajor(&m.lo, ws.dgdulo_all, Ti, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
+            a.split = 1;
+        }
         a.num_mtiles = (Ti + kBM - 1) / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = 2 * I / kBK;
         a.rows_valid = Ti;
         a.gate_up_split = I;
-        a.outh = ws.yx_all;
-        a.ld_outh = H;
+        set_row_output(s, a, ws.yx_all, ws.yx32);
         Timed tm_(h, MOE_K_BWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
@@ -1045,6 +1117,12 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
                               mg->strides[3][1], mg_bf16, st, &m.c0, &a.c0_tab));
         MOE_TRY(routed_mg_map(h, TB_MG_U, mg->routed_up, mg->expert_ptrs[1], I, H, mg->strides[4][0],
                               mg->strides[4][1], mg_bf16, st, &m.c1, &a.c1_tab));
+        if (s.act32) {  // [dg|du] as hi + lo terms
+            if (!(mx ? map_mnmajor(&m.lo, v.dgdulo, rows, 2 * I, 2 * I)
+                     : map_mnmajor(&m.lo, ws.dgdulo_all, rows_all, 2 * I, 2 * I)))
+                return MOE_ERR_INVALID_ARG;
+            a.split = 1;
+        }
         if (mx) {
             if (!map_mnmajor(&m.a, v.dgdu, rows, 2 * I, 2 * I) || !map_mnmajor(&m.b0, v.x_perm, rows, H, H))
                 return MOE_ERR_INVALID_ARG;
@@ -1053,12 +1131,14 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         } else {
             if (!map_mnmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I) ||
                 !map_mnmajor(&m.b0, b.x_all, rows_all, H, H) ||
+                !map_mnmajor(&m.g0, saved->hidden, Ti, H, H) ||
                 !map_main_grad(&m.s0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1], mg_bf16) ||
                 !map_main_grad(&m.s1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
                 return MOE_ERR_INVALID_ARG;
             a.seg_off = b.seg_x;
             a.groups = E + 1;
             a.group0_shared = 1;
+            a.g0_operand = 2;   // x rows of the shared expert: hidden
         }
         m.b1 = m.b0;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
@@ -1074,6 +1154,11 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.tile_counter = ws.tile_counters + 1;
         MOE_TRY(routed_mg_map(h, TB_MG_D, mg->routed_down, mg->expert_ptrs[2], H, I, mg->strides[5][0],
                               mg->strides[5][1], mg_bf16, st, &m.c0, &a.c0_tab));
+        if (s.act32) {  // p * a as hi + lo terms
+            if (!(mx ? map_mnmajor(&m.lo, v.aplo, rows, I, I) : map_mnmajor(&m.lo, ws.aplo_all, rows_all, I, I)))
+                return MOE_ERR_INVALID_ARG;
+            a.split = 2;
+        }
         if (mx) {
             if (!map_mnmajor(&m.a, v.go_perm, rows, H, H) || !map_mnmajor(&m.b0, v.ap, rows, I, I))
                 return MOE_ERR_INVALID_ARG;
@@ -1081,11 +1166,13 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
             a.groups = E;
         } else {
             if (!map_mnmajor(&m.a, ws.go_all, rows_all, H, H) || !map_mnmajor(&m.b0, ws.ap_all, rows_all, I, I) ||
+                !map_mnmajor(&m.g0, go, Ti, H, H) ||
                 !map_main_grad(&m.s0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16))
                 return MOE_ERR_INVALID_ARG;
             a.seg_off = b.seg_x;
             a.groups = E + 1;
             a.group0_shared = 1;
+            a.g0_operand = 1;   // grad_out rows of the shared expert: grad_out
         }
         m.b1 = m.b0;
         m.c1 = m.c0;
@@ -1098,6 +1185,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         const int bn = s.bn_wfc1;
         if (!map_mnmajor(&m.a, ws.dgdu_all, Ti, 2 * I, 2 * I) || !map_mnmajor(&m.b0, saved->hidden, Ti, H, H))
             return MOE_ERR_INVALID_ARG;
+        if (s.act32) {
+            if (!map_mnmajor(&m.lo, ws.dgdulo_all, Ti, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
+            a.split = 1;
+        }
         m.b1 = m.b0;
         a.seg_len = Ti;
         a.groups = 1;
@@ -1115,8 +1206,12 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     if (mx) {  // shared wgrad of down (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wd;
-        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, gated ? ws.ap_all : b.a_all, Ti, I, I))
+        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, (gated || s.act32) ? ws.ap_all : b.a_all, Ti, I, I))
             return MOE_ERR_INVALID_ARG;
+        if (s.act32) {
+            if (!map_mnmajor(&m.lo, ws.aplo_all, Ti, I, I)) return MOE_ERR_INVALID_ARG;
+            a.split = 2;
+        }
         m.b1 = m.b0;
         a.seg_len = Ti;
         a.groups = 1;
@@ -1131,7 +1226,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // dhidden = shared + un-permuted routed dgrad; dense dprobs
     Timed tm_(h, MOE_K_UNPERMUTE, st);
-    MOE_CU(launch_unpermute(ws.yx_all, v.yx, b.row_of, b.ids, v.partial, s.n_part, Ti, H, k, E,
+    MOE_CU(launch_unpermute(s.act32 ? static_cast<const void*>(ws.yx32) : ws.yx_all,
+                            s.act32 ? static_cast<const void*>(v.yx32) : v.yx, s.act32, b.row_of, b.ids, v.partial,
+                            s.n_part, Ti, H, k, E,
                             gated ? ws.dz : nullptr,
                             gated ? static_cast<const __nv_bfloat16*>(w->shared_output_gate) : nullptr,
                             static_cast<__nv_bfloat16*>(dhidden), dprobs, saved->topk, h->sms, st));

@@ -28,8 +28,6 @@
 #include "device_common.cuh"
 #include "internal.h"
 
-#include <mutex>
-
 namespace moe {
 
 namespace {
@@ -427,7 +425,7 @@ __global__ void __launch_bounds__(1024) route_scan_chunks_kernel(int* __restrict
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     const int* __restrict__ ids, const float* __restrict__ pp, const int* __restrict__ rank,
     const int* __restrict__ chunk_base, const int* __restrict__ counts, const int* __restrict__ offs_pad, int T,
-    int E, int k, int shared_rows,
+    int E, int k, int shared_rows, int copy_shared,
     const uint4* __restrict__ hidden, int vec_per_row, int* __restrict__ perm_src, float* __restrict__ pp_perm,
     int* __restrict__ row_of, uint4* __restrict__ x_perm, uint8_t* __restrict__ x_q, uint8_t* __restrict__ x_sf) {
     pdl_wait();
@@ -464,6 +462,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
             perm_src[pos] = tok ? t : -1;
             pp_perm[pos] = tok ? 1.0f : 0.0f;  // the shared output gate, when there is one, overwrites it
         }
+        if (!copy_shared) return;  // the GEMMs read the shared rows from hidden itself
         uint4* dst = x_perm + pos * vec_per_row;
         if (tok)
             for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(hidden + int64_t(t) * vec_per_row + v);
@@ -567,14 +566,14 @@ cudaError_t launch_route_scan_chunks(int* hist, int T, int E, int* counts, int* 
 
 cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank, const int* chunk_base,
                                const int* counts, const int* offs_pad, int T, int E, int k, int shared_rows,
-                               const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm, int* row_of,
-                               __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st) {
+                               bool copy_shared, const __nv_bfloat16* hidden, int H, int* perm_src, float* pp_perm,
+                               int* row_of, __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st) {
     const int64_t items = int64_t(T) * k + int64_t(E) * kBM + shared_rows;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const cudaError_t e = launch_pdl(route_place_kernel, dim3(unsigned(blocks)), dim3(32 * kWarpsPerBlock), 0, st,
                                      ids, pp, rank, chunk_base, counts, offs_pad, T, E, k, shared_rows,
-                                     reinterpret_cast<const uint4*>(hidden), H / 8, perm_src, pp_perm, row_of,
-                                     reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
+                                     copy_shared ? 1 : 0, reinterpret_cast<const uint4*>(hidden), H / 8, perm_src,
+                                     pp_perm, row_of, reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
     count_launch();
     return e;
 }
@@ -606,20 +605,13 @@ namespace {
 constexpr int64_t kNoAllocMaxRoutes = int64_t(1) << 17;  // T * k, 512 KB of int32
 static __device__ __align__(256) int g_noalloc_rank[kNoAllocMaxRoutes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-int* g_noalloc_rank_ptr[kMaxDevices] = {};
-
-// device address of the scratch array on the current device, resolved once
-int* noalloc_scratch(int device) {
-    if (device < 0 || device >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_rank_ptr[device]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || !p) return nullptr;
-        g_noalloc_rank_ptr[device] = static_cast<int*>(p);
-    }
-    return g_noalloc_rank_ptr[device];
+// device address of the scratch array on the current device, resolved on every
+// call (cheap once the library's device code is loaded on the device, and never
+// stale after a device reset or a new primary context)
+int* noalloc_scratch() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || !p) return nullptr;
+    return static_cast<int*>(p);
 }
 
 __global__ void __launch_bounds__(1024) route_scan_compact_kernel(const int* __restrict__ counts, int E,
@@ -659,9 +651,7 @@ extern "C" moe_status moe_route_noalloc(int64_t T, int64_t E, int64_t k, const u
     if (T * k > kNoAllocMaxRoutes || T > route_rank_max_tokens()) return MOE_ERR_UNSUPPORTED;
     if (!counts || !offsets || !routing_error) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!routing_map || !probs || !ids || !pp || !perm_src || !row_of)) return MOE_ERR_INVALID_ARG;
-    int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) return MOE_ERR_CUDA;
-    int* rank = noalloc_scratch(device);
+    int* rank = noalloc_scratch();
     if (!rank) return MOE_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(routing_error, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;

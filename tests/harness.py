@@ -26,6 +26,7 @@ class Case:
     limit: float = 0.0    # swiglu_limit
     gated: bool = False   # shared expert with an output gate
     mg_bf16: bool = False  # bf16 main_grad buffers
+    act_bf16: bool = False  # bf16 activations (MOE_ACT_BF16) instead of the default fp32 ones
 
 
 def config_case(cfg_id: int, T: int | None = None, variant: str | None = None) -> Case:
@@ -94,7 +95,8 @@ def run_gpu(inp: Inputs, backward=True, main_grads=None, layer=None) -> GpuResul
     if layer is None:
         layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, device=inp.hidden.device,
                            routed_wtype=M.binding.MOE_W_MXFP8 if c.mx else M.binding.MOE_W_BF16,
-                           swiglu_limit=c.limit)
+                           swiglu_limit=c.limit,
+                           act_precision=M.binding.MOE_ACT_BF16 if c.act_bf16 else M.binding.MOE_ACT_FP32)
     wv = weight_views(inp)
     if c.mx:
         layer.prepare_weights(wv)
@@ -180,26 +182,37 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def oracle_full(inp: Inputs, precision="bf16"):
-    """Oracle forward + backward over all tokens (bf16 mode: with its rounding envelope)."""
+def oracle_full(inp: Inputs, precision="exact"):
+    """Oracle forward + backward over all tokens. The cache also carries the bf16
+    mode's rounding envelope ("envelope", bf16 mode only) and the clamp's
+    gradient-mask alternatives ("jumps", the other modes; zero without a clamp)."""
     W = oracle_weights(inp)
     out, cache = O.forward(f64(inp.hidden), inp.probs_np, inp.map_np, W, inp.case.k, precision=precision,
                            swiglu_limit=inp.case.limit)
     go = f64(inp.grad_out)
     dx, dprobs, grads = O.backward(go, cache, W)
-    cache["envelope"] = O.envelope(go, cache, W) if precision in ("bf16", "mxfp8") else None
+    cache["envelope"] = O.envelope(go, cache, W) if precision == "bf16" else None
+    cache["jumps"] = O.clamp_jumps(go, cache, W) if precision != "bf16" else None
     return out, dx, dprobs, grads, cache
 
 
-def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3, env=None):
+# The BF16 tolerance read per element (|gpu - ref| <= rtol |ref| + atol max|ref|,
+# max over the whole compared tensor), and the MXFP8 one.
+BF16_TOL = dict(rtol=2e-2, atol_frac=1e-3)
+MX_TOL = dict(rtol=6e-2, atol_frac=6e-3)
+
+
+def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3, env=None, scale=None):
     """Per element |gpu - ref| <= rtol*|ref| + atol_frac*max|ref| (the BF16 tolerance),
-    plus the oracle's rounding envelope ``env`` where given (the other valid bf16
-    roundings of operands that sit at a rounding midpoint within fp32 precision)."""
+    plus ``env`` where given: the other valid results of a discrete decision taken
+    in fp32 (the bf16 mode's rounding envelope, or the clamp's gradient-mask
+    alternatives). ``scale`` overrides max|ref| (a sample of a larger tensor)."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     assert gpu.shape == ref.shape, (name, gpu.shape, ref.shape)
     assert np.all(np.isfinite(gpu)), f"{name}: non-finite values in the CUDA result"
-    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if scale is None:
+        scale = float(np.max(np.abs(ref))) if ref.size else 0.0
     err = np.abs(gpu - ref)
     bound = rtol * np.abs(ref) + atol_frac * scale
     if env is not None:
@@ -210,6 +223,19 @@ def assert_close(gpu, ref, name, rtol=2e-2, atol_frac=1e-3, env=None):
         raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} elements out of tolerance; worst at {i}: "
                              f"gpu={gpu[i]:.6g} ref={ref[i]:.6g}; max|err|/max|ref|={err.max() / max(scale, 1e-300):.3g}")
     return float(err.max() / max(scale, 1e-300)) if ref.size else 0.0
+
+
+def count_outside(gpu, ref, rtol, atol_frac, env=None):
+    """(elements outside rtol |ref| + atol_frac max|ref| (+ env), worst err / bound)."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if not ref.size:
+        return 0, 0.0
+    bound = rtol * np.abs(ref) + atol_frac * np.max(np.abs(ref))
+    if env is not None:
+        bound = bound + np.asarray(env, np.float64)
+    err = np.abs(gpu - ref)
+    return int(np.sum(err > bound)), float(np.max(err / np.maximum(bound, 1e-300)))
 
 
 # Normwise bound against the exact (fp64, unrounded) oracle. Each result passes
@@ -244,3 +270,115 @@ def assert_normwise(gpu, ref, name, bound=EXACT_NORMWISE, env=None):
     r = float(np.max(err) / scale)
     assert r <= bound, f"{name}: max|gpu-exact|/max|exact| = {r:.3g} > {bound}"
     return r
+
+
+def _named(out, dx, dprobs, grads, I, routed_experts):
+    """The layer's results by name; routed weight gradients as the whole
+    [E', I, H] / [E', H, I] tensors over ``routed_experts`` (one main_grad buffer each)."""
+    r = {"out": out, "dhidden": dx, "dprobs": dprobs, "dW shared gate": grads["shared_gate"],
+         "dW shared up": grads["shared_up"], "dW shared down": grads["shared_down"]}
+    if "shared_output_gate" in grads:
+        r["dW shared output gate"] = grads["shared_output_gate"]
+    if routed_experts:
+        for j, kind in enumerate(("gate", "up", "down")):
+            r[f"dW routed {kind}"] = np.stack([grads["routed"][e][j] for e in routed_experts])
+    return r
+
+
+def gpu_named(inp: Inputs, res: GpuResult, routed_experts):
+    """The CUDA results in the layout of ``_named`` (main_grad updates as after - before)."""
+    I = inp.case.I
+    d = {n: f64(res.main_grads[n]) - f64(inp.main_grads[n]) for n in inp.main_grads}
+    grads = dict(shared_gate=d["shared_fc1"][:I], shared_up=d["shared_fc1"][I:], shared_down=d["shared_fc2"],
+                 routed={e: (d["routed_fc1"][e, :I], d["routed_fc1"][e, I:], d["routed_fc2"][e])
+                         for e in routed_experts})
+    if "shared_output_gate" in d:
+        grads["shared_output_gate"] = d["shared_output_gate"]
+    return _named(f64(res.out), f64(res.dhidden), f64(res.dprobs), grads, I, routed_experts)
+
+
+def _env_named(env, routed_experts):
+    if env is None:
+        return {}
+    r = {"out": env["out"], "dhidden": env["dhidden"], "dprobs": env["dprobs"], "dW shared gate": env["shared_gate"],
+         "dW shared up": env["shared_up"], "dW shared down": env["shared_down"]}
+    if "shared_output_gate" in env:
+        r["dW shared output gate"] = env["shared_output_gate"]
+    if routed_experts:
+        for j, kind in enumerate(("gate", "up", "down")):
+            r[f"dW routed {kind}"] = np.stack([env["routed"][e][j] for e in routed_experts])
+    return r
+
+
+def _normwise(a, r):
+    scale = float(np.max(np.abs(r))) if np.size(r) else 0.0
+    return float(np.max(np.abs(np.asarray(a) - r)) / scale) if scale > 0 else 0.0
+
+
+def compare_layer(inp: Inputs, res: GpuResult, exact_counts=None, mx_exact_bound=True):
+    """Every output and weight gradient of the CUDA layer against the oracle on the
+    same inputs, element by element. Experts without tokens must keep their
+    main_grad bitwise. Returns {name: max|gpu - ref| / max|ref|} against the exact
+    oracle.
+
+    * fp32 activations (the default), BF16 routed weights: against the exact
+      definition, |gpu - ref| <= 2e-2 |ref| + 1e-3 max|ref|, no envelope (with a
+      swiglu_limit, plus the clamp's gradient-mask alternatives at its bounds).
+    * fp32 activations, MXFP8 routed weights: against the MXFP8 method (the
+      oracle's mxfp8 mode: same dequantised weights, the four GEMM activation
+      operands quantised) within 6e-2 |ref| + 6e-3 max|ref|, and against the
+      exact definition on the same dequantised weights within
+      max|gpu - ref| <= 6e-2 max|ref| (``mx_exact_bound``, the workloads' sizes);
+      otherwise no further from it than the MXFP8 method itself is (the
+      mxfp8-mode oracle's own distance x 1.05 + 1e-3, or 6e-2 if that is larger).
+    * bf16 activations: against the bf16-mode oracle plus its rounding envelope
+      within the BF16 tolerance (BF16 weights), and against the exact definition
+      normwise (1e-2 BF16, 6e-2 MXFP8).
+    ``exact_counts`` (a dict) receives, per tensor, the elements outside the per
+    element tolerance against the exact definition and the worst err/bound."""
+    c = inp.case
+    I = c.I
+    counts = inp.map_np.sum(0)
+    experts = [int(e) for e in np.flatnonzero(counts > 0)]
+    for e in np.flatnonzero(counts == 0):    # an expert with no tokens keeps its main_grad bitwise
+        assert torch.equal(res.main_grads["routed_fc1"][e], inp.main_grads["routed_fc1"][e]), e
+        assert torch.equal(res.main_grads["routed_fc2"][e], inp.main_grads["routed_fc2"][e]), e
+    got = gpu_named(inp, res, experts)
+    tol = MX_TOL if c.mx else BF16_TOL
+    ex = oracle_full(inp, "exact")
+    ref_x = _named(*ex[:4], I, experts)
+    jumps = _env_named(ex[4]["jumps"], experts) if c.limit else {}
+    errs = {}
+    if not c.act_bf16:
+        if c.mx:
+            mx = oracle_full(inp, "mxfp8")
+            ref_m = _named(*mx[:4], I, experts)
+            jm = _env_named(mx[4]["jumps"], experts) if c.limit else {}
+            for n, r in ref_m.items():
+                errs["mxfp8-mode " + n] = assert_close(got[n], r, "mxfp8-mode " + n, env=jm.get(n), **tol)
+        for n, r in ref_x.items():
+            if c.mx:
+                if mx_exact_bound:
+                    errs[n] = assert_normwise(got[n], r, n, bound=tol["rtol"], env=jumps.get(n))
+                else:
+                    # no further from the exact definition than the MXFP8 method itself is
+                    # (its own error grows on experts with few tokens, and with a clamp,
+                    # whose masks follow the quantised SwiGLU inputs)
+                    own = _normwise(ref_m[n], r)
+                    errs[n] = assert_normwise(got[n], r, n, bound=max(tol["rtol"], 1.05 * own + 1e-3))
+                    errs["mxfp8 method vs exact " + n] = own
+            else:
+                errs[n] = assert_close(got[n], r, n, env=jumps.get(n), **tol)
+    else:
+        if not c.mx:
+            bf = oracle_full(inp, "bf16")
+            env = _env_named(bf[4]["envelope"], experts)
+            for n, r in _named(*bf[:4], I, experts).items():
+                assert_close(got[n], r, "bf16-mode " + n, env=env[n], **tol)
+        for n, r in ref_x.items():
+            errs[n] = assert_normwise(got[n], r, n, bound=tol["rtol"] if c.mx else EXACT_NORMWISE,
+                                      env=jumps.get(n))
+    if exact_counts is not None:
+        for n, r in ref_x.items():
+            exact_counts[n] = count_outside(got[n], r, tol["rtol"], tol["atol_frac"], env=jumps.get(n))
+    return errs

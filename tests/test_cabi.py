@@ -89,7 +89,7 @@ def _c_layout(tmp_path):
         pytest.skip("no C compiler")
     fields = {
         "moe_config": ["max_tokens", "hidden", "num_experts", "topk", "inter", "routed_wtype", "swiglu_limit",
-                       "recompute_dispatch"],
+                       "recompute_dispatch", "act_precision"],
         "moe_wview": ["data", "expert_stride", "row_stride", "scale", "col_data", "col_scale", "expert_ptrs"],
         "moe_weights": ["shared_gate", "shared_up", "shared_down", "routed_gate", "routed_up", "routed_down",
                         "shared_output_gate"],
@@ -126,6 +126,18 @@ def test_recompute_dispatch_flag():
     assert M.moe_workspace_size(_cfg(recompute_dispatch=1)) > M.moe_workspace_size(_cfg())
     with pytest.raises(M.MoeError) as ei:
         M.moe_saved_size(_cfg(recompute_dispatch=2))
+    assert ei.value.status == 1
+
+
+def test_act_precision_flag():
+    """fp32 activations (the default) keep [g|u] in fp32 in the saved state and need
+    the lo-term and fp32 row buffers in the workspace; other values are rejected."""
+    fp32 = _cfg()
+    bf16 = _cfg(act_precision=M.binding.MOE_ACT_BF16)
+    assert M.moe_saved_size(fp32) > M.moe_saved_size(bf16)
+    assert M.moe_workspace_size(fp32) > M.moe_workspace_size(bf16)
+    with pytest.raises(M.MoeError) as ei:
+        M.moe_saved_size(_cfg(act_precision=2))
     assert ei.value.status == 1
 
 

@@ -2,11 +2,12 @@
 through the C ABI, against the oracle with the same clamp and gate.
 
 Same bars as the plain layer: per element |gpu - ref| <= 2e-2 |ref| +
-1e-3 max|ref| + env against the bf16-mode oracle (env now also covers the
-clamp's mask jumps at its bounds and the gate's fp32 evaluation), normwise
-1e-2 against the exact oracle; MXFP8 routed experts against the mxfp8-mode
-oracle with 6e-2 / 6e-3. Every case checks that the clamp is active on a
-sizeable share of the SwiGLU inputs, so a kernel that ignored it would fail.
+1e-3 max|ref| against the exact definition, plus, where a SwiGLU input's fp32
+evaluation lies within its error band of a clamp bound, the other gradient
+mask's effect (either side is a correct result); MXFP8 routed experts against
+the mxfp8-mode oracle with 6e-2 / 6e-3 and normwise 6e-2 against the exact
+definition. Every case checks that the clamp is active on a sizeable share of
+the SwiGLU inputs, so a kernel that ignored it would fail.
 """
 import dataclasses
 

@@ -3,26 +3,30 @@
 * quantisation (moe_quantize_mxfp8) is compared bit-exactly with the oracle
   codec on the same bf16 input, rowwise and columnwise;
 * the layer with MXFP8 routed weights is compared, per element, with the oracle
-  in mxfp8 mode -- the method: the same dequantised weights, the GEMM operands
-  quantised on the fly at the same points -- within
-  |gpu - ref| <= 6e-2 |ref| + 6e-3 max|ref| + env (env: the oracle's envelope of
-  the other valid roundings of operands at a rounding midpoint within fp32
-  evaluation precision) for every output and weight gradient;
-* the distance from the exact oracle on the same dequantised weights with
-  unquantised activations is reported (it measures MXFP8's own approximation
-  error, e.g. dW_down averages the E4M3 error of a over only n_e tokens).
+  in mxfp8 mode -- the MXFP8 method on the same dequantised weights: the routed
+  forward and dgrad GEMMs' activation operands (x, a; grad_out, [dg|du])
+  quantised on the fly, nothing else rounded -- within
+  |gpu - ref| <= 6e-2 |ref| + 6e-3 max|ref| for every output and weight gradient,
+  no envelope;
+* and with the exact definition on the same dequantised weights (unquantised
+  activations) within max|gpu - ref| <= 6e-2 max|ref| at the workloads' sizes
+  (on small layers, whose experts see few tokens, and with a clamp, MXFP8's own
+  error can exceed that: there the GPU must be no further from the exact
+  definition than the mxfp8-mode oracle is). Per element that bound
+  cannot hold: an E4M3 operand carries a relative error of up to 2^-4, and the
+  mxfp8-mode oracle itself, oracle against oracle, falls outside
+  6e-2 |ref| + 6e-3 max|ref| of the exact one on thousands of elements; the
+  counts are printed.
 """
 import numpy as np
 import pytest
 import torch
 
 from oracle import mxfp8 as MX
-from tests.harness import Case, assert_close, config_case, f64, make_inputs, oracle_full, run_gpu
+from tests.harness import (MX_TOL, Case, assert_close, assert_normwise, compare_layer, config_case, f64,
+                           make_inputs, run_gpu)
 
 pytestmark = pytest.mark.gpu
-
-MX_RTOL, MX_ATOL = 6e-2, 6e-3
-
 
 def _bf16_matrix(rows, cols, seed):
     g = torch.Generator().manual_seed(seed)
@@ -49,45 +53,10 @@ def test_quantiser_bit_exact(axis):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
-def _compare(inp, res):
-    c = inp.case
-    I = c.I
-    mg0 = {n: f64(t) for n, t in inp.main_grads.items()}
-    mg1 = {n: f64(t) for n, t in res.main_grads.items()}
-    d = {n: mg1[n] - mg0[n] for n in mg0}
-    got = {"out": f64(res.out), "dhidden": f64(res.dhidden), "dprobs": f64(res.dprobs)}
-    errs = {}
-    for prec in ("mxfp8", "exact"):
-        out, dx, dprobs, grads, cache = oracle_full(inp, prec)
-        env = cache["envelope"]
-        ref = {"out": out, "dhidden": dx, "dprobs": dprobs}
-        ev = {}
-        if env is not None:
-            ev = {"out": env["out"], "dhidden": env["dhidden"], "dprobs": env["dprobs"],
-                  "dW shared gate": env["shared_gate"], "dW shared up": env["shared_up"],
-                  "dW shared down": env["shared_down"]}
-        for e, (dWg, dWu, dWd) in grads["routed"].items():
-            for j, (kind, r, gv) in enumerate((("gate", dWg, d["routed_fc1"][e, :I]),
-                                               ("up", dWu, d["routed_fc1"][e, I:]),
-                                               ("down", dWd, d["routed_fc2"][e]))):
-                ref[f"dW routed {kind}[{e}]"] = r
-                got[f"dW routed {kind}[{e}]"] = gv
-                if env is not None:
-                    ev[f"dW routed {kind}[{e}]"] = env["routed"][e][j]
-        ref["dW shared gate"], got["dW shared gate"] = grads["shared_gate"], d["shared_fc1"][:I]
-        ref["dW shared up"], got["dW shared up"] = grads["shared_up"], d["shared_fc1"][I:]
-        ref["dW shared down"], got["dW shared down"] = grads["shared_down"], d["shared_fc2"]
-        if "shared_output_gate" in grads:
-            ref["dW shared output gate"] = grads["shared_output_gate"]
-            got["dW shared output gate"] = d["shared_output_gate"]
-            if env is not None:
-                ev["dW shared output gate"] = env["shared_output_gate"]
-        for n, r in ref.items():
-            if prec == "mxfp8":
-                errs[n] = assert_close(got[n], r, n, rtol=MX_RTOL, atol_frac=MX_ATOL, env=ev.get(n))
-            else:
-                errs["exact " + n] = float(np.max(np.abs(got[n] - r)) / max(np.max(np.abs(r)), 1e-300))
-    return errs
+def _compare(inp, res, mx_exact_bound=False):
+    counts = {}
+    errs = compare_layer(inp, res, exact_counts=counts, mx_exact_bound=mx_exact_bound)
+    return errs, counts
 
 
 MX_SMALL = {
@@ -100,20 +69,18 @@ MX_SMALL = {
 def test_mxfp8_layer_parity_small(name):
     inp = make_inputs(MX_SMALL[name])
     res = run_gpu(inp)
-    errs = _compare(inp, res)
+    errs, _ = _compare(inp, res)
     assert res.layer.device_status() == 0
-    print(name, "vs exact oracle:", {n: f"{v:.2e}" for n, v in errs.items() if n.startswith("exact") and "[" not in n})
+    print(name, "max|err|/max|exact|:", {n: f"{v:.2e}" for n, v in errs.items()})
 
 
 def test_mxfp8_layer_parity_config3_full():
     """Proxy-like layer with MXFP8 routed weights (T=4096, H=2048, E=96, top-6, I=1024)."""
     inp = make_inputs(config_case(3))
     res = run_gpu(inp)
-    errs = _compare(inp, res)
-    print("config 3 max|err|/max|ref|:", {n: f"{v:.2e}" for n, v in errs.items() if "[" not in n})
-    print("config 3 routed dW vs exact oracle, worst expert:",
-          {k: f"{max(v for n, v in errs.items() if n.startswith('exact dW routed ' + k)):.2e}"
-           for k in ("gate", "up", "down")})
+    errs, counts = _compare(inp, res, mx_exact_bound=True)
+    print("config 3 max|err|/max|exact|:", {n: f"{v:.2e}" for n, v in errs.items()})
+    print("config 3 elements outside 6e-2|exact| + 6e-3 max|exact|:", {n: v[0] for n, v in counts.items()})
 
 
 @pytest.mark.slow
@@ -153,39 +120,46 @@ def test_mxfp8_layer_parity_config4_sampled():
     rng = np.random.default_rng(4)
     toks = np.sort(rng.choice(c.T, 16, replace=False))
     tt = torch.from_numpy(toks).to(inp.hidden.device)
-    ref, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], inp.map_np[toks], W, c.k, precision="mxfp8")
     go = f64(inp.grad_out[tt])
-    rdx, rdp, _ = O.backward(go, cache, W)
-    env = O.envelope(go, cache, W)
-    kw = dict(rtol=MX_RTOL, atol_frac=MX_ATOL)
-    assert_close(f64(out[tt]), ref, "out (sampled)", env=env["out"], **kw)
-    assert_close(f64(dh[tt]), rdx, "dhidden (sampled)", env=env["dhidden"], **kw)
-    assert_close(f64(dp[tt]), rdp, "dprobs (sampled)", env=env["dprobs"], **kw)
+    got = {"out (sampled)": f64(out[tt]), "dhidden (sampled)": f64(dh[tt]), "dprobs (sampled)": f64(dp[tt])}
+    for prec in ("mxfp8", "exact"):
+        ref, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], inp.map_np[toks], W, c.k, precision=prec)
+        rdx, rdp, _ = O.backward(go, cache, W)
+        for (n, g), r in zip(got.items(), (ref, rdx, rdp)):
+            if prec == "mxfp8":
+                assert_close(g, r, n, **MX_TOL)
+            else:
+                assert_normwise(g, r, n, bound=MX_TOL["rtol"])
 
-    for e in (hot, med):
-        rows = np.flatnonzero(inp.map_np[:, e])
-        m = np.zeros((rows.size, c.E), bool)
-        m[:, e] = True
-        rt = torch.from_numpy(rows).to(inp.hidden.device)
-        _, ce = O.forward(f64(inp.hidden[rt]), inp.probs_np[rows], m, W, c.k, precision="mxfp8")
-        goe = f64(inp.grad_out[rt])
-        _, _, ge = O.backward(goe, ce, W)
-        ee = O.envelope(goe, ce, W)["routed"][e]
-        d1 = f64(mg["routed_fc1"][e]) - mg0[e][0].double().numpy()
-        d2 = f64(mg["routed_fc2"][e]) - mg0[e][1].double().numpy()
-        assert_close(d1[:I], ge["routed"][e][0], f"dW routed gate[{e}]", env=ee[0], **kw)
-        assert_close(d1[I:], ge["routed"][e][1], f"dW routed up[{e}]", env=ee[1], **kw)
-        assert_close(d2, ge["routed"][e][2], f"dW routed down[{e}]", env=ee[2], **kw)
+    for prec in ("mxfp8", "exact"):
+        refs, gots = [], []
+        for e in (hot, med):
+            rows = np.flatnonzero(inp.map_np[:, e])
+            m = np.zeros((rows.size, c.E), bool)
+            m[:, e] = True
+            rt = torch.from_numpy(rows).to(inp.hidden.device)
+            _, ce = O.forward(f64(inp.hidden[rt]), inp.probs_np[rows], m, W, c.k, precision=prec)
+            _, _, ge = O.backward(f64(inp.grad_out[rt]), ce, W)
+            refs.append(ge["routed"][e])
+            d1 = f64(mg["routed_fc1"][e]) - mg0[e][0].double().numpy()
+            d2 = f64(mg["routed_fc2"][e]) - mg0[e][1].double().numpy()
+            gots.append((d1[:I], d1[I:], d2))
+        for j, kind in enumerate(("gate", "up", "down")):
+            g, r = np.stack([x[j] for x in gots]), np.stack([x[j] for x in refs])
+            if prec == "mxfp8":
+                assert_close(g, r, f"dW routed {kind} (busiest, median)", **MX_TOL)
+            else:
+                assert_normwise(g, r, f"dW routed {kind} (busiest, median)", bound=MX_TOL["rtol"])
     for e, before in idle_before.items():
         assert torch.equal(mg["routed_fc1"][e], before)
 
+    # the shared expert is BF16 with fp32 activations: against the exact definition
     m0 = np.zeros_like(inp.map_np)
-    _, cs = O.forward(f64(inp.hidden), inp.probs_np, m0, W, c.k, precision="mxfp8")
-    gall = f64(inp.grad_out)
-    _, _, gs = O.backward(gall, cs, W)
-    es = O.envelope(gall, cs, W)
+    _, cs = O.forward(f64(inp.hidden), inp.probs_np, m0, W, c.k, precision="exact")
+    _, _, gs = O.backward(f64(inp.grad_out), cs, W)
     d1 = f64(mg["shared_fc1"]) - mg0_shared["shared_fc1"].double().numpy()
     d2 = f64(mg["shared_fc2"]) - mg0_shared["shared_fc2"].double().numpy()
-    assert_close(d1[:I], gs["shared_gate"], "dW shared gate", env=es["shared_gate"], **kw)
-    assert_close(d1[I:], gs["shared_up"], "dW shared up", env=es["shared_up"], **kw)
-    assert_close(d2, gs["shared_down"], "dW shared down", env=es["shared_down"], **kw)
+    kw = dict(rtol=2e-2, atol_frac=1e-3)
+    assert_close(d1[:I], gs["shared_gate"], "dW shared gate", **kw)
+    assert_close(d1[I:], gs["shared_up"], "dW shared up", **kw)
+    assert_close(d2, gs["shared_down"], "dW shared down", **kw)

@@ -18,12 +18,13 @@ import numpy as np
 import pytest
 import torch
 
+from moe_inputs import make_routing
 from tests.harness import Case, config_case, make_inputs, run_gpu
 
 pytestmark = pytest.mark.gpu
 
 
-def _regular(inp):
+def _regular(inp, status=0):
     import mixture_experts_layer_pack_gb300 as M
     res = run_gpu(inp, backward=False)
     c = inp.case
@@ -36,11 +37,11 @@ def _regular(inp):
                row_of=torch.empty((c.T, c.k), dtype=torch.int32, device=dev))
     M.moe_export_routing(res.layer.handle, res.layer.saved, **out)
     torch.cuda.synchronize()
-    assert res.layer.device_status() == 0
+    assert res.layer.device_status() == status
     return {n: t.cpu() for n, t in out.items()}
 
 
-def _noalloc(inp):
+def _noalloc(inp, error=0):
     import mixture_experts_layer_pack_gb300 as M
     c = inp.case
     dev = inp.hidden.device
@@ -54,7 +55,7 @@ def _noalloc(inp):
     M.moe_route_noalloc(c.T, c.E, c.k, inp.routing_map.view(torch.uint8), inp.probs, out["ids"], out["pp"],
                         out["counts"], out["offsets"], out["perm_src"], out["row_of"], err)
     torch.cuda.synchronize()
-    assert int(err.item()) == 0
+    assert int(err.item()) == error
     return {n: t.cpu() for n, t in out.items()}
 
 
@@ -82,3 +83,24 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     with pytest.raises(MoeError) as ei:
         M.moe_route_noalloc(T, E, k, z, z, z, z, z, z, z, z, z)
     assert ei.value.status == 2                              # MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_drops_rows_with_too_many_routes_like_the_regular_path():
+    """Rows of the map with k + 1 routes: routing_error is 1 and those rows are
+    dropped (every slot -1), bitwise as the regular entry points drop them (which
+    report MOE_ERR_ROUTING through the device status)."""
+    c = Case(T=300, H=128, E=8, k=2, I=64, seed=61, drop="iid")
+    r = make_routing(c.T, c.E, c.k, c.seed, c.routing, c.drop)
+    bad = [3, 50, 299]
+    for t in bad:
+        r.routing_map[t, :] = False
+        r.routing_map[t, [1, 4, 6]] = True                      # three routes with k = 2
+        r.probs[t, [1, 4, 6]] = 0.25
+    inp = make_inputs(c, routing=r)
+    want = _regular(inp, status=3)                              # MOE_ERR_ROUTING
+    got = _noalloc(inp, error=1)
+    for name in want:
+        assert torch.equal(got[name], want[name]), name
+    assert np.all(got["ids"].numpy()[bad] == -1) and np.all(got["row_of"].numpy()[bad] == -1)
+    R = int(want["offsets"][-1])
+    assert R == int(inp.map_np.sum()) - 3 * len(bad)
