@@ -42,6 +42,11 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--main-grad-dtype", choices=("fp32", "bf16"), default="fp32",
                    help="dtype of the main_grad buffers the backward accumulates into")
+    p.add_argument("--act-precision", choices=("fp32", "bf16"), default="fp32",
+                   help="activations between the expert GEMMs (include/moe.h, moe_act)")
+    p.add_argument("--per-config", default="3,4,5",
+                   help="further workloads measured after the headline one (comma list; empty: none)")
+    p.add_argument("--per-config-steps", type=int, default=10)
     return p.parse_args(argv)
 
 
@@ -150,48 +155,57 @@ def gpu_id_for(dev_index):
 
 # ----------------------------------------------------------------- algorithmic work
 MX_ROUTED_GEMMS = ("gemm_fwd_gu_routed", "gemm_fwd_down_routed", "gemm_bwd_down_routed", "gemm_bwd_gu_routed")
+# GEMM classes whose derived operand reaches the tensor cores as hi + lo bf16 terms
+# with fp32 activations (the K range runs twice)
+SPLIT_GEMMS = ("gemm_fwd_down", "gemm_bwd_gu", "gemm_wgrad_fc1", "gemm_wgrad_down")
 
 
-def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4):
+def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4, act32=True):
     """(algorithmic flops, algorithmic HBM bytes) of one launch of a kernel class.
 
-    Bytes count each operand read once and each result written once (no padding
-    rows, no re-reads); flops count a multiply-add as 2. Weights of experts
+    Bytes count each distinct operand element read once and each result written
+    once (no padding rows, no re-reads: a hidden or grad_out row that k routes
+    gather is read once); flops count a multiply-add as 2. Weights of experts
     without tokens are not read. mx: the routed forward/dgrad GEMMs read MXFP8
     operands (1 byte + 1/32 byte of scale per element) and the producers of
     those operands also write their MXFP8 copies. mg_bytes: main_grad element
-    size (read and written once by the weight-gradient kernels). With BF16 routed
-    weights (not mx) the shared expert runs as group 0 of the routed launches:
-    their classes carry the shared work too, and the routing kernels copy its rows."""
+    size (read and written once by the weight-gradient kernels). act32: g|u, y and
+    dx are fp32 (4 bytes) and the derived GEMM operands a, [dg|du], p*a are two
+    bf16 terms (4 bytes); else all of them bf16. With BF16 routed weights (not
+    mx) the shared expert runs as group 0 of the routed launches: their classes
+    carry the shared work too (their group 0 reads hidden / grad_out rows directly)."""
     b2, b4 = 2, 4
     bq = 1 + 1 / 32                          # MXFP8 element incl. its share of the scale
+    f = 4 if act32 else 2                    # fp32 (or bf16) activation / two-term operand element
     wb = bq if mx else b2                    # routed weight element
-    ab = bq if mx else b2                    # routed fprop/dgrad activation operand element
+    ab = bq if mx else b2                    # routed fprop/dgrad input-row operand element
+    a_in = bq if mx else f                   # routed down / dgrad-gate-up derived operand element
+    a_out = b2 if mx else f                  # routed gate/up epilogue's a (hi only when its GEMM is MXFP8)
     W_fc1, W_down = E_act * 2 * I * H * wb, E_act * H * I * wb
     q_a = R * I * bq if mx else 0
     q_dgdu = R * 2 * I * bq if mx else 0
     q_rows = R * H * bq if mx else 0
+    gu_in = 2 * I * f if act32 else 3 * I * b2   # dgrad-down epilogue: fp32 g|u, or bf16 a and g|u
     table = {
         "route_pack": (0, T * E + T * k * (b4 * 3 + b4)),
         "route_scan": (0, T * E + T * k * b4 + E * b4),
-        "route_place": (0, T * k * 12 + R * 12 + 2 * R * H * b2 + q_rows),
-        "gather_rows": (0, 2 * R * H * b2 + q_rows),
-        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * ab + W_fc1 + R * I * b2 + R * 2 * I * b2 + q_a),
-        "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * b2 + T * 2 * I * b2),
-        "gemm_fwd_down_routed": (2 * R * I * H, R * I * ab + W_down + R * H * b2),
-        "gemm_fwd_down_shared": (2 * T * I * H, T * I * b2 + H * I * b2 + T * H * b2),
-        "combine": (0, T * H * b2 + R * H * b2 + T * k * b4 + T * H * b2),
-        "gemm_bwd_down_routed": (2 * R * H * I, R * H * ab + W_down + R * I * b2 + R * 2 * I * b2
-                                 + R * 2 * I * b2 + R * I * b2 + q_dgdu),
-        "gemm_bwd_down_shared": (2 * T * H * I, T * H * b2 + H * I * b2 + T * I * b2 + T * 2 * I * b2
-                                 + T * 2 * I * b2),
-        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * ab + W_fc1 + R * H * b2),
-        "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * b2 + 2 * I * H * b2 + T * H * b2),
-        "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * b2 + R * H * b2 + E_act * 2 * I * H * 2 * mg_bytes),
-        "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * b2 + E_act * H * I * 2 * mg_bytes),
-        "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * b2 + T * H * b2 + 2 * I * H * 2 * mg_bytes),
-        "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * b2 + H * I * 2 * mg_bytes),
-        "unpermute": (0, T * H * b2 + R * H * b2 + T * H * b2 + T * E * b4),
+        "route_place": (0, T * k * 12 + R * 12 + T * H * b2 + R * H * b2 + q_rows),
+        "gather_rows": (0, T * H * b2 + R * H * b2 + q_rows),
+        "gemm_fwd_gu_routed": (4 * R * H * I, R * H * ab + W_fc1 + R * I * a_out + R * 2 * I * f + q_a),
+        "gemm_fwd_gu_shared": (4 * T * H * I, T * H * b2 + 2 * I * H * b2 + T * I * f + T * 2 * I * f),
+        "gemm_fwd_down_routed": (2 * R * I * H, R * I * a_in + W_down + R * H * f),
+        "gemm_fwd_down_shared": (2 * T * I * H, T * I * f + H * I * b2 + T * H * f),
+        "combine": (0, T * H * f + R * H * f + T * k * 8 + T * H * b2),
+        "gemm_bwd_down_routed": (2 * R * H * I, R * H * ab + W_down + R * gu_in + R * 2 * I * f + R * I * f
+                                 + q_dgdu),
+        "gemm_bwd_down_shared": (2 * T * H * I, T * H * b2 + H * I * b2 + T * gu_in + T * 2 * I * f + T * I * f),
+        "gemm_bwd_gu_routed": (4 * R * I * H, R * 2 * I * a_in + W_fc1 + R * H * f),
+        "gemm_bwd_gu_shared": (4 * T * I * H, T * 2 * I * f + 2 * I * H * b2 + T * H * f),
+        "gemm_wgrad_fc1_routed": (4 * R * I * H, R * 2 * I * f + R * H * b2 + E_act * 2 * I * H * 2 * mg_bytes),
+        "gemm_wgrad_down_routed": (2 * R * H * I, R * H * b2 + R * I * f + E_act * H * I * 2 * mg_bytes),
+        "gemm_wgrad_fc1_shared": (4 * T * I * H, T * 2 * I * f + T * H * b2 + 2 * I * H * 2 * mg_bytes),
+        "gemm_wgrad_down_shared": (2 * T * H * I, T * H * b2 + T * I * f + H * I * 2 * mg_bytes),
+        "unpermute": (0, T * H * f + R * H * f + T * H * b2 + T * E * b4),
         "shared_gate_fwd": (2 * T * H, T * H * b2 + H * b2 + T * b4),
         "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 2 * mg_bytes),
     }
@@ -200,14 +214,20 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4):
             rf, rb = table[f"gemm_{op}_routed"]
             sf, sb = table[f"gemm_{op}_shared"]
             table[f"gemm_{op}_routed"] = (rf + sf, rb + sb)
-        if name == "gemm_bwd_down_routed":  # the shared rows' p * a and partials, as for the routed rows
-            f, b = table[name]
-            table[name] = (f, b + T * I * b2)
-        f, b = table["route_place"]
-        table["route_place"] = (f, b + 2 * T * H * b2 + T * 8)
-        f, b = table["gather_rows"]
-        table["gather_rows"] = (f, b + 2 * T * H * b2)
+        f_, b_ = table["route_place"]
+        table["route_place"] = (f_, b_ + T * 8)   # the shared rows' source and scale (the GEMMs read hidden)
     return table[name]
+
+
+def mma_flops(name, flops, mx=False, act32=True):
+    """Tensor-core work a GEMM launch executes: its algorithmic flops, twice over
+    where a two-term operand runs the K range twice (fp32 activations; not the
+    routed MXFP8 GEMMs, whose operands are quantised single terms)."""
+    if not act32 or not name.startswith(SPLIT_GEMMS):
+        return flops
+    if mx and name in MX_ROUTED_GEMMS:
+        return flops
+    return 2 * flops
 
 
 def roofline_of(name, ms_per_launch, work, peaks, peaks_kind, traffic=None, fp8=False):
@@ -314,21 +334,17 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- our arm
-def run_ours(args):
-    import numpy as np
+def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank):
+    """One workload through the C ABI: K timed steps (forward + backward) after W
+    warm-up steps, the per-kernel table from an untimed pass, the dominant
+    kernel's roofline from its live duration inside the timed region. ``full``
+    adds forward/backward timed apart, the CUDA-graph replay and the end-to-end
+    host-buffer leg."""
     import torch
 
     import mixture_experts_layer_pack_gb300 as M
     import moe_inputs as MI
 
-    rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    cid = args.config
     c = MI.CONFIGS[cid]
     mx = c["routed"] == "mxfp8"
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
@@ -336,19 +352,21 @@ def run_ours(args):
     r = MI.config_routing(cid)
     R = int(r.routing_map.sum())
     E_act = int((r.routing_map.sum(0) > 0).sum())
+    act32 = args.act_precision == "fp32"
     w = MI.make_weights(H, I, E, seed, device=dev)
     hidden, grad_out = MI.make_activations(T, H, seed, device=dev)
     mg = MI.make_main_grads(H, I, E, seed, device=dev)
     mg_bf16 = args.main_grad_dtype == "bf16"
     mg_bytes = 2 if mg_bf16 else 4
-    workload = MI.WORKLOAD_NAMES[cid] + ("-bf16-main-grad" if mg_bf16 else "")
+    workload = MI.WORKLOAD_NAMES[cid] + ("-bf16-main-grad" if mg_bf16 else "") + ("" if act32 else "-bf16-act")
     if mg_bf16:
         mg = {n: t.to(torch.bfloat16) for n, t in mg.items()}
     probs = torch.from_numpy(r.probs).to(dev)
     rmap = torch.from_numpy(r.routing_map).to(dev).view(torch.uint8)
 
     layer = M.MoELayer(T, H, E, k, I, device=dev,
-                       routed_wtype=M.binding.MOE_W_MXFP8 if mx else M.binding.MOE_W_BF16)
+                       routed_wtype=M.binding.MOE_W_MXFP8 if mx else M.binding.MOE_W_BF16,
+                       act_precision=M.binding.MOE_ACT_FP32 if act32 else M.binding.MOE_ACT_BF16)
     wv = M.weights_from_combined(w["shared_fc1"], w["shared_fc2"], w["routed_fc1"], w["routed_fc2"])
     if mx:   # MXFP8 routed weights (rowwise + columnwise), prepared outside the timed region
         wmx = MI.make_mxfp8_weights(w)
@@ -369,7 +387,7 @@ def run_ours(args):
         M.moe_forward(layer.handle, T, hidden, probs, rmap, wv, out, layer.saved, stream)
         M.moe_backward(layer.handle, grad_out, layer.saved, dh, dp, mgv, stream)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     if layer.device_status() != 0:
@@ -380,13 +398,13 @@ def run_ours(args):
     M.moe_profile_read(layer.handle)                     # drop anything recorded before
     M.moe_profile_select(layer.handle, None)
     M.moe_profile_enable(layer.handle, True)
-    n_profile = max(5, args.steps // 4)
+    n_profile = max(5, steps // 4) if full else 3
     for _ in range(n_profile):
         step()
     torch.cuda.synchronize()
     M.moe_profile_enable(layer.handle, False)
     kernels = M.moe_profile_read(layer.handle)
-    top = max((n for n, (tot, c) in kernels.items() if c), key=lambda n: kernels[n][0])
+    top = max((n for n, (tot, cnt) in kernels.items() if cnt), key=lambda n: kernels[n][0])
 
     # ---- timed region: K steps, events only around the dominant kernel (live
     # duration for its roofline), clocks sampled
@@ -399,7 +417,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -412,10 +430,51 @@ def run_ours(args):
     top_ms_per_launch = top_ms / max(top_n, 1)
     ms = ev0.elapsed_time(ev1)
     ms_max = reduce_max([ms], world, dev)[0]
-    value = aggregate([args.steps * T] * world, ms_max / 1e3)
+    value = aggregate([steps * T] * world, ms_max / 1e3)
     flops = useful_flops(R, T, H, I)
-    tflops = flops * args.steps * world / (ms_max / 1e3) / 1e12
+    tflops = flops * steps * world / (ms_max / 1e3) / 1e12
     peaks, peaks_kind = load_peaks()
+
+    # ---- roofline of the dominant kernel (its duration from the timed region);
+    # the per-kernel table comes from the untimed per-kernel pass
+    per_kernel = {}
+    for name, (tot, n) in kernels.items():
+        if n:
+            per_kernel[name] = {"ms_per_launch": tot / n, "launches": n, "share": 0.0}
+    total_k = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
+    for v in per_kernel.values():
+        v["share"] = v["ms_per_launch"] * v["launches"] / total_k if total_k else 0.0
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            traffic = json.load(open(tr_path)).get(workload, {}).get(top)
+        except Exception:
+            traffic = None
+    work = lambda n: kernel_work(n, T, H, E, k, I, R, E_act, mx, mg_bytes, act32)  # noqa: E731
+    roof = roofline_of(top, top_ms_per_launch, work(top), peaks, peaks_kind, traffic,
+                       fp8=mx and top in MX_ROUTED_GEMMS)
+    roof["timed_launches"] = top_n
+    roof["mma_flops"] = mma_flops(top, work(top)[0], mx, act32)
+    for name, v in per_kernel.items():
+        f, b = work(name)
+        ms_l = v["ms_per_launch"] * 1e-3
+        v["tflops"] = f / ms_l / 1e12 if f else 0.0
+        v["mma_tflops"] = mma_flops(name, f, mx, act32) / ms_l / 1e12 if f else 0.0
+        v["gbs"] = b / ms_l / 1e9
+
+    res = {"workload": workload, "T": T, "H": H, "E": E, "k": k, "I": I, "valid_routes": R, "mx": mx,
+           "routing": c["routing"], "drop": c["drop"], "steps": steps, "warmup": warmup, "value": value,
+           "ms_per_step": ms_max / steps, "tflops": tflops, "useful_flops_per_step": flops,
+           "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+           "pct_fp8_peak": 100.0 * tflops / (2 * peaks["bf16_tflops"]) if mx else None,
+           "roofline": roof, "kernels": per_kernel, "n_profile": n_profile, "top": top, "gpu_launches": launches,
+           "clocks": clocks, "peaks": peaks, "peaks_kind": peaks_kind, "mg_bf16": mg_bf16, "act32": act32,
+           "l2": "inputs larger than L2: routed weights %.2f GB + main_grad %.2f GB per step"
+                 % (3 * E * I * H * (1.03 if mx else 2) / 1e9, 3 * (E + 1) * I * H * mg_bytes / 1e9)}
+    if not full:
+        layer.close()
+        return res
 
     # ---- forward and backward timed apart, and the step replayed as one CUDA graph
     # (no per-kernel events; launch gaps are what the graph removes)
@@ -429,9 +488,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
-    n_split = max(5, args.steps // 4)
-    fwd_ms = timed(lambda: M.moe_forward(layer.handle, T, hidden, probs, rmap, wv, out, layer.saved, stream), n_split)
-    bwd_ms = timed(lambda: M.moe_backward(layer.handle, grad_out, layer.saved, dh, dp, mgv, stream), n_split)
+    n_split = max(5, steps // 4)
+    res["fwd_ms"] = timed(lambda: M.moe_forward(layer.handle, T, hidden, probs, rmap, wv, out, layer.saved, stream),
+                          n_split)
+    res["bwd_ms"] = timed(lambda: M.moe_backward(layer.handle, grad_out, layer.saved, dh, dp, mgv, stream), n_split)
     graph = None
     try:
         cap = torch.cuda.Stream(device=dev)
@@ -443,12 +503,13 @@ def run_ours(args):
         torch.cuda.synchronize()
         for _ in range(3):
             g.replay()
-        graph_ms = reduce_max([timed(g.replay, max(10, args.steps // 2))], world, dev)[0]
+        graph_ms = reduce_max([timed(g.replay, max(10, steps // 2))], world, dev)[0]
         graph = {"ms_per_step": graph_ms, "value": T * world / (graph_ms / 1e3), "unit": "tokens/s",
-                 "kernels_per_step": launches // max(args.steps, 1)}
+                 "kernels_per_step": launches // max(steps, 1)}
         del g
     except Exception as ex:                              # capture is reported, not required
         graph = {"unavailable": f"{type(ex).__name__}: {ex}"}
+    res["cuda_graph"] = graph
     if layer.device_status() != 0:
         raise SystemExit("device status reported an error")
 
@@ -473,7 +534,7 @@ def run_ours(args):
     for i in range(3):
         e2e_step(i)
     pipe.synchronize()
-    e2e_steps = max(10, args.steps // 4)
+    e2e_steps = max(10, steps // 4)
     barrier(world)
     t0 = time.perf_counter()
     for i in range(e2e_steps):
@@ -483,59 +544,79 @@ def run_ours(args):
     e2e_s = reduce_max([time.perf_counter() - t0], world, dev)[0]
     h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_grad, h_probs, h_map))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dh, h_dp))
-    e2e = {"value": aggregate([e2e_steps * T] * world, e2e_s), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    res["e2e"] = {"value": aggregate([e2e_steps * T] * world, e2e_s), "unit": "tokens/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del pipe
+    layer.close()
+    return res
 
-    # ---- roofline of the dominant kernel (its duration from the timed region);
-    # the per-kernel table comes from the untimed per-kernel pass
-    per_kernel = {}
-    for name, (tot, n) in kernels.items():
-        if n:
-            per_kernel[name] = {"ms_per_launch": tot / n, "launches": n, "share": 0.0}
-    total_k = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
-    for v in per_kernel.values():
-        v["share"] = v["ms_per_launch"] * v["launches"] / total_k if total_k else 0.0
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
+
+def per_config_entry(res):
+    """The compact record of one extra workload."""
+    roof = res["roofline"]
+    return {"workload": res["workload"], "steps": res["steps"], "warmup": res["warmup"],
+            "ms_per_step": res["ms_per_step"], "tokens_per_s": res["value"], "useful_tflops": res["tflops"],
+            "pct_bf16_peak": res["pct_bf16_peak"], "pct_fp8_peak": res["pct_fp8_peak"],
+            "roofline": {kk: roof[kk] for kk in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                 "ms_per_launch", "traffic", "peak_source")},
+            "kernels": {n: {"ms_per_launch": v["ms_per_launch"], "share": v["share"], "gbs": v["gbs"],
+                            "tflops": v["tflops"], "mma_tflops": v["mma_tflops"]} for n, v in res["kernels"].items()},
+            "gpu_launches_per_step": res["gpu_launches"] // max(res["steps"], 1), "clocks": res["clocks"]}
+
+
+def run_ours(args):
+    import torch
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    res = measure_config(args.config, args, args.steps, args.warmup, True, dev, world, rank, local_rank)
+    torch.cuda.empty_cache()
+    cid = args.config
+    per_config = {}
+    extra = [int(x) for x in args.per_config.split(",") if x.strip()] if args.per_config else []
+    for other in extra:
+        if other == cid:
+            continue
         try:
-            traffic = json.load(open(tr_path)).get(workload, {}).get(top)
-        except Exception:
-            traffic = None
-    roof = roofline_of(top, top_ms_per_launch, kernel_work(top, T, H, E, k, I, R, E_act, mx, mg_bytes), peaks,
-                       peaks_kind, traffic, fp8=mx and top in MX_ROUTED_GEMMS)
-    roof["timed_launches"] = top_n
-    for name, v in per_kernel.items():
-        f, b = kernel_work(name, T, H, E, k, I, R, E_act, mx, mg_bytes)
-        ms_l = v["ms_per_launch"] * 1e-3
-        v["tflops"] = f / ms_l / 1e12 if f else 0.0
-        v["gbs"] = b / ms_l / 1e9
+            r2 = measure_config(other, args, args.per_config_steps, 3, False, dev, world, rank, local_rank)
+            per_config[str(other)] = per_config_entry(r2)
+        except torch.cuda.OutOfMemoryError as ex:
+            per_config[str(other)] = {"unavailable": f"out of device memory: {ex}"}
+        torch.cuda.empty_cache()
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+    peaks, peaks_kind = res["peaks"], res["peaks_kind"]
+    mx = res["mx"]
+    line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 routed / bf16 shared" if mx else "bf16",
             "data": "synthetic (seeded routing, N(0,0.02) weights, N(0,1) activations; random init)",
-            "config": {"workload": workload, "T": T, "H": H, "E": E, "k": k, "I": I,
-                       "valid_routes": R, "routing": f"seeded router stand-in ({c['routing']}, drop={c['drop']})",
+            "config": {"workload": res["workload"], "T": res["T"], "H": res["H"], "E": res["E"], "k": res["k"],
+                       "I": res["I"], "valid_routes": res["valid_routes"],
+                       "routing": f"seeded router stand-in ({res['routing']}, drop={res['drop']})",
                        "main_grad": f"{args.main_grad_dtype}, accumulated in place every step",
-                       "l2": "inputs larger than L2: routed weights %.2f GB + main_grad %.2f GB per step"
-                             % (3 * E * I * H * 2 / 1e9, 3 * (E + 1) * I * H * (2 if mg_bf16 else 4) / 1e9),
+                       "activations": ("fp32 between the expert GEMMs, derived GEMM operands as hi + lo bf16 terms"
+                                       if res["act32"] else "bf16 between the expert GEMMs"),
+                       "l2": res["l2"],
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "tflops": tflops,
-            "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
-            "pct_fp8_peak": 100.0 * tflops / (2 * peaks["bf16_tflops"]) if mx else None,
+            "tflops": res["tflops"], "pct_bf16_peak": res["pct_bf16_peak"], "pct_fp8_peak": res["pct_fp8_peak"],
             "peaks": {**peaks, "source": peaks_kind},
-            "useful_flops_per_step": flops,
-            "roofline": roof, "kernels": per_kernel,
-            "kernels_note": f"per-kernel CUDA events over {n_profile} untimed steps; the timed region brackets "
-                            f"only {top}",
-            "gpu_launches": launches, "clocks": clocks, "e2e": e2e,
-            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "cuda_graph": graph}
+            "useful_flops_per_step": res["useful_flops_per_step"],
+            "roofline": res["roofline"], "kernels": res["kernels"],
+            "kernels_note": f"per-kernel CUDA events over {res['n_profile']} untimed steps; the timed region "
+                            f"brackets only {res['top']}",
+            "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "e2e": res["e2e"],
+            "fwd_ms": res["fwd_ms"], "bwd_ms": res["bwd_ms"], "cuda_graph": res["cuda_graph"]}
+    if per_config:
+        line["per_config"] = per_config
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cid)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

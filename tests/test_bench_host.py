@@ -70,14 +70,16 @@ def test_kernel_work_table_covers_every_kernel_class():
 def test_kernel_work_counts_the_shared_expert_in_the_bf16_grouped_launches():
     """BF16 routed weights: the shared expert is group 0 of the routed launches, so their
     algorithmic work is the routed formula at R + T rows and E_act + 1 experts; with
-    MXFP8 the routed classes count the routed experts only."""
+    MXFP8 the routed classes count the routed experts only. fp32 activations: the
+    two-term [dg|du] operand is 4 bytes an element; bf16 activations: 2."""
     T, H, E, k, I, R, Ea = 4096, 2048, 96, 6, 1024, 24576, 96
-    f, b = bench.kernel_work("gemm_wgrad_fc1_routed", T, H, E, k, I, R, Ea, mx=False, mg_bytes=4)
-    assert f == 4 * (R + T) * I * H
-    assert b == (R + T) * 2 * I * 2 + (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 * 4
-    f, b = bench.kernel_work("gemm_fwd_gu_routed", T, H, E, k, I, R, Ea, mx=False)
-    assert f == 4 * (R + T) * H * I
-    assert b == (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 + (R + T) * I * 2 + (R + T) * 2 * I * 2
+    for act32, f_ in ((True, 4), (False, 2)):
+        f, b = bench.kernel_work("gemm_wgrad_fc1_routed", T, H, E, k, I, R, Ea, mx=False, mg_bytes=4, act32=act32)
+        assert f == 4 * (R + T) * I * H
+        assert b == (R + T) * 2 * I * f_ + (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 * 4
+        f, b = bench.kernel_work("gemm_fwd_gu_routed", T, H, E, k, I, R, Ea, mx=False, act32=act32)
+        assert f == 4 * (R + T) * H * I
+        assert b == (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 + (R + T) * I * f_ + (R + T) * 2 * I * f_
     f, _ = bench.kernel_work("gemm_wgrad_fc1_routed", T, H, E, k, I, R, Ea, mx=True)
     assert f == 4 * R * I * H
     # the useful flops of a step: forward, dgrad and wgrad over routed and shared rows
@@ -85,3 +87,20 @@ def test_kernel_work_counts_the_shared_expert_in_the_bf16_grouped_launches():
         bench.kernel_work(n, T, H, E, k, I, R, Ea, mx=False)[0]
         for n in ("gemm_fwd_gu_routed", "gemm_fwd_down_routed", "gemm_bwd_down_routed", "gemm_bwd_gu_routed",
                   "gemm_wgrad_fc1_routed", "gemm_wgrad_down_routed"))
+    # the tensor work executed: the four GEMMs with a two-term operand run K twice
+    assert bench.mma_flops("gemm_fwd_down_routed", 10, mx=False, act32=True) == 20
+    assert bench.mma_flops("gemm_fwd_gu_routed", 10, mx=False, act32=True) == 10
+    assert bench.mma_flops("gemm_fwd_down_routed", 10, mx=True, act32=True) == 10
+    assert bench.mma_flops("gemm_wgrad_fc1_routed", 10, mx=True, act32=True) == 20
+    assert bench.mma_flops("gemm_bwd_gu_routed", 10, mx=False, act32=False) == 10
+
+
+def test_gather_kernels_count_each_source_row_once():
+    """A hidden (or grad_out) row that k routes gather is read from HBM once: the
+    placement and the grad gather count T rows read and R rows written (the shared
+    expert's GEMMs read hidden and grad_out themselves)."""
+    T, H, E, k, I, R, Ea = 4096, 2048, 96, 6, 1024, 24576, 96
+    _, b = bench.kernel_work("gather_rows", T, H, E, k, I, R, Ea, mx=False)
+    assert b == T * H * 2 + R * H * 2
+    _, b = bench.kernel_work("gather_rows", T, H, E, k, I, R, Ea, mx=True)
+    assert b == pytest.approx(T * H * 2 + R * H * 2 + R * H * (1 + 1 / 32))
