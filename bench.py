@@ -47,6 +47,10 @@ def parse_args(argv=None):
     p.add_argument("--per-config", default="3,4,5",
                    help="further workloads measured after the headline one (comma list; empty: none)")
     p.add_argument("--per-config-steps", type=int, default=10)
+    p.add_argument("--experts", type=int, default=0,
+                   help="a reduced instance of the workload: this many routed experts (same H, I, top-k); "
+                        "the token count scales with it unless --tokens is given (profiling captures)")
+    p.add_argument("--tokens", type=int, default=0, help="with --experts: the token count of the reduced instance")
     return p.parse_args(argv)
 
 
@@ -345,11 +349,18 @@ def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank)
     import mixture_experts_layer_pack_gb300 as M
     import moe_inputs as MI
 
-    c = MI.CONFIGS[cid]
+    c = dict(MI.CONFIGS[cid])
+    reduced = ""
+    if args.experts and cid == args.config:
+        # a reduced instance: fewer experts, the same tokens per expert on average
+        T0, E0 = c["T"], c["E"]
+        c["E"] = args.experts
+        c["T"] = args.tokens or max(128, (T0 * args.experts // E0 + 127) // 128 * 128)
+        reduced = f"-reduced-E{c['E']}-T{c['T']}"
     mx = c["routed"] == "mxfp8"
     T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
     seed = MI.seed_of(cid)
-    r = MI.config_routing(cid)
+    r = MI.make_routing(T, E, k, seed, c["routing"], c["drop"])
     R = int(r.routing_map.sum())
     E_act = int((r.routing_map.sum(0) > 0).sum())
     act32 = args.act_precision == "fp32"
@@ -358,7 +369,8 @@ def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank)
     mg = MI.make_main_grads(H, I, E, seed, device=dev)
     mg_bf16 = args.main_grad_dtype == "bf16"
     mg_bytes = 2 if mg_bf16 else 4
-    workload = MI.WORKLOAD_NAMES[cid] + ("-bf16-main-grad" if mg_bf16 else "") + ("" if act32 else "-bf16-act")
+    workload = (MI.WORKLOAD_NAMES[cid] + reduced + ("-bf16-main-grad" if mg_bf16 else "") +
+                ("" if act32 else "-bf16-act"))
     if mg_bf16:
         mg = {n: t.to(torch.bfloat16) for n, t in mg.items()}
     probs = torch.from_numpy(r.probs).to(dev)

@@ -308,6 +308,25 @@ __device__ __forceinline__ void copy_quant_row(const uint4* src, uint4* dst, uin
     }
 }
 
+// dst[0, n) = src[0, n) in 16-byte vectors (src null: zeros), by one warp: each lane
+// has up to eight vectors in flight before it stores any
+__device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* __restrict__ dst, int n) {
+    const int lane = threadIdx.x & 31;
+    for (int base = 0; base < n; base += 32 * 8) {
+        uint4 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int v = base + j * 32 + lane;
+            w[j] = (src && v < n) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int v = base + j * 32 + lane;
+            if (v < n) dst[v] = w[j];
+        }
+    }
+}
+
 // SwiGLU pieces: silu(z) = z * sigmoid(z); d silu / dz = s (1 + z (1 - s))
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
 

@@ -27,7 +27,6 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     pdl_wait();
     pdl_trigger();
     const int rows = min(row0 + *n_dev, max_rows);
-    const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
         const int t = perm_src[r];
@@ -36,12 +35,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
             copy_quant_row(t >= 0 ? src + int64_t(t) * vec_per_row : nullptr, d, dst_q, dst_sf, r, vec_per_row);
             continue;
         }
-        if (t >= 0) {
-            const uint4* s = src + int64_t(t) * vec_per_row;
-            for (int v = lane; v < vec_per_row; v += 32) d[v] = __ldg(s + v);
-        } else {
-            for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
-        }
+        copy_row(t >= 0 ? src + int64_t(t) * vec_per_row : nullptr, d, vec_per_row);
     }
 }
 
@@ -151,10 +145,45 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
     }
 }
 
+// acc += sum over the valid slots s of (8 elements of row row_of_t[s] at column vector
+// v), in slot order: the row indices of up to four slots, then their rows, are loaded
+// before any is added
+template <bool F32>
+__device__ __forceinline__ void add_slots(float (&acc)[8], const void* __restrict__ rows, int vec_per_row, int v,
+                                          const int* __restrict__ row_of_t, int k) {
+    constexpr int B = 4;
+    for (int s0 = 0; s0 < k; s0 += B) {
+        int r[B];
+        Vec8<F32> val[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) r[j] = s0 + j < k ? __ldg(row_of_t + s0 + j) : -1;
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+            if (r[j] >= 0) val[j].load(rows, int64_t(r[j]) * vec_per_row + v);
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (r[j] < 0) continue;
+            float f[8];
+            val[j].to_float(f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+    }
+}
+
+// the dprob of route row r: the sum of its n_part partial dot products, in order
+__device__ __forceinline__ float route_dprob(const float* __restrict__ partial, int n_part, int r) {
+    const float* p = partial + int64_t(r) * n_part;
+    float val = 0.0f;
+    for (int j = 0; j < n_part; ++j) val += __ldg(p + j);
+    return val;
+}
+
 // dhidden[t] = dx_shared[t] (+ dz[t] w, the shared output gate's term) + sum
 // over valid slots of dx_perm[row_of[t,s]];
 // dprobs[t,e] = sum of the dprob partials of the route (t,e), 0 off the map; with
-// slot_dprobs, dprobs[t,s] of slot s instead (0 for an empty slot)
+// slot_dprobs, dprobs[t,s] of slot s instead (0 for an empty slot); written by a
+// second grid-stride pass over the dprobs entries
 template <bool F32>
 __global__ void __launch_bounds__(256) unpermute_kernel(const void* __restrict__ dxs, const void* __restrict__ dxp,
                                                         const int* __restrict__ row_of, const int* __restrict__ ids,
@@ -183,21 +212,13 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const void* __restrict__
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = fmaf(d, wf[j], acc[j]);
         }
-        for (int s = 0; s < k; ++s) {
-            const int r = __ldg(row_of + int64_t(t) * k + s);
-            if (r >= 0) add_x8<F32>(acc, dxp, int64_t(r) * vec_per_row + v);
-        }
+        add_slots<F32>(acc, dxp, vec_per_row, v, row_of + int64_t(t) * k, k);
         dhidden[i] = pack_bf16x8(acc);
     }
     if (slot_dprobs) {
         for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < int64_t(T) * k; i += stride) {
             const int r = __ldg(row_of + i);
-            float val = 0.0f;
-            if (r >= 0) {
-                const float* p = partial + int64_t(r) * n_part;
-                for (int j = 0; j < n_part; ++j) val += p[j];
-            }
-            dprobs[i] = val;
+            dprobs[i] = r >= 0 ? route_dprob(partial, n_part, r) : 0.0f;
         }
         return;
     }
@@ -206,13 +227,9 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const void* __restrict__
         const int t = int(i / E);
         const int e = int(i - int64_t(t) * E);
         float val = 0.0f;
-        for (int s = 0; s < k; ++s) {
-            if (__ldg(ids + int64_t(t) * k + s) == e) {
-                const int r = __ldg(row_of + int64_t(t) * k + s);
-                const float* p = partial + int64_t(r) * n_part;
-                for (int j = 0; j < n_part; ++j) val += p[j];
-            }
-        }
+        for (int s = 0; s < k; ++s)
+            if (__ldg(ids + int64_t(t) * k + s) == e)
+                val = route_dprob(partial, n_part, __ldg(row_of + int64_t(t) * k + s));
         dprobs[i] = val;
     }
 }

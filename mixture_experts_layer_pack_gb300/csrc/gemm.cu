@@ -42,22 +42,26 @@ constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
 constexpr uint32_t kStageTileBytes = 32 * 32 * 4;  // fp32 staging box of one epilogue warp (32 rows x 32 cols)
 constexpr int kRing = 4;  // weight gradient: depth of the claimed-tile ring
 
-// SPLIT (the down projection, the dgrad through gate/up): the A operand comes as
-// hi + lo bf16 terms and its lo tile rides in the same stage, so the B tile is
-// loaded once for both products
+// SPLIT: one operand comes as hi + lo bf16 terms (the A operand of the down
+// projection and of the dgrad through gate/up; A or B of the weight gradients) and
+// its lo tile rides in the same stage (L_BYTES: an A tile, or for the weight
+// gradient the larger of A and B), so the other operand's tile crosses L2 once for
+// both products
 template <int OP, int BN, bool SPLIT = false>
 struct Cfg {
-    static_assert(!SPLIT || OP == OP_FWD_DOWN || OP == OP_BWD_GU, "paired lo tiles: A operand of fprop/dgrad");
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = BN * kBK * 2;
-    static constexpr uint32_t L_BYTES = SPLIT ? A_BYTES : 0;
+    static constexpr uint32_t L_BYTES = SPLIT ? ((OP == OP_WGRAD && B_BYTES > A_BYTES) ? B_BYTES : A_BYTES) : 0;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + L_BYTES;
     // the weight-gradient epilogue double-buffers its main_grad boxes, so it
-    // gives up operand stages (its K per tile is one expert's short segment)
+    // gives up operand stages (its K per tile is one expert's short segment); the
+    // SwiGLU-backward epilogue (dgrad-down) moves more bytes than its mainloop, and
+    // three stages leave it more of the memory system than four (measured)
     static constexpr int BUFS = (OP == OP_WGRAD) ? 2 : 1;
     static constexpr int STAGES =
-        (OP == OP_WGRAD) ? ((BN == 256) ? 3 : (BN == 128 ? 5 : 6))
-                         : (SPLIT ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)));
+        (OP == OP_WGRAD) ? (SPLIT ? ((BN == 256) ? 2 : 3) : ((BN == 256) ? 3 : (BN == 128 ? 5 : 6)))
+                         : (SPLIT ? ((BN == 256) ? 3 : 4)
+                                  : ((BN == 256) ? (OP == OP_BWD_DOWN ? 3 : 4) : (BN == 128 ? 6 : 8)));
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
     static constexpr uint32_t STAGING = kEpiWarps * BUFS * kStageTileBytes;
     static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING + 1024 + 512;
@@ -82,12 +86,8 @@ __host__ __device__ constexpr uint32_t instr_desc() {
            (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
 }
 
-// Weight gradient with a split operand: the K range runs twice, the first
-// kb_half blocks with the hi terms and the next kb_half with the lo terms (the
-// other operand's blocks load again), into one accumulator. (The forward and
-// dgrad GEMMs carry the lo tile in the same stage instead: SPLIT builds.)
 struct Tile {
-    int mt, nt, e, k_lo, kblocks, kb_half;
+    int mt, nt, e, k_lo, kblocks;
 };
 
 template <int OP>
@@ -103,15 +103,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a) {
         const int hi = a.seg_off ? a.seg_off[t.e + 1] : a.seg_len;
         t.k_lo = lo;
         t.kblocks = (hi - lo + kBK - 1) / kBK;
-        t.kb_half = a.split ? t.kblocks : INT_MAX;
-        if (a.split) t.kblocks *= 2;
     } else {
         t.mt = tile / a.n_tiles;
         t.nt = tile - t.mt * a.n_tiles;
         t.e = a.mtile_expert ? a.mtile_expert[t.mt] : 0;
         t.k_lo = 0;
         t.kblocks = a.k_blocks;
-        t.kb_half = INT_MAX;
     }
     return t;
 }
@@ -140,16 +137,22 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint8_t* sa, 
     if (g0 && a.g0_operand == 1) mA = mG;
     if (OP == OP_WGRAD) {
         if (g0 && a.g0_operand == 2) mB0 = mG;
-        if (kb >= t.kb_half) {  // the second pass of a split weight gradient: the lo terms
-            kb -= t.kb_half;
-            if (a.split == 1) mA = mL;
-            else mB0 = mL;
-        }
         const int krow = t.k_lo + kb * kBK;
 #pragma unroll
         for (int c = 0; c < kBM / 64; ++c) tma_load_2d(sa + c * kMnChunkBytes, mA, bar, t.mt * kBM + 64 * c, krow);
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * kMnChunkBytes, mB0, bar, t.nt * BN + 64 * c, krow);
+        if (SPLIT) {
+            if (a.split == 2) {
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c)
+                    tma_load_2d(sl + c * kMnChunkBytes, mL, bar, t.nt * BN + 64 * c, krow);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBM / 64; ++c)
+                    tma_load_2d(sl + c * kMnChunkBytes, mL, bar, t.mt * kBM + 64 * c, krow);
+            }
+        }
         return;
     }
     const int k0 = kb * kBK;
@@ -805,7 +808,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES +
+                                                            (SPLIT ? (args.split == 2 ? C::B_BYTES : C::A_BYTES) : 0));
                     issue_loads<OP, BN, SPLIT>(t, kb, sa, sa + C::A_BYTES, sa + C::A_BYTES + C::B_BYTES, &tmA, &tmB0,
                                                &tmB1, &tmS0, &tmS1, &tmL, &tmG, &full[stage], args);
                     filled |= 1u << stage;
@@ -866,13 +870,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                                  : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
                         mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if (SPLIT) {  // the lo terms of A times the same B, into the same accumulator
+                    if (SPLIT) {
                         const uint32_t l_addr = b_addr + C::B_BYTES;
+                        const bool lo_b = args.split == 2;
+                        const uint32_t a2 = lo_b ? a_addr : l_addr;
+                        const uint32_t b2 = lo_b ? l_addr : b_addr;
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint64_t ad = smem_desc(l_addr + kk * 32, 16, kSwizzleAtom);
-                            const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 2048, kMnChunkBytes, kSwizzleAtom)
-                                                     : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
+                            const uint64_t ad = A_MN ? smem_desc(a2 + kk * 2048, kMnChunkBytes, kSwizzleAtom)
+                                                     : smem_desc(a2 + kk * 32, 16, kSwizzleAtom);
+                            const uint64_t bd = B_MN ? smem_desc(b2 + kk * 2048, kMnChunkBytes, kSwizzleAtom)
+                                                     : smem_desc(b2 + kk * 32, 16, kSwizzleAtom);
                             mma_bf16(d_tmem, ad, bd, IDESC, 1u);
                         }
                     }
@@ -1195,12 +1203,11 @@ cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStrea
     return e;
 }
 
-// the split (paired-stage) builds exist for the down projection and the dgrad
-// through gate/up; a split weight gradient runs its K range twice in the plain build
+// the split builds exist for the GEMMs that take a two-term operand
 template <int OP, bool CLAMP = false>
 cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
-    constexpr bool CAN_SPLIT = OP == OP_FWD_DOWN || OP == OP_BWD_GU;
-    if (a.split && !CAN_SPLIT && OP != OP_WGRAD) return cudaErrorInvalidValue;
+    constexpr bool CAN_SPLIT = OP == OP_FWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD;
+    if (a.split && !CAN_SPLIT) return cudaErrorInvalidValue;
     if (CAN_SPLIT && a.split) {
         switch (bn) {
             case 256: return launch_one<OP, 256, CLAMP, CAN_SPLIT>(m, a, grid, st);

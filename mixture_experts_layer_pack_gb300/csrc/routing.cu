@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         if (x_q)
             copy_quant_row(src, dst, x_q, x_sf, pos, vec_per_row);
         else
-            for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+            copy_row(src, dst, vec_per_row);
         return;
     }
     const int64_t j = item - n_routes;
@@ -463,11 +463,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
             pp_perm[pos] = tok ? 1.0f : 0.0f;  // the shared output gate, when there is one, overwrites it
         }
         if (!copy_shared) return;  // the GEMMs read the shared rows from hidden itself
-        uint4* dst = x_perm + pos * vec_per_row;
-        if (tok)
-            for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(hidden + int64_t(t) * vec_per_row + v);
-        else
-            for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        copy_row(tok ? hidden + int64_t(t) * vec_per_row : nullptr, x_perm + pos * vec_per_row, vec_per_row);
         return;
     }
     const int e = int(j / kBM);
@@ -484,7 +480,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     if (x_q)
         copy_quant_row(nullptr, dst, x_q, x_sf, pos, vec_per_row);
     else
-        for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        copy_row(nullptr, dst, vec_per_row);
 }
 
 __global__ void export_routing_kernel(const int* __restrict__ ids, const int* __restrict__ row_of,

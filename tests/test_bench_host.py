@@ -104,3 +104,32 @@ def test_gather_kernels_count_each_source_row_once():
     assert b == T * H * 2 + R * H * 2
     _, b = bench.kernel_work("gather_rows", T, H, E, k, I, R, Ea, mx=True)
     assert b == pytest.approx(T * H * 2 + R * H * 2 + R * H * (1 + 1 / 32))
+
+
+# Per-launch times (ms) of every kernel class at the proxy-like workload (T=4096,
+# H=2048, E=96 top-6, I=1024, R=24576 routes, every expert with tokens), measured on
+# one GB300 with `python bench.py` (CUDA events, fp32 and bf16 activations).
+RECORDED_MS = {
+    True: {"route_place": 0.0253, "gather_rows": 0.0265, "gemm_fwd_gu_routed": 0.2650,
+           "gemm_fwd_down_routed": 0.1875, "combine": 0.0476, "gemm_bwd_down_routed": 0.2415,
+           "gemm_bwd_gu_routed": 0.3459, "gemm_wgrad_fc1_routed": 0.6144, "gemm_wgrad_down_routed": 0.3190,
+           "unpermute": 0.0550},
+    False: {"route_place": 0.0248, "gather_rows": 0.0269, "gemm_fwd_gu_routed": 0.2304,
+            "gemm_fwd_down_routed": 0.1197, "combine": 0.0312, "gemm_bwd_down_routed": 0.2086,
+            "gemm_bwd_gu_routed": 0.2178, "gemm_wgrad_fc1_routed": 0.5335, "gemm_wgrad_down_routed": 0.2819,
+            "unpermute": 0.0390},
+}
+
+
+@pytest.mark.parametrize("act32", [True, False])
+def test_recorded_kernel_rates_stay_below_the_measured_peaks(act32):
+    """The algorithmic bytes (and flops) of every kernel class over its measured time
+    stay at or below the measured copy bandwidth (and bf16 tensor peak) x 1.05: the
+    byte counts do not count a row that several routes read as read several times."""
+    T, H, E, k, I, R, Ea = 4096, 2048, 96, 6, 1024, 24576, 96
+    peaks = bench.load_peaks()[0]
+    for name, ms in RECORDED_MS[act32].items():
+        f, b = bench.kernel_work(name, T, H, E, k, I, R, Ea, mx=False, mg_bytes=4, act32=act32)
+        assert b / (ms * 1e-3) / 1e9 <= 1.05 * peaks["hbm_gbs"], name
+        mma = bench.mma_flops(name, f, mx=False, act32=act32)
+        assert mma / (ms * 1e-3) / 1e12 <= 1.05 * peaks["bf16_tflops"], name
