@@ -213,11 +213,14 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4, act32=True)
         "shared_gate_fwd": (2 * T * H, T * H * b2 + H * b2 + T * b4),
         "shared_gate_bwd": (2 * T * H, T * H * b2 + T * b4 * 3 + H * 2 * mg_bytes),
     }
+    # the shared expert is group 0 of the routed launches: of all six GEMMs with BF16
+    # routed weights, of the two weight gradients with MXFP8 ones
+    for op in ("wgrad_fc1", "wgrad_down") if mx else ("fwd_gu", "fwd_down", "bwd_down", "bwd_gu", "wgrad_fc1",
+                                                      "wgrad_down"):
+        rf, rb = table[f"gemm_{op}_routed"]
+        sf, sb = table[f"gemm_{op}_shared"]
+        table[f"gemm_{op}_routed"] = (rf + sf, rb + sb)
     if not mx:
-        for op in ("fwd_gu", "fwd_down", "bwd_down", "bwd_gu", "wgrad_fc1", "wgrad_down"):
-            rf, rb = table[f"gemm_{op}_routed"]
-            sf, sb = table[f"gemm_{op}_shared"]
-            table[f"gemm_{op}_routed"] = (rf + sf, rb + sb)
         f_, b_ = table["route_place"]
         table["route_place"] = (f_, b_ + T * 8)   # the shared rows' source and scale (the GEMMs read hidden)
     return table[name]

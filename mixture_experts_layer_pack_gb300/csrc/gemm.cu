@@ -783,22 +783,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t filled = 0, fill_parity = 0;  // per stage: ever filled / parity of its last fill
             bool ok = true;
             int claimed = 0;  // weight gradient: tiles published into the ring so far
+            // weight gradient: the tile claimed for the next turn; its claim (an atomic on
+            // the launch's counter) is issued a turn ahead, so its round trip overlaps the
+            // current tile's loads
+            int ahead = (OP == OP_WGRAD) ? atomicAdd(args.tile_counter, 1) : 0;
             for (int next = blockIdx.x; ok; next += gridDim.x) {
                 int tile = next;
                 if (OP == OP_WGRAD) {
-                    // claim the next tile with work from the launch's counter and publish
-                    // it (-1 once the counter has passed the last tile)
+                    // publish the claimed tile with work (-1 once the counter has passed
+                    // the last tile), then claim the next one
                     const int slot = claimed % kRing;
                     if (!mbar_wait(&ring_empty[slot], ((claimed / kRing) & 1) ^ 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
-                    do {
+                    tile = ahead;
+                    while (tile < total_tiles && decode_tile<OP>(tile, args).kblocks == 0)
                         tile = atomicAdd(args.tile_counter, 1);
-                    } while (tile < total_tiles && decode_tile<OP>(tile, args).kblocks == 0);
                     ring_tile[slot] = tile < total_tiles ? tile : -1;
                     mbar_arrive(&ring_full[slot]);
                     ++claimed;
+                    if (tile < total_tiles) ahead = atomicAdd(args.tile_counter, 1);
                 }
                 if (tile >= total_tiles) break;
                 const Tile t = decode_tile<OP>(tile, args);

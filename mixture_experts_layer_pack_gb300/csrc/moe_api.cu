@@ -846,7 +846,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
                                   b.hist, ws.status, st)); }
     { Timed tm_(h, MOE_K_ROUTE_SCAN, st);
     MOE_CU(launch_route_scan_chunks(b.hist, Ti, E, b.counts, b.offsets, b.offs_pad, b.mtile_expert, b.meta,
-                                    v.R0 / kBM, mx ? nullptr : b.mtile_x, b.seg_x, st)); }
+                                    v.R0 / kBM, b.mtile_x, b.seg_x, st)); }
     MOE_TRY(redispatch(h, saved, st));
     GemmMaps m{};
     // down projection (y in bf16; the combine weights it by the route's prob or the gate)
@@ -956,6 +956,17 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
 
     // the weight-gradient launches claim their tiles from these counters
     MOE_CU(cudaMemsetAsync(ws.tile_counters, 0, 4 * sizeof(int), st));
+    if (mx && v.R0 > Ti) {
+        // the shared expert's separate dgrad-down launch writes rows [0, T); the grouped
+        // weight gradients read its region up to R0, so the rows past T hold zeros
+        const size_t tail = size_t(v.R0 - Ti);
+        MOE_CU(cudaMemsetAsync(ws.dgdu_all + size_t(Ti) * 2 * I, 0, tail * 2 * I * sizeof(__nv_bfloat16), st));
+        MOE_CU(cudaMemsetAsync(ws.ap_all + size_t(Ti) * I, 0, tail * I * sizeof(__nv_bfloat16), st));
+        if (s.act32) {
+            MOE_CU(cudaMemsetAsync(ws.dgdulo_all + size_t(Ti) * 2 * I, 0, tail * 2 * I * sizeof(__nv_bfloat16), st));
+            MOE_CU(cudaMemsetAsync(ws.aplo_all + size_t(Ti) * I, 0, tail * I * sizeof(__nv_bfloat16), st));
+        }
+    }
     // recompute_dispatch: the rows, the gate values and a, [g|u] again, into the workspace
     if (s.recompute) MOE_TRY(redispatch(h, saved, st));
     { Timed tm_(h, MOE_K_GATHER, st);
@@ -1023,10 +1034,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.n_tiles = I / bn;
         a.k_blocks = H / kBK;
         a.rows_valid = Ti;
-        // fp32 activations: the down projection's weight gradient takes (gate *) a from
-        // here as hi + lo terms; bf16 ones: a itself unless gated
-        set_bwd_down_io(s, a, b.a_all, b.gu_all, b.gu32, ws.dgdu_all, ws.dgdulo_all,
-                        (gated || s.act32) ? ws.ap_all : nullptr, ws.aplo_all);
+        // (gate *) a for the down projection's weight gradient (its shared rows)
+        set_bwd_down_io(s, a, b.a_all, b.gu_all, b.gu32, ws.dgdu_all, ws.dgdulo_all, ws.ap_all, ws.aplo_all);
         if (gated) {  // the gate acts as the shared rows' prob: dgate partials, gate * a_shared
             a.row_scale = b.pp_all;
             a.partial = ws.partial_s;
@@ -1103,8 +1112,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         Timed tm_(h, MOE_K_BWD_GU_SHARED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    // wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e (BF16 routed weights: the
-    // shared expert as group 0, whose long K range is claimed first)
+    // wgrad of gate/up: main_grad[e] += [dg|du]_e^T X_e, the shared expert as group 0
+    // (its long K range is claimed first); both weight gradients are BF16 GEMMs with
+    // either routed weight type
     {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wfc1;
@@ -1118,28 +1128,19 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         MOE_TRY(routed_mg_map(h, TB_MG_U, mg->routed_up, mg->expert_ptrs[1], I, H, mg->strides[4][0],
                               mg->strides[4][1], mg_bf16, st, &m.c1, &a.c1_tab));
         if (s.act32) {  // [dg|du] as hi + lo terms
-            if (!(mx ? map_mnmajor(&m.lo, v.dgdulo, rows, 2 * I, 2 * I)
-                     : map_mnmajor(&m.lo, ws.dgdulo_all, rows_all, 2 * I, 2 * I)))
-                return MOE_ERR_INVALID_ARG;
+            if (!map_mnmajor(&m.lo, ws.dgdulo_all, rows_all, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
             a.split = 1;
         }
-        if (mx) {
-            if (!map_mnmajor(&m.a, v.dgdu, rows, 2 * I, 2 * I) || !map_mnmajor(&m.b0, v.x_perm, rows, H, H))
-                return MOE_ERR_INVALID_ARG;
-            a.seg_off = b.offs_pad;
-            a.groups = E;
-        } else {
-            if (!map_mnmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I) ||
-                !map_mnmajor(&m.b0, b.x_all, rows_all, H, H) ||
-                !map_mnmajor(&m.g0, saved->hidden, Ti, H, H) ||
-                !map_main_grad(&m.s0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1], mg_bf16) ||
-                !map_main_grad(&m.s1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
-                return MOE_ERR_INVALID_ARG;
-            a.seg_off = b.seg_x;
-            a.groups = E + 1;
-            a.group0_shared = 1;
-            a.g0_operand = 2;   // x rows of the shared expert: hidden
-        }
+        // the shared expert is group 0 (its x rows: hidden), with either routed weight type
+        if (!map_mnmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I) || !map_mnmajor(&m.b0, b.x_all, rows_all, H, H) ||
+            !map_mnmajor(&m.g0, saved->hidden, Ti, H, H) ||
+            !map_main_grad(&m.s0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1], mg_bf16) ||
+            !map_main_grad(&m.s1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
+            return MOE_ERR_INVALID_ARG;
+        a.seg_off = b.seg_x;
+        a.groups = E + 1;
+        a.group0_shared = 1;
+        a.g0_operand = 2;
         m.b1 = m.b0;
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.groups) * a.m_tiles * a.n_tiles, h->sms), st));
@@ -1155,74 +1156,23 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         MOE_TRY(routed_mg_map(h, TB_MG_D, mg->routed_down, mg->expert_ptrs[2], H, I, mg->strides[5][0],
                               mg->strides[5][1], mg_bf16, st, &m.c0, &a.c0_tab));
         if (s.act32) {  // p * a as hi + lo terms
-            if (!(mx ? map_mnmajor(&m.lo, v.aplo, rows, I, I) : map_mnmajor(&m.lo, ws.aplo_all, rows_all, I, I)))
-                return MOE_ERR_INVALID_ARG;
+            if (!map_mnmajor(&m.lo, ws.aplo_all, rows_all, I, I)) return MOE_ERR_INVALID_ARG;
             a.split = 2;
         }
-        if (mx) {
-            if (!map_mnmajor(&m.a, v.go_perm, rows, H, H) || !map_mnmajor(&m.b0, v.ap, rows, I, I))
-                return MOE_ERR_INVALID_ARG;
-            a.seg_off = b.offs_pad;
-            a.groups = E;
-        } else {
-            if (!map_mnmajor(&m.a, ws.go_all, rows_all, H, H) || !map_mnmajor(&m.b0, ws.ap_all, rows_all, I, I) ||
-                !map_mnmajor(&m.g0, go, Ti, H, H) ||
-                !map_main_grad(&m.s0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16))
-                return MOE_ERR_INVALID_ARG;
-            a.seg_off = b.seg_x;
-            a.groups = E + 1;
-            a.group0_shared = 1;
-            a.g0_operand = 1;   // grad_out rows of the shared expert: grad_out
-        }
+        // the shared expert is group 0 (its grad_out rows: grad_out), with either routed weight type
+        if (!map_mnmajor(&m.a, ws.go_all, rows_all, H, H) || !map_mnmajor(&m.b0, ws.ap_all, rows_all, I, I) ||
+            !map_mnmajor(&m.g0, go, Ti, H, H) ||
+            !map_main_grad(&m.s0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16))
+            return MOE_ERR_INVALID_ARG;
+        a.seg_off = b.seg_x;
+        a.groups = E + 1;
+        a.group0_shared = 1;
+        a.g0_operand = 1;
         m.b1 = m.b0;
         m.c1 = m.c0;
         m.s1 = m.s0;
         Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.groups) * a.m_tiles * a.n_tiles, h->sms), st));
-    }
-    if (mx) {  // shared wgrad of gate/up (BF16)
-        GemmArgs a = base_args(ws.status, s);
-        const int bn = s.bn_wfc1;
-        if (!map_mnmajor(&m.a, ws.dgdu_all, Ti, 2 * I, 2 * I) || !map_mnmajor(&m.b0, saved->hidden, Ti, H, H))
-            return MOE_ERR_INVALID_ARG;
-        if (s.act32) {
-            if (!map_mnmajor(&m.lo, ws.dgdulo_all, Ti, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
-            a.split = 1;
-        }
-        m.b1 = m.b0;
-        a.seg_len = Ti;
-        a.groups = 1;
-        a.m_tiles = 2 * I / kBM;
-        a.n_tiles = H / bn;
-        if (!map_main_grad(&m.c0, mg->shared_gate, 1, I, H, 0, mg->strides[0][1], mg_bf16) ||
-            !map_main_grad(&m.c1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
-            return MOE_ERR_INVALID_ARG;
-        a.m_split = I;
-        a.mg_bf16 = mg_bf16;
-        a.tile_counter = ws.tile_counters + 2;
-        Timed tm_(h, MOE_K_WGRAD_FC1_SHARED, st);
-        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
-    }
-    if (mx) {  // shared wgrad of down (BF16)
-        GemmArgs a = base_args(ws.status, s);
-        const int bn = s.bn_wd;
-        if (!map_mnmajor(&m.a, go, Ti, H, H) || !map_mnmajor(&m.b0, (gated || s.act32) ? ws.ap_all : b.a_all, Ti, I, I))
-            return MOE_ERR_INVALID_ARG;
-        if (s.act32) {
-            if (!map_mnmajor(&m.lo, ws.aplo_all, Ti, I, I)) return MOE_ERR_INVALID_ARG;
-            a.split = 2;
-        }
-        m.b1 = m.b0;
-        a.seg_len = Ti;
-        a.groups = 1;
-        a.m_tiles = H / kBM;
-        a.n_tiles = I / bn;
-        if (!map_main_grad(&m.c0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16)) return MOE_ERR_INVALID_ARG;
-        m.c1 = m.c0;
-        a.mg_bf16 = mg_bf16;
-        a.tile_counter = ws.tile_counters + 3;
-        Timed tm_(h, MOE_K_WGRAD_DOWN_SHARED, st);
-        MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.m_tiles) * a.n_tiles, h->sms), st));
     }
     // dhidden = shared + un-permuted routed dgrad; dense dprobs
     Timed tm_(h, MOE_K_UNPERMUTE, st);

@@ -70,7 +70,7 @@ def test_kernel_work_table_covers_every_kernel_class():
 def test_kernel_work_counts_the_shared_expert_in_the_bf16_grouped_launches():
     """BF16 routed weights: the shared expert is group 0 of the routed launches, so their
     algorithmic work is the routed formula at R + T rows and E_act + 1 experts; with
-    MXFP8 the routed classes count the routed experts only. fp32 activations: the
+    MXFP8 routed weights only the two weight gradients are grouped that way. fp32 activations: the
     two-term [dg|du] operand is 4 bytes an element; bf16 activations: 2."""
     T, H, E, k, I, R, Ea = 4096, 2048, 96, 6, 1024, 24576, 96
     for act32, f_ in ((True, 4), (False, 2)):
@@ -80,8 +80,10 @@ def test_kernel_work_counts_the_shared_expert_in_the_bf16_grouped_launches():
         f, b = bench.kernel_work("gemm_fwd_gu_routed", T, H, E, k, I, R, Ea, mx=False, act32=act32)
         assert f == 4 * (R + T) * H * I
         assert b == (R + T) * H * 2 + (Ea + 1) * 2 * I * H * 2 + (R + T) * I * f_ + (R + T) * 2 * I * f_
+    f, _ = bench.kernel_work("gemm_fwd_gu_routed", T, H, E, k, I, R, Ea, mx=True)
+    assert f == 4 * R * I * H                         # MXFP8: the shared expert's forward runs apart
     f, _ = bench.kernel_work("gemm_wgrad_fc1_routed", T, H, E, k, I, R, Ea, mx=True)
-    assert f == 4 * R * I * H
+    assert f == 4 * (R + T) * I * H                   # its weight gradients are group 0 of the routed ones
     # the useful flops of a step: forward, dgrad and wgrad over routed and shared rows
     assert bench.useful_flops(R, T, H, I) == sum(
         bench.kernel_work(n, T, H, E, k, I, R, Ea, mx=False)[0]
