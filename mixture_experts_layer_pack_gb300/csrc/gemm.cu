@@ -41,6 +41,7 @@ constexpr uint32_t kMnChunkBytes = 8192;  // 64 K-rows x 128 bytes
 
 constexpr uint32_t kStageTileBytes = 32 * 32 * 4;  // fp32 staging box of one epilogue warp (32 rows x 32 cols)
 constexpr int kRing = 4;  // weight gradient: depth of the claimed-tile ring
+constexpr int kRingInts = 6;  // a ring slot: the tile index, then its decoded mt, nt, e, k_lo, kblocks
 
 // SPLIT: one operand comes as hi + lo bf16 terms (the A operand of the down
 // projection and of the dgrad through gate/up; A or B of the weight gradients) and
@@ -550,18 +551,27 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
     const bool bf = args.mg_bf16 != 0;
     const int bw = bf ? 64 : 32;                           // box width in elements
     const int nb = (BN / bw - half + kEpiHalves - 1) / kEpiHalves;  // boxes of this warp per tile
-    // tile at ring position pos (-1: no more tiles, -2: the wait gave up); the
-    // position is released to the producer as soon as it has been read
-    auto ring_take = [&](int pos) -> int {
-        int v = -2;
+    // tile at ring position pos (-1: no more tiles, -2: the wait gave up) and its
+    // decoded coordinates, as the producer published them; the position is released
+    // to the producer as soon as it has been read
+    auto ring_take = [&](int pos, Tile& tt) -> int {
+        int v[kRingInts] = {-2, 0, 0, 0, 0, 0};
         if (lane == 0) {
             const int slot = pos % kRing;
             if (mbar_wait(const_cast<uint64_t*>(&ring_full[slot]), (pos / kRing) & 1, abort_flag, args.status)) {
-                v = ring_tile[slot];
+#pragma unroll
+                for (int j = 0; j < kRingInts; ++j) v[j] = ring_tile[slot * kRingInts + j];
                 mbar_arrive(&ring_empty[slot]);
             }
         }
-        return __shfl_sync(0xffffffffu, v, 0);
+#pragma unroll
+        for (int j = 0; j < kRingInts; ++j) v[j] = __shfl_sync(0xffffffffu, v[j], 0);
+        tt.mt = v[1];
+        tt.nt = v[2];
+        tt.e = v[3];
+        tt.k_lo = v[4];
+        tt.kblocks = v[5];
+        return v[0];
     };
     // box (tile t, c-th box of this warp): destination map and coordinates (group
     // 0's own maps when it is the shared expert; a routed expert's own descriptor
@@ -586,8 +596,8 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
     };
 
     int rpos = 0;
-    int cur = ring_take(rpos++);
-    Tile t = decode_tile<OP_WGRAD>(cur >= 0 ? cur : 0, args);
+    Tile t;
+    int cur = ring_take(rpos++, t);
     uint32_t pending = 0, parity = 0;  // per buffer: a load in flight / parity of its next completion
     if (nb > 0 && cur >= 0 && lane == 0) {
         load_box(t, 0, 0);
@@ -606,9 +616,9 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
         tc_fence_after();
         const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
         // the producer publishes the next tile once this one's loads are issued
-        const int nxt = ring_take(rpos++);
+        Tile tn;
+        const int nxt = ring_take(rpos++, tn);
         if (nxt == -2) break;
-        const Tile tn = decode_tile<OP_WGRAD>(nxt >= 0 ? nxt : 0, args);
 #pragma unroll 1
         for (int c = 0; c < nb; ++c) {
             const int b = jb & 1;
@@ -722,7 +732,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* ring_full = mg_bar + 2 * kEpiWarps;
     uint64_t* ring_empty = ring_full + kRing;
     int* ring_tile = reinterpret_cast<int*>(ring_empty + kRing);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_tile + kRing);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_tile + kRing * kRingInts);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -789,6 +799,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int ahead = (OP == OP_WGRAD) ? atomicAdd(args.tile_counter, 1) : 0;
             for (int next = blockIdx.x; ok; next += gridDim.x) {
                 int tile = next;
+                Tile tw{};  // weight gradient: the claimed tile, decoded once here
                 if (OP == OP_WGRAD) {
                     // publish the claimed tile with work (-1 once the counter has passed
                     // the last tile), then claim the next one
@@ -798,15 +809,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tile = ahead;
-                    while (tile < total_tiles && decode_tile<OP>(tile, args).kblocks == 0)
+                    Tile tt = decode_tile<OP>(tile < total_tiles ? tile : 0, args);
+                    while (tile < total_tiles && tt.kblocks == 0) {
                         tile = atomicAdd(args.tile_counter, 1);
-                    ring_tile[slot] = tile < total_tiles ? tile : -1;
+                        tt = decode_tile<OP>(tile < total_tiles ? tile : 0, args);
+                    }
+                    int* rs = ring_tile + slot * kRingInts;
+                    rs[0] = tile < total_tiles ? tile : -1;
+                    rs[1] = tt.mt;
+                    rs[2] = tt.nt;
+                    rs[3] = tt.e;
+                    rs[4] = tt.k_lo;
+                    rs[5] = tt.kblocks;
                     mbar_arrive(&ring_full[slot]);
                     ++claimed;
                     if (tile < total_tiles) ahead = atomicAdd(args.tile_counter, 1);
+                    tw = tt;
                 }
                 if (tile >= total_tiles) break;
-                const Tile t = decode_tile<OP>(tile, args);
+                const Tile t = (OP == OP_WGRAD) ? tw : decode_tile<OP>(tile, args);
                 for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) {
                         ok = false;
@@ -842,16 +863,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int next = blockIdx.x; ok; next += gridDim.x) {
                 int tile = next;
-                if (OP == OP_WGRAD) {  // the next claimed tile, in the producer's order
+                Tile t;
+                if (OP == OP_WGRAD) {  // the next claimed tile, in the producer's order, decoded there
                     const int slot = rpos % kRing;
                     if (!mbar_wait(&ring_full[slot], (rpos / kRing) & 1, abort_flag, args.status)) break;
-                    tile = ring_tile[slot];
+                    const int* rs = ring_tile + slot * kRingInts;
+                    tile = rs[0];
+                    t.mt = rs[1];
+                    t.nt = rs[2];
+                    t.e = rs[3];
+                    t.k_lo = rs[4];
+                    t.kblocks = rs[5];
                     mbar_arrive(&ring_empty[slot]);
                     ++rpos;
                     if (tile < 0) break;
+                } else {
+                    if (tile >= total_tiles) break;
+                    t = decode_tile<OP>(tile, args);
                 }
                 if (tile >= total_tiles) break;
-                const Tile t = decode_tile<OP>(tile, args);
                 if (t.kblocks == 0) continue;
                 const int buf = it & 1;
                 const uint32_t use = uint32_t(it >> 1);
