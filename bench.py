@@ -528,7 +528,8 @@ def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank)
     if layer.device_status() != 0:
         raise SystemExit("device status reported an error")
 
-    # ---- end to end through the public API: pinned host inputs in, results out
+    # ---- end to end through the C ABI's host-buffer entry (moe_host_step): pinned
+    # host inputs in, results out, every step
     h_hidden = hidden.cpu().pin_memory()
     h_grad = grad_out.cpu().pin_memory()
     h_probs = probs.cpu().pin_memory()
@@ -540,7 +541,7 @@ def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank)
     # step's download while the host could still be reading them
     h_res = [(h_out, h_dh, h_dp)] + [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                                            for t in (h_out, h_dh, h_dp))]
-    pipe = layer.host_steps(T)
+    pipe = layer.host_pipe(T)
 
     def e2e_step(i):
         pipe.step(h_hidden, h_probs, h_map, h_grad, wv, mgv, *h_res[i % 2])
@@ -560,8 +561,8 @@ def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank)
     h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_grad, h_probs, h_map))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dh, h_dp))
     res["e2e"] = {"value": aggregate([e2e_steps * T] * world, e2e_s), "unit": "tokens/s",
-                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    del pipe
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": "moe_host_step"}
+    pipe.close()
     layer.close()
     return res
 

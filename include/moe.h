@@ -248,6 +248,54 @@ moe_status moe_forward_topk(moe_handle* h, int64_t T, const void* hidden, const 
 moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* saved,
                         void* dhidden, float* dprobs, const moe_main_grads* mg, void* stream);
 
+/* The configuration a handle was created with. */
+moe_status moe_handle_config(const moe_handle* h, moe_config* cfg);
+
+/* ---- Steps fed from HOST memory ----
+ * A forward + backward step whose inputs and results live in host memory
+ * (the pages' backend is called with device tensors; this pipeline is the
+ * library's own entry for callers that hold a batch on the host). Each step
+ * copies hidden, probs, routing_map and grad_out to the device, runs
+ * moe_forward and moe_backward on them, and copies out, dhidden and dprobs
+ * back. The copies run on two streams of the pipeline's own, joined to the
+ * compute stream by events, into two alternating device staging sets, so that
+ * one step's uploads and downloads overlap the kernels of its neighbours. */
+typedef struct moe_host_pipe moe_host_pipe;
+
+/* Bytes of device memory a pipeline for steps of exactly T tokens needs (two
+ * staging sets of hidden, probs, routing_map, grad_out, out, dhidden, dprobs,
+ * and one saved state); 1 <= T <= cfg->max_tokens. */
+moe_status moe_host_pipe_size(const moe_config* cfg, int64_t T, size_t* bytes);
+
+/* Creates a pipeline of `h` over caller-owned device memory (256-byte aligned,
+ * >= moe_host_pipe_size bytes for h's configuration, kept alive and unused by
+ * others until moe_host_pipe_destroy). The pipeline owns two non-blocking CUDA
+ * streams and six events (host-side objects, released by destroy); it
+ * allocates no device memory. */
+moe_status moe_host_pipe_create(moe_handle* h, int64_t T, void* memory, size_t bytes, moe_host_pipe** out);
+
+/* Enqueues one step and returns. HOST pointers: hidden[T,H] bf16, probs[T,E]
+ * fp32, routing_map[T,E] bytes, grad_out[T,H] bf16 in; out[T,H] bf16,
+ * dhidden[T,H] bf16, dprobs[T,E] fp32 receive the results (dense dprobs, as
+ * moe_backward after moe_forward). w and mg as for moe_forward / moe_backward
+ * (device weights and main_grads: main_grad += dW every step, steps applied in
+ * call order). Inputs must stay unchanged, and results unread, until the step
+ * is complete (moe_host_pipe_sync). Page-locked host memory (cudaHostAlloc,
+ * cudaHostRegister) gives asynchronous copies; pageable memory works but the
+ * call then returns only after the step's downloads are done. `stream` is the
+ * compute stream (any stream; the pipeline orders its steps itself).
+ * Argument errors return before anything is enqueued; the device status
+ * (moe_device_status) reports kernel-detected errors as for moe_forward. */
+moe_status moe_host_step(moe_host_pipe* p, const void* hidden, const float* probs, const uint8_t* routing_map,
+                         const void* grad_out, const moe_weights* w, const moe_main_grads* mg, void* out,
+                         void* dhidden, float* dprobs, void* stream);
+
+/* Blocks until every enqueued step's results are in host memory. */
+moe_status moe_host_pipe_sync(moe_host_pipe* p);
+
+/* Waits for the pipeline's steps, then releases its streams and events. */
+void moe_host_pipe_destroy(moe_host_pipe* p);
+
 /* MXFP8 weight preparation (PR #6572, Design > MCore-owned parameters:
  * converted scale layouts refreshed once per optimizer iteration at stable
  * addresses; PR #8210 review on _swizzle_mxfp8_scale): converts the routed

@@ -53,7 +53,9 @@ _LOCK = threading.Lock()
 EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size", "moe_saved_create",
             "moe_saved_destroy", "moe_forward", "moe_backward", "moe_export_routing", "moe_device_status",
             "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name",
-            "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8", "moe_profile_select")
+            "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8", "moe_profile_select",
+            "moe_forward_topk", "moe_handle_config", "moe_host_pipe_size", "moe_host_pipe_create", "moe_host_step",
+            "moe_host_pipe_sync", "moe_host_pipe_destroy")
 MOE_K_COUNT = 20
 
 
@@ -103,10 +105,19 @@ def load(build_if_missing: bool = True):
                                          c_void_p]
         L.moe_status_string.argtypes = [c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_handle_config.argtypes = [c_void_p, P(moe_config)]
+        L.moe_host_pipe_size.argtypes = [P(moe_config), c_int64, P(c_size_t)]
+        L.moe_host_pipe_create.argtypes = [c_void_p, c_int64, c_void_p, c_size_t, P(c_void_p)]
+        L.moe_host_step.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, P(moe_weights),
+                                    P(moe_main_grads), c_void_p, c_void_p, c_void_p, c_void_p]
+        L.moe_host_pipe_sync.argtypes = [c_void_p]
+        L.moe_host_pipe_destroy.argtypes = [c_void_p]
+        L.moe_host_pipe_destroy.restype = None
         for name in ("moe_workspace_size", "moe_saved_size", "moe_create", "moe_saved_create", "moe_forward",
                      "moe_backward", "moe_export_routing", "moe_device_status", "moe_profile_enable",
                      "moe_profile_read", "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8",
-                     "moe_profile_select"):
+                     "moe_profile_select", "moe_handle_config", "moe_host_pipe_size", "moe_host_pipe_create",
+                     "moe_host_step", "moe_host_pipe_sync"):
             getattr(L, name).restype = c_int32
         _LIB = L
         return L
@@ -183,6 +194,41 @@ def moe_forward_topk(h, T, hidden, topk_ids, topk_probs, weights: moe_weights, o
 def moe_backward(h, grad_out, saved, dhidden, dprobs, main_grads: moe_main_grads, stream=None):
     _check(load().moe_backward(h, _ptr(grad_out), saved, _ptr(dhidden), _ptr(dprobs), ctypes.byref(main_grads),
                                _stream_ptr(stream)), "moe_backward")
+
+
+def moe_handle_config(h) -> moe_config:
+    c = moe_config()
+    _check(load().moe_handle_config(h, ctypes.byref(c)), "moe_handle_config")
+    return c
+
+
+def moe_host_pipe_size(cfg: moe_config, T: int) -> int:
+    n = c_size_t(0)
+    _check(load().moe_host_pipe_size(ctypes.byref(cfg), int(T), ctypes.byref(n)), "moe_host_pipe_size")
+    return n.value
+
+
+def moe_host_pipe_create(h, T: int, memory) -> c_void_p:
+    p = c_void_p()
+    _check(load().moe_host_pipe_create(h, int(T), _ptr(memory), memory.numel() * memory.element_size(),
+                                       ctypes.byref(p)), "moe_host_pipe_create")
+    return p
+
+
+def moe_host_step(p, hidden, probs, routing_map, grad_out, weights: moe_weights, main_grads: moe_main_grads,
+                  out, dhidden, dprobs, stream=None):
+    """One forward + backward step from HOST tensors (include/moe.h, moe_host_step)."""
+    _check(load().moe_host_step(p, _ptr(hidden), _ptr(probs), _ptr(routing_map), _ptr(grad_out),
+                                ctypes.byref(weights), ctypes.byref(main_grads), _ptr(out), _ptr(dhidden),
+                                _ptr(dprobs), _stream_ptr(stream)), "moe_host_step")
+
+
+def moe_host_pipe_sync(p):
+    _check(load().moe_host_pipe_sync(p), "moe_host_pipe_sync")
+
+
+def moe_host_pipe_destroy(p):
+    load().moe_host_pipe_destroy(p)
 
 
 def moe_export_routing(h, saved, ids=None, pp=None, counts=None, offsets=None, perm_src=None, row_of=None,
@@ -429,9 +475,9 @@ class MoELayer:
     def device_status(self, stream=None) -> int:
         return moe_device_status(self.handle, stream)
 
-    def host_steps(self, T):
-        """A HostSteps pipeline of forward + backward steps of T tokens from host buffers."""
-        return HostSteps(self, T)
+    def host_pipe(self, T):
+        """A HostPipe of forward + backward steps of T tokens from host buffers."""
+        return HostPipe(self, T)
 
     def close(self):
         if getattr(self, "handle", None) is not None:
@@ -446,92 +492,57 @@ class MoELayer:
             pass
 
 
-class HostSteps:
-    """Forward + backward steps of a layer fed from pinned host buffers, with the
-    copies overlapped with the GPU work of the neighbouring steps.
-
-    Each step's inputs go up on an upload stream into one of two device staging
-    sets while the previous step computes; its results come down on a download
-    stream while the next step computes. Every step still uploads its own inputs
-    and downloads its own results. `step` only enqueues work and returns an event
-    that completes when that step's results are in the host buffers; the host
-    buffers of a step must stay untouched until then. Steps run in call order on
-    one compute stream, so main_grad accumulates exactly as with sequential calls."""
+class HostPipe:
+    """Forward + backward steps of a layer fed from host buffers, through the C
+    ABI's host pipeline (moe_host_pipe_create / moe_host_step): every step
+    uploads its inputs and downloads its results, the copies overlapped with the
+    kernels of the neighbouring steps. Device staging memory is a torch buffer
+    held here; the steps apply to main_grad in call order."""
 
     def __init__(self, layer: "MoELayer", T: int):
         import torch
         self.layer = layer
         self.T = int(T)
-        dev = layer.device
-        H, E = layer.cfg.hidden, layer.cfg.num_experts
-        self.up = torch.cuda.Stream(dev)
-        self.compute = torch.cuda.Stream(dev)
-        self.down = torch.cuda.Stream(dev)
-
-        def staging():
-            return {"hidden": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
-                    "probs": torch.empty((T, E), dtype=torch.float32, device=dev),
-                    "map": torch.empty((T, E), dtype=torch.uint8, device=dev),
-                    "grad": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
-                    "out": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
-                    "dh": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
-                    "dp": torch.empty((T, E), dtype=torch.float32, device=dev)}
-
-        self.sets = [staging(), staging()]
-        self.uploaded = [torch.cuda.Event(), torch.cuda.Event()]    # the set's inputs are on the device
-        self.computed = [torch.cuda.Event(), torch.cuda.Event()]    # its step ran: inputs free, results ready
-        self.downloaded = [torch.cuda.Event(), torch.cuda.Event()]  # its results are in host memory
-        self.used = [False, False]
-        self.n = 0
+        self.compute = torch.cuda.Stream(layer.device)
+        self.memory = torch.empty(moe_host_pipe_size(layer.cfg, self.T), dtype=torch.uint8, device=layer.device)
+        with torch.cuda.device(layer.device):
+            self.pipe = moe_host_pipe_create(layer.handle, self.T, self.memory)
 
     def step(self, hidden, probs, routing_map, grad_out, weights: moe_weights, main_grads: moe_main_grads,
              out, dhidden, dprobs):
-        """Enqueues one step: host (pinned) hidden[T,H] bf16, probs[T,E] f32, routing_map[T,E]
+        """Enqueues one step: host hidden[T,H] bf16, probs[T,E] f32, routing_map[T,E]
         (bool or uint8), grad_out[T,H] bf16 in; host out[T,H], dhidden[T,H] bf16 and
-        dprobs[T,E] f32 receive the results. Returns the step's completion event."""
+        dprobs[T,E] f32 receive the results once `synchronize` returns. Page-locked
+        tensors only (pageable ones would make every call wait for its step)."""
         import torch
         for t in (hidden, probs, routing_map, grad_out, out, dhidden, dprobs):
-            if t.is_cuda or not t.is_pinned():
-                raise ValueError("HostSteps.step takes pinned host tensors")
+            if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+                raise ValueError("HostPipe.step takes contiguous pinned host tensors")
         if hidden.shape[0] != self.T:
             raise ValueError("token count differs from the pipeline's")
-        s = self.n % 2
-        self.n += 1
-        b = self.sets[s]
-        if self.used[s]:
-            self.up.wait_event(self.computed[s])        # the set's previous step has read its inputs
-        with torch.cuda.stream(self.up):
-            b["hidden"].copy_(hidden, non_blocking=True)
-            b["probs"].copy_(probs, non_blocking=True)
-            b["map"].copy_(routing_map.view(torch.uint8), non_blocking=True)
-            b["grad"].copy_(grad_out, non_blocking=True)
-            self.uploaded[s].record(self.up)
-        self.compute.wait_event(self.uploaded[s])
-        if self.used[s]:
-            self.compute.wait_event(self.downloaded[s])  # the set's previous results have left
-        self.layer.forward(b["hidden"], b["probs"], b["map"], weights, out=b["out"], stream=self.compute)
-        self.layer.backward(b["grad"], main_grads, dhidden=b["dh"], dprobs=b["dp"], stream=self.compute)
-        self.computed[s].record(self.compute)
-        self.down.wait_event(self.computed[s])
-        with torch.cuda.stream(self.down):
-            out.copy_(b["out"], non_blocking=True)
-            dhidden.copy_(b["dh"], non_blocking=True)
-            dprobs.copy_(b["dp"], non_blocking=True)
-            self.downloaded[s].record(self.down)
-        self.used[s] = True
-        return self.downloaded[s]
+        H, E = self.layer.cfg.hidden, self.layer.cfg.num_experts
+        for t, shape, dt in ((hidden, (self.T, H), torch.bfloat16), (grad_out, (self.T, H), torch.bfloat16),
+                             (out, (self.T, H), torch.bfloat16), (dhidden, (self.T, H), torch.bfloat16),
+                             (probs, (self.T, E), torch.float32), (dprobs, (self.T, E), torch.float32)):
+            if tuple(t.shape) != shape or t.dtype != dt:
+                raise ValueError("host tensor of the wrong shape or dtype")
+        if tuple(routing_map.shape) != (self.T, E) or routing_map.element_size() != 1:
+            raise ValueError("routing_map must be [T,E] bytes")
+        moe_host_step(self.pipe, hidden, probs, routing_map, grad_out, weights, main_grads, out, dhidden, dprobs,
+                      self.compute)
 
     def synchronize(self):
-        """Waits for every enqueued step (results in host memory)."""
-        self.up.synchronize()
-        self.compute.synchronize()
-        self.down.synchronize()
+        """Waits until every enqueued step's results are in host memory."""
+        moe_host_pipe_sync(self.pipe)
+
+    def close(self):
+        if getattr(self, "pipe", None) is not None:
+            moe_host_pipe_destroy(self.pipe)   # waits for the steps in flight
+            self.pipe = None
 
     def __del__(self):
-        # the staging buffers go back to the caching allocator with this object:
-        # no copy or kernel of the pipeline may still be using them
         try:
-            self.synchronize()
+            self.close()
         except Exception:
             pass
 

@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmoe.so")
-SOURCES = ["gemm.cu", "routing.cu", "elementwise.cu", "mxfp8.cu", "gate.cu", "moe_api.cu"]
+SOURCES = ["gemm.cu", "routing.cu", "elementwise.cu", "mxfp8.cu", "gate.cu", "moe_api.cu", "host_pipe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

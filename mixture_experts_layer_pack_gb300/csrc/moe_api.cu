@@ -665,6 +665,12 @@ moe_status moe_create(const moe_config* cfg, void* workspace, size_t workspace_b
     return MOE_OK;
 }
 
+moe_status moe_handle_config(const moe_handle* h, moe_config* cfg) {
+    if (!h || !cfg) return MOE_ERR_INVALID_ARG;
+    *cfg = h->cfg;
+    return MOE_OK;
+}
+
 void moe_destroy(moe_handle* h) {
     if (!h) return;
     for (auto& r : h->recs) {

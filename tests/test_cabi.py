@@ -78,6 +78,26 @@ def test_null_arguments_rejected():
     assert L.moe_create(ctypes.byref(_cfg()), None, 0, ctypes.byref(h)) == 1
     assert L.moe_forward(None, 0, None, None, None, None, None, None, None) == 1
     assert L.moe_backward(None, None, None, None, None, None, None) == 1
+    p = ctypes.c_void_p()
+    assert L.moe_host_pipe_create(None, 16, None, 0, ctypes.byref(p)) == 1
+    assert L.moe_host_step(None, *([None] * 10)) == 1
+    assert L.moe_host_pipe_sync(None) == 1
+    assert L.moe_handle_config(None, ctypes.byref(_cfg())) == 1
+
+
+def test_host_pipe_sizes():
+    """Two staging sets of T rows and one saved state: the size grows with T by
+    2 x (4 [T,H] bf16 + 2 [T,E] fp32 + 1 [T,E] byte) per token, and T must lie in
+    [1, max_tokens]."""
+    c = _cfg()
+    a, b = M.moe_host_pipe_size(c, 1024), M.moe_host_pipe_size(c, 2048)
+    per_token = 2 * (4 * c.hidden * 2 + 2 * c.num_experts * 4 + c.num_experts)
+    assert b - a == pytest.approx(1024 * per_token, abs=2 * 14 * 256)   # 256-byte rounding of 14 buffers
+    assert a > M.moe_saved_size(c)
+    for T in (0, c.max_tokens + 1):
+        with pytest.raises(B.MoeError) as ei:
+            M.moe_host_pipe_size(c, T)
+        assert ei.value.status == 1
 
 
 def _c_layout(tmp_path):
