@@ -252,11 +252,10 @@ __device__ __forceinline__ float e8m0_scale(uint32_t code) {
 }
 
 // four fp32 -> four E4M3 codes (round to nearest even, saturating at +-448), first in the low byte
+// (two paired conversions: the first value of each pair lands in the low byte)
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-    return uint32_t(__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3)) |
-           (uint32_t(__nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3)) << 8) |
-           (uint32_t(__nv_cvt_float_to_fp8(c, __NV_SATFINITE, __NV_E4M3)) << 16) |
-           (uint32_t(__nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3)) << 24);
+    return uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3)) |
+           (uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3)) << 16);
 }
 
 // value of an E4M3 code
@@ -328,6 +327,8 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* _
 }
 
 // SwiGLU pieces: silu(z) = z * sigmoid(z); d silu / dz = s (1 + z (1 - s))
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// logistic function with the hardware reciprocal: a few ulp from the correctly rounded
+// value; 0 where exp(-z) overflows
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 }  // namespace moe

@@ -980,12 +980,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // copies into a per-stage TMEM slot with tcgen05.cp; the four K=32 MMAs of a
 // stage select their K block through the scale-factor id of the instruction
 // descriptor.
+// (the dgrad-down's SwiGLU-backward epilogue moves more bytes than its mainloop:
+// three stages leave it more of the memory system than five, 206 against 235 us
+// at T=4096, H=2048, E=96 top-6, I=1024; the other ops stream operands, five)
+template <int OP>
 struct MxCfg {
     static constexpr uint32_t A_BYTES = kBM * kMxBK;
     static constexpr uint32_t B_BYTES = kMxBN * kMxBK;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t SF_BYTES = 1024;  // A atom + B atom
-    static constexpr int STAGES = 5;
+    static constexpr int STAGES = OP == OP_BWD_DOWN ? 3 : 5;
     static constexpr uint32_t STAGING = kEpiWarps * kStageTileBytes;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t SF_TMEM = 2 * kMxBN;  // scale slots after the two accumulators, 8 columns a stage
@@ -1030,7 +1034,7 @@ template <int OP, bool CLAMP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-    using C = MxCfg;
+    using C = MxCfg<OP>;
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU);
     constexpr int STAGES = C::STAGES;
     constexpr int BN = kMxBN;
@@ -1212,11 +1216,11 @@ cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaSt
     static bool attr_set = false;
     auto kern = moe_gemm_mx_kernel<OP, CLAMP>;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(MxCfg::SMEM));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(MxCfg<OP>::SMEM));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), MxCfg::SMEM, st, m.a, m.b0, m.b1, a);
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), MxCfg<OP>::SMEM, st, m.a, m.b0, m.b1, a);
     count_launch();
     return e;
 }
