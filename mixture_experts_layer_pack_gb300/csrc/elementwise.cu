@@ -16,27 +16,43 @@ namespace moe {
 
 namespace {
 
-// dst[r] = src[perm_src[r]] for every permuted row (zero for padding rows);
-// one warp per row, 16-byte vectors
+// The grad gather, walked from the token side: item t*k + s copies row t of src
+// to the permuted row row_of[t,s] of dst (nothing for a missing route); items
+// past T*k zero the padding rows at the end of each expert's segment
+// (offs_pad[e] + counts[e] up to the next multiple of 128). Consecutive warps
+// take the slots of one token, so each source row leaves DRAM once however its
+// slots are spread over the experts. One warp per item, 16-byte vectors; with
+// dst_q the row is also quantised to MXFP8 along H.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
-                                                          const int* __restrict__ perm_src,
-                                                          const int* __restrict__ n_dev, int row0, int max_rows,
-                                                          int vec_per_row,
-                                                          uint4* __restrict__ dst, uint8_t* __restrict__ dst_q,
-                                                          uint8_t* __restrict__ dst_sf) {
+                                                          const int* __restrict__ row_of,
+                                                          const int* __restrict__ counts,
+                                                          const int* __restrict__ offs_pad, int T, int E, int k,
+                                                          int vec_per_row, uint4* __restrict__ dst,
+                                                          uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf) {
     pdl_wait();
     pdl_trigger();
-    const int rows = min(row0 + *n_dev, max_rows);
-    const int warps = (gridDim.x * blockDim.x) >> 5;
-    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
-        const int t = perm_src[r];
-        uint4* d = dst + int64_t(r) * vec_per_row;
-        if (dst_q) {  // also quantise the row to MXFP8 (the routed dgrad-down GEMM's operand)
-            copy_quant_row(t >= 0 ? src + int64_t(t) * vec_per_row : nullptr, d, dst_q, dst_sf, r, vec_per_row);
-            continue;
-        }
-        copy_row(t >= 0 ? src + int64_t(t) * vec_per_row : nullptr, d, vec_per_row);
+    const int64_t item = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int64_t n_routes = int64_t(T) * k;
+    const uint4* from = nullptr;
+    int64_t pos;
+    if (item < n_routes) {
+        pos = __ldg(row_of + item);
+        if (pos < 0) return;
+        from = src + (item / k) * vec_per_row;
+    } else {
+        const int64_t j = item - n_routes;
+        if (j >= int64_t(E) * kBM) return;
+        const int e = int(j / kBM);
+        const int r = int(j % kBM);
+        const int cnt = __ldg(counts + e);
+        if (r >= (cnt + kBM - 1) / kBM * kBM - cnt) return;
+        pos = __ldg(offs_pad + e) + cnt + r;
     }
+    uint4* d = dst + pos * vec_per_row;
+    if (dst_q)  // the routed dgrad-down GEMM's operand
+        copy_quant_row(from, d, dst_q, dst_sf, pos, vec_per_row);
+    else
+        copy_row(from, d, vec_per_row);
 }
 
 // 8 elements of a row, element index 8 * i: one 16-byte vector of bf16 or two of fp32
@@ -243,12 +259,13 @@ int grid_for(int64_t work, int threads, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* n_dev, int row0,
-                               int max_rows, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms,
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* row_of, const int* counts, const int* offs_pad,
+                               int T, int E, int k, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf,
                                cudaStream_t st) {
-    const int grid = grid_for(int64_t(max_rows) * 32, 256, num_sms);
-    const cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, st,
-                                     reinterpret_cast<const uint4*>(src), perm_src, n_dev, row0, max_rows, H / 8,
+    const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
+    const int64_t blocks = (items + 7) / 8;
+    const cudaError_t e = launch_pdl(gather_rows_kernel, dim3(unsigned(blocks)), dim3(256), 0, st,
+                                     reinterpret_cast<const uint4*>(src), row_of, counts, offs_pad, T, E, k, H / 8,
                                      reinterpret_cast<uint4*>(dst), dst_q, dst_sf);
     count_launch();
     return e;

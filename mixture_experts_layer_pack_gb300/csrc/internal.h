@@ -152,8 +152,10 @@ cudaError_t launch_export_routing(const int* ids, const int* row_of, const int* 
 
 // elementwise / copy
 // dst row r (r < row0 + *n_dev, r < max_rows) = src row perm_src[r], a zero row where it is -1
-cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_src, const int* n_dev, int row0,
-                               int max_rows, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf, int num_sms,
+// dst[row_of[t,s]] = src[t] for every valid route, zero padding rows (counts, offs_pad:
+// the routed segments); with dst_q also the rows' MXFP8 quantisation along H
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* row_of, const int* counts, const int* offs_pad,
+                               int T, int E, int k, int H, __nv_bfloat16* dst, uint8_t* dst_q, uint8_t* dst_sf,
                                cudaStream_t st);
 // ys, y (and dxs, dxp): fp32 rows when f32, else bf16
 cudaError_t launch_combine(const void* ys, const float* gate, const void* y, bool f32, const int* row_of,

@@ -976,10 +976,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     // recompute_dispatch: the rows, the gate values and a, [g|u] again, into the workspace
     if (s.recompute) MOE_TRY(redispatch(h, saved, st));
     { Timed tm_(h, MOE_K_GATHER, st);
-    if (mx)
-        MOE_CU(launch_gather_rows(go, v.perm_src, b.meta + 2, 0, rows, H, v.go_perm, ws.go_q, ws.go_sf, h->sms, st));
-    else  // routed rows (the GEMMs read the shared expert's rows from grad_out itself)
-        MOE_CU(launch_gather_rows(go, v.perm_src, b.meta + 2, 0, rows, H, v.go_perm, nullptr, nullptr, h->sms, st)); }
+    // routed rows only: the GEMMs read the shared expert's rows from grad_out itself
+    MOE_CU(launch_gather_rows(go, b.row_of, b.counts, b.offs_pad, Ti, E, k, H, v.go_perm, mx ? ws.go_q : nullptr,
+                              mx ? ws.go_sf : nullptr, st)); }
 
     GemmMaps m{};
     // dgrad through the down projection + SwiGLU backward + dprob partials
