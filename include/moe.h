@@ -88,7 +88,20 @@ typedef struct {
     float swiglu_limit;   /* 0: no clamp; L > 0: SwiGLU input clamp (above) */
     int32_t recompute_dispatch; /* 0 or 1; see below */
     int32_t act_precision; /* moe_act: MOE_ACT_FP32 (0, default) or MOE_ACT_BF16 */
+    int32_t no_shared_expert; /* 0 (default): the layer has the shared expert; 1: see below */
 } moe_config;
+/* no_shared_expert = 1: routed experts only. out[t] = sum_s pp[t,s] y[t,s],
+ * dhidden the routed part alone; the shared weight views, the shared main_grad
+ * buffers and the output gate are ignored (NULL is fine; an output gate is
+ * MOE_ERR_INVALID_ARG). This is the owner-side step of expert parallelism
+ * (PR #6572, Validation: EP16 / EP64; "core.transformer.moe.megakernel.mok.backend",
+ * MoKMegakernel: ep_group): a rank that owns experts [e0, e1) runs them on the
+ * token rows it received, in expert order, through moe_forward_topk on a handle
+ * with num_experts = e1 - e0 and topk = 1 (ids = local expert, probs = the
+ * route's prob): out rows come back prob-weighted, and the matching
+ * moe_backward gives the rows' dx (prob-weighted), the per-route dprob in
+ * dprobs[n,1] and the local experts' main_grad accumulation. The token side
+ * keeps the shared expert and sums the returned rows. */
 /* recompute_dispatch = 1 (redispatch in backward: PR #8210 review thread on
  * CUDA graphs, per-layer replay needs the saved schedule and activations to
  * survive pending microbatches, which a redispatch in backward provides): a
@@ -137,6 +150,7 @@ typedef struct {
 } moe_wview;
 
 typedef struct {
+    /* (with no_shared_expert the three shared views are ignored) */
     moe_wview shared_gate, shared_up, shared_down, routed_gate, routed_up, routed_down;
     /* Optional output gate of the shared expert ("core.transformer.moe.megakernel.
      * mok.runtime", _MoKAutograd.forward: shared_output_gate_weight;
@@ -152,7 +166,8 @@ typedef struct {
  * strides[i] = {expert_stride, row_stride} in elements (expert_stride unused
  * for the shared three). Fused accumulation is mandatory (PR #6572, Design >
  * Gradient accumulation): every pointer must be non-null, 16-byte aligned,
- * strides multiples of 16 bytes. shared_output_gate is the [H] main_grad of
+ * strides multiples of 16 bytes (with no_shared_expert the shared three are
+ * ignored and may be NULL). shared_output_gate is the [H] main_grad of
  * the shared expert's output gate: required (16-byte aligned) when the forward
  * recorded in `saved` had a gate, ignored otherwise.
  * dtype (moe_gtype) applies to every buffer. MOE_G_FP32: main_grad += dW in

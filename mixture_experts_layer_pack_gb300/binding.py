@@ -25,7 +25,7 @@ WEIGHT_NAMES = ("shared_gate", "shared_up", "shared_down", "routed_gate", "route
 class moe_config(ctypes.Structure):
     _fields_ = [("max_tokens", c_int64), ("hidden", c_int64), ("num_experts", c_int64), ("topk", c_int64),
                 ("inter", c_int64), ("routed_wtype", c_int32), ("swiglu_limit", c_float),
-                ("recompute_dispatch", c_int32), ("act_precision", c_int32)]
+                ("recompute_dispatch", c_int32), ("act_precision", c_int32), ("no_shared_expert", c_int32)]
 
 
 class moe_wview(ctypes.Structure):
@@ -330,10 +330,12 @@ def wview(t, scale=None, col_data=None, col_scale=None) -> moe_wview:
 
 def weights_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, shared_output_gate=None) -> moe_weights:
     """Gate/up views of combined FC1 weights ([2I,H], [E,2I,H]): rows [0,I) gate, [I,2I) up;
-    optional bf16 [H] shared-expert output gate."""
-    inter = shared_fc1.shape[0] // 2
-    return moe_weights(wview(shared_fc1[:inter]), wview(shared_fc1[inter:]), wview(shared_fc2),
-                       wview(routed_fc1[:, :inter]), wview(routed_fc1[:, inter:]), wview(routed_fc2),
+    optional bf16 [H] shared-expert output gate. shared_fc1 / shared_fc2 None: no shared
+    views (a layer without a shared expert ignores them)."""
+    inter = routed_fc1.shape[1] // 2
+    shared = (moe_wview(), moe_wview(), moe_wview()) if shared_fc1 is None else \
+        (wview(shared_fc1[:inter]), wview(shared_fc1[inter:]), wview(shared_fc2))
+    return moe_weights(*shared, wview(routed_fc1[:, :inter]), wview(routed_fc1[:, inter:]), wview(routed_fc2),
                        None if shared_output_gate is None else shared_output_gate.data_ptr())
 
 
@@ -341,16 +343,19 @@ def main_grads_from_combined(shared_fc1, shared_fc2, routed_fc1, routed_fc2, sha
     """Six-buffer main_grad order over combined FC1/FC2 buffers, all fp32 or all
     bf16 (plus the optional [H] main_grad of the shared-expert output gate)."""
     import torch
-    inter = shared_fc1.shape[0] // 2
-    views = (shared_fc1[:inter], shared_fc1[inter:], shared_fc2,
-             routed_fc1[:, :inter], routed_fc1[:, inter:], routed_fc2)
-    dtypes = {v.dtype for v in views} | ({shared_output_gate.dtype} if shared_output_gate is not None else set())
+    inter = routed_fc1.shape[1] // 2
+    shared = (None, None, None) if shared_fc1 is None else (shared_fc1[:inter], shared_fc1[inter:], shared_fc2)
+    views = shared + (routed_fc1[:, :inter], routed_fc1[:, inter:], routed_fc2)
+    present = [v for v in views if v is not None]
+    dtypes = {v.dtype for v in present} | ({shared_output_gate.dtype} if shared_output_gate is not None else set())
     if dtypes not in ({torch.float32}, {torch.bfloat16}):
         raise ValueError(f"main_grad buffers must be all fp32 or all bf16, got {dtypes}")
-    m = moe_main_grads(*[v.data_ptr() for v in views])
+    m = moe_main_grads(*[None if v is None else v.data_ptr() for v in views])
     m.dtype = MOE_G_BF16 if dtypes == {torch.bfloat16} else MOE_G_FP32
     m.shared_output_gate = None if shared_output_gate is None else shared_output_gate.data_ptr()
     for i, v in enumerate(views):
+        if v is None:
+            continue
         if v.dim() == 3:
             m.strides[i][0], m.strides[i][1] = v.stride(0), v.stride(1)
         else:
@@ -427,11 +432,12 @@ class MoELayer:
     """Holds a handle, its workspace and one saved-state block (all torch device memory)."""
 
     def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16,
-                 swiglu_limit=0.0, recompute_dispatch=False, act_precision=None):
+                 swiglu_limit=0.0, recompute_dispatch=False, act_precision=None, shared_expert=True):
         import torch
         self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, float(swiglu_limit),
                               int(bool(recompute_dispatch)),
-                              MOE_ACT_FP32 if act_precision is None else int(act_precision))
+                              MOE_ACT_FP32 if act_precision is None else int(act_precision),
+                              0 if shared_expert else 1)
         self.device = torch.device(device)
         ws = moe_workspace_size(self.cfg)
         sv = moe_saved_size(self.cfg)

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
         const int t = int(i / vec_per_row);
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        fma_x8<F32>(acc, ys, i, gate ? __ldg(gate + t) : 1.0f);
+        if (ys) fma_x8<F32>(acc, ys, i, gate ? __ldg(gate + t) : 1.0f);  // no shared expert: ys null
         acc_slots<F32>(acc, y, vec_per_row, v, row_of + int64_t(t) * k, pp + int64_t(t) * k, k);
         out[i] = pack_bf16x8(acc);
     }
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const void* __restrict__
         const int t = int(i / vec_per_row);
         const int v = int(i - int64_t(t) * vec_per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        add_x8<F32>(acc, dxs, i);
+        if (dxs) add_x8<F32>(acc, dxs, i);  // no shared expert: dxs null
         if (dz) {
             const float d = __ldg(dz + t);
             const uint4 wv = __ldg(gate_w + v);

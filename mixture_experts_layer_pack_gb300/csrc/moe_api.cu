@@ -45,6 +45,7 @@ struct Shape {
     bool recompute;   // recompute_dispatch: the backward redoes placement and gate/up
     bool act32;       // MOE_ACT_FP32: fp32 g|u, y, dx; derived GEMM operands as hi + lo bf16 terms
     float limit;      // swiglu_limit (0: none)
+    bool shared;      // the layer has the shared expert (no_shared_expert = 0)
 };
 
 // carves consecutive 256-byte aligned pieces out of one block
@@ -67,6 +68,8 @@ moe_status check_config(const moe_config* c, Shape* s) {
     if (!(c->swiglu_limit >= 0.0f) || !std::isfinite(c->swiglu_limit)) return MOE_ERR_INVALID_ARG;
     if (c->recompute_dispatch != 0 && c->recompute_dispatch != 1) return MOE_ERR_INVALID_ARG;
     if (c->act_precision != MOE_ACT_FP32 && c->act_precision != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->no_shared_expert != 0 && c->no_shared_expert != 1) return MOE_ERR_INVALID_ARG;
+    s->shared = c->no_shared_expert == 0;
     s->recompute = c->recompute_dispatch != 0;
     s->act32 = c->act_precision == MOE_ACT_FP32;
     s->limit = c->swiglu_limit;
@@ -81,7 +84,7 @@ moe_status check_config(const moe_config* c, Shape* s) {
     s->k = c->topk;
     s->I = c->inter;
     s->rows = align_up(size_t(s->Tmax * s->k + s->E * (kBM - 1)), kBM);
-    s->srows = align_up(size_t(s->Tmax), kBM);
+    s->srows = s->shared ? align_up(size_t(s->Tmax), kBM) : 0;
     if (s->rows + s->srows >= INT_MAX / 2 || s->Tmax * s->k >= INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
     if (s->Tmax > route_rank_max_tokens()) return MOE_ERR_UNSUPPORTED;
     s->bn_gu = pick_bn(2 * s->I, true);
@@ -253,7 +256,7 @@ size_t carve_saved(const Shape& s, uint8_t* base, SavedBufs* b) {
 
 Views views_of(const Shape& s, const SavedBufs& b, const Workspace& w, int64_t T) {
     Views v;
-    v.R0 = int(align_up(size_t(T), kBM));
+    v.R0 = s.shared ? int(align_up(size_t(T), kBM)) : 0;
     const int64_t r = v.R0;
     v.perm_src = b.perm_src_all + r;
     v.pp_perm = b.pp_all + r;
@@ -296,8 +299,9 @@ bool check_mx_view(const moe_wview& v, int64_t N, int64_t K) {
 
 bool check_weights(const Shape& s, const moe_weights* w) {
     if (!w) return false;
-    const bool shared = check_view(w->shared_gate, s.I, s.H, false) && check_view(w->shared_up, s.I, s.H, false) &&
-                        check_view(w->shared_down, s.H, s.I, false);
+    const bool shared = !s.shared || (check_view(w->shared_gate, s.I, s.H, false) &&
+                                      check_view(w->shared_up, s.I, s.H, false) &&
+                                      check_view(w->shared_down, s.H, s.I, false));
     if (s.mx)
         return shared && check_mx_view(w->routed_gate, s.I, s.H) && check_mx_view(w->routed_up, s.I, s.H) &&
                check_mx_view(w->routed_down, s.H, s.I);
@@ -322,12 +326,13 @@ bool map_u8_weight(CUtensorMap* m, const void* data, const moe_wview& v, int64_t
     return encode_map(m, data, 3, dims, strides, box, MAP_U8);
 }
 
-bool check_mg(const moe_main_grads* m) {
+bool check_mg(const moe_main_grads* m, bool shared) {
     if (!m) return false;
     if (m->dtype != MOE_G_FP32 && m->dtype != MOE_G_BF16) return false;
     const int64_t q = m->dtype == MOE_G_BF16 ? 8 : 4;  // elements per 16 bytes
     void* const p[6] = {m->shared_gate, m->shared_up, m->shared_down, m->routed_gate, m->routed_up, m->routed_down};
     for (int i = 0; i < 6; ++i) {
+        if (i < 3 && !shared) continue;                  // no shared expert: ignored
         if (m->strides[i][1] % q || m->strides[i][1] <= 0) return false;
         if (i >= 3 && m->expert_ptrs[i - 3]) continue;  // per-expert table: checked as it is encoded
         if (!p[i] || !aligned16(p[i])) return false;
@@ -373,6 +378,25 @@ bool map_weight(CUtensorMap* m, const moe_wview& v, int64_t E, int64_t rows, int
     const uint64_t strides[2] = {uint64_t(v.row_stride) * 2, uint64_t(es) * 2};
     const uint32_t box[3] = {box_cols, box_rows, 1};
     return encode_map(m, v.data, 3, dims, strides, box);
+}
+
+// Without a shared expert the grouped BF16 GEMMs keep their group 0 empty (no
+// tiles, an empty K range): its weight and main_grad descriptors are encoded
+// but never used, so they are pointed at any 16-byte aligned device memory.
+moe_wview unused_view(const void* any16, const Shape& s) {
+    moe_wview v;
+    std::memset(&v, 0, sizeof(v));
+    v.data = any16;
+    v.row_stride = std::max(s.H, s.I);
+    return v;
+}
+
+void set_unused_shared_main_grads(moe_main_grads* mg, void* any16, const Shape& s) {
+    mg->shared_gate = mg->shared_up = mg->shared_down = any16;
+    for (int i = 0; i < 3; ++i) {
+        mg->strides[i][0] = 0;
+        mg->strides[i][1] = std::max(s.H, s.I);
+    }
 }
 
 GemmArgs base_args(int* status, const Shape& s) {
@@ -795,7 +819,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    if (mx) {  // shared gate/up + SwiGLU (BF16) into the shared rows
+    if (mx && s.shared) {  // shared gate/up + SwiGLU (BF16) into the shared rows
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
         if (!map_kmajor(&m.a, hidden, Ti, H, H) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, bn / 2) ||
@@ -828,13 +852,18 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
     const bool mx = s.mx;
     if (mx && !h->weights_prepared) return MOE_ERR_STATE;
     const bool gated = w->shared_output_gate != nullptr;
-    if (gated && !aligned16(w->shared_output_gate)) return MOE_ERR_INVALID_ARG;
+    if (gated && (!aligned16(w->shared_output_gate) || !s.shared)) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const SavedBufs& b = saved->b;
     const Workspace& ws = h->ws;
     saved->T = T;
     saved->hidden = hidden;
     saved->w = *w;
+    if (!s.shared && T > 0) {
+        const moe_wview u = unused_view(hidden, s);
+        saved->w.shared_gate = saved->w.shared_up = saved->w.shared_down = u;
+    }
+    w = &saved->w;
     saved->valid = true;
     saved->gated = gated;
     saved->topk = topk;
@@ -897,7 +926,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_FWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    if (mx) {  // shared down projection (BF16)
+    if (mx && s.shared) {  // shared down projection (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
         if (!map_kmajor(&m.a, b.a_all, Ti, I, I) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, bn))
@@ -917,7 +946,8 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
     }
     // combine
     Timed tm_(h, MOE_K_COMBINE, st);
-    MOE_CU(launch_combine(s.act32 ? static_cast<const void*>(ws.yx32) : ws.yx_all, gated ? b.pp_all : nullptr,
+    const void* ys = s.shared ? (s.act32 ? static_cast<const void*>(ws.yx32) : ws.yx_all) : nullptr;
+    MOE_CU(launch_combine(ys, gated ? b.pp_all : nullptr,
                           s.act32 ? static_cast<const void*>(v.yx32) : v.yx, s.act32, b.row_of, b.pp, Ti, H, k,
                           static_cast<__nv_bfloat16*>(out), h->sms, st));
     return MOE_OK;
@@ -941,7 +971,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
                         const moe_main_grads* mg, void* stream) {
     if (!h || !saved || saved->h != h) return MOE_ERR_INVALID_ARG;
     if (!saved->valid) return MOE_ERR_STATE;
-    if (!check_mg(mg)) return MOE_ERR_INVALID_ARG;
+    if (!check_mg(mg, h->s.shared)) return MOE_ERR_INVALID_ARG;
     const bool gated = saved->gated;
     if (gated && (!mg->shared_output_gate || !aligned16(mg->shared_output_gate))) return MOE_ERR_INVALID_ARG;
     const bool mg_bf16 = mg->dtype == MOE_G_BF16;
@@ -959,6 +989,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     const Views v = views_of(s, b, ws, T);
     const int rows_all = v.R0 + rows;
     const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(grad_out);
+    moe_main_grads mg_local = *mg;  // without a shared expert: its (ignored) buffers point at the workspace
+    if (!s.shared) set_unused_shared_main_grads(&mg_local, ws.go_all, s);
+    mg = &mg_local;
 
     // the weight-gradient launches claim their tiles from these counters
     MOE_CU(cudaMemsetAsync(ws.tile_counters, 0, 4 * sizeof(int), st));
@@ -1029,7 +1062,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_DOWN, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    if (mx) {  // shared dgrad through the down projection + SwiGLU backward (BF16)
+    if (mx && s.shared) {  // shared dgrad through the down projection + SwiGLU backward (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
         if (!map_kmajor(&m.a, go, Ti, H, H) || !map_weight(&m.b0, w->shared_down, 1, H, I, 64, 64))
@@ -1098,7 +1131,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
         MOE_CU(launch_gemm(OP_BWD_GU, bn, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
     }
-    if (mx) {  // shared dgrad through gate/up (BF16)
+    if (mx && s.shared) {  // shared dgrad through gate/up (BF16)
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
         if (!map_kmajor(&m.a, ws.dgdu_all, Ti, 2 * I, 2 * I) || !map_weight(&m.b0, w->shared_gate, 1, I, H, 64, 64) ||
@@ -1181,7 +1214,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     }
     // dhidden = shared + un-permuted routed dgrad; dense dprobs
     Timed tm_(h, MOE_K_UNPERMUTE, st);
-    MOE_CU(launch_unpermute(s.act32 ? static_cast<const void*>(ws.yx32) : ws.yx_all,
+    const void* dxs = s.shared ? (s.act32 ? static_cast<const void*>(ws.yx32) : ws.yx_all) : nullptr;
+    MOE_CU(launch_unpermute(dxs,
                             s.act32 ? static_cast<const void*>(v.yx32) : v.yx, s.act32, b.row_of, b.ids, v.partial,
                             s.n_part, Ti, H, k, E,
                             gated ? ws.dz : nullptr,

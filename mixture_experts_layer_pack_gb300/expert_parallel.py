@@ -26,7 +26,12 @@ dispatch grad_out rows the same way, the owners compute dgrad and accumulate
 their experts' weight gradients, return dx rows and the per-route dprob.
 The experts, the shared expert and the sums are the caller's (``ep_forward`` /
 ``ep_backward`` take them as functions), so the exchange runs the same with
-NCCL on GPUs or gloo on CPU ranks. The collectives move every row through the
+NCCL on GPUs or gloo on CPU ranks. On a GPU the owner's experts are the
+library's own routed-only step: a ``MoELayer(..., num_experts=len(local),
+topk=1, shared_expert=False)`` run with ``forward_topk`` on the received rows
+(ids = local expert, probs = the route's prob) returns the prob-weighted
+expert outputs, and its ``backward`` the rows' dx, the per-route dprob and the
+local experts' main_grad accumulation. The collectives move every row through the
 receiving rank's own memory: nothing reads a peer's memory directly.
 """
 from __future__ import annotations

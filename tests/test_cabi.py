@@ -109,7 +109,7 @@ def _c_layout(tmp_path):
         pytest.skip("no C compiler")
     fields = {
         "moe_config": ["max_tokens", "hidden", "num_experts", "topk", "inter", "routed_wtype", "swiglu_limit",
-                       "recompute_dispatch", "act_precision"],
+                       "recompute_dispatch", "act_precision", "no_shared_expert"],
         "moe_wview": ["data", "expert_stride", "row_stride", "scale", "col_data", "col_scale", "expert_ptrs"],
         "moe_weights": ["shared_gate", "shared_up", "shared_down", "routed_gate", "routed_up", "routed_down",
                         "shared_output_gate"],
@@ -137,6 +137,17 @@ def test_ctypes_structs_match_the_c_header(tmp_path):
         assert c[(s.__name__, "size")] == ctypes.sizeof(s), s.__name__
         for f, _ in s._fields_:
             assert c[(s.__name__, f)] == getattr(s, f).offset, (s.__name__, f)
+
+
+def test_no_shared_expert_flag():
+    """Without a shared expert the row buffers lose their shared region (T rows of
+    every per-row buffer); 0 and 1 are the only values."""
+    c = _cfg()
+    assert M.moe_workspace_size(_cfg(no_shared_expert=1)) < M.moe_workspace_size(c)
+    assert M.moe_saved_size(_cfg(no_shared_expert=1)) < M.moe_saved_size(c)
+    with pytest.raises(M.MoeError) as ei:
+        M.moe_workspace_size(_cfg(no_shared_expert=2))
+    assert ei.value.status == 1
 
 
 def test_recompute_dispatch_flag():
