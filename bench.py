@@ -47,6 +47,9 @@ def parse_args(argv=None):
     p.add_argument("--per-config", default="3,4,5",
                    help="further workloads measured after the headline one (comma list; empty: none)")
     p.add_argument("--per-config-steps", type=int, default=10)
+    p.add_argument("--ep-owner", type=int, default=16,
+                   help="also time the expert-parallel owner step of the headline workload at this EP degree "
+                        "(0: skip)")
     p.add_argument("--experts", type=int, default=0,
                    help="a reduced instance of the workload: this many routed experts (same H, I, top-k); "
                         "the token count scales with it unless --tokens is given (profiling captures)")
@@ -567,6 +570,62 @@ def measure_config(cid, args, steps, warmup, full, dev, world, rank, local_rank)
     return res
 
 
+def measure_ep_owner(cid, ep, steps, warmup, dev):
+    """The owner-side step of expert parallelism at EP degree ``ep`` for workload
+    ``cid``: the rank holding E/ep experts runs them (a routed-only handle, top-1)
+    on the rows all ep ranks route to them -- T*k rows for ep ranks of T tokens
+    each, split over the local experts in proportion to a seeded multinomial --
+    forward + backward with main_grad accumulation. CUDA events over ``steps``
+    steps after ``warmup``; useful FLOPs 18 n H I per step."""
+    import numpy as np
+    import torch
+    import moe_inputs as MI
+    import mixture_experts_layer_pack_gb300 as M
+    c = MI.CONFIGS[cid]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    if E % ep or c["routed"] != "bf16":
+        return {"unavailable": f"E={E} not divisible by EP{ep}, or MXFP8 routed weights (BF16 owner step only)"}
+    el = E // ep
+    n = T * k
+    seed = MI.seed_of(cid) + 101
+    rng = np.random.default_rng(seed)
+    counts = rng.multinomial(n, np.full(el, 1.0 / el))
+    ids = torch.from_numpy(np.repeat(np.arange(el, dtype=np.int32), counts)[:, None]).to(dev)
+    probs = torch.from_numpy(rng.uniform(0.05, 0.5, size=(n, 1)).astype(np.float32)).to(dev)
+    w = MI.make_weights(H, I, el, seed, device=dev)
+    rows, go = MI.make_activations(n, H, seed, device=dev)
+    mg = MI.make_main_grads(H, I, el, seed, device=dev)
+    layer = M.MoELayer(n, H, el, 1, I, device=dev, shared_expert=False)
+    wv = M.weights_from_combined(None, None, w["routed_fc1"], w["routed_fc2"])
+    mgv = M.main_grads_from_combined(None, None, mg["routed_fc1"], mg["routed_fc2"])
+    out = torch.empty_like(rows)
+    dx = torch.empty_like(rows)
+    dp = torch.empty((n, 1), dtype=torch.float32, device=dev)
+
+    def step():
+        layer.forward_topk(rows, ids, probs, wv, out=out)
+        layer.backward(go, mgv, dhidden=dx, dprobs=dp)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise SystemExit("device status reported an error in the owner step")
+    ms = t0.elapsed_time(t1) / steps
+    flops = 18.0 * n * H * I
+    layer.close()
+    return {"workload": f"{MI.WORKLOAD_NAMES[cid]}-EP{ep}-owner", "experts": el, "rows": n,
+            "rows_per_expert": [int(x) for x in counts], "steps": steps, "warmup": warmup, "ms_per_step": ms,
+            "rows_per_s": n / (ms * 1e-3), "useful_tflops": flops / (ms * 1e-3) / 1e12,
+            "note": "routed-only handle, top-1 over the received rows; the all-to-all exchange is not timed"}
+
+
 def per_config_entry(res):
     """The compact record of one extra workload."""
     roof = res["roofline"]
@@ -605,6 +664,11 @@ def run_ours(args):
             per_config[str(other)] = {"unavailable": f"out of device memory: {ex}"}
         torch.cuda.empty_cache()
 
+    ep_owner = None
+    if args.ep_owner > 1 and world == 1:
+        ep_owner = measure_ep_owner(cid, args.ep_owner, max(10, args.per_config_steps), 3, dev)
+        torch.cuda.empty_cache()
+
     peaks, peaks_kind = res["peaks"], res["peaks_kind"]
     mx = res["mx"]
     line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -629,6 +693,8 @@ def run_ours(args):
             "fwd_ms": res["fwd_ms"], "bwd_ms": res["bwd_ms"], "cuda_graph": res["cuda_graph"]}
     if per_config:
         line["per_config"] = per_config
+    if ep_owner is not None:
+        line["ep_owner_step"] = ep_owner
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cid)
     if rank == 0:
