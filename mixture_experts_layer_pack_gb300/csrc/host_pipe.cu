@@ -176,9 +176,14 @@ moe_status moe_host_step(moe_host_pipe* p, const void* hidden, const float* prob
     if (p->used[s]) PIPE_CU(cudaStreamWaitEvent(st, p->downloaded[s], 0));
     if (p->used[prev]) PIPE_CU(cudaStreamWaitEvent(st, p->computed[prev], 0));
     moe_status r = moe_forward(p->h, p->T, b.hidden, b.probs, b.map, w, b.out, p->saved, stream);
-    if (r != MOE_OK) return r;
-    r = moe_backward(p->h, b.grad_out, p->saved, b.dhidden, b.dprobs, mg, stream);
-    if (r != MOE_OK) return r;
+    if (r == MOE_OK) r = moe_backward(p->h, b.grad_out, p->saved, b.dhidden, b.dprobs, mg, stream);
+    if (r != MOE_OK) {
+        // the set's uploads, and whatever part of the step was enqueued, finish before
+        // the next step may write the same staging set
+        cudaStreamSynchronize(p->up);
+        cudaStreamSynchronize(st);
+        return r;
+    }
     PIPE_CU(cudaEventRecord(p->computed[s], st));
 
     // downloads

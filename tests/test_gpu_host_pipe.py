@@ -136,3 +136,39 @@ def test_host_pipe_rejects_bad_arguments():
         M.moe_host_step(pipe.pipe, None, *host[1:], wv, mgv, *res)
     pipe.close()
     layer.close()
+
+
+def test_host_pipe_usable_after_a_rejected_step():
+    """A step whose backward is rejected (a null main_grad pointer) returns the
+    error after its uploads and forward were enqueued; the pipeline drains it, and
+    the next steps give the results of sequential calls."""
+    case = Case(T=160, H=256, E=8, k=2, I=128, seed=85)
+    inp = make_inputs(case)
+    c = inp.case
+    wv = weight_views(inp)
+    hid, gos = _steps_inputs(inp, 2)
+    ref, mg_s = _sequential(inp, hid, gos, wv)
+    layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I)
+    mg_p, mgv_p = _grads(inp)
+    pipe = layer.host_pipe(c.T)
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    rmap = pin(inp.routing_map.view(torch.uint8))
+    probs = pin(inp.probs)
+    bad = M.main_grads_from_combined(mg_p["shared_fc1"], mg_p["shared_fc2"], mg_p["routed_fc1"], mg_p["routed_fc2"])
+    bad.routed_down = None
+    junk = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ref[0]]
+    with pytest.raises(B.MoeError):
+        pipe.step(pin(hid[0]), probs, rmap, pin(gos[0]), wv, bad, *junk)
+    res = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in r) for r in ref]
+    for i in range(2):
+        pipe.step(pin(hid[i]), probs, rmap, pin(gos[i]), wv, mgv_p, *res[i])
+    pipe.synchronize()
+    assert layer.device_status() == 0
+    for i in range(2):
+        for got, want, name in zip(res[i], ref[i], ("out", "dhidden", "dprobs")):
+            assert torch.equal(got, want.cpu()), (i, name)
+    torch.cuda.synchronize()
+    for n in mg_s:
+        assert torch.equal(mg_p[n], mg_s[n]), n
+    pipe.close()
+    layer.close()
