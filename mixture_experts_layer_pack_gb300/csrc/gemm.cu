@@ -114,6 +114,20 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a) {
     return t;
 }
 
+// block-scaled GEMM tile `tile` when a CTA tile is NH adjacent 128-column tiles:
+// its m tile, expert, and its first 128-column tile (nt in units of 128 columns)
+template <int NH>
+__device__ __forceinline__ Tile decode_mx_tile(int tile, const GemmArgs& a) {
+    const int pairs = a.n_tiles / NH;
+    Tile t;
+    t.mt = tile / pairs;
+    t.nt = (tile - t.mt * pairs) * NH;
+    t.e = a.mtile_expert ? a.mtile_expert[t.mt] : 0;
+    t.k_lo = 0;
+    t.kblocks = a.k_blocks;
+    return t;
+}
+
 // bounded wait that ignores the abort flag (used while winding down)
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
     const uint64_t t0 = globaltimer_ns();
@@ -980,20 +994,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // copies into a per-stage TMEM slot with tcgen05.cp; the four K=32 MMAs of a
 // stage select their K block through the scale-factor id of the instruction
 // descriptor.
-// (the dgrad-down's SwiGLU-backward epilogue moves more bytes than its mainloop:
-// three stages leave it more of the memory system than five, 206 against 235 us
-// at T=4096, H=2048, E=96 top-6, I=1024; the other ops stream operands, five)
-template <int OP>
+// NH = 2: a CTA's tile is two adjacent 128-column tiles of the same rows, which
+// share the stage's A tile (their B halves, scale atoms and accumulators side by
+// side), so that a stage brings 48 KB for the work two 32 KB stages did: the
+// operand fill rate of an SM from L2, not the tensor pipe, bounds these GEMMs.
+// The accumulator pair then takes 256 TMEM columns, so it is single-buffered (the
+// loads of the next tile go on while the epilogue drains it).
+// The dgrad-down's SwiGLU-backward epilogue moves more bytes than its mainloop:
+// it keeps NH = 1 and three stages (206 against 235 us with five at T=4096,
+// H=2048, E=96 top-6, I=1024); the other ops stream operands: five stages at
+// NH = 1, three (as many as fit) at NH = 2.
+template <int OP, int NH>
 struct MxCfg {
     static constexpr uint32_t A_BYTES = kBM * kMxBK;
-    static constexpr uint32_t B_BYTES = kMxBN * kMxBK;
+    static constexpr uint32_t B_HALF = kMxBN * kMxBK;          // one 128-column tile's B
+    static constexpr uint32_t B_BYTES = NH * B_HALF;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t SF_BYTES = 1024;  // A atom + B atom
-    static constexpr int STAGES = OP == OP_BWD_DOWN ? 3 : 5;
+    static constexpr uint32_t SF_BYTES = 512 * (1 + NH);       // A atom + NH B atoms
+    static constexpr int STAGES = OP == OP_BWD_DOWN ? 3 : (NH == 1 ? 5 : 3);
+    static constexpr int ACC = NH == 1 ? 2 : 1;                // accumulator buffers of NH x 128 columns
     static constexpr uint32_t STAGING = kEpiWarps * kStageTileBytes;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t SF_TMEM = 2 * kMxBN;  // scale slots after the two accumulators, 8 columns a stage
-    static constexpr size_t SMEM = size_t(STAGES) * (STAGE_BYTES + SF_BYTES) + STAGING + 1024 + 256;
+    static constexpr uint32_t SF_TMEM = 2 * kMxBN;             // scale slots after the accumulators
+    static constexpr uint32_t SF_COLS = 4 * (1 + NH);          // TMEM columns of a stage's scale slot
+    static constexpr uint32_t SF_REGION = (STAGES * SF_BYTES + 1023) / 1024 * 1024;  // keeps the staging 1 KB aligned
+    static_assert(SF_TMEM + STAGES * SF_COLS <= TMEM_COLS, "tensor memory");
+    static_assert(ACC * NH * kMxBN <= SF_TMEM, "accumulators");
+    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + SF_REGION + STAGING + 1024 + 256;
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 // instruction descriptor of kind::mxf8f6f4 with E4M3 A and B, UE8M0 scales, M = 128, N = 128
@@ -1030,11 +1058,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-template <int OP, bool CLAMP>
+template <int OP, bool CLAMP, int NH>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-    using C = MxCfg<OP>;
+    using C = MxCfg<OP, NH>;
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU);
     constexpr int STAGES = C::STAGES;
     constexpr int BN = kMxBN;
@@ -1042,7 +1070,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sf_smem = smem + STAGES * C::STAGE_BYTES;
-    float* staging = reinterpret_cast<float*>(sf_smem + STAGES * C::SF_BYTES);  // 1024-byte aligned
+    float* staging = reinterpret_cast<float*>(sf_smem + C::SF_REGION);  // 1024-byte aligned
     uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(staging) + C::STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
@@ -1077,7 +1105,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     pdl_wait();  // from here on the predecessor's writes are visible (prologue above touched no global memory)
     pdl_trigger();
-    const int total_tiles = (args.num_mtiles_dev ? *args.num_mtiles_dev : args.num_mtiles) * args.n_tiles;
+    // a.n_tiles counts 128-column tiles; a CTA tile is NH of them (tile index in units of NH)
+    const int total_tiles = (args.num_mtiles_dev ? *args.num_mtiles_dev : args.num_mtiles) * (args.n_tiles / NH);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1086,40 +1115,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile<OP>(tile, args);
+                const Tile t = decode_mx_tile<NH>(tile, args);
                 for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
-                    uint8_t* sb = sa + C::A_BYTES;
                     uint8_t* ssf = sf_smem + stage * C::SF_BYTES;
                     uint64_t* bar = &full[stage];
                     const int k0 = kb * kMxBK;
                     mbar_arrive_expect_tx(bar, C::STAGE_BYTES + C::SF_BYTES);
                     tma_load_2d(sa, &tmA, bar, k0, t.mt * kBM);
+                    bulk_load(ssf, args.sfa + (int64_t(t.mt) * args.sfa_kgroups + kb) * 512, 512, bar);
                     // an expert's payload: its own descriptor (z = 0) from a per-expert table, or the 3D map at z = e
                     const CUtensorMap* B0 = args.b0_tab ? args.b0_tab + t.e : &tmB0;
                     const CUtensorMap* B1 = args.b1_tab ? args.b1_tab + t.e : &tmB1;
                     const int z0 = args.b0_tab ? 0 : t.e;
                     const int z1 = args.b1_tab ? 0 : t.e;
-                    if (OP == OP_FWD_GU) {
-                        tma_load_3d(sb, B0, bar, k0, t.nt * (BN / 2), z0);
-                        tma_load_3d(sb + (BN / 2) * kMxBK, B1, bar, k0, t.nt * (BN / 2), z1);
-                    } else if (OP == OP_FWD_DOWN) {
-                        tma_load_3d(sb, B0, bar, k0, t.nt * BN, z0);
-                    } else if (OP == OP_BWD_DOWN) {
-                        tma_load_3d(sb, B0, bar, t.nt * BN, k0, z0);
-                    } else {
-                        const bool up = k0 >= args.gate_up_split;
-                        tma_load_3d(sb, up ? B1 : B0, bar, t.nt * BN, up ? k0 - args.gate_up_split : k0,
-                                    up ? z1 : z0);
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf) {  // the B tile and scale atom of 128-column tile nt
+                        const int nt = t.nt + hf;
+                        uint8_t* sb = sa + C::A_BYTES + hf * C::B_HALF;
+                        if (OP == OP_FWD_GU) {
+                            tma_load_3d(sb, B0, bar, k0, nt * (kMxBN / 2), z0);
+                            tma_load_3d(sb + (kMxBN / 2) * kMxBK, B1, bar, k0, nt * (kMxBN / 2), z1);
+                        } else if (OP == OP_FWD_DOWN) {
+                            tma_load_3d(sb, B0, bar, k0, nt * kMxBN, z0);
+                        } else if (OP == OP_BWD_DOWN) {
+                            tma_load_3d(sb, B0, bar, nt * kMxBN, k0, z0);
+                        } else {
+                            const bool up = k0 >= args.gate_up_split;
+                            tma_load_3d(sb, up ? B1 : B0, bar, nt * kMxBN, up ? k0 - args.gate_up_split : k0,
+                                        up ? z1 : z0);
+                        }
+                        bulk_load(ssf + 512 * (1 + hf),
+                                  args.sfb + ((int64_t(t.e) * args.sfb_ntiles + nt) * args.sfb_kgroups + kb) * 512,
+                                  512, bar);
                     }
-                    bulk_load(ssf, args.sfa + (int64_t(t.mt) * args.sfa_kgroups + kb) * 512, 512, bar);
-                    bulk_load(ssf + 512,
-                              args.sfb + ((int64_t(t.e) * args.sfb_ntiles + t.nt) * args.sfb_kgroups + kb) * 512,
-                              512, bar);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -1141,13 +1174,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile<OP>(tile, args);
-                const int buf = it & 1;
-                const uint32_t use = uint32_t(it >> 1);
+                const Tile t = decode_mx_tile<NH>(tile, args);
+                const int buf = C::ACC == 2 ? (it & 1) : 0;
+                const uint32_t use = uint32_t(C::ACC == 2 ? (it >> 1) : it);
                 ++it;
                 if (!mbar_wait(&tempty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * NH * BN);
                 for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, args.status)) {
                         ok = false;
@@ -1155,18 +1188,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + C::A_BYTES;
                     const uint32_t sf_addr = smem_u32(sf_smem + stage * C::SF_BYTES);
-                    const uint32_t sfa_t = tmem_base + C::SF_TMEM + uint32_t(stage * 8);
-                    const uint32_t sfb_t = sfa_t + 4;
+                    const uint32_t sfa_t = tmem_base + C::SF_TMEM + uint32_t(stage) * C::SF_COLS;
                     tmem_cp_sf(sfa_t, sf_smem_desc(sf_addr));
-                    tmem_cp_sf(sfb_t, sf_smem_desc(sf_addr + 512));
 #pragma unroll
-                    for (int kk = 0; kk < kMxBK / 32; ++kk) {
-                        const uint64_t ad = smem_desc(a_addr + kk * 32, 16, kSwizzleAtom);
-                        const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 32 * 128, 16384, kSwizzleAtom)
-                                                 : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
-                        mma_mx(d_tmem, ad, bd, mx_idesc<B_MN>(uint32_t(kk)), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+                    for (int hf = 0; hf < NH; ++hf) tmem_cp_sf(sfa_t + 4 * (1 + hf), sf_smem_desc(sf_addr + 512 * (1 + hf)));
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf) {  // 128-column tile nt + hf: its B half, scales, accumulator
+                        const uint32_t b_addr = a_addr + C::A_BYTES + hf * C::B_HALF;
+                        const uint32_t sfb_t = sfa_t + 4 * (1 + hf);
+#pragma unroll
+                        for (int kk = 0; kk < kMxBK / 32; ++kk) {
+                            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, kSwizzleAtom);
+                            const uint64_t bd = B_MN ? smem_desc(b_addr + kk * 32 * 128, 16384, kSwizzleAtom)
+                                                     : smem_desc(b_addr + kk * 32, 16, kSwizzleAtom);
+                            mma_mx(d_tmem + hf * BN, ad, bd, mx_idesc<B_MN>(uint32_t(kk)), sfa_t, sfb_t,
+                                   (kb | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&empty[stage]);
                     if (++stage == STAGES) {
@@ -1186,9 +1224,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float* my_staging = staging + (warp - 2) * (kStageTileBytes / 4);
         int it = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile<OP>(tile, args);
-            const int buf = it & 1;
-            const uint32_t use = uint32_t(it >> 1);
+            const Tile t = decode_mx_tile<NH>(tile, args);
+            const int buf = C::ACC == 2 ? (it & 1) : 0;
+            const uint32_t use = uint32_t(C::ACC == 2 ? (it >> 1) : it);
             ++it;
             int ok = 0;
             if (lane == 0) ok = mbar_wait(&tfull[buf], use & 1, abort_flag, args.status) ? 1 : 0;
@@ -1196,8 +1234,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            epilogue_tile<OP, BN, true, CLAMP>(t, t_row, q, half, args, my_staging);
+#pragma unroll 1
+            for (int hf = 0; hf < NH; ++hf) {  // each 128-column tile as its own epilogue tile
+                Tile th = t;
+                th.nt = t.nt + hf;
+                const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t((buf * NH + hf) * BN);
+                epilogue_tile<OP, BN, true, CLAMP>(th, t_row, q, half, args, my_staging);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -1211,18 +1254,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int OP, bool CLAMP>
-cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
+template <int OP, bool CLAMP, int NH>
+cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int sms, cudaStream_t st) {
     static bool attr_set = false;
-    auto kern = moe_gemm_mx_kernel<OP, CLAMP>;
+    using C = MxCfg<OP, NH>;
+    auto kern = moe_gemm_mx_kernel<OP, CLAMP, NH>;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(MxCfg<OP>::SMEM));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), MxCfg<OP>::SMEM, st, m.a, m.b0, m.b1, a);
+    const int64_t tiles = int64_t(a.num_mtiles) * (a.n_tiles / NH);
+    const int grid = int(tiles < sms ? tiles : sms);
+    if (grid <= 0) return cudaSuccess;
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), C::SMEM, st, m.a, m.b0, m.b1, a);
     count_launch();
     return e;
+}
+
+template <int OP, bool CLAMP>
+cudaError_t launch_mx_nh(int nh, const GemmMaps& m, const GemmArgs& a, int sms, cudaStream_t st) {
+    if (nh == 2 && OP != OP_BWD_DOWN && a.n_tiles % 2 == 0) return launch_mx_one<OP, CLAMP, (OP == OP_BWD_DOWN ? 1 : 2)>(m, a, sms, st);
+    return launch_mx_one<OP, CLAMP, 1>(m, a, sms, st);
 }
 
 template <int OP, int BN, bool CLAMP, bool SPLIT>
@@ -1265,19 +1318,18 @@ cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cu
 
 }  // namespace
 
-cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
-    if (grid <= 0) return cudaSuccess;
+cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int nh, int sms, cudaStream_t st) {
     const bool clamp = a.swiglu_limit > 0.0f;
     switch (op) {
         // the SwiGLU epilogues come in a clamped and an unclamped build
         case OP_FWD_GU:
-            return clamp ? launch_mx_one<OP_FWD_GU, true>(m, a, grid, st)
-                         : launch_mx_one<OP_FWD_GU, false>(m, a, grid, st);
-        case OP_FWD_DOWN: return launch_mx_one<OP_FWD_DOWN, false>(m, a, grid, st);
+            return clamp ? launch_mx_nh<OP_FWD_GU, true>(nh, m, a, sms, st)
+                         : launch_mx_nh<OP_FWD_GU, false>(nh, m, a, sms, st);
+        case OP_FWD_DOWN: return launch_mx_nh<OP_FWD_DOWN, false>(nh, m, a, sms, st);
         case OP_BWD_DOWN:
-            return clamp ? launch_mx_one<OP_BWD_DOWN, true>(m, a, grid, st)
-                         : launch_mx_one<OP_BWD_DOWN, false>(m, a, grid, st);
-        case OP_BWD_GU: return launch_mx_one<OP_BWD_GU, false>(m, a, grid, st);
+            return clamp ? launch_mx_one<OP_BWD_DOWN, true, 1>(m, a, sms, st)
+                         : launch_mx_one<OP_BWD_DOWN, false, 1>(m, a, sms, st);
+        case OP_BWD_GU: return launch_mx_nh<OP_BWD_GU, false>(nh, m, a, sms, st);
         default: return cudaErrorInvalidValue;
     }
 }

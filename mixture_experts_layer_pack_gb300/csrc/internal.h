@@ -112,7 +112,10 @@ int pick_bn(int64_t n, bool split_gate_up);
 
 cudaError_t launch_gemm(int op, int bn, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
 // block-scaled MXFP8 GEMM (N tile 128, K stage 128); ops FWD_GU, FWD_DOWN, BWD_DOWN, BWD_GU
-cudaError_t launch_gemm_mx(int op, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
+// nh = 2: a CTA tile is two adjacent 128-column tiles sharing the A stage (the
+// gate/up forward, down forward and dgrad through gate/up; n_tiles even); else 1.
+// The grid is min(tiles, sms).
+cudaError_t launch_gemm_mx(int op, const GemmMaps& maps, const GemmArgs& args, int nh, int sms, cudaStream_t st);
 constexpr int kMxBN = 128;
 constexpr int kMxBK = 128;
 

@@ -46,6 +46,9 @@ struct Shape {
     bool act32;       // MOE_ACT_FP32: fp32 g|u, y, dx; derived GEMM operands as hi + lo bf16 terms
     float limit;      // swiglu_limit (0: none)
     bool shared;      // the layer has the shared expert (no_shared_expert = 0)
+    // block-scaled GEMMs: 128-column tiles per CTA tile (1 or 2) of the gate/up forward, the
+    // down forward and the dgrad through gate/up
+    int mx_nh_gu, mx_nh_down, mx_nh_bgu;
 };
 
 // carves consecutive 256-byte aligned pieces out of one block
@@ -96,6 +99,15 @@ moe_status check_config(const moe_config* c, Shape* s) {
     if (!s->bn_gu || !s->bn_down || !s->bn_bd || !s->bn_bgu || !s->bn_wfc1 || !s->bn_wd) return MOE_ERR_UNSUPPORTED;
     s->n_part = int(s->I / (s->mx ? kMxBN : s->bn_bd)) * kEpiHalves;
     s->n_part_s = int(s->I / s->bn_bd) * kEpiHalves;
+    // Pairs of 128-column tiles share a stage's A tile (a quarter fewer bytes a stage) but
+    // get three stages instead of five and a single-buffered accumulator: measured at
+    // T=4096 H=2048 E=96 top-6 I=1024 and T=8192 H=7168 E=384 top-6 I=2048, the dgrad
+    // through gate/up gains at both (178 -> 172, 2554 -> 2420 us), the gate/up forward
+    // only with a long K (2590 -> 2484 us at H = 7168; 192 -> 213 us at H = 2048), the
+    // down forward at neither
+    s->mx_nh_gu = s->H / kMxBK >= 32 ? 2 : 1;
+    s->mx_nh_down = 1;
+    s->mx_nh_bgu = 2;
     return MOE_OK;
 }
 
@@ -795,7 +807,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         a.sfb_ntiles = 2 * I / 128;
         a.sfb_kgroups = H / 128;
         Timed tm_(h, MOE_K_FWD_GU_ROUTED, st);
-        MOE_CU(launch_gemm_mx(OP_FWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+        MOE_CU(launch_gemm_mx(OP_FWD_GU, m, a, s.mx_nh_gu, h->sms, st));
     } else {  // shared expert (group 0) and routed experts in one launch
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_gu;
@@ -903,7 +915,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         a.sfb_ntiles = H / 128;
         a.sfb_kgroups = I / 128;
         Timed tm_(h, MOE_K_FWD_DOWN_ROUTED, st);
-        MOE_CU(launch_gemm_mx(OP_FWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+        MOE_CU(launch_gemm_mx(OP_FWD_DOWN, m, a, s.mx_nh_down, h->sms, st));
     } else {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_down;
@@ -1039,7 +1051,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.sfb_ntiles = I / 128;
         a.sfb_kgroups = H / 128;
         Timed tm_(h, MOE_K_BWD_DOWN_ROUTED, st);
-        MOE_CU(launch_gemm_mx(OP_BWD_DOWN, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+        MOE_CU(launch_gemm_mx(OP_BWD_DOWN, m, a, 1, h->sms, st));
     } else {  // shared expert (group 0: its rows' scale is the gate, or 1) and routed experts
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bd;
@@ -1107,7 +1119,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.sfb_ntiles = H / 128;
         a.sfb_kgroups = 2 * I / 128;
         Timed tm_(h, MOE_K_BWD_GU_ROUTED, st);
-        MOE_CU(launch_gemm_mx(OP_BWD_GU, m, a, grid_of(int64_t(a.num_mtiles) * a.n_tiles, h->sms), st));
+        MOE_CU(launch_gemm_mx(OP_BWD_GU, m, a, s.mx_nh_bgu, h->sms, st));
     } else {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_bgu;
