@@ -48,7 +48,7 @@ constexpr int kRingInts = 6;  // a ring slot: the tile index, then its decoded m
 // its lo tile rides in the same stage (L_BYTES: an A tile, or for the weight
 // gradient the larger of A and B), so the other operand's tile crosses L2 once for
 // both products
-template <int OP, int BN, bool SPLIT = false>
+template <int OP, int BN, bool SPLIT = false, bool DEEP = false>
 struct Cfg {
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = BN * kBK * 2;
@@ -62,7 +62,7 @@ struct Cfg {
     static constexpr int STAGES =
         (OP == OP_WGRAD) ? (SPLIT ? ((BN == 256) ? 2 : 3) : ((BN == 256) ? 3 : (BN == 128 ? 5 : 6)))
                          : (SPLIT ? ((BN == 256) ? 3 : 4)
-                                  : ((BN == 256) ? (OP == OP_BWD_DOWN ? 3 : 4) : (BN == 128 ? 6 : 8)));
+                                  : ((BN == 256) ? (OP == OP_BWD_DOWN && !DEEP ? 3 : 4) : (BN == 128 ? 6 : 8)));
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
     static constexpr uint32_t STAGING = kEpiWarps * BUFS * kStageTileBytes;
     static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING + 1024 + 512;
@@ -720,14 +720,14 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
     __syncwarp();
 }
 
-template <int OP, int BN, bool CLAMP, bool SPLIT>
+template <int OP, int BN, bool CLAMP, bool SPLIT, bool DEEP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
                     const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmS0,
                     const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmL,
                     const __grid_constant__ CUtensorMap tmG, const GemmArgs args) {
-    using C = Cfg<OP, BN, SPLIT>;
+    using C = Cfg<OP, BN, SPLIT, DEEP>;
     constexpr bool A_MN = (OP == OP_WGRAD);
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD);
     constexpr uint32_t IDESC = instr_desc<BN, A_MN, B_MN>();
@@ -1002,16 +1002,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // loads of the next tile go on while the epilogue drains it).
 // The dgrad-down's SwiGLU-backward epilogue moves more bytes than its mainloop:
 // it keeps NH = 1 and three stages (206 against 235 us with five at T=4096,
-// H=2048, E=96 top-6, I=1024); the other ops stream operands: five stages at
-// NH = 1, three (as many as fit) at NH = 2.
-template <int OP, int NH>
+// H=2048, E=96 top-6, I=1024) unless its K is long (DEEP: five stages, 1.88 ->
+// 1.67 ms at H=7168); the other ops stream operands: five stages at NH = 1,
+// three (as many as fit) at NH = 2.
+template <int OP, int NH, bool DEEP = false>
 struct MxCfg {
     static constexpr uint32_t A_BYTES = kBM * kMxBK;
     static constexpr uint32_t B_HALF = kMxBN * kMxBK;          // one 128-column tile's B
     static constexpr uint32_t B_BYTES = NH * B_HALF;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t SF_BYTES = 512 * (1 + NH);       // A atom + NH B atoms
-    static constexpr int STAGES = OP == OP_BWD_DOWN ? 3 : (NH == 1 ? 5 : 3);
+    static constexpr int STAGES = (OP == OP_BWD_DOWN && !DEEP) ? 3 : (NH == 1 ? 5 : 3);
     static constexpr int ACC = NH == 1 ? 2 : 1;                // accumulator buffers of NH x 128 columns
     static constexpr uint32_t STAGING = kEpiWarps * kStageTileBytes;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -1058,11 +1059,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-template <int OP, bool CLAMP, int NH>
+template <int OP, bool CLAMP, int NH, bool DEEP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-    using C = MxCfg<OP, NH>;
+    using C = MxCfg<OP, NH, DEEP>;
     constexpr bool B_MN = (OP == OP_BWD_DOWN || OP == OP_BWD_GU);
     constexpr int STAGES = C::STAGES;
     constexpr int BN = kMxBN;
@@ -1254,11 +1255,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int OP, bool CLAMP, int NH>
+template <int OP, bool CLAMP, int NH, bool DEEP = false>
 cudaError_t launch_mx_one(const GemmMaps& m, const GemmArgs& a, int sms, cudaStream_t st) {
     static bool attr_set = false;
-    using C = MxCfg<OP, NH>;
-    auto kern = moe_gemm_mx_kernel<OP, CLAMP, NH>;
+    using C = MxCfg<OP, NH, DEEP>;
+    auto kern = moe_gemm_mx_kernel<OP, CLAMP, NH, DEEP>;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
         if (e != cudaSuccess) return e;
@@ -1278,12 +1279,12 @@ cudaError_t launch_mx_nh(int nh, const GemmMaps& m, const GemmArgs& a, int sms, 
     return launch_mx_one<OP, CLAMP, 1>(m, a, sms, st);
 }
 
-template <int OP, int BN, bool CLAMP, bool SPLIT>
+template <int OP, int BN, bool CLAMP, bool SPLIT, bool DEEP = false>
 cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     static bool attr_set = false;
-    using C = Cfg<OP, BN, SPLIT>;
+    using C = Cfg<OP, BN, SPLIT, DEEP>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory per CTA");
-    auto kern = moe_gemm_kernel<OP, BN, CLAMP, SPLIT>;
+    auto kern = moe_gemm_kernel<OP, BN, CLAMP, SPLIT, DEEP>;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
         if (e != cudaSuccess) return e;
@@ -1308,6 +1309,9 @@ cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cu
             default: return cudaErrorInvalidValue;
         }
     }
+    // the dgrad-down with a long K (a.deep_stages): four stages, its epilogue a smaller share
+    if constexpr (OP == OP_BWD_DOWN)
+        if (bn == 256 && a.deep_stages) return launch_one<OP, 256, CLAMP, false, true>(m, a, grid, st);
     switch (bn) {
         case 256: return launch_one<OP, 256, CLAMP, false>(m, a, grid, st);
         case 128: return launch_one<OP, 128, CLAMP, false>(m, a, grid, st);
@@ -1327,6 +1331,9 @@ cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int nh,
                          : launch_mx_nh<OP_FWD_GU, false>(nh, m, a, sms, st);
         case OP_FWD_DOWN: return launch_mx_nh<OP_FWD_DOWN, false>(nh, m, a, sms, st);
         case OP_BWD_DOWN:
+            if (a.deep_stages)
+                return clamp ? launch_mx_one<OP_BWD_DOWN, true, 1, true>(m, a, sms, st)
+                             : launch_mx_one<OP_BWD_DOWN, false, 1, true>(m, a, sms, st);
             return clamp ? launch_mx_one<OP_BWD_DOWN, true, 1>(m, a, sms, st)
                          : launch_mx_one<OP_BWD_DOWN, false, 1>(m, a, sms, st);
         case OP_BWD_GU: return launch_mx_nh<OP_BWD_GU, false>(nh, m, a, sms, st);

@@ -28,6 +28,18 @@ from tests.harness import (MX_TOL, Case, assert_close, assert_normwise, compare_
 
 pytestmark = pytest.mark.gpu
 
+
+def _check_mx(gpu, ref_mx, ref_exact, name):
+    """An MXFP8 result on a sample of a full-size layer: per element within the MXFP8
+    tolerance of the MXFP8 method (the oracle's mxfp8 mode), and normwise no further
+    from the exact definition than 6e-2, or than the method itself is on this sample
+    (x 1.05 + 1e-3): the sample's own max|ref| is the scale, so a few tokens can put
+    the method's own distance above 6e-2 where the whole tensor's would not be."""
+    assert_close(gpu, ref_mx, "mxfp8-mode " + name, **MX_TOL)
+    scale = float(np.max(np.abs(ref_exact)))
+    own = float(np.max(np.abs(ref_mx - ref_exact)) / scale) if scale > 0 else 0.0
+    assert_normwise(gpu, ref_exact, name, bound=max(MX_TOL["rtol"], 1.05 * own + 1e-3))
+
 def _bf16_matrix(rows, cols, seed):
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(rows, cols, generator=g) * torch.exp(torch.randn(rows, 1, generator=g) * 3)
@@ -125,15 +137,15 @@ def test_mxfp8_layer_parity_config4_sampled():
     tt = torch.from_numpy(toks).to(inp.hidden.device)
     go = f64(inp.grad_out[tt])
     got = {"out (sampled)": f64(out[tt]), "dhidden (sampled)": f64(dh[tt]), "dprobs (sampled)": f64(dp[tt])}
+    refs = {}
     for prec in ("mxfp8", "exact"):
         ref, cache = O.forward(f64(inp.hidden[tt]), inp.probs_np[toks], inp.map_np[toks], W, c.k, precision=prec)
         rdx, rdp, _ = O.backward(go, cache, W)
-        for (n, g), r in zip(got.items(), (ref, rdx, rdp)):
-            if prec == "mxfp8":
-                assert_close(g, r, n, **MX_TOL)
-            else:
-                assert_normwise(g, r, n, bound=MX_TOL["rtol"])
+        refs[prec] = dict(zip(got, (ref, rdx, rdp)))
+    for n, g in got.items():
+        _check_mx(g, refs["mxfp8"][n], refs["exact"][n], n)
 
+    refw = {}
     for prec in ("mxfp8", "exact"):
         refs, gots = [], []
         for e in picked:
@@ -147,12 +159,11 @@ def test_mxfp8_layer_parity_config4_sampled():
             d1 = f64(mg["routed_fc1"][e]) - mg0[e][0].double().numpy()
             d2 = f64(mg["routed_fc2"][e]) - mg0[e][1].double().numpy()
             gots.append((d1[:I], d1[I:], d2))
-        for j, kind in enumerate(("gate", "up", "down")):
-            g, r = np.stack([x[j] for x in gots]), np.stack([x[j] for x in refs])
-            if prec == "mxfp8":
-                assert_close(g, r, f"dW routed {kind} (busiest, median, least busy)", **MX_TOL)
-            else:
-                assert_normwise(g, r, f"dW routed {kind} (busiest, median, least busy)", bound=MX_TOL["rtol"])
+        refw[prec] = refs
+    for j, kind in enumerate(("gate", "up", "down")):
+        g = np.stack([x[j] for x in gots])
+        _check_mx(g, np.stack([x[j] for x in refw["mxfp8"]]), np.stack([x[j] for x in refw["exact"]]),
+                  f"dW routed {kind} (busiest, median, least busy)")
     for e, before in idle_before.items():
         assert torch.equal(mg["routed_fc1"][e], before)
 
