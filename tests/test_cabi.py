@@ -191,3 +191,42 @@ def test_mx_expert_tables_pointer_layout():
     bad = [torch.zeros((N, K // 16), dtype=torch.uint8) for _ in range(E)]   # wrong scale row stride
     with pytest.raises(ValueError):
         M.set_mx_expert_tables(B.moe_weights(), up=(q, cq, bad, csc))
+
+
+def test_a_c_program_links_and_calls_the_library(tmp_path):
+    """A plain C caller: compiled against include/moe.h, linked against libmoe.so,
+    it queries sizes, gets the argument errors of the header's contract and the
+    kernel names -- everything that needs no GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    M.load()
+    lib = B.lib_path()
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "moe.h"
+int main(void) {
+    moe_config c = {4096, 2048, 96, 6, 1024, MOE_W_BF16, 0.0f, 0, MOE_ACT_FP32, 0};
+    size_t ws = 0, sv = 0, pipe = 0;
+    if (moe_workspace_size(&c, &ws) != MOE_OK || ws == 0) return 1;
+    if (moe_saved_size(&c, &sv) != MOE_OK || sv == 0) return 2;
+    if (moe_host_pipe_size(&c, 4096, &pipe) != MOE_OK || pipe <= sv) return 3;
+    if (moe_workspace_size(NULL, &ws) != MOE_ERR_INVALID_ARG) return 4;
+    c.hidden = 2000;                                   /* not a multiple of 128 */
+    if (moe_workspace_size(&c, &ws) != MOE_ERR_UNSUPPORTED) return 5;
+    if (moe_forward(NULL, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL) != MOE_ERR_INVALID_ARG) return 6;
+    for (int i = 0; i < MOE_K_COUNT; ++i)
+        if (!moe_kernel_name(i)) return 7;
+    printf("%s %s\n", moe_kernel_name(MOE_K_WGRAD_FC1_ROUTED), moe_status_string(MOE_ERR_ROUTING));
+    return 0;
+}
+""")
+    exe = tmp_path / "caller"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), lib,
+                    "-Wl,-rpath," + os.path.dirname(lib), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.split()[0] == "gemm_wgrad_fc1_routed"
