@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--per-config", default="3,4,5",
                    help="further workloads measured after the headline one (comma list; empty: none)")
     p.add_argument("--per-config-steps", type=int, default=10)
+    p.add_argument("--act-variant", type=int, default=1,
+                   help="also time the headline workload with the other activation precision (0: skip)")
     p.add_argument("--ep-owner", type=int, default=16,
                    help="also time the expert-parallel owner step of the headline workload at this EP degree "
                         "(0: skip)")
@@ -664,6 +666,17 @@ def run_ours(args):
             per_config[str(other)] = {"unavailable": f"out of device memory: {ex}"}
         torch.cuda.empty_cache()
 
+    act_variant = None
+    if args.act_variant:
+        import copy
+        a2 = copy.copy(args)
+        a2.act_precision = "bf16" if args.act_precision == "fp32" else "fp32"
+        r3 = measure_config(cid, a2, args.per_config_steps, 3, False, dev, world, rank, local_rank)
+        act_variant = {"act_precision": a2.act_precision, **per_config_entry(r3),
+                       "note": ("single bf16 activations between the expert GEMMs: faster; its parity is against "
+                                "the bf16-rounding oracle, normwise 1e-2 of the exact definition")
+                       if a2.act_precision == "bf16" else "fp32 activations, two-term operands"}
+        torch.cuda.empty_cache()
     ep_owner = None
     if args.ep_owner > 1 and world == 1:
         ep_owner = measure_ep_owner(cid, args.ep_owner, max(10, args.per_config_steps), 3, dev)
@@ -695,6 +708,8 @@ def run_ours(args):
         line["per_config"] = per_config
     if ep_owner is not None:
         line["ep_owner_step"] = ep_owner
+    if act_variant is not None:
+        line["act_precision_variant"] = act_variant
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cid)
     if rank == 0:
