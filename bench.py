@@ -189,7 +189,9 @@ def kernel_work(name, T, H, E, k, I, R, E_act, mx=False, mg_bytes=4, act32=True)
     wb = bq if mx else b2                    # routed weight element
     ab = bq if mx else b2                    # routed fprop/dgrad input-row operand element
     a_in = bq if mx else f                   # routed down / dgrad-gate-up derived operand element
-    a_out = b2 if mx else f                  # routed gate/up epilogue's a (hi only when its GEMM is MXFP8)
+    # routed gate/up epilogue's a besides its MXFP8 copy: none with fp32 activations (the dgrad-down
+    # recomputes a from g, u), bf16 with bf16 ones; two terms when the down projection is BF16
+    a_out = (0 if act32 else b2) if mx else f
     W_fc1, W_down = E_act * 2 * I * H * wb, E_act * H * I * wb
     q_a = R * I * bq if mx else 0
     q_dgdu = R * 2 * I * bq if mx else 0

@@ -796,7 +796,9 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         a.n_tiles = 2 * I / kMxBN;
         a.k_blocks = H / kMxBK;
         a.gate_up_split = I;
-        set_gu_outputs(s, a, v.a, nullptr, v.gu, v.gu32);
+        // the routed down projection takes a quantised (a_q); a bf16 copy of a is read only by
+        // the bf16-activation dgrad-down (the fp32 one recomputes a from g, u)
+        set_gu_outputs(s, a, s.act32 ? nullptr : v.a, nullptr, v.gu, v.gu32);
         a.q_out = b.a_q;
         a.ld_q = I;
         a.q_sf = b.a_sf;
