@@ -52,15 +52,18 @@ template <int OP, int BN, bool SPLIT = false, bool DEEP = false>
 struct Cfg {
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = BN * kBK * 2;
-    static constexpr uint32_t L_BYTES = SPLIT ? ((OP == OP_WGRAD && B_BYTES > A_BYTES) ? B_BYTES : A_BYTES) : 0;
+    // (DEEP weight gradient: the A operand is the split one, its lo tile an A tile)
+    static constexpr uint32_t L_BYTES = SPLIT ? ((OP == OP_WGRAD && B_BYTES > A_BYTES && !DEEP) ? B_BYTES : A_BYTES) : 0;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + L_BYTES;
     // the weight-gradient epilogue double-buffers its main_grad boxes, so it
     // gives up operand stages (its K per tile is one expert's short segment); the
     // SwiGLU-backward epilogue (dgrad-down) moves more bytes than its mainloop, and
     // three stages leave it more of the memory system than four (measured)
-    static constexpr int BUFS = (OP == OP_WGRAD) ? 2 : 1;
+    // A DEEP weight gradient (long K per tile: the mainloop, not the main_grad stream, is the
+    // bound) gives the epilogue one box buffer per warp and the operands a third stage.
+    static constexpr int BUFS = (OP == OP_WGRAD) ? (DEEP ? 1 : 2) : 1;
     static constexpr int STAGES =
-        (OP == OP_WGRAD) ? (SPLIT ? ((BN == 256) ? 2 : 3) : ((BN == 256) ? 3 : (BN == 128 ? 5 : 6)))
+        (OP == OP_WGRAD) ? (SPLIT ? ((BN == 256) ? (DEEP ? 3 : 2) : 3) : ((BN == 256) ? 3 : (BN == 128 ? 5 : 6)))
                          : (SPLIT ? ((BN == 256) ? 3 : 4)
                                   : ((BN == 256) ? (OP == OP_BWD_DOWN && !DEEP ? 3 : 4) : (BN == 128 ? 6 : 8)));
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators; 128/256/512 are legal sizes
@@ -554,7 +557,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 // is TMA-stored back: one add per element, so the result is
 // fl32(main_grad + dW), or bf16(main_grad + bf16(dW)) for bf16 main_grad,
 // whatever the schedule.
-template <int BN>
+template <int BN, int BUFS>
 __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tmem_base, int q, int half,
                                                float* bufs, uint64_t* mg_bar, uint64_t* tfull, uint64_t* tempty,
                                                const uint64_t* ring_full, uint64_t* ring_empty,
@@ -609,6 +612,110 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
         tma_load_3d(bufs + b * (kStageTileBytes / 4), mc, &mg_bar[b], x, y, z);
     };
 
+    // add accumulator column chunk `col` into the box in buffer b (its row `lane`: 128 bytes,
+    // 16-byte unit j at j ^ (lane % 8), the 128-byte swizzle)
+    auto add_box = [&](const float (&v)[32], const float (&v2)[32], int b) {
+        uint4* srow = reinterpret_cast<uint4*>(bufs + b * (kStageTileBytes / 4) + lane * 32);
+        if (bf) {
+            // bf16(main_grad + bf16(dW)) as one packed rounding of the exact sum of two
+            // bf16 values: that sum is exact in fp32 unless their exponents differ by
+            // more than 15, and then the smaller lies below half a bf16 ulp of the
+            // larger either way, so this equals the fp32 add followed by rounding
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 m = srow[j ^ (lane & 7)];
+                uint32_t* mw = reinterpret_cast<uint32_t*>(&m);
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const int cidx = 8 * (j & 3) + 2 * z;
+                    const float d0 = j < 4 ? v[cidx] : v2[cidx];
+                    const float d1 = j < 4 ? v[cidx + 1] : v2[cidx + 1];
+                    const __nv_bfloat162 sum =
+                        __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&mw[z]), __floats2bfloat162_rn(d0, d1));
+                    mw[z] = *reinterpret_cast<const uint32_t*>(&sum);
+                }
+                srow[j ^ (lane & 7)] = m;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float4 m = reinterpret_cast<float4*>(srow)[j ^ (lane & 7)];
+                m.x += v[4 * j];
+                m.y += v[4 * j + 1];
+                m.z += v[4 * j + 2];
+                m.w += v[4 * j + 3];
+                reinterpret_cast<float4*>(srow)[j ^ (lane & 7)] = m;
+            }
+        }
+    };
+
+    if constexpr (BUFS == 1) {
+        // one box buffer: load, add, store, one box after the other (the tile's mainloop,
+        // long for these tiles, runs meanwhile on the other accumulator)
+        int rpos = 0;
+        Tile t;
+        int cur = ring_take(rpos++, t);
+        uint32_t parity = 0;
+        int it = 0;
+        bool ok = true;
+        while (ok && cur >= 0) {
+            const int acc = it & 1;
+            const uint32_t use = uint32_t(it >> 1);
+            ++it;
+            int w = 0;
+            if (lane == 0) w = mbar_wait(&tfull[acc], use & 1, abort_flag, args.status) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+            Tile tn;
+            const int nxt = ring_take(rpos++, tn);
+            if (nxt == -2) break;
+#pragma unroll 1
+            for (int c = 0; c < nb; ++c) {
+                if (lane == 0) {
+                    bulk_wait_read<0>();  // the previous store has read the buffer out
+                    load_box(t, c, 0);
+                }
+                const uint32_t col = uint32_t((half + c * kEpiHalves) * bw);
+                float v[32], v2[32];
+                tmem_ld32(t_row + col, v);
+                if (bf) tmem_ld32(t_row + col + 32, v2);
+                if (lane == 0) w = mbar_wait(&mg_bar[0], parity & 1, abort_flag, args.status) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                    ok = false;
+                    break;
+                }
+                (void)mbar_try_wait(&mg_bar[0], parity & 1);  // every lane acquires the box
+                __syncwarp();
+                parity ^= 1u;
+                add_box(v, v2, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const CUtensorMap* mc;
+                    int x, y, z;
+                    box(t, c, mc, x, y, z);
+                    tma_store_3d(mc, bufs, x, y, z);
+                    bulk_commit();
+                }
+            }
+            if (!ok) {
+                // a box load may be in flight: let it land before the buffer is given up
+                if (lane == 0) mbar_wait_drain(&mg_bar[0], parity & 1, args.status);
+                break;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            cur = nxt;
+            t = tn;
+        }
+        if (lane == 0) bulk_wait<0>();  // every store completes
+        __syncwarp();
+        return;
+    }
+
     int rpos = 0;
     Tile t;
     int cur = ring_take(rpos++, t);
@@ -660,39 +767,7 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
             __syncwarp();
             pending &= ~(1u << b);
             parity ^= 1u << b;
-            // row `lane` of the box: 128 bytes, 16-byte unit j at j ^ (lane % 8) (128-byte swizzle)
-            uint4* srow = reinterpret_cast<uint4*>(bufs + b * (kStageTileBytes / 4) + lane * 32);
-            if (bf) {
-                // bf16(main_grad + bf16(dW)) as one packed rounding of the exact sum of two
-                // bf16 values: that sum is exact in fp32 unless their exponents differ by
-                // more than 15, and then the smaller lies below half a bf16 ulp of the
-                // larger either way, so this equals the fp32 add followed by rounding
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 m = srow[j ^ (lane & 7)];
-                    uint32_t* mw = reinterpret_cast<uint32_t*>(&m);
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) {
-                        const int cidx = 8 * (j & 3) + 2 * z;
-                        const float d0 = j < 4 ? v[cidx] : v2[cidx];
-                        const float d1 = j < 4 ? v[cidx + 1] : v2[cidx + 1];
-                        const __nv_bfloat162 sum =
-                            __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&mw[z]), __floats2bfloat162_rn(d0, d1));
-                        mw[z] = *reinterpret_cast<const uint32_t*>(&sum);
-                    }
-                    srow[j ^ (lane & 7)] = m;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float4 m = reinterpret_cast<float4*>(srow)[j ^ (lane & 7)];
-                    m.x += v[4 * j];
-                    m.y += v[4 * j + 1];
-                    m.z += v[4 * j + 2];
-                    m.w += v[4 * j + 3];
-                    reinterpret_cast<float4*>(srow)[j ^ (lane & 7)] = m;
-                }
-            }
+            add_box(v, v2, b);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -952,7 +1027,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int half = (warp - 2) >> 2;
         float* my_staging = staging + (warp - 2) * C::BUFS * (kStageTileBytes / 4);
         if constexpr (OP == OP_WGRAD) {
-            wgrad_epilogue<BN>(args, tmem_base, q, half, my_staging, mg_bar + 2 * (warp - 2), tfull, tempty,
+            wgrad_epilogue<BN, C::BUFS>(args, tmem_base, q, half, my_staging, mg_bar + 2 * (warp - 2), tfull, tempty,
                                ring_full, ring_empty, ring_tile, abort_flag, &tmC0, &tmC1,
                                &tmS0, &tmS1);
         } else {
@@ -1301,6 +1376,8 @@ template <int OP, bool CLAMP = false>
 cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
     constexpr bool CAN_SPLIT = OP == OP_FWD_DOWN || OP == OP_BWD_GU || OP == OP_WGRAD;
     if (a.split && !CAN_SPLIT) return cudaErrorInvalidValue;
+    if constexpr (OP == OP_WGRAD)  // long K per tile, A the split operand: the deep build
+        if (bn == 256 && a.split == 1 && a.deep_stages) return launch_one<OP, 256, CLAMP, true, true>(m, a, grid, st);
     if (CAN_SPLIT && a.split) {
         switch (bn) {
             case 256: return launch_one<OP, 256, CLAMP, CAN_SPLIT>(m, a, grid, st);

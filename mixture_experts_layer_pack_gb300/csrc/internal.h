@@ -63,7 +63,8 @@ struct GemmArgs {
     __nv_bfloat16* out1lo;      // lo terms of out1 (p * a)
     int64_t ld_out1lo;
     int split;                  // 1: A, 2: B operand comes as hi (its map) + lo (map lo) terms
-    int deep_stages;            // dgrad-down with a long K: more stages (BF16 N tile 256: four; MXFP8: five)
+    int deep_stages;            // long K: dgrad-down more stages (BF16 N tile 256: four; MXFP8: five); gate/up
+                                // weight gradient with a two-term A: three stages, one main_grad box buffer
     int g0_operand;             // group 0 (the shared expert) reads its token rows through map g0:
                                 // 1: the A operand, 2: the B operand (0: the row buffer like the others)
     const float* row_scale;     // BWD_DOWN: per-row prob (null: 1)

@@ -1187,6 +1187,9 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         if (s.act32) {  // [dg|du] as hi + lo terms
             if (!map_mnmajor(&m.lo, ws.dgdulo_all, rows_all, 2 * I, 2 * I)) return MOE_ERR_INVALID_ARG;
             a.split = 1;
+            // with ~512 or more rows per expert a tile's mainloop outlasts its main_grad
+            // read-add-store: a third operand stage beats the second box buffer
+            a.deep_stages = int64_t(Ti) * k >= 512 * int64_t(E) ? 1 : 0;
         }
         // the shared expert is group 0 (its x rows: hidden), with either routed weight type
         if (!map_mnmajor(&m.a, ws.dgdu_all, rows_all, 2 * I, 2 * I) || !map_mnmajor(&m.b0, b.x_all, rows_all, H, H) ||

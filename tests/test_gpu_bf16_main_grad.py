@@ -76,6 +76,7 @@ CASES = {
     "bn64_skewed_gated": Case(T=517, H=384, E=12, k=3, I=192, seed=52, routing="zipf", drop="multi",
                               mg_bf16=True, gated=True, limit=0.3),
     "mxfp8": Case(T=300, H=256, E=8, k=2, I=128, seed=53, mx=True, mg_bf16=True),
+    "long_k": Case(T=1100, H=256, E=4, k=2, I=128, seed=54, mg_bf16=True),   # the deep weight-gradient build
 }
 
 

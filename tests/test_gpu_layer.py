@@ -31,6 +31,9 @@ SMALL = {
     "odd_experts": Case(T=333, H=128, E=13, k=3, I=64, seed=24, drop="iid"),   # byte-wise map rows
     "max_experts_topk": Case(T=256, H=128, E=1024, k=32, I=64, seed=25),         # the largest E and k
     "single_expert": Case(T=200, H=128, E=1, k=1, I=64, seed=26),
+    # ~512 rows per expert and more: the gate/up weight gradient's deep build (three stages,
+    # one main_grad box buffer per warp)
+    "long_k": Case(T=1100, H=256, E=4, k=2, I=128, seed=27, drop="iid"),
 }
 
 
