@@ -595,6 +595,15 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
     // at z = 0 when main_grad comes as a per-expert table, else the 3D map)
     auto box = [&](const Tile& t, int c, const CUtensorMap*& mc, int& x, int& y, int& z) {
         const int m0 = t.mt * kBM + q * 32;
+        if (args.mg_trans) {  // main_grad row = accumulator column, main_grad column = accumulator row
+            const bool sh = args.group0_shared && t.e == 0;
+            const int re = t.e - args.group0_shared;
+            mc = sh ? mS0 : (args.c0_tab ? args.c0_tab + re : mC0);
+            z = (sh || args.c0_tab) ? 0 : re;
+            x = m0;
+            y = t.nt * BN + (half + c * kEpiHalves) * bw;
+            return;
+        }
         const bool hi = m0 >= args.m_split;
         const bool sh = args.group0_shared && t.e == 0;
         const int re = t.e - args.group0_shared;
@@ -689,7 +698,17 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
                 (void)mbar_try_wait(&mg_bar[0], parity & 1);  // every lane acquires the box
                 __syncwarp();
                 parity ^= 1u;
-                add_box(v, v2, 0);
+                if (args.mg_trans) {
+                    // box row r (main_grad row) gets accumulator column r of this lane's row:
+                    // element (r, lane) of the 128-byte-swizzled fp32 box
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        float* e = bufs + r * 32 + ((((lane >> 2) ^ (r & 7)) << 2) | (lane & 3));
+                        *e += v[r];
+                    }
+                } else {
+                    add_box(v, v2, 0);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

@@ -70,6 +70,8 @@ struct GemmArgs {
     const float* row_scale;     // BWD_DOWN: per-row prob (null: 1)
     float* partial;             // per row: n_tiles * kEpiHalves partial dot products (null: skip)
     int m_split;                // WGRAD rows >= m_split go to the second main_grad map at row - m_split
+    int mg_trans;               // WGRAD (deep build, fp32 main_grad): the accumulator tile is the
+                                // transpose of the main_grad tile (its rows are main_grad columns)
     int inter;
     float swiglu_limit;         // > 0: SwiGLU inputs clamped, g <= L, |u| <= L (FWD_GU, BWD_DOWN epilogues)
     int mg_bf16;                // WGRAD: main_grad is bf16 (bf16(mg + bf16(dW))), else fp32 (mg + dW)

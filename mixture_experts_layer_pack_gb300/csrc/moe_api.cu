@@ -1205,8 +1205,36 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         Timed tm_(h, MOE_K_WGRAD_FC1_ROUTED, st);
         MOE_CU(launch_gemm(OP_WGRAD, bn, m, a, grid_of(int64_t(a.groups) * a.m_tiles * a.n_tiles, h->sms), st));
     }
-    // wgrad of down: main_grad[e] += go_e^T (p a)_e
-    {
+    // wgrad of down: main_grad[e] += go_e^T (p a)_e. With long tiles (the deep build, fp32
+    // main_grad) it runs transposed: the accumulator tile is (p a)_e^T go_e, whose split operand
+    // (p a as two terms) is A, so that its lo tile is the smaller one, and the epilogue adds
+    // it into main_grad's boxes transposed
+    const bool down_trans = s.act32 && !mg_bf16 && H % 256 == 0 && int64_t(Ti) * k >= 512 * int64_t(E);
+    if (down_trans) {
+        GemmArgs a = base_args(ws.status, s);
+        a.m_tiles = I / kBM;
+        a.n_tiles = H / 256;
+        a.mg_bf16 = 0;
+        a.tile_counter = ws.tile_counters + 1;
+        MOE_TRY(routed_mg_map(h, TB_MG_D, mg->routed_down, mg->expert_ptrs[2], H, I, mg->strides[5][0],
+                              mg->strides[5][1], false, st, &m.c0, &a.c0_tab));
+        if (!map_mnmajor(&m.a, ws.ap_all, rows_all, I, I) || !map_mnmajor(&m.lo, ws.aplo_all, rows_all, I, I) ||
+            !map_mnmajor(&m.b0, ws.go_all, rows_all, H, H) || !map_mnmajor(&m.g0, go, Ti, H, H) ||
+            !map_main_grad(&m.s0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], false))
+            return MOE_ERR_INVALID_ARG;
+        a.split = 1;
+        a.deep_stages = 1;
+        a.mg_trans = 1;
+        a.seg_off = b.seg_x;
+        a.groups = E + 1;
+        a.group0_shared = 1;
+        a.g0_operand = 2;  // group 0's B: grad_out rows
+        m.b1 = m.b0;
+        m.c1 = m.c0;
+        m.s1 = m.s0;
+        Timed tm_(h, MOE_K_WGRAD_DOWN_ROUTED, st);
+        MOE_CU(launch_gemm(OP_WGRAD, 256, m, a, grid_of(int64_t(a.groups) * a.m_tiles * a.n_tiles, h->sms), st));
+    } else {
         GemmArgs a = base_args(ws.status, s);
         const int bn = s.bn_wd;
         a.m_tiles = H / kBM;
