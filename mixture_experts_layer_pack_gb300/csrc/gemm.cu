@@ -658,6 +658,14 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
         }
     };
 
+    // the transposed add (mg_trans, fp32 main_grad): box row r (a main_grad row) gets
+    // accumulator column r of this lane's row, element (r, lane) of the 128-byte-swizzled box
+    auto add_box_t = [&](const float (&v)[32], int b) {
+        float* base = bufs + b * (kStageTileBytes / 4);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) base[r * 32 + ((((lane >> 2) ^ (r & 7)) << 2) | (lane & 3))] += v[r];
+    };
+
     if constexpr (BUFS == 1) {
         // one box buffer: load, add, store, one box after the other (the tile's mainloop,
         // long for these tiles, runs meanwhile on the other accumulator)
@@ -698,17 +706,10 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
                 (void)mbar_try_wait(&mg_bar[0], parity & 1);  // every lane acquires the box
                 __syncwarp();
                 parity ^= 1u;
-                if (args.mg_trans) {
-                    // box row r (main_grad row) gets accumulator column r of this lane's row:
-                    // element (r, lane) of the 128-byte-swizzled fp32 box
-#pragma unroll
-                    for (int r = 0; r < 32; ++r) {
-                        float* e = bufs + r * 32 + ((((lane >> 2) ^ (r & 7)) << 2) | (lane & 3));
-                        *e += v[r];
-                    }
-                } else {
+                if (args.mg_trans)
+                    add_box_t(v, 0);
+                else
                     add_box(v, v2, 0);
-                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -786,7 +787,10 @@ __device__ __forceinline__ void wgrad_epilogue(const GemmArgs& args, uint32_t tm
             __syncwarp();
             pending &= ~(1u << b);
             parity ^= 1u << b;
-            add_box(v, v2, b);
+            if (args.mg_trans)
+                add_box_t(v, b);
+            else
+                add_box(v, v2, b);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {

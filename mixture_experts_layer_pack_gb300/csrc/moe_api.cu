@@ -1208,8 +1208,10 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
     // wgrad of down: main_grad[e] += go_e^T (p a)_e. With long tiles (the deep build, fp32
     // main_grad) it runs transposed: the accumulator tile is (p a)_e^T go_e, whose split operand
     // (p a as two terms) is A, so that its lo tile is the smaller one, and the epilogue adds
-    // it into main_grad's boxes transposed
-    const bool down_trans = s.act32 && !mg_bf16 && H % 256 == 0 && int64_t(Ti) * k >= 512 * int64_t(E);
+    // it into main_grad's boxes transposed. (With short tiles the main_grad stream is the
+    // bound and the transposed add slows it: config 2 317 -> 323 us, config 4 7.26 -> 7.88 ms.)
+    const bool down_deep = int64_t(Ti) * k >= 512 * int64_t(E);
+    const bool down_trans = s.act32 && !mg_bf16 && H % 256 == 0 && down_deep;
     if (down_trans) {
         GemmArgs a = base_args(ws.status, s);
         a.m_tiles = I / kBM;
