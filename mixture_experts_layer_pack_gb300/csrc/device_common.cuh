@@ -273,36 +273,46 @@ __device__ __forceinline__ int64_t sf_atom_offset(int64_t r, int kb, int k_block
 
 // Warp-wide copy of one bf16 row (src null: zeros) that also writes its MXFP8
 // quantisation along the row: a lane owns 8 consecutive elements (16 bytes), 4
-// consecutive lanes one 32-element block. vec_per_row = row length / 8 must be
-// a multiple of 4; all 32 lanes must call it.
-__device__ __forceinline__ void copy_quant_row(const uint4* src, uint4* dst, uint8_t* q, uint8_t* sf, int64_t row,
+// consecutive lanes one 32-element block. Each lane loads up to four vectors
+// before it converts and stores any. vec_per_row = row length / 8 must be a
+// multiple of 4; all 32 lanes must call it.
+__device__ __forceinline__ void copy_quant_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int64_t row,
                                                int vec_per_row) {
+    constexpr int kInFlight = 4;
     const int lane = threadIdx.x & 31;
     const int k_blocks = vec_per_row / 4;
     uint8_t* qrow = q + row * int64_t(vec_per_row) * 8;
-    for (int base = 0; base < vec_per_row; base += 32) {
-        const int v = base + lane;
-        const bool active = v < vec_per_row;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (active && src) w = __ldg(src + v);
-        float f[8];
-        unpack_bf16x2(w.x, f[0], f[1]);
-        unpack_bf16x2(w.y, f[2], f[3]);
-        unpack_bf16x2(w.z, f[4], f[5]);
-        unpack_bf16x2(w.w, f[6], f[7]);
-        float amax = 0.0f;
+    for (int base = 0; base < vec_per_row; base += 32 * kInFlight) {
+        uint4 w[kInFlight];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const uint32_t code = e8m0_code(amax);
-        const float mul = e8m0_inv_scale(code);
-        if (active) {
-            dst[v] = w;
-            *reinterpret_cast<uint2*>(qrow + int64_t(v) * 8) =
-                make_uint2(e4m3x4(f[0] * mul, f[1] * mul, f[2] * mul, f[3] * mul),
-                           e4m3x4(f[4] * mul, f[5] * mul, f[6] * mul, f[7] * mul));
-            if ((lane & 3) == 0) sf[sf_atom_offset(row, v >> 2, k_blocks)] = uint8_t(code);
+        for (int j = 0; j < kInFlight; ++j) {
+            const int v = base + j * 32 + lane;
+            w[j] = (src && v < vec_per_row) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kInFlight; ++j) {
+            // a 4-lane block is active or idle as a whole: vec_per_row is a multiple of 4
+            const int v = base + j * 32 + lane;
+            float f[8];
+            unpack_bf16x2(w[j].x, f[0], f[1]);
+            unpack_bf16x2(w[j].y, f[2], f[3]);
+            unpack_bf16x2(w[j].z, f[4], f[5]);
+            unpack_bf16x2(w[j].w, f[6], f[7]);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const uint32_t code = e8m0_code(amax);
+            const float mul = e8m0_inv_scale(code);
+            if (v < vec_per_row) {
+                dst[v] = w[j];
+                *reinterpret_cast<uint2*>(qrow + int64_t(v) * 8) =
+                    make_uint2(e4m3x4(f[0] * mul, f[1] * mul, f[2] * mul, f[3] * mul),
+                               e4m3x4(f[4] * mul, f[5] * mul, f[6] * mul, f[7] * mul));
+                if ((lane & 3) == 0) sf[sf_atom_offset(row, v >> 2, k_blocks)] = uint8_t(code);
+            }
         }
     }
 }
