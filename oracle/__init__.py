@@ -6,7 +6,8 @@ does.
 
 Parity pins: every function here is checked by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` against values fixed by the pages or by mathematics
-(closed forms, finite differences, brute force, library routines, spec values).
-The only function without such a pin is the optional SwiGLU clamp, which the
-oracle does not implement (parity unpinned; the library rejects it).
+(closed forms, finite differences, brute force, library routines, spec values),
+the swiglu_limit clamp and the shared output gate included (central finite
+differences of every gradient with the clamp active, a single unit worked by
+hand, and a limit too large to bind leaving the layer unchanged).
 """
