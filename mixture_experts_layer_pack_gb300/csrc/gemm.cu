@@ -105,8 +105,13 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a) {
         t.nt = r - t.mt * a.n_tiles;
         const int lo = a.seg_off ? a.seg_off[t.e] : 0;
         const int hi = a.seg_off ? a.seg_off[t.e + 1] : a.seg_len;
+        int len = hi - lo;
+        if (a.seg_off && a.seg_rows) {
+            const int valid = (a.group0_shared && t.e == 0) ? a.g0_rows : a.seg_rows[t.e - a.group0_shared];
+            len = min(len, valid);
+        }
         t.k_lo = lo;
-        t.kblocks = (hi - lo + kBK - 1) / kBK;
+        t.kblocks = (len + kBK - 1) / kBK;
     } else {
         t.mt = tile / a.n_tiles;
         t.nt = tile - t.mt * a.n_tiles;

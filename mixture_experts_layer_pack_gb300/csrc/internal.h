@@ -39,6 +39,10 @@ struct GemmArgs {
     // segment scheduling (OP_WGRAD)
     const int* seg_off;         // [groups+1] row offsets of each group's K range; null: [0, seg_len)
     int seg_len;
+    const int* seg_rows;        // with seg_off: valid rows of each routed group (its token count); a group's
+                                // K range then ends with its last 64-row block that holds a valid row (the
+                                // padding rows after it are zero and add nothing). null: the whole range
+    int g0_rows;                // with seg_rows and group0_shared: valid rows of group 0 (the tokens)
     int groups;
     int m_tiles;                // M / 128
     // epilogue operands

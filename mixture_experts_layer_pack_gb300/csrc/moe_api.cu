@@ -1198,6 +1198,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
             !map_main_grad(&m.s1, mg->shared_up, 1, I, H, 0, mg->strides[1][1], mg_bf16))
             return MOE_ERR_INVALID_ARG;
         a.seg_off = b.seg_x;
+        a.seg_rows = b.counts;
+        a.g0_rows = s.shared ? Ti : 0;
         a.groups = E + 1;
         a.group0_shared = 1;
         a.g0_operand = 2;
@@ -1228,6 +1230,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.deep_stages = 1;
         a.mg_trans = 1;
         a.seg_off = b.seg_x;
+        a.seg_rows = b.counts;
+        a.g0_rows = s.shared ? Ti : 0;
         a.groups = E + 1;
         a.group0_shared = 1;
         a.g0_operand = 2;  // group 0's B: grad_out rows
@@ -1255,6 +1259,8 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
             !map_main_grad(&m.s0, mg->shared_down, 1, H, I, 0, mg->strides[2][1], mg_bf16))
             return MOE_ERR_INVALID_ARG;
         a.seg_off = b.seg_x;
+        a.seg_rows = b.counts;
+        a.g0_rows = s.shared ? Ti : 0;
         a.groups = E + 1;
         a.group0_shared = 1;
         a.g0_operand = 1;

@@ -3,7 +3,8 @@ re-runs the row placement, the shared output gate and the gate/up GEMMs.
 
 Results are bitwise those of the default mode, also with two microbatches in
 flight on one handle (forward 1, forward 2, backward 2, backward 1), and the
-saved state is a small fraction of the default one."""
+saved state is a small fraction of the default one. The routed-only layer
+(no shared expert, the owner step of expert parallelism) takes the same path."""
 import pytest
 import torch
 
@@ -12,15 +13,17 @@ from tests.harness import Case, make_inputs, weight_views
 
 pytestmark = pytest.mark.gpu
 
-CASES = {
-    "bf16_gated_clamp": Case(T=300, H=256, E=8, k=2, I=128, seed=101, drop="iid", gated=True, limit=0.5),
-    "mxfp8": Case(T=260, H=256, E=6, k=2, I=128, seed=102, mx=True),
+CASES = {   # (case, shared expert)
+    "bf16_gated_clamp": (Case(T=300, H=256, E=8, k=2, I=128, seed=101, drop="iid", gated=True, limit=0.5), True),
+    "mxfp8": (Case(T=260, H=256, E=6, k=2, I=128, seed=102, mx=True), True),
+    "routed_only": (Case(T=280, H=256, E=8, k=2, I=128, seed=103, limit=0.5), False),
+    "routed_only_mxfp8": (Case(T=250, H=256, E=6, k=2, I=128, seed=104, mx=True), False),
 }
 
 
-def _layer(c, recompute):
+def _layer(c, recompute, shared=True):
     return M.MoELayer(c.T, c.H, c.E, c.k, c.I, routed_wtype=M.binding.MOE_W_MXFP8 if c.mx else M.binding.MOE_W_BF16,
-                      swiglu_limit=c.limit, recompute_dispatch=recompute)
+                      swiglu_limit=c.limit, recompute_dispatch=recompute, shared_expert=shared)
 
 
 def _grads(inp):
@@ -31,7 +34,8 @@ def _grads(inp):
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_recompute_matches_saved_activations_bitwise(name):
-    inp = make_inputs(CASES[name])
+    case, shared = CASES[name]
+    inp = make_inputs(case)
     c = inp.case
     wv = weight_views(inp)
     rmap = inp.routing_map.view(torch.uint8)
@@ -39,7 +43,7 @@ def test_recompute_matches_saved_activations_bitwise(name):
     batches = [(inp.hidden, inp.grad_out), (inp.hidden * -1.5, inp.grad_out * 0.5)]
 
     ref = []                                   # default mode, one microbatch at a time
-    A = _layer(c, False)
+    A = _layer(c, False, shared)
     if c.mx:
         A.prepare_weights(wv)
     for hid, go in batches:
@@ -50,7 +54,7 @@ def test_recompute_matches_saved_activations_bitwise(name):
     torch.cuda.synchronize()
     assert A.device_status() == 0
 
-    B = _layer(c, True)                        # recompute mode, both microbatches in flight
+    B = _layer(c, True, shared)                # recompute mode, both microbatches in flight
     if c.mx:
         B.prepare_weights(wv)
     assert M.moe_saved_size(B.cfg) * 4 < M.moe_saved_size(A.cfg)
