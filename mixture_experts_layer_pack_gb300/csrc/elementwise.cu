@@ -19,7 +19,8 @@ namespace {
 // The grad gather, walked from the token side: item t*k + s copies row t of src
 // to the permuted row row_of[t,s] of dst (nothing for a missing route); items
 // past T*k zero the padding rows at the end of each expert's segment
-// (offs_pad[e] + counts[e] up to the next multiple of 128). Consecutive warps
+// (offs_pad[e] + counts[e] up to the next multiple of 64: the weight gradients' K
+// ranges end there, and the padding rows after it are read by nothing). Consecutive warps
 // take the slots of one token, so each source row leaves DRAM once however its
 // slots are spread over the experts. One warp per item, 16-byte vectors; with
 // dst_q the row is also quantised to MXFP8 along H.
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
         const int e = int(j / kBM);
         const int r = int(j % kBM);
         const int cnt = __ldg(counts + e);
-        if (r >= (cnt + kBM - 1) / kBM * kBM - cnt) return;
+        if (r >= (cnt + kBK - 1) / kBK * kBK - cnt) return;
         pos = __ldg(offs_pad + e) + cnt + r;
     }
     uint4* d = dst + pos * vec_per_row;

@@ -265,7 +265,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
     const int m_base = t.mt * kBM + q * 32;
     const int sub_row = lane >> 3;
     const int sub_col = 4 * (lane & 7);
-    const bool lane_row_valid = m_base + lane < a.rows_valid;
+    // rows a later kernel reads: below rows_valid and, with group row counts, below the end
+    // of the tile's group's last 64-row block that holds a valid row
+    int row_lim = a.rows_valid;
+    if (a.seg_off && a.seg_rows) {
+        const int valid = (a.group0_shared && t.e == 0) ? a.g0_rows : a.seg_rows[t.e - a.group0_shared];
+        row_lim = min(row_lim, a.seg_off[t.e] + (valid + kBK - 1) / kBK * kBK);
+    }
+    const bool lane_row_valid = m_base + lane < row_lim;
 
     if (OP == OP_FWD_GU) {
         const int j0 = t.nt * (BN / 2);
@@ -305,12 +312,12 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                     if (MX) {  // the routed down projection's operand: a quantised along I
                         uint32_t code;
                         const uint32_t qv = mx_quant_lane4(av, code);
-                        if (row < a.rows_valid) {
+                        if (row < row_lim) {
                             *reinterpret_cast<uint32_t*>(a.q_out + int64_t(row) * a.ld_q + col) = qv;
                             if ((lane & 7) == 0) a.q_sf[sf_atom_offset(row, col >> 5, a.q_kblocks)] = uint8_t(code);
                         }
                     }
-                    if (row >= a.rows_valid) continue;
+                    if (row >= row_lim) continue;
                     float* gu = a.outf + int64_t(row) * a.ld_outf;
                     *reinterpret_cast<float4*>(gu + col) = g4;
                     *reinterpret_cast<float4*>(gu + a.inter + col) = u4;
@@ -346,7 +353,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                     // 32-column block); a itself becomes its exact dequantised value
                     uint32_t code;
                     const uint32_t qv = mx_quant_lane4(av, code);
-                    if (row < a.rows_valid) {
+                    if (row < row_lim) {
                         *reinterpret_cast<uint32_t*>(a.q_out + int64_t(row) * a.ld_q + col) = qv;
                         if ((lane & 7) == 0) a.q_sf[sf_atom_offset(row, col >> 5, a.q_kblocks)] = uint8_t(code);
                     }
@@ -354,7 +361,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 #pragma unroll
                     for (int z = 0; z < 4; ++z) av[z] = e4m3_value(qv >> (8 * z)) * sc;
                 }
-                if (row >= a.rows_valid) continue;
+                if (row >= row_lim) continue;
                 *reinterpret_cast<uint2*>(a.out0 + int64_t(row) * a.ld_out0 + col) =
                     make_uint2(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]));
                 __nv_bfloat16* gu = a.outh + int64_t(row) * a.ld_outh;
@@ -373,7 +380,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             for (int i = 0; i < 8; ++i) {
                 const float4 x = staged(staging, i);
                 const int row = m_base + i * 4 + sub_row;
-                if (row >= a.rows_valid) continue;
+                if (row >= row_lim) continue;
                 if (a.outf)
                     *reinterpret_cast<float4*>(a.outf + int64_t(row) * a.ld_outf + col) = x;
                 else
@@ -402,7 +409,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int row = m_base + i * 4 + sub_row;
-                    if (row < a.rows_valid) {
+                    if (row < row_lim) {
                         const float* gu = a.inf + int64_t(row) * a.ld_inf;
                         gq[i] = __ldg(reinterpret_cast<const float4*>(gu + col));
                         uq[i] = __ldg(reinterpret_cast<const float4*>(gu + a.inter + col));
@@ -442,7 +449,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                         uint32_t cg, cu;
                         const uint32_t qg = mx_quant_lane4(dg, cg);
                         const uint32_t qu = mx_quant_lane4(du, cu);
-                        if (row < a.rows_valid) {
+                        if (row < row_lim) {
                             uint8_t* qo = a.q_out + int64_t(row) * a.ld_q;
                             *reinterpret_cast<uint32_t*>(qo + col) = qg;
                             *reinterpret_cast<uint32_t*>(qo + a.inter + col) = qu;
@@ -452,7 +459,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                             }
                         }
                     }
-                    if (row >= a.rows_valid) continue;
+                    if (row >= row_lim) continue;
                     const int64_t o = int64_t(row) * a.ld_out0 + col;
                     const int64_t ol = int64_t(row) * a.ld_out0lo + col;
                     store_split4(a.out0 + o, a.out0lo ? a.out0lo + ol : nullptr, dg);
@@ -470,7 +477,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = m_base + i * 4 + sub_row;
-                if (row < a.rows_valid) {
+                if (row < row_lim) {
                     aw[i] = __ldg(reinterpret_cast<const uint2*>(a.in0 + int64_t(row) * a.ld_in0 + col));
                     const __nv_bfloat16* gu = a.inh + int64_t(row) * a.ld_inh;
                     gw[i] = __ldg(reinterpret_cast<const uint2*>(gu + col));
@@ -517,7 +524,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                     uint32_t cg, cu;
                     const uint32_t qg = mx_quant_lane4(dg, cg);
                     const uint32_t qu = mx_quant_lane4(du, cu);
-                    if (row < a.rows_valid) {
+                    if (row < row_lim) {
                         uint8_t* qo = a.q_out + int64_t(row) * a.ld_q;
                         *reinterpret_cast<uint32_t*>(qo + col) = qg;
                         *reinterpret_cast<uint32_t*>(qo + a.inter + col) = qu;
@@ -527,7 +534,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
                         }
                     }
                 }
-                if (row >= a.rows_valid) continue;
+                if (row >= row_lim) continue;
                 __nv_bfloat16* o = a.out0 + int64_t(row) * a.ld_out0;
                 *reinterpret_cast<uint2*>(o + col) = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
                 *reinterpret_cast<uint2*>(o + a.inter + col) =
@@ -546,7 +553,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, int
             v += __shfl_xor_sync(0xffffffffu, v, 2);
             v += __shfl_xor_sync(0xffffffffu, v, 4);
             const int row = m_base + i * 4 + sub_row;
-            if ((lane & 7) == 0 && row < a.rows_valid && a.partial)
+            if ((lane & 7) == 0 && row < row_lim && a.partial)
                 a.partial[(int64_t(row) * a.n_tiles + t.nt) * kEpiHalves + half] = v;
         }
     }

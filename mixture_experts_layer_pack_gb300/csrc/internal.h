@@ -38,10 +38,13 @@ struct GemmArgs {
     int gate_up_split;          // I: offset of the up half (N for FWD_GU, K for BWD_GU)
     // segment scheduling (OP_WGRAD)
     const int* seg_off;         // [groups+1] row offsets of each group's K range; null: [0, seg_len)
+                                // (OP 0..3: each group's first row, for the row limits below)
     int seg_len;
-    const int* seg_rows;        // with seg_off: valid rows of each routed group (its token count); a group's
-                                // K range then ends with its last 64-row block that holds a valid row (the
-                                // padding rows after it are zero and add nothing). null: the whole range
+    const int* seg_rows;        // with seg_off: valid rows of each routed group (its token count). OP_WGRAD:
+                                // a group's K range ends with its last 64-row block that holds a valid row
+                                // (the padding rows after it are zero and add nothing); OP 0..3: the
+                                // epilogue stores only rows below that block's end (the padding past it
+                                // is read by nothing). null: every row
     int g0_rows;                // with seg_rows and group0_shared: valid rows of group 0 (the tokens)
     int groups;
     int m_tiles;                // M / 128

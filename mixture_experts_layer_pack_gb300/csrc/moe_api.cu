@@ -424,6 +424,19 @@ GemmArgs base_args(int* status, const Shape& s) {
 
 int grid_of(int64_t tiles, int sms) { return int(tiles < sms ? tiles : sms); }
 
+// Row tiles of the routed GEMMs (gate/up, down, dgrad-down, dgrad through gate/up):
+// a group's rows past its last 64-row block that holds a valid row are padding that
+// nothing reads -- the weight gradients' K ranges end at that block, the combine,
+// the un-permute and the dprob scatter read valid rows only -- so the epilogues store
+// (and the dgrad-down loads) rows below that bound only. start: each group's first
+// row; rows: each routed group's valid rows; g0_rows: group 0's when it is the shared
+// expert (group0_shared).
+void set_row_limits(GemmArgs& a, const int* start, const int* rows, int g0_rows) {
+    a.seg_off = start;
+    a.seg_rows = rows;
+    a.g0_rows = g0_rows;
+}
+
 // Gate/up epilogue outputs: a (hi terms; with fp32 activations also the lo terms,
 // where a_lo is given) and [g|u] (bf16, or fp32 with fp32 activations).
 void set_gu_outputs(const Shape& s, GemmArgs& a, __nv_bfloat16* a_hi, __nv_bfloat16* a_lo, __nv_bfloat16* gu,
@@ -792,6 +805,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
             return MOE_ERR_INVALID_ARG;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
+        set_row_limits(a, b.offs_pad, b.counts, 0);
         a.num_mtiles = rows / kBM;
         a.n_tiles = 2 * I / kMxBN;
         a.k_blocks = H / kMxBK;
@@ -825,6 +839,7 @@ static moe_status redispatch(moe_handle* h, const moe_saved* saved, cudaStream_t
         a.group0_shared = 1;
         a.mtile_expert = b.mtile_x;
         a.num_mtiles_dev = b.meta + 3;
+        set_row_limits(a, b.seg_x, b.counts, s.shared ? Ti : 0);
         a.num_mtiles = rows_all / kBM;
         a.n_tiles = 2 * I / bn;
         a.k_blocks = H / kBK;
@@ -907,6 +922,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         m.b1 = m.b0;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
+        set_row_limits(a, b.offs_pad, b.counts, 0);
         a.num_mtiles = rows / kBM;
         a.n_tiles = H / kMxBN;
         a.k_blocks = I / kMxBK;
@@ -933,6 +949,7 @@ static moe_status forward_impl(moe_handle* h, int64_t T, const void* hidden, con
         a.group0_shared = 1;
         a.mtile_expert = b.mtile_x;
         a.num_mtiles_dev = b.meta + 3;
+        set_row_limits(a, b.seg_x, b.counts, s.shared ? Ti : 0);
         a.num_mtiles = rows_all / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = I / kBK;
@@ -1037,6 +1054,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         m.b1 = m.b0;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
+        set_row_limits(a, b.offs_pad, b.counts, 0);
         a.num_mtiles = rows / kBM;
         a.n_tiles = I / kMxBN;
         a.k_blocks = H / kMxBK;
@@ -1068,6 +1086,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.group0_shared = 1;
         a.mtile_expert = b.mtile_x;
         a.num_mtiles_dev = b.meta + 3;
+        set_row_limits(a, b.seg_x, b.counts, s.shared ? Ti : 0);
         a.num_mtiles = rows_all / kBM;
         a.n_tiles = I / bn;
         a.k_blocks = H / kBK;
@@ -1115,6 +1134,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
             return MOE_ERR_INVALID_ARG;
         a.mtile_expert = b.mtile_expert;
         a.num_mtiles_dev = b.meta;
+        set_row_limits(a, b.offs_pad, b.counts, 0);
         a.num_mtiles = rows / kBM;
         a.n_tiles = H / kMxBN;
         a.k_blocks = 2 * I / kMxBK;
@@ -1142,6 +1162,7 @@ moe_status moe_backward(moe_handle* h, const void* grad_out, const moe_saved* sa
         a.group0_shared = 1;
         a.mtile_expert = b.mtile_x;
         a.num_mtiles_dev = b.meta + 3;
+        set_row_limits(a, b.seg_x, b.counts, s.shared ? Ti : 0);
         a.num_mtiles = rows_all / kBM;
         a.n_tiles = H / bn;
         a.k_blocks = 2 * I / kBK;

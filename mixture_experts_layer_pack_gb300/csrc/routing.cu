@@ -11,7 +11,9 @@
 // Order is deterministic: slots list a token's experts in ascending id order;
 // within an expert, routes are ordered by token index. Each expert segment is
 // padded to a multiple of 128 rows so that a GEMM row tile never spans two
-// experts; padding rows have source token -1, prob 0 and zero activations.
+// experts; padding rows have source token -1 and prob 0, and zero activations up
+// to the end of the expert's last 64-row block that holds a route (the weight
+// gradients' K ranges end there; the padding rows after it are read by nothing).
 //
 // The forward's three launches:
 //   pack+rank  one thread per token, 128-token blocks: ids[t,:], pp[t,:], -1 slots;
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         perm_src[pos] = -1;
         pp_perm[pos] = 0.0f;
     }
+    if (r >= (cnt + kBK - 1) / kBK * kBK - cnt) return;  // past the last 64-row block with a route
     uint4* dst = x_perm + int64_t(pos) * vec_per_row;
     if (x_q)
         copy_quant_row(nullptr, dst, x_q, x_sf, pos, vec_per_row);
