@@ -432,7 +432,9 @@ class MoELayer:
     """Holds a handle, its workspace and one saved-state block (all torch device memory)."""
 
     def __init__(self, max_tokens, hidden, num_experts, topk, inter, device="cuda", routed_wtype=MOE_W_BF16,
-                 swiglu_limit=0.0, recompute_dispatch=False, act_precision=None, shared_expert=True):
+                 swiglu_limit=0.0, recompute_dispatch=False, act_precision=None, shared_expert=True, fill=None):
+        """fill: a byte value written over the workspace and saved-state memory before the
+        handle is created (None: left as allocated); no result may depend on it."""
         import torch
         self.cfg = moe_config(max_tokens, hidden, num_experts, topk, inter, routed_wtype, float(swiglu_limit),
                               int(bool(recompute_dispatch)),
@@ -443,6 +445,9 @@ class MoELayer:
         sv = moe_saved_size(self.cfg)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
         self.saved_mem = torch.empty(sv, dtype=torch.uint8, device=self.device)
+        if fill is not None:
+            self.workspace.fill_(int(fill))
+            self.saved_mem.fill_(int(fill))
         with torch.cuda.device(self.device):
             self.handle = moe_create(self.cfg, self.workspace)
             self.saved = moe_saved_create(self.handle, self.saved_mem)

@@ -176,6 +176,36 @@ def test_determinism():
         assert torch.equal(a.main_grads[n], b.main_grads[n]), n
 
 
+@pytest.mark.parametrize("case", [
+    Case(T=300, H=256, E=8, k=2, I=128, seed=35, drop="iid"),                 # fp32 activations
+    Case(T=517, H=384, E=12, k=3, I=192, seed=36, routing="zipf", act_bf16=True),
+    Case(T=290, H=256, E=6, k=2, I=128, seed=37, mx=True, limit=0.5),
+])
+def test_results_do_not_depend_on_workspace_contents(case):
+    """The workspace and saved-state memory filled with NaN bytes (0xFF) or with zeros
+    before the handle is created: bitwise the same results, two steps each. Padding rows
+    past each expert's last 64-row block that holds a route are never written, so this
+    also shows that nothing reads them into a result."""
+    import mixture_experts_layer_pack_gb300 as M
+    inp = make_inputs(case)
+    c = inp.case
+    res = []
+    for fill in (0x00, 0xFF):
+        layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I, routed_wtype=M.binding.MOE_W_MXFP8 if c.mx else M.binding.MOE_W_BF16,
+                           swiglu_limit=c.limit,
+                           act_precision=M.binding.MOE_ACT_BF16 if c.act_bf16 else M.binding.MOE_ACT_FP32, fill=fill)
+        steps = [run_gpu(inp, layer=layer) for _ in range(2)]
+        assert layer.device_status() == 0
+        res.append(steps)
+        layer.close()
+    for a, b in zip(*res):
+        for name, x, y in (("out", a.out, b.out), ("dhidden", a.dhidden, b.dhidden), ("dprobs", a.dprobs, b.dprobs)):
+            assert torch.equal(x, y), name
+        for n in a.main_grads:
+            assert torch.equal(a.main_grads[n], b.main_grads[n]), n
+    assert torch.isfinite(res[1][0].out.float()).all()
+
+
 def test_rows_without_routes_and_zero_token_experts():
     c = Case(T=200, H=128, E=6, k=2, I=64, seed=31)
     r = make_routing(c.T, c.E, c.k, c.seed)
