@@ -373,6 +373,13 @@ moe_status moe_route_noalloc(int64_t T, int64_t E, int64_t k, const uint8_t* rou
  * call (MOE_OK, MOE_ERR_ROUTING or MOE_ERR_TIMEOUT) and clears it. */
 moe_status moe_device_status(moe_handle* h, void* stream);
 
+/* Test hook for the timeout path: enqueues one block that waits on an mbarrier
+ * nothing completes, with the same bounded wait the GEMM kernels use; the wait
+ * gives up after the library's limit (2 s), records MOE_ERR_TIMEOUT in the
+ * handle's device status (read by moe_device_status) and the block exits, so
+ * the context and the handle stay usable. Asynchronous on `stream`. */
+moe_status moe_selftest_timeout(moe_handle* h, void* stream);
+
 /* Number of kernels this library has launched in this process. */
 uint64_t moe_launch_count(void);
 

@@ -8,7 +8,7 @@ from .binding import (HostPipe, MoELayer, MoeError, load, main_grads_from_combin
                       moe_host_step,
                       moe_destroy, moe_device_status, moe_export_routing, moe_forward, moe_forward_topk, moe_kernel_name, moe_launch_count,
                       moe_profile_enable, moe_profile_read, moe_profile_select, moe_route_noalloc,
-                      moe_prepare_weights, moe_quantize_mxfp8, mxfp8_weight, mxfp8_view,
+                      moe_prepare_weights, moe_quantize_mxfp8, moe_selftest_timeout, mxfp8_weight, mxfp8_view,
                       moe_main_grads, moe_saved_create, moe_saved_destroy, moe_saved_size, moe_weights,
                       moe_workspace_size, set_expert_tables, set_main_grad_tables, set_mx_expert_tables, weights_from_combined, wview)
 
@@ -17,6 +17,6 @@ __all__ = ["HostPipe", "MoELayer", "MoeError", "load", "main_grads_from_combined
            "moe_host_step",
            "moe_destroy", "moe_device_status", "moe_export_routing", "moe_forward", "moe_forward_topk", "moe_kernel_name",
            "moe_launch_count", "moe_profile_enable", "moe_profile_read", "moe_profile_select", "moe_route_noalloc",
-           "moe_prepare_weights", "moe_quantize_mxfp8", "mxfp8_weight", "mxfp8_view",
+           "moe_prepare_weights", "moe_quantize_mxfp8", "moe_selftest_timeout", "mxfp8_weight", "mxfp8_view",
            "moe_main_grads", "moe_saved_create", "moe_saved_destroy", "moe_saved_size", "moe_weights",
            "moe_workspace_size", "set_expert_tables", "set_main_grad_tables", "set_mx_expert_tables", "weights_from_combined", "wview"]

@@ -14,6 +14,7 @@ c_int64, c_int32, c_float, c_void_p, c_size_t = (ctypes.c_int64, ctypes.c_int32,
                                                  ctypes.c_void_p, ctypes.c_size_t)
 
 MOE_OK = 0
+MOE_ERR_ROUTING, MOE_ERR_TIMEOUT = 3, 5    # device-detected errors (moe_device_status)
 MOE_W_BF16, MOE_W_MXFP8 = 0, 1
 MOE_G_FP32, MOE_G_BF16 = 0, 1
 MOE_ACT_FP32, MOE_ACT_BF16 = 0, 1   # activations between the expert GEMMs (include/moe.h, moe_act)
@@ -55,7 +56,7 @@ EXPORTED = ("moe_workspace_size", "moe_create", "moe_destroy", "moe_saved_size",
             "moe_launch_count", "moe_status_string", "moe_profile_enable", "moe_profile_read", "moe_kernel_name",
             "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8", "moe_profile_select",
             "moe_forward_topk", "moe_handle_config", "moe_host_pipe_size", "moe_host_pipe_create", "moe_host_step",
-            "moe_host_pipe_sync", "moe_host_pipe_destroy")
+            "moe_host_pipe_sync", "moe_host_pipe_destroy", "moe_selftest_timeout")
 MOE_K_COUNT = 20
 
 
@@ -92,6 +93,7 @@ def load(build_if_missing: bool = True):
         L.moe_backward.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, P(moe_main_grads), c_void_p]
         L.moe_export_routing.argtypes = [c_void_p, c_void_p] + [c_void_p] * 6 + [c_void_p]
         L.moe_device_status.argtypes = [c_void_p, c_void_p]
+        L.moe_selftest_timeout.argtypes = [c_void_p, c_void_p]
         L.moe_launch_count.argtypes = []
         L.moe_launch_count.restype = ctypes.c_uint64
         L.moe_profile_enable.argtypes = [c_void_p, c_int32]
@@ -117,7 +119,7 @@ def load(build_if_missing: bool = True):
                      "moe_backward", "moe_export_routing", "moe_device_status", "moe_profile_enable",
                      "moe_profile_read", "moe_route_noalloc", "moe_prepare_weights", "moe_quantize_mxfp8",
                      "moe_profile_select", "moe_handle_config", "moe_host_pipe_size", "moe_host_pipe_create",
-                     "moe_host_step", "moe_host_pipe_sync"):
+                     "moe_host_step", "moe_host_pipe_sync", "moe_selftest_timeout"):
             getattr(L, name).restype = c_int32
         _LIB = L
         return L
@@ -239,6 +241,12 @@ def moe_export_routing(h, saved, ids=None, pp=None, counts=None, offsets=None, p
 
 def moe_device_status(h, stream=None) -> int:
     return int(load().moe_device_status(h, _stream_ptr(stream)))
+
+
+def moe_selftest_timeout(h, stream=None):
+    """Enqueues the timeout-path test: one bounded wait that gives up (2 s) and records
+    MOE_ERR_TIMEOUT in the handle's device status."""
+    _check(load().moe_selftest_timeout(h, _stream_ptr(stream)), "moe_selftest_timeout")
 
 
 def moe_route_noalloc(T, E, k, routing_map, probs, ids, pp, counts, offsets, perm_src, row_of, routing_error,

@@ -1434,6 +1434,27 @@ cudaError_t launch_bn(int bn, const GemmMaps& m, const GemmArgs& a, int grid, cu
 
 }  // namespace
 
+namespace {
+// thread 0 waits on a barrier of phase 0 that nothing arrives at: mbar_wait gives up after
+// kWaitLimitNs, setting the abort flag and the timeout bit of *status
+__global__ void wait_selftest_kernel(int* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        (void)mbar_wait(&bar, 0, &abort_flag, status);
+    }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* status, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(status);
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_mx(int op, const GemmMaps& m, const GemmArgs& a, int nh, int sms, cudaStream_t st) {
     const bool clamp = a.swiglu_limit > 0.0f;
     switch (op) {

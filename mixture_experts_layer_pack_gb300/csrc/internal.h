@@ -122,6 +122,9 @@ bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims
 int pick_bn(int64_t n, bool split_gate_up);
 
 cudaError_t launch_gemm(int op, int bn, const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t st);
+// one block waiting on an mbarrier that nothing completes (the bounded wait gives up and
+// sets the timeout bit of *status): the test of the timeout path
+cudaError_t launch_wait_selftest(int* status, cudaStream_t st);
 // block-scaled MXFP8 GEMM (N tile 128, K stage 128); ops FWD_GU, FWD_DOWN, BWD_DOWN, BWD_GU
 // nh = 2: a CTA tile is two adjacent 128-column tiles sharing the A stage (the
 // gate/up forward, down forward and dgrad through gate/up; n_tiles even); else 1.

@@ -1410,6 +1410,12 @@ const char* moe_kernel_name(int kernel_class) {
     return (kernel_class >= 0 && kernel_class < MOE_K_COUNT) ? kKernelNames[kernel_class] : nullptr;
 }
 
+moe_status moe_selftest_timeout(moe_handle* h, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    MOE_CU(moe::launch_wait_selftest(h->ws.status, static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
 moe_status moe_device_status(moe_handle* h, void* stream) {
     if (!h) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

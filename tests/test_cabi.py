@@ -83,6 +83,7 @@ def test_null_arguments_rejected():
     assert L.moe_host_step(None, *([None] * 10)) == 1
     assert L.moe_host_pipe_sync(None) == 1
     assert L.moe_handle_config(None, ctypes.byref(_cfg())) == 1
+    assert L.moe_selftest_timeout(None, None) == 1
 
 
 def test_host_pipe_sizes():

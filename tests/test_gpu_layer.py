@@ -329,3 +329,27 @@ def test_layer_parity_config5_sampled():
     for n in mg:
         expect = (inp.main_grads[n] + dW[n]) + dW[n]      # fp32 adds on the device
         assert torch.equal(mg[n], expect), n
+
+
+def test_bounded_wait_gives_up_and_the_handle_stays_usable():
+    """The timeout path: a wait that nothing completes gives up after the library's limit
+    (2 s), moe_device_status reports MOE_ERR_TIMEOUT once and clears it, and the same
+    handle then runs a layer step that matches the one before."""
+    import time
+    import mixture_experts_layer_pack_gb300 as M
+    inp = make_inputs(SMALL["tiles_ragged"])
+    c = inp.case
+    layer = M.MoELayer(c.T, c.H, c.E, c.k, c.I)
+    before = run_gpu(inp, layer=layer)
+    assert layer.device_status() == 0
+    t0 = time.monotonic()
+    M.moe_selftest_timeout(layer.handle)
+    assert layer.device_status() == M.binding.MOE_ERR_TIMEOUT
+    assert time.monotonic() - t0 >= 1.5
+    assert layer.device_status() == 0
+    after = run_gpu(inp, layer=layer)
+    assert layer.device_status() == 0
+    assert torch.equal(before.out, after.out) and torch.equal(before.dhidden, after.dhidden)
+    for n in before.main_grads:
+        assert torch.equal(before.main_grads[n], after.main_grads[n]), n
+    layer.close()
