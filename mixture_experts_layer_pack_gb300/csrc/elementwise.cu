@@ -24,6 +24,8 @@ namespace {
 // take the slots of one token, so each source row leaves DRAM once however its
 // slots are spread over the experts. One warp per item, 16-byte vectors; with
 // dst_q the row is also quantised to MXFP8 along H.
+// QUANT: dst_q / dst_sf are set (MXFP8 routed weights); a build of its own (see route_place)
+template <bool QUANT>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                           const int* __restrict__ row_of,
                                                           const int* __restrict__ counts,
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
         pos = __ldg(offs_pad + e) + cnt + r;
     }
     uint4* d = dst + pos * vec_per_row;
-    if (dst_q)  // the routed dgrad-down GEMM's operand
+    if constexpr (QUANT)  // the routed dgrad-down GEMM's operand
         copy_quant_row(from, d, dst_q, dst_sf, pos, vec_per_row);
     else
         copy_row(from, d, vec_per_row);
@@ -265,7 +267,8 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* row_of, cons
                                cudaStream_t st) {
     const int64_t items = int64_t(T) * k + int64_t(E) * kBM;
     const int64_t blocks = (items + 7) / 8;
-    const cudaError_t e = launch_pdl(gather_rows_kernel, dim3(unsigned(blocks)), dim3(256), 0, st,
+    const cudaError_t e = launch_pdl(dst_q ? gather_rows_kernel<true> : gather_rows_kernel<false>,
+                                     dim3(unsigned(blocks)), dim3(256), 0, st,
                                      reinterpret_cast<const uint4*>(src), row_of, counts, offs_pad, T, E, k, H / 8,
                                      reinterpret_cast<uint4*>(dst), dst_q, dst_sf);
     count_launch();

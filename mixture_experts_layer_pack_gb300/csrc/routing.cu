@@ -424,6 +424,9 @@ __global__ void __launch_bounds__(1024) route_scan_chunks_kernel(int* __restrict
 // (token t for t < T, a zero row after it). With x_q set, the copied row is also quantised to MXFP8 along H (the routed
 // gate/up GEMM's operand): E4M3 codes to x_q, scales to x_sf in the MMA's
 // scale-factor layout.
+// QUANT: x_q / x_sf are set (MXFP8 routed weights); a build of its own, so that the
+// bf16-only copy keeps its smaller register footprint and twice the resident warps
+template <bool QUANT>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     const int* __restrict__ ids, const float* __restrict__ pp, const int* __restrict__ rank,
     const int* __restrict__ chunk_base, const int* __restrict__ counts, const int* __restrict__ offs_pad, int T,
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
         }
         const uint4* src = hidden + int64_t(t) * vec_per_row;
         uint4* dst = x_perm + int64_t(pos) * vec_per_row;
-        if (x_q)
+        if constexpr (QUANT)
             copy_quant_row(src, dst, x_q, x_sf, pos, vec_per_row);
         else
             copy_row(src, dst, vec_per_row);
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) route_place_kernel(
     }
     if (r >= (cnt + kBK - 1) / kBK * kBK - cnt) return;  // past the last 64-row block with a route
     uint4* dst = x_perm + int64_t(pos) * vec_per_row;
-    if (x_q)
+    if constexpr (QUANT)
         copy_quant_row(nullptr, dst, x_q, x_sf, pos, vec_per_row);
     else
         copy_row(nullptr, dst, vec_per_row);
@@ -569,7 +572,8 @@ cudaError_t launch_route_place(const int* ids, const float* pp, const int* rank,
                                int* row_of, __nv_bfloat16* x_perm, uint8_t* x_q, uint8_t* x_sf, cudaStream_t st) {
     const int64_t items = int64_t(T) * k + int64_t(E) * kBM + shared_rows;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const cudaError_t e = launch_pdl(route_place_kernel, dim3(unsigned(blocks)), dim3(32 * kWarpsPerBlock), 0, st,
+    const cudaError_t e = launch_pdl(x_q ? route_place_kernel<true> : route_place_kernel<false>, dim3(unsigned(blocks)),
+                                     dim3(32 * kWarpsPerBlock), 0, st,
                                      ids, pp, rank, chunk_base, counts, offs_pad, T, E, k, shared_rows,
                                      copy_shared ? 1 : 0, reinterpret_cast<const uint4*>(hidden), H / 8, perm_src,
                                      pp_perm, row_of, reinterpret_cast<uint4*>(x_perm), x_q, x_sf);
