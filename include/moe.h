@@ -40,7 +40,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, misaligned view */
-    MOE_ERR_UNSUPPORTED = 2,  /* a configuration the pages' backend also rejects, or a shape this build does not tile */
+    MOE_ERR_UNSUPPORTED = 2,  /* a configuration the pages' backend also rejects, or a shape the kernels do not tile */
     MOE_ERR_ROUTING = 3,      /* a routing_map row has more than k routes (device-detected) */
     MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     MOE_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (device-detected) */
