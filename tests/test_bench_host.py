@@ -112,14 +112,14 @@ def test_gather_kernels_count_each_source_row_once():
 # H=2048, E=96 top-6, I=1024, R=24576 routes, every expert with tokens), measured on
 # one GB300 with `python bench.py` (CUDA events, fp32 and bf16 activations).
 RECORDED_MS = {
-    True: {"route_place": 0.0253, "gather_rows": 0.0265, "gemm_fwd_gu_routed": 0.2650,
-           "gemm_fwd_down_routed": 0.1875, "combine": 0.0476, "gemm_bwd_down_routed": 0.2415,
-           "gemm_bwd_gu_routed": 0.3459, "gemm_wgrad_fc1_routed": 0.6144, "gemm_wgrad_down_routed": 0.3190,
+    True: {"route_place": 0.0240, "gather_rows": 0.0222, "gemm_fwd_gu_routed": 0.2565,
+           "gemm_fwd_down_routed": 0.1846, "combine": 0.0467, "gemm_bwd_down_routed": 0.2206,
+           "gemm_bwd_gu_routed": 0.3326, "gemm_wgrad_fc1_routed": 0.5868, "gemm_wgrad_down_routed": 0.3078,
            "unpermute": 0.0550},
-    False: {"route_place": 0.0248, "gather_rows": 0.0269, "gemm_fwd_gu_routed": 0.2304,
-            "gemm_fwd_down_routed": 0.1197, "combine": 0.0312, "gemm_bwd_down_routed": 0.2086,
-            "gemm_bwd_gu_routed": 0.2178, "gemm_wgrad_fc1_routed": 0.5335, "gemm_wgrad_down_routed": 0.2819,
-            "unpermute": 0.0390},
+    False: {"route_place": 0.0240, "gather_rows": 0.0227, "gemm_fwd_gu_routed": 0.2269,
+            "gemm_fwd_down_routed": 0.1188, "combine": 0.0314, "gemm_bwd_down_routed": 0.2505,
+            "gemm_bwd_gu_routed": 0.2170, "gemm_wgrad_fc1_routed": 0.5361, "gemm_wgrad_down_routed": 0.2821,
+            "unpermute": 0.0393},
 }
 
 
@@ -135,3 +135,26 @@ def test_recorded_kernel_rates_stay_below_the_measured_peaks(act32):
         assert b / (ms * 1e-3) / 1e9 <= 1.05 * peaks["hbm_gbs"], name
         mma = bench.mma_flops(name, f, mx=False, act32=act32)
         assert mma / (ms * 1e-3) / 1e12 <= 1.05 * peaks["bf16_tflops"], name
+
+
+def test_recorded_traffic_matches_the_algorithmic_bytes():
+    """profiles/traffic.json holds the ncu DRAM bytes (read + write) of the dominant launch
+    of every workload the bench reports. Each lies within [0.9, 1.25] x the launch's
+    algorithmic bytes at that workload's routing: far above would mean operand re-reads
+    (or a stale capture), far below an accounting that counts bytes the launch never moves."""
+    import json
+    import os
+    import moe_inputs as MI
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        traffic = json.load(f)
+    for cid in (2, 3, 4, 5):
+        assert MI.WORKLOAD_NAMES[cid] in traffic, cid
+    for wl, entries in traffic.items():
+        cid = next(c for c, n in MI.WORKLOAD_NAMES.items() if wl.startswith(n))
+        c = MI.CONFIGS[cid]
+        r = MI.config_routing(cid)
+        R, Ea = int(r.routing_map.sum()), int((r.routing_map.sum(0) > 0).sum())
+        for name, t in entries.items():
+            _, b = bench.kernel_work(name, c["T"], c["H"], c["E"], c["k"], c["I"], R, Ea,
+                                     mx=c["routed"] == "mxfp8", mg_bytes=4, act32=not wl.endswith("-bf16-act"))
+            assert 0.9 <= t / b <= 1.25, (wl, name, t / b)
