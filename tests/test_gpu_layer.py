@@ -353,3 +353,33 @@ def test_bounded_wait_gives_up_and_the_handle_stays_usable():
     for n in before.main_grads:
         assert torch.equal(before.main_grads[n], after.main_grads[n]), n
     layer.close()
+
+
+def test_nan_in_one_token_stays_in_that_token():
+    """A NaN in one token's hidden row: every other token's out, dhidden and dprobs row,
+    and the main_grad of every routed expert the token is not routed to, are bitwise those
+    of the clean run (each GEMM output row depends on its own input row only, each weight
+    gradient's K range covers its expert's routes only, and padding rows are never read
+    into a result); the token's own out row is NaN."""
+    import dataclasses as dc
+    inp = make_inputs(SMALL["tiles_ragged"])
+    c = inp.case
+    clean = run_gpu(inp)
+    t0 = int(np.flatnonzero(inp.map_np.sum(1) > 0)[10])   # a token with routes
+    hid = inp.hidden.clone()
+    hid[t0, 5] = float("nan")
+    bad = run_gpu(dc.replace(inp, hidden=hid))
+    assert bad.layer.device_status() == 0
+    keep = torch.ones(c.T, dtype=torch.bool, device=hid.device)
+    keep[t0] = False
+    assert torch.equal(bad.out[keep], clean.out[keep])
+    assert torch.equal(bad.dhidden[keep], clean.dhidden[keep])
+    assert torch.equal(bad.dprobs[keep], clean.dprobs[keep])
+    assert torch.isnan(bad.out[t0].float()).any()
+    routed_to = set(np.flatnonzero(inp.map_np[t0]).tolist())
+    assert routed_to and len(routed_to) < c.E
+    for e in range(c.E):
+        if e in routed_to:
+            continue
+        for n in ("routed_fc1", "routed_fc2"):
+            assert torch.equal(bad.main_grads[n][e], clean.main_grads[n][e]), (n, e)
