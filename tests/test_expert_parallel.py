@@ -1,7 +1,7 @@
-"""Expert-parallel dispatch and combine on CPU ranks (gloo, world size 2).
+"""Expert-parallel dispatch and combine on CPU ranks (gloo, world sizes 2 and 3).
 
-Each rank holds half of the tokens and owns a contiguous range of the routed
-experts (the first rank one more when E is odd). The exchange
+Each rank holds its share of the tokens and owns a contiguous range of the routed
+experts (the first E mod W ranks one more). The exchange
 (mixture_experts_layer_pack_gb300.expert_parallel) moves the token rows to the
 owners and back; the experts, the shared expert and the sums on either side are
 the fp64 oracle's. Against the single-rank oracle over all tokens:
@@ -28,6 +28,7 @@ from mixture_experts_layer_pack_gb300 import expert_parallel as EP
 CASES = {
     "even": dict(T=96, H=64, E=6, k=2, I=32, seed=71),
     "odd_experts_missing_routes": dict(T=80, H=64, E=5, k=3, I=32, seed=72),
+    "three_ranks": dict(T=91, H=64, E=7, k=2, I=32, seed=73, world=3),
 }
 
 
@@ -179,16 +180,17 @@ def test_partition_is_contiguous_and_covers_every_expert():
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_expert_parallel_matches_single_rank_oracle(name):
+    world = CASES[name].get("world", 2)
     ctx = mp.get_context("spawn")
     q = ctx.SimpleQueue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, name, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, name, q)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:
         p.join(timeout=300)
-    results = dict(q.get() for _ in range(2)) if all(p.exitcode == 0 for p in procs) else {}
+    results = dict(q.get() for _ in range(world)) if all(p.exitcode == 0 for p in procs) else {}
     for p in procs:
         if p.is_alive():
             p.kill()
-    assert results == {0: "ok", 1: "ok"}, [p.exitcode for p in procs]
+    assert results == {r: "ok" for r in range(world)}, (results, [p.exitcode for p in procs])
